@@ -1,0 +1,128 @@
+"""CPU oracle of the HiSparse decode-step resolver -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+may import this package. The library (``hierarchical_sparse_attention_gb300``) never
+does, and the two share no code: the oracle is plain single-threaded C
+(``hs_oracle.c``) that follows the pages' steps in order, built with gcc, wrapped
+here with ctypes.
+
+Every function here is pinned by the CPU tests (brute force, textbook LRU,
+invariants, special cases); see ``hs_oracle.c`` for the sources and readings.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+
+ERR_TOKEN, ERR_DUP, ERR_STATE, ERR_HOSTROW, ERR_DEVROW, ERR_SEQLEN = 1, 2, 4, 8, 16, 32
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+class Geom(ctypes.Structure):
+    _fields_ = [("top_k", ctypes.c_int32), ("hot_slots", ctypes.c_int32),
+                ("row_bytes", ctypes.c_int32), ("num_layers", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("max_context", ctypes.c_int32),
+                ("max_pages", ctypes.c_int32), ("host_rows", ctypes.c_int64),
+                ("device_rows", ctypes.c_int64)]
+
+
+def build(force: bool = False) -> str:
+    """Compile hs_oracle.c into liboracle.so next to it."""
+    src = os.path.join(_HERE, "hs_oracle.c")
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(src):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", src, "-o", tmp])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = os.environ.get("HS_ORACLE_LIB")  # tests load deliberately broken builds this way
+        if not path:
+            path = build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        lib.oracle_resolve.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32] + [P] * 13
+        lib.oracle_resolve.restype = None
+        lib.oracle_backup.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32] + [P] * 7
+        lib.oracle_backup.restype = None
+        lib.oracle_hot_bytes_per_request.argtypes = [ctypes.c_int32] * 4
+        lib.oracle_hot_bytes_per_request.restype = ctypes.c_int64
+        _lib = lib
+    return _lib
+
+
+def _p(a: Optional[np.ndarray]) -> Optional[int]:
+    return None if a is None else a.ctypes.data
+
+
+def _i32(a: np.ndarray, shape=None) -> np.ndarray:
+    assert a.dtype == np.int32 and a.flags.c_contiguous, "int32 C-contiguous array expected"
+    if shape is not None:
+        assert a.shape == tuple(shape), (a.shape, shape)
+    return a
+
+
+def hot_bytes_per_request(top_k: int, n_spec: int, row_bytes: int, layers: int) -> int:
+    return int(_load().oracle_hot_bytes_per_request(top_k, n_spec, row_bytes, layers))
+
+
+class Oracle:
+    """State-free wrapper: the caller owns every array (as with the library)."""
+
+    def __init__(self, top_k: int, hot_slots: int, row_bytes: int, num_layers: int,
+                 max_context: int, host_rows: int, device_rows: int, page_size: int = 0,
+                 max_pages: int = 0):
+        self.g = Geom(top_k, hot_slots, row_bytes, num_layers, page_size, max_context, max_pages,
+                      host_rows, device_rows)
+        self.lib = _load()
+
+    def _pools(self, pools: Sequence[np.ndarray], rows: int):
+        assert len(pools) == self.g.num_layers
+        for p in pools:
+            assert p.dtype == np.uint8 and p.flags.c_contiguous and p.size >= rows * self.g.row_bytes
+        return (ctypes.c_void_p * len(pools))(*[p.ctypes.data for p in pools])
+
+    def resolve(self, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs,
+                device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows,
+                miss_counts, host_pools, device_pools) -> int:
+        g = self.g
+        R = seq_lens.shape[0]
+        _i32(top_k_tokens, (R, g.top_k)); _i32(seq_lens); _i32(host_cache_locs, (R, g.max_context))
+        _i32(device_buffer_locs, (R, g.hot_slots + 1)); _i32(device_buffer_tokens, (R, g.hot_slots))
+        _i32(lru_slots, (R, g.hot_slots)); _i32(lru_clock, (R,)); _i32(out_rows, (R, g.top_k))
+        if resident_pages is not None:
+            _i32(resident_pages, (R, g.max_pages))
+        if miss_counts is not None:
+            _i32(miss_counts, (R,))
+        err = ctypes.c_uint32(0)
+        hp = self._pools(host_pools, g.host_rows)
+        dp = self._pools(device_pools, g.device_rows)
+        self.lib.oracle_resolve(ctypes.byref(g), R, _p(top_k_tokens), _p(seq_lens), _p(host_cache_locs),
+                                _p(device_buffer_locs), _p(device_buffer_tokens), _p(lru_slots),
+                                _p(lru_clock), _p(resident_pages), _p(out_rows), _p(miss_counts),
+                                hp, dp, ctypes.byref(err))
+        return int(err.value)
+
+    def backup(self, seq_lens, host_cache_locs, device_buffer_locs, resident_pages, host_pools,
+               device_pools) -> int:
+        g = self.g
+        R = seq_lens.shape[0]
+        _i32(seq_lens); _i32(host_cache_locs, (R, g.max_context)); _i32(device_buffer_locs, (R, g.hot_slots + 1))
+        if resident_pages is not None:
+            _i32(resident_pages, (R, g.max_pages))
+        err = ctypes.c_uint32(0)
+        hp = self._pools(host_pools, g.host_rows)
+        dp = self._pools(device_pools, g.device_rows)
+        self.lib.oracle_backup(ctypes.byref(g), R, _p(seq_lens), _p(host_cache_locs),
+                               _p(device_buffer_locs), _p(resident_pages), hp, dp, ctypes.byref(err))
+        return int(err.value)

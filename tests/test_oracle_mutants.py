@@ -1,0 +1,54 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of oracle/hs_oracle.c (a flipped comparison, a
+dropped update, an off-by-one), builds it with gcc into a temporary library, and runs the
+pin suite against it in a child process. The child must report at least one failing pin.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "hs_oracle.c")
+
+MUTANTS = [
+    ("tie_to_highest_slot", "if (x->slot != y->slot) return x->slot < y->slot ? -1 : 1;",
+     "if (x->slot != y->slot) return x->slot < y->slot ? 1 : -1;"),
+    ("evict_newest_stamp", "if (x->stamp != y->stamp) return x->stamp < y->stamp ? -1 : 1;",
+     "if (x->stamp != y->stamp) return x->stamp < y->stamp ? 1 : -1;"),
+    ("free_slots_last", "if (x->occupied != y->occupied) return x->occupied < y->occupied ? -1 : 1;",
+     "if (x->occupied != y->occupied) return x->occupied < y->occupied ? 1 : -1;"),
+    ("clock_not_stored", "    lru_clock[r] = c;\n", "\n"),
+    ("hit_not_refreshed", "        stamps[s] = c;\n        used[s] = 1;", "        used[s] = 1;"),
+    ("newest_not_reserved", "if (cls[i] == E_VALID && tk[i] == S - 1) {", "if (cls[i] == E_VALID && tk[i] == S) {"),
+    ("fast_path_off_by_one", "  if (S <= H) {\n      for", "  if (S < H) {\n      for"),
+    ("victims_reversed", "int32_t v = cand[j].slot;", "int32_t v = cand[m - 1 - j].slot;"),
+    ("token_as_host_row", "int64_t h = hcl[t];", "int64_t h = t;"),
+    ("hit_wrong_row", "out[i] = checked_row(dbl[s], g->device_rows, err);\n        cls[i] = E_DONE;",
+     "out[i] = checked_row(dbl[s + 1], g->device_rows, err);\n        cls[i] = E_DONE;"),
+    ("resident_offset_wrong", "return (int64_t)p * g->page_size + t % g->page_size;",
+     "return (int64_t)p * g->page_size + (t + 1) % g->page_size;"),
+    ("sanitize_too_loose", "tokens[s] < -1 || tokens[s] >= S - 1)", "tokens[s] < -1 || tokens[s] >= S)"),
+    ("backup_always_reserved", "if (row < 0) row = S <= H ? dbl[t] : dbl[H];", "if (row < 0) row = dbl[H];"),
+    ("duplicates_not_rejected", "else if (first_at[t] >= 0)", "else if (first_at[t] >= 2000000000)"),
+    ("misses_not_zero_filled", "else memset(dst, 0, (size_t)B);", "else (void)dst;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    csrc = tmp_path / "mutant.c"
+    csrc.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", str(csrc), "-o", str(lib)])
+    code = ("import sys; sys.path[:0] = [%r, %r]; import test_oracle_pins as t; "
+            "n = t.run_all_pins(); print('failed pins:', n); sys.exit(0 if n else 3)"
+            % (ROOT, os.path.join(ROOT, "tests")))
+    env = dict(os.environ, HS_ORACLE_LIB=str(lib))
+    p = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+    assert p.returncode != 3, f"mutant {name} survived every pin:\n{p.stdout}\n{p.stderr}"
+    assert p.returncode == 0, f"mutant {name}: pin run crashed (rc {p.returncode}):\n{p.stderr[-2000:]}"
