@@ -1,0 +1,210 @@
+// C ABI of libhs (declared in include/hs.h): host-side validation, pool binding and
+// the stream-ordered launches. Nothing here allocates device or pinned memory or
+// synchronises on the hot path (hs_resolve / hs_backup).
+#include <cstdlib>
+#include <cstring>
+
+#include "hs_internal.h"
+
+struct hs_handle {
+  hs_config cfg;
+  hs::Geometry g;
+  const hs::Pools* pools;  // pools table inside the caller's workspace
+  uint32_t* err_word;      // error word inside the caller's workspace
+  int device;
+};
+
+namespace {
+
+bool config_ok(const hs_config* c) {
+  if (!c) return false;
+  if (c->max_requests < 1 || c->top_k < 1 || c->top_k > HS_MAX_TOP_K) return false;
+  if (c->hot_slots < c->top_k || c->hot_slots > HS_MAX_HOT_SLOTS) return false;
+  if (c->row_bytes < 1 || c->num_layers < 1 || c->num_layers > HS_MAX_LAYERS) return false;
+  if (c->max_context < 1 || c->page_size < 0 || c->max_pages < 0) return false;
+  if (c->page_size > 0 &&
+      (int64_t)c->max_pages * c->page_size < (int64_t)c->max_context)
+    return false;
+  return true;
+}
+
+int ceil_log2(int64_t x) {
+  int b = 0;
+  while (((int64_t)1 << b) < x) ++b;
+  return b;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+size_t hs_workspace_bytes(const hs_config* cfg) { return config_ok(cfg) ? hs::kWorkspaceBytes : 0; }
+
+hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* device_pools,
+                    int64_t host_rows, int64_t device_rows, void* workspace, hs_handle** out) {
+  if (!out) return HS_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !host_pools || !device_pools || !workspace) return HS_ERR_INVALID_ARG;
+  if (!config_ok(cfg)) return HS_ERR_INVALID_CONFIG;
+  // Row tables are int32: every row index must fit.
+  if (host_rows < 1 || device_rows < 1 || host_rows > INT32_MAX || device_rows > INT32_MAX)
+    return HS_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
+
+  hs::Geometry g{};
+  g.K = cfg->top_k;
+  g.H = cfg->hot_slots;
+  g.B = cfg->row_bytes;
+  g.L = cfg->num_layers;
+  g.page_size = cfg->page_size;
+  g.max_context = cfg->max_context;
+  g.max_pages = cfg->max_pages;
+  g.hash_bits = ceil_log2(2 * (int64_t)cfg->top_k);
+  if (g.hash_bits < 5) g.hash_bits = 5;
+  g.sort_cap = 1 << ceil_log2(cfg->top_k);
+  if (g.hash_bits < ceil_log2(cfg->top_k) + 1) g.hash_bits = ceil_log2(cfg->top_k) + 1;  // room for the aliases
+  g.host_rows = host_rows;
+  g.device_rows = device_rows;
+
+  hs::Pools pools{};
+  bool a16 = (g.B % 16) == 0, a4 = (g.B % 4) == 0;
+  for (int l = 0; l < g.L; ++l) {
+    if (!host_pools[l] || !device_pools[l]) return HS_ERR_INVALID_ARG;
+    cudaPointerAttributes ha{}, da{};
+    if (cudaPointerGetAttributes(&ha, host_pools[l]) != cudaSuccess) {
+      cudaGetLastError();
+      return HS_ERR_INVALID_ARG;
+    }
+    if (ha.type != cudaMemoryTypeHost || !ha.devicePointer) return HS_ERR_INVALID_ARG;  // not pinned+mapped
+    if (cudaPointerGetAttributes(&da, device_pools[l]) != cudaSuccess) {
+      cudaGetLastError();
+      return HS_ERR_INVALID_ARG;
+    }
+    if ((da.type != cudaMemoryTypeDevice && da.type != cudaMemoryTypeManaged) || da.device != dev)
+      return HS_ERR_INVALID_ARG;
+    pools.host[l] = static_cast<const uint8_t*>(ha.devicePointer);
+    pools.dev[l] = static_cast<uint8_t*>(device_pools[l]);
+    a16 = a16 && aligned(pools.host[l], 16) && aligned(pools.dev[l], 16);
+    a4 = a4 && aligned(pools.host[l], 4) && aligned(pools.dev[l], 4);
+  }
+  g.vec = a16 ? 16 : (a4 ? 4 : 1);
+
+  cudaPointerAttributes wa{};
+  if (cudaPointerGetAttributes(&wa, workspace) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_INVALID_ARG;
+  }
+  if ((wa.type != cudaMemoryTypeDevice && wa.type != cudaMemoryTypeManaged) || wa.device != dev ||
+      !aligned(workspace, 16))
+    return HS_ERR_INVALID_ARG;
+
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return HS_ERR_CUDA;
+  if (hs::resolve_smem_bytes(g) > (size_t)optin) return HS_ERR_INVALID_CONFIG;
+  if (hs::resolve_prepare(g) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemset(ws, 0, hs::kWorkspaceBytes) != cudaSuccess) return HS_ERR_CUDA;
+  if (cudaMemcpy(ws + hs::kPoolsOffset, &pools, sizeof(pools), cudaMemcpyHostToDevice) != cudaSuccess)
+    return HS_ERR_CUDA;
+
+  hs_handle* h = static_cast<hs_handle*>(std::calloc(1, sizeof(hs_handle)));
+  if (!h) return HS_ERR_INVALID_ARG;
+  h->cfg = *cfg;
+  h->g = g;
+  h->pools = reinterpret_cast<const hs::Pools*>(ws + hs::kPoolsOffset);
+  h->err_word = reinterpret_cast<uint32_t*>(ws + hs::kErrOffset);
+  h->device = dev;
+  *out = h;
+  return HS_OK;
+}
+
+hs_status hs_resolve(hs_handle* h, int32_t num_requests, const int32_t* top_k_tokens,
+                     const int32_t* seq_lens, const int32_t* host_cache_locs,
+                     const int32_t* device_buffer_locs, int32_t* device_buffer_tokens, int32_t* lru_slots,
+                     int32_t* lru_clock, const int32_t* resident_pages, int32_t* out_rows,
+                     int32_t* miss_counts, hs_stream_t stream) {
+  if (!h || num_requests < 0 || num_requests > h->cfg.max_requests) return HS_ERR_INVALID_ARG;
+  if (num_requests == 0) return HS_OK;
+  if (!top_k_tokens || !seq_lens || !host_cache_locs || !device_buffer_locs || !device_buffer_tokens ||
+      !lru_slots || !lru_clock || !out_rows)
+    return HS_ERR_INVALID_ARG;
+  if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
+  hs::ResolveArgs a{top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs, device_buffer_tokens,
+                    lru_slots, lru_clock, resident_pages, out_rows, miss_counts};
+  if (hs::launch_resolve(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+    return HS_ERR_CUDA;
+  return HS_OK;
+}
+
+hs_status hs_backup(hs_handle* h, int32_t num_requests, const int32_t* seq_lens,
+                    const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
+                    const int32_t* resident_pages, hs_stream_t stream) {
+  if (!h || num_requests < 0 || num_requests > h->cfg.max_requests) return HS_ERR_INVALID_ARG;
+  if (num_requests == 0) return HS_OK;
+  if (!seq_lens || !host_cache_locs || !device_buffer_locs) return HS_ERR_INVALID_ARG;
+  if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
+  hs::BackupArgs a{seq_lens, host_cache_locs, device_buffer_locs, resident_pages};
+  if (hs::launch_backup(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+    return HS_ERR_CUDA;
+  return HS_OK;
+}
+
+hs_status hs_get_error(hs_handle* h, uint32_t* flags, int clear) {
+  if (!h || !flags) return HS_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;
+  if (cudaMemcpy(flags, h->err_word, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return HS_ERR_CUDA;
+  if (clear && cudaMemset(h->err_word, 0, sizeof(uint32_t)) != cudaSuccess) return HS_ERR_CUDA;
+  if (clear && cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;
+  return *flags ? HS_ERR_DEVICE_FLAGGED : HS_OK;
+}
+
+hs_status hs_destroy(hs_handle* h) {
+  std::free(h);
+  return HS_OK;
+}
+
+const char* hs_status_str(hs_status s) {
+  switch (s) {
+    case HS_OK: return "ok";
+    case HS_ERR_INVALID_ARG: return "invalid argument";
+    case HS_ERR_INVALID_CONFIG: return "invalid configuration";
+    case HS_ERR_CUDA: return "CUDA error";
+    case HS_ERR_DEVICE_FLAGGED: return "device flagged anomalies in the inputs";
+    case HS_ERR_TIMEOUT: return "timed out";
+  }
+  return "unknown status";
+}
+
+hs_status hs_host_register(void* ptr, size_t bytes, void** device_ptr) {
+  if (!ptr || !bytes || !device_ptr) return HS_ERR_INVALID_ARG;
+  *device_ptr = nullptr;
+  if (cudaHostRegister(ptr, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  if (cudaHostGetDevicePointer(device_ptr, ptr, 0) != cudaSuccess) {
+    cudaGetLastError();
+    cudaHostUnregister(ptr);
+    return HS_ERR_CUDA;
+  }
+  return HS_OK;
+}
+
+hs_status hs_host_unregister(void* ptr) {
+  if (!ptr) return HS_ERR_INVALID_ARG;
+  if (cudaHostUnregister(ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  return HS_OK;
+}
+
+}  // extern "C"

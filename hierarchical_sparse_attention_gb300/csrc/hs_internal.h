@@ -1,0 +1,68 @@
+// Internal launch interface between the C ABI (hs_api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "hs.h"
+
+namespace hs {
+
+constexpr int kResolveThreads = 1024;  // one CTA of 32 warps per request
+constexpr int kBackupThreads = 256;    // 8 warps, one (request, layer) row per warp
+constexpr int kMaxLayers = HS_MAX_LAYERS;
+
+// Per-layer pool base addresses as the kernels dereference them. hs_create writes this
+// table into the caller's workspace at kPoolsOffset, so kernels index it by layer from
+// global/shared memory instead of copying a by-value parameter array to local memory.
+struct Pools {
+  const uint8_t* host[kMaxLayers];  // device-side addresses of the pinned, mapped host pools
+  uint8_t* dev[kMaxLayers];
+};
+
+// Everything the kernels need to know about one layer group, fixed at hs_create.
+struct Geometry {
+  int32_t K, H, B, L;
+  int32_t page_size, max_context, max_pages;
+  int32_t hash_bits;  // top-k hash table holds 1 << hash_bits >= 2K entries
+  int32_t sort_cap;   // power of two >= K: capacity of the victim sort buffer
+  int32_t vec;        // bytes per copy piece: 16, 4 or 1
+  int64_t host_rows, device_rows;
+};
+
+struct ResolveArgs {
+  const int32_t* top_k_tokens;
+  const int32_t* seq_lens;
+  const int32_t* host_cache_locs;
+  const int32_t* device_buffer_locs;
+  int32_t* device_buffer_tokens;
+  int32_t* lru_slots;
+  int32_t* lru_clock;
+  const int32_t* resident_pages;
+  int32_t* out_rows;
+  int32_t* miss_counts;
+};
+
+struct BackupArgs {
+  const int32_t* seq_lens;
+  const int32_t* host_cache_locs;
+  const int32_t* device_buffer_locs;
+  const int32_t* resident_pages;
+};
+
+// Workspace layout (device memory owned by the caller).
+constexpr size_t kErrOffset = 0;     // uint32 sticky HS_FLAG_* word
+constexpr size_t kPoolsOffset = 64;  // Pools table
+constexpr size_t kWorkspaceBytes = 256;
+static_assert(kPoolsOffset + sizeof(Pools) <= kWorkspaceBytes, "workspace too small for the pools table");
+
+size_t resolve_smem_bytes(const Geometry& g);
+cudaError_t resolve_prepare(const Geometry& g);
+cudaError_t launch_resolve(const Geometry& g, const Pools* pools, const ResolveArgs& a, int32_t num_requests,
+                           uint32_t* err_word, cudaStream_t stream);
+cudaError_t launch_backup(const Geometry& g, const Pools* pools, const BackupArgs& a, int32_t num_requests,
+                          uint32_t* err_word, cudaStream_t stream);
+
+}  // namespace hs

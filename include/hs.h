@@ -1,0 +1,200 @@
+/*
+ * hs.h -- C ABI of libhs: the HiSparse decode-step resolver / swap-in on GB300 (sm_103a).
+ *
+ * Once per decode step, for every request of the batch, the resolver takes the indexer's
+ * top-k token positions and gives back the physical device row that sparse attention must
+ * read for each of them. A token is found, in this order, in a GPU-resident page, in the
+ * request's fixed-size hot buffer (refreshing its LRU stamp), or else it is copied from
+ * pinned host memory into the least-recently-used buffer slot that this step does not need.
+ * Short sequences that fit the buffer take a no-copy fast path. A second call copies the
+ * newest token's row back to host memory (eager backup).
+ *
+ * Sources, by page title and section:
+ *   "HiSparse: Turbocharging Sparse Attention with Hierarchical Memory" (LMSYS blog, as
+ *       translated in "vLLM HiSparse local KV offload architecture") - "Efficient swap-in
+ *       kernel": one kernel finds the top-k misses in the device buffer, picks LRU
+ *       victims, updates the table and fetches the missing rows from host memory.
+ *   "HiSparse: moving the long-context decode capacity bottleneck from GPU memory to CPU
+ *       memory" - "Per decode step workflow" (swap-in with a fast path when
+ *       seq_len <= device_buffer_size; eager backup of the last token), "Core: swap-in
+ *       CUDA kernel" (parameters top_k_tokens, seq_lens, host_cache_locs,
+ *       device_buffer_locs, lru_slots), "How capacity is computed" (the per-request buffer
+ *       carries an extra page for the new token).
+ *   "vLLM HiSparse local KV offload architecture" - "Hot-row lookup and LRU" and
+ *       "Performance invariants" (resident, then hot, then pinned host; all decisions on
+ *       the GPU; no device readback; graph-capturable; layers sharing an indexer share
+ *       one miss plan).
+ *   "vLLM Hybrid HiSparse source implementation analysis" - 7.1 (per-slot state, one
+ *       hot region per request), 7.2 (resident short-circuit, hot hits, miss plan and
+ *       victims, corruption tripwires, gather that zeroes a destination whose source row
+ *       is out of range), 7.3 (flat physical row IDs), 7.4 (IndexShare replay).
+ *   "Hierarchical Sparse Attention" (Alibaba Tair KVCache) - 2.4.3 "LRU Diff Kernel"
+ *       (evict only when the buffer is full, coldest first).
+ *
+ * Policy (fixed; the CPU oracle in the tests implements the same steps):
+ *   For request r with S = seq_lens[r] and every top-k entry t = top_k_tokens[r][i]:
+ *   - t < 0 is padding: out = -1.  t >= S: out = -1, flag HS_FLAG_TOKEN.  A valid token
+ *     repeated in the row: the first occurrence is resolved, later ones get -1 and
+ *     HS_FLAG_DUP.
+ *   - Resident: if resident_pages[r][t / page_size] = p >= 0, out = p*page_size + t%page_size.
+ *   - Fast path (S <= H): out = device_buffer_locs[r][t]; device_buffer_tokens[r][S-1]
+ *     is set to S-1; the clock, stamps and pools are untouched.
+ *   - Otherwise (slow path): c = ++lru_clock[r].
+ *       newest token t = S-1 -> out = device_buffer_locs[r][H] (the reserved row).
+ *       Slot state outside (token in [-1, S-2], stamp in [0, c-1]) is reset to
+ *       (-1, 0) and flagged HS_FLAG_STATE.
+ *       Hit: the lowest slot s holding t; lru_slots[r][s] = c; out = device_buffer_locs[r][s].
+ *       (Several slots holding t also flag HS_FLAG_STATE.)
+ *       Misses, in top-k order, take victims among the slots not hit in this call:
+ *       free slots (token -1) by ascending slot, then occupied slots by ascending
+ *       (stamp, slot). Miss j takes victim j: token and stamp c are stored, and for each
+ *       layer the row host_pool[l][host_cache_locs[r][t]] is copied to
+ *       device_pool[l][device_buffer_locs[r][victim]].
+ *   - A host row outside [0, host_rows) zero-fills the destination (HS_FLAG_HOSTROW). A
+ *     physical row outside [0, device_rows) gives out = -1 and writes nothing
+ *     (HS_FLAG_DEVROW). S outside [0, max_context] leaves the request untouched with
+ *     out = -1 (HS_FLAG_SEQLEN).
+ *
+ * Memory and ownership. The caller owns every buffer; the library allocates no device or
+ * pinned memory and never synchronises inside hs_resolve / hs_backup. Device pointers are
+ * CUDA device memory of the device current at hs_create. Host pools are pinned and mapped
+ * (cudaHostAlloc(..., cudaHostAllocMapped) or hs_host_register); the kernels read and
+ * write them directly over the host link. All arrays are dense, row-major, int32:
+ *   top_k_tokens         [R, K]            device, read
+ *   seq_lens             [R]               device, read
+ *   host_cache_locs      [R, max_context]  device, read      token -> host row
+ *   device_buffer_locs   [R, H+1]          device, read      slot -> device row; slot H is
+ *                                                            the newest-token row
+ *   device_buffer_tokens [R, H]            device, read/write slot -> token, -1 = free
+ *   lru_slots            [R, H]            device, read/write per-slot LRU stamp
+ *   lru_clock            [R]               device, read/write per-request clock
+ *   resident_pages       [R, max_pages]    device, read, or NULL   page -> device page
+ *   out_rows             [R, K]            device, write     physical row per entry
+ *   miss_counts          [R]               device, write, or NULL
+ * Initial state: long requests tokens = -1, stamps = 0, clock = 0; requests with
+ * S <= H hold token s in slot s (rows already written) for s < S.
+ * Preconditions not checked on the device: device_buffer_locs rows are distinct and
+ * disjoint from resident rows; the forward pass has written the newest token's row to
+ * its resident row, or to slot S-1 when S <= H, else to slot H, before hs_resolve.
+ * Calls that share state arrays must be ordered on one stream.
+ *
+ * Errors. Host-side validation returns a status synchronously. A failed launch returns
+ * HS_ERR_CUDA. Data anomalies met on the device are OR-ed as HS_FLAG_* bits into the
+ * error word in the caller's workspace and never trap; hs_get_error reads them.
+ */
+#ifndef HS_H_
+#define HS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define HS_API __attribute__((visibility("default")))
+#else
+#define HS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* hs_stream_t;
+
+typedef enum {
+  HS_OK = 0,
+  HS_ERR_INVALID_ARG = 1,    /* null pointer, size out of range, wrong memory kind */
+  HS_ERR_INVALID_CONFIG = 2, /* configuration the kernels cannot run (limits below) */
+  HS_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
+  HS_ERR_DEVICE_FLAGGED = 4, /* hs_get_error found HS_FLAG_* bits set */
+  HS_ERR_TIMEOUT = 5         /* reserved for bounded device waits (none in this version) */
+} hs_status;
+
+/* Device-side anomaly bits in the workspace error word (sticky until cleared). */
+#define HS_FLAG_TOKEN 1u   /* top-k entry >= seq_len */
+#define HS_FLAG_DUP 2u     /* repeated valid token in one top-k row */
+#define HS_FLAG_STATE 4u   /* corrupt slot token/stamp, or a token held by two slots */
+#define HS_FLAG_HOSTROW 8u /* host row out of range: destination zero-filled */
+#define HS_FLAG_DEVROW 16u /* device row out of range: output -1, nothing written */
+#define HS_FLAG_SEQLEN 32u /* seq_len outside [0, max_context]: request skipped */
+
+/* Limits of this build. */
+#define HS_MAX_TOP_K 4096
+#define HS_MAX_HOT_SLOTS 16384
+#define HS_MAX_LAYERS 8
+
+/* Configuration of one layer group (layers that share one indexer top-k and therefore
+ * one slot map; "vLLM Hybrid HiSparse source implementation analysis" 7.4).
+ *   max_requests  largest R passed to hs_resolve / hs_backup
+ *   top_k         K, 1..HS_MAX_TOP_K
+ *   hot_slots     H (device_buffer_size), K..HS_MAX_HOT_SLOTS
+ *   row_bytes     B, bytes of one token's KV row in one layer (656 for fp8 MLA)
+ *   num_layers    L, 1..HS_MAX_LAYERS
+ *   page_size     residency page size in tokens; 0 disables resident_pages
+ *   max_context   row stride of host_cache_locs; seq_len may not exceed it
+ *   max_pages     row stride of resident_pages; >= ceil(max_context / page_size) */
+typedef struct {
+  int32_t max_requests;
+  int32_t top_k;
+  int32_t hot_slots;
+  int32_t row_bytes;
+  int32_t num_layers;
+  int32_t page_size;
+  int32_t max_context;
+  int32_t max_pages;
+} hs_config;
+
+typedef struct hs_handle hs_handle;
+
+/* Bytes of device workspace hs_create needs (error word and reserved space); 0 if the
+ * configuration is invalid. */
+HS_API size_t hs_workspace_bytes(const hs_config* cfg);
+
+/* Validate the configuration and bind the pools. host_pools / device_pools are arrays of
+ * num_layers pointers to [host_rows, row_bytes] pinned+mapped host pools and
+ * [device_rows, row_bytes] device pools. workspace is caller-owned device memory of
+ * hs_workspace_bytes(cfg) bytes, zeroed here (synchronously). Allocates only the small
+ * host-side handle. Returns HS_ERR_INVALID_ARG / HS_ERR_INVALID_CONFIG / HS_ERR_CUDA on
+ * failure, with *out set to NULL. */
+HS_API hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* device_pools,
+                    int64_t host_rows, int64_t device_rows, void* workspace, hs_handle** out);
+
+/* One decode step of the resolver for requests 0..num_requests-1 (layout above): one
+ * kernel launch on `stream`, no allocation, no synchronisation, capturable in a CUDA
+ * graph. num_requests == 0 is a no-op. */
+HS_API hs_status hs_resolve(hs_handle* h, int32_t num_requests, const int32_t* top_k_tokens,
+                     const int32_t* seq_lens, const int32_t* host_cache_locs,
+                     const int32_t* device_buffer_locs, int32_t* device_buffer_tokens,
+                     int32_t* lru_slots, int32_t* lru_clock, const int32_t* resident_pages,
+                     int32_t* out_rows, int32_t* miss_counts, hs_stream_t stream);
+
+/* Eager backup ("Per decode step workflow", step 5): for every request with seq_len >= 1
+ * and every layer, copy the newest token's row -- its resident row, else slot seq_len-1
+ * when seq_len <= H, else slot H -- to host_pool[l][host_cache_locs[r][seq_len-1]].
+ * One kernel launch on `stream`; same rules as hs_resolve. */
+HS_API hs_status hs_backup(hs_handle* h, int32_t num_requests, const int32_t* seq_lens,
+                    const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
+                    const int32_t* resident_pages, hs_stream_t stream);
+
+/* Read the workspace error word (synchronises the device; not for the hot path). With
+ * clear != 0 the word is reset to zero. Returns HS_ERR_DEVICE_FLAGGED when any bit is set. */
+HS_API hs_status hs_get_error(hs_handle* h, uint32_t* flags, int clear);
+
+/* Free the host-side handle. Buffers stay the caller's. NULL is accepted. */
+HS_API hs_status hs_destroy(hs_handle* h);
+
+/* Static description of a status code. */
+HS_API const char* hs_status_str(hs_status s);
+
+/* Page-lock an existing host range for the kernels' direct access (cudaHostRegister with
+ * the mapped and portable flags) and return the device-side address in *device_ptr. */
+HS_API hs_status hs_host_register(void* ptr, size_t bytes, void** device_ptr);
+
+/* Undo hs_host_register. */
+HS_API hs_status hs_host_unregister(void* ptr);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HS_H_ */

@@ -15,9 +15,11 @@ def pytest_configure(config):
 
 @pytest.fixture(scope="session", autouse=True)
 def _built_cpu_libs():
-    """Compile the oracle and the row generator (gcc, seconds) before any test."""
+    """Compile the oracle, the row generator (gcc) and libhs.so (nvcc, sm_103a) once."""
     import oracle
     import workloads
+    from hierarchical_sparse_attention_gb300 import build as hs_build
     oracle.build()
     workloads.build_rowgen()
+    hs_build.build()
     yield

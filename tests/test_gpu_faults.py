@@ -1,0 +1,207 @@
+"""Tripwires, invalid inputs and API misuse on the GPU, against the oracle.
+
+Faults are planted in the input data on the host (corrupt slot state, out-of-range
+tokens and rows, repeated tokens, oversize seq_len); the kernels must flag them in the
+error word and behave exactly as the oracle does. Nothing here can fault the GPU: every
+planted value is caught by the kernels' own range checks before it is used as an index.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads as W  # noqa: E402
+from harness import OracleSim, poison_host_newest  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+ERR = dict(TOKEN=1, DUP=2, STATE=4, HOSTROW=8, DEVROW=16, SEQLEN=32)
+
+
+@pytest.fixture
+def pair():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gpu_harness import GpuSim, host_pools
+    wl = W.make("dsa", requests=4, top_k=256, hot_slots=512, steps=12, seq0=(6000, 7000, 8000, 300))
+    host = host_pools(wl)
+    orc = OracleSim(wl, host_pools=host)
+    gpu = GpuSim(wl, host, orc.dev)
+    yield wl, orc, gpu
+    gpu.close()
+
+
+def step_both(wl, orc, gpu, step, tk=None, sl=None, hcl=None, dbl=None):
+    import hierarchical_sparse_attention_gb300 as hs
+    gpu.write_newest(step)
+    orc.write_newest(step)
+    poison_host_newest(wl, step, orc.host)
+    tk = wl.top_k_tokens(step) if tk is None else tk
+    sl = wl.seq_lens(step) if sl is None else sl
+    gpu.upload(step, top_k=tk, seq_lens=sl)
+    saved = (gpu.hcl, gpu.dbl)
+    if hcl is not None:
+        gpu.hcl = torch.from_numpy(hcl).cuda()
+    if dbl is not None:
+        gpu.dbl = torch.from_numpy(dbl).cuda()
+    gpu.resolve()
+    gpu.backup()
+    torch.cuda.synchronize()
+    gpu.hcl, gpu.dbl = saved
+    oerr = orc.resolve(step, top_k=tk, seq_lens=sl, host_cache_locs=hcl, device_buffer_locs=dbl)
+    if hcl is None and dbl is None:
+        oerr |= orc.backup(step, seq_lens=sl)
+    else:
+        oerr |= orc.orc.backup(sl, wl.host_cache_locs if hcl is None else hcl,
+                               wl.device_buffer_locs if dbl is None else dbl, wl.resident_pages, orc.host, orc.dev)
+    g = gpu.state()
+    for k, o in (("out", orc.out), ("miss", orc.miss), ("tokens", orc.tokens), ("stamps", orc.stamps),
+                 ("clock", orc.clock)):
+        np.testing.assert_array_equal(g[k], o, err_msg=f"step {step}: {k}")
+    gerr = hs.hs_get_error(gpu.h, clear=True)
+    assert gerr == oerr
+    for layer in range(wl.L):
+        assert np.array_equal(gpu.dev[layer].cpu().numpy(), orc.dev[layer]), "device pools differ"
+    return gerr
+
+
+def warm(wl, orc, gpu, n=3):
+    for s in range(n):
+        assert step_both(wl, orc, gpu, s) == 0
+
+
+def set_both(gpu, orc, name, r, s, v):
+    getattr(orc, name)[r, s] = v
+    t = gpu.tok if name == "tokens" else gpu.st
+    t[r, s] = v
+
+
+def test_corrupt_slot_state(pair):
+    wl, orc, gpu = pair
+    warm(wl, orc, gpu)
+    set_both(gpu, orc, "stamps", 0, 5, 10**6)  # stamp from the future
+    set_both(gpu, orc, "stamps", 1, 7, -3)  # negative stamp
+    set_both(gpu, orc, "tokens", 1, 9, 10**7)  # token beyond the sequence
+    set_both(gpu, orc, "tokens", 2, 11, -9)  # token below -1
+    # two slots hold the same token that this step looks up
+    tk = wl.top_k_tokens(3)
+    held = orc.tokens[2]
+    S = int(wl.seq_lens(3)[2])
+    t = next(int(x) for x in tk[2] if x >= 0 and x != S - 1 and x in set(held.tolist()))
+    s0 = int(np.nonzero(held == t)[0][0])
+    other = next(s for s in range(wl.H) if s != s0 and orc.tokens[2, s] >= 0)
+    set_both(gpu, orc, "tokens", 2, other, t)
+    err = step_both(wl, orc, gpu, 3)
+    assert err == ERR["STATE"]
+    for s in range(4, 8):
+        assert step_both(wl, orc, gpu, s) in (0, ERR["STATE"])
+
+
+def test_bad_and_repeated_tokens(pair):
+    wl, orc, gpu = pair
+    warm(wl, orc, gpu)
+    tk = wl.top_k_tokens(3).copy()
+    S = wl.seq_lens(3)
+    tk[0, 0] = S[0] + 17  # beyond the sequence
+    tk[1, 3] = tk[1, 4]  # repeated token
+    tk[2, :] = -1  # all padding
+    err = step_both(wl, orc, gpu, 3, tk=tk)
+    assert err == ERR["TOKEN"] | ERR["DUP"]
+
+
+def test_host_row_out_of_range_zero_fills(pair):
+    wl, orc, gpu = pair
+    warm(wl, orc, gpu)
+    tk = wl.top_k_tokens(3)
+    hcl = wl.host_cache_locs.copy()
+    S = wl.seq_lens(3)
+    for r in range(3):  # a token of each long request that is not in its hot set
+        held = set(orc.tokens[r].tolist())
+        t = next(int(x) for x in tk[r] if x >= 0 and x != S[r] - 1 and int(x) not in held)
+        hcl[r, t] = wl.host_rows + 5 if r != 1 else -4
+    err = step_both(wl, orc, gpu, 3, hcl=hcl)
+    assert err == ERR["HOSTROW"]
+
+
+def test_device_row_out_of_range(pair):
+    wl, orc, gpu = pair
+    warm(wl, orc, gpu)
+    dbl = wl.device_buffer_locs.copy()
+    dbl[0, wl.H] = wl.device_rows + 3  # reserved newest row of a long request
+    dbl[1, 17] = -2  # a hot slot
+    dbl[3, 5] = 1 << 30  # a fast-path slot
+    err = step_both(wl, orc, gpu, 3, dbl=dbl)
+    assert err & ERR["DEVROW"]
+
+
+def test_seq_len_beyond_max_context(pair):
+    wl, orc, gpu = pair
+    warm(wl, orc, gpu)
+    sl = wl.seq_lens(3).copy()
+    sl[1] = wl.max_context + 1
+    err = step_both(wl, orc, gpu, 3, sl=sl)
+    assert err == ERR["SEQLEN"]
+
+
+def test_api_misuse():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import hierarchical_sparse_attention_gb300 as hs
+    from gpu_harness import alloc_host
+    cfg = hs.make_config(2, 64, 128, 576, 1, 0, 1024, 0)
+    dev = torch.zeros(1000 * 576, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(hs.hs_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    host = alloc_host(1000 * 576)
+    with pytest.raises(hs.HsError) as e:  # host pool not registered
+        hs.hs_create(cfg, [host], [dev], 1000, 1000, ws)
+    assert e.value.status == hs.HS_ERR_INVALID_ARG
+    hs.hs_host_register(host)
+    try:
+        with pytest.raises(hs.HsError) as e:  # device pool given as host memory
+            hs.hs_create(cfg, [host], [host], 1000, 1000, ws)
+        assert e.value.status == hs.HS_ERR_INVALID_ARG
+        with pytest.raises(hs.HsError) as e:  # workspace on the host
+            hs.hs_create(cfg, [host], [dev], 1000, 1000, host)
+        assert e.value.status == hs.HS_ERR_INVALID_ARG
+        with pytest.raises(hs.HsError) as e:  # more rows than int32 tables can address
+            hs.hs_create(cfg, [host], [dev], 1 << 33, 1000, ws)
+        assert e.value.status == hs.HS_ERR_INVALID_ARG
+        big = hs.make_config(2, 4096, 16384, 576, 1, 0, 1024, 0)  # shared memory does not fit
+        with pytest.raises(hs.HsError) as e:
+            hs.hs_create(big, [host], [dev], 1000, 1000, ws)
+        assert e.value.status == hs.HS_ERR_INVALID_CONFIG
+        h = hs.hs_create(cfg, [host], [dev], 1000, 1000, ws)
+        i32 = lambda *s: torch.zeros(s, dtype=torch.int32, device="cuda")  # noqa: E731
+        tk, sl, hcl, dbl = i32(2, 64), i32(2), i32(2, 1024), i32(2, 129)
+        tok, st, clk, out, miss = i32(2, 128), i32(2, 128), i32(2), i32(2, 64), i32(2)
+        with pytest.raises(hs.HsError) as e:  # more requests than configured
+            hs.hs_resolve(h, 3, tk, sl, hcl, dbl, tok, st, clk, None, out, miss)
+        assert e.value.status == hs.HS_ERR_INVALID_ARG
+        with pytest.raises(hs.HsError) as e:  # missing table
+            hs.hs_resolve(h, 2, tk, sl, None, dbl, tok, st, clk, None, out, miss)
+        assert e.value.status == hs.HS_ERR_INVALID_ARG
+        with pytest.raises(hs.HsError) as e:  # resident pages without a page size
+            hs.hs_resolve(h, 2, tk, sl, hcl, dbl, tok, st, clk, i32(2, 4), out, miss)
+        assert e.value.status == hs.HS_ERR_INVALID_ARG
+        out.fill_(123)
+        hs.hs_resolve(h, 0, tk, sl, hcl, dbl, tok, st, clk, None, out, miss)  # empty batch: no-op
+        hs.hs_backup(h, 0, sl, hcl, dbl, None)
+        torch.cuda.synchronize()
+        assert int(out.min()) == 123 and int(out.max()) == 123
+        assert hs.hs_get_error(h) == 0
+        hs.hs_destroy(h)
+    finally:
+        hs.hs_host_unregister(host)
+
+
+def test_partial_batch_leaves_other_requests_alone(pair):
+    wl, orc, gpu = pair
+    warm(wl, orc, gpu)
+    before = gpu.state()
+    gpu.write_newest(3)
+    gpu.upload(3)
+    gpu.resolve(num_requests=2)
+    torch.cuda.synchronize()
+    after = gpu.state()
+    for k in ("tokens", "stamps", "clock"):
+        np.testing.assert_array_equal(after[k][2:], before[k][2:])
+    np.testing.assert_array_equal(after["out"][2:], before["out"][2:])

@@ -1,0 +1,138 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, bit-exact.
+
+Each step, both sides get the same seeded inputs; the test compares the physical row
+table, the miss counts, the slot map, the stamps, the clock and the error flags every
+step, the eager backup's host rows every step, and the whole device pools (hot rows,
+reserved rows, resident pages) at intervals and at the end. All comparisons are exact:
+the path is integer bookkeeping and byte copies.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads as W  # noqa: E402
+from harness import OracleSim, host_newest_ok, poison_host_newest  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import hierarchical_sparse_attention_gb300 as hs  # noqa: F401
+    from gpu_harness import GpuSim, host_pools
+    return GpuSim, host_pools
+
+
+def compare_step(gpu, orc, what):
+    import hierarchical_sparse_attention_gb300 as hs
+    g = gpu.state()
+    np.testing.assert_array_equal(g["out"], orc.out, err_msg=f"{what}: out_rows")
+    np.testing.assert_array_equal(g["miss"], orc.miss, err_msg=f"{what}: miss_counts")
+    np.testing.assert_array_equal(g["tokens"], orc.tokens, err_msg=f"{what}: device_buffer_tokens")
+    np.testing.assert_array_equal(g["stamps"], orc.stamps, err_msg=f"{what}: lru_slots")
+    np.testing.assert_array_equal(g["clock"], orc.clock, err_msg=f"{what}: lru_clock")
+    return hs.hs_get_error(gpu.h, clear=True)
+
+
+def compare_pools(gpu, orc, what):
+    for layer in range(len(gpu.dev)):
+        d = gpu.dev[layer].cpu().numpy()
+        if not np.array_equal(d, orc.dev[layer]):
+            rows = np.nonzero((d.reshape(-1, orc.wl.B) != orc.dev[layer].reshape(-1, orc.wl.B)).any(1))[0]
+            raise AssertionError(f"{what}: device pool layer {layer} differs in {len(rows)} rows, e.g. {rows[:8]}")
+
+
+def run_parity(wl, host=None, steps=None, pool_every=8, graph_from=None):
+    GpuSim, host_pools = _gpu()
+    host = host if host is not None else host_pools(wl)
+    orc = OracleSim(wl, host_pools=host)
+    gpu = GpuSim(wl, host, orc.dev)
+    steps = wl.steps if steps is None else steps
+    graph = None
+    try:
+        for step in range(steps):
+            gpu.write_newest(step)
+            orc.write_newest(step)
+            poison_host_newest(wl, step, host)
+            gpu.upload(step)
+            if graph_from is not None and step >= graph_from:
+                if graph is None:
+                    graph = torch.cuda.CUDAGraph()
+                    s = torch.cuda.Stream()
+                    s.wait_stream(torch.cuda.current_stream())
+                    with torch.cuda.graph(graph, stream=s):
+                        gpu.resolve(stream=torch.cuda.current_stream())
+                        gpu.backup(stream=torch.cuda.current_stream())
+                    torch.cuda.current_stream().wait_stream(s)
+                graph.replay()  # inputs were refreshed in place by upload()
+            else:
+                gpu.resolve()
+                gpu.backup()
+            torch.cuda.synchronize()
+            assert host_newest_ok(wl, step, host), f"step {step}: backup did not restore the newest host rows"
+            oerr = orc.resolve(step)
+            oerr |= orc.backup(step)
+            gerr = compare_step(gpu, orc, f"{wl.cfg.name} step {step}")
+            assert gerr == oerr, f"step {step}: flags gpu {gerr} oracle {oerr}"
+            if (step + 1) % pool_every == 0 or step == steps - 1:
+                compare_pools(gpu, orc, f"{wl.cfg.name} step {step}")
+    finally:
+        gpu.close()
+    return orc
+
+
+def test_tiny():
+    orc = run_parity(W.make("tiny"), pool_every=1)
+    assert orc.miss[0] > 0
+
+
+def test_tiny_fast_to_slow_transition():
+    wl = W.make("tiny", seq0=(8192, 120))  # request 1 outgrows the 128-slot buffer at step 9
+    run_parity(wl, pool_every=1)
+
+
+def test_dsa_decode_shape():
+    run_parity(W.make("dsa"), pool_every=16)
+
+
+def test_mixed_residency_1m():
+    run_parity(W.make("mixed1m"), pool_every=16)
+
+
+def test_indexshare_4_layers():
+    run_parity(W.make("indexshare"), pool_every=32)
+
+
+def test_miss_rate_sweep():
+    _, host_pools = _gpu()
+    base = W.make("sweep_h4096_f0.8")
+    host = host_pools(base)  # token rows and host layout do not depend on the sweep point
+    for h in W.SWEEP_HOT:
+        for f in W.SWEEP_REUSE:
+            wl = W.make(f"sweep_h{h}_f{f}")
+            assert wl.host_rows == base.host_rows
+            run_parity(wl, host=host, pool_every=32)
+
+
+@pytest.mark.parametrize("shape", [
+    dict(requests=3, top_k=1000, hot_slots=3001, row_bytes=100, layers=3, seq0=(9000, 2000, 2500)),  # 4-byte path
+    dict(requests=2, top_k=77, hot_slots=131, row_bytes=37, layers=2, seq0=(5000, 90)),  # byte path
+    dict(requests=5, top_k=1, hot_slots=1, row_bytes=48, layers=1, seq0=(40, 1, 2, 3, 500)),  # K = H = 1
+    dict(requests=4, top_k=2, hot_slots=2, row_bytes=32, layers=2, seq0=(40, 1, 2, 300)),  # K = H = 2
+    dict(requests=2, top_k=2048, hot_slots=2048, row_bytes=656, layers=1, seq0=(300000, 2100)),  # H = K
+])
+def test_ragged_shapes(shape):
+    kw = dict(shape)
+    kw.setdefault("steps", 10)
+    wl = W.make("tiny", fmt=W.FMT_U8, **kw)
+    run_parity(wl, pool_every=1)
+
+
+def test_graph_capture_replay():
+    run_parity(W.make("dsa", requests=8, steps=12), pool_every=4, graph_from=2)
+
+
+def test_graph_capture_replay_indexshare():
+    run_parity(W.make("indexshare", requests=16, steps=8, layers=2), pool_every=4, graph_from=1)
