@@ -106,9 +106,9 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return HS_ERR_CUDA;
   if (hs::resolve_smem_bytes(g) > (size_t)optin) return HS_ERR_INVALID_CONFIG;
-  if (hs::resolve_prepare(g) != cudaSuccess) {
+  if (const cudaError_t e = hs::resolve_prepare(g); e != cudaSuccess) {
     cudaGetLastError();
-    return HS_ERR_CUDA;
+    return e == cudaErrorInvalidValue ? HS_ERR_INVALID_CONFIG : HS_ERR_CUDA;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (cudaMemset(ws, 0, hs::kWorkspaceBytes) != cudaSuccess) return HS_ERR_CUDA;

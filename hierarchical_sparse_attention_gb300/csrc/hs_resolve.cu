@@ -577,9 +577,20 @@ __global__ void __launch_bounds__(T, 1)
 
 size_t resolve_smem_bytes(const Geometry& g) { return make_layout(g).total; }
 
+// Raise the kernel's dynamic shared-memory ceiling to the most the device allows beside
+// the kernel's static shared memory (not to this geometry's size): the attribute is per
+// function and device, so a smaller value set for one handle would make launches of a
+// larger, earlier handle fail.
 cudaError_t resolve_prepare(const Geometry& g) {
-  return cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)resolve_smem_bytes(g));
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa{};
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, resolve_kernel);
+  if (e != cudaSuccess) return e;
+  const int max_dynamic = optin - (int)fa.sharedSizeBytes;
+  if (resolve_smem_bytes(g) > (size_t)max_dynamic) return cudaErrorInvalidValue;
+  return cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic);
 }
 
 cudaError_t launch_resolve(const Geometry& g, const Pools* pools, const ResolveArgs& a, int32_t num_requests,

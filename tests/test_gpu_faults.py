@@ -205,3 +205,32 @@ def test_partial_batch_leaves_other_requests_alone(pair):
     for k in ("tokens", "stamps", "clock"):
         np.testing.assert_array_equal(after[k][2:], before[k][2:])
     np.testing.assert_array_equal(after["out"][2:], before["out"][2:])
+
+
+def test_two_handles_with_different_shared_memory_sizes():
+    """Creating a smaller handle after a larger one must not break the larger one's launches."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gpu_harness import GpuSim, host_pools
+    big = W.make("dsa", requests=2, top_k=2048, hot_slots=6144, steps=2, seq0=(20000, 30000))
+    small = W.make("tiny", steps=2)
+    hb, hsm = host_pools(big), host_pools(small)
+    ob, osm = OracleSim(big, host_pools=hb), OracleSim(small, host_pools=hsm)
+    gb = GpuSim(big, hb, ob.dev)
+    gs = GpuSim(small, hsm, osm.dev)  # created second, needs less shared memory
+    try:
+        for s in range(2):
+            for wl, o, g in ((big, ob, gb), (small, osm, gs)):
+                g.write_newest(s)
+                o.write_newest(s)
+                g.upload(s)
+                g.resolve()
+                g.backup()
+                torch.cuda.synchronize()
+                o.resolve(s)
+                o.backup(s)
+                np.testing.assert_array_equal(g.state()["out"], o.out)
+                np.testing.assert_array_equal(g.state()["stamps"], o.stamps)
+    finally:
+        gb.close()
+        gs.close()
