@@ -26,7 +26,8 @@ HS_MAX_TOP_K, HS_MAX_HOT_SLOTS, HS_MAX_LAYERS = 4096, 16384, 8
 
 # Every symbol include/hs.h declares (checked against the library by the tests).
 EXPORTS = ("hs_workspace_bytes", "hs_create", "hs_resolve", "hs_backup", "hs_get_error", "hs_destroy",
-           "hs_status_str", "hs_host_register", "hs_host_unregister")
+           "hs_status_str", "hs_host_register", "hs_host_unregister", "hs_resolve_noalloc")
+HS_NOALLOC_MAX_LAYERS = 8
 
 
 class hs_config(ctypes.Structure):
@@ -65,6 +66,8 @@ def _load() -> ctypes.CDLL:
     lib.hs_host_register.restype = ctypes.c_int
     lib.hs_host_unregister.argtypes = [P]
     lib.hs_host_unregister.restype = ctypes.c_int
+    lib.hs_resolve_noalloc.argtypes = [cfgp, P, P, i64, i64, i32] + [P] * 11 + [P]
+    lib.hs_resolve_noalloc.restype = ctypes.c_int
     return lib
 
 
@@ -190,3 +193,19 @@ def hs_host_register(host_array, nbytes: Optional[int] = None) -> int:
 
 def hs_host_unregister(host_array) -> None:
     _check(_lib.hs_host_unregister(_addr(host_array)), "hs_host_unregister")
+
+
+def hs_resolve_noalloc(cfg: hs_config, host_pools: Sequence, device_pools: Sequence, host_rows: int,
+                       device_rows: int, num_requests: int, top_k_tokens, seq_lens, host_cache_locs,
+                       device_buffer_locs, device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows,
+                       miss_counts, error_flags=None, stream=None) -> None:
+    """hs_resolve without a handle or workspace, for callers that cannot allocate device
+    memory: the library keeps the scratch in its own device array (see include/hs.h)."""
+    hp = (ctypes.c_void_p * len(host_pools))(*[_addr(p) for p in host_pools])
+    dp = (ctypes.c_void_p * len(device_pools))(*[_addr(p) for p in device_pools])
+    _check(_lib.hs_resolve_noalloc(ctypes.byref(cfg), hp if len(host_pools) else None,
+                                   dp if len(device_pools) else None, host_rows, device_rows, num_requests,
+                                   _addr(top_k_tokens), _addr(seq_lens), _addr(host_cache_locs),
+                                   _addr(device_buffer_locs), _addr(device_buffer_tokens), _addr(lru_slots),
+                                   _addr(lru_clock), _addr(resident_pages), _addr(out_rows), _addr(miss_counts),
+                                   _addr(error_flags), _stream(stream)), "hs_resolve_noalloc")

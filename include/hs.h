@@ -193,6 +193,37 @@ HS_API hs_status hs_host_register(void* ptr, size_t bytes, void** device_ptr);
 /* Undo hs_host_register. */
 HS_API hs_status hs_host_unregister(void* ptr);
 
+/* hs_resolve for callers that cannot allocate device memory. The pages have no
+ * counterpart for this entry point: it exists for callers with no way to make the
+ * workspace allocation hs_create needs -- engines whose device memory is all planned
+ * before decoding starts, plugins running inside another framework's allocator, or
+ * processes that must not call cudaMalloc on the decode path.
+ *
+ * It takes the configuration and pools that hs_create takes, plus every argument of
+ * hs_resolve, and runs the same resolve kernel with the same results. Instead of a
+ * caller workspace it uses a 256-byte file-scope device array inside the library: the
+ * error word and the pools table of at most HS_NOALLOC_MAX_LAYERS layers (num_layers
+ * above that: HS_ERR_INVALID_CONFIG). Every device that loads the library holds its own
+ * copy of that array until the process exits. The call allocates nothing: no cudaMalloc,
+ * no cudaFree, no allocating library routine.
+ *
+ * The first call on a device, with that device current, looks up the array's device
+ * address (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ * capture. Each call then queues, on `stream`, a copy of the pools table and a clear of
+ * the error word into the array, the resolve kernel, and, when error_flags is not NULL,
+ * a copy of this call's HS_FLAG_* bits into error_flags (one uint32 in device memory).
+ * All calls share the array and it keeps the last call's contents, so calls whose work
+ * overlaps on the GPU (on streams not ordered against each other) race; order them on
+ * one stream. Returns the status codes of hs_create and hs_resolve. */
+#define HS_NOALLOC_MAX_LAYERS 8
+HS_API hs_status hs_resolve_noalloc(const hs_config* cfg, void* const* host_pools, void* const* device_pools,
+                                    int64_t host_rows, int64_t device_rows, int32_t num_requests,
+                                    const int32_t* top_k_tokens, const int32_t* seq_lens,
+                                    const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
+                                    int32_t* device_buffer_tokens, int32_t* lru_slots, int32_t* lru_clock,
+                                    const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
+                                    uint32_t* error_flags, hs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
