@@ -63,7 +63,7 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   g.page_size = cfg->page_size;
   g.max_context = cfg->max_context;
   g.max_pages = cfg->max_pages;
-  g.hash_bits = ceil_log2(2 * (int64_t)cfg->top_k);
+  g.hash_bits = ceil_log2(4 * (int64_t)cfg->top_k);  // top-k hash at most a quarter full
   if (g.hash_bits < 5) g.hash_bits = 5;
   g.sort_cap = 1 << ceil_log2(cfg->top_k);
   if (g.hash_bits < ceil_log2(cfg->top_k) + 1) g.hash_bits = ceil_log2(cfg->top_k) + 1;  // room for the aliases
@@ -106,7 +106,7 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return HS_ERR_CUDA;
   if (hs::resolve_smem_bytes(g) > (size_t)optin) return HS_ERR_INVALID_CONFIG;
-  if (const cudaError_t e = hs::resolve_prepare(g); e != cudaSuccess) {
+  if (const cudaError_t e = hs::resolve_prepare(g, cfg->max_requests); e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorInvalidValue ? HS_ERR_INVALID_CONFIG : HS_ERR_CUDA;
   }

@@ -29,6 +29,8 @@ struct Geometry {
   int32_t hash_bits;  // top-k hash table holds 1 << hash_bits >= 2K entries
   int32_t sort_cap;   // power of two >= K: capacity of the victim sort buffer
   int32_t vec;        // bytes per copy piece: 16, 4 or 1
+  int32_t copy_ctas;  // copy CTAs clustered with each request's resolve CTA (0: it copies alone)
+  int32_t copy_cap;   // misses one copy CTA can stage (all layers) in its shared memory
   int64_t host_rows, device_rows;
 };
 
@@ -58,8 +60,12 @@ constexpr size_t kPoolsOffset = 64;  // Pools table
 constexpr size_t kWorkspaceBytes = 256;
 static_assert(kPoolsOffset + sizeof(Pools) <= kWorkspaceBytes, "workspace too small for the pools table");
 
+// Dynamic shared memory of one resolve-kernel CTA for geometry g.
 size_t resolve_smem_bytes(const Geometry& g);
-cudaError_t resolve_prepare(const Geometry& g);
+// Choose the copy CTAs per request (sets g.copy_ctas / g.copy_cap from the device's shared
+// memory, SM count and max_requests) and raise the kernel's dynamic shared-memory limit.
+// cudaErrorInvalidValue: g does not fit the device.
+cudaError_t resolve_prepare(Geometry& g, int32_t max_requests);
 cudaError_t launch_resolve(const Geometry& g, const Pools* pools, const ResolveArgs& a, int32_t num_requests,
                            uint32_t* err_word, cudaStream_t stream);
 cudaError_t launch_backup(const Geometry& g, const Pools* pools, const BackupArgs& a, int32_t num_requests,

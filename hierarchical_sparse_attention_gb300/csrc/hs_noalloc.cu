@@ -95,7 +95,7 @@ hs_status hs_resolve_noalloc(const hs_config* cfg, void* const* host_pools, void
   g.page_size = cfg->page_size;
   g.max_context = cfg->max_context;
   g.max_pages = cfg->max_pages;
-  g.hash_bits = ceil_log2_i64(2 * (int64_t)cfg->top_k);
+  g.hash_bits = ceil_log2_i64(4 * (int64_t)cfg->top_k);  // top-k hash at most a quarter full
   if (g.hash_bits < 5) g.hash_bits = 5;
   g.sort_cap = 1 << ceil_log2_i64(cfg->top_k);
   if (g.hash_bits < ceil_log2_i64(cfg->top_k) + 1) g.hash_bits = ceil_log2_i64(cfg->top_k) + 1;
@@ -121,7 +121,7 @@ hs_status hs_resolve_noalloc(const hs_config* cfg, void* const* host_pools, void
     a4 = a4 && aligned_to(pools.host[l], 4) && aligned_to(pools.dev[l], 4);
   }
   g.vec = a16 ? 16 : (a4 ? 4 : 1);
-  if (hs::resolve_prepare(g) != cudaSuccess) {
+  if (hs::resolve_prepare(g, cfg->max_requests) != cudaSuccess) {
     cudaGetLastError();
     return HS_ERR_INVALID_CONFIG;  // shared memory does not fit this device
   }

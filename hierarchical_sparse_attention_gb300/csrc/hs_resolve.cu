@@ -11,27 +11,39 @@
 //     then hot row with LRU refresh, then a victim filled from pinned host memory).
 //   "vLLM Hybrid HiSparse source implementation analysis", 7.2 (resident short-circuit;
 //     a shared-memory hash of the top-k; ballot/scan compaction of the misses; victims
-//     from the cold end; out-of-range state downgraded to a re-miss; warp-wide 16-byte
-//     copies that zero the destination when the source row is out of range), 7.3 (flat
-//     physical row IDs) and 7.4 (layers sharing the indexer reuse the same slot plan).
+//     from the cold end; out-of-range state downgraded to a re-miss; wide vector copies
+//     that zero the destination when the source row is out of range), 7.3 (flat physical
+//     row IDs) and 7.4 (layers sharing the indexer reuse the same slot plan).
 //   "Hierarchical Sparse Attention" (Alibaba Tair), 2.4.3 "LRU Diff Kernel" (evict only
 //     when the buffer is full, coldest first).
 //
-// Phases of one CTA (request r), all state in shared memory:
-//   1  load the top-k row, reject padding / out-of-range tokens, build an open-addressing
-//      hash (Knuth multiplicative) of the valid tokens; repeated tokens keep the first index
-//   2  classify: resident row, fast-path identity, reserved newest row, or hot lookup
-//   3  load slot tokens and stamps, reset corrupt entries, probe each slot's token in the
-//      hash; the lowest slot holding a looked-up token claims it (atomicMin)
-//   4  hits: stamp = clock, output the slot's row
-//   5  one packed block scan compacts the misses (top-k order) and the free slots (slot order);
-//      each miss's host row is looked up and a bulk L2 prefetch of it is issued right away
-//   6  if misses outnumber free slots: radix-select the stamp threshold over the occupied,
-//      un-hit slots, gather exactly the needed victims, bitonic-sort them by (stamp, slot)
-//   7  pair miss j with victim j, update the map, build the copy plan
-//   8  write back the changed slots, the output row table and the clock
-//   9  copy every miss row of every layer (now mostly in L2) to its victim's device row
-//      (16-byte pieces spread over all 1024 threads, several loads in flight per thread)
+// The step is latency-bound (a few MB over the host link, a few tens of KB of state per
+// request), so the kernel is arranged to start the host-link transfer as early as
+// possible and to hide the rest of the bookkeeping behind it. Each request gets a thread
+// block cluster: CTA 0 resolves, and up to three copy CTAs on other SMs move the miss rows.
+// Phases of the resolve CTA (request r):
+//   0  cp.async the top-k row, the slot map, the stamps and the slot->row table into
+//      shared memory while the hash table is cleared
+//   1  reject padding / out-of-range tokens; hash the valid ones (open addressing,
+//      Knuth multiplicative); a repeated token keeps its first index
+//   2  classify each entry: resident row, fast-path identity, reserved newest row, or hot
+//      lookup
+//   3  reset corrupt slots; probe each slot's token; the first slot to claim a looked-up
+//      token takes the hit (stamp = clock). Two holders of one token (corrupt state only)
+//      are settled afterwards in favour of the lowest slot
+//   4  hits output their slot's row; each miss token is handed, through distributed shared
+//      memory, to a copy CTA, which starts pulling its host row(s) into its own shared
+//      memory while the resolve CTA goes on (split cluster barrier, phase A)
+//   5  one packed block scan orders the misses (top-k order) and the free slots (slot order)
+//   6  if misses outnumber free slots: radix-select the stamp threshold among occupied,
+//      un-hit slots, take exactly the needed victims and order them by (stamp, slot)
+//   7  pair miss j with victim j: update the map; send each handed-off miss's device row
+//      to its copy CTA (cluster barrier, phase B)
+//   8  write back the changed slots, the row table and the clock
+//   9  copy the misses no copy CTA took (none, unless the copy CTAs' staging is full or
+//      the geometry runs without them) straight from host memory
+// A copy CTA: wait for its miss tokens (phase A), look up their host rows, cp.async the
+// rows into shared memory, wait for the device rows (phase B), then store them.
 #include <climits>
 
 #include "hs_internal.h"
@@ -44,18 +56,27 @@ constexpr int NW = T / 32;
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int32_t INF = 0x7fffffff;
 constexpr int kCopyUnroll = 4;
+constexpr int kRankSortMax = 1024;  // victims ordered by counting ranks up to this many
 
-enum : uint8_t { C_PAD = 0, C_BAD, C_DUP, C_VALID, C_RES, C_FAST, C_NEWEST, C_LOOKUP };
+enum : uint8_t { C_PAD = 0, C_BAD, C_DUP, C_RES, C_FAST, C_NEWEST, C_LOOKUP };
+constexpr uint8_t C_BADROW = 0x80;  // with C_RES / C_FAST / C_NEWEST: its row is out of range
 enum : uint8_t { SF_USED = 1, SF_DIRTY = 2 };
-enum { SC_LO = 0, SC_HI, SC_DIGIT, SC_RANK, SC_COUNT };
+enum { SC_LO = 0, SC_HI, SC_DIGIT, SC_RANK, SC_CONFLICT, SC_STAGED, SC_DIRECT, SC_COUNT };
 
-// Shared-memory carve-up; identical arithmetic on host (size) and device (pointers).
-// The top-k hash (1 << hash_bits = 2 * sort_cap int32 keys and values) is dead after
-// phase 3, so the victim sort keys (phase 6) and the copy plan (phases 7-9) reuse it:
-// 8*sort_cap bytes of keys, then K source rows and K destination rows (K <= sort_cap).
+// Shared-memory carve-up of the resolve CTA; identical arithmetic on host (size) and device
+// (pointers). The top-k hash (1 << hash_bits buckets of one 64-bit word: token << 32 |
+// top-k index; at least 2 * sort_cap of them) is dead after phase 3, so it holds the
+// victim keys of phase 6 and the copy plan of phases 7-9. The slot->row table gets three
+// spare words so it can start at its global row's 16-byte phase (whole-vector loads).
 struct Layout {
-  size_t hkey, hval, keys, psrc, pdst, tk, out, claim, miss, vict, tok, stamp, sent, cls, sflag, wsum, hist,
+  size_t hash, keys, psrc, pdst, tk, out, claim, miss, vict, tok, stamp, dbl, stage_of, cls, sflag, wsum, hist,
       sc, total;
+};
+
+// Shared-memory carve-up of a copy CTA: the miss tokens it was handed, their host rows,
+// their device rows, and the staging area (copy_cap misses x L rows of B bytes).
+struct CopyLayout {
+  size_t count, tok, hrow, drow, stage, total;
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -64,10 +85,9 @@ __host__ __device__ inline Layout make_layout(const Geometry& g) {
   Layout l;
   size_t o = 0;
   const size_t K = (size_t)g.K, H = (size_t)g.H, HS = (size_t)1 << g.hash_bits;
-  l.hkey = o; o = align16(o + 4 * HS);
-  l.hval = o; o = align16(o + 4 * HS);
-  l.keys = l.hkey;
-  l.psrc = l.hkey + sizeof(uint64_t) * (size_t)g.sort_cap;
+  l.hash = o; o = align16(o + 8 * HS);
+  l.keys = l.hash;
+  l.psrc = l.hash + sizeof(uint64_t) * (size_t)g.sort_cap;
   l.pdst = l.psrc + 4 * K;
   l.tk = o; o = align16(o + 4 * K);
   l.out = o; o = align16(o + 4 * K);
@@ -76,12 +96,26 @@ __host__ __device__ inline Layout make_layout(const Geometry& g) {
   l.vict = o; o = align16(o + 4 * K);
   l.tok = o; o = align16(o + 4 * H);
   l.stamp = o; o = align16(o + 4 * H);
-  l.sent = o; o = align16(o + 2 * H);
+  l.dbl = o; o = align16(o + 4 * (H + 1 + 3));
+  l.stage_of = o; o = align16(o + 2 * K);
   l.cls = o; o = align16(o + K);
   l.sflag = o; o = align16(o + H);
   l.wsum = o; o = align16(o + 4 * (NW + 1));
   l.hist = o; o = align16(o + 4 * 256);
   l.sc = o; o = align16(o + 4 * SC_COUNT);
+  l.total = o;
+  return l;
+}
+
+__host__ __device__ inline CopyLayout make_copy_layout(const Geometry& g) {
+  CopyLayout l;
+  size_t o = 0;
+  const size_t cap = (size_t)g.copy_cap;
+  l.count = o; o = align16(o + 16);
+  l.tok = o; o = align16(o + 4 * cap);
+  l.hrow = o; o = align16(o + 4 * cap);
+  l.drow = o; o = align16(o + 4 * cap);
+  l.stage = o; o = align16(o + cap * (size_t)g.L * (size_t)g.B);
   l.total = o;
   return l;
 }
@@ -120,29 +154,43 @@ __device__ __forceinline__ uint32_t hash_slot(int32_t t, int bits) {
   return ((uint32_t)t * 2654435761u) >> (32 - bits);
 }
 
-// Insert token t for top-k index i; a repeated token keeps the smallest index.
-__device__ __forceinline__ void hash_insert(int32_t* hkey, int32_t* hval, int bits, int32_t t, int32_t i) {
+constexpr uint64_t kEmpty = ~0ull;  // bucket never written (tokens are < 2^31)
+
+// Insert token t for top-k index i; a repeated token keeps the smallest index (same key
+// bits, so the 64-bit minimum picks the smaller index).
+__device__ __forceinline__ void hash_insert(unsigned long long* tab, int bits, int32_t t, int32_t i) {
   const uint32_t mask = (1u << bits) - 1;
+  const unsigned long long w = ((unsigned long long)(uint32_t)t << 32) | (uint32_t)i;
   uint32_t h = hash_slot(t, bits);
-  for (;;) {  // ends: the table is at most half full
-    const int32_t prev = atomicCAS(&hkey[h], -1, t);
-    if (prev == -1 || prev == t) {
-      atomicMin(&hval[h], i);
+  for (;;) {  // ends: the table is at most a quarter full
+    const unsigned long long prev = atomicCAS(&tab[h], kEmpty, w);
+    if (prev == kEmpty) return;
+    if ((uint32_t)(prev >> 32) == (uint32_t)t) {
+      atomicMin(&tab[h], w);
       return;
     }
     h = (h + 1) & mask;
   }
 }
 
-__device__ __forceinline__ int hash_find(const int32_t* hkey, int bits, int32_t t) {
+// Top-k index recorded for token t, or -1.
+__device__ __forceinline__ int32_t hash_find(const unsigned long long* tab, int bits, int32_t t) {
   const uint32_t mask = (1u << bits) - 1;
   uint32_t h = hash_slot(t, bits);
-  for (;;) {  // ends: at least half the table is empty
-    const int32_t k = hkey[h];
-    if (k == t) return (int)h;
-    if (k == -1) return -1;
+  for (;;) {  // ends: at least three quarters of the table are empty
+    const unsigned long long w = tab[h];
+    if (w == kEmpty) return -1;
+    if ((uint32_t)(w >> 32) == (uint32_t)t) return (int32_t)(uint32_t)w;
     h = (h + 1) & mask;
   }
+}
+
+// Top-k index whose token a slot holds, if that entry is a hot lookup; else -1.
+__device__ __forceinline__ int32_t lookup_entry(const unsigned long long* tab, const uint8_t* cls, int bits,
+                                                int32_t tkn) {
+  if (tkn < 0) return -1;
+  const int32_t i = hash_find(tab, bits, tkn);
+  return (i >= 0 && cls[i] == C_LOOKUP) ? i : -1;
 }
 
 __device__ __forceinline__ int32_t checked_row(int64_t row, int64_t rows, uint32_t& flags) {
@@ -152,6 +200,47 @@ __device__ __forceinline__ int32_t checked_row(int64_t row, int64_t rows, uint32
   }
   return (int32_t)row;
 }
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Asynchronous copies global -> shared (completed by cp_async_wait_all + a barrier).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+// Queue an asynchronous copy of n int32 from global src to shared dst: 16-byte pieces over
+// the part where both addresses are 16-byte aligned (same phase), 4-byte pieces elsewhere.
+__device__ __forceinline__ void cp_async_words(int32_t* dst, const int32_t* src, int n) {
+  const int head = ((uintptr_t)src & 15) == ((uintptr_t)smem_addr(dst) & 15)
+                       ? min(n, (int)((16 - ((uintptr_t)src & 15)) & 15) / 4)
+                       : n;
+  const int body = (n - head) & ~3;
+  for (int i = threadIdx.x; i < head; i += T) cp_async4(dst + i, src + i);
+  for (int i = threadIdx.x; i < body / 4; i += T) cp_async16(dst + head + 4 * i, src + head + 4 * i);
+  for (int i = head + body + threadIdx.x; i < n; i += T) cp_async4(dst + i, src + i);
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Thread block cluster primitives: this CTA's rank, a store into another CTA's shared
+// memory (distributed shared memory), and the split cluster barrier. A release-arrive
+// publishes this thread's earlier stores (local or remote) to threads that acquire-wait.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void st_remote(const void* local_addr, uint32_t rank, int32_t v) {
+  uint32_t raddr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_addr(local_addr)), "r"(rank));
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(raddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 // Ascending bitonic sort of n (a power of two) 64-bit keys in shared memory.
 __device__ void bitonic_sort(uint64_t* keys, int n) {
@@ -175,21 +264,10 @@ __device__ void bitonic_sort(uint64_t* keys, int n) {
 // Miss rows are read once: stream them past the caches.
 __device__ __forceinline__ uint4 load_host16(const uint4* p) { return __ldcs(p); }
 
-// Start pulling a host row into L2 as soon as the miss is known, so the link transfer
-// overlaps victim selection; the copy in phase 9 then reads it from L2.
-__device__ __forceinline__ void prefetch_row_l2(const uint8_t* p, int bytes, int vec) {
-  if (vec == 16) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-  } else {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    for (uintptr_t line = a & ~uintptr_t(127); line < a + (uintptr_t)bytes; line += 128)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
-  }
-}
-
-// Copy the m planned rows of every layer: host pool -> device pool (phase 9).
+// Phase 9 of the resolve CTA: copy every planned miss row of every layer straight from
+// host memory to its victim's device row (psrc < 0: zero-fill; pdst < 0: nothing to do,
+// e.g. a row a copy CTA moves).
 __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc, const int32_t* pdst, int m) {
-  // p lives in shared memory: the per-layer bases are indexed without a local copy.
   if (g.vec == 16) {
     const int per_row = g.B >> 4;
     const int per_miss = per_row * g.L;
@@ -242,6 +320,65 @@ __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc
   }
 }
 
+// A copy CTA of request r (cluster rank >= 1). Phase A delivers up to copy_cap miss tokens;
+// their host rows are looked up and read at once into shared memory (plain 16-byte loads,
+// kCopyUnroll in flight per thread: many more bytes in flight per SM than cp.async gets
+// from host memory), so the link transfer overlaps the resolve CTA's victim selection.
+// Phase B delivers each miss's device row (-1: nothing to write); the staged rows are then
+// stored there (zeros when the host row is out of range, which this CTA flags).
+__device__ void copy_cta(const Geometry& g, const Pools& p, const int32_t* __restrict__ hcl_row,
+                         unsigned char* smem, uint32_t* err_word) {
+  const CopyLayout cl = make_copy_layout(g);
+  const int32_t* c_count = reinterpret_cast<const int32_t*>(smem + cl.count);
+  const int32_t* c_tok = reinterpret_cast<const int32_t*>(smem + cl.tok);
+  int32_t* c_hrow = reinterpret_cast<int32_t*>(smem + cl.hrow);
+  const int32_t* c_drow = reinterpret_cast<const int32_t*>(smem + cl.drow);
+  uint8_t* c_stage = smem + cl.stage;
+  uint32_t flags = 0;
+
+  cluster_arrive();  // phase A: the resolve CTA has written the tokens and the count
+  cluster_wait();
+  const int n = c_count[0];
+  for (int e = threadIdx.x; e < n; e += T) {
+    const int32_t hr = hcl_row[c_tok[e]];
+    c_hrow[e] = (hr >= 0 && (int64_t)hr < g.host_rows) ? hr : -1;
+  }
+  __syncthreads();
+  const int per_row = g.B >> 4;
+  const int per_miss = per_row * g.L;
+  const int total = n * per_miss;
+  for (int base = threadIdx.x; base < total; base += T * kCopyUnroll) {
+    uint4 v[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int c = base + u * T;
+      if (c < total) {
+        const int e = c / per_miss, rem = c - e * per_miss, l = rem / per_row, q = rem - l * per_row;
+        const int32_t hr = c_hrow[e];
+        v[u] = hr >= 0 ? load_host16(reinterpret_cast<const uint4*>(p.host[l] + (size_t)hr * g.B) + q)
+                       : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int c = base + u * T;
+      if (c < total) reinterpret_cast<uint4*>(c_stage)[c] = v[u];  // row e, layer l: (e*L + l)*B
+    }
+  }
+  cluster_arrive();  // phase B: the resolve CTA has written the device rows
+  cluster_wait();
+  __syncthreads();
+  for (int e = threadIdx.x; e < n; e += T)
+    if (c_drow[e] >= 0 && c_hrow[e] < 0) flags |= HS_FLAG_HOSTROW;  // destination is zero-filled
+  for (int c = threadIdx.x; c < total; c += T) {
+    const int e = c / per_miss, rem = c - e * per_miss, l = rem / per_row, q = rem - l * per_row;
+    const int32_t d = c_drow[e];
+    if (d >= 0) reinterpret_cast<uint4*>(p.dev[l] + (size_t)d * g.B)[q] = reinterpret_cast<const uint4*>(c_stage)[c];
+  }
+  const uint32_t f = __reduce_or_sync(FULL, flags);
+  if ((threadIdx.x & 31) == 0 && f) atomicOr(err_word, f);
+}
+
 __device__ __forceinline__ void flush_flags(uint32_t flags, uint32_t* err_word) {
   const uint32_t f = __reduce_or_sync(FULL, flags);
   if ((threadIdx.x & 31) == 0 && f) atomicOr(err_word, f);
@@ -250,8 +387,29 @@ __device__ __forceinline__ void flush_flags(uint32_t flags, uint32_t* err_word) 
 __global__ void __launch_bounds__(T, 1)
     resolve_kernel(const Geometry g, const Pools* __restrict__ pools, const ResolveArgs a,
                    uint32_t* __restrict__ err_word) {
+  // The eager backup touches only the newest token's rows, which this kernel never reads
+  // or writes: let it launch now and run beside the resolve (it orders its own exit).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ Pools s_pools;
+  const int tid = threadIdx.x;
+  const int C = g.copy_ctas;
+  const uint32_t rank = C > 0 ? cluster_rank() : 0u;
+  const int r = blockIdx.x / (C + 1);  // one cluster of C + 1 CTAs per request
+  if (tid < (int)(sizeof(Pools) / sizeof(uint64_t)))
+    reinterpret_cast<uint64_t*>(&s_pools)[tid] = reinterpret_cast<const uint64_t*>(pools)[tid];
+  if (C > 0) {
+    // Every CTA of the cluster runs (and a copy CTA has cleared its count) before any
+    // CTA touches another's shared memory.
+    if (rank > 0 && tid == 0) reinterpret_cast<int32_t*>(smem + make_copy_layout(g).count)[0] = 0;
+    cluster_arrive();
+    cluster_wait();
+    if (rank > 0) {
+      copy_cta(g, s_pools, a.host_cache_locs + (size_t)r * g.max_context, smem, err_word);
+      return;
+    }
+  }
   const Layout lay = make_layout(g);
   uint64_t* s_keys = reinterpret_cast<uint64_t*>(smem + lay.keys);
   int32_t* s_tk = reinterpret_cast<int32_t*>(smem + lay.tk);
@@ -261,29 +419,27 @@ __global__ void __launch_bounds__(T, 1)
   int32_t* s_vict = reinterpret_cast<int32_t*>(smem + lay.vict);
   int32_t* s_psrc = reinterpret_cast<int32_t*>(smem + lay.psrc);
   int32_t* s_pdst = reinterpret_cast<int32_t*>(smem + lay.pdst);
-  int32_t* s_hkey = reinterpret_cast<int32_t*>(smem + lay.hkey);
-  int32_t* s_hval = reinterpret_cast<int32_t*>(smem + lay.hval);
+  unsigned long long* s_hash = reinterpret_cast<unsigned long long*>(smem + lay.hash);
   int32_t* s_tok = reinterpret_cast<int32_t*>(smem + lay.tok);
   int32_t* s_stamp = reinterpret_cast<int32_t*>(smem + lay.stamp);
-  int16_t* s_sent = reinterpret_cast<int16_t*>(smem + lay.sent);
+  // the table starts at the same 16-byte phase as its global row
+  int32_t* s_dbl = reinterpret_cast<int32_t*>(smem + lay.dbl) +
+                   ((((uintptr_t)(a.device_buffer_locs + (size_t)r * (g.H + 1))) & 15) >> 2);
+  int16_t* s_stage_of = reinterpret_cast<int16_t*>(smem + lay.stage_of);
   uint8_t* s_cls = smem + lay.cls;
   uint8_t* s_sflag = smem + lay.sflag;
   int32_t* s_wsum = reinterpret_cast<int32_t*>(smem + lay.wsum);
   int32_t* s_hist = reinterpret_cast<int32_t*>(smem + lay.hist);
   uint32_t* s_sc = reinterpret_cast<uint32_t*>(smem + lay.sc);
 
-  // The eager backup touches only the newest token's rows, which this kernel never reads
-  // or writes: let it launch now and run beside the resolve (it orders its own exit).
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  const int tid = threadIdx.x;
-  const int r = blockIdx.x;
   const int K = g.K, H = g.H;
   const int HS = 1 << g.hash_bits;
   const int32_t S = a.seq_lens[r];
   const int32_t* tk_g = a.top_k_tokens + (size_t)r * K;
   int32_t* out_g = a.out_rows + (size_t)r * K;
-  const int32_t* dbl = a.device_buffer_locs + (size_t)r * (H + 1);
+  const int32_t* dbl_g = a.device_buffer_locs + (size_t)r * (H + 1);
+  int32_t* tok_g = a.device_buffer_tokens + (size_t)r * H;
+  int32_t* st_g = a.lru_slots + (size_t)r * H;
   uint32_t flags = 0;
 
   if (S < 0 || S > g.max_context) {
@@ -294,123 +450,175 @@ __global__ void __launch_bounds__(T, 1)
     }
     return;
   }
+  const bool fast = S <= H;
 
-  // ---- phase 1: top-k row, validity, hash of the valid tokens
-  for (int h = tid; h < HS; h += T) {
-    s_hkey[h] = -1;
-    s_hval[h] = INF;
+  // ---- phase 0: state into shared memory, asynchronously
+  cp_async_words(s_tk, tk_g, K);
+  cp_async_words(s_dbl, dbl_g, H + 1);
+  if (!fast) {
+    cp_async_words(s_tok, tok_g, H);
+    cp_async_words(s_stamp, st_g, H);
   }
-  if (tid == 0) {
-    s_sc[SC_LO] = 0xffffffffu;
-    s_sc[SC_HI] = 0u;
-  }
-  if (tid < (int)(sizeof(Pools) / sizeof(uint64_t)))
-    reinterpret_cast<uint64_t*>(&s_pools)[tid] = reinterpret_cast<const uint64_t*>(pools)[tid];
+  cp_async_commit();
+  for (int h = tid; h < HS; h += T) s_hash[h] = kEmpty;
+  for (int i = tid; i < K; i += T) s_claim[i] = INF;
+  if (tid < SC_COUNT) s_sc[tid] = tid == SC_LO ? 0xffffffffu : 0u;
+  cp_async_wait_all();
   __syncthreads();
+
+  // ---- phase 1: validity, class and the hash of the valid tokens. A repeated token is
+  // only known once every insert is done, so classes and rows here are provisional for
+  // repeats (settled in phase 4, or right below on the fast path).
   for (int i = tid; i < K; i += T) {
-    const int32_t t = tk_g[i];
+    const int32_t t = s_tk[i];
     uint8_t c;
+    int64_t row = -1;
     if (t < 0) {
       c = C_PAD;
     } else if (t >= S) {
       c = C_BAD;
       flags |= HS_FLAG_TOKEN;
     } else {
-      c = C_VALID;
-      hash_insert(s_hkey, s_hval, g.hash_bits, t, i);
+      hash_insert(s_hash, g.hash_bits, t, i);
+      int32_t page = -1;
+      if (a.resident_pages) page = a.resident_pages[(size_t)r * g.max_pages + t / g.page_size];
+      if (page >= 0) {
+        c = C_RES;
+        row = (int64_t)page * g.page_size + t % g.page_size;
+      } else if (fast) {
+        c = C_FAST;
+        row = s_dbl[t];
+      } else if (t == S - 1) {
+        c = C_NEWEST;
+        row = s_dbl[H];
+      } else {
+        c = C_LOOKUP;
+      }
+      if (c != C_LOOKUP && (row < 0 || row >= g.device_rows)) {
+        c |= C_BADROW;
+        row = -1;
+      }
     }
-    s_tk[i] = t;
     s_cls[i] = c;
-    s_out[i] = -1;
-    s_claim[i] = INF;
-  }
-  __syncthreads();
-
-  // ---- phase 2: classify (resident, fast path, newest, hot lookup)
-  const bool fast = S <= H;
-  for (int i = tid; i < K; i += T) {
-    if (s_cls[i] != C_VALID) continue;
-    const int32_t t = s_tk[i];
-    const int h = hash_find(s_hkey, g.hash_bits, t);
-    if (s_hval[h] != i) {
-      s_cls[i] = C_DUP;
-      flags |= HS_FLAG_DUP;
-      continue;
-    }
-    int32_t page = -1;
-    if (a.resident_pages) page = a.resident_pages[(size_t)r * g.max_pages + t / g.page_size];
-    if (page >= 0) {
-      s_out[i] = checked_row((int64_t)page * g.page_size + t % g.page_size, g.device_rows, flags);
-      s_cls[i] = C_RES;
-    } else if (fast) {
-      s_out[i] = checked_row(dbl[t], g.device_rows, flags);
-      s_cls[i] = C_FAST;
-    } else if (t == S - 1) {
-      s_out[i] = checked_row(dbl[H], g.device_rows, flags);
-      s_cls[i] = C_NEWEST;
-    } else {
-      s_cls[i] = C_LOOKUP;
-    }
+    s_out[i] = (int32_t)row;
   }
   __syncthreads();
 
   if (fast) {
-    for (int i = tid; i < K; i += T) out_g[i] = s_out[i];
+    for (int i = tid; i < K; i += T) {
+      const uint8_t c = s_cls[i];
+      int32_t o = s_out[i];
+      if (c != C_PAD && c != C_BAD) {
+        if (hash_find(s_hash, g.hash_bits, s_tk[i]) != i) {
+          flags |= HS_FLAG_DUP;
+          o = -1;
+        } else if (c & C_BADROW) {
+          flags |= HS_FLAG_DEVROW;
+        }
+      }
+      out_g[i] = o;
+    }
     if (tid == 0) {
-      if (S >= 1) a.device_buffer_tokens[(size_t)r * H + (S - 1)] = S - 1;
+      if (S >= 1) tok_g[S - 1] = S - 1;
       if (a.miss_counts) a.miss_counts[r] = 0;
     }
     flush_flags(flags, err_word);
     return;
   }
 
-  // ---- phase 3: slot state, tripwires, membership probe
+  // ---- phase 3: tripwires, membership probe, hits
   const int32_t clock = a.lru_clock[r] + 1;
-  int32_t* tok_g = a.device_buffer_tokens + (size_t)r * H;
-  int32_t* st_g = a.lru_slots + (size_t)r * H;
   for (int s = tid; s < H; s += T) {
-    int32_t tkn = tok_g[s];
-    int32_t st = st_g[s];
+    int32_t tkn = s_tok[s];
+    const int32_t st = s_stamp[s];
     uint8_t f = 0;
     if (st < 0 || st > clock - 1 || tkn < -1 || tkn >= S - 1) {
       tkn = -1;
-      st = 0;
+      s_tok[s] = -1;
+      s_stamp[s] = 0;
       f = SF_DIRTY;
       flags |= HS_FLAG_STATE;
     }
-    int32_t ent = -1;
-    if (tkn >= 0) {
-      const int h = hash_find(s_hkey, g.hash_bits, tkn);
-      if (h >= 0) {
-        const int32_t i = s_hval[h];
-        if (s_cls[i] == C_LOOKUP) {
-          ent = i;
-          atomicMin(&s_claim[i], s);
+    const int32_t i = lookup_entry(s_hash, s_cls, g.hash_bits, tkn);
+    if (i >= 0) {
+      if (atomicCAS(&s_claim[i], INF, s) == INF) {
+        s_stamp[s] = clock;
+        f |= SF_USED | SF_DIRTY;
+      } else {
+        s_sc[SC_CONFLICT] = 1u;  // a second slot holds the token: settled below
+      }
+    }
+    s_sflag[s] = f;
+  }
+  __syncthreads();
+
+  if (s_sc[SC_CONFLICT]) {
+    // Corrupt state only: several slots hold one looked-up token. The lowest slot is the
+    // hit; an earlier claim by another slot is undone (its stamp is still in global memory,
+    // untouched, since a corrupt stamp would have freed the slot).
+    for (int i = tid; i < K; i += T) s_vict[i] = INF;
+    __syncthreads();
+    for (int s = tid; s < H; s += T) {
+      const int32_t i = lookup_entry(s_hash, s_cls, g.hash_bits, s_tok[s]);
+      if (i >= 0) atomicMin(&s_vict[i], s);
+    }
+    __syncthreads();
+    for (int s = tid; s < H; s += T) {
+      const int32_t i = lookup_entry(s_hash, s_cls, g.hash_bits, s_tok[s]);
+      if (i < 0) continue;
+      const int32_t w = s_vict[i];
+      if (s != w) flags |= HS_FLAG_STATE;
+      if (s_claim[i] == w) continue;
+      if (s == s_claim[i]) {
+        s_stamp[s] = st_g[s];
+        s_sflag[s] &= (uint8_t)~SF_USED;
+      } else if (s == w) {
+        s_stamp[s] = clock;
+        s_sflag[s] |= SF_USED | SF_DIRTY;
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < K; i += T)
+      if (s_vict[i] != INF) s_claim[i] = s_vict[i];
+    __syncthreads();
+  }
+
+  // ---- phase 4: repeats settle; misses go to the copy CTAs; hits output their slot's row
+  const int hand_cap = C * g.copy_cap;  // misses the copy CTAs can stage
+  const CopyLayout cl = make_copy_layout(g);
+  for (int i = tid; i < K; i += T) {
+    int16_t so = -1;
+    const uint8_t cls = s_cls[i];
+    if (cls != C_PAD && cls != C_BAD && hash_find(s_hash, g.hash_bits, s_tk[i]) != i) {
+      s_cls[i] = C_DUP;  // a later repeat of a valid token
+      s_out[i] = -1;
+      flags |= HS_FLAG_DUP;
+    } else if (cls & C_BADROW) {
+      flags |= HS_FLAG_DEVROW;
+    } else if (cls == C_LOOKUP) {
+      const int32_t c = s_claim[i];
+      if (c != INF) {
+        s_out[i] = checked_row(s_dbl[c], g.device_rows, flags);
+      } else if (hand_cap > 0) {
+        const uint32_t k = atomicAdd(&s_sc[SC_STAGED], 1u);
+        if ((int)k < hand_cap) {  // miss k goes to copy CTA 1 + k % C, entry k / C
+          st_remote(smem + cl.tok + 4 * (size_t)(k / C), 1 + k % C, s_tk[i]);
+          so = (int16_t)k;
         }
       }
     }
-    s_tok[s] = tkn;
-    s_stamp[s] = st;
-    s_sflag[s] = f;
-    s_sent[s] = (int16_t)ent;
+    s_stage_of[i] = so;
   }
-  __syncthreads();
-
-  // ---- phase 4: hits refresh their stamp
-  for (int s = tid; s < H; s += T) {
-    const int32_t i = s_sent[s];
-    if (i < 0) continue;
-    if (s_claim[i] == s) {
-      s_stamp[s] = clock;
-      s_sflag[s] |= SF_USED | SF_DIRTY;
-      s_out[i] = checked_row(dbl[s], g.device_rows, flags);
-    } else {
-      flags |= HS_FLAG_STATE;  // a second slot holds the same token
+  if (C > 0) {
+    __syncthreads();
+    if (tid < C) {
+      const int n = min((int)s_sc[SC_STAGED], hand_cap);
+      st_remote(smem + cl.count, 1 + tid, n / C + (tid < n % C ? 1 : 0));
     }
+    cluster_arrive();  // phase A: the copy CTAs may start pulling rows
   }
-  __syncthreads();
 
-  // ---- phase 5: compact misses (top-k order) and free slots (slot order) in one scan
+  // ---- phase 5: order the misses (top-k order) and the free slots (slot order), one scan
   const int ept = (K + T - 1) / T;
   const int spt = (H + T - 1) / T;
   const int i0 = min(K, tid * ept), i1 = min(K, i0 + ept);
@@ -425,14 +633,7 @@ __global__ void __launch_bounds__(T, 1)
   {
     int pos = packed >> 16;
     for (int i = i0; i < i1; ++i)
-      if (s_cls[i] == C_LOOKUP && s_claim[i] == INF) {
-        const int32_t hr = a.host_cache_locs[(size_t)r * g.max_context + s_tk[i]];
-        const bool ok = hr >= 0 && (int64_t)hr < g.host_rows;
-        s_psrc[pos] = ok ? hr : -1;
-        if (ok)
-          for (int l = 0; l < g.L; ++l) prefetch_row_l2(s_pools.host[l] + (size_t)hr * g.B, g.B, g.vec);
-        s_miss[pos++] = i;
-      }
+      if (s_cls[i] == C_LOOKUP && s_claim[i] == INF) s_miss[pos++] = i;
     pos = packed & 0xffff;
     for (int s = s0; s < s1; ++s)
       if (s_tok[s] == -1) {
@@ -527,33 +728,60 @@ __global__ void __launch_bounds__(T, 1)
         ++p_eq;
       }
     }
-    int n = 1;
-    while (n < m2) n <<= 1;
-    for (int i = m2 + tid; i < n; i += T) s_keys[i] = ~0ull;
     __syncthreads();
-    bitonic_sort(s_keys, n);
-    for (int j = tid; j < m2; j += T) s_vict[take_free + j] = (int32_t)(s_keys[j] & 0xffffffffu);
+    if (m2 <= kRankSortMax) {
+      // the keys are distinct: a victim's rank is the number of smaller keys
+      for (int j = tid; j < m2; j += T) {
+        const uint64_t kj = s_keys[j];
+        int rk = 0;
+        for (int u = 0; u < m2; ++u) rk += s_keys[u] < kj;
+        s_vict[take_free + rk] = (int32_t)(kj & 0xffffffffu);
+      }
+    } else {
+      int n = 1;
+      while (n < m2) n <<= 1;
+      for (int i = m2 + tid; i < n; i += T) s_keys[i] = ~0ull;
+      __syncthreads();
+      bitonic_sort(s_keys, n);
+      for (int j = tid; j < m2; j += T) s_vict[take_free + j] = (int32_t)(s_keys[j] & 0xffffffffu);
+    }
   }
   __syncthreads();
 
   // ---- phase 7: miss j takes victim j
+  if (C > 0) cluster_wait();  // phase A complete (the copy CTAs arrived at their start)
   for (int j = tid; j < m; j += T) {
     const int32_t v = s_vict[j];
     const int32_t i = s_miss[j];
-    const int32_t t = s_tk[i];
-    if ((uint32_t)v >= (uint32_t)H) {  // unreachable by construction; never index with it
-      flags |= HS_FLAG_STATE;
-      s_pdst[j] = -1;
-      continue;
+    const int k = s_stage_of[i];
+    int32_t d = -1;
+    if ((uint32_t)v < (uint32_t)H) {
+      s_tok[v] = s_tk[i];
+      s_stamp[v] = clock;
+      s_sflag[v] |= SF_DIRTY;
+      d = checked_row(s_dbl[v], g.device_rows, flags);
+    } else {
+      flags |= HS_FLAG_STATE;  // unreachable by construction; never index with it
     }
-    s_tok[v] = t;
-    s_stamp[v] = clock;
-    s_sflag[v] |= SF_DIRTY;
-    const int32_t d = checked_row(dbl[v], g.device_rows, flags);
     s_out[i] = d;
-    if (d >= 0 && s_psrc[j] < 0) flags |= HS_FLAG_HOSTROW;  // destination is zero-filled
-    s_pdst[j] = d;
+    if (k >= 0) {  // a copy CTA moves this one
+      st_remote(smem + cl.drow + 4 * (size_t)(k / C), 1 + k % C, d);
+      s_pdst[j] = -1;
+    } else {
+      s_sc[SC_DIRECT] = 1u;
+      int32_t hr = -1;
+      if (d >= 0) {
+        hr = a.host_cache_locs[(size_t)r * g.max_context + s_tk[i]];
+        if (hr < 0 || (int64_t)hr >= g.host_rows) {
+          hr = -1;
+          flags |= HS_FLAG_HOSTROW;  // destination is zero-filled
+        }
+      }
+      s_psrc[j] = hr;
+      s_pdst[j] = d;
+    }
   }
+  if (C > 0) cluster_arrive();  // phase B: the copy CTAs have their device rows
   __syncthreads();
 
   // ---- phase 8: write back changed slots, the row table and the clock
@@ -568,35 +796,92 @@ __global__ void __launch_bounds__(T, 1)
     if (a.miss_counts) a.miss_counts[r] = m;
   }
 
-  // ---- phase 9: miss rows, all layers, from pinned host memory
-  copy_rows(g, s_pools, s_psrc, s_pdst, m);
+  // ---- phase 9: misses no copy CTA took, all layers, straight from host memory
+  if (s_sc[SC_DIRECT]) copy_rows(g, s_pools, s_psrc, s_pdst, m);
   flush_flags(flags, err_word);
+  if (C > 0) cluster_wait();  // phase B complete; the copy CTAs finish on their own
 }
 
 }  // namespace
 
-size_t resolve_smem_bytes(const Geometry& g) { return make_layout(g).total; }
+size_t resolve_smem_bytes(const Geometry& g) {
+  const size_t a = make_layout(g).total;
+  const size_t b = g.copy_ctas > 0 ? make_copy_layout(g).total : 0;
+  return a > b ? a : b;
+}
 
-// Raise the kernel's dynamic shared-memory ceiling to the most the device allows beside
-// the kernel's static shared memory (not to this geometry's size): the attribute is per
-// function and device, so a smaller value set for one handle would make launches of a
-// larger, earlier handle fail.
-cudaError_t resolve_prepare(const Geometry& g) {
-  int dev = 0, optin = 0;
+// Raise the kernel's dynamic shared-memory limit to the device maximum beside its static
+// shared memory (not to this geometry's size: the attribute is per function and device, so
+// a smaller value set for one handle would make launches of a larger, earlier handle
+// fail), then choose the copy CTAs. Each request gets C = SMs / max_requests - 1 of them
+// (at most 3), so a full batch spreads over the GPU, each staging as many misses as its
+// shared memory holds; none when rows are not 16-byte copyable or the cluster does not fit.
+cudaError_t resolve_prepare(Geometry& g, int32_t max_requests) {
+  int dev = 0, optin = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaFuncAttributes fa{};
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, resolve_kernel);
   if (e != cudaSuccess) return e;
   const int max_dynamic = optin - (int)fa.sharedSizeBytes;
-  if (resolve_smem_bytes(g) > (size_t)max_dynamic) return cudaErrorInvalidValue;
-  return cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic);
+  g.copy_ctas = 0;
+  g.copy_cap = 0;
+  if (make_layout(g).total > (size_t)max_dynamic) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic);
+  if (e != cudaSuccess) return e;
+
+  int C = max_requests > 0 ? sms / max_requests - 1 : 0;
+  C = C < 0 ? 0 : (C > 3 ? 3 : C);
+  if (g.vec != 16) C = 0;
+  if (C > 0) {
+    const size_t per_miss = 12 + (size_t)g.L * (size_t)g.B;
+    size_t cap = ((size_t)max_dynamic - 256) / per_miss;
+    if (cap > (size_t)g.K) cap = (size_t)g.K;
+    Geometry t = g;
+    t.copy_ctas = C;
+    t.copy_cap = (int32_t)cap;
+    while (t.copy_cap > 0 && resolve_smem_bytes(t) > (size_t)max_dynamic) --t.copy_cap;
+    if (t.copy_cap > 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(C + 1));
+      cfg.blockDim = dim3(T);
+      cfg.dynamicSmemBytes = resolve_smem_bytes(t);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)(C + 1);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, resolve_kernel, &cfg) == cudaSuccess && clusters > 0) {
+        g.copy_ctas = C;
+        g.copy_cap = t.copy_cap;
+      } else {
+        cudaGetLastError();
+      }
+    }
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_resolve(const Geometry& g, const Pools* pools, const ResolveArgs& a, int32_t num_requests,
                            uint32_t* err_word, cudaStream_t stream) {
-  resolve_kernel<<<num_requests, T, resolve_smem_bytes(g), stream>>>(g, pools, a, err_word);
-  return cudaGetLastError();
+  const unsigned per_request = (unsigned)(g.copy_ctas + 1);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_requests * per_request);
+  cfg.blockDim = dim3(T);
+  cfg.dynamicSmemBytes = resolve_smem_bytes(g);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = per_request;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = g.copy_ctas > 0 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, resolve_kernel, g, pools, a, err_word);
 }
 
 }  // namespace hs
