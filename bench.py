@@ -163,6 +163,20 @@ def newest_rows(wl, step):
     return rows, data
 
 
+def ncu_traffic(config: str) -> dict:
+    """Per-launch traffic of the resolve kernel from the committed ncu capture, when that
+    capture was taken on this workload and on the kernel source as it is now; else {}."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+        src = open(os.path.join(ROOT, rec["kernel_source"]), "rb").read()
+    except (OSError, ValueError, KeyError):
+        return {}
+    if rec.get("workload") != config or hashlib.sha256(src).hexdigest()[:16] != rec.get("sha256_16"):
+        return {}
+    return rec
+
+
 # ------------------------------------------------------------------------------------------
 def cpu_oracle_run(wl, host, steps, nthreads=1):
     """Time the CPU oracle over `steps` decode steps (resolve + backup, bytes included).
@@ -392,6 +406,7 @@ def run_ours(args, ws, rank, local):
     except (OSError, ValueError):
         pass
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    traffic = ncu_traffic(args.config)
 
     # ---- end to end through the C ABI with host buffers: H2D of the step's inputs from
     # pinned memory, the two calls, D2H of the row table and miss counts, per step
@@ -438,11 +453,17 @@ def run_ours(args, ws, rank, local):
         "misses_per_step": float(misses.mean()), "miss_h2d_gbs": link_gbs, "h2d_ceiling_gbs": h2d_ceiling,
         "miss_h2d_frac_of_ceiling": link_gbs / h2d_ceiling,
         "roofline": {"bound": "host_link", "achieved": link_gbs, "peak": h2d_ceiling, "unit": "GB/s",
-                     "frac": link_gbs / h2d_ceiling, "traffic": None,
+                     "frac": link_gbs / h2d_ceiling,
+                     "traffic": traffic.get("sysmem_read_bytes_per_launch"),
+                     "traffic_metric": "ncu syslts sysmem read sectors x 32 B per launch (null: kernel changed)",
+                     "algorithmic_bytes_per_launch": float(miss_bytes.mean()),
                      "kernel": "resolve_kernel",
                      "peak_source": "pinned cudaMemcpy H2D, 1 GiB, best of 12, measured in this run",
                      "hbm": {"achieved": hbm_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": hbm_gbs / hbm_peak,
-                             "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)"}},
+                             "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)",
+                             "traffic": (traffic["dram_read_bytes_per_launch"] + traffic["dram_write_bytes_per_launch"])
+                             if traffic else None,
+                             "algorithmic_bytes_per_launch": float(hbm_bytes.mean())}},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
                 "steps": e2e_steps, "timing": "wall clock per step, host enqueue to stream sync"},
         "gpu_launches": 2 * K_,
