@@ -11,6 +11,7 @@ struct hs_handle {
   hs::Geometry g;
   const hs::Pools* pools;  // pools table inside the caller's workspace
   uint32_t* err_word;      // error word inside the caller's workspace
+  int16_t* hint;           // token -> slot hint table inside the caller's workspace
   int device;
 };
 
@@ -40,7 +41,9 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 extern "C" {
 
-size_t hs_workspace_bytes(const hs_config* cfg) { return config_ok(cfg) ? hs::kWorkspaceBytes : 0; }
+size_t hs_workspace_bytes(const hs_config* cfg) {
+  return config_ok(cfg) ? hs::kWorkspaceBytes + hs::hint_bytes(cfg->max_requests, cfg->max_context) : 0;
+}
 
 hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* device_pools,
                     int64_t host_rows, int64_t device_rows, void* workspace, hs_handle** out) {
@@ -112,6 +115,9 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (cudaMemset(ws, 0, hs::kWorkspaceBytes) != cudaSuccess) return HS_ERR_CUDA;
+  if (cudaMemset(ws + hs::kWorkspaceBytes, 0xFF, hs::hint_bytes(cfg->max_requests, cfg->max_context)) !=
+      cudaSuccess)
+    return HS_ERR_CUDA;  // every hint starts at -1 (no slot)
   if (cudaMemcpy(ws + hs::kPoolsOffset, &pools, sizeof(pools), cudaMemcpyHostToDevice) != cudaSuccess)
     return HS_ERR_CUDA;
 
@@ -121,6 +127,7 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   h->g = g;
   h->pools = reinterpret_cast<const hs::Pools*>(ws + hs::kPoolsOffset);
   h->err_word = reinterpret_cast<uint32_t*>(ws + hs::kErrOffset);
+  h->hint = reinterpret_cast<int16_t*>(ws + hs::kWorkspaceBytes);
   h->device = dev;
   *out = h;
   return HS_OK;
@@ -137,7 +144,7 @@ hs_status hs_resolve(hs_handle* h, int32_t num_requests, const int32_t* top_k_to
       !lru_slots || !lru_clock || !out_rows)
     return HS_ERR_INVALID_ARG;
   if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
-  hs::ResolveArgs a{top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs, device_buffer_tokens,
+  hs::ResolveArgs a{h->hint, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs, device_buffer_tokens,
                     lru_slots, lru_clock, resident_pages, out_rows, miss_counts};
   if (hs::launch_resolve(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
     return HS_ERR_CUDA;

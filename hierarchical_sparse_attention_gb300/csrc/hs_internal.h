@@ -35,6 +35,7 @@ struct Geometry {
 };
 
 struct ResolveArgs {
+  int16_t* hint;  // [R, max_context] token -> slot guess (-1: none) in the workspace, or NULL
   const int32_t* top_k_tokens;
   const int32_t* seq_lens;
   const int32_t* host_cache_locs;
@@ -57,8 +58,17 @@ struct BackupArgs {
 // Workspace layout (device memory owned by the caller).
 constexpr size_t kErrOffset = 0;     // uint32 sticky HS_FLAG_* word
 constexpr size_t kPoolsOffset = 64;  // Pools table
-constexpr size_t kWorkspaceBytes = 256;
+constexpr size_t kWorkspaceBytes = 256;  // header: error word + pools table
 static_assert(kPoolsOffset + sizeof(Pools) <= kWorkspaceBytes, "workspace too small for the pools table");
+constexpr int kMaxEntriesPerThread = (HS_MAX_TOP_K + kResolveThreads - 1) / kResolveThreads;
+
+// After the header, hs_create's workspace holds the token -> slot hint table: one int16 per
+// (request, token position), the slot that last took the token (-1: none). The kernels keep
+// it current and use it only to start miss transfers early; every result still comes from
+// the exact slot probe, so a stale entry costs time, never correctness.
+inline size_t hint_bytes(int64_t max_requests, int64_t max_context) {
+  return (size_t)(((max_requests * max_context * 2) + 255) & ~(int64_t)255);
+}
 
 // Dynamic shared memory of one resolve-kernel CTA for geometry g.
 size_t resolve_smem_bytes(const Geometry& g);

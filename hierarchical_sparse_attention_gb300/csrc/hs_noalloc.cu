@@ -134,7 +134,8 @@ hs_status hs_resolve_noalloc(const hs_config* cfg, void* const* host_pools, void
     cudaGetLastError();
     return HS_ERR_CUDA;
   }
-  hs::ResolveArgs a{top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs, device_buffer_tokens,
+  // no hint table here: misses start their transfer after the exact probe
+  hs::ResolveArgs a{nullptr, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs, device_buffer_tokens,
                     lru_slots, lru_clock, resident_pages, out_rows, miss_counts};
   uint32_t* err_word = reinterpret_cast<uint32_t*>(scratch + hs::kErrOffset);
   if (hs::launch_resolve(g, reinterpret_cast<const hs::Pools*>(scratch + hs::kPoolsOffset), a, num_requests,

@@ -61,7 +61,7 @@ constexpr int kRankSortMax = 1024;  // victims ordered by counting ranks up to t
 enum : uint8_t { C_PAD = 0, C_BAD, C_DUP, C_RES, C_FAST, C_NEWEST, C_LOOKUP };
 constexpr uint8_t C_BADROW = 0x80;  // with C_RES / C_FAST / C_NEWEST: its row is out of range
 enum : uint8_t { SF_USED = 1, SF_DIRTY = 2 };
-enum { SC_LO = 0, SC_HI, SC_DIGIT, SC_RANK, SC_CONFLICT, SC_STAGED, SC_DIRECT, SC_COUNT };
+enum { SC_LO = 0, SC_HI, SC_DIGIT, SC_RANK, SC_CONFLICT, SC_DIRECT, SC_COUNT };
 
 // Shared-memory carve-up of the resolve CTA; identical arithmetic on host (size) and device
 // (pointers). The top-k hash (1 << hash_bits buckets of one 64-bit word: token << 32 |
@@ -69,14 +69,17 @@ enum { SC_LO = 0, SC_HI, SC_DIGIT, SC_RANK, SC_CONFLICT, SC_STAGED, SC_DIRECT, S
 // victim keys of phase 6 and the copy plan of phases 7-9. The slot->row table gets three
 // spare words so it can start at its global row's 16-byte phase (whole-vector loads).
 struct Layout {
-  size_t hash, keys, psrc, pdst, tk, out, claim, miss, vict, tok, stamp, dbl, stage_of, cls, sflag, wsum, hist,
-      sc, total;
+  size_t hash, keys, psrc, pdst, tk, out, claim, miss, vict, tok, stamp, dbl, cls, sflag, wsum, hist, sc, total;
 };
 
-// Shared-memory carve-up of a copy CTA: the miss tokens it was handed, their host rows,
-// their device rows, and the staging area (copy_cap misses x L rows of B bytes).
+// Shared-memory carve-up of a copy CTA q (rank 1..C). It owns top-k entries
+// [(q-1) * per, q * per) with per = ceil(K / C): their outcomes, published by the resolve CTA
+// (res: device row of a miss, -2 - slot for a hit, -1 otherwise), its slice of the top-k row,
+// the slot map (to check hints), per entry the staging index and host row, the lists of
+// staged and of directly copied entries, two counters, and the staging area (copy_cap
+// entries x L rows of B bytes).
 struct CopyLayout {
-  size_t count, tok, hrow, drow, stage, total;
+  size_t res, tk, tok, stg, hrow, list, dlist, cnt, stage, total;
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -97,7 +100,6 @@ __host__ __device__ inline Layout make_layout(const Geometry& g) {
   l.tok = o; o = align16(o + 4 * H);
   l.stamp = o; o = align16(o + 4 * H);
   l.dbl = o; o = align16(o + 4 * (H + 1 + 3));
-  l.stage_of = o; o = align16(o + 2 * K);
   l.cls = o; o = align16(o + K);
   l.sflag = o; o = align16(o + H);
   l.wsum = o; o = align16(o + 4 * (NW + 1));
@@ -107,14 +109,22 @@ __host__ __device__ inline Layout make_layout(const Geometry& g) {
   return l;
 }
 
+__host__ __device__ inline int copy_slice(const Geometry& g) {
+  return g.copy_ctas > 0 ? (g.K + g.copy_ctas - 1) / g.copy_ctas : 0;
+}
+
 __host__ __device__ inline CopyLayout make_copy_layout(const Geometry& g) {
   CopyLayout l;
   size_t o = 0;
-  const size_t cap = (size_t)g.copy_cap;
-  l.count = o; o = align16(o + 16);
-  l.tok = o; o = align16(o + 4 * cap);
-  l.hrow = o; o = align16(o + 4 * cap);
-  l.drow = o; o = align16(o + 4 * cap);
+  const size_t per = (size_t)copy_slice(g), cap = (size_t)g.copy_cap;
+  l.res = o; o = align16(o + 4 * per);
+  l.tk = o; o = align16(o + 4 * per);
+  l.tok = o; o = align16(o + 4 * (size_t)g.H);
+  l.stg = o; o = align16(o + 2 * per);
+  l.hrow = o; o = align16(o + 4 * per);
+  l.list = o; o = align16(o + 2 * cap);
+  l.dlist = o; o = align16(o + 2 * per);
+  l.cnt = o; o = align16(o + 16);
   l.stage = o; o = align16(o + cap * (size_t)g.L * (size_t)g.B);
   l.total = o;
   return l;
@@ -320,60 +330,144 @@ __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc
   }
 }
 
-// A copy CTA of request r (cluster rank >= 1). Phase A delivers up to copy_cap miss tokens;
-// their host rows are looked up and read at once into shared memory (plain 16-byte loads,
-// kCopyUnroll in flight per thread: many more bytes in flight per SM than cp.async gets
-// from host memory), so the link transfer overlaps the resolve CTA's victim selection.
-// Phase B delivers each miss's device row (-1: nothing to write); the staged rows are then
-// stored there (zeros when the host row is out of range, which this CTA flags).
-__device__ void copy_cta(const Geometry& g, const Pools& p, const int32_t* __restrict__ hcl_row,
-                         unsigned char* smem, uint32_t* err_word) {
+// Copy CTA q of request r (cluster rank q >= 1; its shared outcome table was cleared to -1
+// and its counters to 0 before the cluster's first barrier).
+// With a hint table and a request past the fast path, it first predicts which of its
+// entries miss: a hot lookup whose hinted slot does not hold it. It looks up the predicted
+// misses' host rows and reads those rows into shared memory right away (16-byte loads,
+// kCopyUnroll in flight per thread), so the host-link transfer runs while the resolve CTA
+// does the exact work. The cluster barrier then publishes the exact outcome of every entry.
+// Exact misses store their staged row; misses that were not staged (no hint, a wrong
+// guess, no room) are copied straight from host memory. A prediction that was a hit
+// repairs the entry's hint.
+__device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a, int r, int q, unsigned char* smem,
+                         uint32_t* err_word) {
   const CopyLayout cl = make_copy_layout(g);
-  const int32_t* c_count = reinterpret_cast<const int32_t*>(smem + cl.count);
-  const int32_t* c_tok = reinterpret_cast<const int32_t*>(smem + cl.tok);
+  const int32_t* c_res = reinterpret_cast<const int32_t*>(smem + cl.res);
+  int32_t* c_tk = reinterpret_cast<int32_t*>(smem + cl.tk);
+  int32_t* c_tok = reinterpret_cast<int32_t*>(smem + cl.tok);
+  int16_t* c_stg = reinterpret_cast<int16_t*>(smem + cl.stg);
   int32_t* c_hrow = reinterpret_cast<int32_t*>(smem + cl.hrow);
-  const int32_t* c_drow = reinterpret_cast<const int32_t*>(smem + cl.drow);
+  int16_t* c_list = reinterpret_cast<int16_t*>(smem + cl.list);
+  int16_t* c_dlist = reinterpret_cast<int16_t*>(smem + cl.dlist);
+  uint32_t* c_cnt = reinterpret_cast<uint32_t*>(smem + cl.cnt);
   uint8_t* c_stage = smem + cl.stage;
-  uint32_t flags = 0;
-
-  cluster_arrive();  // phase A: the resolve CTA has written the tokens and the count
-  cluster_wait();
-  const int n = c_count[0];
-  for (int e = threadIdx.x; e < n; e += T) {
-    const int32_t hr = hcl_row[c_tok[e]];
-    c_hrow[e] = (hr >= 0 && (int64_t)hr < g.host_rows) ? hr : -1;
-  }
-  __syncthreads();
+  const int tid = threadIdx.x;
+  const int per = copy_slice(g);
+  const int e0 = (q - 1) * per;
+  const int ne = max(0, min(g.K, e0 + per) - e0);
+  const int32_t S = a.seq_lens[r];
+  const bool predict = a.hint != nullptr && S > g.H && S <= g.max_context;
+  int16_t* hint_row = a.hint ? a.hint + (size_t)r * g.max_context : nullptr;
+  const int32_t* hcl_row = a.host_cache_locs + (size_t)r * g.max_context;
+  const int32_t* tk_g = a.top_k_tokens + (size_t)r * g.K + e0;
   const int per_row = g.B >> 4;
   const int per_miss = per_row * g.L;
-  const int total = n * per_miss;
-  for (int base = threadIdx.x; base < total; base += T * kCopyUnroll) {
+  uint32_t flags = 0;
+  int staged = 0;
+
+  if (predict) {
+    cp_async_words(c_tk, tk_g, ne);
+    cp_async_words(c_tok, a.device_buffer_tokens + (size_t)r * g.H, g.H);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    for (int e = tid; e < ne; e += T) {
+      const int32_t t = c_tk[e];
+      int16_t st = -1;  // -1: not predicted to miss; -2: predicted, no staging room
+      if (t >= 0 && t < S - 1 &&
+          !(a.resident_pages && a.resident_pages[(size_t)r * g.max_pages + t / g.page_size] >= 0)) {
+        const int gs = hint_row[t];
+        if (!(gs >= 0 && gs < g.H && c_tok[gs] == t)) {
+          const uint32_t k = atomicAdd(&c_cnt[0], 1u);
+          if ((int)k < g.copy_cap) {
+            st = (int16_t)k;
+            c_list[k] = (int16_t)e;
+            const int32_t hr = hcl_row[t];
+            c_hrow[e] = (hr >= 0 && (int64_t)hr < g.host_rows) ? hr : -1;
+          } else {
+            st = -2;
+          }
+        }
+      }
+      c_stg[e] = st;
+    }
+    __syncthreads();
+    staged = min((int)c_cnt[0], g.copy_cap);
+    const int total = staged * per_miss;
+    for (int base = tid; base < total; base += T * kCopyUnroll) {
+      uint4 v[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int c = base + u * T;
+        if (c < total) {
+          const int k = c / per_miss, rem = c - k * per_miss, l = rem / per_row, qq = rem - l * per_row;
+          const int32_t hr = c_hrow[c_list[k]];
+          v[u] = hr >= 0 ? load_host16(reinterpret_cast<const uint4*>(p.host[l] + (size_t)hr * g.B) + qq)
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int c = base + u * T;
+        if (c < total) reinterpret_cast<uint4*>(c_stage)[c] = v[u];  // entry k, layer l at (k*L + l)*B
+      }
+    }
+  }
+  cluster_arrive();  // phase B: the resolve CTA has published every entry's outcome
+  cluster_wait();
+  __syncthreads();
+
+  // staged entries that are exact misses
+  for (int c = tid; c < staged * per_miss; c += T) {
+    const int k = c / per_miss, rem = c - k * per_miss, l = rem / per_row, qq = rem - l * per_row;
+    const int e = c_list[k];
+    const int32_t d = c_res[e];
+    if (d >= 0)
+      reinterpret_cast<uint4*>(p.dev[l] + (size_t)d * g.B)[qq] =
+          c_hrow[e] >= 0 ? reinterpret_cast<const uint4*>(c_stage)[c] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  // the rest: hint repairs, and the list of exact misses to copy straight from host
+  for (int e = tid; e < ne; e += T) {
+    const int32_t d = c_res[e];
+    const int st = predict ? c_stg[e] : -1;
+    if (d >= 0) {
+      if (st >= 0) {
+        if (c_hrow[e] < 0) flags |= HS_FLAG_HOSTROW;  // destination was zero-filled
+      } else {
+        const int32_t t = predict ? c_tk[e] : tk_g[e];
+        const int32_t hr = hcl_row[t];
+        const bool ok = hr >= 0 && (int64_t)hr < g.host_rows;
+        if (!ok) flags |= HS_FLAG_HOSTROW;
+        c_hrow[e] = ok ? hr : -1;
+        c_dlist[atomicAdd(&c_cnt[1], 1u)] = (int16_t)e;
+      }
+    } else if (d <= -2 && st != -1) {
+      hint_row[c_tk[e]] = (int16_t)(-2 - d);  // predicted a miss, was a hit in slot -2 - d
+    }
+  }
+  __syncthreads();
+  const int nd = (int)c_cnt[1];
+  const int dtotal = nd * per_miss;
+  for (int base = tid; base < dtotal; base += T * kCopyUnroll) {
     uint4 v[kCopyUnroll];
+    uint4* dst[kCopyUnroll];
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {
       const int c = base + u * T;
-      if (c < total) {
-        const int e = c / per_miss, rem = c - e * per_miss, l = rem / per_row, q = rem - l * per_row;
+      dst[u] = nullptr;
+      if (c < dtotal) {
+        const int j = c / per_miss, rem = c - j * per_miss, l = rem / per_row, qq = rem - l * per_row;
+        const int e = c_dlist[j];
         const int32_t hr = c_hrow[e];
-        v[u] = hr >= 0 ? load_host16(reinterpret_cast<const uint4*>(p.host[l] + (size_t)hr * g.B) + q)
+        dst[u] = reinterpret_cast<uint4*>(p.dev[l] + (size_t)c_res[e] * g.B) + qq;
+        v[u] = hr >= 0 ? load_host16(reinterpret_cast<const uint4*>(p.host[l] + (size_t)hr * g.B) + qq)
                        : make_uint4(0u, 0u, 0u, 0u);
       }
     }
 #pragma unroll
-    for (int u = 0; u < kCopyUnroll; ++u) {
-      const int c = base + u * T;
-      if (c < total) reinterpret_cast<uint4*>(c_stage)[c] = v[u];  // row e, layer l: (e*L + l)*B
-    }
-  }
-  cluster_arrive();  // phase B: the resolve CTA has written the device rows
-  cluster_wait();
-  __syncthreads();
-  for (int e = threadIdx.x; e < n; e += T)
-    if (c_drow[e] >= 0 && c_hrow[e] < 0) flags |= HS_FLAG_HOSTROW;  // destination is zero-filled
-  for (int c = threadIdx.x; c < total; c += T) {
-    const int e = c / per_miss, rem = c - e * per_miss, l = rem / per_row, q = rem - l * per_row;
-    const int32_t d = c_drow[e];
-    if (d >= 0) reinterpret_cast<uint4*>(p.dev[l] + (size_t)d * g.B)[q] = reinterpret_cast<const uint4*>(c_stage)[c];
+    for (int u = 0; u < kCopyUnroll; ++u)
+      if (dst[u]) *dst[u] = v[u];
   }
   const uint32_t f = __reduce_or_sync(FULL, flags);
   if ((threadIdx.x & 31) == 0 && f) atomicOr(err_word, f);
@@ -400,13 +494,18 @@ __global__ void __launch_bounds__(T, 1)
   if (tid < (int)(sizeof(Pools) / sizeof(uint64_t)))
     reinterpret_cast<uint64_t*>(&s_pools)[tid] = reinterpret_cast<const uint64_t*>(pools)[tid];
   if (C > 0) {
-    // Every CTA of the cluster runs (and a copy CTA has cleared its count) before any
-    // CTA touches another's shared memory.
-    if (rank > 0 && tid == 0) reinterpret_cast<int32_t*>(smem + make_copy_layout(g).count)[0] = 0;
+    // Every CTA of the cluster runs (and each copy CTA has cleared its outcome table and
+    // counters) before any CTA touches another's shared memory.
+    if (rank > 0) {
+      const CopyLayout cl0 = make_copy_layout(g);
+      int32_t* res = reinterpret_cast<int32_t*>(smem + cl0.res);
+      for (int e = tid; e < copy_slice(g); e += T) res[e] = -1;
+      if (tid < 4) reinterpret_cast<uint32_t*>(smem + cl0.cnt)[tid] = 0u;
+    }
     cluster_arrive();
     cluster_wait();
     if (rank > 0) {
-      copy_cta(g, s_pools, a.host_cache_locs + (size_t)r * g.max_context, smem, err_word);
+      copy_cta(g, s_pools, a, r, (int)rank, smem, err_word);
       return;
     }
   }
@@ -425,7 +524,6 @@ __global__ void __launch_bounds__(T, 1)
   // the table starts at the same 16-byte phase as its global row
   int32_t* s_dbl = reinterpret_cast<int32_t*>(smem + lay.dbl) +
                    ((((uintptr_t)(a.device_buffer_locs + (size_t)r * (g.H + 1))) & 15) >> 2);
-  int16_t* s_stage_of = reinterpret_cast<int16_t*>(smem + lay.stage_of);
   uint8_t* s_cls = smem + lay.cls;
   uint8_t* s_sflag = smem + lay.sflag;
   int32_t* s_wsum = reinterpret_cast<int32_t*>(smem + lay.wsum);
@@ -469,6 +567,7 @@ __global__ void __launch_bounds__(T, 1)
   // ---- phase 1: validity, class and the hash of the valid tokens. A repeated token is
   // only known once every insert is done, so classes and rows here are provisional for
   // repeats (settled in phase 4, or right below on the fast path).
+  int16_t* hint_row = a.hint ? a.hint + (size_t)r * g.max_context : nullptr;
   for (int i = tid; i < K; i += T) {
     const int32_t t = s_tk[i];
     uint8_t c;
@@ -522,6 +621,8 @@ __global__ void __launch_bounds__(T, 1)
       if (S >= 1) tok_g[S - 1] = S - 1;
       if (a.miss_counts) a.miss_counts[r] = 0;
     }
+    if (hint_row)  // slot t holds token t: the hints are exact when the sequence outgrows the buffer
+      for (int t = tid; t < S; t += T) hint_row[t] = (int16_t)t;
     flush_flags(flags, err_word);
     return;
   }
@@ -583,11 +684,11 @@ __global__ void __launch_bounds__(T, 1)
     __syncthreads();
   }
 
-  // ---- phase 4: repeats settle; misses go to the copy CTAs; hits output their slot's row
-  const int hand_cap = C * g.copy_cap;  // misses the copy CTAs can stage
+  // ---- phase 4: repeats settle; hits output their slot's row (and tell the entry's copy
+  // CTA which slot, so a wrong miss prediction can repair its hint)
+  const int per = copy_slice(g);
   const CopyLayout cl = make_copy_layout(g);
   for (int i = tid; i < K; i += T) {
-    int16_t so = -1;
     const uint8_t cls = s_cls[i];
     if (cls != C_PAD && cls != C_BAD && hash_find(s_hash, g.hash_bits, s_tk[i]) != i) {
       s_cls[i] = C_DUP;  // a later repeat of a valid token
@@ -599,23 +700,9 @@ __global__ void __launch_bounds__(T, 1)
       const int32_t c = s_claim[i];
       if (c != INF) {
         s_out[i] = checked_row(s_dbl[c], g.device_rows, flags);
-      } else if (hand_cap > 0) {
-        const uint32_t k = atomicAdd(&s_sc[SC_STAGED], 1u);
-        if ((int)k < hand_cap) {  // miss k goes to copy CTA 1 + k % C, entry k / C
-          st_remote(smem + cl.tok + 4 * (size_t)(k / C), 1 + k % C, s_tk[i]);
-          so = (int16_t)k;
-        }
+        if (C > 0) st_remote(smem + cl.res + 4 * (size_t)(i % per), 1 + i / per, -2 - c);
       }
     }
-    s_stage_of[i] = so;
-  }
-  if (C > 0) {
-    __syncthreads();
-    if (tid < C) {
-      const int n = min((int)s_sc[SC_STAGED], hand_cap);
-      st_remote(smem + cl.count, 1 + tid, n / C + (tid < n % C ? 1 : 0));
-    }
-    cluster_arrive();  // phase A: the copy CTAs may start pulling rows
   }
 
   // ---- phase 5: order the misses (top-k order) and the free slots (slot order), one scan
@@ -748,14 +835,17 @@ __global__ void __launch_bounds__(T, 1)
   }
   __syncthreads();
 
-  // ---- phase 7: miss j takes victim j
-  if (C > 0) cluster_wait();  // phase A complete (the copy CTAs arrived at their start)
+  // ---- phase 7: miss j takes victim j; the entry's copy CTA gets its device row
   for (int j = tid; j < m; j += T) {
     const int32_t v = s_vict[j];
     const int32_t i = s_miss[j];
-    const int k = s_stage_of[i];
     int32_t d = -1;
     if ((uint32_t)v < (uint32_t)H) {
+      if (hint_row) {
+        const int32_t old_tok = s_tok[v];
+        if (old_tok >= 0) hint_row[old_tok] = -1;  // evicted
+        hint_row[s_tk[i]] = (int16_t)v;
+      }
       s_tok[v] = s_tk[i];
       s_stamp[v] = clock;
       s_sflag[v] |= SF_DIRTY;
@@ -764,8 +854,8 @@ __global__ void __launch_bounds__(T, 1)
       flags |= HS_FLAG_STATE;  // unreachable by construction; never index with it
     }
     s_out[i] = d;
-    if (k >= 0) {  // a copy CTA moves this one
-      st_remote(smem + cl.drow + 4 * (size_t)(k / C), 1 + k % C, d);
+    if (C > 0) {  // the copy CTA owning entry i moves this row
+      st_remote(smem + cl.res + 4 * (size_t)(i % per), 1 + i / per, d);
       s_pdst[j] = -1;
     } else {
       s_sc[SC_DIRECT] = 1u;
@@ -781,7 +871,7 @@ __global__ void __launch_bounds__(T, 1)
       s_pdst[j] = d;
     }
   }
-  if (C > 0) cluster_arrive();  // phase B: the copy CTAs have their device rows
+  if (C > 0) cluster_arrive();  // phase B: every outcome is published to the copy CTAs
   __syncthreads();
 
   // ---- phase 8: write back changed slots, the row table and the clock
@@ -835,13 +925,16 @@ cudaError_t resolve_prepare(Geometry& g, int32_t max_requests) {
   C = C < 0 ? 0 : (C > 3 ? 3 : C);
   if (g.vec != 16) C = 0;
   if (C > 0) {
-    const size_t per_miss = 12 + (size_t)g.L * (size_t)g.B;
-    size_t cap = ((size_t)max_dynamic - 256) / per_miss;
-    if (cap > (size_t)g.K) cap = (size_t)g.K;
     Geometry t = g;
     t.copy_ctas = C;
-    t.copy_cap = (int32_t)cap;
-    while (t.copy_cap > 0 && resolve_smem_bytes(t) > (size_t)max_dynamic) --t.copy_cap;
+    t.copy_cap = 0;
+    const size_t fixed = make_copy_layout(t).total + 64;  // + alignment slack
+    if (fixed < (size_t)max_dynamic) {
+      size_t cap = ((size_t)max_dynamic - fixed) / (2 + (size_t)g.L * (size_t)g.B);
+      if (cap > (size_t)copy_slice(t)) cap = (size_t)copy_slice(t);
+      t.copy_cap = (int32_t)cap;
+      while (t.copy_cap > 0 && resolve_smem_bytes(t) > (size_t)max_dynamic) --t.copy_cap;
+    }
     if (t.copy_cap > 0) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)(C + 1));

@@ -146,8 +146,14 @@ typedef struct {
 
 typedef struct hs_handle hs_handle;
 
-/* Bytes of device workspace hs_create needs (error word and reserved space); 0 if the
- * configuration is invalid. */
+/* Bytes of device workspace hs_create needs; 0 if the configuration is invalid. The
+ * workspace holds the sticky error word, the per-layer pool table, and a token -> slot hint
+ * table of max_requests x max_context int16 entries (so about 2 bytes per token of context
+ * per request). The kernels keep the hints current and use them only to start a miss's
+ * host transfer before the exact slot probe finishes; every result comes from the probe,
+ * so hints left stale by changes the caller makes to the state arrays cost time, never
+ * correctness. The caller keeps the workspace for the handle's lifetime and does not
+ * write to it. */
 HS_API size_t hs_workspace_bytes(const hs_config* cfg);
 
 /* Validate the configuration and bind the pools. host_pools / device_pools are arrays of

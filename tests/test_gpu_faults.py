@@ -234,3 +234,23 @@ def test_two_handles_with_different_shared_memory_sizes():
     finally:
         gb.close()
         gs.close()
+
+
+def test_stale_or_garbage_hints_do_not_change_results(pair):
+    """The token -> slot hints in the workspace only start transfers early: overwriting them
+    with garbage, or resetting a request's state behind their back, leaves every result exact."""
+    wl, orc, gpu = pair
+    warm(wl, orc, gpu)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    junk = torch.randint(-32768, 32767, (gpu.ws.numel() // 2 - 128,), generator=g, dtype=torch.int16)
+    gpu.ws.view(torch.int16)[128:].copy_(junk)  # keep the 256-byte header, scramble the hints
+    assert step_both(wl, orc, gpu, 3) == 0
+    # request 0 starts over with an empty buffer; its hints still describe the old contents
+    for name in ("tokens", "stamps"):
+        getattr(orc, name)[0, :] = -1 if name == "tokens" else 0
+    orc.clock[0] = 0
+    gpu.tok[0].fill_(-1)
+    gpu.st[0].fill_(0)
+    gpu.clk[0] = 0
+    for s in range(4, 8):
+        assert step_both(wl, orc, gpu, s) == 0
