@@ -28,6 +28,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 METRIC = "top-k rows resolved/s"
+_HOST_POOLS = {}  # registered host pools kept across runs that share a host layout
 UNIT = "rows/s"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -42,6 +43,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="run every miss-rate sweep point (hot slots x reuse), one JSON line each")
     return ap.parse_args()
 
 
@@ -127,16 +130,28 @@ def max_over_ranks(x: float, ws: int) -> float:
     return float(t.item())
 
 
-def alloc_host(nbytes: int) -> np.ndarray:
-    """Host pool bytes: page-aligned, on transparent huge pages where allowed (the GPU's
-    first access to each host page is expensive; huge pages make those rare)."""
-    import mmap
-    m = mmap.mmap(-1, nbytes, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
-    try:
-        m.madvise(mmap.MADV_HUGEPAGE)
-    except (AttributeError, OSError):
-        pass
-    return np.frombuffer(m, dtype=np.uint8, count=nbytes)
+_POOL_OBJS = []  # workloads.HostPool objects behind the arrays in use
+
+
+def alloc_host(nbytes: int):
+    """Host pool bytes: huge pages when the host gives the whole pool, else driver-pinned
+    memory (workloads.HostPool: the GPU reads random host rows fastest from huge pages).
+    Returns (array, needs hs_host_register)."""
+    import workloads as W
+    pool = W.HostPool(nbytes)
+    _POOL_OBJS.append(pool)
+    return pool.array, pool.needs_register
+
+
+def host_device_ptr(arr) -> int:
+    """Device-side address of driver-pinned, mapped host memory."""
+    import ctypes
+    import workloads as W
+    dp = ctypes.c_void_p()
+    err = W._CudaRt.get().cudaHostGetDevicePointer(ctypes.byref(dp), ctypes.c_void_p(arr.ctypes.data), 0)
+    if err != 0:
+        raise RuntimeError(f"cudaHostGetDevicePointer failed ({err})")
+    return dp.value
 
 
 class _DeviceView:
@@ -147,12 +162,19 @@ class _DeviceView:
                                          "version": 3}
 
 
+TOUCH_PASSES = 8
+
+
 def touch_host_pool_from_gpu(dev_ptr: int, nbytes: int) -> None:
-    """Read the whole registered host pool once from the GPU (set-up, outside timing), so
-    the timed steps see a host pool whose mappings the GPU has already used."""
+    """Read the whole registered host pool from the GPU, TOUCH_PASSES times (set-up,
+    outside timing), so the timed steps see a host pool whose mappings the GPU has already
+    used. One pass is not enough: regions first reached by the resolve kernel's random row
+    reads then cost ~0.5 ms once each in the first few dozen steps; eight passes (or ~64
+    warm-up steps) leave none."""
     import torch
     v = torch.as_tensor(_DeviceView(dev_ptr, nbytes), device="cuda")
-    v[::8].sum().item()
+    for _ in range(TOUCH_PASSES):
+        v[::8].sum().item()
 
 
 def newest_rows(wl, step):
@@ -234,7 +256,7 @@ def run_reference(args, ws, rank):
     import workloads as W
     steps = args.warmup + args.steps
     wl = W.make(args.config, args.seed, steps=steps)
-    host = [alloc_host(wl.host_rows * wl.B) for _ in range(wl.L)]
+    host = [np.empty(wl.host_rows * wl.B, dtype=np.uint8) for _ in range(wl.L)]  # CPU only
     for l in range(wl.L):
         wl.fill_host_pool(l, host[l])
     for s in range(steps):
@@ -269,11 +291,23 @@ def run_ours(args, ws, rank, local):
     wl = W.make(args.config, args.seed + 1000 * rank, steps=total_steps)
     R, K, H, B, L = wl.R, wl.K, wl.H, wl.B, wl.L
 
-    # ---- inputs: host pool (pinned, mapped), device pool, tables, all steps' top-k
-    host = [alloc_host(wl.host_rows * B) for _ in range(L)]
-    for l in range(L):
-        wl.fill_host_pool(l, host[l])
-        touch_host_pool_from_gpu(hs.hs_host_register(host[l]), host[l].nbytes)
+    # ---- inputs: host pool (pinned, mapped), device pool, tables, all steps' top-k. The
+    # sweep points share one host layout, so their host pool is built once.
+    key = (args.config.split("_")[0], args.seed + 1000 * rank, wl.host_rows, B, L, total_steps)
+    if key not in _HOST_POOLS:
+        for old in list(_HOST_POOLS):
+            for p, reg in _HOST_POOLS.pop(old):
+                if reg:
+                    hs.hs_host_unregister(p)
+            for obj in _POOL_OBJS:
+                obj.free()
+            _POOL_OBJS.clear()
+        pools = [alloc_host(wl.host_rows * B) for _ in range(L)]
+        for l, (arr, reg) in enumerate(pools):
+            wl.fill_host_pool(l, arr)
+            touch_host_pool_from_gpu(hs.hs_host_register(arr) if reg else host_device_ptr(arr), arr.nbytes)
+        _HOST_POOLS[key] = pools
+    host = [arr for arr, _ in _HOST_POOLS[key]]
     dpool = []
     for l in range(L):
         init = np.full(wl.device_rows * B, 0xA5, dtype=np.uint8)
@@ -482,8 +516,7 @@ def run_ours(args, ws, rank, local):
                                        nthreads=ncores)
         line["cpu_baseline_threaded"] = {"value": rows_m / sec_m, "unit": UNIT, "cores": ncores,
                                          "kind": "oracle sharded by request over threads"}
-    for p in host:
-        hs.hs_host_unregister(p)
+    hs.hs_destroy(h)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -493,6 +526,12 @@ def main():
     ws, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.sweep:
+        import workloads as W
+        for hot in W.SWEEP_HOT:
+            for reuse in W.SWEEP_REUSE:
+                args.config = f"sweep_h{hot}_f{reuse}"
+                run_ours(args, ws, rank, local)
     else:
         run_ours(args, ws, rank, local)
     if ws > 1:

@@ -75,11 +75,10 @@ struct Layout {
 // Shared-memory carve-up of a copy CTA q (rank 1..C). It owns top-k entries
 // [(q-1) * per, q * per) with per = ceil(K / C): their outcomes, published by the resolve CTA
 // (res: device row of a miss, -2 - slot for a hit, -1 otherwise), its slice of the top-k row,
-// the slot map (to check hints), per entry the staging index and host row, the lists of
-// staged and of directly copied entries, two counters, and the staging area (copy_cap
-// entries x L rows of B bytes).
+// per entry the staging index and host row, the lists of staged and of directly copied
+// entries, two counters, and the staging area (copy_cap entries x L rows of B bytes).
 struct CopyLayout {
-  size_t res, tk, tok, stg, hrow, list, dlist, cnt, stage, total;
+  size_t res, tk, stg, hrow, list, dlist, cnt, stage, total;
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -119,7 +118,6 @@ __host__ __device__ inline CopyLayout make_copy_layout(const Geometry& g) {
   const size_t per = (size_t)copy_slice(g), cap = (size_t)g.copy_cap;
   l.res = o; o = align16(o + 4 * per);
   l.tk = o; o = align16(o + 4 * per);
-  l.tok = o; o = align16(o + 4 * (size_t)g.H);
   l.stg = o; o = align16(o + 2 * per);
   l.hrow = o; o = align16(o + 4 * per);
   l.list = o; o = align16(o + 2 * cap);
@@ -333,7 +331,9 @@ __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc
 // Copy CTA q of request r (cluster rank q >= 1; its shared outcome table was cleared to -1
 // and its counters to 0 before the cluster's first barrier).
 // With a hint table and a request past the fast path, it first predicts which of its
-// entries miss: a hot lookup whose hinted slot does not hold it. It looks up the predicted
+// entries miss: a hot lookup with no hinted slot (the hints are exact while the caller
+// leaves the state to the kernels; a stale one only turns a miss into an unpredicted one,
+// and the miss's new slot rewrites it). It looks up the predicted
 // misses' host rows and reads those rows into shared memory right away (16-byte loads,
 // kCopyUnroll in flight per thread), so the host-link transfer runs while the resolve CTA
 // does the exact work. The cluster barrier then publishes the exact outcome of every entry.
@@ -345,7 +345,6 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
   const CopyLayout cl = make_copy_layout(g);
   const int32_t* c_res = reinterpret_cast<const int32_t*>(smem + cl.res);
   int32_t* c_tk = reinterpret_cast<int32_t*>(smem + cl.tk);
-  int32_t* c_tok = reinterpret_cast<int32_t*>(smem + cl.tok);
   int16_t* c_stg = reinterpret_cast<int16_t*>(smem + cl.stg);
   int32_t* c_hrow = reinterpret_cast<int32_t*>(smem + cl.hrow);
   int16_t* c_list = reinterpret_cast<int16_t*>(smem + cl.list);
@@ -368,7 +367,6 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
 
   if (predict) {
     cp_async_words(c_tk, tk_g, ne);
-    cp_async_words(c_tok, a.device_buffer_tokens + (size_t)r * g.H, g.H);
     cp_async_commit();
     cp_async_wait_all();
     __syncthreads();
@@ -378,7 +376,7 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
       if (t >= 0 && t < S - 1 &&
           !(a.resident_pages && a.resident_pages[(size_t)r * g.max_pages + t / g.page_size] >= 0)) {
         const int gs = hint_row[t];
-        if (!(gs >= 0 && gs < g.H && c_tok[gs] == t)) {
+        if (!(gs >= 0 && gs < g.H)) {
           const uint32_t k = atomicAdd(&c_cnt[0], 1u);
           if ((int)k < g.copy_cap) {
             st = (int16_t)k;
@@ -561,6 +559,7 @@ __global__ void __launch_bounds__(T, 1)
   for (int h = tid; h < HS; h += T) s_hash[h] = kEmpty;
   for (int i = tid; i < K; i += T) s_claim[i] = INF;
   if (tid < SC_COUNT) s_sc[tid] = tid == SC_LO ? 0xffffffffu : 0u;
+  if (tid < 256) s_hist[tid] = 0;
   cp_async_wait_all();
   __syncthreads();
 
@@ -641,14 +640,18 @@ __global__ void __launch_bounds__(T, 1)
       flags |= HS_FLAG_STATE;
     }
     const int32_t i = lookup_entry(s_hash, s_cls, g.hash_bits, tkn);
+    bool used = false;
     if (i >= 0) {
       if (atomicCAS(&s_claim[i], INF, s) == INF) {
         s_stamp[s] = clock;
         f |= SF_USED | SF_DIRTY;
+        used = true;
       } else {
         s_sc[SC_CONFLICT] = 1u;  // a second slot holds the token: settled below
       }
     }
+    if (tkn >= 0 && !used)  // an eviction candidate: count it by age, oldest bin = 255 and up
+      atomicAdd(&s_hist[min(clock - 1 - st, 255)], 1);
     s_sflag[s] = f;
   }
   __syncthreads();
@@ -733,54 +736,29 @@ __global__ void __launch_bounds__(T, 1)
 
   // ---- phase 6: the m2 oldest occupied, un-hit slots, ordered by (stamp, slot)
   if (m2 > 0) {
-    uint32_t lo = 0xffffffffu, hi = 0u;
-    for (int s = tid; s < H; s += T)
-      if (s_tok[s] >= 0 && !(s_sflag[s] & SF_USED)) {
-        lo = min(lo, (uint32_t)s_stamp[s]);
-        hi = max(hi, (uint32_t)s_stamp[s]);
-      }
-    lo = __reduce_min_sync(FULL, lo);
-    hi = __reduce_max_sync(FULL, hi);
-    if ((tid & 31) == 0) {
-      atomicMin(&s_sc[SC_LO], lo);
-      atomicMax(&s_sc[SC_HI], hi);
-    }
-    __syncthreads();
-    const uint32_t base = s_sc[SC_LO];
-    const uint32_t maxd = s_sc[SC_HI] - base;
-    const int nbits = maxd ? 32 - __clz(maxd) : 0;
-    const int passes = (nbits + 7) >> 3;
-    uint32_t prefix = 0;
-    int rank = m2;  // 1-based rank of the last victim among the candidates
-    for (int pz = passes - 1; pz >= 0; --pz) {
-      const int shift = pz * 8;
-      if (tid < 256) s_hist[tid] = 0;
-      __syncthreads();
-      for (int s = tid; s < H; s += T) {
-        if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
-        const uint32_t d = (uint32_t)s_stamp[s] - base;
-        const bool match = (shift + 8 >= 32) || ((d >> (shift + 8)) == (prefix >> (shift + 8)));
-        if (match) atomicAdd(&s_hist[(d >> shift) & 255], 1);
-      }
-      __syncthreads();
-      if (tid < 32) {
+    // Threshold from the age histogram phase 3 built (age = clock - 1 - stamp, ages of 255
+    // and more share the last bin): exact when phase 3's claims stood and the threshold age
+    // is below 255; otherwise an exact radix select over the stamps.
+    bool by_age = s_sc[SC_CONFLICT] == 0u;
+    if (by_age) {
+      if (tid < 32) {  // lane l holds bins 255-8l .. 248-8l: the oldest first
         int loc[8];
         int sum = 0;
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-          loc[b] = s_hist[tid * 8 + b];
+          loc[b] = s_hist[255 - (tid * 8 + b)];
           sum += loc[b];
         }
         const int incl = warp_incl_scan(sum);
-        const unsigned ball = __ballot_sync(FULL, incl >= rank);
+        const unsigned ball = __ballot_sync(FULL, incl >= m2);
         const int first = __ffs(ball) - 1;
         if (tid == first) {
           int cum = incl - sum;
 #pragma unroll
           for (int b = 0; b < 8; ++b) {
-            if (cum + loc[b] >= rank) {
-              s_sc[SC_DIGIT] = (uint32_t)(tid * 8 + b);
-              s_sc[SC_RANK] = (uint32_t)(rank - cum);
+            if (cum + loc[b] >= m2) {
+              s_sc[SC_DIGIT] = (uint32_t)(255 - (tid * 8 + b));
+              s_sc[SC_RANK] = (uint32_t)(m2 - cum);
               break;
             }
             cum += loc[b];
@@ -788,41 +766,128 @@ __global__ void __launch_bounds__(T, 1)
         }
       }
       __syncthreads();
-      prefix |= s_sc[SC_DIGIT] << shift;
-      rank = (int)s_sc[SC_RANK];
+      by_age = s_sc[SC_DIGIT] < 255u;
+    }
+    if (by_age) {
+      const int32_t age_thr = (int32_t)s_sc[SC_DIGIT];
+      const int need_eq = (int)s_sc[SC_RANK];  // victims taken among the candidates of that age
+      const int n_gt = m2 - need_eq;            // candidates older than the threshold
+      int c_gt = 0, c_eq = 0;
+      for (int s = s0; s < s1; ++s) {
+        if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
+        const int32_t age = clock - 1 - s_stamp[s];
+        c_gt += age > age_thr;
+        c_eq += age == age_thr;
+      }
+      int tot2;
+      const int pk = block_excl_scan((c_gt << 16) | c_eq, s_wsum, &tot2);
+      int p_gt = pk >> 16, p_eq = pk & 0xffff;
+      for (int s = s0; s < s1; ++s) {
+        if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
+        const int32_t age = clock - 1 - s_stamp[s];
+        const uint64_t key = ((uint64_t)(uint32_t)s_stamp[s] << 32) | (uint32_t)s;
+        if (age > age_thr) {
+          s_keys[p_gt++] = key;
+        } else if (age == age_thr) {
+          if (p_eq < need_eq) s_keys[n_gt + p_eq] = key;
+          ++p_eq;
+        }
+      }
+    } else {
+      uint32_t lo = 0xffffffffu, hi = 0u;
+      for (int s = tid; s < H; s += T)
+        if (s_tok[s] >= 0 && !(s_sflag[s] & SF_USED)) {
+          lo = min(lo, (uint32_t)s_stamp[s]);
+          hi = max(hi, (uint32_t)s_stamp[s]);
+        }
+      lo = __reduce_min_sync(FULL, lo);
+      hi = __reduce_max_sync(FULL, hi);
+      if ((tid & 31) == 0) {
+        atomicMin(&s_sc[SC_LO], lo);
+        atomicMax(&s_sc[SC_HI], hi);
+      }
       __syncthreads();
-    }
-    const uint32_t thr = prefix;    // stamp - base of the last victim
-    const int need_eq = rank;       // victims taken among the candidates at the threshold
-    const int n_lt = m2 - need_eq;  // candidates strictly below the threshold
-    int c_lt = 0, c_eq = 0;
-    for (int s = s0; s < s1; ++s) {
-      if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
-      const uint32_t d = (uint32_t)s_stamp[s] - base;
-      c_lt += d < thr;
-      c_eq += d == thr;
-    }
-    int tot2;
-    const int pk = block_excl_scan((c_lt << 16) | c_eq, s_wsum, &tot2);
-    int p_lt = pk >> 16, p_eq = pk & 0xffff;
-    for (int s = s0; s < s1; ++s) {
-      if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
-      const uint32_t d = (uint32_t)s_stamp[s] - base;
-      if (d < thr) {
-        s_keys[p_lt++] = ((uint64_t)d << 32) | (uint32_t)s;
-      } else if (d == thr) {
-        if (p_eq < need_eq) s_keys[n_lt + p_eq] = ((uint64_t)d << 32) | (uint32_t)s;
-        ++p_eq;
+      const uint32_t base = s_sc[SC_LO];
+      const uint32_t maxd = s_sc[SC_HI] - base;
+      const int nbits = maxd ? 32 - __clz(maxd) : 0;
+      const int passes = (nbits + 7) >> 3;
+      uint32_t prefix = 0;
+      int rank = m2;  // 1-based rank of the last victim among the candidates
+      for (int pz = passes - 1; pz >= 0; --pz) {
+        const int shift = pz * 8;
+        if (tid < 256) s_hist[tid] = 0;
+        __syncthreads();
+        for (int s = tid; s < H; s += T) {
+          if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
+          const uint32_t d = (uint32_t)s_stamp[s] - base;
+          const bool match = (shift + 8 >= 32) || ((d >> (shift + 8)) == (prefix >> (shift + 8)));
+          if (match) atomicAdd(&s_hist[(d >> shift) & 255], 1);
+        }
+        __syncthreads();
+        if (tid < 32) {
+          int loc[8];
+          int sum = 0;
+  #pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            loc[b] = s_hist[tid * 8 + b];
+            sum += loc[b];
+          }
+          const int incl = warp_incl_scan(sum);
+          const unsigned ball = __ballot_sync(FULL, incl >= rank);
+          const int first = __ffs(ball) - 1;
+          if (tid == first) {
+            int cum = incl - sum;
+  #pragma unroll
+            for (int b = 0; b < 8; ++b) {
+              if (cum + loc[b] >= rank) {
+                s_sc[SC_DIGIT] = (uint32_t)(tid * 8 + b);
+                s_sc[SC_RANK] = (uint32_t)(rank - cum);
+                break;
+              }
+              cum += loc[b];
+            }
+          }
+        }
+        __syncthreads();
+        prefix |= s_sc[SC_DIGIT] << shift;
+        rank = (int)s_sc[SC_RANK];
+        __syncthreads();
+      }
+      const uint32_t thr = prefix;    // stamp - base of the last victim
+      const int need_eq = rank;       // victims taken among the candidates at the threshold
+      const int n_lt = m2 - need_eq;  // candidates strictly below the threshold
+      int c_lt = 0, c_eq = 0;
+      for (int s = s0; s < s1; ++s) {
+        if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
+        const uint32_t d = (uint32_t)s_stamp[s] - base;
+        c_lt += d < thr;
+        c_eq += d == thr;
+      }
+      int tot2;
+      const int pk = block_excl_scan((c_lt << 16) | c_eq, s_wsum, &tot2);
+      int p_lt = pk >> 16, p_eq = pk & 0xffff;
+      for (int s = s0; s < s1; ++s) {
+        if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
+        const uint32_t d = (uint32_t)s_stamp[s] - base;
+        if (d < thr) {
+          s_keys[p_lt++] = ((uint64_t)d << 32) | (uint32_t)s;
+        } else if (d == thr) {
+          if (p_eq < need_eq) s_keys[n_lt + p_eq] = ((uint64_t)d << 32) | (uint32_t)s;
+          ++p_eq;
+        }
       }
     }
     __syncthreads();
     if (m2 <= kRankSortMax) {
-      // the keys are distinct: a victim's rank is the number of smaller keys
-      for (int j = tid; j < m2; j += T) {
+      // the keys are distinct: a victim's rank is the number of smaller keys; one warp per
+      // victim, its lanes splitting the comparisons
+      const int lane = tid & 31;
+      for (int j = tid >> 5; j < m2; j += NW) {
         const uint64_t kj = s_keys[j];
         int rk = 0;
-        for (int u = 0; u < m2; ++u) rk += s_keys[u] < kj;
-        s_vict[take_free + rk] = (int32_t)(kj & 0xffffffffu);
+        for (int u = lane; u < m2; u += 32) rk += s_keys[u] < kj;
+        rk = __reduce_add_sync(FULL, rk);
+        if (lane == 0) s_vict[take_free + rk] = (int32_t)(kj & 0xffffffffu);
       }
     } else {
       int n = 1;

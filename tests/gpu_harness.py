@@ -5,8 +5,6 @@ hs_host_register and shared with the oracle run, which reads the same bytes.
 """
 from __future__ import annotations
 
-import mmap
-
 import numpy as np
 import torch
 
@@ -15,16 +13,20 @@ import workloads as W
 from harness import newest_writes
 
 
+_POOLS = {}  # data address -> workloads.HostPool (keeps the memory alive, knows how it was pinned)
+
+
 def alloc_host(nbytes: int) -> np.ndarray:
-    """Page-aligned host bytes (unpinned until registered), backed by transparent huge pages
-    where the kernel allows: the GPU pays its first-access cost per host page, and huge
-    pages make that cost rare."""
-    m = mmap.mmap(-1, max(nbytes, 1), flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
-    try:
-        m.madvise(mmap.MADV_HUGEPAGE)
-    except (AttributeError, OSError):
-        pass
-    return np.frombuffer(m, dtype=np.uint8, count=nbytes)
+    """Host bytes for a KV pool (huge pages when the host gives the whole pool, else
+    driver-pinned memory; see workloads.HostPool)."""
+    pool = W.HostPool(nbytes)
+    _POOLS[pool.array.ctypes.data] = pool
+    return pool.array
+
+
+def needs_register(arr: np.ndarray) -> bool:
+    pool = _POOLS.get(arr.ctypes.data)
+    return True if pool is None else pool.needs_register
 
 
 def host_pools(wl: W.Workload, nthreads: int = 0):
@@ -42,8 +44,9 @@ class GpuSim:
         self.host = host
         self.registered = []
         for p in host:
-            hs.hs_host_register(p)
-            self.registered.append(p)
+            if needs_register(p):
+                hs.hs_host_register(p)
+                self.registered.append(p)
         dev = torch.device(device)
         self.dev = [torch.from_numpy(np.ascontiguousarray(m)).to(dev) for m in dev_init]
         self.hcl = torch.from_numpy(wl.host_cache_locs).to(dev)

@@ -146,11 +146,12 @@ def test_api_misuse():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import hierarchical_sparse_attention_gb300 as hs
-    from gpu_harness import alloc_host
     cfg = hs.make_config(2, 64, 128, 576, 1, 0, 1024, 0)
     dev = torch.zeros(1000 * 576, dtype=torch.uint8, device="cuda")
     ws = torch.zeros(hs.hs_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
-    host = alloc_host(1000 * 576)
+    import mmap
+    raw = mmap.mmap(-1, 1000 * 576, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+    host = np.frombuffer(raw, dtype=np.uint8)
     with pytest.raises(hs.HsError) as e:  # host pool not registered
         hs.hs_create(cfg, [host], [dev], 1000, 1000, ws)
     assert e.value.status == hs.HS_ERR_INVALID_ARG

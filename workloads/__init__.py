@@ -84,6 +84,112 @@ def _ptr(a: np.ndarray) -> int:
 
 
 # --------------------------------------------------------------------------------------
+# host pool memory
+# --------------------------------------------------------------------------------------
+_HUGE = 0
+
+
+def _huge_page_bytes() -> int:
+    global _HUGE
+    if not _HUGE:
+        try:
+            _HUGE = int(open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size").read())
+        except (OSError, ValueError):
+            _HUGE = 2 << 20
+    return _HUGE
+
+
+def _huge_backed_bytes(addr: int, nbytes: int) -> int:
+    """AnonHugePages of the mapping that starts at addr (from /proc/self/smaps)."""
+    try:
+        lines = open("/proc/self/smaps").read().splitlines()
+    except OSError:
+        return 0
+    inside = False
+    for ln in lines:
+        head = ln.split()[0] if ln else ""
+        if "-" in head and ":" not in head:
+            lo = int(head.split("-")[0], 16)
+            inside = lo == addr
+        elif inside and ln.startswith("AnonHugePages:"):
+            return int(ln.split()[1]) * 1024
+    return 0
+
+
+class _CudaRt:
+    lib = None
+
+    @classmethod
+    def get(cls):
+        if cls.lib is None:
+            for name in ("libcudart.so", "libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so"):
+                try:
+                    cls.lib = ctypes.CDLL(name)
+                    break
+                except OSError:
+                    continue
+            if cls.lib is None:
+                raise OSError("libcudart not found")
+        return cls.lib
+
+
+class HostPool:
+    """Host memory for one layer's KV pool, pinned and mapped for the GPU.
+
+    The GPU reads random rows of a host pool fastest when the pool sits on huge pages:
+    with ordinary pages its translations thrash, and when the host cannot give the whole
+    pool transparent huge pages the fallback regions do. So the pool is an anonymous
+    mapping advised onto transparent huge pages, and if the kernel does not back every
+    byte with them it is replaced by driver-pinned memory (cudaHostAlloc, mapped and
+    portable). `array` is the bytes; `needs_register` tells whether the caller must still
+    page-lock it (hs_host_register), i.e. the huge-page path."""
+
+    def __init__(self, nbytes: int):
+        import mmap
+        self.nbytes = int(nbytes)
+        self._mmap = None
+        self._cuda_ptr = None
+        huge = _huge_page_bytes()
+        m = mmap.mmap(-1, max(self.nbytes, 1), flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        arr = np.frombuffer(m, dtype=np.uint8, count=self.nbytes)
+        ok = False
+        try:
+            m.madvise(mmap.MADV_HUGEPAGE)
+            arr[::huge] = 0  # fault every huge page in
+            ok = _huge_backed_bytes(arr.ctypes.data, self.nbytes) >= (self.nbytes // huge) * huge
+        except (AttributeError, OSError, ValueError):
+            ok = False
+        if ok or self.nbytes < huge:
+            self._mmap = m
+            self.array = arr
+            self.needs_register = True
+            return
+        del arr
+        m.close()
+        rt = _CudaRt.get()
+        ptr = ctypes.c_void_p()
+        # cudaHostAllocPortable | cudaHostAllocMapped
+        err = rt.cudaHostAlloc(ctypes.byref(ptr), ctypes.c_size_t(self.nbytes), ctypes.c_uint(1 | 2))
+        if err != 0 or not ptr.value:
+            raise MemoryError(f"cudaHostAlloc of {self.nbytes} bytes failed ({err})")
+        self._cuda_ptr = ptr.value
+        self.array = np.ctypeslib.as_array((ctypes.c_uint8 * self.nbytes).from_address(ptr.value))
+        self.needs_register = False
+
+    def free(self):
+        if self._cuda_ptr:
+            _CudaRt.get().cudaFreeHost(ctypes.c_void_p(self._cuda_ptr))
+            self._cuda_ptr = None
+        self.array = None
+        if self._mmap is not None:
+            try:
+                self._mmap.close()
+            except BufferError:
+                pass  # views still alive; the mapping goes with them
+            self._mmap = None
+
+
+# --------------------------------------------------------------------------------------
 # configurations
 # --------------------------------------------------------------------------------------
 @dataclass
