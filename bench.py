@@ -500,6 +500,8 @@ def run_ours(args, ws, rank, local):
                              "algorithmic_bytes_per_launch": float(hbm_bytes.mean())}},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
                 "steps": e2e_steps, "timing": "wall clock per step, host enqueue to stream sync"},
+        "host_pool": ("huge pages, hs_host_register" if _HOST_POOLS[key][0][1]
+                      else "cudaHostAlloc (host could not back the pool with huge pages)"),
         "gpu_launches": 2 * K_,
         "device_flags": err,
         "clocks": clocks.summary(),
@@ -526,6 +528,19 @@ def main():
     ws, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.sweep and ws == 1:
+        # One process per point, as a serving process holds one pool for its lifetime:
+        # tearing down and rebuilding tens of GB of pinned host memory inside one process
+        # leaves later points on fragmented memory (no huge pages) or with host-link stalls.
+        import workloads as W
+        fwd = ["--steps", str(args.steps), "--warmup", str(args.warmup), "--seed", str(args.seed)]
+        fwd += ["--no-cpu-baseline"] * args.no_cpu_baseline + ["--no-clocks"] * args.no_clocks
+        for hot in W.SWEEP_HOT:
+            for reuse in W.SWEEP_REUSE:
+                r = subprocess.run([sys.executable, os.path.abspath(__file__), "--config",
+                                    f"sweep_h{hot}_f{reuse}"] + fwd)
+                if r.returncode != 0:
+                    sys.exit(r.returncode)
     elif args.sweep:
         import workloads as W
         for hot in W.SWEEP_HOT:
