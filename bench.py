@@ -188,15 +188,24 @@ def newest_rows(wl, step):
 def ncu_traffic(config: str) -> dict:
     """Per-launch traffic of the resolve kernel from the committed ncu capture, when that
     capture was taken on this workload and on the kernel source as it is now; else {}."""
-    import hashlib
     try:
         rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
-        src = open(os.path.join(ROOT, rec["kernel_source"]), "rb").read()
+        code = kernel_code_hash(os.path.join(ROOT, rec["kernel_source"]))
     except (OSError, ValueError, KeyError):
         return {}
-    if rec.get("workload") != config or hashlib.sha256(src).hexdigest()[:16] != rec.get("sha256_16"):
+    if rec.get("workload") != config or code != rec.get("code_sha256_16"):
         return {}
     return rec
+
+
+def kernel_code_hash(path: str) -> str:
+    """sha256[:16] of a CUDA source with its // comments and all whitespace removed, so a
+    comment edit does not retire a profile of the same code."""
+    import hashlib
+    import re
+    text = open(path, encoding="utf-8").read()
+    code = re.sub(r"//[^\n]*", "", text)
+    return hashlib.sha256(re.sub(r"\s+", "", code).encode()).hexdigest()[:16]
 
 
 # ------------------------------------------------------------------------------------------

@@ -1,4 +1,4 @@
-// Fused decode-step resolver / swap-in: one CTA of 1024 threads per request.
+// Fused decode-step resolver / swap-in: one thread block cluster per request.
 //
 // Sources (page title, section):
 //   "HiSparse: Turbocharging Sparse Attention with Hierarchical Memory" (LMSYS), "Efficient
@@ -20,30 +20,34 @@
 // The step is latency-bound (a few MB over the host link, a few tens of KB of state per
 // request), so the kernel is arranged to start the host-link transfer as early as
 // possible and to hide the rest of the bookkeeping behind it. Each request gets a thread
-// block cluster: CTA 0 resolves, and up to three copy CTAs on other SMs move the miss rows.
+// block cluster of 1024-thread CTAs: CTA 0 resolves, and up to three copy CTAs on other
+// SMs move the miss rows.
 // Phases of the resolve CTA (request r):
 //   0  cp.async the top-k row, the slot map, the stamps and the slot->row table into
 //      shared memory while the hash table is cleared
 //   1  reject padding / out-of-range tokens; hash the valid ones (open addressing,
-//      Knuth multiplicative); a repeated token keeps its first index
-//   2  classify each entry: resident row, fast-path identity, reserved newest row, or hot
-//      lookup
+//      Knuth multiplicative; a repeated token keeps its first index) and classify each
+//      entry: resident row, fast-path identity, reserved newest row, or hot lookup
 //   3  reset corrupt slots; probe each slot's token; the first slot to claim a looked-up
-//      token takes the hit (stamp = clock). Two holders of one token (corrupt state only)
-//      are settled afterwards in favour of the lowest slot
-//   4  hits output their slot's row; each miss token is handed, through distributed shared
-//      memory, to a copy CTA, which starts pulling its host row(s) into its own shared
-//      memory while the resolve CTA goes on (split cluster barrier, phase A)
+//      token takes the hit (stamp = clock) and the other candidates enter an age
+//      histogram. Two holders of one token (corrupt state only) are settled afterwards in
+//      favour of the lowest slot
+//   4  hits output their slot's row and tell the entry's copy CTA the slot
 //   5  one packed block scan orders the misses (top-k order) and the free slots (slot order)
-//   6  if misses outnumber free slots: radix-select the stamp threshold among occupied,
-//      un-hit slots, take exactly the needed victims and order them by (stamp, slot)
-//   7  pair miss j with victim j: update the map; send each handed-off miss's device row
-//      to its copy CTA (cluster barrier, phase B)
+//   6  if misses outnumber free slots: the stamp threshold among occupied, un-hit slots
+//      comes from the age histogram (exact radix select when the histogram cannot decide);
+//      exactly the needed victims are gathered and ordered by (stamp, slot)
+//   7  pair miss j with victim j: update the map and the token->slot hints; publish each
+//      miss's device row to its copy CTA (distributed shared memory, then the release half
+//      of the split cluster barrier)
 //   8  write back the changed slots, the row table and the clock
-//   9  copy the misses no copy CTA took (none, unless the copy CTAs' staging is full or
-//      the geometry runs without them) straight from host memory
-// A copy CTA: wait for its miss tokens (phase A), look up their host rows, cp.async the
-// rows into shared memory, wait for the device rows (phase B), then store them.
+//   9  copy the misses no copy CTA took (only when the geometry runs without copy CTAs)
+//      straight from host memory
+// A copy CTA owns a slice of the top-k row. At kernel start it predicts its slice's
+// misses from the token->slot hint table (a looked-up token with no hinted slot), looks
+// up their host rows and pulls them into shared memory while the resolve CTA does the
+// exact work; after the cluster barrier it stores the staged rows of exact misses to their
+// device rows and copies any unpredicted miss straight from host memory.
 #include <climits>
 
 #include "hs_internal.h"
