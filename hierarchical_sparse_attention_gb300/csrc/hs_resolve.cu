@@ -60,7 +60,6 @@ constexpr int NW = T / 32;
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int32_t INF = 0x7fffffff;
 constexpr int kCopyUnroll = 4;
-constexpr int kRankSortMax = 1024;  // victims ordered by counting ranks up to this many
 
 enum : uint8_t { C_PAD = 0, C_BAD, C_DUP, C_RES, C_FAST, C_NEWEST, C_LOOKUP };
 constexpr uint8_t C_BADROW = 0x80;  // with C_RES / C_FAST / C_NEWEST: its row is out of range
@@ -140,26 +139,6 @@ __device__ __forceinline__ int warp_incl_scan(int x) {
     if (lane >= o) x += y;
   }
   return x;
-}
-
-// Exclusive prefix sum of v over the CTA, in thread order. Ends synchronised, so wsum
-// can be reused by the next call.
-__device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int incl = warp_incl_scan(v);
-  if (lane == 31) wsum[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    const int s = wsum[lane];
-    const int si = warp_incl_scan(s);
-    wsum[lane] = si - s;
-    if (lane == 31) wsum[NW] = si;
-  }
-  __syncthreads();
-  const int res = incl - v + wsum[w];
-  *total = wsum[NW];
-  __syncthreads();
-  return res;
 }
 
 __device__ __forceinline__ uint32_t hash_slot(int32_t t, int bits) {
@@ -377,6 +356,9 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
     for (int e = tid; e < ne; e += T) {
       const int32_t t = c_tk[e];
       int16_t st = -1;  // -1: not predicted to miss; -2: predicted, no staging room
+      // The host-row lookup waits for the prediction: issuing it for every entry up front
+      // saves a round trip but adds one HBM request per top-k entry at kernel start, which
+      // delays the whole cluster's loads more than it saves (measured).
       if (t >= 0 && t < S - 1 &&
           !(a.resident_pages && a.resident_pages[(size_t)r * g.max_pages + t / g.page_size] >= 0)) {
         const int gs = hint_row[t];
@@ -416,6 +398,7 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
       }
     }
   }
+  cluster_wait();    // phase A (arrived at kernel start)
   cluster_arrive();  // phase B: the resolve CTA has published every entry's outcome
   cluster_wait();
   __syncthreads();
@@ -496,8 +479,10 @@ __global__ void __launch_bounds__(T, 1)
   if (tid < (int)(sizeof(Pools) / sizeof(uint64_t)))
     reinterpret_cast<uint64_t*>(&s_pools)[tid] = reinterpret_cast<const uint64_t*>(pools)[tid];
   if (C > 0) {
-    // Every CTA of the cluster runs (and each copy CTA has cleared its outcome table and
-    // counters) before any CTA touches another's shared memory.
+    // Barrier phase A: every CTA of the cluster runs, and each copy CTA has cleared its
+    // outcome table and counters, before the resolve CTA stores into a copy CTA's shared
+    // memory. Only that first remote store waits for it (phase 4); the copy CTAs start
+    // their own work at once.
     if (rank > 0) {
       const CopyLayout cl0 = make_copy_layout(g);
       int32_t* res = reinterpret_cast<int32_t*>(smem + cl0.res);
@@ -505,8 +490,8 @@ __global__ void __launch_bounds__(T, 1)
       if (tid < 4) reinterpret_cast<uint32_t*>(smem + cl0.cnt)[tid] = 0u;
     }
     cluster_arrive();
-    cluster_wait();
     if (rank > 0) {
+      __syncthreads();  // the CTA's own clears before its threads read the counters
       copy_cta(g, s_pools, a, r, (int)rank, smem, err_word);
       return;
     }
@@ -630,33 +615,47 @@ __global__ void __launch_bounds__(T, 1)
     return;
   }
 
-  // ---- phase 3: tripwires, membership probe, hits
+  // ---- phase 3: tripwires, membership probe, hits. From here on warp w walks its own run
+  // of slots [sw0, sw1) and of top-k entries [ew0, ew1), 32 consecutive ones at a time, so
+  // shared loads are conflict-free and ballots count in slot / entry order.
+  const int lane = tid & 31, warp = tid >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int SW = (H + T - 1) / T * 32, EW = (K + T - 1) / T * 32;
+  const int sw0 = min(H, warp * SW), sw1 = min(H, sw0 + SW);
+  const int ew0 = min(K, warp * EW), ew1 = min(K, ew0 + EW);
   const int32_t clock = a.lru_clock[r] + 1;
-  for (int s = tid; s < H; s += T) {
-    int32_t tkn = s_tok[s];
-    const int32_t st = s_stamp[s];
-    uint8_t f = 0;
-    if (st < 0 || st > clock - 1 || tkn < -1 || tkn >= S - 1) {
-      tkn = -1;
-      s_tok[s] = -1;
-      s_stamp[s] = 0;
-      f = SF_DIRTY;
-      flags |= HS_FLAG_STATE;
-    }
-    const int32_t i = lookup_entry(s_hash, s_cls, g.hash_bits, tkn);
-    bool used = false;
-    if (i >= 0) {
-      if (atomicCAS(&s_claim[i], INF, s) == INF) {
-        s_stamp[s] = clock;
-        f |= SF_USED | SF_DIRTY;
-        used = true;
-      } else {
-        s_sc[SC_CONFLICT] = 1u;  // a second slot holds the token: settled below
+  int wfree = 0;  // free slots in this warp's run
+  for (int b = sw0; b < sw1; b += 32) {
+    const int s = b + lane;
+    bool is_free = false;
+    if (s < sw1) {
+      int32_t tkn = s_tok[s];
+      const int32_t st = s_stamp[s];
+      uint8_t f = 0;
+      if (st < 0 || st > clock - 1 || tkn < -1 || tkn >= S - 1) {
+        tkn = -1;
+        s_tok[s] = -1;
+        s_stamp[s] = 0;
+        f = SF_DIRTY;
+        flags |= HS_FLAG_STATE;
       }
+      const int32_t i = lookup_entry(s_hash, s_cls, g.hash_bits, tkn);
+      bool used = false;
+      if (i >= 0) {
+        if (atomicCAS(&s_claim[i], INF, s) == INF) {
+          s_stamp[s] = clock;
+          f |= SF_USED | SF_DIRTY;
+          used = true;
+        } else {
+          s_sc[SC_CONFLICT] = 1u;  // a second slot holds the token: settled below
+        }
+      }
+      if (tkn >= 0 && !used)  // an eviction candidate: count it by age, oldest bin = 255 and up
+        atomicAdd(&s_hist[min(clock - 1 - st, 255)], 1);
+      s_sflag[s] = f;
+      is_free = tkn == -1;
     }
-    if (tkn >= 0 && !used)  // an eviction candidate: count it by age, oldest bin = 255 and up
-      atomicAdd(&s_hist[min(clock - 1 - st, 255)], 1);
-    s_sflag[s] = f;
+    wfree += __popc(__ballot_sync(FULL, is_free));
   }
   __syncthreads();
 
@@ -695,54 +694,73 @@ __global__ void __launch_bounds__(T, 1)
   // CTA which slot, so a wrong miss prediction can repair its hint)
   const int per = copy_slice(g);
   const CopyLayout cl = make_copy_layout(g);
-  for (int i = tid; i < K; i += T) {
-    const uint8_t cls = s_cls[i];
-    if (cls != C_PAD && cls != C_BAD && hash_find(s_hash, g.hash_bits, s_tk[i]) != i) {
-      s_cls[i] = C_DUP;  // a later repeat of a valid token
-      s_out[i] = -1;
-      flags |= HS_FLAG_DUP;
-    } else if (cls & C_BADROW) {
-      flags |= HS_FLAG_DEVROW;
-    } else if (cls == C_LOOKUP) {
-      const int32_t c = s_claim[i];
-      if (c != INF) {
-        s_out[i] = checked_row(s_dbl[c], g.device_rows, flags);
-        if (C > 0) st_remote(smem + cl.res + 4 * (size_t)(i % per), 1 + i / per, -2 - c);
+  if (C > 0) cluster_wait();  // phase A: the copy CTAs run and their tables are cleared
+  int wmiss = 0;  // misses in this warp's run of entries
+  for (int b = ew0; b < ew1; b += 32) {
+    const int i = b + lane;
+    bool is_miss = false;
+    if (i < ew1) {
+      const uint8_t cls = s_cls[i];
+      if (cls != C_PAD && cls != C_BAD && hash_find(s_hash, g.hash_bits, s_tk[i]) != i) {
+        s_cls[i] = C_DUP;  // a later repeat of a valid token
+        s_out[i] = -1;
+        flags |= HS_FLAG_DUP;
+      } else if (cls & C_BADROW) {
+        flags |= HS_FLAG_DEVROW;
+      } else if (cls == C_LOOKUP) {
+        const int32_t c = s_claim[i];
+        if (c != INF) {
+          s_out[i] = checked_row(s_dbl[c], g.device_rows, flags);
+          if (C > 0) st_remote(smem + cl.res + 4 * (size_t)(i % per), 1 + i / per, -2 - c);
+        } else {
+          is_miss = true;
+        }
       }
     }
+    wmiss += __popc(__ballot_sync(FULL, is_miss));
   }
+  if (lane == 0) s_wsum[warp] = (wmiss << 16) | wfree;
+  __syncthreads();
 
-  // ---- phase 5: order the misses (top-k order) and the free slots (slot order), one scan
-  const int ept = (K + T - 1) / T;
-  const int spt = (H + T - 1) / T;
-  const int i0 = min(K, tid * ept), i1 = min(K, i0 + ept);
-  const int s0 = min(H, tid * spt), s1 = min(H, s0 + spt);
-  int nmiss = 0, nfree = 0;
-  for (int i = i0; i < i1; ++i) nmiss += (s_cls[i] == C_LOOKUP && s_claim[i] == INF);
-  for (int s = s0; s < s1; ++s) nfree += (s_tok[s] == -1);
-  int packed_total;
-  const int packed = block_excl_scan((nmiss << 16) | nfree, s_wsum, &packed_total);
-  const int m = packed_total >> 16;
-  const int F = packed_total & 0xffff;
+  // ---- phase 5: order the misses (top-k order) and the free slots (slot order): each
+  // warp's base is the sum of the earlier warps' counts (16-bit fields: m <= K, F <= H)
+  int m, F;
   {
-    int pos = packed >> 16;
-    for (int i = i0; i < i1; ++i)
-      if (s_cls[i] == C_LOOKUP && s_claim[i] == INF) s_miss[pos++] = i;
-    pos = packed & 0xffff;
-    for (int s = s0; s < s1; ++s)
-      if (s_tok[s] == -1) {
-        if (pos < m) s_vict[pos] = s;
-        ++pos;
-      }
+    const int v = lane < NW ? s_wsum[lane] : 0;
+    const int tot = __reduce_add_sync(FULL, v);
+    const int before = __reduce_add_sync(FULL, lane < warp ? v : 0);
+    m = tot >> 16;
+    F = tot & 0xffff;
+    int pos = before >> 16;
+    for (int b = ew0; b < ew1; b += 32) {
+      const int i = b + lane;
+      const bool p = i < ew1 && s_cls[i] == C_LOOKUP && s_claim[i] == INF;
+      const unsigned bal = __ballot_sync(FULL, p);
+      if (p) s_miss[pos + __popc(bal & lt_mask)] = i;
+      pos += __popc(bal);
+    }
+    pos = before & 0xffff;
+    for (int b = sw0; b < sw1 && pos < m; b += 32) {
+      const int s = b + lane;
+      const bool p = s < sw1 && s_tok[s] == -1;
+      const unsigned bal = __ballot_sync(FULL, p);
+      const int at = pos + __popc(bal & lt_mask);
+      if (p && at < m) s_vict[at] = s;
+      pos += __popc(bal);
+    }
   }
   const int take_free = min(m, F);
   const int m2 = m - take_free;
 
   // ---- phase 6: the m2 oldest occupied, un-hit slots, ordered by (stamp, slot)
   if (m2 > 0) {
-    // Threshold from the age histogram phase 3 built (age = clock - 1 - stamp, ages of 255
-    // and more share the last bin): exact when phase 3's claims stood and the threshold age
-    // is below 255; otherwise an exact radix select over the stamps.
+    // The threshold stamp thr_st: every candidate with an older stamp is a victim, and so
+    // are the need_eq lowest-numbered candidates stamped thr_st. It comes from the age
+    // histogram phase 3 built (age = clock - 1 - stamp, ages of 255 and more share the last
+    // bin) when phase 3's claims stood and the threshold age is below 255; otherwise from an
+    // exact radix select over the stamps.
+    int32_t thr_st = 0;
+    int need_eq = 0;
     bool by_age = s_sc[SC_CONFLICT] == 0u;
     if (by_age) {
       if (tid < 32) {  // lane l holds bins 255-8l .. 248-8l: the oldest first
@@ -771,33 +789,10 @@ __global__ void __launch_bounds__(T, 1)
       }
       __syncthreads();
       by_age = s_sc[SC_DIGIT] < 255u;
+      thr_st = clock - 1 - (int32_t)s_sc[SC_DIGIT];
+      need_eq = (int)s_sc[SC_RANK];
     }
-    if (by_age) {
-      const int32_t age_thr = (int32_t)s_sc[SC_DIGIT];
-      const int need_eq = (int)s_sc[SC_RANK];  // victims taken among the candidates of that age
-      const int n_gt = m2 - need_eq;            // candidates older than the threshold
-      int c_gt = 0, c_eq = 0;
-      for (int s = s0; s < s1; ++s) {
-        if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
-        const int32_t age = clock - 1 - s_stamp[s];
-        c_gt += age > age_thr;
-        c_eq += age == age_thr;
-      }
-      int tot2;
-      const int pk = block_excl_scan((c_gt << 16) | c_eq, s_wsum, &tot2);
-      int p_gt = pk >> 16, p_eq = pk & 0xffff;
-      for (int s = s0; s < s1; ++s) {
-        if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
-        const int32_t age = clock - 1 - s_stamp[s];
-        const uint64_t key = ((uint64_t)(uint32_t)s_stamp[s] << 32) | (uint32_t)s;
-        if (age > age_thr) {
-          s_keys[p_gt++] = key;
-        } else if (age == age_thr) {
-          if (p_eq < need_eq) s_keys[n_gt + p_eq] = key;
-          ++p_eq;
-        }
-      }
-    } else {
+    if (!by_age) {
       uint32_t lo = 0xffffffffu, hi = 0u;
       for (int s = tid; s < H; s += T)
         if (s_tok[s] >= 0 && !(s_sflag[s] & SF_USED)) {
@@ -831,7 +826,7 @@ __global__ void __launch_bounds__(T, 1)
         if (tid < 32) {
           int loc[8];
           int sum = 0;
-  #pragma unroll
+#pragma unroll
           for (int b = 0; b < 8; ++b) {
             loc[b] = s_hist[tid * 8 + b];
             sum += loc[b];
@@ -841,7 +836,7 @@ __global__ void __launch_bounds__(T, 1)
           const int first = __ffs(ball) - 1;
           if (tid == first) {
             int cum = incl - sum;
-  #pragma unroll
+#pragma unroll
             for (int b = 0; b < 8; ++b) {
               if (cum + loc[b] >= rank) {
                 s_sc[SC_DIGIT] = (uint32_t)(tid * 8 + b);
@@ -857,41 +852,57 @@ __global__ void __launch_bounds__(T, 1)
         rank = (int)s_sc[SC_RANK];
         __syncthreads();
       }
-      const uint32_t thr = prefix;    // stamp - base of the last victim
-      const int need_eq = rank;       // victims taken among the candidates at the threshold
-      const int n_lt = m2 - need_eq;  // candidates strictly below the threshold
-      int c_lt = 0, c_eq = 0;
-      for (int s = s0; s < s1; ++s) {
-        if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
-        const uint32_t d = (uint32_t)s_stamp[s] - base;
-        c_lt += d < thr;
-        c_eq += d == thr;
-      }
-      int tot2;
-      const int pk = block_excl_scan((c_lt << 16) | c_eq, s_wsum, &tot2);
-      int p_lt = pk >> 16, p_eq = pk & 0xffff;
-      for (int s = s0; s < s1; ++s) {
-        if (s_tok[s] < 0 || (s_sflag[s] & SF_USED)) continue;
-        const uint32_t d = (uint32_t)s_stamp[s] - base;
-        if (d < thr) {
-          s_keys[p_lt++] = ((uint64_t)d << 32) | (uint32_t)s;
-        } else if (d == thr) {
-          if (p_eq < need_eq) s_keys[n_lt + p_eq] = ((uint64_t)d << 32) | (uint32_t)s;
-          ++p_eq;
+      thr_st = (int32_t)(base + prefix);  // the last victim's stamp
+      need_eq = rank;                     // victims taken among the candidates stamped thr_st
+    }
+    // Gather: warp by warp in slot order, candidates older than the threshold to
+    // [0, n_lt), the first need_eq at it to [n_lt, m2). Keys (stamp, slot) are distinct.
+    const int n_lt = m2 - need_eq;
+    int c_lt = 0, c_eq = 0;
+    for (int b = sw0; b < sw1; b += 32) {
+      const int s = b + lane;
+      const bool cand = s < sw1 && s_tok[s] >= 0 && !(s_sflag[s] & SF_USED);
+      const int32_t st = cand ? s_stamp[s] : 0;
+      c_lt += __popc(__ballot_sync(FULL, cand && st < thr_st));
+      c_eq += __popc(__ballot_sync(FULL, cand && st == thr_st));
+    }
+    __syncthreads();  // every warp has read phase 5's counts
+    if (lane == 0) s_wsum[warp] = (c_lt << 16) | c_eq;
+    __syncthreads();
+    {
+      const int before = __reduce_add_sync(FULL, lane < warp ? s_wsum[lane] : 0);
+      int p_lt = before >> 16, p_eq = before & 0xffff;
+      for (int b = sw0; b < sw1; b += 32) {
+        const int s = b + lane;
+        const bool cand = s < sw1 && s_tok[s] >= 0 && !(s_sflag[s] & SF_USED);
+        const int32_t st = cand ? s_stamp[s] : 0;
+        const bool lt = cand && st < thr_st, eq = cand && st == thr_st;
+        const unsigned bl = __ballot_sync(FULL, lt), be = __ballot_sync(FULL, eq);
+        const uint64_t key = ((uint64_t)(uint32_t)st << 32) | (uint32_t)s;
+        if (lt) s_keys[p_lt + __popc(bl & lt_mask)] = key;
+        if (eq) {
+          const int q = p_eq + __popc(be & lt_mask);
+          if (q < need_eq) s_keys[n_lt + q] = key;
         }
+        p_lt += __popc(bl);
+        p_eq += __popc(be);
       }
     }
     __syncthreads();
-    if (m2 <= kRankSortMax) {
-      // the keys are distinct: a victim's rank is the number of smaller keys; one warp per
-      // victim, its lanes splitting the comparisons
-      const int lane = tid & 31;
-      for (int j = tid >> 5; j < m2; j += NW) {
-        const uint64_t kj = s_keys[j];
+    if (m2 <= T) {
+      // a victim's rank is the number of smaller keys: one thread per victim, reading the
+      // keys two at a time as broadcasts
+      if (tid < m2) {
+        const uint64_t kj = s_keys[tid];
+        const ulonglong2* kp = reinterpret_cast<const ulonglong2*>(s_keys);
         int rk = 0;
-        for (int u = lane; u < m2; u += 32) rk += s_keys[u] < kj;
-        rk = __reduce_add_sync(FULL, rk);
-        if (lane == 0) s_vict[take_free + rk] = (int32_t)(kj & 0xffffffffu);
+#pragma unroll 4
+        for (int u = 0; u < (m2 >> 1); ++u) {
+          const ulonglong2 kk = kp[u];
+          rk += (int)(kk.x < kj) + (int)(kk.y < kj);
+        }
+        if (m2 & 1) rk += (int)(s_keys[m2 - 1] < kj);
+        s_vict[take_free + rk] = (int32_t)(kj & 0xffffffffu);
       }
     } else {
       int n = 1;
