@@ -55,6 +55,11 @@ def _load():
         lib.oracle_resolve.restype = None
         lib.oracle_backup.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32] + [P] * 7
         lib.oracle_backup.restype = None
+        lib.oracle_invalidate_tokens.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32] + [P] * 6
+        lib.oracle_invalidate_tokens.restype = None
+        lib.oracle_invalidate_host_rows.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32, P, P, P,
+                                                    ctypes.c_int32, P, P, P]
+        lib.oracle_invalidate_host_rows.restype = None
         lib.oracle_hot_bytes_per_request.argtypes = [ctypes.c_int32] * 4
         lib.oracle_hot_bytes_per_request.restype = ctypes.c_int64
         _lib = lib
@@ -125,4 +130,28 @@ class Oracle:
         dp = self._pools(device_pools, g.device_rows)
         self.lib.oracle_backup(ctypes.byref(g), R, _p(seq_lens), _p(host_cache_locs),
                                _p(device_buffer_locs), _p(resident_pages), hp, dp, ctypes.byref(err))
+        return int(err.value)
+
+    def invalidate_tokens(self, seq_lens, offsets, tokens, device_buffer_tokens, lru_slots) -> int:
+        """Request r's tokens tokens[offsets[r]:offsets[r+1]] leave its hot set."""
+        g = self.g
+        R = seq_lens.shape[0]
+        _i32(seq_lens); _i32(offsets, (R + 1,)); _i32(tokens)
+        _i32(device_buffer_tokens, (R, g.hot_slots)); _i32(lru_slots, (R, g.hot_slots))
+        assert int(offsets[0]) == 0 and int(offsets[-1]) <= tokens.size and np.all(np.diff(offsets) >= 0)
+        err = ctypes.c_uint32(0)
+        self.lib.oracle_invalidate_tokens(ctypes.byref(g), R, _p(seq_lens), _p(offsets), _p(tokens),
+                                          _p(device_buffer_tokens), _p(lru_slots), ctypes.byref(err))
+        return int(err.value)
+
+    def invalidate_host_rows(self, seq_lens, host_cache_locs, rows, device_buffer_tokens, lru_slots) -> int:
+        """Every slot whose token's host row is in `rows` leaves its request's hot set."""
+        g = self.g
+        R = seq_lens.shape[0]
+        _i32(seq_lens); _i32(host_cache_locs, (R, g.max_context)); _i32(rows)
+        _i32(device_buffer_tokens, (R, g.hot_slots)); _i32(lru_slots, (R, g.hot_slots))
+        err = ctypes.c_uint32(0)
+        self.lib.oracle_invalidate_host_rows(ctypes.byref(g), R, _p(seq_lens), _p(host_cache_locs), _p(rows),
+                                             int(rows.size), _p(device_buffer_tokens), _p(lru_slots),
+                                             ctypes.byref(err))
         return int(err.value)

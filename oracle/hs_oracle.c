@@ -289,6 +289,74 @@ void oracle_backup(const oracle_geom* g, int32_t num_requests, const int32_t* se
   }
 }
 
+/*
+ * Invalidation of hot slots ([vLLM-impl] section 6, invalidation propagation: when a host
+ * block is handed to other content, hot entries that point at its old rows must go; rows
+ * rewritten by prefill in this step are cleared exactly). A cleared slot is free again
+ * (token -1, stamp 0, as a reset slot), so the next lookup of its token misses and copies
+ * the current host row. The clock does not move.
+ * Readings: slots are keyed by token, so the exact clear names tokens; only tokens in
+ * [0, seq_len - 1) are considered (no valid slot holds any other); requests on the fast
+ * path (seq_len <= H) are left alone, since their device rows are the tokens' own rows,
+ * which the forward pass rewrites in place; seq_len outside [0, max_context] skips the
+ * request (ERR_SEQLEN).
+ */
+static int invalidation_applies(const oracle_geom* g, int32_t S, uint32_t* err) {
+  if (S < 0 || S > g->max_context) {
+    *err |= OR_ERR_SEQLEN;
+    return 0;
+  }
+  return S > g->hot_slots;
+}
+
+static void clear_slot(int32_t* tokens, int32_t* stamps, int32_t s) {
+  tokens[s] = -1;
+  stamps[s] = 0;
+}
+
+/* The tokens clear[offsets[r] .. offsets[r+1]) of request r leave its hot set. */
+void oracle_invalidate_tokens(const oracle_geom* g, int32_t num_requests, const int32_t* seq_lens,
+                              const int32_t* offsets, const int32_t* clear,
+                              int32_t* device_buffer_tokens, int32_t* lru_slots, uint32_t* err) {
+  const int32_t H = g->hot_slots;
+  for (int32_t r = 0; r < num_requests; ++r) {
+    const int32_t S = seq_lens[r];
+    if (!invalidation_applies(g, S, err)) continue;
+    int32_t* tokens = device_buffer_tokens + (int64_t)r * H;
+    int32_t* stamps = lru_slots + (int64_t)r * H;
+    for (int32_t k = offsets[r]; k < offsets[r + 1]; ++k) {
+      const int32_t t = clear[k];
+      if (t < 0 || t >= S - 1) continue;
+      for (int32_t s = 0; s < H; ++s)
+        if (tokens[s] == t) clear_slot(tokens, stamps, s);
+    }
+  }
+}
+
+/* Every slot whose token's host row (host_cache_locs[r][token]) is one of rows[0..n)
+ * leaves the hot set, in every request. */
+void oracle_invalidate_host_rows(const oracle_geom* g, int32_t num_requests, const int32_t* seq_lens,
+                                 const int32_t* host_cache_locs, const int32_t* rows, int32_t n,
+                                 int32_t* device_buffer_tokens, int32_t* lru_slots, uint32_t* err) {
+  const int32_t H = g->hot_slots;
+  for (int32_t r = 0; r < num_requests; ++r) {
+    const int32_t S = seq_lens[r];
+    if (!invalidation_applies(g, S, err)) continue;
+    int32_t* tokens = device_buffer_tokens + (int64_t)r * H;
+    int32_t* stamps = lru_slots + (int64_t)r * H;
+    const int32_t* hcl = host_cache_locs + (int64_t)r * g->max_context;
+    for (int32_t s = 0; s < H; ++s) {
+      const int32_t t = tokens[s];
+      if (t < 0 || t >= S - 1) continue;
+      for (int32_t j = 0; j < n; ++j)
+        if (rows[j] == hcl[t]) {
+          clear_slot(tokens, stamps, s);
+          break;
+        }
+    }
+  }
+}
+
 /* Per-request GPU bytes of the hot buffer: (n_spec + 2) * top_k rows of row_bytes for
  * each layer ([vLLM-impl] 7.1 region_stride = (max_decode_query_len + 1) * top_k with
  * max_decode_query_len = 1 + n_spec; section 9 gives 2 x 2048 x 656 B x 60 ~ 155 MiB). */

@@ -34,6 +34,11 @@ MUTANTS = [
     ("backup_always_reserved", "if (row < 0) row = S <= H ? dbl[t] : dbl[H];", "if (row < 0) row = dbl[H];"),
     ("duplicates_not_rejected", "else if (first_at[t] >= 0)", "else if (first_at[t] >= 2000000000)"),
     ("misses_not_zero_filled", "else memset(dst, 0, (size_t)B);", "else (void)dst;"),
+    ("invalidate_keeps_stamp", "  tokens[s] = -1;\n  stamps[s] = 0;\n}", "  tokens[s] = -1;\n}"),
+    ("invalidate_fast_path_too", "  return S > g->hot_slots;\n}", "  return 1;\n}"),
+    ("invalidate_skips_first_token", "for (int32_t k = offsets[r]; k < offsets[r + 1]; ++k)",
+     "for (int32_t k = offsets[r] + 1; k < offsets[r + 1]; ++k)"),
+    ("invalidate_row_is_token", "if (rows[j] == hcl[t]) {", "if (rows[j] == t) {"),
 ]
 
 

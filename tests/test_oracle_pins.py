@@ -405,6 +405,10 @@ def run_all_pins() -> int:
     checks += [lambda s=s: test_brute_force_tiny(s) for s in range(2)]
     checks += [lambda h=h: test_textbook_lru_k1(h) for h in (2, 5)]
     checks += [lambda n=n: test_invariants(n) for n in ("tiny", "mixed_small")]
+    import test_oracle_invalidate as inv
+    checks += [inv.test_invalidate_golden]
+    checks += [lambda n=n: inv.test_token_and_host_row_forms_agree(n) for n in ("tiny", "mixed_small")]
+    checks += [lambda n=n: inv.test_next_resolve_refetches_cleared_tokens(n) for n in ("tiny", "dsa_small")]
     failed = 0
     for c in checks:
         try:
