@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--op", default="step", choices=["step", "invalidate_tokens", "invalidate_host_rows"],
+                    help="step: the decode step (default); invalidate_*: one hot-slot invalidation call")
     ap.add_argument("--sweep", action="store_true",
                     help="run every miss-rate sweep point (hot slots x reuse), one JSON line each")
     return ap.parse_args()
@@ -532,11 +534,112 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------------------------
+def measured_hbm_peak() -> float:
+    try:
+        return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("hbm_gbs", 6800.0))
+    except (OSError, ValueError):
+        return 6800.0
+
+
+REWRITTEN = 64  # positions per request a prefill chunk rewrote on the host
+
+
+def run_invalidate(args, ws, rank, local):
+    """One hot-slot invalidation call per timed iteration on a seeded mid-decode slot map of
+    the workload's shape: by token (each request drops the REWRITTEN positions before its
+    newest token) or by host row (the sorted host rows of the same positions). The state is
+    restored and L2 flushed before each call, outside the timed events."""
+    import torch
+    import hierarchical_sparse_attention_gb300 as hs
+    import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = W.make(args.config, args.seed + 1000 * rank, steps=1)
+    R, K, H, B, L = wl.R, wl.K, wl.H, wl.B, wl.L
+    tok0, st0, _ = wl.warm_slot_state(args.seed + 1000 * rank)
+    offs, toks = wl.rewritten_positions(REWRITTEN)
+    S = wl.seq_lens(0)
+    rows = np.unique(np.concatenate([wl.host_cache_locs[r, toks[offs[r]:offs[r + 1]]] for r in range(R)]))
+    rows = rows.astype(np.int32)
+    g_tok0, g_st0 = torch.from_numpy(tok0).to(dev), torch.from_numpy(st0).to(dev)
+    tok, st = g_tok0.clone(), g_st0.clone()
+    g_S, g_offs, g_toks = (torch.from_numpy(x).to(dev) for x in (S, offs, toks))
+    g_hcl, g_rows = torch.from_numpy(wl.host_cache_locs).to(dev), torch.from_numpy(rows).to(dev)
+    cfg = hs.make_config(R, K, H, B, L, wl.ps, wl.max_context, wl.max_pages)
+    wsp = torch.zeros(hs.hs_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    hostp = [np.zeros(16 * B, dtype=np.uint8) for _ in range(L)]
+    for p in hostp:
+        hs.hs_host_register(p)
+    devp = [torch.zeros(16 * B, dtype=torch.uint8, device=dev) for _ in range(L)]
+    h = hs.hs_create(cfg, hostp, devp, 16, 16, wsp)  # the invalidation never touches pools
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def call():
+        if args.op == "invalidate_tokens":
+            hs.hs_invalidate_tokens(h, R, g_S, g_offs, g_toks, tok, st, stream)
+        else:
+            hs.hs_invalidate_host_rows(h, R, g_S, g_hcl, g_rows, rows.size, tok, st, stream)
+
+    for _ in range(args.warmup):
+        tok.copy_(g_tok0); st.copy_(g_st0)
+        call()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local, enabled=not args.no_clocks) as clocks:
+        for i in range(args.steps):
+            tok.copy_(g_tok0); st.copy_(g_st0)
+            flush.zero_()
+            evs[i][0].record(stream)
+            call()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    ms = [e[0].elapsed_time(e[1]) for e in evs]
+    err = hs.hs_get_error(h, clear=True)
+    cleared = int((tok != g_tok0).sum().item())
+    hs.hs_destroy(h)
+    for p in hostp:
+        hs.hs_host_unregister(p)
+    mean_s = max_over_ranks(sum(ms) / len(ms) * 1e-3, ws)
+    # algorithmic bytes per call: the slot maps read, the list(s) read, cleared slots written
+    # (token + stamp, and the hint), plus the host-row lookups of held tokens in the row form
+    slots_read = int(((S > H) * H).sum()) * 4
+    held = int((tok0 >= 0).sum())
+    list_bytes = (toks.size + R + 1) * 4 if args.op == "invalidate_tokens" else rows.size * 4 + held * 4
+    alg = slots_read + list_bytes + cleared * 10
+    hbm = measured_hbm_peak()
+    line = {
+        "metric": f"{args.op.replace('invalidate_', 'hs_invalidate_')} latency", "value": 1e6 * mean_s,
+        "unit": "us", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_s,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": f"{args.config}: {R} requests x {H} hot slots, seq {int(S.max())}, "
+                               f"{REWRITTEN} rewritten positions per request"
+                               + (f" ({rows.size} sorted host rows)" if args.op != "invalidate_tokens" else ""),
+                   "l2": "flushed between timed calls (256 MiB write)", "parallelism": f"requests sharded, dp{ws}"},
+        "p50_us": 1e3 * float(np.median(ms)), "slots_cleared": cleared,
+        "roofline": {"bound": "hbm", "achieved": alg / mean_s / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": alg / mean_s / 1e9 / hbm, "traffic": None, "algorithmic_bytes_per_launch": alg,
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)",
+                     "note": "one CTA per request over a few KB of state each: launch latency, not HBM, bounds it"},
+        "gpu_launches": args.steps, "device_flags": err, "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.op != "step":
+        run_invalidate(args, ws, rank, local)
     elif args.sweep and ws == 1:
         # One process per point, as a serving process holds one pool for its lifetime:
         # tearing down and rebuilding tens of GB of pinned host memory inside one process

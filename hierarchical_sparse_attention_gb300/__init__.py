@@ -22,11 +22,13 @@ LIB_PATH = os.path.join(_HERE, "libhs.so")
 
 HS_OK, HS_ERR_INVALID_ARG, HS_ERR_INVALID_CONFIG, HS_ERR_CUDA, HS_ERR_DEVICE_FLAGGED, HS_ERR_TIMEOUT = range(6)
 HS_FLAG_TOKEN, HS_FLAG_DUP, HS_FLAG_STATE, HS_FLAG_HOSTROW, HS_FLAG_DEVROW, HS_FLAG_SEQLEN = 1, 2, 4, 8, 16, 32
+HS_FLAG_ORDER = 64
 HS_MAX_TOP_K, HS_MAX_HOT_SLOTS, HS_MAX_LAYERS = 4096, 16384, 8
 
 # Every symbol include/hs.h declares (checked against the library by the tests).
 EXPORTS = ("hs_workspace_bytes", "hs_create", "hs_resolve", "hs_backup", "hs_get_error", "hs_destroy",
-           "hs_status_str", "hs_host_register", "hs_host_unregister", "hs_resolve_noalloc")
+           "hs_status_str", "hs_host_register", "hs_host_unregister", "hs_resolve_noalloc",
+           "hs_invalidate_tokens", "hs_invalidate_host_rows")
 HS_NOALLOC_MAX_LAYERS = 8
 
 
@@ -56,6 +58,10 @@ def _load() -> ctypes.CDLL:
     lib.hs_resolve.restype = ctypes.c_int
     lib.hs_backup.argtypes = [P, i32, P, P, P, P, P]
     lib.hs_backup.restype = ctypes.c_int
+    lib.hs_invalidate_tokens.argtypes = [P, i32] + [P] * 5 + [P]
+    lib.hs_invalidate_tokens.restype = ctypes.c_int
+    lib.hs_invalidate_host_rows.argtypes = [P, i32, P, P, P, i32, P, P, P]
+    lib.hs_invalidate_host_rows.restype = ctypes.c_int
     lib.hs_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
     lib.hs_get_error.restype = ctypes.c_int
     lib.hs_destroy.argtypes = [P]
@@ -164,6 +170,20 @@ def hs_backup(h: Handle, num_requests: int, seq_lens, host_cache_locs, device_bu
               stream=None) -> None:
     _check(_lib.hs_backup(h.ptr if h else None, num_requests, _addr(seq_lens), _addr(host_cache_locs),
                           _addr(device_buffer_locs), _addr(resident_pages), _stream(stream)), "hs_backup")
+
+
+def hs_invalidate_tokens(h: Handle, num_requests: int, seq_lens, token_offsets, tokens, device_buffer_tokens,
+                         lru_slots, stream=None) -> None:
+    _check(_lib.hs_invalidate_tokens(h.ptr if h else None, num_requests, _addr(seq_lens), _addr(token_offsets),
+                                     _addr(tokens), _addr(device_buffer_tokens), _addr(lru_slots),
+                                     _stream(stream)), "hs_invalidate_tokens")
+
+
+def hs_invalidate_host_rows(h: Handle, num_requests: int, seq_lens, host_cache_locs, rows, n: int,
+                            device_buffer_tokens, lru_slots, stream=None) -> None:
+    _check(_lib.hs_invalidate_host_rows(h.ptr if h else None, num_requests, _addr(seq_lens), _addr(host_cache_locs),
+                                        _addr(rows), n, _addr(device_buffer_tokens), _addr(lru_slots),
+                                        _stream(stream)), "hs_invalidate_host_rows")
 
 
 def hs_get_error(h: Handle, clear: bool = False) -> int:

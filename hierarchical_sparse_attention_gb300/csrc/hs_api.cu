@@ -164,6 +164,30 @@ hs_status hs_backup(hs_handle* h, int32_t num_requests, const int32_t* seq_lens,
   return HS_OK;
 }
 
+hs_status hs_invalidate_tokens(hs_handle* h, int32_t num_requests, const int32_t* seq_lens,
+                               const int32_t* token_offsets, const int32_t* tokens, int32_t* device_buffer_tokens,
+                               int32_t* lru_slots, hs_stream_t stream) {
+  if (!h || num_requests < 0 || num_requests > h->cfg.max_requests) return HS_ERR_INVALID_ARG;
+  if (num_requests == 0) return HS_OK;
+  if (!seq_lens || !token_offsets || !tokens || !device_buffer_tokens || !lru_slots) return HS_ERR_INVALID_ARG;
+  hs::InvalidateArgs a{h->hint, seq_lens, token_offsets, tokens, device_buffer_tokens, lru_slots};
+  if (hs::launch_invalidate_tokens(h->g, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+    return HS_ERR_CUDA;
+  return HS_OK;
+}
+
+hs_status hs_invalidate_host_rows(hs_handle* h, int32_t num_requests, const int32_t* seq_lens,
+                                  const int32_t* host_cache_locs, const int32_t* rows, int32_t n,
+                                  int32_t* device_buffer_tokens, int32_t* lru_slots, hs_stream_t stream) {
+  if (!h || num_requests < 0 || num_requests > h->cfg.max_requests || n < 0) return HS_ERR_INVALID_ARG;
+  if (num_requests == 0 || n == 0) return HS_OK;
+  if (!seq_lens || !host_cache_locs || !rows || !device_buffer_tokens || !lru_slots) return HS_ERR_INVALID_ARG;
+  hs::InvalidateRowsArgs a{h->hint, seq_lens, host_cache_locs, rows, n, device_buffer_tokens, lru_slots};
+  if (hs::launch_invalidate_host_rows(h->g, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+    return HS_ERR_CUDA;
+  return HS_OK;
+}
+
 hs_status hs_get_error(hs_handle* h, uint32_t* flags, int clear) {
   if (!h || !flags) return HS_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;

@@ -12,6 +12,7 @@ namespace hs {
 
 constexpr int kResolveThreads = 1024;  // one CTA of 32 warps per request
 constexpr int kBackupThreads = 256;    // 8 warps, one (request, layer) row per warp
+constexpr int kInvalidateThreads = 1024;  // one CTA per request
 constexpr int kMaxLayers = HS_MAX_LAYERS;
 
 // Per-layer pool base addresses as the kernels dereference them. hs_create writes this
@@ -55,6 +56,25 @@ struct BackupArgs {
   const int32_t* resident_pages;
 };
 
+struct InvalidateArgs {
+  int16_t* hint;  // or NULL
+  const int32_t* seq_lens;
+  const int32_t* token_offsets;  // [R + 1]
+  const int32_t* tokens;
+  int32_t* device_buffer_tokens;
+  int32_t* lru_slots;
+};
+
+struct InvalidateRowsArgs {
+  int16_t* hint;  // or NULL
+  const int32_t* seq_lens;
+  const int32_t* host_cache_locs;
+  const int32_t* rows;  // ascending
+  int32_t n;
+  int32_t* device_buffer_tokens;
+  int32_t* lru_slots;
+};
+
 // Workspace layout (device memory owned by the caller).
 constexpr size_t kErrOffset = 0;     // uint32 sticky HS_FLAG_* word
 constexpr size_t kPoolsOffset = 64;  // Pools table
@@ -80,5 +100,9 @@ cudaError_t launch_resolve(const Geometry& g, const Pools* pools, const ResolveA
                            uint32_t* err_word, cudaStream_t stream);
 cudaError_t launch_backup(const Geometry& g, const Pools* pools, const BackupArgs& a, int32_t num_requests,
                           uint32_t* err_word, cudaStream_t stream);
+cudaError_t launch_invalidate_tokens(const Geometry& g, const InvalidateArgs& a, int32_t num_requests,
+                                     uint32_t* err_word, cudaStream_t stream);
+cudaError_t launch_invalidate_host_rows(const Geometry& g, const InvalidateRowsArgs& a, int32_t num_requests,
+                                        uint32_t* err_word, cudaStream_t stream);
 
 }  // namespace hs

@@ -117,6 +117,7 @@ typedef enum {
 #define HS_FLAG_HOSTROW 8u /* host row out of range: destination zero-filled */
 #define HS_FLAG_DEVROW 16u /* device row out of range: output -1, nothing written */
 #define HS_FLAG_SEQLEN 32u /* seq_len outside [0, max_context]: request skipped */
+#define HS_FLAG_ORDER 64u  /* hs_invalidate_host_rows: rows not ascending, nothing cleared */
 
 /* Limits of this build. */
 #define HS_MAX_TOP_K 4096
@@ -181,6 +182,35 @@ HS_API hs_status hs_resolve(hs_handle* h, int32_t num_requests, const int32_t* t
 HS_API hs_status hs_backup(hs_handle* h, int32_t num_requests, const int32_t* seq_lens,
                     const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
                     const int32_t* resident_pages, hs_stream_t stream);
+
+/* Hot-slot invalidation by token ("vLLM Hybrid HiSparse source implementation analysis",
+ * 6, invalidation propagation: rows rewritten on the host leave the hot set exactly).
+ * For each request r, every slot holding one of the tokens
+ * tokens[token_offsets[r] .. token_offsets[r+1]) becomes free (token -1, stamp 0) and the
+ * token's hint is dropped, so the next hs_resolve misses on it and copies its current host
+ * row. Only tokens in [0, seq_len - 1) count (no valid slot holds another). Requests with
+ * seq_len <= H are on the fast path and are left alone: their device rows are the tokens'
+ * own rows, which the forward pass rewrites in place. seq_len outside [0, max_context]
+ * skips the request (HS_FLAG_SEQLEN). The clock does not move.
+ *   seq_lens      [R]      device, read
+ *   token_offsets [R + 1]  device, read, non-decreasing (CSR row pointers; not checked)
+ *   tokens        [token_offsets[R]] device, read, any order, repeats and -1 allowed
+ * One kernel launch on `stream`; never synchronises or allocates; graph-capturable. */
+HS_API hs_status hs_invalidate_tokens(hs_handle* h, int32_t num_requests, const int32_t* seq_lens,
+                                      const int32_t* token_offsets, const int32_t* tokens,
+                                      int32_t* device_buffer_tokens, int32_t* lru_slots, hs_stream_t stream);
+
+/* Hot-slot invalidation by host row (same section: host blocks handed to other content).
+ * Every slot of every request past the fast path whose token's host row
+ * host_cache_locs[r][token] is one of rows[0 .. n) becomes free as above.
+ *   rows [n] device, read, ascending, repeats allowed. When n <= 8192 every CTA checks the
+ *   order and, if it is broken, clears nothing and sets HS_FLAG_ORDER; a longer list is
+ *   binary-searched as given (its order is not checked).
+ * One kernel launch on `stream`; same rules as hs_invalidate_tokens. */
+HS_API hs_status hs_invalidate_host_rows(hs_handle* h, int32_t num_requests, const int32_t* seq_lens,
+                                         const int32_t* host_cache_locs, const int32_t* rows, int32_t n,
+                                         int32_t* device_buffer_tokens, int32_t* lru_slots,
+                                         hs_stream_t stream);
 
 /* Read the workspace error word (synchronises the device; not for the hot path). With
  * clear != 0 the word is reset to zero. Returns HS_ERR_DEVICE_FLAGGED when any bit is set. */

@@ -433,6 +433,36 @@ class Workload:
                 tok[r, : S - 1] = np.arange(S - 1, dtype=np.int32)
         return tok, np.zeros((self.R, self.H), dtype=np.int32), np.zeros(self.R, dtype=np.int32)
 
+    def warm_slot_state(self, seed: int, fill: float = 0.8, clock: int = 50):
+        """A seeded mid-decode slot map for requests past the fast path: a `fill` share of
+        the slots hold distinct tokens below seq_len - 1 (the most recent positions first,
+        as a decode's working set), stamps in [1, clock]; clock [R] = clock. Requests that
+        fit the buffer keep the initial identity map."""
+        rng = np.random.default_rng(seed)
+        tok, st, _ = self.initial_state()
+        for r in range(self.R):
+            S = int(self.seq0[r])
+            if S <= self.H:
+                continue
+            n = min(int(fill * self.H), S - 1)
+            recent = np.arange(S - 1 - 4 * n, S - 1) if S - 1 >= 4 * n else np.arange(S - 1)
+            held = rng.choice(recent, size=n, replace=False).astype(np.int32)
+            slots = rng.permutation(self.H)[:n]
+            tok[r, slots] = held
+            st[r, slots] = rng.integers(1, clock + 1, size=n)
+        return tok, st, np.full(self.R, clock, dtype=np.int32)
+
+    def rewritten_positions(self, count: int):
+        """CSR lists of the `count` positions before the newest one, per request: the rows a
+        chunk of prefill (or a rejected speculative draft) rewrote on the host."""
+        offs, toks = [0], []
+        for r in range(self.R):
+            S = int(self.seq0[r])
+            t = np.arange(max(0, S - 1 - count), max(0, S - 1), dtype=np.int32)
+            toks.append(t)
+            offs.append(offs[-1] + t.size)
+        return np.array(offs, dtype=np.int32), np.concatenate(toks) if toks else np.zeros(0, np.int32)
+
     def initial_device_writes(self):
         """(requests, tokens, device rows) the caller writes before step 0: the fast-path
         buffer contents and the resident pages' rows (all tokens before the newest)."""
