@@ -53,6 +53,12 @@ def _load():
         P = ctypes.c_void_p
         lib.oracle_resolve.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32] + [P] * 13
         lib.oracle_resolve.restype = None
+        lib.oracle_resolve_plan.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32] + [P] * 13 + [ctypes.c_int32,
+                                                                                                P, P, P]
+        lib.oracle_resolve_plan.restype = None
+        lib.oracle_gather.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32, P, P, P, P, ctypes.c_int32,
+                                      ctypes.c_int32, P, P, P]
+        lib.oracle_gather.restype = None
         lib.oracle_backup.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32] + [P] * 7
         lib.oracle_backup.restype = None
         lib.oracle_invalidate_tokens.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32] + [P] * 6
@@ -81,6 +87,13 @@ def hot_bytes_per_request(top_k: int, n_spec: int, row_bytes: int, layers: int) 
     return int(_load().oracle_hot_bytes_per_request(top_k, n_spec, row_bytes, layers))
 
 
+class Plan:
+    """A recorded miss plan: per request `count` misses, miss j = (tokens[j], dst[j])."""
+
+    def __init__(self, tokens: np.ndarray, dst: np.ndarray, count: np.ndarray):
+        self.tokens, self.dst, self.count = tokens, dst, count
+
+
 class Oracle:
     """State-free wrapper: the caller owns every array (as with the library)."""
 
@@ -99,7 +112,10 @@ class Oracle:
 
     def resolve(self, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs,
                 device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows,
-                miss_counts, host_pools, device_pools) -> int:
+                miss_counts, host_pools, device_pools, copy_layers: Optional[int] = None,
+                plan: Optional["Plan"] = None) -> int:
+        """One decode step. With copy_layers < num_layers only the leader layers [0,
+        copy_layers) get their miss rows; with a Plan the miss plan is recorded for gather()."""
         g = self.g
         R = seq_lens.shape[0]
         _i32(top_k_tokens, (R, g.top_k)); _i32(seq_lens); _i32(host_cache_locs, (R, g.max_context))
@@ -112,10 +128,36 @@ class Oracle:
         err = ctypes.c_uint32(0)
         hp = self._pools(host_pools, g.host_rows)
         dp = self._pools(device_pools, g.device_rows)
-        self.lib.oracle_resolve(ctypes.byref(g), R, _p(top_k_tokens), _p(seq_lens), _p(host_cache_locs),
-                                _p(device_buffer_locs), _p(device_buffer_tokens), _p(lru_slots),
-                                _p(lru_clock), _p(resident_pages), _p(out_rows), _p(miss_counts),
-                                hp, dp, ctypes.byref(err))
+        args = (ctypes.byref(g), R, _p(top_k_tokens), _p(seq_lens), _p(host_cache_locs),
+                _p(device_buffer_locs), _p(device_buffer_tokens), _p(lru_slots), _p(lru_clock),
+                _p(resident_pages), _p(out_rows), _p(miss_counts), hp, dp, ctypes.byref(err))
+        if copy_layers is None and plan is None:
+            self.lib.oracle_resolve(*args)
+        else:
+            cl = g.num_layers if copy_layers is None else int(copy_layers)
+            assert 0 <= cl <= g.num_layers
+            if plan is not None:
+                _i32(plan.tokens, (R, g.top_k)); _i32(plan.dst, (R, g.top_k)); _i32(plan.count, (R,))
+            self.lib.oracle_resolve_plan(*args, cl, _p(plan.tokens) if plan else None,
+                                         _p(plan.dst) if plan else None, _p(plan.count) if plan else None)
+        return int(err.value)
+
+    def new_plan(self, R: int) -> "Plan":
+        return Plan(np.zeros((R, self.g.top_k), np.int32), np.zeros((R, self.g.top_k), np.int32),
+                    np.zeros(R, np.int32))
+
+    def gather(self, plan: "Plan", host_cache_locs, first_layer: int, num_layers: int, host_pools,
+               device_pools) -> int:
+        """Copy the plan's rows for layers [first_layer, first_layer + num_layers)."""
+        g = self.g
+        R = plan.count.shape[0]
+        _i32(host_cache_locs, (R, g.max_context))
+        assert 0 <= first_layer and first_layer + num_layers <= g.num_layers
+        err = ctypes.c_uint32(0)
+        hp = self._pools(host_pools, g.host_rows)
+        dp = self._pools(device_pools, g.device_rows)
+        self.lib.oracle_gather(ctypes.byref(g), R, _p(plan.count), _p(plan.tokens), _p(plan.dst),
+                               _p(host_cache_locs), first_layer, num_layers, hp, dp, ctypes.byref(err))
         return int(err.value)
 
     def backup(self, seq_lens, host_cache_locs, device_buffer_locs, resident_pages, host_pools,

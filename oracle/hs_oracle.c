@@ -112,12 +112,13 @@ static int64_t resident_row(const oracle_geom* g, const int32_t* resident_pages,
  * host_pools / device_pools: num_layers pointers to [rows, row_bytes] byte pools.
  * Error bits are OR-ed into *err.
  */
-void oracle_resolve(const oracle_geom* g, int32_t num_requests, const int32_t* top_k_tokens,
-                    const int32_t* seq_lens, const int32_t* host_cache_locs,
-                    const int32_t* device_buffer_locs, int32_t* device_buffer_tokens,
-                    int32_t* lru_slots, int32_t* lru_clock, const int32_t* resident_pages,
-                    int32_t* out_rows, int32_t* miss_counts, uint8_t* const* host_pools,
-                    uint8_t* const* device_pools, uint32_t* err) {
+void oracle_resolve_plan(const oracle_geom* g, int32_t num_requests, const int32_t* top_k_tokens,
+                         const int32_t* seq_lens, const int32_t* host_cache_locs,
+                         const int32_t* device_buffer_locs, int32_t* device_buffer_tokens,
+                         int32_t* lru_slots, int32_t* lru_clock, const int32_t* resident_pages,
+                         int32_t* out_rows, int32_t* miss_counts, uint8_t* const* host_pools,
+                         uint8_t* const* device_pools, uint32_t* err, int32_t copy_layers,
+                         int32_t* plan_tokens, int32_t* plan_dst, int32_t* plan_count) {
   const int32_t K = g->top_k, H = g->hot_slots, B = g->row_bytes;
   int32_t* cls = (int32_t*)malloc(sizeof(int32_t) * (size_t)K);
   int32_t* first_at = (int32_t*)malloc(sizeof(int32_t) * (size_t)(g->max_context + 1));
@@ -139,6 +140,7 @@ void oracle_resolve(const oracle_geom* g, int32_t num_requests, const int32_t* t
 
     for (int32_t i = 0; i < K; ++i) out[i] = -1;
     if (miss_counts) miss_counts[r] = 0;
+    if (plan_count) plan_count[r] = 0;
     if (S < 0 || S > g->max_context) {
       *err |= OR_ERR_SEQLEN;
       continue;
@@ -222,6 +224,7 @@ void oracle_resolve(const oracle_geom* g, int32_t num_requests, const int32_t* t
     for (int32_t s = 0; s < H; ++s)
       if (tokens[s] >= 0) holders[tokens[s]] = 0, lowest_slot[tokens[s]] = -1;
     if (miss_counts) miss_counts[r] = m;
+    if (plan_count) plan_count[r] = m;
 
     /* Victims: among slots not hit now, free slots first (lowest index first), then the
      * oldest stamps, ties to the lowest slot ([Tair-HSA] 2.4.3: evict only when the buffer
@@ -247,11 +250,15 @@ void oracle_resolve(const oracle_geom* g, int32_t num_requests, const int32_t* t
       stamps[v] = c;
       int32_t d = checked_row(dbl[v], g->device_rows, err);
       out[i] = d;
+      if (plan_tokens) {  /* the miss plan, in miss order: token and destination row */
+        plan_tokens[(int64_t)r * K + j] = t;
+        plan_dst[(int64_t)r * K + j] = d;
+      }
       if (d < 0) continue;
       int64_t h = hcl[t];
       int host_ok = h >= 0 && h < g->host_rows;
       if (!host_ok) *err |= OR_ERR_HOSTROW;
-      for (int32_t l = 0; l < g->num_layers; ++l) {
+      for (int32_t l = 0; l < copy_layers; ++l) {
         uint8_t* dst = device_pools[l] + (size_t)d * (size_t)B;
         if (host_ok) memcpy(dst, host_pools[l] + (size_t)h * (size_t)B, (size_t)B);
         else memset(dst, 0, (size_t)B);
@@ -259,6 +266,53 @@ void oracle_resolve(const oracle_geom* g, int32_t num_requests, const int32_t* t
     }
   }
   free(cls); free(first_at); free(lowest_slot); free(holders); free(used); free(misses); free(cand);
+}
+
+/* The whole step: every layer of the group gets its miss rows; no plan is kept. */
+void oracle_resolve(const oracle_geom* g, int32_t num_requests, const int32_t* top_k_tokens,
+                    const int32_t* seq_lens, const int32_t* host_cache_locs,
+                    const int32_t* device_buffer_locs, int32_t* device_buffer_tokens,
+                    int32_t* lru_slots, int32_t* lru_clock, const int32_t* resident_pages,
+                    int32_t* out_rows, int32_t* miss_counts, uint8_t* const* host_pools,
+                    uint8_t* const* device_pools, uint32_t* err) {
+  oracle_resolve_plan(g, num_requests, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs,
+                      device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows, miss_counts,
+                      host_pools, device_pools, err, g->num_layers, NULL, NULL, NULL);
+}
+
+/*
+ * Follower gather ([vLLM-impl] 7.4: layers that share the indexer see the same indices and
+ * get the same slot plan; each follower copies its own bytes following the leader's plan,
+ * with no LRU work; [vLLM-arch] "Performance invariants": compatible layers share one miss
+ * plan). The plan is what oracle_resolve_plan recorded: per request, plan_count[r] misses,
+ * miss j being token plan_tokens[r][j] bound for device row plan_dst[r][j] (-1: none). For
+ * each layer in [first_layer, first_layer + num_layers) the token's host row is copied to
+ * that device row, or zeros when the host row is outside the pool (ERR_HOSTROW).
+ */
+void oracle_gather(const oracle_geom* g, int32_t num_requests, const int32_t* plan_count,
+                   const int32_t* plan_tokens, const int32_t* plan_dst, const int32_t* host_cache_locs,
+                   int32_t first_layer, int32_t num_layers, uint8_t* const* host_pools,
+                   uint8_t* const* device_pools, uint32_t* err) {
+  const int32_t K = g->top_k, B = g->row_bytes;
+  for (int32_t r = 0; r < num_requests; ++r) {
+    const int32_t* hcl = host_cache_locs + (int64_t)r * g->max_context;
+    for (int32_t j = 0; j < plan_count[r]; ++j) {
+      const int32_t t = plan_tokens[(int64_t)r * K + j];
+      const int32_t d = plan_dst[(int64_t)r * K + j];
+      if (d < 0) continue;
+      const int64_t src_row = hcl[t];
+      const int src_ok = src_row >= 0 && src_row < g->host_rows;
+      if (!src_ok) *err |= OR_ERR_HOSTROW;
+      for (int32_t l = first_layer; l < first_layer + num_layers; ++l) {
+        uint8_t* to = device_pools[l] + (size_t)d * (size_t)B;
+        if (!src_ok) {
+          memset(to, 0, (size_t)B);
+          continue;
+        }
+        memcpy(to, host_pools[l] + (size_t)src_row * (size_t)B, (size_t)B);
+      }
+    }
+  }
 }
 
 /*

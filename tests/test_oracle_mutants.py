@@ -39,6 +39,11 @@ MUTANTS = [
     ("invalidate_skips_first_token", "for (int32_t k = offsets[r]; k < offsets[r + 1]; ++k)",
      "for (int32_t k = offsets[r] + 1; k < offsets[r + 1]; ++k)"),
     ("invalidate_row_is_token", "if (rows[j] == hcl[t]) {", "if (rows[j] == t) {"),
+    ("gather_drops_last_layer", "for (int32_t l = first_layer; l < first_layer + num_layers; ++l) {",
+     "for (int32_t l = first_layer; l < first_layer + num_layers - 1; ++l) {"),
+    ("plan_drops_first_miss", "plan_dst[(int64_t)r * K + j] = d;", "plan_dst[(int64_t)r * K + j] = j == 0 ? -1 : d;"),
+    ("leader_copies_every_layer", "for (int32_t l = 0; l < copy_layers; ++l) {",
+     "for (int32_t l = 0; l < g->num_layers; ++l) {"),
 ]
 
 

@@ -409,6 +409,10 @@ def run_all_pins() -> int:
     checks += [inv.test_invalidate_golden]
     checks += [lambda n=n: inv.test_token_and_host_row_forms_agree(n) for n in ("tiny", "mixed_small")]
     checks += [lambda n=n: inv.test_next_resolve_refetches_cleared_tokens(n) for n in ("tiny", "dsa_small")]
+    import test_oracle_split as sp
+    checks += [lambda c=c, gs=gs: sp.test_split_equals_fused(c, gs) for c, gs in sp.SPLITS[:2]]
+    checks += [lambda n=n: sp.test_plan_is_the_steps_misses(n) for n in ("dsa_small", "indexshare_small")]
+    checks += [sp.test_leader_only_leaves_followers]
     failed = 0
     for c in checks:
         try:
