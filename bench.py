@@ -43,8 +43,9 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "invalidate_tokens", "invalidate_host_rows"],
-                    help="step: the decode step (default); invalidate_*: one hot-slot invalidation call")
+    ap.add_argument("--op", default="step", choices=["step", "invalidate_tokens", "invalidate_host_rows", "split"],
+                    help="step: the decode step (default); invalidate_*: one hot-slot invalidation call; "
+                         "split: leader resolve + follower gathers on a copy stream vs the fused step")
     ap.add_argument("--sweep", action="store_true",
                     help="run every miss-rate sweep point (hot slots x reuse), one JSON line each")
     return ap.parse_args()
@@ -633,11 +634,151 @@ def run_invalidate(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_split(args, ws, rank, local):
+    """A layer group's decode step two ways over the same steps: fused (hs_resolve copies
+    every layer) and split (hs_resolve_layers copies layer 0, then hs_gather copies each
+    follower layer on a copy stream behind its own event). Per step it times, from the
+    step's start: layer 0 ready, each follower ready, all layers ready."""
+    import torch
+    import hierarchical_sparse_attention_gb300 as hs
+    import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    W_, K_ = args.warmup, args.steps
+    total = W_ + K_
+    wl = W.make(args.config, args.seed + 1000 * rank, steps=total)
+    R, K, H, B, L = wl.R, wl.K, wl.H, wl.B, wl.L
+    assert L >= 2, "the split needs at least two layers"
+    pools = [alloc_host(wl.host_rows * B) for _ in range(L)]
+    for l, (arr, reg) in enumerate(pools):
+        wl.fill_host_pool(l, arr)
+        touch_host_pool_from_gpu(hs.hs_host_register(arr) if reg else host_device_ptr(arr), arr.nbytes)
+    host = [arr for arr, _ in pools]
+    dpool = []
+    for l in range(L):
+        init = np.full(wl.device_rows * B, 0xA5, dtype=np.uint8)
+        rq, tk0, rows0 = wl.initial_device_writes()
+        wl.scatter_rows(l, rq, tk0, rows0, init)
+        dpool.append(torch.from_numpy(init).to(dev))
+    topk_all = torch.from_numpy(np.stack([wl.top_k_tokens(s) for s in range(total)])).to(dev)
+    seq_all = torch.from_numpy(np.stack([wl.seq_lens(s) for s in range(total)])).to(dev)
+    newest = [newest_rows(wl, s) for s in range(total)]
+    newest_idx = torch.from_numpy(np.stack([n[0] for n in newest])).to(dev)
+    newest_dat = [torch.from_numpy(np.stack([n[1][l] for n in newest])).to(dev) for l in range(L)]
+    hcl = torch.from_numpy(wl.host_cache_locs).to(dev)
+    dbl = torch.from_numpy(wl.device_buffer_locs).to(dev)
+    rp = None if wl.resident_pages is None else torch.from_numpy(wl.resident_pages).to(dev)
+    tok0, st0, clk0 = wl.initial_state()
+    tk_buf = torch.empty((R, K), dtype=torch.int32, device=dev)
+    sl_buf = torch.empty((R,), dtype=torch.int32, device=dev)
+    out = torch.empty((R, K), dtype=torch.int32, device=dev)
+    miss = torch.empty((R,), dtype=torch.int32, device=dev)
+    cfg = hs.make_config(R, K, H, B, L, wl.ps, wl.max_context, wl.max_pages)
+    wsps = {v: torch.zeros(hs.hs_workspace_bytes(cfg), dtype=torch.uint8, device=dev) for v in ("fused", "split", "split0")}
+    handles = {v: hs.hs_create(cfg, host, dpool, wl.host_rows, wl.device_rows, wsps[v]) for v in wsps}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def forward_stand_in(s):
+        for l in range(L):
+            dpool[l].view(-1, B).index_copy_(0, newest_idx[s], newest_dat[l][s])
+        tk_buf.copy_(topk_all[s])
+        sl_buf.copy_(seq_all[s])
+
+    # two copies of the slot state, one per variant; both variants see the same inputs, so
+    # they make the same decisions and write the same rows
+    states = {v: tuple(torch.from_numpy(x).to(dev) for x in (tok0, st0, clk0)) for v in ("fused", "split", "split0")}
+
+    def one_step(s, variant, evs):
+        tok, st, clk = states[variant]
+        h = handles[variant]  # each variant keeps its own hints and plan
+        forward_stand_in(s)
+        flush.zero_()
+        if evs is not None:
+            evs[0].record(stream)
+        if variant in ("split", "split0"):
+            if variant == "split":
+                hs.hs_resolve_layers(h, R, tk_buf, sl_buf, hcl, dbl, tok, st, clk, rp, out, miss, 1, stream)
+            else:  # the resolve copies nothing; layer 0 is gathered right behind it
+                hs.hs_resolve_layers(h, R, tk_buf, sl_buf, hcl, dbl, tok, st, clk, rp, out, miss, 0, stream)
+                hs.hs_gather(h, R, hcl, 0, 1, stream)
+            if evs is not None:
+                evs[1].record(stream)  # layer 0 ready
+            lead = torch.cuda.Event()
+            lead.record(stream)
+            copy.wait_event(lead)
+            for l in range(1, L):
+                hs.hs_gather(h, R, hcl, l, 1, copy)
+                if evs is not None:
+                    evs[1 + l].record(copy)  # layer l ready
+            done = torch.cuda.Event()
+            done.record(copy)
+            stream.wait_event(done)
+        else:
+            hs.hs_resolve(h, R, tk_buf, sl_buf, hcl, dbl, tok, st, clk, rp, out, miss, stream)
+            if evs is not None:
+                for l in range(L):
+                    evs[1 + l].record(stream)  # every layer ready at once
+        hs.hs_backup(h, R, sl_buf, hcl, dbl, rp, stream)
+
+    # steps interleave the variants (fused, then split, on the same step's inputs), so both
+    # meet the host pool in the same state
+    for s in range(W_):
+        for v in ("fused", "split", "split0"):
+            one_step(s, v, None)
+    torch.cuda.synchronize()
+    evs = {v: [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(K_)]
+           for v in ("fused", "split", "split0")}
+    barrier(ws)
+    torch.cuda.synchronize()
+    for i in range(K_):
+        for v in ("fused", "split", "split0"):
+            one_step(W_ + i, v, evs[v][i])
+    torch.cuda.synchronize()
+    barrier(ws)
+    res = {v: np.array([[e[0].elapsed_time(e[1 + l]) * 1e3 for l in range(L)] for e in evs[v]]) for v in evs}
+    err = 0
+    for h in handles.values():
+        err |= hs.hs_get_error(h, clear=True)
+        hs.hs_destroy(h)
+    for arr, reg in pools:
+        if reg:
+            hs.hs_host_unregister(arr)
+    f, sp, s0 = res["fused"], res["split"], res["split0"]
+    line = {
+        "metric": "time to first layer ready (leader resolve + follower gathers)", "value": float(sp[:, 0].mean()),
+        "unit": "us", "n_gpus": ws, "steps": K_, "warmup": W_, "ms_per_step": float(sp[:, -1].mean()) / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {R} requests, top_k {K}, {H} hot slots, {B}-byte rows, {L} layers",
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "split": "hs_resolve_layers(copy_layers=1) then hs_gather(l, 1) for l = 1..L-1 on a copy stream"},
+        "split_layer_ready_us_mean": [float(x) for x in sp.mean(0)],
+        "split_layer_ready_us_p50": [float(x) for x in np.median(sp, 0)],
+        "fused_all_layers_ready_us_p50": float(np.median(f[:, -1])),
+        "fused_all_layers_ready_us_mean": float(f[:, -1].mean()),
+        "split_all_layers_ready_us_mean": float(sp.max(1).mean()),
+        "first_layer_ready_speedup": float(f[:, -1].mean() / sp[:, 0].mean()),
+        "split0_layer_ready_us_p50": [float(x) for x in np.median(s0, 0)],
+        "split0": "hs_resolve_layers(copy_layers=0), hs_gather(0, 1) on the same stream, followers on the copy stream",
+        "misses_per_step": float(miss.sum().item()),
+        "gpu_launches": K_ * (1 + (L - 1) + 1), "device_flags": err,
+        "host_pool": "huge pages, hs_host_register" if pools[0][1] else "cudaHostAlloc",
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.op == "split":
+        if args.config == "dsa":
+            args.config = "indexshare"  # the split needs a layer group
+        run_split(args, ws, rank, local)
     elif args.op != "step":
         run_invalidate(args, ws, rank, local)
     elif args.sweep and ws == 1:

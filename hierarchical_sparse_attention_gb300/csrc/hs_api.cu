@@ -12,6 +12,9 @@ struct hs_handle {
   const hs::Pools* pools;  // pools table inside the caller's workspace
   uint32_t* err_word;      // error word inside the caller's workspace
   int16_t* hint;           // token -> slot hint table inside the caller's workspace
+  int32_t* plan_tok;       // follower plan inside the caller's workspace: tokens [R, K],
+  int32_t* plan_dst;       //   device rows [R, K],
+  int32_t* plan_cnt;       //   counts [R]
   int device;
 };
 
@@ -42,7 +45,9 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 extern "C" {
 
 size_t hs_workspace_bytes(const hs_config* cfg) {
-  return config_ok(cfg) ? hs::kWorkspaceBytes + hs::hint_bytes(cfg->max_requests, cfg->max_context) : 0;
+  return config_ok(cfg) ? hs::kWorkspaceBytes + hs::hint_bytes(cfg->max_requests, cfg->max_context) +
+                              hs::plan_bytes(cfg->max_requests, cfg->top_k)
+                        : 0;
 }
 
 hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* device_pools,
@@ -118,6 +123,9 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   if (cudaMemset(ws + hs::kWorkspaceBytes, 0xFF, hs::hint_bytes(cfg->max_requests, cfg->max_context)) !=
       cudaSuccess)
     return HS_ERR_CUDA;  // every hint starts at -1 (no slot)
+  uint8_t* plan = ws + hs::kWorkspaceBytes + hs::hint_bytes(cfg->max_requests, cfg->max_context);
+  if (cudaMemset(plan, 0, hs::plan_bytes(cfg->max_requests, cfg->top_k)) != cudaSuccess)
+    return HS_ERR_CUDA;  // no plan yet: a gather before the first resolve copies nothing
   if (cudaMemcpy(ws + hs::kPoolsOffset, &pools, sizeof(pools), cudaMemcpyHostToDevice) != cudaSuccess)
     return HS_ERR_CUDA;
 
@@ -128,8 +136,32 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   h->pools = reinterpret_cast<const hs::Pools*>(ws + hs::kPoolsOffset);
   h->err_word = reinterpret_cast<uint32_t*>(ws + hs::kErrOffset);
   h->hint = reinterpret_cast<int16_t*>(ws + hs::kWorkspaceBytes);
+  const size_t RK = (size_t)cfg->max_requests * (size_t)cfg->top_k;
+  h->plan_tok = reinterpret_cast<int32_t*>(plan);
+  h->plan_dst = h->plan_tok + RK;
+  h->plan_cnt = h->plan_dst + RK;
   h->device = dev;
   *out = h;
+  return HS_OK;
+}
+
+hs_status hs_resolve_layers(hs_handle* h, int32_t num_requests, const int32_t* top_k_tokens,
+                            const int32_t* seq_lens, const int32_t* host_cache_locs,
+                            const int32_t* device_buffer_locs, int32_t* device_buffer_tokens, int32_t* lru_slots,
+                            int32_t* lru_clock, const int32_t* resident_pages, int32_t* out_rows,
+                            int32_t* miss_counts, int32_t copy_layers, hs_stream_t stream) {
+  if (!h || num_requests < 0 || num_requests > h->cfg.max_requests) return HS_ERR_INVALID_ARG;
+  if (copy_layers < 0 || copy_layers > h->cfg.num_layers) return HS_ERR_INVALID_ARG;
+  if (num_requests == 0) return HS_OK;
+  if (!top_k_tokens || !seq_lens || !host_cache_locs || !device_buffer_locs || !device_buffer_tokens ||
+      !lru_slots || !lru_clock || !out_rows)
+    return HS_ERR_INVALID_ARG;
+  if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
+  hs::ResolveArgs a{h->hint,   top_k_tokens, seq_lens,   host_cache_locs, device_buffer_locs, device_buffer_tokens,
+                    lru_slots, lru_clock,    resident_pages, out_rows,   miss_counts,        copy_layers,
+                    h->plan_tok, h->plan_dst, h->plan_cnt};
+  if (hs::launch_resolve(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+    return HS_ERR_CUDA;
   return HS_OK;
 }
 
@@ -138,15 +170,20 @@ hs_status hs_resolve(hs_handle* h, int32_t num_requests, const int32_t* top_k_to
                      const int32_t* device_buffer_locs, int32_t* device_buffer_tokens, int32_t* lru_slots,
                      int32_t* lru_clock, const int32_t* resident_pages, int32_t* out_rows,
                      int32_t* miss_counts, hs_stream_t stream) {
+  if (!h) return HS_ERR_INVALID_ARG;
+  return hs_resolve_layers(h, num_requests, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs,
+                           device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows, miss_counts,
+                           h->cfg.num_layers, stream);
+}
+
+hs_status hs_gather(hs_handle* h, int32_t num_requests, const int32_t* host_cache_locs, int32_t first_layer,
+                    int32_t num_layers, hs_stream_t stream) {
   if (!h || num_requests < 0 || num_requests > h->cfg.max_requests) return HS_ERR_INVALID_ARG;
-  if (num_requests == 0) return HS_OK;
-  if (!top_k_tokens || !seq_lens || !host_cache_locs || !device_buffer_locs || !device_buffer_tokens ||
-      !lru_slots || !lru_clock || !out_rows)
-    return HS_ERR_INVALID_ARG;
-  if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
-  hs::ResolveArgs a{h->hint, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs, device_buffer_tokens,
-                    lru_slots, lru_clock, resident_pages, out_rows, miss_counts};
-  if (hs::launch_resolve(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+  if (first_layer < 0 || num_layers < 0 || first_layer + num_layers > h->cfg.num_layers) return HS_ERR_INVALID_ARG;
+  if (num_requests == 0 || num_layers == 0) return HS_OK;
+  if (!host_cache_locs) return HS_ERR_INVALID_ARG;
+  hs::GatherArgs a{host_cache_locs, h->plan_tok, h->plan_dst, h->plan_cnt, first_layer, num_layers};
+  if (hs::launch_gather(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
     return HS_ERR_CUDA;
   return HS_OK;
 }

@@ -13,6 +13,8 @@ namespace hs {
 constexpr int kResolveThreads = 1024;  // one CTA of 32 warps per request
 constexpr int kBackupThreads = 256;    // 8 warps, one (request, layer) row per warp
 constexpr int kInvalidateThreads = 1024;  // one CTA per request
+constexpr int kGatherThreads = 256;        // one CTA per (request, run of kGatherMisses misses)
+constexpr int kGatherMisses = 32;
 constexpr int kMaxLayers = HS_MAX_LAYERS;
 
 // Per-layer pool base addresses as the kernels dereference them. hs_create writes this
@@ -47,6 +49,18 @@ struct ResolveArgs {
   const int32_t* resident_pages;
   int32_t* out_rows;
   int32_t* miss_counts;
+  int32_t copy_layers;  // layers [0, copy_layers) get their miss rows in this call
+  int32_t* plan_tok;    // [R, K] miss tokens in miss order (the follower plan), or NULL
+  int32_t* plan_dst;    // [R, K] their device rows (-1: none)
+  int32_t* plan_cnt;    // [R] misses per request
+};
+
+struct GatherArgs {
+  const int32_t* host_cache_locs;
+  const int32_t* plan_tok;
+  const int32_t* plan_dst;
+  const int32_t* plan_cnt;
+  int32_t first_layer, num_layers;
 };
 
 struct BackupArgs {
@@ -90,6 +104,12 @@ inline size_t hint_bytes(int64_t max_requests, int64_t max_context) {
   return (size_t)(((max_requests * max_context * 2) + 255) & ~(int64_t)255);
 }
 
+// After the hints: the follower plan the last resolve recorded, tokens [R, K], device rows
+// [R, K] and counts [R] (int32 each).
+inline size_t plan_bytes(int64_t max_requests, int64_t top_k) {
+  return (size_t)(((max_requests * top_k * 8 + max_requests * 4) + 255) & ~(int64_t)255);
+}
+
 // Dynamic shared memory of one resolve-kernel CTA for geometry g.
 size_t resolve_smem_bytes(const Geometry& g);
 // Choose the copy CTAs per request (sets g.copy_ctas / g.copy_cap from the device's shared
@@ -99,6 +119,8 @@ cudaError_t resolve_prepare(Geometry& g, int32_t max_requests);
 cudaError_t launch_resolve(const Geometry& g, const Pools* pools, const ResolveArgs& a, int32_t num_requests,
                            uint32_t* err_word, cudaStream_t stream);
 cudaError_t launch_backup(const Geometry& g, const Pools* pools, const BackupArgs& a, int32_t num_requests,
+                          uint32_t* err_word, cudaStream_t stream);
+cudaError_t launch_gather(const Geometry& g, const Pools* pools, const GatherArgs& a, int32_t num_requests,
                           uint32_t* err_word, cudaStream_t stream);
 cudaError_t launch_invalidate_tokens(const Geometry& g, const InvalidateArgs& a, int32_t num_requests,
                                      uint32_t* err_word, cudaStream_t stream);

@@ -255,13 +255,14 @@ __device__ void bitonic_sort(uint64_t* keys, int n) {
 // Miss rows are read once: stream them past the caches.
 __device__ __forceinline__ uint4 load_host16(const uint4* p) { return __ldcs(p); }
 
-// Phase 9 of the resolve CTA: copy every planned miss row of every layer straight from
+// Phase 9 of the resolve CTA: copy every planned miss row of layers [0, L) straight from
 // host memory to its victim's device row (psrc < 0: zero-fill; pdst < 0: nothing to do,
 // e.g. a row a copy CTA moves).
-__device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc, const int32_t* pdst, int m) {
+__device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc, const int32_t* pdst, int m,
+                          int L) {
   if (g.vec == 16) {
     const int per_row = g.B >> 4;
-    const int per_miss = per_row * g.L;
+    const int per_miss = per_row * L;
     const int total = m * per_miss;
     for (int base = threadIdx.x; base < total; base += T * kCopyUnroll) {
       uint4 v[kCopyUnroll];
@@ -290,7 +291,7 @@ __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc
     }
   } else if (g.vec == 4) {
     const int per_row = g.B >> 2;
-    const int per_miss = per_row * g.L;
+    const int per_miss = per_row * L;
     const int total = m * per_miss;
     for (int c = threadIdx.x; c < total; c += T) {
       const int j = c / per_miss, rem = c - j * per_miss, l = rem / per_row, q = rem - l * per_row;
@@ -300,7 +301,7 @@ __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc
       reinterpret_cast<uint32_t*>(p.dev[l] + (size_t)d * g.B)[q] = v;
     }
   } else {
-    const int per_miss = g.B * g.L;
+    const int per_miss = g.B * L;
     const int total = m * per_miss;
     for (int c = threadIdx.x; c < total; c += T) {
       const int j = c / per_miss, rem = c - j * per_miss, l = rem / g.B, q = rem - l * g.B;
@@ -339,12 +340,12 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
   const int e0 = (q - 1) * per;
   const int ne = max(0, min(g.K, e0 + per) - e0);
   const int32_t S = a.seq_lens[r];
-  const bool predict = a.hint != nullptr && S > g.H && S <= g.max_context;
+  const bool predict = a.hint != nullptr && a.copy_layers > 0 && S > g.H && S <= g.max_context;
   int16_t* hint_row = a.hint ? a.hint + (size_t)r * g.max_context : nullptr;
   const int32_t* hcl_row = a.host_cache_locs + (size_t)r * g.max_context;
   const int32_t* tk_g = a.top_k_tokens + (size_t)r * g.K + e0;
   const int per_row = g.B >> 4;
-  const int per_miss = per_row * g.L;
+  const int per_miss = per_row * a.copy_layers;  // the leader layers this call copies
   uint32_t flags = 0;
   int staged = 0;
 
@@ -531,6 +532,7 @@ __global__ void __launch_bounds__(T, 1)
     for (int i = tid; i < K; i += T) out_g[i] = -1;
     if (tid == 0) {
       if (a.miss_counts) a.miss_counts[r] = 0;
+      if (a.plan_cnt) a.plan_cnt[r] = 0;
       atomicOr(err_word, HS_FLAG_SEQLEN);
     }
     return;
@@ -608,6 +610,7 @@ __global__ void __launch_bounds__(T, 1)
     if (tid == 0) {
       if (S >= 1) tok_g[S - 1] = S - 1;
       if (a.miss_counts) a.miss_counts[r] = 0;
+      if (a.plan_cnt) a.plan_cnt[r] = 0;
     }
     if (hint_row)  // slot t holds token t: the hints are exact when the sequence outgrows the buffer
       for (int t = tid; t < S; t += T) hint_row[t] = (int16_t)t;
@@ -934,6 +937,10 @@ __global__ void __launch_bounds__(T, 1)
       flags |= HS_FLAG_STATE;  // unreachable by construction; never index with it
     }
     s_out[i] = d;
+    if (a.plan_tok) {  // the miss plan the follower layers replay: token and destination row
+      a.plan_tok[(size_t)r * K + j] = s_tk[i];
+      a.plan_dst[(size_t)r * K + j] = d;
+    }
     if (C > 0) {  // the copy CTA owning entry i moves this row
       st_remote(smem + cl.res + 4 * (size_t)(i % per), 1 + i / per, d);
       s_pdst[j] = -1;
@@ -964,10 +971,11 @@ __global__ void __launch_bounds__(T, 1)
   if (tid == 0) {
     a.lru_clock[r] = clock;
     if (a.miss_counts) a.miss_counts[r] = m;
+    if (a.plan_cnt) a.plan_cnt[r] = m;
   }
 
-  // ---- phase 9: misses no copy CTA took, all layers, straight from host memory
-  if (s_sc[SC_DIRECT]) copy_rows(g, s_pools, s_psrc, s_pdst, m);
+  // ---- phase 9: misses no copy CTA took, the leader layers, straight from host memory
+  if (s_sc[SC_DIRECT]) copy_rows(g, s_pools, s_psrc, s_pdst, m, a.copy_layers);
   flush_flags(flags, err_word);
   if (C > 0) cluster_wait();  // phase B complete; the copy CTAs finish on their own
 }

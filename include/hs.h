@@ -153,7 +153,9 @@ typedef struct hs_handle hs_handle;
  * per request). The kernels keep the hints current and use them only to start a miss's
  * host transfer before the exact slot probe finishes; every result comes from the probe,
  * so hints left stale by changes the caller makes to the state arrays cost time, never
- * correctness. The caller keeps the workspace for the handle's lifetime and does not
+ * correctness. After the hints comes the follower plan of the last resolve: miss tokens
+ * and device rows, max_requests x top_k int32 each, and max_requests counts (hs_gather
+ * replays it). The caller keeps the workspace for the handle's lifetime and does not
  * write to it. */
 HS_API size_t hs_workspace_bytes(const hs_config* cfg);
 
@@ -174,6 +176,30 @@ HS_API hs_status hs_resolve(hs_handle* h, int32_t num_requests, const int32_t* t
                      const int32_t* device_buffer_locs, int32_t* device_buffer_tokens,
                      int32_t* lru_slots, int32_t* lru_clock, const int32_t* resident_pages,
                      int32_t* out_rows, int32_t* miss_counts, hs_stream_t stream);
+
+/* hs_resolve for a layer group split into a leader and followers ("vLLM Hybrid HiSparse
+ * source implementation analysis", 7.4: layers that share the indexer share the slot plan
+ * and copy only their own bytes). The step is resolved exactly as by hs_resolve, but miss
+ * rows are copied only for layers [0, copy_layers) (0 <= copy_layers <= num_layers), and
+ * the miss plan -- per request, the miss tokens and their device rows in miss order -- is
+ * kept in the workspace for hs_gather. hs_resolve is this call with copy_layers =
+ * num_layers (it records the plan too). Same rules as hs_resolve. */
+HS_API hs_status hs_resolve_layers(hs_handle* h, int32_t num_requests, const int32_t* top_k_tokens,
+                                   const int32_t* seq_lens, const int32_t* host_cache_locs,
+                                   const int32_t* device_buffer_locs, int32_t* device_buffer_tokens,
+                                   int32_t* lru_slots, int32_t* lru_clock, const int32_t* resident_pages,
+                                   int32_t* out_rows, int32_t* miss_counts, int32_t copy_layers,
+                                   hs_stream_t stream);
+
+/* Follower gather: copy the last resolve's miss rows for layers [first_layer, first_layer +
+ * num_layers) -- host_pool[l][host_cache_locs[r][token]] to device_pool[l][row] for every
+ * planned miss, zeros (HS_FLAG_HOSTROW) when the host row is out of range -- with no LRU
+ * work. host_cache_locs [R, max_context] device, read (the resolve's). It must run after
+ * that resolve (same stream, or an event) and before the next one; calls for different
+ * layers may run on other streams concurrently. One kernel launch; no allocation, no
+ * synchronisation; graph-capturable. num_layers == 0 is a no-op. */
+HS_API hs_status hs_gather(hs_handle* h, int32_t num_requests, const int32_t* host_cache_locs,
+                           int32_t first_layer, int32_t num_layers, hs_stream_t stream);
 
 /* Eager backup ("Per decode step workflow", step 5): for every request with seq_len >= 1
  * and every layer, copy the newest token's row -- its resident row, else slot seq_len-1
