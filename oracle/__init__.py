@@ -56,6 +56,10 @@ def _load():
         lib.oracle_resolve_plan.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32] + [P] * 13 + [ctypes.c_int32,
                                                                                                 P, P, P]
         lib.oracle_resolve_plan.restype = None
+        lib.oracle_resolve_spec.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32, ctypes.c_int32] + [P] * 13
+        lib.oracle_resolve_spec.restype = None
+        lib.oracle_backup_spec.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32, ctypes.c_int32] + [P] * 8
+        lib.oracle_backup_spec.restype = None
         lib.oracle_gather.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32, P, P, P, P, ctypes.c_int32,
                                       ctypes.c_int32, P, P, P]
         lib.oracle_gather.restype = None
@@ -196,4 +200,45 @@ class Oracle:
         self.lib.oracle_invalidate_host_rows(ctypes.byref(g), R, _p(seq_lens), _p(host_cache_locs), _p(rows),
                                              int(rows.size), _p(device_buffer_tokens), _p(lru_slots),
                                              ctypes.byref(err))
+        return int(err.value)
+
+    def resolve_spec(self, top_k_tokens, committed_lens, host_cache_locs, device_buffer_locs,
+                     device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows, miss_counts,
+                     host_pools, device_pools) -> int:
+        """A speculative batch of Q = top_k_tokens.shape[0] verify steps, in order: step q
+        resolves top_k_tokens[q] for committed_lens + q + 1 tokens into out_rows[q];
+        device_buffer_locs is [R, H + Q] (H slots, then Q reserved rows)."""
+        g = self.g
+        Q, R = top_k_tokens.shape[0], committed_lens.shape[0]
+        _i32(top_k_tokens, (Q, R, g.top_k)); _i32(committed_lens); _i32(host_cache_locs, (R, g.max_context))
+        _i32(device_buffer_locs, (R, g.hot_slots + Q)); _i32(device_buffer_tokens, (R, g.hot_slots))
+        _i32(lru_slots, (R, g.hot_slots)); _i32(lru_clock, (R,)); _i32(out_rows, (Q, R, g.top_k))
+        if resident_pages is not None:
+            _i32(resident_pages, (R, g.max_pages))
+        if miss_counts is not None:
+            _i32(miss_counts, (Q, R))
+        err = ctypes.c_uint32(0)
+        hp = self._pools(host_pools, g.host_rows)
+        dp = self._pools(device_pools, g.device_rows)
+        self.lib.oracle_resolve_spec(ctypes.byref(g), R, Q, _p(top_k_tokens), _p(committed_lens),
+                                     _p(host_cache_locs), _p(device_buffer_locs), _p(device_buffer_tokens),
+                                     _p(lru_slots), _p(lru_clock), _p(resident_pages), _p(out_rows),
+                                     _p(miss_counts), hp, dp, ctypes.byref(err))
+        return int(err.value)
+
+    def backup_spec(self, num_queries: int, committed_lens, accepted, host_cache_locs, device_buffer_locs,
+                    resident_pages, host_pools, device_pools) -> int:
+        """Back up the first accepted[r] positions of a speculative batch of num_queries."""
+        g = self.g
+        R = committed_lens.shape[0]
+        _i32(committed_lens); _i32(accepted, (R,)); _i32(host_cache_locs, (R, g.max_context))
+        _i32(device_buffer_locs, (R, g.hot_slots + num_queries))
+        if resident_pages is not None:
+            _i32(resident_pages, (R, g.max_pages))
+        err = ctypes.c_uint32(0)
+        hp = self._pools(host_pools, g.host_rows)
+        dp = self._pools(device_pools, g.device_rows)
+        self.lib.oracle_backup_spec(ctypes.byref(g), R, num_queries, _p(committed_lens), _p(accepted),
+                                    _p(host_cache_locs), _p(device_buffer_locs), _p(resident_pages), hp, dp,
+                                    ctypes.byref(err))
         return int(err.value)

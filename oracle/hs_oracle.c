@@ -112,13 +112,18 @@ static int64_t resident_row(const oracle_geom* g, const int32_t* resident_pages,
  * host_pools / device_pools: num_layers pointers to [rows, row_bytes] byte pools.
  * Error bits are OR-ed into *err.
  */
-void oracle_resolve_plan(const oracle_geom* g, int32_t num_requests, const int32_t* top_k_tokens,
+/* One resolve call. spec_q < 0: a plain decode step (seq_lens are the lengths, the one new
+ * position is the newest token); spec_q >= 0: verify step spec_q of a speculative batch of
+ * spec_n queries (seq_lens are the committed lengths S0). device_buffer_locs rows hold
+ * H + spec_n entries (H slots, then the reserved rows). */
+static void resolve_call(const oracle_geom* g, int32_t num_requests, const int32_t* top_k_tokens,
                          const int32_t* seq_lens, const int32_t* host_cache_locs,
                          const int32_t* device_buffer_locs, int32_t* device_buffer_tokens,
                          int32_t* lru_slots, int32_t* lru_clock, const int32_t* resident_pages,
                          int32_t* out_rows, int32_t* miss_counts, uint8_t* const* host_pools,
                          uint8_t* const* device_pools, uint32_t* err, int32_t copy_layers,
-                         int32_t* plan_tokens, int32_t* plan_dst, int32_t* plan_count) {
+                         int32_t* plan_tokens, int32_t* plan_dst, int32_t* plan_count, int32_t spec_q,
+                         int32_t spec_n) {
   const int32_t K = g->top_k, H = g->hot_slots, B = g->row_bytes;
   int32_t* cls = (int32_t*)malloc(sizeof(int32_t) * (size_t)K);
   int32_t* first_at = (int32_t*)malloc(sizeof(int32_t) * (size_t)(g->max_context + 1));
@@ -131,12 +136,19 @@ void oracle_resolve_plan(const oracle_geom* g, int32_t num_requests, const int32
 
   for (int32_t r = 0; r < num_requests; ++r) {
     const int32_t* tk = top_k_tokens + (int64_t)r * K;
-    const int32_t* dbl = device_buffer_locs + (int64_t)r * (H + 1);
+    const int32_t* dbl = device_buffer_locs + (int64_t)r * (H + spec_n);
     const int32_t* hcl = host_cache_locs + (int64_t)r * g->max_context;
     int32_t* tokens = device_buffer_tokens + (int64_t)r * H;
     int32_t* stamps = lru_slots + (int64_t)r * H;
     int32_t* out = out_rows + (int64_t)r * K;
-    const int32_t S = seq_lens[r];
+    /* Verify step q of a speculative batch attends over S0 + q + 1 tokens. The batch's
+     * positions [S0, S0 + Q) -- S0 the token the last round sampled, then the drafts -- are
+     * new to the cache and sit in the reserved rows H + (t - S0)
+     * ([vLLM-impl] 7.1: the buffer is (n_spec + 2) x top_k rows; 7.4: each verify step gets
+     * its own plan and shares the request's hot state). A plain step's one new position is
+     * the newest token, seq_len - 1, in row H. */
+    const int32_t S = spec_q < 0 ? seq_lens[r] : seq_lens[r] + spec_q + 1;
+    const int32_t base = spec_q < 0 ? S - 1 : seq_lens[r];
 
     for (int32_t i = 0; i < K; ++i) out[i] = -1;
     if (miss_counts) miss_counts[r] = 0;
@@ -171,7 +183,12 @@ void oracle_resolve_plan(const oracle_geom* g, int32_t num_requests, const int32
     if (S <= H) {
       for (int32_t i = 0; i < K; ++i)
         if (cls[i] == E_VALID) out[i] = checked_row(dbl[tk[i]], g->device_rows, err);
-      if (S >= 1) tokens[S - 1] = S - 1;
+      if (spec_q < 0) {
+        if (S >= 1) tokens[S - 1] = S - 1;
+      } else {  /* committed positions only: S0 (the token the last round sampled) and the
+                 * ones before it the previous batch may have accepted, never the drafts */
+        for (int32_t t = base - spec_n > 0 ? base - spec_n : 0; t <= base; ++t) tokens[t] = t;
+      }
       continue;
     }
 
@@ -179,17 +196,17 @@ void oracle_resolve_plan(const oracle_geom* g, int32_t num_requests, const int32
     const int32_t c = lru_clock[r] + 1;
     lru_clock[r] = c;
 
-    /* The newest token lives in the reserved row H ([SGLang-analysis] "How capacity is
-     * computed": the buffer carries one extra page for the new token). */
+    /* New positions live in the reserved rows after the H slots ([SGLang-analysis] "How
+     * capacity is computed": the buffer carries an extra page for the new token). */
     for (int32_t i = 0; i < K; ++i)
-      if (cls[i] == E_VALID && tk[i] == S - 1) {
-        out[i] = checked_row(dbl[H], g->device_rows, err);
+      if (cls[i] == E_VALID && tk[i] >= base) {
+        out[i] = checked_row(dbl[H + (tk[i] - base)], g->device_rows, err);
         cls[i] = E_NEWEST;
       }
 
     /* Tripwires: corrupt slot state becomes a free slot ([vLLM-impl] 7.2 phase 3). */
     for (int32_t s = 0; s < H; ++s) {
-      if (stamps[s] < 0 || stamps[s] > c - 1 || tokens[s] < -1 || tokens[s] >= S - 1) {
+      if (stamps[s] < 0 || stamps[s] > c - 1 || tokens[s] < -1 || tokens[s] >= base) {
         tokens[s] = -1;
         stamps[s] = 0;
         *err |= OR_ERR_STATE;
@@ -268,6 +285,41 @@ void oracle_resolve_plan(const oracle_geom* g, int32_t num_requests, const int32
   free(cls); free(first_at); free(lowest_slot); free(holders); free(used); free(misses); free(cand);
 }
 
+void oracle_resolve_plan(const oracle_geom* g, int32_t num_requests, const int32_t* top_k_tokens,
+                         const int32_t* seq_lens, const int32_t* host_cache_locs,
+                         const int32_t* device_buffer_locs, int32_t* device_buffer_tokens,
+                         int32_t* lru_slots, int32_t* lru_clock, const int32_t* resident_pages,
+                         int32_t* out_rows, int32_t* miss_counts, uint8_t* const* host_pools,
+                         uint8_t* const* device_pools, uint32_t* err, int32_t copy_layers,
+                         int32_t* plan_tokens, int32_t* plan_dst, int32_t* plan_count) {
+  resolve_call(g, num_requests, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs, device_buffer_tokens,
+               lru_slots, lru_clock, resident_pages, out_rows, miss_counts, host_pools, device_pools, err,
+               copy_layers, plan_tokens, plan_dst, plan_count, -1, 1);
+}
+
+/*
+ * A speculative batch ([vLLM-arch] speculative decoding: each verify step is resolved and
+ * consumed in order, with its own replayable plan rows and the request's shared hot state,
+ * so a later step cannot reuse a hot row before the earlier step consumed it; [vLLM-impl]
+ * 7.4 and 7.1: one resolve per verify step over a slice of the workspace, buffer of
+ * (n_spec + 2) x top_k rows). num_queries = n_spec + 1 verify steps run in order: step q
+ * resolves top_k_tokens[q] (each [R, K]) for S0 + q + 1 tokens into out_rows[q] and
+ * miss_counts[q] (or NULL), every layer copied. committed_lens are the S0.
+ */
+void oracle_resolve_spec(const oracle_geom* g, int32_t num_requests, int32_t num_queries,
+                         const int32_t* top_k_tokens, const int32_t* committed_lens,
+                         const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
+                         int32_t* device_buffer_tokens, int32_t* lru_slots, int32_t* lru_clock,
+                         const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
+                         uint8_t* const* host_pools, uint8_t* const* device_pools, uint32_t* err) {
+  const int64_t RK = (int64_t)num_requests * g->top_k;
+  for (int32_t q = 0; q < num_queries; ++q)
+    resolve_call(g, num_requests, top_k_tokens + q * RK, committed_lens, host_cache_locs, device_buffer_locs,
+                 device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows + q * RK,
+                 miss_counts ? miss_counts + (int64_t)q * num_requests : NULL, host_pools, device_pools, err,
+                 g->num_layers, NULL, NULL, NULL, q, num_queries);
+}
+
 /* The whole step: every layer of the group gets its miss rows; no plan is kept. */
 void oracle_resolve(const oracle_geom* g, int32_t num_requests, const int32_t* top_k_tokens,
                     const int32_t* seq_lens, const int32_t* host_cache_locs,
@@ -275,9 +327,9 @@ void oracle_resolve(const oracle_geom* g, int32_t num_requests, const int32_t* t
                     int32_t* lru_slots, int32_t* lru_clock, const int32_t* resident_pages,
                     int32_t* out_rows, int32_t* miss_counts, uint8_t* const* host_pools,
                     uint8_t* const* device_pools, uint32_t* err) {
-  oracle_resolve_plan(g, num_requests, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs,
-                      device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows, miss_counts,
-                      host_pools, device_pools, err, g->num_layers, NULL, NULL, NULL);
+  resolve_call(g, num_requests, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs, device_buffer_tokens,
+               lru_slots, lru_clock, resident_pages, out_rows, miss_counts, host_pools, device_pools, err,
+               g->num_layers, NULL, NULL, NULL, -1, 1);
 }
 
 /*
@@ -407,6 +459,38 @@ void oracle_invalidate_host_rows(const oracle_geom* g, int32_t num_requests, con
           clear_slot(tokens, stamps, s);
           break;
         }
+    }
+  }
+}
+
+/*
+ * Backup after a speculative batch: the first accepted[r] of the batch's positions S0 + j
+ * (j < num_queries) are now committed; each one's row goes to its host row, every layer.
+ * The row is its resident row when its page is resident, slot S0 + j while the sequence
+ * then fit the buffer (S0 + j + 1 <= H), else the reserved row H + j. accepted outside
+ * [0, num_queries] or a position past max_context skips the request (ERR_SEQLEN).
+ */
+void oracle_backup_spec(const oracle_geom* g, int32_t num_requests, int32_t num_queries,
+                        const int32_t* committed_lens, const int32_t* accepted, const int32_t* host_cache_locs,
+                        const int32_t* device_buffer_locs, const int32_t* resident_pages,
+                        uint8_t* const* host_pools, uint8_t* const* device_pools, uint32_t* err) {
+  const int32_t H = g->hot_slots, B = g->row_bytes;
+  for (int32_t r = 0; r < num_requests; ++r) {
+    const int32_t S0 = committed_lens[r], n = accepted[r];
+    if (S0 < 0 || n < 0 || n > num_queries || (int64_t)S0 + n > g->max_context) {
+      *err |= OR_ERR_SEQLEN;
+      continue;
+    }
+    const int32_t* dbl = device_buffer_locs + (int64_t)r * (H + num_queries);
+    for (int32_t j = 0; j < n; ++j) {
+      const int32_t t = S0 + j;
+      int64_t row = resident_row(g, resident_pages, r, t);
+      if (row < 0) row = t + 1 <= H ? dbl[t] : dbl[H + j];
+      if (row < 0 || row >= g->device_rows) { *err |= OR_ERR_DEVROW; continue; }
+      const int64_t h = host_cache_locs[(int64_t)r * g->max_context + t];
+      if (h < 0 || h >= g->host_rows) { *err |= OR_ERR_HOSTROW; continue; }
+      for (int32_t l = 0; l < g->num_layers; ++l)
+        memcpy(host_pools[l] + (size_t)h * (size_t)B, device_pools[l] + (size_t)row * (size_t)B, (size_t)B);
     }
   }
 }

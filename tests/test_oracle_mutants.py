@@ -22,7 +22,7 @@ MUTANTS = [
      "if (x->occupied != y->occupied) return x->occupied < y->occupied ? 1 : -1;"),
     ("clock_not_stored", "    lru_clock[r] = c;\n", "\n"),
     ("hit_not_refreshed", "        stamps[s] = c;\n        used[s] = 1;", "        used[s] = 1;"),
-    ("newest_not_reserved", "if (cls[i] == E_VALID && tk[i] == S - 1) {", "if (cls[i] == E_VALID && tk[i] == S) {"),
+    ("newest_not_reserved", "if (cls[i] == E_VALID && tk[i] >= base) {", "if (cls[i] == E_VALID && tk[i] > base) {"),
     ("fast_path_off_by_one", "  if (S <= H) {\n      for", "  if (S < H) {\n      for"),
     ("victims_reversed", "int32_t v = cand[j].slot;", "int32_t v = cand[m - 1 - j].slot;"),
     ("token_as_host_row", "int64_t h = hcl[t];", "int64_t h = t;"),
@@ -30,7 +30,7 @@ MUTANTS = [
      "out[i] = checked_row(dbl[s + 1], g->device_rows, err);\n        cls[i] = E_DONE;"),
     ("resident_offset_wrong", "return (int64_t)p * g->page_size + t % g->page_size;",
      "return (int64_t)p * g->page_size + (t + 1) % g->page_size;"),
-    ("sanitize_too_loose", "tokens[s] < -1 || tokens[s] >= S - 1)", "tokens[s] < -1 || tokens[s] >= S)"),
+    ("sanitize_too_loose", "tokens[s] < -1 || tokens[s] >= base)", "tokens[s] < -1 || tokens[s] >= base + 1)"),
     ("backup_always_reserved", "if (row < 0) row = S <= H ? dbl[t] : dbl[H];", "if (row < 0) row = dbl[H];"),
     ("duplicates_not_rejected", "else if (first_at[t] >= 0)", "else if (first_at[t] >= 2000000000)"),
     ("misses_not_zero_filled", "else memset(dst, 0, (size_t)B);", "else (void)dst;"),
@@ -44,6 +44,11 @@ MUTANTS = [
     ("plan_drops_first_miss", "plan_dst[(int64_t)r * K + j] = d;", "plan_dst[(int64_t)r * K + j] = j == 0 ? -1 : d;"),
     ("leader_copies_every_layer", "for (int32_t l = 0; l < copy_layers; ++l) {",
      "for (int32_t l = 0; l < g->num_layers; ++l) {"),
+    ("spec_one_reserved_row", "out[i] = checked_row(dbl[H + (tk[i] - base)], g->device_rows, err);",
+     "out[i] = checked_row(dbl[H], g->device_rows, err);"),
+    ("spec_marks_before_s0_only", "t <= base; ++t) tokens[t] = t;", "t < base; ++t) tokens[t] = t;"),
+    ("spec_backup_first_reserved_row", "if (row < 0) row = t + 1 <= H ? dbl[t] : dbl[H + j];",
+     "if (row < 0) row = t + 1 <= H ? dbl[t] : dbl[H];"),
 ]
 
 

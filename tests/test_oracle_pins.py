@@ -413,6 +413,9 @@ def run_all_pins() -> int:
     checks += [lambda c=c, gs=gs: sp.test_split_equals_fused(c, gs) for c, gs in sp.SPLITS[:2]]
     checks += [lambda n=n: sp.test_plan_is_the_steps_misses(n) for n in ("dsa_small", "indexshare_small")]
     checks += [sp.test_leader_only_leaves_followers]
+    import test_oracle_spec as spec
+    checks += [spec.test_spec_golden, lambda: spec.test_one_query_batch_is_a_plain_step("tiny"),
+               lambda: spec.test_replayable_plans("dsa_small", 4)]
     failed = 0
     for c in checks:
         try:
