@@ -43,7 +43,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "invalidate_tokens", "invalidate_host_rows", "split"],
+    ap.add_argument("--op", default="step",
+                    choices=["step", "invalidate_tokens", "invalidate_host_rows", "split", "spec"],
                     help="step: the decode step (default); invalidate_*: one hot-slot invalidation call; "
                          "split: leader resolve + follower gathers on a copy stream vs the fused step")
     ap.add_argument("--sweep", action="store_true",
@@ -770,11 +771,135 @@ def run_split(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+SPEC_QUERIES = 4  # n_spec = 3 draft tokens (MTP3) + the sampled one
+
+
+def run_spec(args, ws, rank, local):
+    """Speculative batches at the workload's shape: Q = SPEC_QUERIES verify steps per batch,
+    H = (Q + 1) * top_k hot slots (the buffer the pages size for n_spec + 2), every position
+    accepted. Per batch the forward stand-in writes the Q new rows, then hs_resolve_spec
+    (Q launches) and hs_backup_spec run; events bracket resolve + backup. Top-k rows keep
+    90 % of the previous verify step's row and draw the rest over the step's length."""
+    import torch
+    import hierarchical_sparse_attention_gb300 as hs
+    import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    Q = SPEC_QUERIES
+    W_, K_ = args.warmup, args.steps
+    nb = W_ + K_
+    wl = W.make(args.config, args.seed + 1000 * rank, steps=nb * Q + 2)
+    R, K, B, L = wl.R, wl.K, wl.B, wl.L
+    H = (Q + 1) * K
+    pools = [alloc_host(wl.host_rows * B) for _ in range(L)]
+    for l, (arr, reg) in enumerate(pools):
+        wl.fill_host_pool(l, arr)
+        touch_host_pool_from_gpu(hs.hs_host_register(arr) if reg else host_device_ptr(arr), arr.nbytes)
+    host = [arr for arr, _ in pools]
+    dev_rows = R * (H + Q)
+    dpool = [torch.full((dev_rows * B,), 0xA5, dtype=torch.uint8, device=dev) for _ in range(L)]
+    dbl_np = np.arange(dev_rows, dtype=np.int32).reshape(R, H + Q)
+    S0 = (wl.seq0 - 1).astype(np.int32)
+    assert int(S0.min()) + 1 > H, "every request starts past the fast path"
+    rng = np.random.default_rng(args.seed + 77)
+    tks, s0s = [], []
+    prev = [rng.choice(int(S0[r]), size=K, replace=False).astype(np.int32) for r in range(R)]
+    for b in range(nb):
+        tk = np.empty((Q, R, K), np.int32)
+        for q in range(Q):
+            for r in range(R):
+                S = int(S0[r]) + q + 1
+                keep = rng.permutation(prev[r])[: int(0.9 * K)]
+                fresh = np.setdiff1d(rng.integers(0, S, size=2 * K).astype(np.int32), keep)
+                fresh = rng.permutation(fresh)[: K - keep.size]
+                row = np.concatenate([keep, fresh])
+                if row.size < K:
+                    row = np.concatenate([row, np.full(K - row.size, -1, np.int32)])
+                tk[q, r] = rng.permutation(row)
+                prev[r] = row[row >= 0]
+        tks.append(tk)
+        s0s.append(S0.copy())
+        S0 = S0 + Q
+    g_tk = torch.from_numpy(np.stack(tks)).to(dev)
+    g_s0 = torch.from_numpy(np.stack(s0s)).to(dev)
+    acc = torch.full((R,), Q, dtype=torch.int32, device=dev)
+    # the forward writes: batch b's position S0 + j of request r goes to reserved row H + j
+    new_rows = torch.from_numpy(dbl_np[:, H:].reshape(-1).astype(np.int64)).to(dev)
+    new_dat = [torch.from_numpy(np.concatenate([wl.rows(l, r, list(range(int(s0s[0][r]), int(s0s[0][r]) + Q)))
+                                                for r in range(R)])).to(dev) for l in range(L)]
+    hcl = torch.from_numpy(wl.host_cache_locs).to(dev)
+    dbl = torch.from_numpy(dbl_np).to(dev)
+    tok = torch.full((R, H), -1, dtype=torch.int32, device=dev)
+    st = torch.zeros((R, H), dtype=torch.int32, device=dev)
+    clk = torch.zeros((R,), dtype=torch.int32, device=dev)
+    out = torch.empty((Q, R, K), dtype=torch.int32, device=dev)
+    miss = torch.empty((Q, R), dtype=torch.int32, device=dev)
+    cfg = hs.make_config(R, K, H, B, L, wl.ps, wl.max_context, wl.max_pages)
+    wsp = torch.zeros(hs.hs_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    h = hs.hs_create(cfg, host, dpool, wl.host_rows, dev_rows, wsp)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    miss_acc = torch.zeros((nb, Q, R), dtype=torch.int64, device=dev)
+
+    def batch(b, evs):
+        for l in range(L):  # the forward pass's new rows (their bytes do not matter here)
+            dpool[l].view(-1, B).index_copy_(0, new_rows, new_dat[l])
+        flush.zero_()
+        if evs is not None:
+            evs[0].record(stream)
+        hs.hs_resolve_spec(h, R, Q, g_tk[b], g_s0[b], hcl, dbl, tok, st, clk, None, out, miss, stream)
+        hs.hs_backup_spec(h, R, Q, g_s0[b], acc, hcl, dbl, None, stream)
+        if evs is not None:
+            evs[1].record(stream)
+        miss_acc[b].copy_(miss)
+
+    for b in range(W_):
+        batch(b, None)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K_)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local, enabled=not args.no_clocks) as clocks:
+        torch.cuda._sleep(int(2e6 * (5 + K_ // 4)))
+        for i in range(K_):
+            batch(W_ + i, evs[i])
+        torch.cuda.synchronize()
+    barrier(ws)
+    ms = [e[0].elapsed_time(e[1]) for e in evs]
+    err = hs.hs_get_error(h, clear=True)
+    hs.hs_destroy(h)
+    for arr, reg in pools:
+        if reg:
+            hs.hs_host_unregister(arr)
+    total_s = max_over_ranks(sum(ms) * 1e-3, ws)
+    rows = int((np.stack(tks[W_:]) >= 0).sum())
+    misses = miss_acc[W_:].sum(dim=2).float().mean(dim=0).cpu().numpy()  # per verify step
+    line = {
+        "metric": "top-k rows resolved/s (speculative batches)", "value": ws * rows / total_s, "unit": "rows/s",
+        "n_gpus": ws, "steps": K_, "warmup": W_, "ms_per_step": 1e3 * total_s / K_, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {R} requests, top_k {K}, {Q} verify steps per batch "
+                               f"(n_spec {Q - 1}), H = (n_spec + 2) * top_k = {H} slots, {B}-byte rows, "
+                               "every draft accepted",
+                   "l2": "flushed between timed batches (256 MiB write)",
+                   "step": "hs_resolve_spec (Q launches) + hs_backup_spec"},
+        "p50_batch_us": 1e3 * float(np.median(ms)), "p50_per_verify_step_us": 1e3 * float(np.median(ms)) / Q,
+        "misses_per_verify_step": [float(x) for x in misses],
+        "gpu_launches": K_ * (Q + 1), "device_flags": err, "clocks": clocks.summary(),
+        "host_pool": "huge pages, hs_host_register" if pools[0][1] else "cudaHostAlloc",
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.op == "spec":
+        run_spec(args, ws, rank, local)
     elif args.op == "split":
         if args.config == "dsa":
             args.config = "indexshare"  # the split needs a layer group

@@ -28,7 +28,9 @@ HS_MAX_TOP_K, HS_MAX_HOT_SLOTS, HS_MAX_LAYERS = 4096, 16384, 8
 # Every symbol include/hs.h declares (checked against the library by the tests).
 EXPORTS = ("hs_workspace_bytes", "hs_create", "hs_resolve", "hs_backup", "hs_get_error", "hs_destroy",
            "hs_status_str", "hs_host_register", "hs_host_unregister", "hs_resolve_noalloc",
-           "hs_invalidate_tokens", "hs_invalidate_host_rows", "hs_resolve_layers", "hs_gather")
+           "hs_invalidate_tokens", "hs_invalidate_host_rows", "hs_resolve_layers", "hs_gather",
+           "hs_resolve_spec", "hs_backup_spec")
+HS_MAX_SPEC_QUERIES = 8
 HS_NOALLOC_MAX_LAYERS = 8
 
 
@@ -61,6 +63,10 @@ def _load() -> ctypes.CDLL:
     lib.hs_resolve_layers.argtypes = [P, i32] + [P] * 10 + [i32, P]
     lib.hs_resolve_layers.restype = ctypes.c_int
     lib.hs_gather.argtypes = [P, i32, P, i32, i32, P]
+    lib.hs_resolve_spec.argtypes = [P, i32, i32] + [P] * 10 + [P]
+    lib.hs_resolve_spec.restype = ctypes.c_int
+    lib.hs_backup_spec.argtypes = [P, i32, i32] + [P] * 5 + [P]
+    lib.hs_backup_spec.restype = ctypes.c_int
     lib.hs_gather.restype = ctypes.c_int
     lib.hs_invalidate_tokens.argtypes = [P, i32] + [P] * 5 + [P]
     lib.hs_invalidate_tokens.restype = ctypes.c_int
@@ -177,6 +183,23 @@ def hs_resolve_layers(h: Handle, num_requests: int, top_k_tokens, seq_lens, host
                                   _addr(host_cache_locs), _addr(device_buffer_locs), _addr(device_buffer_tokens),
                                   _addr(lru_slots), _addr(lru_clock), _addr(resident_pages), _addr(out_rows),
                                   _addr(miss_counts), copy_layers, _stream(stream)), "hs_resolve_layers")
+
+
+def hs_resolve_spec(h: Handle, num_requests: int, num_queries: int, top_k_tokens, committed_lens, host_cache_locs,
+                    device_buffer_locs, device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows,
+                    miss_counts, stream=None) -> None:
+    _check(_lib.hs_resolve_spec(h.ptr if h else None, num_requests, num_queries, _addr(top_k_tokens),
+                                _addr(committed_lens), _addr(host_cache_locs), _addr(device_buffer_locs),
+                                _addr(device_buffer_tokens), _addr(lru_slots), _addr(lru_clock),
+                                _addr(resident_pages), _addr(out_rows), _addr(miss_counts), _stream(stream)),
+           "hs_resolve_spec")
+
+
+def hs_backup_spec(h: Handle, num_requests: int, num_queries: int, committed_lens, accepted, host_cache_locs,
+                   device_buffer_locs, resident_pages, stream=None) -> None:
+    _check(_lib.hs_backup_spec(h.ptr if h else None, num_requests, num_queries, _addr(committed_lens),
+                               _addr(accepted), _addr(host_cache_locs), _addr(device_buffer_locs),
+                               _addr(resident_pages), _stream(stream)), "hs_backup_spec")
 
 
 def hs_gather(h: Handle, num_requests: int, host_cache_locs, first_layer: int, num_layers: int,

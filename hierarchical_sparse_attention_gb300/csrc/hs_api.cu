@@ -159,7 +159,7 @@ hs_status hs_resolve_layers(hs_handle* h, int32_t num_requests, const int32_t* t
   if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
   hs::ResolveArgs a{h->hint,   top_k_tokens, seq_lens,   host_cache_locs, device_buffer_locs, device_buffer_tokens,
                     lru_slots, lru_clock,    resident_pages, out_rows,   miss_counts,        copy_layers,
-                    h->plan_tok, h->plan_dst, h->plan_cnt};
+                    h->plan_tok, h->plan_dst, h->plan_cnt, -1, 1};
   if (hs::launch_resolve(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
     return HS_ERR_CUDA;
   return HS_OK;
@@ -174,6 +174,45 @@ hs_status hs_resolve(hs_handle* h, int32_t num_requests, const int32_t* top_k_to
   return hs_resolve_layers(h, num_requests, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs,
                            device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows, miss_counts,
                            h->cfg.num_layers, stream);
+}
+
+hs_status hs_resolve_spec(hs_handle* h, int32_t num_requests, int32_t num_queries, const int32_t* top_k_tokens,
+                          const int32_t* committed_lens, const int32_t* host_cache_locs,
+                          const int32_t* device_buffer_locs, int32_t* device_buffer_tokens, int32_t* lru_slots,
+                          int32_t* lru_clock, const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
+                          hs_stream_t stream) {
+  if (!h || num_requests < 0 || num_requests > h->cfg.max_requests) return HS_ERR_INVALID_ARG;
+  if (num_queries < 1 || num_queries > HS_MAX_SPEC_QUERIES) return HS_ERR_INVALID_ARG;
+  if (num_requests == 0) return HS_OK;
+  if (!top_k_tokens || !committed_lens || !host_cache_locs || !device_buffer_locs || !device_buffer_tokens ||
+      !lru_slots || !lru_clock || !out_rows)
+    return HS_ERR_INVALID_ARG;
+  if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
+  const size_t RK = (size_t)num_requests * (size_t)h->cfg.top_k;
+  // The verify steps run in order on the stream, one launch each, over the shared state.
+  for (int32_t q = 0; q < num_queries; ++q) {
+    hs::ResolveArgs a{h->hint,   top_k_tokens + q * RK, committed_lens, host_cache_locs, device_buffer_locs,
+                      device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows + q * RK,
+                      miss_counts ? miss_counts + (size_t)q * num_requests : nullptr, h->cfg.num_layers,
+                      nullptr,   nullptr,      nullptr,  q, num_queries};
+    if (hs::launch_resolve(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+      return HS_ERR_CUDA;
+  }
+  return HS_OK;
+}
+
+hs_status hs_backup_spec(hs_handle* h, int32_t num_requests, int32_t num_queries, const int32_t* committed_lens,
+                         const int32_t* accepted, const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
+                         const int32_t* resident_pages, hs_stream_t stream) {
+  if (!h || num_requests < 0 || num_requests > h->cfg.max_requests) return HS_ERR_INVALID_ARG;
+  if (num_queries < 1 || num_queries > HS_MAX_SPEC_QUERIES) return HS_ERR_INVALID_ARG;
+  if (num_requests == 0) return HS_OK;
+  if (!committed_lens || !accepted || !host_cache_locs || !device_buffer_locs) return HS_ERR_INVALID_ARG;
+  if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
+  hs::BackupArgs a{committed_lens, host_cache_locs, device_buffer_locs, resident_pages, accepted, num_queries};
+  if (hs::launch_backup(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+    return HS_ERR_CUDA;
+  return HS_OK;
 }
 
 hs_status hs_gather(hs_handle* h, int32_t num_requests, const int32_t* host_cache_locs, int32_t first_layer,
@@ -195,7 +234,7 @@ hs_status hs_backup(hs_handle* h, int32_t num_requests, const int32_t* seq_lens,
   if (num_requests == 0) return HS_OK;
   if (!seq_lens || !host_cache_locs || !device_buffer_locs) return HS_ERR_INVALID_ARG;
   if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
-  hs::BackupArgs a{seq_lens, host_cache_locs, device_buffer_locs, resident_pages};
+  hs::BackupArgs a{seq_lens, host_cache_locs, device_buffer_locs, resident_pages, nullptr, 1};
   if (hs::launch_backup(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
     return HS_ERR_CUDA;
   return HS_OK;

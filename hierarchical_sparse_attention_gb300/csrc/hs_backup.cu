@@ -1,5 +1,5 @@
-// Eager backup: the newest token's KV row, device -> pinned host, one warp per
-// (request, layer).
+// Eager backup: the newest token's KV row -- or, after a speculative batch, the rows of its
+// accepted positions -- device -> pinned host, one warp per (request, layer, position).
 //
 // Source: "HiSparse: moving the long-context decode capacity bottleneck from GPU memory to
 // CPU memory", "Per decode step workflow", step 5 (after attention, the last token's KV is
@@ -7,7 +7,10 @@
 // resident page when that page is GPU-resident ("vLLM HiSparse local KV offload
 // architecture", "Hot-row lookup and LRU"), in buffer slot seq_len-1 while the sequence
 // fits the buffer, else in the reserved slot H ("How capacity is computed": the buffer
-// carries an extra page for the new token).
+// carries an extra page for the new token). A speculative batch's positions S0 + j sit in
+// their resident rows, in slot S0 + j while the sequence then fit the buffer, else in the
+// reserved row H + j ("vLLM Hybrid HiSparse source implementation analysis", 7.1: the buffer
+// holds (n_spec + 2) x top_k rows).
 #include "hs_internal.h"
 
 namespace hs {
@@ -35,28 +38,36 @@ __global__ void __launch_bounds__(kBackupThreads)
                   uint32_t* __restrict__ err_word) {
   const int lane = threadIdx.x & 31;
   const int w = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
-  const bool active = w < num_requests * g.L;  // whole warps
-  const int r = active ? w / g.L : 0, l = active ? w - r * g.L : 0;
-  const int32_t S = active ? a.seq_lens[r] : 0;
+  const int per_req = g.L * a.spec_n;
+  const bool active = w < num_requests * per_req;  // whole warps
+  const int r = active ? w / per_req : 0, rem = active ? w - r * per_req : 0;
+  const int l = rem / a.spec_n, j = rem - l * a.spec_n;
   uint32_t flag = 0;
   int64_t row = -1, host = -1;
-  if (!active) {
-    // spare warp of the last block: nothing to copy
-  } else if (S < 0 || S > g.max_context) {
-    flag = HS_FLAG_SEQLEN;
-  } else if (S >= 1) {
-    const int32_t t = S - 1;
-    int32_t page = -1;
-    if (a.resident_pages) page = a.resident_pages[(size_t)r * g.max_pages + t / g.page_size];
-    if (page >= 0) row = (int64_t)page * g.page_size + t % g.page_size;
-    else row = a.device_buffer_locs[(size_t)r * (g.H + 1) + (S <= g.H ? t : g.H)];
-    host = a.host_cache_locs[(size_t)r * g.max_context + t];
-    if (row < 0 || row >= g.device_rows) flag = HS_FLAG_DEVROW;
-    else if (host < 0 || host >= g.host_rows) flag = HS_FLAG_HOSTROW;
+  if (active) {
+    // position base + j for j < n: the newest token (base = S - 1, n = 1 unless empty), or a
+    // speculative batch's accepted positions (base = S0, n = accepted)
+    const int32_t in = a.seq_lens[r];
+    const int32_t n = a.accepted ? a.accepted[r] : (in >= 1 ? 1 : 0);
+    const int32_t base = a.accepted ? in : in - 1;
+    const bool bad = a.accepted ? (in < 0 || n < 0 || n > a.spec_n || (int64_t)in + n > g.max_context)
+                                : (in < 0 || in > g.max_context);
+    if (bad) {
+      if (j == 0) flag = HS_FLAG_SEQLEN;
+    } else if (j < n) {
+      const int32_t t = base + j;
+      int32_t page = -1;
+      if (a.resident_pages) page = a.resident_pages[(size_t)r * g.max_pages + t / g.page_size];
+      if (page >= 0) row = (int64_t)page * g.page_size + t % g.page_size;
+      else row = a.device_buffer_locs[(size_t)r * (g.H + a.spec_n) + (t + 1 <= g.H ? t : g.H + j)];
+      host = a.host_cache_locs[(size_t)r * g.max_context + t];
+      if (row < 0 || row >= g.device_rows) flag = HS_FLAG_DEVROW;
+      else if (host < 0 || host >= g.host_rows) flag = HS_FLAG_HOSTROW;
+    }
   }
   if (flag) {
     if (lane == 0) atomicOr(err_word, flag);
-  } else if (row >= 0) {  // row < 0: empty sequence, nothing to back up
+  } else if (row >= 0) {  // row < 0: nothing to back up here
     copy_row(g, pools, l, row, host, lane);
   }
   // Launched as a programmatic dependent of the resolve, this kernel may run beside it
@@ -69,7 +80,7 @@ __global__ void __launch_bounds__(kBackupThreads)
 
 cudaError_t launch_backup(const Geometry& g, const Pools* pools, const BackupArgs& a, int32_t num_requests,
                           uint32_t* err_word, cudaStream_t stream) {
-  const long long warps = (long long)num_requests * g.L;
+  const long long warps = (long long)num_requests * g.L * a.spec_n;
   const int per_block = kBackupThreads / 32;
   const unsigned blocks = (unsigned)((warps + per_block - 1) / per_block);
   cudaLaunchConfig_t cfg = {};

@@ -34,6 +34,8 @@ struct Geometry {
   int32_t vec;        // bytes per copy piece: 16, 4 or 1
   int32_t copy_ctas;  // copy CTAs clustered with each request's resolve CTA (0: it copies alone)
   int32_t copy_cap;   // misses one copy CTA can stage (all layers) in its shared memory
+  int32_t dbl_smem;   // 1: the resolve CTA stages the slot -> row table in shared memory; 0: it
+                      // reads it from global memory (large H, where the table does not fit)
   int64_t host_rows, device_rows;
 };
 
@@ -53,6 +55,9 @@ struct ResolveArgs {
   int32_t* plan_tok;    // [R, K] miss tokens in miss order (the follower plan), or NULL
   int32_t* plan_dst;    // [R, K] their device rows (-1: none)
   int32_t* plan_cnt;    // [R] misses per request
+  int32_t spec_q;       // -1: a plain step (seq_lens are lengths); q >= 0: verify step q of a
+                        // speculative batch (seq_lens are the batch's first positions S0)
+  int32_t spec_n;       // reserved rows after the H slots (1, or the batch's Q)
 };
 
 struct GatherArgs {
@@ -64,10 +69,12 @@ struct GatherArgs {
 };
 
 struct BackupArgs {
-  const int32_t* seq_lens;
+  const int32_t* seq_lens;  // lengths, or the batch's first positions S0 with `accepted`
   const int32_t* host_cache_locs;
   const int32_t* device_buffer_locs;
   const int32_t* resident_pages;
+  const int32_t* accepted;  // NULL: the newest position; else [R] accepted positions of a batch
+  int32_t spec_n;           // reserved rows after the H slots (1, or the batch's Q)
 };
 
 struct InvalidateArgs {

@@ -137,7 +137,7 @@ hs_status hs_resolve_noalloc(const hs_config* cfg, void* const* host_pools, void
   // no hint table here (misses start their transfer after the exact probe) and no plan
   hs::ResolveArgs a{nullptr,   top_k_tokens, seq_lens,       host_cache_locs, device_buffer_locs, device_buffer_tokens,
                     lru_slots, lru_clock,    resident_pages, out_rows,        miss_counts,        g.L,
-                    nullptr,   nullptr,      nullptr};  // every layer; no follower plan
+                    nullptr,   nullptr,      nullptr,        -1,              1};  // every layer; no plan
   uint32_t* err_word = reinterpret_cast<uint32_t*>(scratch + hs::kErrOffset);
   if (hs::launch_resolve(g, reinterpret_cast<const hs::Pools*>(scratch + hs::kPoolsOffset), a, num_requests,
                          err_word, s) != cudaSuccess)

@@ -101,7 +101,7 @@ __host__ __device__ inline Layout make_layout(const Geometry& g) {
   l.vict = o; o = align16(o + 4 * K);
   l.tok = o; o = align16(o + 4 * H);
   l.stamp = o; o = align16(o + 4 * H);
-  l.dbl = o; o = align16(o + 4 * (H + 1 + 3));
+  l.dbl = o; o = align16(o + (g.dbl_smem ? 4 * (H + 1 + 3) : 0));
   l.cls = o; o = align16(o + K);
   l.sflag = o; o = align16(o + H);
   l.wsum = o; o = align16(o + 4 * (NW + 1));
@@ -339,7 +339,8 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
   const int per = copy_slice(g);
   const int e0 = (q - 1) * per;
   const int ne = max(0, min(g.K, e0 + per) - e0);
-  const int32_t S = a.seq_lens[r];
+  const int32_t S = a.spec_q < 0 ? a.seq_lens[r] : a.seq_lens[r] + a.spec_q + 1;
+  const int32_t base = a.spec_q < 0 ? S - 1 : a.seq_lens[r];  // first position new to the cache
   const bool predict = a.hint != nullptr && a.copy_layers > 0 && S > g.H && S <= g.max_context;
   int16_t* hint_row = a.hint ? a.hint + (size_t)r * g.max_context : nullptr;
   const int32_t* hcl_row = a.host_cache_locs + (size_t)r * g.max_context;
@@ -360,7 +361,7 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
       // The host-row lookup waits for the prediction: issuing it for every entry up front
       // saves a round trip but adds one HBM request per top-k entry at kernel start, which
       // delays the whole cluster's loads more than it saves (measured).
-      if (t >= 0 && t < S - 1 &&
+      if (t >= 0 && t < base &&
           !(a.resident_pages && a.resident_pages[(size_t)r * g.max_pages + t / g.page_size] >= 0)) {
         const int gs = hint_row[t];
         if (!(gs >= 0 && gs < g.H)) {
@@ -510,8 +511,8 @@ __global__ void __launch_bounds__(T, 1)
   int32_t* s_tok = reinterpret_cast<int32_t*>(smem + lay.tok);
   int32_t* s_stamp = reinterpret_cast<int32_t*>(smem + lay.stamp);
   // the table starts at the same 16-byte phase as its global row
-  int32_t* s_dbl = reinterpret_cast<int32_t*>(smem + lay.dbl) +
-                   ((((uintptr_t)(a.device_buffer_locs + (size_t)r * (g.H + 1))) & 15) >> 2);
+  int32_t* s_dbl_staged = reinterpret_cast<int32_t*>(smem + lay.dbl) +
+                          ((((uintptr_t)(a.device_buffer_locs + (size_t)r * (g.H + a.spec_n))) & 15) >> 2);
   uint8_t* s_cls = smem + lay.cls;
   uint8_t* s_sflag = smem + lay.sflag;
   int32_t* s_wsum = reinterpret_cast<int32_t*>(smem + lay.wsum);
@@ -520,10 +521,15 @@ __global__ void __launch_bounds__(T, 1)
 
   const int K = g.K, H = g.H;
   const int HS = 1 << g.hash_bits;
-  const int32_t S = a.seq_lens[r];
+  // A plain step's one new position is the newest token, S - 1. Verify step q of a
+  // speculative batch attends over S0 + q + 1 tokens, and the batch's positions t >= S0 (the
+  // token the last round sampled, then the drafts) sit in the reserved rows H + (t - S0).
+  const int32_t S = a.spec_q < 0 ? a.seq_lens[r] : a.seq_lens[r] + a.spec_q + 1;
+  const int32_t base = a.spec_q < 0 ? S - 1 : a.seq_lens[r];
   const int32_t* tk_g = a.top_k_tokens + (size_t)r * K;
   int32_t* out_g = a.out_rows + (size_t)r * K;
-  const int32_t* dbl_g = a.device_buffer_locs + (size_t)r * (H + 1);
+  const int32_t* dbl_g = a.device_buffer_locs + (size_t)r * (H + a.spec_n);
+  const int32_t* s_dbl = g.dbl_smem ? s_dbl_staged : dbl_g;  // slot -> row table
   int32_t* tok_g = a.device_buffer_tokens + (size_t)r * H;
   int32_t* st_g = a.lru_slots + (size_t)r * H;
   uint32_t flags = 0;
@@ -541,7 +547,7 @@ __global__ void __launch_bounds__(T, 1)
 
   // ---- phase 0: state into shared memory, asynchronously
   cp_async_words(s_tk, tk_g, K);
-  cp_async_words(s_dbl, dbl_g, H + 1);
+  if (g.dbl_smem) cp_async_words(s_dbl_staged, dbl_g, H + 1);
   if (!fast) {
     cp_async_words(s_tok, tok_g, H);
     cp_async_words(s_stamp, st_g, H);
@@ -577,9 +583,9 @@ __global__ void __launch_bounds__(T, 1)
       } else if (fast) {
         c = C_FAST;
         row = s_dbl[t];
-      } else if (t == S - 1) {
+      } else if (t >= base) {
         c = C_NEWEST;
-        row = s_dbl[H];
+        row = t == base ? s_dbl[H] : dbl_g[H + (t - base)];
       } else {
         c = C_LOOKUP;
       }
@@ -607,8 +613,13 @@ __global__ void __launch_bounds__(T, 1)
       }
       out_g[i] = o;
     }
+    if (a.spec_q < 0) {
+      if (tid == 0 && S >= 1) tok_g[S - 1] = S - 1;
+    } else {  // committed positions only: S0 and the ones before it the last batch accepted
+      const int32_t t = max(0, base - a.spec_n) + tid;  // spec_n + 1 <= T threads
+      if (t <= base) tok_g[t] = t;
+    }
     if (tid == 0) {
-      if (S >= 1) tok_g[S - 1] = S - 1;
       if (a.miss_counts) a.miss_counts[r] = 0;
       if (a.plan_cnt) a.plan_cnt[r] = 0;
     }
@@ -635,7 +646,7 @@ __global__ void __launch_bounds__(T, 1)
       int32_t tkn = s_tok[s];
       const int32_t st = s_stamp[s];
       uint8_t f = 0;
-      if (st < 0 || st > clock - 1 || tkn < -1 || tkn >= S - 1) {
+      if (st < 0 || st > clock - 1 || tkn < -1 || tkn >= base) {
         tkn = -1;
         s_tok[s] = -1;
         s_stamp[s] = 0;
@@ -1005,6 +1016,8 @@ cudaError_t resolve_prepare(Geometry& g, int32_t max_requests) {
   const int max_dynamic = optin - (int)fa.sharedSizeBytes;
   g.copy_ctas = 0;
   g.copy_cap = 0;
+  g.dbl_smem = 1;
+  if (make_layout(g).total > (size_t)max_dynamic) g.dbl_smem = 0;  // the row table stays in global memory
   if (make_layout(g).total > (size_t)max_dynamic) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic);
   if (e != cudaSuccess) return e;

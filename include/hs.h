@@ -123,6 +123,7 @@ typedef enum {
 #define HS_MAX_TOP_K 4096
 #define HS_MAX_HOT_SLOTS 16384
 #define HS_MAX_LAYERS 8
+#define HS_MAX_SPEC_QUERIES 8 /* verify steps of one speculative batch (n_spec + 1) */
 
 /* Configuration of one layer group (layers that share one indexer top-k and therefore
  * one slot map; "vLLM Hybrid HiSparse source implementation analysis" 7.4).
@@ -190,6 +191,40 @@ HS_API hs_status hs_resolve_layers(hs_handle* h, int32_t num_requests, const int
                                    int32_t* lru_slots, int32_t* lru_clock, const int32_t* resident_pages,
                                    int32_t* out_rows, int32_t* miss_counts, int32_t copy_layers,
                                    hs_stream_t stream);
+
+/* A speculative batch ("vLLM HiSparse local KV offload architecture", speculative
+ * decoding: each verify step is resolved and consumed in order, with its own replayable
+ * plan rows and the request's shared hot state; "vLLM Hybrid HiSparse source
+ * implementation analysis", 7.4 and 7.1: one resolve per verify step, a buffer of
+ * (n_spec + 2) x top_k rows). num_queries = Q = n_spec + 1 (1..HS_MAX_SPEC_QUERIES) verify
+ * steps run in order, one kernel launch each: step q resolves top_k_tokens[q] for
+ * committed_lens[r] + q + 1 tokens into out_rows[q] and miss_counts[q]. The batch's
+ * positions t >= S0 = committed_lens[r] (the token the last round sampled, then the drafts;
+ * the forward pass has written them) resolve to the reserved rows H + (t - S0): with Q
+ * queries, device_buffer_locs is [R, H + Q]. The clock advances once per slow-path verify
+ * step, so with H >= (Q + 1) * top_k no verify step evicts a row an earlier step of the batch
+ * resolved: every step's out_rows stay valid until the batch is consumed. On the fast path a
+ * batch records slots S0 - Q .. S0 (committed), never its drafts.
+ *   top_k_tokens [Q, R, K], out_rows [Q, R, K], miss_counts [Q, R] or NULL; the rest as in
+ *   hs_resolve. No follower plan is recorded. */
+HS_API hs_status hs_resolve_spec(hs_handle* h, int32_t num_requests, int32_t num_queries,
+                                 const int32_t* top_k_tokens, const int32_t* committed_lens,
+                                 const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
+                                 int32_t* device_buffer_tokens, int32_t* lru_slots, int32_t* lru_clock,
+                                 const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
+                                 hs_stream_t stream);
+
+/* Eager backup after a speculative batch: the first accepted[r] positions S0 + j of the
+ * batch (S0 = committed_lens[r], 0 <= accepted <= num_queries) are now committed, and each
+ * one's row -- its resident row, slot S0 + j while the sequence then fit the buffer
+ * (S0 + j + 1 <= H), else the reserved row H + j -- goes to its host row, every layer.
+ * hs_backup is this call with num_queries = 1, committed_lens = seq_len - 1, accepted = 1.
+ * accepted outside [0, num_queries] or past max_context skips the request (HS_FLAG_SEQLEN).
+ * One kernel launch; same rules as hs_backup. */
+HS_API hs_status hs_backup_spec(hs_handle* h, int32_t num_requests, int32_t num_queries,
+                                const int32_t* committed_lens, const int32_t* accepted,
+                                const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
+                                const int32_t* resident_pages, hs_stream_t stream);
 
 /* Follower gather: copy the last resolve's miss rows for layers [first_layer, first_layer +
  * num_layers) -- host_pool[l][host_cache_locs[r][token]] to device_pool[l][row] for every

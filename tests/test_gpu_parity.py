@@ -136,3 +136,9 @@ def test_graph_capture_replay():
 
 def test_graph_capture_replay_indexshare():
     run_parity(W.make("indexshare", requests=16, steps=8, layers=2), pool_every=4, graph_from=1)
+
+
+def test_large_buffer_row_table_in_global():
+    """H = 5 x top_k = 10,240 slots at top_k 2048 (the speculative sizing): the resolve CTA's
+    shared memory cannot hold the slot -> row table too, so it reads it from global memory."""
+    run_parity(W.make("dsa", 8, requests=3, hot_slots=10240, steps=8, seq0=(40000, 52000, 30000)))

@@ -117,17 +117,26 @@ class SpecRun:
             return int(wl.resident_pages[r, t // wl.ps]) * wl.ps + t % wl.ps
         return int(self.dbl[r, t] if t + 1 <= self.H else self.dbl[r, self.H + j])
 
-    def batch(self):
-        wl, Q, K = self.wl, self.Q, self.wl.K
-        # the forward pass writes the batch's Q new positions; their host rows are not yet valid
+    def forward(self):
+        """What the forward pass does before a batch: write its Q new positions' rows to their
+        device rows; their host rows are not valid yet (poisoned). Returns the writes as
+        (request, token, device row, host row)."""
+        wl, writes = self.wl, []
         for r in range(wl.R):
-            for j in range(Q):
+            for j in range(self.Q):
                 t = int(self.S0[r]) + j
                 row = self.row_of(r, t, j)
+                h = int(wl.host_cache_locs[r, t])
+                writes.append((r, t, row, h))
                 for layer in range(wl.L):
                     self.dev[layer][row * wl.B:(row + 1) * wl.B] = wl.rows(layer, r, [t])[0]
-                    h = int(wl.host_cache_locs[r, t])
                     self.host[layer][h * wl.B:(h + 1) * wl.B] = 0xEE
+        return writes
+
+    def topk(self):
+        """Q seeded top-k rows: 70 % of the previous batch's last row (still in range), the
+        rest fresh, every verify step over its own length S0 + q + 1."""
+        wl, Q, K = self.wl, self.Q, self.wl.K
         tk = np.full((Q, wl.R, K), -1, np.int32)
         for q in range(Q):
             for r in range(wl.R):
@@ -138,35 +147,49 @@ class SpecRun:
                 fresh = self.rng.choice(pool, size=min(K - keep.size, pool.size), replace=False)
                 row = np.concatenate([keep, fresh]).astype(np.int32)
                 tk[q, r, : row.size] = self.rng.permutation(row)
-        out = np.zeros((Q, wl.R, K), np.int32)
+        return tk
+
+    def resolve(self, tk):
+        wl, Q = self.wl, self.Q
+        out = np.zeros((Q, wl.R, wl.K), np.int32)
         miss = np.zeros((Q, wl.R), np.int32)
         err = self.orc.resolve_spec(tk, self.S0, wl.host_cache_locs, self.dbl, self.tok, self.st, self.clk,
                                     wl.resident_pages, out, miss, self.host, self.dev)
         for r in range(wl.R):
             self.prev[r] = tk[Q - 1, r][tk[Q - 1, r] >= 0]
+        return out, miss, err
+
+    def batch(self):
+        self.forward()
+        tk = self.topk()
+        out, miss, err = self.resolve(tk)
         return tk, out, miss, err
 
-    def accept(self):
+    def accept(self, acc=None, check=True):
         wl = self.wl
-        acc = self.rng.integers(1, self.Q + 1, size=wl.R).astype(np.int32)
-        err = self.orc.backup_spec(self.Q, self.S0, acc, wl.host_cache_locs, self.dbl, wl.resident_pages,
+        if acc is None:
+            acc = self.rng.integers(1, self.Q + 1, size=wl.R).astype(np.int32)
+        S0 = self.S0.copy()
+        err = self.orc.backup_spec(self.Q, S0, acc, wl.host_cache_locs, self.dbl, wl.resident_pages,
                                    self.host, self.dev)
-        for r in range(wl.R):
-            for j in range(int(acc[r])):
-                t = int(self.S0[r]) + j
-                h = int(wl.host_cache_locs[r, t])
-                for layer in range(wl.L):
-                    assert np.array_equal(self.host[layer][h * wl.B:(h + 1) * wl.B], wl.rows(layer, r, [t])[0])
+        if check:
+            for r in range(wl.R):
+                for j in range(int(acc[r])):
+                    t = int(S0[r]) + j
+                    h = int(wl.host_cache_locs[r, t])
+                    for layer in range(wl.L):
+                        assert np.array_equal(self.host[layer][h * wl.B:(h + 1) * wl.B], wl.rows(layer, r, [t])[0])
         self.S0 = self.S0 + acc
-        return err
+        return acc, S0, err
 
 
-def _spec_workload(name):
-    """A small workload with room for six batches of up to four accepted positions."""
+def _spec_workload(name, steps=40):
+    """A small workload with room for `steps` accepted positions per request (default: six
+    batches of up to four)."""
     from test_oracle_pins import SMALL
     kw = dict(SMALL[name])
     base = kw.pop("base", name)
-    kw["steps"] = 40
+    kw["steps"] = steps
     return W.make(base, 12, **kw)
 
 
@@ -192,7 +215,7 @@ def test_replayable_plans(name, Q):
         tk, out, miss, err = run.batch()
         assert err == 0
         assert not _overwrites(run, tk, out), "a verify step reused a row an earlier step of its batch resolved"
-        assert run.accept() == 0
+        assert run.accept()[2] == 0
 
 
 def test_too_small_a_buffer_breaks_replay():
