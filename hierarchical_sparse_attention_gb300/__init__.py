@@ -29,7 +29,7 @@ HS_MAX_TOP_K, HS_MAX_HOT_SLOTS, HS_MAX_LAYERS = 4096, 16384, 8
 EXPORTS = ("hs_workspace_bytes", "hs_create", "hs_resolve", "hs_backup", "hs_get_error", "hs_destroy",
            "hs_status_str", "hs_host_register", "hs_host_unregister", "hs_resolve_noalloc",
            "hs_invalidate_tokens", "hs_invalidate_host_rows", "hs_resolve_layers", "hs_gather",
-           "hs_resolve_spec", "hs_backup_spec")
+           "hs_resolve_spec", "hs_backup_spec", "hs_reset_hints")
 HS_MAX_SPEC_QUERIES = 8
 HS_NOALLOC_MAX_LAYERS = 8
 
@@ -63,6 +63,8 @@ def _load() -> ctypes.CDLL:
     lib.hs_resolve_layers.argtypes = [P, i32] + [P] * 10 + [i32, P]
     lib.hs_resolve_layers.restype = ctypes.c_int
     lib.hs_gather.argtypes = [P, i32, P, i32, i32, P]
+    lib.hs_reset_hints.argtypes = [P, P]
+    lib.hs_reset_hints.restype = ctypes.c_int
     lib.hs_resolve_spec.argtypes = [P, i32, i32] + [P] * 10 + [P]
     lib.hs_resolve_spec.restype = ctypes.c_int
     lib.hs_backup_spec.argtypes = [P, i32, i32] + [P] * 5 + [P]
@@ -226,6 +228,10 @@ def hs_invalidate_host_rows(h: Handle, num_requests: int, seq_lens, host_cache_l
     _check(_lib.hs_invalidate_host_rows(h.ptr if h else None, num_requests, _addr(seq_lens), _addr(host_cache_locs),
                                         _addr(rows), n, _addr(device_buffer_tokens), _addr(lru_slots),
                                         _stream(stream)), "hs_invalidate_host_rows")
+
+
+def hs_reset_hints(h: Handle, stream=None) -> None:
+    _check(_lib.hs_reset_hints(h.ptr if h else None, _stream(stream)), "hs_reset_hints")
 
 
 def hs_get_error(h: Handle, clear: bool = False) -> int:

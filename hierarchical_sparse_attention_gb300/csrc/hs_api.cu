@@ -264,6 +264,16 @@ hs_status hs_invalidate_host_rows(hs_handle* h, int32_t num_requests, const int3
   return HS_OK;
 }
 
+hs_status hs_reset_hints(hs_handle* h, hs_stream_t stream) {
+  if (!h) return HS_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(h->hint, 0xFF, hs::hint_bytes(h->cfg.max_requests, h->cfg.max_context),
+                      (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  return HS_OK;
+}
+
 hs_status hs_get_error(hs_handle* h, uint32_t* flags, int clear) {
   if (!h || !flags) return HS_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;

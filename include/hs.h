@@ -273,6 +273,13 @@ HS_API hs_status hs_invalidate_host_rows(hs_handle* h, int32_t num_requests, con
                                          int32_t* device_buffer_tokens, int32_t* lru_slots,
                                          hs_stream_t stream);
 
+/* Forget every token -> slot hint (the table becomes -1, as hs_create leaves it), in stream
+ * order. Call it after changing device_buffer_tokens outside the library -- a request row
+ * handed to a new sequence, a restored checkpoint -- so the copy CTAs' miss predictions
+ * match the new state again. Results never depend on it: stale hints cost only speed. One
+ * cudaMemsetAsync of max_requests x max_context x 2 bytes; graph-capturable. */
+HS_API hs_status hs_reset_hints(hs_handle* h, hs_stream_t stream);
+
 /* Read the workspace error word (synchronises the device; not for the hot path). With
  * clear != 0 the word is reset to zero. Returns HS_ERR_DEVICE_FLAGGED when any bit is set. */
 HS_API hs_status hs_get_error(hs_handle* h, uint32_t* flags, int clear);

@@ -255,3 +255,21 @@ def test_stale_or_garbage_hints_do_not_change_results(pair):
     gpu.clk[0] = 0
     for s in range(4, 8):
         assert step_both(wl, orc, gpu, s) == 0
+
+
+def test_reset_hints_after_state_change(pair):
+    """hs_reset_hints empties the hint table (every entry -1, as hs_create leaves it) in stream
+    order; later steps stay exact and refill it."""
+    import hierarchical_sparse_attention_gb300 as hs
+    wl, orc, gpu = pair
+    warm(wl, orc, gpu)
+    n = wl.R * wl.max_context
+    hints = gpu.ws[256: 256 + 2 * n].view(torch.int16)
+    assert int((hints != -1).sum().item()) > 0  # the warm steps wrote hints
+    gpu.ws.view(torch.int16)[128: 128 + n].fill_(1234)
+    hs.hs_reset_hints(gpu.h)
+    torch.cuda.synchronize()
+    assert bool((hints == -1).all().item())
+    for s in range(3, 6):
+        assert step_both(wl, orc, gpu, s) == 0
+    assert int((hints != -1).sum().item()) > 0
