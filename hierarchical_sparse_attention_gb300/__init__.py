@@ -23,13 +23,16 @@ LIB_PATH = os.path.join(_HERE, "libhs.so")
 HS_OK, HS_ERR_INVALID_ARG, HS_ERR_INVALID_CONFIG, HS_ERR_CUDA, HS_ERR_DEVICE_FLAGGED, HS_ERR_TIMEOUT = range(6)
 HS_FLAG_TOKEN, HS_FLAG_DUP, HS_FLAG_STATE, HS_FLAG_HOSTROW, HS_FLAG_DEVROW, HS_FLAG_SEQLEN = 1, 2, 4, 8, 16, 32
 HS_FLAG_ORDER = 64
+HS_FLAG_TIMEOUT = 128
+HS_MAX_MLA_SPLITS = 16
 HS_MAX_TOP_K, HS_MAX_HOT_SLOTS, HS_MAX_LAYERS = 4096, 16384, 8
 
 # Every symbol include/hs.h declares (checked against the library by the tests).
 EXPORTS = ("hs_workspace_bytes", "hs_create", "hs_resolve", "hs_backup", "hs_get_error", "hs_destroy",
            "hs_status_str", "hs_host_register", "hs_host_unregister", "hs_resolve_noalloc",
            "hs_invalidate_tokens", "hs_invalidate_host_rows", "hs_resolve_layers", "hs_gather",
-           "hs_resolve_spec", "hs_backup_spec", "hs_reset_hints")
+           "hs_resolve_spec", "hs_backup_spec", "hs_reset_hints", "hs_sparse_mla_workspace_bytes",
+           "hs_sparse_mla_decode")
 HS_MAX_SPEC_QUERIES = 8
 HS_NOALLOC_MAX_LAYERS = 8
 
@@ -63,6 +66,10 @@ def _load() -> ctypes.CDLL:
     lib.hs_resolve_layers.argtypes = [P, i32] + [P] * 10 + [i32, P]
     lib.hs_resolve_layers.restype = ctypes.c_int
     lib.hs_gather.argtypes = [P, i32, P, i32, i32, P]
+    lib.hs_sparse_mla_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.hs_sparse_mla_workspace_bytes.restype = sz
+    lib.hs_sparse_mla_decode.argtypes = [i32, i32, i32, i32, P, P, i64, P, ctypes.c_float, P, P, P, sz, P, P]
+    lib.hs_sparse_mla_decode.restype = ctypes.c_int
     lib.hs_reset_hints.argtypes = [P, P]
     lib.hs_reset_hints.restype = ctypes.c_int
     lib.hs_resolve_spec.argtypes = [P, i32, i32] + [P] * 10 + [P]
@@ -228,6 +235,18 @@ def hs_invalidate_host_rows(h: Handle, num_requests: int, seq_lens, host_cache_l
     _check(_lib.hs_invalidate_host_rows(h.ptr if h else None, num_requests, _addr(seq_lens), _addr(host_cache_locs),
                                         _addr(rows), n, _addr(device_buffer_tokens), _addr(lru_slots),
                                         _stream(stream)), "hs_invalidate_host_rows")
+
+
+def hs_sparse_mla_workspace_bytes(num_requests: int, num_heads: int, splits: int) -> int:
+    return int(_lib.hs_sparse_mla_workspace_bytes(num_requests, num_heads, splits))
+
+
+def hs_sparse_mla_decode(num_requests: int, num_heads: int, top_k: int, splits: int, q, kv_pool, pool_rows: int,
+                         out_rows, sm_scale: float, o, lse, workspace, workspace_bytes: int, error_flags,
+                         stream=None) -> None:
+    _check(_lib.hs_sparse_mla_decode(num_requests, num_heads, top_k, splits, _addr(q), _addr(kv_pool), pool_rows,
+                                     _addr(out_rows), float(sm_scale), _addr(o), _addr(lse), _addr(workspace),
+                                     workspace_bytes, _addr(error_flags), _stream(stream)), "hs_sparse_mla_decode")
 
 
 def hs_reset_hints(h: Handle, stream=None) -> None:

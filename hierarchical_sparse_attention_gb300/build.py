@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "hs")
 LIB = os.path.join(PKG, "libhs.so")
-SOURCES = ["hs_resolve.cu", "hs_backup.cu", "hs_gather.cu", "hs_invalidate.cu", "hs_api.cu", "hs_noalloc.cu"]
+SOURCES = ["hs_resolve.cu", "hs_backup.cu", "hs_gather.cu", "hs_invalidate.cu", "hs_sparse_mla.cu", "hs_api.cu", "hs_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-I", INCLUDE, "-I", CSRC]

@@ -264,6 +264,36 @@ hs_status hs_invalidate_host_rows(hs_handle* h, int32_t num_requests, const int3
   return HS_OK;
 }
 
+size_t hs_sparse_mla_workspace_bytes(int32_t num_requests, int32_t num_heads, int32_t splits) {
+  if (num_requests < 1 || num_heads < 1 || num_heads > 128 || splits < 1 || splits > HS_MAX_MLA_SPLITS) return 0;
+  if (splits == 1) return 0;
+  const size_t rows = (size_t)splits * num_requests * num_heads;
+  return rows * 512 * sizeof(float) + rows * sizeof(float);
+}
+
+hs_status hs_sparse_mla_decode(int32_t num_requests, int32_t num_heads, int32_t top_k, int32_t splits,
+                               const uint16_t* q, const uint8_t* kv_pool, int64_t pool_rows,
+                               const int32_t* out_rows, float sm_scale, float* o, float* lse, void* workspace,
+                               size_t workspace_bytes, uint32_t* error_flags, hs_stream_t stream) {
+  if (num_requests < 0 || num_heads < 1 || num_heads > 128 || top_k < 1 || splits < 1 ||
+      splits > HS_MAX_MLA_SPLITS || pool_rows < 1)
+    return HS_ERR_INVALID_ARG;
+  if (num_requests == 0) return HS_OK;
+  if (!q || !kv_pool || !out_rows || !o || !lse || !error_flags) return HS_ERR_INVALID_ARG;
+  if (((uintptr_t)q % 16) || ((uintptr_t)kv_pool % 16) || ((uintptr_t)o % 16)) return HS_ERR_INVALID_ARG;
+  const size_t need = hs_sparse_mla_workspace_bytes(num_requests, num_heads, splits);
+  if (need > 0 && (!workspace || workspace_bytes < need || ((uintptr_t)workspace % 16))) return HS_ERR_INVALID_ARG;
+  const size_t rows = (size_t)splits * num_requests * num_heads;
+  float* part_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  float* part_lse = splits > 1 ? part_o + rows * 512 : nullptr;
+  hs::SparseMlaArgs a{q, kv_pool, pool_rows, out_rows, top_k, num_heads, splits, sm_scale, o, lse};
+  if (hs::launch_sparse_mla(a, num_requests, part_o, part_lse, error_flags, (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  return HS_OK;
+}
+
 hs_status hs_reset_hints(hs_handle* h, hs_stream_t stream) {
   if (!h) return HS_ERR_INVALID_ARG;
   if (cudaMemsetAsync(h->hint, 0xFF, hs::hint_bytes(h->cfg.max_requests, h->cfg.max_context),

@@ -96,6 +96,17 @@ struct InvalidateRowsArgs {
   int32_t* lru_slots;
 };
 
+struct SparseMlaArgs {
+  const uint16_t* q;      // [R, num_heads, 576] bf16
+  const uint8_t* kv_pool; // [pool_rows, 656] fp8 MLA rows
+  int64_t pool_rows;
+  const int32_t* out_rows;  // [R, top_k], -1: none
+  int32_t top_k, num_heads, splits;
+  float sm_scale;
+  float* o;    // [R, num_heads, 512]
+  float* lse;  // [R, num_heads]
+};
+
 // Workspace layout (device memory owned by the caller).
 constexpr size_t kErrOffset = 0;     // uint32 sticky HS_FLAG_* word
 constexpr size_t kPoolsOffset = 64;  // Pools table
@@ -129,6 +140,9 @@ cudaError_t launch_backup(const Geometry& g, const Pools* pools, const BackupArg
                           uint32_t* err_word, cudaStream_t stream);
 cudaError_t launch_gather(const Geometry& g, const Pools* pools, const GatherArgs& a, int32_t num_requests,
                           uint32_t* err_word, cudaStream_t stream);
+size_t sparse_mla_smem_bytes();
+cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, float* part_o, float* part_lse,
+                              uint32_t* err, cudaStream_t stream);
 cudaError_t launch_invalidate_tokens(const Geometry& g, const InvalidateArgs& a, int32_t num_requests,
                                      uint32_t* err_word, cudaStream_t stream);
 cudaError_t launch_invalidate_host_rows(const Geometry& g, const InvalidateRowsArgs& a, int32_t num_requests,

@@ -1,0 +1,373 @@
+// Synthetic consumer of the resolver's row table: sparse-MLA decode attention on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// Sources (page title, section): "vLLM Hybrid HiSparse source implementation analysis", 7.3
+// (the sparse attention kernel reads the pool's flat view through the table of physical
+// rows) and 9 (an fp8 sparse-MLA row: 512 B of e4m3 latent, 16 B of four fp32 scales, 128 B
+// of bf16 RoPE); "HiSparse: Turbocharging Sparse Attention with Hierarchical Memory" (decode
+// attention only over the top-k positions, through the sparse MLA backend).
+//
+// Per request r and query head h over the valid rows j of out_rows[r]:
+//   s[h, j] = sm_scale * (q[h, :512] . latent_j + q[h, 512:] . rope_j), latent_j = e4m3 x scale
+//   o[h]    = softmax_j(s[h]) . latent,   lse[h] = log sum_j exp s[h, j]
+// (MLA decode with the absorbed projection: keys are the 576-dim rows, values their latent.)
+//
+// Layout of the work: a CTA of 128 threads takes (request r, half u of the 512 value dims,
+// split p of the rows); thread t owns head t (tensor-memory lane t). The request's Q, 128 x 576
+// bf16, sits in shared memory in the 128-byte-swizzled K-major layout (144 KB). The rows are
+// taken 32 at a time: their 656-B records are gathered through the row table with cp.async
+// (the next block's as soon as this one's are dequantised), dequantised to bf16 (e4m3 -> f16 in hardware,
+// times the row's scale) into a swizzled tile, S = Q . K^T is 36 MMAs of M 128, N 32, K 16
+// into tensor memory, the online softmax runs in registers (one head per thread), P goes
+// back to shared memory as bf16, and O += P . V is two MMAs of N 256 reading the same tile's
+// latent part as an MN-major operand. O (128 x 256 fp32) stays in tensor memory and is
+// rescaled there only when a head's running maximum grows. With more than one split a small
+// kernel merges the splits by their log-sum-exp.
+#include "hs_internal.h"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace hs {
+namespace {
+
+constexpr int T = 128;           // threads: one per head
+constexpr int MH = 128;          // MMA M: heads (padded with zero rows)
+constexpr int BJ = 32;           // rows per block (MMA N of S, K of P . V)
+constexpr int DQK = 576, DL = 512, ROWB = 656;
+constexpr int ATOMS = DQK / 64;  // 9 swizzle atoms of 64 bf16 along the 576 dims
+constexpr int HALF = DL / 2;     // value dims per CTA
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL = 0, O_COL = 256;
+
+// shared memory carve-up (offsets from a 1024-B aligned base)
+constexpr uint32_t SQ = 0;                               // 9 atoms x 128 rows x 128 B
+constexpr uint32_t SKV = SQ + ATOMS * MH * 128;          // 9 atoms x 32 rows x 128 B
+constexpr uint32_t SP = SKV + ATOMS * BJ * 128;          // 128 rows x 128 B (P, K-major, 32 of 64 used)
+constexpr uint32_t SRAW = SP + MH * 128;                 // 32 raw records
+constexpr uint32_t SVALID = SRAW + BJ * ROWB;            // 2 x 32 int (per block parity)
+constexpr uint32_t SMEM_USED = SVALID + 2 * BJ * 4;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;        // + alignment slack
+constexpr uint64_t kWaitNs = 100000000ull;               // 100 ms bound on an mbarrier wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Byte offset of (row, k) in a K-major tile whose rows are 128 B (64 bf16), swizzled in
+// 8-row groups of 1024 B: the 16-B chunk index is XOR-ed with row % 8.
+__device__ __forceinline__ uint32_t sw128(int row, int k) {
+  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((((k * 2) >> 4) ^ (row & 7)) << 4) + ((k * 2) & 15));
+}
+
+// Shared-memory matrix descriptor: start, leading / stride byte offsets, 128-B swizzle.
+__device__ __forceinline__ uint64_t mdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major, B K- or
+// MN-major, N and M.
+__host__ __device__ constexpr uint32_t idesc(int n, int m, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ uint64_t gtime() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for a phase of an mbarrier; false when the bound ran out.
+__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = gtime();
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (gtime() - t0 > kWaitNs) return false;
+  }
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Two e4m3 codes (low byte first) to two floats, exactly (e4m3 is a subset of f16).
+__device__ __forceinline__ float2 e4m3x2(uint16_t codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tmov.b16 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "h"(codes));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// Issue the cp.async gather of block b's raw records and mark its rows (flags by parity).
+__device__ __forceinline__ void gather_block(const SparseMlaArgs& a, int r, int j_begin, int j_end, int b,
+                                             uint8_t* base) {
+  uint8_t* raw = base + SRAW;
+  int32_t* valid = reinterpret_cast<int32_t*>(base + SVALID) + (b & 1) * BJ;
+  const int j0 = j_begin + b * BJ;
+  for (int c = threadIdx.x; c < BJ * (ROWB / 16); c += T) {
+    const int row = c / (ROWB / 16), q = c - row * (ROWB / 16);
+    const int j = j0 + row;
+    const int32_t pr = j < j_end ? a.out_rows[(size_t)r * a.top_k + j] : -1;
+    const bool ok = pr >= 0 && (int64_t)pr < a.pool_rows;
+    if (q == 0) valid[row] = ok;
+    if (ok) cp16(smem_u32(raw + row * ROWB + q * 16), a.kv_pool + (size_t)pr * ROWB + q * 16);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a, float* __restrict__ part_o,
+                                                          float* __restrict__ part_lse, uint32_t* __restrict__ err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ uint32_t s_taddr;
+  __shared__ __align__(8) uint64_t s_bar_s, s_bar_o;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int r = blockIdx.x, u = blockIdx.y, p = blockIdx.z;
+  const int per = (a.top_k + a.splits - 1) / a.splits;
+  const int j_begin = p * per, j_end = min(a.top_k, j_begin + per);
+  const int nblk = j_end > j_begin ? (j_end - j_begin + BJ - 1) / BJ : 0;
+
+  // Q of request r into the swizzled K-major tile (zero rows past the last head)
+  for (int c = tid; c < MH * (DQK / 8); c += T) {
+    const int h = c / (DQK / 8), ch = c - h * (DQK / 8), d = ch * 8;
+    uint8_t* dst = base + SQ + (d >> 6) * (MH * 128) + sw128(h, d & 63);
+    if (h < a.num_heads) cp16(smem_u32(dst), a.q + ((size_t)r * a.num_heads + h) * DQK + d);
+    else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  if (nblk > 0) gather_block(a, r, j_begin, j_end, 0, base);
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar_s)) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar_o)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_taddr)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  const uint32_t tbase = s_taddr;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's tensor-memory lanes
+  const float sl2 = a.sm_scale * 1.4426950408889634f;      // scores in log2 units
+  float m_run = -INFINITY, l_run = 0.f;
+  bool ok = true;
+
+  for (int b = 0; b < nblk; ++b) {
+    const int buf = b & 1;
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // this block's records have landed
+    // the tile is free once the previous block's P . V has read it; a wait that ran out
+    // ends the loop for the whole CTA
+    if (b > 0 && !bar_wait(&s_bar_o, (b - 1) & 1)) ok = false;
+    if (!__syncthreads_and(ok)) break;
+    // dequantise: latent = e4m3 x scale -> bf16, RoPE copied; invalid rows are zero
+    {
+      const uint8_t* raw = base + SRAW;
+      const int32_t* valid = reinterpret_cast<const int32_t*>(base + SVALID) + buf * BJ;
+      for (int c = tid; c < BJ * (DQK / 2); c += T) {
+        const int row = c / (DQK / 2), d = (c - row * (DQK / 2)) * 2;
+        uint32_t packed = 0u;
+        if (valid[row]) {
+          const uint8_t* rec = raw + row * ROWB;
+          if (d < DL) {
+            const float sc = reinterpret_cast<const float*>(rec + DL)[d >> 7];
+            const float2 v = e4m3x2(*reinterpret_cast<const uint16_t*>(rec + d));
+            const __nv_bfloat162 bv = __floats2bfloat162_rn(v.x * sc, v.y * sc);
+            packed = *reinterpret_cast<const uint32_t*>(&bv);
+          } else {
+            packed = *reinterpret_cast<const uint32_t*>(rec + DL + 16 + 2 * (d - DL));
+          }
+        }
+        *reinterpret_cast<uint32_t*>(base + SKV + (d >> 6) * (BJ * 128) + sw128(row, d & 63)) = packed;
+      }
+    }
+    fence_async_smem();
+    tc_before();
+    __syncthreads();
+    tc_after();
+    // the raw buffer is consumed: the next block's records go out under this block's math
+    if (b + 1 < nblk) gather_block(a, r, j_begin, j_end, b + 1, base);
+    if (tid == 0) {  // S = Q . K^T: 9 atoms x 4 steps of K 16
+      for (int kk = 0; kk < ATOMS * 4; ++kk) {
+        const int at = kk >> 2, w = kk & 3;
+        mma(tbase + S_COL, mdesc(smem_u32(base + SQ + at * (MH * 128) + w * 32), 16, 1024),
+            mdesc(smem_u32(base + SKV + at * (BJ * 128) + w * 32), 16, 1024), idesc(BJ, MH, false), kk > 0);
+      }
+      commit(&s_bar_s);
+    }
+    if (!bar_wait(&s_bar_s, b & 1)) ok = false;
+    if (!__syncthreads_and(ok)) break;
+    tc_after();
+    // online softmax for head tid over this block's 32 rows
+    float s[BJ];
+    {
+      float t0[16], t1[16];
+      tmem_ld16(tbase + lane_off + S_COL, t0);
+      tmem_ld16(tbase + lane_off + S_COL + 16, t1);
+      const int32_t* valid = reinterpret_cast<const int32_t*>(base + SVALID) + buf * BJ;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        s[j] = valid[j] ? t0[j] * sl2 : -INFINITY;
+        s[16 + j] = valid[16 + j] ? t1[j] * sl2 : -INFINITY;
+      }
+    }
+    float bm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < BJ; ++j) bm = fmaxf(bm, s[j]);
+    const float m_new = fmaxf(m_run, bm);
+    const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);  // m_run = -inf: O is still 0
+    float psum = 0.f;
+    uint32_t pk[BJ / 2];
+#pragma unroll
+    for (int j = 0; j < BJ; j += 2) {
+      const float p0 = m_new == -INFINITY ? 0.f : exp2f(s[j] - m_new);
+      const float p1 = m_new == -INFINITY ? 0.f : exp2f(s[j + 1] - m_new);
+      const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+      psum += __low2float(pb) + __high2float(pb);  // the normaliser sums what P . V uses
+      pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+    }
+    l_run = l_run * alpha + psum;
+    m_run = m_new;
+#pragma unroll
+    for (int j = 0; j < BJ; j += 2)
+      *reinterpret_cast<uint32_t*>(base + SP + sw128(tid, j)) = pk[j >> 1];
+    // rescale O where a running maximum grew (the previous P . V is complete: waited above)
+    if (b > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      for (int c = 0; c < HALF; c += 16) {
+        float v[16];
+        tmem_ld16(tbase + lane_off + O_COL + c, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= alpha;
+        tmem_st16(tbase + lane_off + O_COL + c, v);
+      }
+    }
+    fence_async_smem();
+    tc_before();
+    __syncthreads();
+    tc_after();
+    if (tid == 0) {  // O += P . V over the block's 32 rows: 2 steps of K 16, N = this half's 256 dims
+      for (int kk = 0; kk < BJ / 16; ++kk)
+        mma(tbase + O_COL, mdesc(smem_u32(base + SP + kk * 32), 16, 1024),
+            mdesc(smem_u32(base + SKV + (u * (HALF / 64)) * (BJ * 128) + kk * 2048), BJ * 128, 1024),
+            idesc(HALF, MH, true), (b > 0 || kk > 0) ? 1u : 0u);
+      commit(&s_bar_o);
+    }
+  }
+  if (ok && nblk > 0 && !bar_wait(&s_bar_o, (nblk - 1) & 1)) ok = false;
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  ok = __syncthreads_and(ok);
+  tc_after();
+  if (!ok) {  // outputs are not valid: flag it and leave them alone
+    if (tid == 0) atomicOr(err, HS_FLAG_TIMEOUT);
+    tc_before();
+    __syncthreads();
+    if (warp == 0)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS) : "memory");
+    return;
+  }
+  // write this split's normalised output and log-sum-exp for head tid
+  const bool live = tid < a.num_heads;
+  const size_t row_out = (((size_t)p * gridDim.x + r) * a.num_heads + tid);  // [split][r][h]
+  const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+  for (int c = 0; c < HALF; c += 16) {
+    float v[16];
+    if (nblk > 0) {
+      tmem_ld16(tbase + lane_off + O_COL + c, v);
+    } else {
+      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    }
+    if (live) {
+      float* dst = part_o + row_out * DL + u * HALF + c;
+#pragma unroll
+      for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
+    }
+  }
+  if (live && u == 0) part_lse[row_out] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+  tc_before();
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS) : "memory");
+}
+
+// Merge the splits of each (request, head): weights exp(lse_p - lse), lse = log sum exp lse_p.
+__global__ void __launch_bounds__(T) combine_kernel(const SparseMlaArgs a, const float* __restrict__ part_o,
+                                                    const float* __restrict__ part_lse) {
+  const int rh = blockIdx.x;  // r * num_heads + h
+  const int R = gridDim.x / a.num_heads;
+  const size_t stride = (size_t)R * a.num_heads;
+  float mx = -INFINITY;
+  for (int p = 0; p < a.splits; ++p) mx = fmaxf(mx, part_lse[p * stride + rh]);
+  float z = 0.f;
+  for (int p = 0; p < a.splits; ++p) z += mx == -INFINITY ? 0.f : expf(part_lse[p * stride + rh] - mx);
+  for (int d = threadIdx.x; d < DL; d += T) {
+    float acc = 0.f;
+    for (int p = 0; p < a.splits; ++p) {
+      const float w = mx == -INFINITY ? 0.f : expf(part_lse[p * stride + rh] - mx) / z;
+      acc += w * part_o[(p * stride + rh) * DL + d];
+    }
+    a.o[(size_t)rh * DL + d] = acc;
+  }
+  if (threadIdx.x == 0) a.lse[rh] = mx == -INFINITY ? -INFINITY : mx + logf(z);
+}
+
+}  // namespace
+
+static_assert(SMEM_BYTES <= 227 * 1024, "the consumer's shared memory exceeds a CTA's limit");
+
+size_t sparse_mla_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, float* part_o, float* part_lse,
+                              uint32_t* err, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const bool direct = a.splits == 1;
+  sparse_mla_kernel<<<dim3(num_requests, 2, a.splits), T, SMEM_BYTES, stream>>>(
+      a, direct ? a.o : part_o, direct ? a.lse : part_lse, err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || direct) return e;
+  combine_kernel<<<num_requests * a.num_heads, T, 0, stream>>>(a, part_o, part_lse);
+  return cudaGetLastError();
+}
+
+}  // namespace hs

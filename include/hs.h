@@ -118,12 +118,14 @@ typedef enum {
 #define HS_FLAG_DEVROW 16u /* device row out of range: output -1, nothing written */
 #define HS_FLAG_SEQLEN 32u /* seq_len outside [0, max_context]: request skipped */
 #define HS_FLAG_ORDER 64u  /* hs_invalidate_host_rows: rows not ascending, nothing cleared */
+#define HS_FLAG_TIMEOUT 128u /* a bounded device wait ran out: that call's outputs are invalid */
 
 /* Limits of this build. */
 #define HS_MAX_TOP_K 4096
 #define HS_MAX_HOT_SLOTS 16384
 #define HS_MAX_LAYERS 8
 #define HS_MAX_SPEC_QUERIES 8 /* verify steps of one speculative batch (n_spec + 1) */
+#define HS_MAX_MLA_SPLITS 16  /* row splits of hs_sparse_mla_decode */
 
 /* Configuration of one layer group (layers that share one indexer top-k and therefore
  * one slot map; "vLLM Hybrid HiSparse source implementation analysis" 7.4).
@@ -272,6 +274,30 @@ HS_API hs_status hs_invalidate_host_rows(hs_handle* h, int32_t num_requests, con
                                          const int32_t* host_cache_locs, const int32_t* rows, int32_t n,
                                          int32_t* device_buffer_tokens, int32_t* lru_slots,
                                          hs_stream_t stream);
+
+/* Synthetic consumer of the row table: sparse-MLA decode attention ("vLLM Hybrid HiSparse
+ * source implementation analysis", 7.3: the sparse attention kernel reads the pool's flat view
+ * through the resolver's physical rows; 9: an fp8 sparse-MLA row is 656 B -- 512 e4m3 latent
+ * codes, 4 fp32 scales (one per 128 codes), 64 bf16 RoPE values). For request r and head h
+ * over the rows j = out_rows[r][i] >= 0:
+ *   s[h, j] = sm_scale * (q[h, :512] . latent_j + q[h, 512:] . rope_j), latent = e4m3 x scale
+ *   o[r, h] = softmax_j(s[h]) . latent,  lse[r, h] = log sum_j exp s[h, j]  (-inf, o = 0 if none)
+ * Computed on the tensor cores in bf16 (latent and P rounded to bf16) with fp32 accumulation
+ * and an online softmax; `splits` (1..HS_MAX_MLA_SPLITS) divides each request's rows over more
+ * CTAs, merged by log-sum-exp in a second kernel.
+ *   q        [R, num_heads, 576] bf16 bits, device, 16-byte aligned (num_heads <= 128)
+ *   kv_pool  [pool_rows, 656] bytes, device (a layer's device pool), 16-byte aligned
+ *   out_rows [R, top_k] device (hs_resolve's output); rows outside the pool count as -1
+ *   o        [R, num_heads, 512] fp32, device, 16-byte aligned; lse [R, num_heads] fp32, device
+ *   workspace: hs_sparse_mla_workspace_bytes(R, num_heads, splits) device bytes (0 for one split)
+ *   error_flags: device uint32, HS_FLAG_TIMEOUT OR-ed in if a bounded wait ran out.
+ * Two kernel launches at most; no allocation, no synchronisation; graph-capturable. */
+HS_API size_t hs_sparse_mla_workspace_bytes(int32_t num_requests, int32_t num_heads, int32_t splits);
+HS_API hs_status hs_sparse_mla_decode(int32_t num_requests, int32_t num_heads, int32_t top_k, int32_t splits,
+                                      const uint16_t* q, const uint8_t* kv_pool, int64_t pool_rows,
+                                      const int32_t* out_rows, float sm_scale, float* o, float* lse,
+                                      void* workspace, size_t workspace_bytes, uint32_t* error_flags,
+                                      hs_stream_t stream);
 
 /* Forget every token -> slot hint (the table becomes -1, as hs_create leaves it), in stream
  * order. Call it after changing device_buffer_tokens outside the library -- a request row

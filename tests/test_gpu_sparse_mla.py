@@ -1,0 +1,171 @@
+"""GPU parity of the synthetic consumer (hs_sparse_mla_decode: sparse-MLA decode attention over
+the resolver's row table, on the tcgen05 tensor cores) against the oracle.
+
+Two comparisons per output:
+* tight: against the oracle's formula evaluated in the kernel's precision (latent rounded to
+  bf16 after the fp32 scale, P rounded to bf16 before the product). The kernel rounds P against
+  each block's running maximum, the model against the final one, so each weight may round
+  differently by 2^-9: |d o| <= 2^-9 * max|v_j - o| <= 2^-8 * max|latent|; with fp32
+  accumulation and exp2 on top, the test allows 6e-3 * max|latent| per element;
+* rigorous: against the exact oracle (float64), a first-order bound of the bf16 rounding:
+  |d o_i| <= 2 * max_j |v_ji| * (3 u + 4 E), u = 2^-9, E = max_j sm_scale * u * sum_d |q_d v_jd|
+  (score error from rounding v; the factor 2 covers second-order terms), and |d lse| <= 2 E + 4 u.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads as W  # noqa: E402
+from oracle import sparse_mla as M  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+U = 2.0 ** -9
+
+
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import hierarchical_sparse_attention_gb300 as hs
+    return hs
+
+
+def _bf16(x):
+    f = x.astype(np.float32).view(np.uint32).astype(np.uint64)
+    f = ((f + 0x7FFF + ((f >> 16) & 1)) >> 16) << 16
+    return f.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def model(q_bits, pool, out_rows, sm_scale):
+    """The oracle's formula in the kernel's precision (see the module docstring)."""
+    R, Hq, _ = q_bits.shape
+    q = M.bf16_decode(q_bits)
+    o = np.zeros((R, Hq, M.D_LATENT))
+    for r in range(R):
+        rows = out_rows[r][out_rows[r] >= 0].astype(np.int64)
+        if rows.size == 0:
+            continue
+        raw = pool.reshape(-1, M.ROW_BYTES)[rows]
+        sc = raw[:, 512:528].copy().view("<f4")
+        lat = _bf16((M.e4m3_decode(raw[:, :512]).astype(np.float32) * np.repeat(sc, 128, axis=1)).astype(np.float64))
+        rope = M.bf16_decode(raw[:, 528:].copy().view("<u2"))
+        s = sm_scale * (q[r, :, :512] @ lat.T + q[r, :, 512:] @ rope.T)
+        p = _bf16(np.exp(s - s.max(1, keepdims=True)))
+        o[r] = (p @ lat) / p.sum(1, keepdims=True)
+    return o
+
+
+def make_case(seed, R, Hq, K, pool_rows, masked=0.1, bad_rows=0):
+    wl = W.make("dsa", seed, requests=R, top_k=min(K, 2048), steps=2)
+    rng = np.random.default_rng(seed)
+    toks = rng.integers(0, 100000, size=pool_rows)
+    pool = np.concatenate([wl.rows(0, 0, [int(t)]) for t in toks]).reshape(-1).astype(np.uint8)
+    out_rows = rng.integers(0, pool_rows, size=(R, K)).astype(np.int32)
+    out_rows[rng.random((R, K)) < masked] = -1
+    if bad_rows:
+        out_rows[0, :bad_rows] = pool_rows + 5  # outside the pool: counted as -1
+    q = wl.queries_bf16(0, Hq)
+    # a scale that gives the synthetic scores about unit spread (uniform e4m3 codes make raw
+    # scores of order 1e3)
+    lat, rope = M.dequant_rows(pool, np.arange(min(pool_rows, 64)))
+    qq = M.bf16_decode(q[0])
+    raw = qq[:, :512] @ lat.T + qq[:, 512:] @ rope.T
+    sm_scale = float(np.float32(1.0 / raw.std()))
+    return q, pool, out_rows, sm_scale
+
+
+def run_gpu(hs, q, pool, out_rows, sm_scale, splits):
+    R, Hq, _ = q.shape
+    K = out_rows.shape[1]
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
+    g_q, g_pool, g_rows = d(q.view(np.int16)), d(pool), d(out_rows)
+    o = torch.full((R, Hq, 512), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((R, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    wsb = hs.hs_sparse_mla_workspace_bytes(R, Hq, splits)
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hs.hs_sparse_mla_decode(R, Hq, K, splits, g_q, g_pool, pool.size // 656, g_rows, sm_scale, o, lse, ws, wsb, err)
+    torch.cuda.synchronize()
+    return o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), int(err.item())
+
+
+def check(q, pool, out_rows, sm_scale, go, glse, what):
+    ro = out_rows.copy()
+    ro[(ro < 0) | (ro >= pool.size // 656)] = -1
+    o, lse = M.sparse_mla_decode(q, pool, ro, sm_scale)
+    mo = model(q, pool, ro, sm_scale)
+    qf = M.bf16_decode(q)
+    for r in range(q.shape[0]):
+        rows = ro[r][ro[r] >= 0].astype(np.int64)
+        if rows.size == 0:
+            assert np.all(go[r] == 0) and np.all(np.isneginf(glse[r])), f"{what}: empty request {r}"
+            continue
+        lat, _ = M.dequant_rows(pool, rows)
+        vmax = np.abs(lat).max(0)  # per value dim
+        E = sm_scale * U * (np.abs(qf[r, :, :512]) @ np.abs(lat).T).max(1)  # per head
+        tight = np.abs(go[r] - mo[r]).max()
+        assert tight <= 6e-3 * np.abs(lat).max(), f"{what}: request {r} differs from the precision model by {tight}"
+        bound = 2 * vmax[None, :] * (3 * U + 4 * E[:, None])
+        assert np.all(np.abs(go[r] - o[r]) <= bound + 1e-6), f"{what}: request {r} outside the rounding bound"
+        assert np.all(np.abs(glse[r] - lse[r]) <= 2 * E + 4 * U), f"{what}: request {r} lse"
+
+
+@pytest.mark.parametrize("R,Hq,K,splits", [(2, 128, 256, 1), (3, 128, 2048, 2), (2, 64, 100, 1), (1, 16, 333, 4),
+                                           (4, 128, 1024, 4)])
+def test_sparse_mla_matches_oracle(R, Hq, K, splits):
+    hs = _gpu()
+    q, pool, out_rows, sm = make_case(R * 7 + K, R, Hq, K, pool_rows=3000)
+    go, glse, err = run_gpu(hs, q, pool, out_rows, sm, splits)
+    assert err == 0
+    check(q, pool, out_rows, sm, go, glse, f"R{R} H{Hq} K{K} splits{splits}")
+
+
+def test_sparse_mla_masked_and_out_of_pool_rows():
+    hs = _gpu()
+    q, pool, out_rows, sm = make_case(5, 3, 128, 200, pool_rows=500, masked=0.5, bad_rows=17)
+    out_rows[2, :] = -1  # a request with no valid row: o = 0, lse = -inf
+    go, glse, err = run_gpu(hs, q, pool, out_rows, sm, 2)
+    assert err == 0
+    check(q, pool, out_rows, sm, go, glse, "masked")
+
+
+def test_sparse_mla_reads_the_resolvers_rows():
+    """The consumer over the row table and device pool a decode step of the resolver left."""
+    hs = _gpu()
+    from gpu_harness import GpuSim, host_pools
+    from harness import OracleSim, poison_host_newest
+    wl = W.make("dsa", 3, requests=3, top_k=512, hot_slots=1024, steps=4, seq0=(6000, 9000, 700))
+    host = host_pools(wl)
+    orc = OracleSim(wl, host_pools=host)
+    gpu = GpuSim(wl, host, orc.dev)
+    try:
+        for step in range(wl.steps):
+            gpu.write_newest(step)
+            orc.write_newest(step)
+            poison_host_newest(wl, step, host)
+            gpu.upload(step)
+            gpu.resolve()
+            gpu.backup()
+            orc.resolve(step)
+            orc.backup(step)
+        torch.cuda.synchronize()
+        assert np.array_equal(gpu.out.cpu().numpy(), orc.out)
+        q = wl.queries_bf16(wl.steps, 128)
+        pool = orc.dev[0]
+        lat, rope = M.dequant_rows(pool, orc.out[0][orc.out[0] >= 0][:64])
+        qq = M.bf16_decode(q[0])
+        sm = float(np.float32(1.0 / (qq[:, :512] @ lat.T + qq[:, 512:] @ rope.T).std()))
+        R, Hq, K = wl.R, 128, wl.K
+        o = torch.zeros((R, Hq, 512), dtype=torch.float32, device="cuda")
+        lse = torch.zeros((R, Hq), dtype=torch.float32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        wsb = hs.hs_sparse_mla_workspace_bytes(R, Hq, 2)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+        hs.hs_sparse_mla_decode(R, Hq, K, 2, torch.from_numpy(q.view(np.int16)).cuda(), gpu.dev[0], wl.device_rows,
+                                gpu.out, sm, o, lse, ws, wsb, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        check(q, pool, orc.out, sm, o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+              "after the resolver")
+    finally:
+        gpu.close()

@@ -463,6 +463,14 @@ class Workload:
             offs.append(offs[-1] + t.size)
         return np.array(offs, dtype=np.int32), np.concatenate(toks) if toks else np.zeros(0, np.int32)
 
+    def queries_bf16(self, step: int, heads: int, dims: int = 576) -> np.ndarray:
+        """Seeded decode queries [R, heads, dims] as bfloat16 bit patterns, ~N(0, 1) (round to
+        nearest even from float32)."""
+        rng = np.random.default_rng((self.seed, 0x51, step, heads))
+        x = rng.standard_normal((self.R, heads, dims)).astype(np.float32).view(np.uint32).astype(np.uint64)
+        x = (x + 0x7FFF + ((x >> 16) & 1)) >> 16
+        return x.astype(np.uint16)
+
     def initial_device_writes(self):
         """(requests, tokens, device rows) the caller writes before step 0: the fast-path
         buffer contents and the resident pages' rows (all tokens before the newest)."""
