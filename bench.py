@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--op", default="step",
-                    choices=["step", "invalidate_tokens", "invalidate_host_rows", "split", "spec"],
+                    choices=["step", "invalidate_tokens", "invalidate_host_rows", "split", "spec", "mla"],
                     help="step: the decode step (default); invalidate_*: one hot-slot invalidation call; "
                          "split: leader resolve + follower gathers on a copy stream vs the fused step")
     ap.add_argument("--sweep", action="store_true",
@@ -782,6 +782,100 @@ def run_split(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+MLA_HEADS = 128  # query heads per request on one GPU (attention data-parallel)
+
+
+def measured_bf16_peak(sustained: bool = False) -> float:
+    try:
+        d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(d.get("bf16_tflops_sustained" if sustained else "bf16_tflops", 1900.0))
+    except (OSError, ValueError):
+        return 1900.0
+
+
+def run_mla(args, ws, rank, local):
+    """The synthetic consumer alone: sparse-MLA decode attention (hs_sparse_mla_decode) over
+    a row table of the workload's shape -- each request's top_k distinct rows drawn from its
+    own part of the device pool (its hot buffer), MLA_HEADS query heads. Times each split
+    count (1, 2, 4) with L2 flushed between calls and reports the fastest as the line."""
+    import torch
+    import hierarchical_sparse_attention_gb300 as hs
+    import workloads as W
+    from collections import OrderedDict
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    wl = W.make(args.config, args.seed + 1000 * rank, steps=2)
+    R, K, H, B = wl.R, wl.K, wl.H, wl.B
+    assert B == 656, "the consumer reads fp8 MLA rows"
+    Hq = MLA_HEADS
+    rng = np.random.default_rng(args.seed + 5)
+    # the device pool holds real rows: each request's buffer rows carry some token's bytes
+    pool = np.empty(wl.device_rows * B, dtype=np.uint8)
+    for r in range(R):
+        toks = rng.integers(0, int(wl.seq0[r]) - 1, size=H + 1)
+        rows = wl.device_buffer_locs[r]
+        data = wl.rows(0, r, [int(t) for t in toks])
+        pool.reshape(-1, B)[rows] = data.reshape(-1, B)
+    out_rows = np.stack([rng.permutation(wl.device_buffer_locs[r][:H])[:K] for r in range(R)]).astype(np.int32)
+    q = wl.queries_bf16(0, Hq)
+    g_pool = torch.from_numpy(pool).to(dev)
+    g_rows = torch.from_numpy(out_rows).to(dev)
+    g_q = torch.from_numpy(q.view(np.int16)).to(dev)
+    o = torch.empty((R, Hq, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((R, Hq), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sm_scale = 1.0 / 1400.0  # about unit-spread scores on the synthetic fp8 rows
+    flops = 2.0 * R * Hq * K * (576 + 512)  # S = Q K^T and O = P V, algorithmic
+    bytes_alg = R * K * B + q.nbytes + o.numel() * 4 + lse.numel() * 4 + out_rows.nbytes
+    res = OrderedDict()
+    for splits in (1, 2, 4):
+        wsb = hs.hs_sparse_mla_workspace_bytes(R, Hq, splits)
+        wsp = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
+
+        def call():
+            hs.hs_sparse_mla_decode(R, Hq, K, splits, g_q, g_pool, wl.device_rows, g_rows, sm_scale, o, lse, wsp,
+                                    wsb, err, stream)
+
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        barrier(ws)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            call()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        ms = [e[0].elapsed_time(e[1]) for e in evs]
+        res[splits] = (max_over_ranks(sum(ms) / len(ms) * 1e-3, ws), float(np.median(ms)) * 1e3)
+    best = min(res, key=lambda k: res[k][0])
+    t = res[best][0]
+    peak = measured_bf16_peak()
+    line = {
+        "metric": "sparse-MLA decode attention over the row table (TFLOP/s)", "value": ws * flops / t / 1e12,
+        "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {R} requests x {Hq} heads x top_k {K} rows of {B} B (fp8 MLA), "
+                               f"576-dim keys, 512-dim values, splits {best}",
+                   "l2": "flushed between timed calls (256 MiB write)"},
+        "per_split_count_us": {str(k): {"mean": 1e6 * v[0], "p50": v[1]} for k, v in res.items()},
+        "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peak, "unit": "TFLOP/s",
+                     "frac": flops / t / 1e12 / peak, "traffic": None,
+                     "peak_source": "MEASURED_PEAKS.json bf16_tflops (of measured)",
+                     "hbm": {"achieved": bytes_alg / t / 1e9, "peak": measured_hbm_peak(), "unit": "GB/s",
+                             "algorithmic_bytes_per_launch": bytes_alg}},
+        "gpu_launches": args.steps * (1 if best == 1 else 2), "device_flags": int(err.item()),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 SPEC_QUERIES = 4  # n_spec = 3 draft tokens (MTP3) + the sampled one
 
 
@@ -909,6 +1003,8 @@ def main():
     ws, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.op == "mla":
+        run_mla(args, ws, rank, local)
     elif args.op == "spec":
         run_spec(args, ws, rank, local)
     elif args.op == "split":

@@ -12,8 +12,10 @@
 //   o[h]    = softmax_j(s[h]) . latent,   lse[h] = log sum_j exp s[h, j]
 // (MLA decode with the absorbed projection: keys are the 576-dim rows, values their latent.)
 //
-// Layout of the work: a CTA of 128 threads takes (request r, half u of the 512 value dims,
-// split p of the rows); thread t owns head t (tensor-memory lane t). The request's Q, 128 x 576
+// Layout of the work: a CTA of 512 threads takes (request r, half u of the 512 value dims,
+// split p of the rows). Every thread gathers and dequantises; thread t < 128 owns head t
+// (tensor-memory lane t) for the softmax, and the four warpgroups share the lanes by column
+// to rescale and read out O. The request's Q, 128 x 576
 // bf16, sits in shared memory in the 128-byte-swizzled K-major layout (144 KB). The rows are
 // taken 32 at a time: their 656-B records are gathered through the row table with cp.async
 // (the next block's as soon as this one's are dequantised), dequantised to bf16 (e4m3 -> f16 in hardware,
@@ -21,7 +23,8 @@
 // into tensor memory, the online softmax runs in registers (one head per thread), P goes
 // back to shared memory as bf16, and O += P . V is two MMAs of N 256 reading the same tile's
 // latent part as an MN-major operand. O (128 x 256 fp32) stays in tensor memory and is
-// rescaled there only when a head's running maximum grows. With more than one split a small
+// rescaled there only when a head's block maximum passes its reference maximum by more than
+// 2^8 (a lazy rescale: P is computed against the reference and stays below 2^8). With more than one split a small
 // kernel merges the splits by their log-sum-exp.
 #include "hs_internal.h"
 
@@ -31,7 +34,8 @@
 namespace hs {
 namespace {
 
-constexpr int T = 128;           // threads: one per head
+constexpr int T = 512;           // threads: four warpgroups; warpgroup 0 owns one head per thread
+constexpr int WG = T / 128;      // warpgroups sharing the tensor-memory lanes (by column)
 constexpr int MH = 128;          // MMA M: heads (padded with zero rows)
 constexpr int BJ = 32;           // rows per block (MMA N of S, K of P . V)
 constexpr int DQK = 576, DL = 512, ROWB = 656;
@@ -49,6 +53,7 @@ constexpr uint32_t SVALID = SRAW + BJ * ROWB;            // 2 x 32 int (per bloc
 constexpr uint32_t SMEM_USED = SVALID + 2 * BJ * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;        // + alignment slack
 constexpr uint64_t kWaitNs = 100000000ull;               // 100 ms bound on an mbarrier wait
+constexpr float kRescaleLog2 = 8.f;                      // reference-maximum slack (log2 units)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -69,6 +74,8 @@ __host__ __device__ constexpr uint32_t idesc(int n, int m, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(m >> 4) << 24);
 }
+constexpr uint32_t kIdescS = idesc(BJ, MH, false);   // S = Q . K^T
+constexpr uint32_t kIdescO = idesc(HALF, MH, true);  // O += P . V (V read MN-major)
 
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
   asm volatile(
@@ -130,6 +137,18 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// OR of a predicate over warpgroup 0's 128 threads (named barrier 1, so warpgroup 1 is not
+// held up).
+__device__ __forceinline__ int __syncthreads_or_wg0(bool pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r;
+}
+
 // Two e4m3 codes (low byte first) to two floats, exactly (e4m3 is a subset of f16).
 __device__ __forceinline__ float2 e4m3x2(uint16_t codes) {
   uint32_t h2;
@@ -160,7 +179,10 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint32_t s_taddr;
   __shared__ __align__(8) uint64_t s_bar_s, s_bar_o;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  __shared__ float s_alpha[MH];  // each head's rescale factor for this block
+  __shared__ int s_rescale;
+  const int tid = threadIdx.x, warp = tid >> 5, wg = tid >> 7;
+  const int head = tid & (MH - 1);  // this thread's tensor-memory lane
   const int r = blockIdx.x, u = blockIdx.y, p = blockIdx.z;
   const int per = (a.top_k + a.splits - 1) / a.splits;
   const int j_begin = p * per, j_end = min(a.top_k, j_begin + per);
@@ -190,8 +212,13 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   __syncthreads();
   tc_after();
   const uint32_t tbase = s_taddr;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's tensor-memory lanes
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's tensor-memory lanes
   const float sl2 = a.sm_scale * 1.4426950408889634f;      // scores in log2 units
+  // operand descriptors at their tiles' starts (start addresses then step in 16-B units)
+  const uint64_t dq0 = mdesc(smem_u32(base + SQ), 16, 1024);
+  const uint64_t dkv0 = mdesc(smem_u32(base + SKV), 16, 1024);
+  const uint64_t dp0 = mdesc(smem_u32(base + SP), 16, 1024);
+  const uint64_t dv0 = mdesc(smem_u32(base + SKV + (u * (HALF / 64)) * (BJ * 128)), BJ * 128, 1024);
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
 
@@ -202,25 +229,30 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
     // ends the loop for the whole CTA
     if (b > 0 && !bar_wait(&s_bar_o, (b - 1) & 1)) ok = false;
     if (!__syncthreads_and(ok)) break;
-    // dequantise: latent = e4m3 x scale -> bf16, RoPE copied; invalid rows are zero
+    // dequantise, one 16-B chunk (8 dims) of the tile per step: latent = e4m3 x scale -> bf16,
+    // RoPE copied; invalid rows are zero
     {
       const uint8_t* raw = base + SRAW;
       const int32_t* valid = reinterpret_cast<const int32_t*>(base + SVALID) + buf * BJ;
-      for (int c = tid; c < BJ * (DQK / 2); c += T) {
-        const int row = c / (DQK / 2), d = (c - row * (DQK / 2)) * 2;
-        uint32_t packed = 0u;
+      for (int c = tid; c < BJ * (DQK / 8); c += T) {
+        const int row = c / (DQK / 8), d = (c - row * (DQK / 8)) * 8;
+        uint4 chunk = make_uint4(0u, 0u, 0u, 0u);
         if (valid[row]) {
           const uint8_t* rec = raw + row * ROWB;
           if (d < DL) {
             const float sc = reinterpret_cast<const float*>(rec + DL)[d >> 7];
-            const float2 v = e4m3x2(*reinterpret_cast<const uint16_t*>(rec + d));
-            const __nv_bfloat162 bv = __floats2bfloat162_rn(v.x * sc, v.y * sc);
-            packed = *reinterpret_cast<const uint32_t*>(&bv);
+            const uint2 codes = *reinterpret_cast<const uint2*>(rec + d);
+            const float2 v0 = e4m3x2((uint16_t)(codes.x & 0xFFFFu)), v1 = e4m3x2((uint16_t)(codes.x >> 16));
+            const float2 v2 = e4m3x2((uint16_t)(codes.y & 0xFFFFu)), v3 = e4m3x2((uint16_t)(codes.y >> 16));
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(v0.x * sc, v0.y * sc), b1 = __floats2bfloat162_rn(v1.x * sc, v1.y * sc);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(v2.x * sc, v2.y * sc), b3 = __floats2bfloat162_rn(v3.x * sc, v3.y * sc);
+            chunk = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                               *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
           } else {
-            packed = *reinterpret_cast<const uint32_t*>(rec + DL + 16 + 2 * (d - DL));
+            chunk = *reinterpret_cast<const uint4*>(rec + DL + 16 + 2 * (d - DL));
           }
         }
-        *reinterpret_cast<uint32_t*>(base + SKV + (d >> 6) * (BJ * 128) + sw128(row, d & 63)) = packed;
+        *reinterpret_cast<uint4*>(base + SKV + (d >> 6) * (BJ * 128) + sw128(row, d & 63)) = chunk;
       }
     }
     fence_async_smem();
@@ -229,53 +261,61 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
     tc_after();
     // the raw buffer is consumed: the next block's records go out under this block's math
     if (b + 1 < nblk) gather_block(a, r, j_begin, j_end, b + 1, base);
-    if (tid == 0) {  // S = Q . K^T: 9 atoms x 4 steps of K 16
+    if (tid == 0) {  // S = Q . K^T: 9 atoms x 4 steps of K 16; descriptors step by constants
+#pragma unroll
       for (int kk = 0; kk < ATOMS * 4; ++kk) {
         const int at = kk >> 2, w = kk & 3;
-        mma(tbase + S_COL, mdesc(smem_u32(base + SQ + at * (MH * 128) + w * 32), 16, 1024),
-            mdesc(smem_u32(base + SKV + at * (BJ * 128) + w * 32), 16, 1024), idesc(BJ, MH, false), kk > 0);
+        mma(tbase + S_COL, dq0 + (uint64_t)((at * (MH * 128) + w * 32) >> 4),
+            dkv0 + (uint64_t)((at * (BJ * 128) + w * 32) >> 4), kIdescS, kk > 0);
       }
       commit(&s_bar_s);
     }
     if (!bar_wait(&s_bar_s, b & 1)) ok = false;
     if (!__syncthreads_and(ok)) break;
     tc_after();
-    // online softmax for head tid over this block's 32 rows
-    float s[BJ];
-    {
-      float t0[16], t1[16];
-      tmem_ld16(tbase + lane_off + S_COL, t0);
-      tmem_ld16(tbase + lane_off + S_COL + 16, t1);
-      const int32_t* valid = reinterpret_cast<const int32_t*>(base + SVALID) + buf * BJ;
+    // online softmax: warpgroup 0, one head per thread, over this block's 32 rows
+    if (wg == 0) {
+      float s[BJ];
+      {
+        float t0[16], t1[16];
+        tmem_ld16(tbase + lane_off + S_COL, t0);
+        tmem_ld16(tbase + lane_off + S_COL + 16, t1);
+        const int32_t* valid = reinterpret_cast<const int32_t*>(base + SVALID) + buf * BJ;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        s[j] = valid[j] ? t0[j] * sl2 : -INFINITY;
-        s[16 + j] = valid[16 + j] ? t1[j] * sl2 : -INFINITY;
+        for (int j = 0; j < 16; ++j) {
+          s[j] = valid[j] ? t0[j] * sl2 : -INFINITY;
+          s[16 + j] = valid[16 + j] ? t1[j] * sl2 : -INFINITY;
+        }
       }
+      float bm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < BJ; ++j) bm = fmaxf(bm, s[j]);
+      // Lazy rescale: a head keeps its reference maximum until the block's maximum exceeds it
+      // by more than kRescaleLog2, so P stays below 2^kRescaleLog2 (exact in bf16 and fp32) and
+      // O in tensor memory is rescaled only on those rare jumps.
+      const float m_new = bm > m_run + kRescaleLog2 || m_run == -INFINITY ? fmaxf(m_run, bm) : m_run;
+      const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);  // m_run = -inf: O is still 0
+      float psum = 0.f;
+#pragma unroll
+      for (int j = 0; j < BJ; j += 2) {
+        const float p0 = m_new == -INFINITY ? 0.f : exp2f(s[j] - m_new);
+        const float p1 = m_new == -INFINITY ? 0.f : exp2f(s[j + 1] - m_new);
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        psum += __low2float(pb) + __high2float(pb);  // the normaliser sums what P . V uses
+        *reinterpret_cast<__nv_bfloat162*>(base + SP + sw128(tid, j)) = pb;
+      }
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+      s_alpha[tid] = alpha;
+      const int any = __syncthreads_or_wg0(alpha != 1.f);
+      if (tid == 0) s_rescale = b > 0 && any;
     }
-    float bm = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < BJ; ++j) bm = fmaxf(bm, s[j]);
-    const float m_new = fmaxf(m_run, bm);
-    const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);  // m_run = -inf: O is still 0
-    float psum = 0.f;
-    uint32_t pk[BJ / 2];
-#pragma unroll
-    for (int j = 0; j < BJ; j += 2) {
-      const float p0 = m_new == -INFINITY ? 0.f : exp2f(s[j] - m_new);
-      const float p1 = m_new == -INFINITY ? 0.f : exp2f(s[j + 1] - m_new);
-      const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-      psum += __low2float(pb) + __high2float(pb);  // the normaliser sums what P . V uses
-      pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
-    }
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
-#pragma unroll
-    for (int j = 0; j < BJ; j += 2)
-      *reinterpret_cast<uint32_t*>(base + SP + sw128(tid, j)) = pk[j >> 1];
-    // rescale O where a running maximum grew (the previous P . V is complete: waited above)
-    if (b > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-      for (int c = 0; c < HALF; c += 16) {
+    __syncthreads();
+    // rescale O where a running maximum grew (the previous P . V is complete: waited above);
+    // warpgroup g takes columns [g * HALF / WG, (g + 1) * HALF / WG) of its lanes
+    if (s_rescale) {
+      const float alpha = s_alpha[head];
+      for (int c = wg * (HALF / WG); c < (wg + 1) * (HALF / WG); c += 16) {
         float v[16];
         tmem_ld16(tbase + lane_off + O_COL + c, v);
 #pragma unroll
@@ -288,10 +328,10 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
     __syncthreads();
     tc_after();
     if (tid == 0) {  // O += P . V over the block's 32 rows: 2 steps of K 16, N = this half's 256 dims
+#pragma unroll
       for (int kk = 0; kk < BJ / 16; ++kk)
-        mma(tbase + O_COL, mdesc(smem_u32(base + SP + kk * 32), 16, 1024),
-            mdesc(smem_u32(base + SKV + (u * (HALF / 64)) * (BJ * 128) + kk * 2048), BJ * 128, 1024),
-            idesc(HALF, MH, true), (b > 0 || kk > 0) ? 1u : 0u);
+        mma(tbase + O_COL, dp0 + (uint64_t)((kk * 32) >> 4), dv0 + (uint64_t)((kk * 2048) >> 4), kIdescO,
+            (b > 0 || kk > 0) ? 1u : 0u);
       commit(&s_bar_o);
     }
   }
@@ -308,10 +348,19 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
     return;
   }
   // write this split's normalised output and log-sum-exp for head tid
-  const bool live = tid < a.num_heads;
-  const size_t row_out = (((size_t)p * gridDim.x + r) * a.num_heads + tid);  // [split][r][h]
+  // warpgroup 0 holds each head's l and m: hand them to warpgroup 1 through shared memory
+  __shared__ float s_l[MH], s_m[MH];
+  if (wg == 0) {
+    s_l[tid] = l_run;
+    s_m[tid] = m_run;
+  }
+  __syncthreads();
+  l_run = s_l[head];
+  m_run = s_m[head];
+  const bool live = head < a.num_heads;
+  const size_t row_out = (((size_t)p * gridDim.x + r) * a.num_heads + head);  // [split][r][h]
   const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-  for (int c = 0; c < HALF; c += 16) {
+  for (int c = wg * (HALF / WG); c < (wg + 1) * (HALF / WG); c += 16) {
     float v[16];
     if (nblk > 0) {
       tmem_ld16(tbase + lane_off + O_COL + c, v);
@@ -324,7 +373,8 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
       for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
     }
   }
-  if (live && u == 0) part_lse[row_out] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+  if (live && u == 0 && wg == 0)
+    part_lse[row_out] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
   tc_before();
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS) : "memory");
