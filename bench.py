@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--op", default="step",
-                    choices=["step", "invalidate_tokens", "invalidate_host_rows", "split", "spec", "mla"],
+                    choices=["step", "invalidate_tokens", "invalidate_host_rows", "split", "spec", "mla", "e2e"],
                     help="step: the decode step (default); invalidate_*: one hot-slot invalidation call; "
                          "split: leader resolve + follower gathers on a copy stream vs the fused step")
     ap.add_argument("--sweep", action="store_true",
@@ -876,6 +876,151 @@ def run_mla(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_e2e(args, ws, rank, local):
+    """The decode step with its consumer: hs_resolve + hs_backup, then the synthetic sparse-MLA
+    attention (hs_sparse_mla_decode, MLA_HEADS heads, 2 splits) over the rows the resolve
+    returned, on layer 0's device pool. Three timed passes over the same steps, each from the
+    same state: resolve + backup (graph), attention alone, the whole step (one graph)."""
+    import torch
+    import hierarchical_sparse_attention_gb300 as hs
+    import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    W_, K_ = args.warmup, args.steps
+    total = W_ + K_
+    wl = W.make(args.config, args.seed + 1000 * rank, steps=total)
+    R, K, H, B, L = wl.R, wl.K, wl.H, wl.B, wl.L
+    assert B == 656, "the consumer reads fp8 MLA rows"
+    pools = [alloc_host(wl.host_rows * B) for _ in range(L)]
+    for l, (arr, reg) in enumerate(pools):
+        wl.fill_host_pool(l, arr)
+        touch_host_pool_from_gpu(hs.hs_host_register(arr) if reg else host_device_ptr(arr), arr.nbytes)
+    host = [arr for arr, _ in pools]
+    dpool = []
+    for l in range(L):
+        init = np.full(wl.device_rows * B, 0xA5, dtype=np.uint8)
+        rq, tk0, rows0 = wl.initial_device_writes()
+        wl.scatter_rows(l, rq, tk0, rows0, init)
+        dpool.append(torch.from_numpy(init).to(dev))
+    topk_all = torch.from_numpy(np.stack([wl.top_k_tokens(s) for s in range(total)])).to(dev)
+    seq_all = torch.from_numpy(np.stack([wl.seq_lens(s) for s in range(total)])).to(dev)
+    newest = [newest_rows(wl, s) for s in range(total)]
+    newest_idx = torch.from_numpy(np.stack([n[0] for n in newest])).to(dev)
+    newest_dat = [torch.from_numpy(np.stack([n[1][l] for n in newest])).to(dev) for l in range(L)]
+    hcl = torch.from_numpy(wl.host_cache_locs).to(dev)
+    dbl = torch.from_numpy(wl.device_buffer_locs).to(dev)
+    tok0, st0, clk0 = wl.initial_state()
+    tok, st, clk = (torch.from_numpy(x).to(dev) for x in (tok0, st0, clk0))
+    tk_buf = torch.empty((R, K), dtype=torch.int32, device=dev)
+    sl_buf = torch.empty((R,), dtype=torch.int32, device=dev)
+    out = torch.empty((R, K), dtype=torch.int32, device=dev)
+    miss = torch.empty((R,), dtype=torch.int32, device=dev)
+    cfg = hs.make_config(R, K, H, B, L, wl.ps, wl.max_context, wl.max_pages)
+    wsp = torch.zeros(hs.hs_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    h = hs.hs_create(cfg, host, dpool, wl.host_rows, wl.device_rows, wsp)
+    Hq, splits = MLA_HEADS, 2
+    qs = [torch.from_numpy(wl.queries_bf16(i, Hq).view(np.int16)).to(dev) for i in range(4)]
+    q_buf = torch.empty_like(qs[0])
+    o = torch.empty((R, Hq, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((R, Hq), dtype=torch.float32, device=dev)
+    mwsb = hs.hs_sparse_mla_workspace_bytes(R, Hq, splits)
+    mws = torch.zeros(max(mwsb, 16), dtype=torch.uint8, device=dev)
+    merr = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def forward_stand_in(s):
+        for l in range(L):
+            dpool[l].view(-1, B).index_copy_(0, newest_idx[s], newest_dat[l][s])
+        tk_buf.copy_(topk_all[s])
+        sl_buf.copy_(seq_all[s])
+        q_buf.copy_(qs[s % 4])
+
+    def resolve_backup(strm):
+        hs.hs_resolve(h, R, tk_buf, sl_buf, hcl, dbl, tok, st, clk, None, out, miss, strm)
+        hs.hs_backup(h, R, sl_buf, hcl, dbl, None, strm)
+
+    def attention(strm):
+        hs.hs_sparse_mla_decode(R, Hq, K, splits, q_buf, dpool[0], wl.device_rows, out, 1.0 / 1400.0, o, lse, mws,
+                                mwsb, merr, strm)
+
+    def reset():
+        tok.copy_(torch.from_numpy(tok0)); st.copy_(torch.from_numpy(st0)); clk.copy_(torch.from_numpy(clk0))
+        hs.hs_reset_hints(h, stream)
+        for s in range(W_):
+            forward_stand_in(s)
+            resolve_backup(stream)
+            attention(stream)
+        torch.cuda.synchronize()
+
+    graphs = {}
+    for name, fns in (("resolve", (resolve_backup,)), ("step", (resolve_backup, attention))):
+        reset()
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for fn in fns:
+                fn(torch.cuda.current_stream())
+        stream.wait_stream(cap)
+        graphs[name] = g
+    times = {}
+    for name in ("resolve", "attention", "step"):
+        reset()
+        for i in range(K_):  # rehearsal, untimed (host-pool first access)
+            forward_stand_in(W_ + i)
+            if name == "attention":
+                resolve_backup(stream)
+                attention(stream)
+            else:
+                graphs[name].replay()
+        torch.cuda.synchronize()
+        reset()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K_)]
+        barrier(ws)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(2e6 * (5 + K_ // 4)))
+        for i in range(K_):
+            forward_stand_in(W_ + i)
+            if name == "attention":
+                resolve_backup(stream)  # untimed: the rows this step's attention reads
+            flush.zero_()
+            evs[i][0].record(stream)
+            if name == "attention":
+                attention(stream)
+            else:
+                graphs[name].replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        ms = [e[0].elapsed_time(e[1]) for e in evs]
+        times[name] = (max_over_ranks(sum(ms) * 1e-3, ws), float(np.median(ms)) * 1e3)
+    err = hs.hs_get_error(h, clear=True)
+    hs.hs_destroy(h)
+    for arr, reg in pools:
+        if reg:
+            hs.hs_host_unregister(arr)
+    rows = int((topk_all[W_:] >= 0).sum().item())
+    t_step = times["step"][0]
+    line = {
+        "metric": "decode steps/s with the sparse-MLA consumer (resolve + backup + attention)",
+        "value": ws * K_ / t_step, "unit": "steps/s", "n_gpus": ws, "steps": K_, "warmup": W_,
+        "ms_per_step": 1e3 * t_step / K_, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int32+bf16", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {R} requests, top_k {K}, {H} hot slots, {B}-byte fp8 MLA rows; "
+                               f"attention {Hq} heads x 576/512 dims, {splits} splits",
+                   "l2": "flushed between timed steps (256 MiB write)"},
+        "p50_us": {k: v[1] for k, v in times.items()},
+        "mean_us": {k: 1e6 * v[0] / K_ for k, v in times.items()},
+        "top_k_rows_resolved_per_s_in_step": ws * rows / t_step,
+        "gpu_launches": K_ * (2 + 2), "device_flags": err, "attention_flags": int(merr.item()),
+        "host_pool": "huge pages, hs_host_register" if pools[0][1] else "cudaHostAlloc",
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 SPEC_QUERIES = 4  # n_spec = 3 draft tokens (MTP3) + the sampled one
 
 
@@ -1003,6 +1148,8 @@ def main():
     ws, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.op == "e2e":
+        run_e2e(args, ws, rank, local)
     elif args.op == "mla":
         run_mla(args, ws, rank, local)
     elif args.op == "spec":
