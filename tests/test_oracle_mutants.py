@@ -8,6 +8,7 @@ import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -67,3 +68,46 @@ def test_mutant_is_caught(tmp_path, name, old, new):
     p = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
     assert p.returncode != 3, f"mutant {name} survived every pin:\n{p.stdout}\n{p.stderr}"
     assert p.returncode == 0, f"mutant {name}: pin run crashed (rc {p.returncode}):\n{p.stderr[-2000:]}"
+
+
+# Planted mistakes in the sparse-MLA decode oracle (oracle/sparse_mla.py). Each copy is loaded
+# as a module of its own and the consumer's pins (tests/test_oracle_sparse_mla.py) run against
+# it in this process; at least one must fail.
+MLA_SRC = os.path.join(ROOT, "oracle", "sparse_mla.py")
+MLA_MUTANTS = [
+    ("e4m3_bias_8", "np.exp2(e.astype(np.float64) - 7.0)", "np.exp2(e.astype(np.float64) - 8.0)"),
+    ("e4m3_subnormal_scale", "m / 8.0 * 2.0 ** -6", "m / 8.0 * 2.0 ** -7"),
+    ("e4m3_nan_missed", "(e == 0xF) & (m == 7)", "(e == 0xF) & (m == 8)"),
+    ("scales_interleaved", "np.repeat(scales, SCALE_BLOCK, axis=1)", "np.tile(scales, SCALE_BLOCK)"),
+    ("rope_left_out", " + q[r, :, D_LATENT:] @ rope.T)", ")"),
+    ("scores_unscaled", "s = sm_scale * (", "s = 1.0 * ("),
+    ("lse_without_max", "lse[r] = (smax + np.log(z))[:, 0]", "lse[r] = np.log(z)[:, 0]"),
+    ("masked_rows_kept", "rows = out_rows[r][out_rows[r] >= 0]", "rows = out_rows[r][out_rows[r] >= -1]"),
+    ("softmax_over_heads", "z = e.sum(axis=1, keepdims=True)", "z = e.sum(axis=0, keepdims=True)"),
+    ("rope_low_half", "(bits.astype(np.uint32) << 16)", "(bits.astype(np.uint32) << 0)"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MLA_MUTANTS, ids=[m[0] for m in MLA_MUTANTS])
+def test_mla_mutant_is_caught(name, old, new):
+    import types
+
+    import test_oracle_sparse_mla as pins
+
+    src = open(MLA_SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mod = types.ModuleType("sparse_mla_mutant")
+    exec(compile(src.replace(old, new), f"<{name}>", "exec"), mod.__dict__)
+    failed = 0
+    saved = pins.M
+    try:
+        pins.M = mod
+        for fn in [getattr(pins, k) for k in dir(pins) if k.startswith("test_")]:
+            try:
+                with np.errstate(all="ignore"):
+                    fn()
+            except Exception:  # an assertion, or the mistake breaking a shape
+                failed += 1
+    finally:
+        pins.M = saved
+    assert failed, f"mutant {name} survived every pin"
