@@ -11,7 +11,7 @@ struct hs_handle {
   hs::Geometry g;
   const hs::Pools* pools;  // pools table inside the caller's workspace
   uint32_t* err_word;      // error word inside the caller's workspace
-  int16_t* hint;           // token -> slot hint table inside the caller's workspace
+  uint32_t* hint;          // residency bitmap inside the caller's workspace
   int32_t* plan_tok;       // follower plan inside the caller's workspace: tokens [R, K],
   int32_t* plan_dst;       //   device rows [R, K],
   int32_t* plan_cnt;       //   counts [R]
@@ -71,6 +71,7 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   g.page_size = cfg->page_size;
   g.max_context = cfg->max_context;
   g.max_pages = cfg->max_pages;
+  g.bit_words = hs::hint_words(cfg->max_context);
   g.hash_bits = ceil_log2(4 * (int64_t)cfg->top_k);  // top-k hash at most a quarter full
   if (g.hash_bits < 5) g.hash_bits = 5;
   g.sort_cap = 1 << ceil_log2(cfg->top_k);
@@ -120,9 +121,9 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (cudaMemset(ws, 0, hs::kWorkspaceBytes) != cudaSuccess) return HS_ERR_CUDA;
-  if (cudaMemset(ws + hs::kWorkspaceBytes, 0xFF, hs::hint_bytes(cfg->max_requests, cfg->max_context)) !=
+  if (cudaMemset(ws + hs::kWorkspaceBytes, 0, hs::hint_bytes(cfg->max_requests, cfg->max_context)) !=
       cudaSuccess)
-    return HS_ERR_CUDA;  // every hint starts at -1 (no slot)
+    return HS_ERR_CUDA;  // no token is known to be resident yet
   uint8_t* plan = ws + hs::kWorkspaceBytes + hs::hint_bytes(cfg->max_requests, cfg->max_context);
   if (cudaMemset(plan, 0, hs::plan_bytes(cfg->max_requests, cfg->top_k)) != cudaSuccess)
     return HS_ERR_CUDA;  // no plan yet: a gather before the first resolve copies nothing
@@ -135,7 +136,7 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   h->g = g;
   h->pools = reinterpret_cast<const hs::Pools*>(ws + hs::kPoolsOffset);
   h->err_word = reinterpret_cast<uint32_t*>(ws + hs::kErrOffset);
-  h->hint = reinterpret_cast<int16_t*>(ws + hs::kWorkspaceBytes);
+  h->hint = reinterpret_cast<uint32_t*>(ws + hs::kWorkspaceBytes);
   const size_t RK = (size_t)cfg->max_requests * (size_t)cfg->top_k;
   h->plan_tok = reinterpret_cast<int32_t*>(plan);
   h->plan_dst = h->plan_tok + RK;
@@ -296,7 +297,7 @@ hs_status hs_sparse_mla_decode(int32_t num_requests, int32_t num_heads, int32_t 
 
 hs_status hs_reset_hints(hs_handle* h, hs_stream_t stream) {
   if (!h) return HS_ERR_INVALID_ARG;
-  if (cudaMemsetAsync(h->hint, 0xFF, hs::hint_bytes(h->cfg.max_requests, h->cfg.max_context),
+  if (cudaMemsetAsync(h->hint, 0, hs::hint_bytes(h->cfg.max_requests, h->cfg.max_context),
                       (cudaStream_t)stream) != cudaSuccess) {
     cudaGetLastError();
     return HS_ERR_CUDA;

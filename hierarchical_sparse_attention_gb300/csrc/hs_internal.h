@@ -36,11 +36,13 @@ struct Geometry {
   int32_t copy_cap;   // misses one copy CTA can stage (all layers) in its shared memory
   int32_t dbl_smem;   // 1: the resolve CTA stages the slot -> row table in shared memory; 0: it
                       // reads it from global memory (large H, where the table does not fit)
+  int32_t bit_words;  // uint32 words per request in the residency bitmap (a multiple of 4)
+  int32_t bits_smem;  // 1: each copy CTA stages its request's bitmap row in shared memory
   int64_t host_rows, device_rows;
 };
 
 struct ResolveArgs {
-  int16_t* hint;  // [R, max_context] token -> slot guess (-1: none) in the workspace, or NULL
+  uint32_t* hint;  // [R, bit_words] residency bitmap in the workspace, or NULL
   const int32_t* top_k_tokens;
   const int32_t* seq_lens;
   const int32_t* host_cache_locs;
@@ -78,7 +80,7 @@ struct BackupArgs {
 };
 
 struct InvalidateArgs {
-  int16_t* hint;  // or NULL
+  uint32_t* hint;  // [R, bit_words] residency bitmap, or NULL
   const int32_t* seq_lens;
   const int32_t* token_offsets;  // [R + 1]
   const int32_t* tokens;
@@ -87,7 +89,7 @@ struct InvalidateArgs {
 };
 
 struct InvalidateRowsArgs {
-  int16_t* hint;  // or NULL
+  uint32_t* hint;  // [R, bit_words] residency bitmap, or NULL
   const int32_t* seq_lens;
   const int32_t* host_cache_locs;
   const int32_t* rows;  // ascending
@@ -114,13 +116,16 @@ constexpr size_t kWorkspaceBytes = 256;  // header: error word + pools table
 static_assert(kPoolsOffset + sizeof(Pools) <= kWorkspaceBytes, "workspace too small for the pools table");
 constexpr int kMaxEntriesPerThread = (HS_MAX_TOP_K + kResolveThreads - 1) / kResolveThreads;
 
-// After the header, hs_create's workspace holds the token -> slot hint table: one int16 per
-// (request, token position), the slot that last took the token (-1: none). The kernels keep
-// it current and use it only to start miss transfers early; every result still comes from
-// the exact slot probe, so a stale entry costs time, never correctness.
+// After the header, hs_create's workspace holds the residency bitmap: one bit per (request,
+// token position), set while the token sits in one of the request's hot slots. Each request's
+// row is hint_words() uint32 words, 16-byte aligned. The kernels keep it current and use it
+// only to start miss transfers early (a clear bit predicts a miss); every result still comes
+// from the exact slot probe, so a stale bit costs time, never correctness.
+inline int32_t hint_words(int64_t max_context) { return (int32_t)(((max_context + 127) / 128) * 4); }
 inline size_t hint_bytes(int64_t max_requests, int64_t max_context) {
-  return (size_t)(((max_requests * max_context * 2) + 255) & ~(int64_t)255);
+  return (size_t)(((max_requests * hint_words(max_context) * 4) + 255) & ~(int64_t)255);
 }
+constexpr int32_t kBitsSmemMax = 64 * 1024;  // largest bitmap row a copy CTA stages
 
 // After the hints: the follower plan the last resolve recorded, tokens [R, K], device rows
 // [R, K] and counts [R] (int32 each).

@@ -6,7 +6,7 @@
 // exactly; the worker matches a sorted list of the affected rows against the hot entries).
 //
 // A cleared slot becomes free (token -1, stamp 0), so the next resolve misses on its token
-// and copies the current row. The clock does not move; the token's hint is dropped. Slots
+// and copies the current row. The clock does not move; the token's residency bit is cleared. Slots
 // are keyed by token, so the exact form names tokens per request; the host-row form names
 // host rows and reaches each held token's row through host_cache_locs. Only tokens in
 // [0, seq_len - 1) count (no valid slot holds another), and requests on the fast path
@@ -32,11 +32,11 @@ __device__ __forceinline__ uint32_t token_bucket(int32_t t) {
   return ((uint32_t)t * 2654435761u) >> (32 - kHashBits);  // Knuth multiplicative
 }
 
-// Clear slot s of a request: free, stamp 0, the token's hint dropped.
-__device__ __forceinline__ void clear_slot(int32_t* tok, int32_t* st, int16_t* hint, int s, int32_t t) {
+// Clear slot s of a request: free, stamp 0, the token's residency bit cleared.
+__device__ __forceinline__ void clear_slot(int32_t* tok, int32_t* st, uint32_t* bits, int s, int32_t t) {
   tok[s] = -1;
   st[s] = 0;
-  if (hint) hint[t] = -1;
+  if (bits) atomicAnd(&bits[t >> 5], ~(1u << (t & 31)));  // the token is no longer resident
 }
 
 // Whether request r's slots are subject to invalidation; flags a bad seq_len.
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(T) invalidate_tokens_kernel(const Geometry g, 
   if (!applies(g, S, err_word)) return;
   const int32_t k0 = a.token_offsets[r], k1 = a.token_offsets[r + 1];
   int32_t* st = a.lru_slots + (size_t)r * g.H;
-  int16_t* hint = a.hint ? a.hint + (size_t)r * g.max_context : nullptr;
+  uint32_t* hint = a.hint ? a.hint + (size_t)r * g.bit_words : nullptr;
   for (int32_t c0 = k0; c0 < k1; c0 += kClearChunk) {
     const int32_t c1 = min(k1, c0 + kClearChunk);
     for (int i = threadIdx.x; i < kClearHash; i += T) s_tab[i] = -1;
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(T) invalidate_host_rows_kernel(const Geometry 
   }
   const int32_t* rows = staged ? s_rows : a.rows;
   int32_t* st = a.lru_slots + (size_t)r * g.H;
-  int16_t* hint = a.hint ? a.hint + (size_t)r * g.max_context : nullptr;
+  uint32_t* hint = a.hint ? a.hint + (size_t)r * g.bit_words : nullptr;
   if (t < 0 || t >= S - 1) return;
   int lo = 0, hi = n;  // first index with rows[i] >= hr
   while (lo < hi) {

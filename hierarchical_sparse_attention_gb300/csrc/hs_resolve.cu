@@ -37,14 +37,14 @@
 //   6  if misses outnumber free slots: the stamp threshold among occupied, un-hit slots
 //      comes from the age histogram (exact radix select when the histogram cannot decide);
 //      exactly the needed victims are gathered and ordered by (stamp, slot)
-//   7  pair miss j with victim j: update the map and the token->slot hints; publish each
+//   7  pair miss j with victim j: update the map and the residency bitmap; publish each
 //      miss's device row to its copy CTA (distributed shared memory, then the release half
 //      of the split cluster barrier)
 //   8  write back the changed slots, the row table and the clock
 //   9  copy the misses no copy CTA took (only when the geometry runs without copy CTAs)
 //      straight from host memory
 // A copy CTA owns a slice of the top-k row. At kernel start it predicts its slice's
-// misses from the token->slot hint table (a looked-up token with no hinted slot), looks
+// misses from the residency bitmap (a looked-up token whose bit is clear), looks
 // up their host rows and pulls them into shared memory while the resolve CTA does the
 // exact work; after the cluster barrier it stores the staged rows of exact misses to their
 // device rows and copies any unpredicted miss straight from host memory.
@@ -79,9 +79,10 @@ struct Layout {
 // [(q-1) * per, q * per) with per = ceil(K / C): their outcomes, published by the resolve CTA
 // (res: device row of a miss, -2 - slot for a hit, -1 otherwise), its slice of the top-k row,
 // per entry the staging index and host row, the lists of staged and of directly copied
-// entries, two counters, and the staging area (copy_cap entries x L rows of B bytes).
+// entries, two counters, the request's residency bitmap row (when it is staged), and the
+// staging area (copy_cap entries x L rows of B bytes).
 struct CopyLayout {
-  size_t res, tk, stg, hrow, list, dlist, cnt, stage, total;
+  size_t res, tk, stg, hrow, list, dlist, cnt, bits, stage, total;
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -126,6 +127,7 @@ __host__ __device__ inline CopyLayout make_copy_layout(const Geometry& g) {
   l.list = o; o = align16(o + 2 * cap);
   l.dlist = o; o = align16(o + 2 * per);
   l.cnt = o; o = align16(o + 16);
+  l.bits = o; o = align16(o + (g.bits_smem ? 4 * (size_t)g.bit_words : 0));
   l.stage = o; o = align16(o + cap * (size_t)g.L * (size_t)g.B);
   l.total = o;
   return l;
@@ -314,16 +316,18 @@ __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc
 
 // Copy CTA q of request r (cluster rank q >= 1; its shared outcome table was cleared to -1
 // and its counters to 0 before the cluster's first barrier).
-// With a hint table and a request past the fast path, it first predicts which of its
-// entries miss: a hot lookup with no hinted slot (the hints are exact while the caller
-// leaves the state to the kernels; a stale one only turns a miss into an unpredicted one,
-// and the miss's new slot rewrites it). It looks up the predicted
+// With a residency bitmap and a request past the fast path, it first predicts which of its
+// entries miss: a hot lookup whose bit is clear (the bits are exact while the caller leaves
+// the state to the kernels; a stale set bit only turns a miss into an unpredicted one, and
+// the miss's new slot rewrites it). The bitmap row comes into shared memory with the top-k
+// slice when it is small enough, so the prediction costs no memory round trip of its own.
+// It looks up the predicted
 // misses' host rows and reads those rows into shared memory right away (16-byte loads,
 // kCopyUnroll in flight per thread), so the host-link transfer runs while the resolve CTA
 // does the exact work. The cluster barrier then publishes the exact outcome of every entry.
-// Exact misses store their staged row; misses that were not staged (no hint, a wrong
-// guess, no room) are copied straight from host memory. A prediction that was a hit
-// repairs the entry's hint.
+// Exact misses store their staged row; misses that were not staged (a stale bit, no
+// room) are copied straight from host memory. A predicted miss that was a hit sets the
+// token's bit again.
 __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a, int r, int q, unsigned char* smem,
                          uint32_t* err_word) {
   const CopyLayout cl = make_copy_layout(g);
@@ -342,7 +346,8 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
   const int32_t S = a.spec_q < 0 ? a.seq_lens[r] : a.seq_lens[r] + a.spec_q + 1;
   const int32_t base = a.spec_q < 0 ? S - 1 : a.seq_lens[r];  // first position new to the cache
   const bool predict = a.hint != nullptr && a.copy_layers > 0 && S > g.H && S <= g.max_context;
-  int16_t* hint_row = a.hint ? a.hint + (size_t)r * g.max_context : nullptr;
+  uint32_t* bits_g = a.hint ? a.hint + (size_t)r * g.bit_words : nullptr;  // residency bitmap row
+  const uint32_t* bits = g.bits_smem ? reinterpret_cast<const uint32_t*>(smem + cl.bits) : bits_g;
   const int32_t* hcl_row = a.host_cache_locs + (size_t)r * g.max_context;
   const int32_t* tk_g = a.top_k_tokens + (size_t)r * g.K + e0;
   const int per_row = g.B >> 4;
@@ -352,6 +357,9 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
 
   if (predict) {
     cp_async_words(c_tk, tk_g, ne);
+    if (g.bits_smem)
+      cp_async_words(reinterpret_cast<int32_t*>(smem + cl.bits), reinterpret_cast<const int32_t*>(bits_g),
+                     g.bit_words);
     cp_async_commit();
     cp_async_wait_all();
     __syncthreads();
@@ -363,8 +371,7 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
       // delays the whole cluster's loads more than it saves (measured).
       if (t >= 0 && t < base &&
           !(a.resident_pages && a.resident_pages[(size_t)r * g.max_pages + t / g.page_size] >= 0)) {
-        const int gs = hint_row[t];
-        if (!(gs >= 0 && gs < g.H)) {
+        if (!((bits[t >> 5] >> (t & 31)) & 1u)) {
           const uint32_t k = atomicAdd(&c_cnt[0], 1u);
           if ((int)k < g.copy_cap) {
             st = (int16_t)k;
@@ -414,7 +421,7 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
       reinterpret_cast<uint4*>(p.dev[l] + (size_t)d * g.B)[qq] =
           c_hrow[e] >= 0 ? reinterpret_cast<const uint4*>(c_stage)[c] : make_uint4(0u, 0u, 0u, 0u);
   }
-  // the rest: hint repairs, and the list of exact misses to copy straight from host
+  // the rest: bitmap repairs, and the list of exact misses to copy straight from host
   for (int e = tid; e < ne; e += T) {
     const int32_t d = c_res[e];
     const int st = predict ? c_stg[e] : -1;
@@ -430,7 +437,8 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
         c_dlist[atomicAdd(&c_cnt[1], 1u)] = (int16_t)e;
       }
     } else if (d <= -2 && st != -1) {
-      hint_row[c_tk[e]] = (int16_t)(-2 - d);  // predicted a miss, was a hit in slot -2 - d
+      const int32_t t = c_tk[e];  // predicted a miss, was a hit: the token is resident
+      atomicOr(&bits_g[t >> 5], 1u << (t & 31));
     }
   }
   __syncthreads();
@@ -563,7 +571,7 @@ __global__ void __launch_bounds__(T, 1)
   // ---- phase 1: validity, class and the hash of the valid tokens. A repeated token is
   // only known once every insert is done, so classes and rows here are provisional for
   // repeats (settled in phase 4, or right below on the fast path).
-  int16_t* hint_row = a.hint ? a.hint + (size_t)r * g.max_context : nullptr;
+  uint32_t* hint_row = a.hint ? a.hint + (size_t)r * g.bit_words : nullptr;  // residency bitmap
   for (int i = tid; i < K; i += T) {
     const int32_t t = s_tk[i];
     uint8_t c;
@@ -623,8 +631,11 @@ __global__ void __launch_bounds__(T, 1)
       if (a.miss_counts) a.miss_counts[r] = 0;
       if (a.plan_cnt) a.plan_cnt[r] = 0;
     }
-    if (hint_row)  // slot t holds token t: the hints are exact when the sequence outgrows the buffer
-      for (int t = tid; t < S; t += T) hint_row[t] = (int16_t)t;
+    if (hint_row) {  // slot t holds token t for every committed t: exact once the sequence outgrows the buffer
+      const int nb = min(S, base + 1);
+      for (int w = tid; w < (nb + 31) / 32; w += T)
+        hint_row[w] = nb - 32 * w >= 32 ? ~0u : (1u << (nb - 32 * w)) - 1u;
+    }
     flush_flags(flags, err_word);
     return;
   }
@@ -705,7 +716,7 @@ __global__ void __launch_bounds__(T, 1)
   }
 
   // ---- phase 4: repeats settle; hits output their slot's row (and tell the entry's copy
-  // CTA which slot, so a wrong miss prediction can repair its hint)
+  // CTA which slot, so a wrong miss prediction can repair the token's bit)
   const int per = copy_slice(g);
   const CopyLayout cl = make_copy_layout(g);
   if (C > 0) cluster_wait();  // phase A: the copy CTAs run and their tables are cleared
@@ -937,8 +948,8 @@ __global__ void __launch_bounds__(T, 1)
     if ((uint32_t)v < (uint32_t)H) {
       if (hint_row) {
         const int32_t old_tok = s_tok[v];
-        if (old_tok >= 0) hint_row[old_tok] = -1;  // evicted
-        hint_row[s_tk[i]] = (int16_t)v;
+        if (old_tok >= 0) atomicAnd(&hint_row[old_tok >> 5], ~(1u << (old_tok & 31)));  // evicted
+        atomicOr(&hint_row[s_tk[i] >> 5], 1u << (s_tk[i] & 31));
       }
       s_tok[v] = s_tk[i];
       s_stamp[v] = clock;
@@ -1016,6 +1027,7 @@ cudaError_t resolve_prepare(Geometry& g, int32_t max_requests) {
   const int max_dynamic = optin - (int)fa.sharedSizeBytes;
   g.copy_ctas = 0;
   g.copy_cap = 0;
+  g.bits_smem = 0;
   g.dbl_smem = 1;
   if (make_layout(g).total > (size_t)max_dynamic) g.dbl_smem = 0;  // the row table stays in global memory
   if (make_layout(g).total > (size_t)max_dynamic) return cudaErrorInvalidValue;
@@ -1029,6 +1041,7 @@ cudaError_t resolve_prepare(Geometry& g, int32_t max_requests) {
     Geometry t = g;
     t.copy_ctas = C;
     t.copy_cap = 0;
+    t.bits_smem = g.bit_words > 0 && 4 * g.bit_words <= kBitsSmemMax ? 1 : 0;
     const size_t fixed = make_copy_layout(t).total + 64;  // + alignment slack
     if (fixed < (size_t)max_dynamic) {
       size_t cap = ((size_t)max_dynamic - fixed) / (2 + (size_t)g.L * (size_t)g.B);
@@ -1052,6 +1065,7 @@ cudaError_t resolve_prepare(Geometry& g, int32_t max_requests) {
       if (cudaOccupancyMaxActiveClusters(&clusters, resolve_kernel, &cfg) == cudaSuccess && clusters > 0) {
         g.copy_ctas = C;
         g.copy_cap = t.copy_cap;
+        g.bits_smem = t.bits_smem;
       } else {
         cudaGetLastError();
       }

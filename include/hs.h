@@ -151,15 +151,18 @@ typedef struct {
 typedef struct hs_handle hs_handle;
 
 /* Bytes of device workspace hs_create needs; 0 if the configuration is invalid. The
- * workspace holds the sticky error word, the per-layer pool table, and a token -> slot hint
- * table of max_requests x max_context int16 entries (so about 2 bytes per token of context
- * per request). The kernels keep the hints current and use them only to start a miss's
- * host transfer before the exact slot probe finishes; every result comes from the probe,
- * so hints left stale by changes the caller makes to the state arrays cost time, never
- * correctness. After the hints comes the follower plan of the last resolve: miss tokens
- * and device rows, max_requests x top_k int32 each, and max_requests counts (hs_gather
- * replays it). The caller keeps the workspace for the handle's lifetime and does not
- * write to it. */
+ * workspace is laid out as:
+ *   - 256 bytes: the sticky error word and the per-layer pool table;
+ *   - the residency bitmap (the miss "hints"): one bit per (request, token position), set
+ *     while the token sits in one of the request's hot slots. Each request's row is
+ *     ceil(max_context / 128) x 16 bytes; the whole bitmap is rounded up to 256 bytes. The
+ *     kernels keep it current and use it only to start a miss's host transfer before the
+ *     exact slot probe finishes (a clear bit predicts a miss). Every result comes from the
+ *     probe, so bits left stale by changes the caller makes to the state arrays cost time,
+ *     never correctness;
+ *   - the follower plan of the last resolve: miss tokens and device rows, max_requests x
+ *     top_k int32 each, then max_requests counts (hs_gather replays it).
+ * The caller keeps the workspace for the handle's lifetime and does not write to it. */
 HS_API size_t hs_workspace_bytes(const hs_config* cfg);
 
 /* Validate the configuration and bind the pools. host_pools / device_pools are arrays of
@@ -250,7 +253,7 @@ HS_API hs_status hs_backup(hs_handle* h, int32_t num_requests, const int32_t* se
  * 6, invalidation propagation: rows rewritten on the host leave the hot set exactly).
  * For each request r, every slot holding one of the tokens
  * tokens[token_offsets[r] .. token_offsets[r+1]) becomes free (token -1, stamp 0) and the
- * token's hint is dropped, so the next hs_resolve misses on it and copies its current host
+ * token's residency bit is cleared, so the next hs_resolve misses on it and copies its current host
  * row. Only tokens in [0, seq_len - 1) count (no valid slot holds another). Requests with
  * seq_len <= H are on the fast path and are left alone: their device rows are the tokens'
  * own rows, which the forward pass rewrites in place. seq_len outside [0, max_context]
@@ -299,11 +302,12 @@ HS_API hs_status hs_sparse_mla_decode(int32_t num_requests, int32_t num_heads, i
                                       void* workspace, size_t workspace_bytes, uint32_t* error_flags,
                                       hs_stream_t stream);
 
-/* Forget every token -> slot hint (the table becomes -1, as hs_create leaves it), in stream
- * order. Call it after changing device_buffer_tokens outside the library -- a request row
- * handed to a new sequence, a restored checkpoint -- so the copy CTAs' miss predictions
- * match the new state again. Results never depend on it: stale hints cost only speed. One
- * cudaMemsetAsync of max_requests x max_context x 2 bytes; graph-capturable. */
+/* Forget the residency bitmap (every bit clear, as hs_create leaves it), in stream order.
+ * Call it after changing device_buffer_tokens outside the library -- a request row handed
+ * to a new sequence, a restored checkpoint -- so the copy CTAs' miss predictions match the
+ * new state again: with every bit clear they first predict every looked-up token to miss,
+ * and each hit sets its bit back. Results never depend on it: stale bits cost only speed.
+ * One cudaMemsetAsync of about max_requests x max_context / 8 bytes; graph-capturable. */
 HS_API hs_status hs_reset_hints(hs_handle* h, hs_stream_t stream);
 
 /* Read the workspace error word (synchronises the device; not for the hot path). With

@@ -238,15 +238,16 @@ def test_two_handles_with_different_shared_memory_sizes():
 
 
 def test_stale_or_garbage_hints_do_not_change_results(pair):
-    """The token -> slot hints in the workspace only start transfers early: overwriting them
-    with garbage, or resetting a request's state behind their back, leaves every result exact."""
+    """The residency bitmap in the workspace only starts transfers early: overwriting it (and
+    the plan after it) with garbage, or resetting a request's state behind its back, leaves
+    every result exact."""
     wl, orc, gpu = pair
     warm(wl, orc, gpu)
     g = torch.Generator(device="cpu").manual_seed(7)
     junk = torch.randint(-32768, 32767, (gpu.ws.numel() // 2 - 128,), generator=g, dtype=torch.int16)
-    gpu.ws.view(torch.int16)[128:].copy_(junk)  # keep the 256-byte header, scramble the hints
+    gpu.ws.view(torch.int16)[128:].copy_(junk)  # keep the 256-byte header, scramble the bitmap
     assert step_both(wl, orc, gpu, 3) == 0
-    # request 0 starts over with an empty buffer; its hints still describe the old contents
+    # request 0 starts over with an empty buffer; its bits still describe the old contents
     for name in ("tokens", "stamps"):
         getattr(orc, name)[0, :] = -1 if name == "tokens" else 0
     orc.clock[0] = 0
@@ -257,19 +258,53 @@ def test_stale_or_garbage_hints_do_not_change_results(pair):
         assert step_both(wl, orc, gpu, s) == 0
 
 
+def bitmap_words(wl):
+    """The residency bitmap region of the workspace, as hs.h lays it out after the header."""
+    words = (wl.max_context + 127) // 128 * 4
+    return words, 256, wl.R * words
+
+
 def test_reset_hints_after_state_change(pair):
-    """hs_reset_hints empties the hint table (every entry -1, as hs_create leaves it) in stream
-    order; later steps stay exact and refill it."""
+    """hs_reset_hints clears the residency bitmap (every bit 0, as hs_create leaves it) in
+    stream order; later steps stay exact and set the bits of the tokens they place again."""
     import hierarchical_sparse_attention_gb300 as hs
     wl, orc, gpu = pair
     warm(wl, orc, gpu)
-    n = wl.R * wl.max_context
-    hints = gpu.ws[256: 256 + 2 * n].view(torch.int16)
-    assert int((hints != -1).sum().item()) > 0  # the warm steps wrote hints
-    gpu.ws.view(torch.int16)[128: 128 + n].fill_(1234)
+    words, off, n = bitmap_words(wl)
+    bits = gpu.ws[off: off + 4 * n].view(torch.int32)
+    assert int((bits != 0).sum().item()) > 0  # the warm steps set bits
+    bits.fill_(0x5A5A5A5A)
     hs.hs_reset_hints(gpu.h)
     torch.cuda.synchronize()
-    assert bool((hints == -1).all().item())
+    assert bool((bits == 0).all().item())
     for s in range(3, 6):
         assert step_both(wl, orc, gpu, s) == 0
-    assert int((hints != -1).sum().item()) > 0
+    assert int((bits != 0).sum().item()) > 0
+
+
+def test_bitmap_matches_slot_map(pair):
+    """While the kernels alone change the state, a set bit always names a token its request
+    holds (a miss is never predicted to hit), and every held token of the last step's top-k
+    has its bit set (placed misses, hits, and predicted misses that hit). Tokens of the
+    starting state that no step touched yet may still be clear: those only cost speed."""
+    wl, orc, gpu = pair
+    warm(wl, orc, gpu)
+    last = 5
+    for s in range(3, last + 1):
+        assert step_both(wl, orc, gpu, s) == 0
+    words, off, n = bitmap_words(wl)
+    bits = gpu.ws[off: off + 4 * n].view(torch.int32).cpu().numpy().view(np.uint32).reshape(wl.R, words)
+    tok = gpu.tok.cpu().numpy()
+    seq = gpu.sl.cpu().numpy()
+    topk = wl.top_k_tokens(last)
+    for r in range(wl.R):
+        got = ((bits[r][:, None] >> np.arange(32, dtype=np.uint32)) & 1).astype(bool).reshape(-1)[:seq[r]]
+        held = np.zeros(seq[r], dtype=bool)
+        held[tok[r][tok[r] >= 0]] = True
+        if seq[r] <= wl.H:  # fast path: slot t holds token t for every committed t
+            np.testing.assert_array_equal(got, held)
+            continue
+        assert not (got & ~held).any(), f"request {r}: a set bit names a token no slot holds"
+        mine = topk[r][(topk[r] >= 0) & (topk[r] < seq[r] - 1)]
+        mine = mine[held[mine]]
+        assert mine.size > 0 and got[mine].all(), f"request {r}: a held top-k token has a clear bit"

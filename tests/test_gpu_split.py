@@ -16,9 +16,9 @@ pytestmark = pytest.mark.gpu
 
 
 def _plan_views(gpu):
-    """The plan region of the workspace, as hs.h lays it out after the hint table."""
+    """The plan region of the workspace, as hs.h lays it out after the residency bitmap."""
     wl = gpu.wl
-    off = 256 + ((wl.R * wl.max_context * 2 + 255) & ~255)
+    off = 256 + ((wl.R * ((wl.max_context + 127) // 128) * 16 + 255) & ~255)
     RK = wl.R * wl.K
     words = gpu.ws[off: off + 4 * (2 * RK + wl.R)].view(torch.int32)
     return words[:RK].view(wl.R, wl.K), words[RK:2 * RK].view(wl.R, wl.K), words[2 * RK:]
