@@ -64,7 +64,11 @@ constexpr int kCopyUnroll = 4;
 enum : uint8_t { C_PAD = 0, C_BAD, C_DUP, C_RES, C_FAST, C_NEWEST, C_LOOKUP };
 constexpr uint8_t C_BADROW = 0x80;  // with C_RES / C_FAST / C_NEWEST: its row is out of range
 enum : uint8_t { SF_USED = 1, SF_DIRTY = 2 };
-enum { SC_LO = 0, SC_HI, SC_DIGIT, SC_RANK, SC_CONFLICT, SC_DIRECT, SC_COUNT };
+enum { SC_LO = 0, SC_HI, SC_DIGIT, SC_RANK, SC_CONFLICT, SC_DIRECT, SC_GATHER, SC_COUNT };
+// Victim phase: gathering every candidate at or below the threshold stamp in one pass saves
+// a counting pass (about a slot pass of work) but ranks n_le keys instead of m2; ranking is
+// n^2 / T compares per thread, so the one pass is taken while n_le^2 - m2^2 stays below this.
+constexpr int kOnePassSlack = 64 * 1024;
 
 // Shared-memory carve-up of the resolve CTA; identical arithmetic on host (size) and device
 // (pointers). The top-k hash (1 << hash_bits buckets of one 64-bit word: token << 32 |
@@ -466,6 +470,22 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
   }
   const uint32_t f = __reduce_or_sync(FULL, flags);
   if ((threadIdx.x & 31) == 0 && f) atomicOr(err_word, f);
+}
+
+// Rank n <= T distinct keys (stamp << 32 | slot) and write the slot of each key whose rank
+// (number of smaller keys) is below m to out[rank]. P threads share a key (P a power of two
+// with n * P <= T, at most a warp), each counting over every P-th key; the group sums with
+// shuffles. Lanes of one warp read the same few keys, so the loads are broadcasts.
+__device__ __forceinline__ void rank_keys(const uint64_t* keys, int n, int m, int32_t* out) {
+  int P = 1;
+  while (P < 32 && n * (P * 2) <= T) P <<= 1;
+  const int key = threadIdx.x / P, part = threadIdx.x & (P - 1);
+  const uint64_t kj = key < n ? keys[key] : 0ull;
+  int rk = 0;
+#pragma unroll 4
+  for (int u = part; u < n; u += P) rk += (int)(keys[u] < kj);
+  for (int o = P >> 1; o > 0; o >>= 1) rk += __shfl_xor_sync(FULL, rk, o);
+  if (key < n && part == 0 && rk < m) out[rk] = (int32_t)(kj & 0xffffffffu);
 }
 
 __device__ __forceinline__ void flush_flags(uint32_t flags, uint32_t* err_word) {
@@ -880,77 +900,85 @@ __global__ void __launch_bounds__(T, 1)
       thr_st = (int32_t)(base + prefix);  // the last victim's stamp
       need_eq = rank;                     // victims taken among the candidates stamped thr_st
     }
-    // Gather: warp by warp in slot order, candidates older than the threshold to
-    // [0, n_lt), the first need_eq at it to [n_lt, m2). Keys (stamp, slot) are distinct.
     const int n_lt = m2 - need_eq;
-    int c_lt = 0, c_eq = 0;
-    for (int b = sw0; b < sw1; b += 32) {
-      const int s = b + lane;
-      const bool cand = s < sw1 && s_tok[s] >= 0 && !(s_sflag[s] & SF_USED);
-      const int32_t st = cand ? s_stamp[s] : 0;
-      c_lt += __popc(__ballot_sync(FULL, cand && st < thr_st));
-      c_eq += __popc(__ballot_sync(FULL, cand && st == thr_st));
-    }
-    __syncthreads();  // every warp has read phase 5's counts
-    if (lane == 0) s_wsum[warp] = (c_lt << 16) | c_eq;
-    __syncthreads();
-    {
-      const int before = __reduce_add_sync(FULL, lane < warp ? s_wsum[lane] : 0);
-      int p_lt = before >> 16, p_eq = before & 0xffff;
+    // From the histogram, n_le = the candidates stamped thr_st or older (exact: the bins below
+    // 255 hold one age each). When they are few, one pass gathers them all, in any order, and
+    // ranking keeps the m2 smallest (stamp, slot) keys.
+    const int n_le = by_age ? n_lt + s_hist[s_sc[SC_DIGIT]] : INT_MAX;
+    if (n_le <= T && n_le <= g.sort_cap && n_le * n_le <= m2 * m2 + kOnePassSlack) {
       for (int b = sw0; b < sw1; b += 32) {
         const int s = b + lane;
         const bool cand = s < sw1 && s_tok[s] >= 0 && !(s_sflag[s] & SF_USED);
         const int32_t st = cand ? s_stamp[s] : 0;
-        const bool lt = cand && st < thr_st, eq = cand && st == thr_st;
-        const unsigned bl = __ballot_sync(FULL, lt), be = __ballot_sync(FULL, eq);
-        const uint64_t key = ((uint64_t)(uint32_t)st << 32) | (uint32_t)s;
-        if (lt) s_keys[p_lt + __popc(bl & lt_mask)] = key;
-        if (eq) {
-          const int q = p_eq + __popc(be & lt_mask);
-          if (q < need_eq) s_keys[n_lt + q] = key;
+        const bool take = cand && st <= thr_st;
+        const unsigned bl = __ballot_sync(FULL, take);
+        if (bl) {
+          int at = 0;
+          if (lane == 0) at = (int)atomicAdd(&s_sc[SC_GATHER], (uint32_t)__popc(bl));
+          at = __shfl_sync(FULL, at, 0) + __popc(bl & lt_mask);
+          if (take && at < n_le) s_keys[at] = ((uint64_t)(uint32_t)st << 32) | (uint32_t)s;
         }
-        p_lt += __popc(bl);
-        p_eq += __popc(be);
       }
-    }
-    __syncthreads();
-    if (m2 <= T) {
-      // a victim's rank is the number of smaller keys: one thread per victim, reading the
-      // keys two at a time as broadcasts
-      if (tid < m2) {
-        const uint64_t kj = s_keys[tid];
-        const ulonglong2* kp = reinterpret_cast<const ulonglong2*>(s_keys);
-        int rk = 0;
-#pragma unroll 4
-        for (int u = 0; u < (m2 >> 1); ++u) {
-          const ulonglong2 kk = kp[u];
-          rk += (int)(kk.x < kj) + (int)(kk.y < kj);
-        }
-        if (m2 & 1) rk += (int)(s_keys[m2 - 1] < kj);
-        s_vict[take_free + rk] = (int32_t)(kj & 0xffffffffu);
-      }
-    } else {
-      int n = 1;
-      while (n < m2) n <<= 1;
-      for (int i = m2 + tid; i < n; i += T) s_keys[i] = ~0ull;
       __syncthreads();
-      bitonic_sort(s_keys, n);
-      for (int j = tid; j < m2; j += T) s_vict[take_free + j] = (int32_t)(s_keys[j] & 0xffffffffu);
+      rank_keys(s_keys, n_le, m2, s_vict + take_free);
+    } else {
+      // Gather: warp by warp in slot order, candidates older than the threshold to
+      // [0, n_lt), the first need_eq at it to [n_lt, m2). Keys (stamp, slot) are distinct.
+      int c_lt = 0, c_eq = 0;
+      for (int b = sw0; b < sw1; b += 32) {
+        const int s = b + lane;
+        const bool cand = s < sw1 && s_tok[s] >= 0 && !(s_sflag[s] & SF_USED);
+        const int32_t st = cand ? s_stamp[s] : 0;
+        c_lt += __popc(__ballot_sync(FULL, cand && st < thr_st));
+        c_eq += __popc(__ballot_sync(FULL, cand && st == thr_st));
+      }
+      __syncthreads();  // every warp has read phase 5's counts
+      if (lane == 0) s_wsum[warp] = (c_lt << 16) | c_eq;
+      __syncthreads();
+      {
+        const int before = __reduce_add_sync(FULL, lane < warp ? s_wsum[lane] : 0);
+        int p_lt = before >> 16, p_eq = before & 0xffff;
+        for (int b = sw0; b < sw1; b += 32) {
+          const int s = b + lane;
+          const bool cand = s < sw1 && s_tok[s] >= 0 && !(s_sflag[s] & SF_USED);
+          const int32_t st = cand ? s_stamp[s] : 0;
+          const bool lt = cand && st < thr_st, eq = cand && st == thr_st;
+          const unsigned bl = __ballot_sync(FULL, lt), be = __ballot_sync(FULL, eq);
+          const uint64_t key = ((uint64_t)(uint32_t)st << 32) | (uint32_t)s;
+          if (lt) s_keys[p_lt + __popc(bl & lt_mask)] = key;
+          if (eq) {
+            const int q = p_eq + __popc(be & lt_mask);
+            if (q < need_eq) s_keys[n_lt + q] = key;
+          }
+          p_lt += __popc(bl);
+          p_eq += __popc(be);
+        }
+      }
+      __syncthreads();
+      if (m2 <= T) {
+        rank_keys(s_keys, m2, m2, s_vict + take_free);  // a victim's place is its key's rank
+      } else {
+        int n = 1;
+        while (n < m2) n <<= 1;
+        for (int i = m2 + tid; i < n; i += T) s_keys[i] = ~0ull;
+        __syncthreads();
+        bitonic_sort(s_keys, n);
+        for (int j = tid; j < m2; j += T) s_vict[take_free + j] = (int32_t)(s_keys[j] & 0xffffffffu);
+      }
     }
   }
   __syncthreads();
 
-  // ---- phase 7: miss j takes victim j; the entry's copy CTA gets its device row
+  // ---- phase 7: miss j takes victim j; the entry's copy CTA gets its device row. The global
+  // writes of this phase (residency bits, plan) come after the barrier arrive: a release
+  // arrive first waits for the thread's earlier writes to complete, which would hold the
+  // copy CTAs back by a global-memory round trip.
   for (int j = tid; j < m; j += T) {
     const int32_t v = s_vict[j];
     const int32_t i = s_miss[j];
-    int32_t d = -1;
+    int32_t d = -1, old_tok = -2;  // -2: no slot taken
     if ((uint32_t)v < (uint32_t)H) {
-      if (hint_row) {
-        const int32_t old_tok = s_tok[v];
-        if (old_tok >= 0) atomicAnd(&hint_row[old_tok >> 5], ~(1u << (old_tok & 31)));  // evicted
-        atomicOr(&hint_row[s_tk[i] >> 5], 1u << (s_tk[i] & 31));
-      }
+      old_tok = s_tok[v];
       s_tok[v] = s_tk[i];
       s_stamp[v] = clock;
       s_sflag[v] |= SF_DIRTY;
@@ -959,10 +987,7 @@ __global__ void __launch_bounds__(T, 1)
       flags |= HS_FLAG_STATE;  // unreachable by construction; never index with it
     }
     s_out[i] = d;
-    if (a.plan_tok) {  // the miss plan the follower layers replay: token and destination row
-      a.plan_tok[(size_t)r * K + j] = s_tk[i];
-      a.plan_dst[(size_t)r * K + j] = d;
-    }
+    s_vict[j] = old_tok;  // the evicted token (-1: a free slot), for the bitmap below
     if (C > 0) {  // the copy CTA owning entry i moves this row
       st_remote(smem + cl.res + 4 * (size_t)(i % per), 1 + i / per, d);
       s_pdst[j] = -1;
@@ -981,6 +1006,17 @@ __global__ void __launch_bounds__(T, 1)
     }
   }
   if (C > 0) cluster_arrive();  // phase B: every outcome is published to the copy CTAs
+  for (int j = tid; j < m; j += T) {  // this thread's misses of the loop above
+    const int32_t t = s_tk[s_miss[j]], old_tok = s_vict[j];
+    if (hint_row && old_tok >= -1) {
+      if (old_tok >= 0) atomicAnd(&hint_row[old_tok >> 5], ~(1u << (old_tok & 31)));  // evicted
+      atomicOr(&hint_row[t >> 5], 1u << (t & 31));
+    }
+    if (a.plan_tok) {  // the miss plan the follower layers replay: token and destination row
+      a.plan_tok[(size_t)r * K + j] = t;
+      a.plan_dst[(size_t)r * K + j] = s_out[s_miss[j]];
+    }
+  }
   __syncthreads();
 
   // ---- phase 8: write back changed slots, the row table and the clock
