@@ -453,9 +453,11 @@ def run_ours(args, ws, rank, local):
     res_s = np.array(res_ms) * 1e-3
     link_gbs = float(miss_bytes.sum() / res_s.sum() / 1e9)
     # HBM algorithmic bytes of one resolve launch: top-k, seq_lens, slot map + stamps read,
-    # host-row lookups for misses, slot->row table, state writes, row table, miss rows written
+    # host-row lookups for misses, slot->row table, state writes, row table, the residency
+    # bitmap row of each request, miss rows written
+    bit_row_bytes = (wl.max_context + 127) // 128 * 16
     hbm_bytes = (4 * R * K + 4 * R + 8 * R * H + 32 * misses + 4 * R * (H + 1) + 8 * R * K + 4 * R * K
-                 + miss_bytes).astype(np.float64)
+                 + R * bit_row_bytes + miss_bytes).astype(np.float64)
     hbm_gbs = float(hbm_bytes.sum() / res_s.sum() / 1e9)
     peaks = {}
     try:
