@@ -111,10 +111,6 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
       !aligned(workspace, 16))
     return HS_ERR_INVALID_ARG;
 
-  int optin = 0;
-  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-    return HS_ERR_CUDA;
-  if (hs::resolve_smem_bytes(g) > (size_t)optin) return HS_ERR_INVALID_CONFIG;
   if (const cudaError_t e = hs::resolve_prepare(g, cfg->max_requests); e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorInvalidValue ? HS_ERR_INVALID_CONFIG : HS_ERR_CUDA;

@@ -135,9 +135,10 @@ inline size_t plan_bytes(int64_t max_requests, int64_t top_k) {
 
 // Dynamic shared memory of one resolve-kernel CTA for geometry g.
 size_t resolve_smem_bytes(const Geometry& g);
-// Choose the copy CTAs per request (sets g.copy_ctas / g.copy_cap from the device's shared
-// memory, SM count and max_requests) and raise the kernel's dynamic shared-memory limit.
-// cudaErrorInvalidValue: g does not fit the device.
+// Fit the resolve CTA's tables to the device's shared memory (sets g.dbl_smem, and for the
+// largest top_k a half-full top-k hash), choose the copy CTAs per request (g.copy_ctas /
+// g.copy_cap / g.bits_smem from the shared memory, SM count and max_requests) and raise the
+// kernel's dynamic shared-memory limit. cudaErrorInvalidValue: g does not fit the device.
 cudaError_t resolve_prepare(Geometry& g, int32_t max_requests);
 cudaError_t launch_resolve(const Geometry& g, const Pools* pools, const ResolveArgs& a, int32_t num_requests,
                            uint32_t* err_word, cudaStream_t stream);

@@ -1064,9 +1064,24 @@ cudaError_t resolve_prepare(Geometry& g, int32_t max_requests) {
   g.copy_ctas = 0;
   g.copy_cap = 0;
   g.bits_smem = 0;
-  g.dbl_smem = 1;
-  if (make_layout(g).total > (size_t)max_dynamic) g.dbl_smem = 0;  // the row table stays in global memory
-  if (make_layout(g).total > (size_t)max_dynamic) return cudaErrorInvalidValue;
+  // The largest layout that fits, in this order: the slot -> row table staged, else read from
+  // global memory; then, for the largest top_k, the same with the top-k hash half full
+  // instead of a quarter (still at least half empty, so every probe loop ends).
+  int half_bits = 0;
+  while ((1 << half_bits) < g.K) ++half_bits;
+  half_bits += 1;  // 2 * sort_cap buckets: room for the keys and plan aliased onto the hash
+  bool fits = false;
+  for (int pass = 0; pass < 2 && !fits; ++pass) {
+    if (pass == 1) {
+      if (g.hash_bits <= half_bits) break;
+      g.hash_bits = half_bits;
+    }
+    for (int d = 1; d >= 0 && !fits; --d) {
+      g.dbl_smem = d;
+      fits = make_layout(g).total <= (size_t)max_dynamic;
+    }
+  }
+  if (!fits) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic);
   if (e != cudaSuccess) return e;
 

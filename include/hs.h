@@ -132,6 +132,10 @@ typedef enum {
  *   max_requests  largest R passed to hs_resolve / hs_backup
  *   top_k         K, 1..HS_MAX_TOP_K
  *   hot_slots     H (device_buffer_size), K..HS_MAX_HOT_SLOTS
+ * K and H must also leave the resolve CTA's tables within the device's shared memory per
+ * block (227 KB on GB300): about 37 K + 9 H bytes (rounding K up to a power of two for its
+ * hash). hs_create rejects a larger pair with HS_ERR_INVALID_CONFIG; e.g. K = 2048 takes any
+ * H up to HS_MAX_HOT_SLOTS, K = 4096 H up to ~8,800.
  *   row_bytes     B, bytes of one token's KV row in one layer (656 for fp8 MLA)
  *   num_layers    L, 1..HS_MAX_LAYERS
  *   page_size     residency page size in tokens; 0 disables resident_pages

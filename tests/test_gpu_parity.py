@@ -122,6 +122,9 @@ def test_miss_rate_sweep():
     dict(requests=5, top_k=1, hot_slots=1, row_bytes=48, layers=1, seq0=(40, 1, 2, 3, 500)),  # K = H = 1
     dict(requests=4, top_k=2, hot_slots=2, row_bytes=32, layers=2, seq0=(40, 1, 2, 300)),  # K = H = 2
     dict(requests=2, top_k=2048, hot_slots=2048, row_bytes=656, layers=1, seq0=(300000, 2100)),  # H = K
+    # the largest top_k: the top-k hash half full; > 1024 victims a step (the bitonic sort)
+    dict(requests=2, top_k=4096, hot_slots=4096, row_bytes=656, layers=1, seq0=(200000, 4100)),
+    dict(requests=2, top_k=4096, hot_slots=8192, row_bytes=656, layers=1, seq0=(200000, 9000)),  # row table global
 ])
 def test_ragged_shapes(shape):
     kw = dict(shape)
