@@ -13,19 +13,25 @@
 // (MLA decode with the absorbed projection: keys are the 576-dim rows, values their latent.)
 //
 // Layout of the work: a CTA of 512 threads takes (request r, half u of the 512 value dims,
-// split p of the rows). Every thread gathers and dequantises; thread t < 128 owns head t
-// (tensor-memory lane t) for the softmax, and the four warpgroups share the lanes by column
-// to rescale and read out O. The request's Q, 128 x 576
-// bf16, sits in shared memory in the 128-byte-swizzled K-major layout (144 KB). The rows are
-// taken 32 at a time: their 656-B records are gathered through the row table with cp.async
-// (the next block's as soon as this one's are dequantised), dequantised to bf16 (e4m3 -> f16 in hardware,
-// times the row's scale) into a swizzled tile, S = Q . K^T is 36 MMAs of M 128, N 32, K 16
-// into tensor memory, the online softmax runs in registers (one head per thread), P goes
-// back to shared memory as bf16, and O += P . V is two MMAs of N 256 reading the same tile's
-// latent part as an MN-major operand. O (128 x 256 fp32) stays in tensor memory and is
-// rescaled there only when a head's block maximum passes its reference maximum by more than
-// 2^8 (a lazy rescale: P is computed against the reference and stays below 2^8). With more than one split a small
-// kernel merges the splits by their log-sum-exp.
+// split p of the rows) and runs a three-role pipeline over blocks of 32 rows:
+//   - producers (warps 5-15) gather each block's 656-B records through the row table straight
+//     into registers (the next block's loads are in flight while the current one is
+//     dequantised), dequantise the latent to bf16 (e4m3 -> f16 in hardware, times the row's
+//     scale), copy the RoPE part, and fill one of two swizzled K-major tiles;
+//   - one issuer warp (warp 4) runs S = Q . K^T (36 MMAs of M 128, N 32, K 16) for a block as
+//     soon as its tile is full, and O += P . V (two MMAs of N 256) for the previous block once
+//     its probabilities are in;
+//   - the softmax warpgroup (warps 0-3, one head per thread, tensor-memory lane = head) reads
+//     S, runs the online softmax and writes P as bf16 into tensor memory, where P . V takes it
+//     as the A operand.
+// The request's Q, 128 x 576 bf16, sits in shared memory in the 128-byte-swizzled K-major layout
+// (144 KB), next to the two 36 KB tiles. Tensor memory holds two S buffers, two P buffers and O
+// (128 x 256 fp32). O is rescaled only when a head's block maximum passes its reference maximum
+// by more than 2^8 (a lazy rescale: P is computed against the reference and stays below 2^8).
+// The roles hand blocks over through mbarriers: tile full (producers -> issuer and softmax),
+// S full (issuer -> softmax), P full (softmax -> issuer), P . V done (issuer -> producers, which
+// may then refill that tile, and softmax, before a rescale). Every wait is bounded. With more
+// than one split a small kernel merges the splits by their log-sum-exp.
 #include "hs_internal.h"
 
 #include <cuda_bf16.h>
@@ -34,22 +40,28 @@
 namespace hs {
 namespace {
 
-constexpr int T = 512;           // threads: four warpgroups; warpgroup 0 owns one head per thread
-constexpr int WG = T / 128;      // warpgroups sharing the tensor-memory lanes (by column)
+constexpr int T = 512;           // threads: four warpgroups
+constexpr int WG = T / 128;      // warpgroups sharing the tensor-memory lanes (by column) at readout
 constexpr int MH = 128;          // MMA M: heads (padded with zero rows)
 constexpr int BJ = 32;           // rows per block (MMA N of S, K of P . V)
 constexpr int DQK = 576, DL = 512, ROWB = 656;
 constexpr int ATOMS = DQK / 64;  // 9 swizzle atoms of 64 bf16 along the 576 dims
 constexpr int HALF = DL / 2;     // value dims per CTA
+constexpr int ISSUER_WARP = 4;   // warp 4 issues the MMAs; warps 0-3 run the softmax
+constexpr int PROD0 = 160;       // first producer thread (warps 5-15)
+constexpr int NPROD = T - PROD0;
+constexpr int CHUNKS = BJ * (DQK / 8);                 // 16-byte tile chunks per block
+constexpr int PER_PROD = (CHUNKS + NPROD - 1) / NPROD;  // chunks per producer thread
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL = 0, O_COL = 256;
+constexpr uint32_t S_COL = 0;    // S of block b at S_COL + 32 (b & 1)
+constexpr uint32_t P_COL = 64;   // P of block b (bf16 pairs) at P_COL + 16 (b & 1)
+constexpr uint32_t O_COL = 256;
 
 // shared memory carve-up (offsets from a 1024-B aligned base)
 constexpr uint32_t SQ = 0;                               // 9 atoms x 128 rows x 128 B
-constexpr uint32_t SKV = SQ + ATOMS * MH * 128;          // 9 atoms x 32 rows x 128 B
-constexpr uint32_t SP = SKV + ATOMS * BJ * 128;          // 128 rows x 128 B (P, K-major, 32 of 64 used)
-constexpr uint32_t SRAW = SP + MH * 128;                 // 32 raw records
-constexpr uint32_t SVALID = SRAW + BJ * ROWB;            // 2 x 32 int (per block parity)
+constexpr uint32_t SKV = SQ + ATOMS * MH * 128;          // two tiles of 9 atoms x 32 rows x 128 B
+constexpr uint32_t KV_TILE = ATOMS * BJ * 128;
+constexpr uint32_t SVALID = SKV + 2 * KV_TILE;           // 2 x 32 int (row valid, per tile)
 constexpr uint32_t SMEM_USED = SVALID + 2 * BJ * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;        // + alignment slack
 constexpr uint64_t kWaitNs = 100000000ull;               // 100 ms bound on an mbarrier wait
@@ -149,6 +161,17 @@ __device__ __forceinline__ int __syncthreads_or_wg0(bool pred) {
   return r;
 }
 
+// AND of a predicate over warpgroup 0's 128 threads (named barrier 1).
+__device__ __forceinline__ int __syncthreads_and_wg0(bool pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r;
+}
+
 // Two e4m3 codes (low byte first) to two floats, exactly (e4m3 is a subset of f16).
 __device__ __forceinline__ float2 e4m3x2(uint16_t codes) {
   uint32_t h2;
@@ -156,21 +179,80 @@ __device__ __forceinline__ float2 e4m3x2(uint16_t codes) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h2));
 }
 
-// Issue the cp.async gather of block b's raw records and mark its rows (flags by parity).
-__device__ __forceinline__ void gather_block(const SparseMlaArgs& a, int r, int j_begin, int j_end, int b,
-                                             uint8_t* base) {
-  uint8_t* raw = base + SRAW;
-  int32_t* valid = reinterpret_cast<int32_t*>(base + SVALID) + (b & 1) * BJ;
-  const int j0 = j_begin + b * BJ;
-  for (int c = threadIdx.x; c < BJ * (ROWB / 16); c += T) {
-    const int row = c / (ROWB / 16), q = c - row * (ROWB / 16);
-    const int j = j0 + row;
-    const int32_t pr = j < j_end ? a.out_rows[(size_t)r * a.top_k + j] : -1;
-    const bool ok = pr >= 0 && (int64_t)pr < a.pool_rows;
-    if (q == 0) valid[row] = ok;
-    if (ok) cp16(smem_u32(raw + row * ROWB + q * 16), a.kv_pool + (size_t)pr * ROWB + q * 16);
+// MMA with A in tensor memory (P of P . V): lane m = row m, column c = A[m][2c], A[m][2c + 1].
+__device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void bar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Bounded wait for the completion of use k of a two-deep barrier pair (parity of k / 2); false
+// when the bound ran out or another role gave up (abort set).
+__device__ __forceinline__ bool pipe_wait(uint64_t* pair, int k, volatile int* abort) {
+  uint64_t* bar = pair + (k & 1);
+  const uint32_t parity = (uint32_t)(k >> 1) & 1u;
+  const uint64_t t0 = gtime();
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (*abort || gtime() - t0 > kWaitNs) {
+      *abort = 1;
+      return false;
+    }
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// A producer's chunks of one block: chunk c = (thread - PROD0) + i * NPROD covers row c / 72,
+// dims [8 (c % 72), 8 (c % 72) + 8). rows[] holds each chunk's pool row (-1: none).
+__device__ __forceinline__ void load_rows(const SparseMlaArgs& a, int r, int j0, int j_end, int pt,
+                                          int32_t (&rows)[PER_PROD]) {
+#pragma unroll
+  for (int i = 0; i < PER_PROD; ++i) {
+    const int c = pt + i * NPROD;
+    const int j = j0 + c / (DQK / 8);
+    int32_t pr = -1;
+    if (c < CHUNKS && j < j_end) {
+      pr = __ldg(a.out_rows + (size_t)r * a.top_k + j);
+      if (!(pr >= 0 && (int64_t)pr < a.pool_rows)) pr = -1;
+    }
+    rows[i] = pr;
+  }
+}
+// The raw bytes of those chunks: 8 codes and the block's scale for a latent chunk, 16 bytes of
+// RoPE otherwise.
+__device__ __forceinline__ uint32_t load_raw(const SparseMlaArgs& a, int pt, const int32_t (&rows)[PER_PROD],
+                                             uint4 (&raw)[PER_PROD]) {
+  uint32_t valid = 0;  // bit i: chunk i's row is a pool row
+#pragma unroll
+  for (int i = 0; i < PER_PROD; ++i) {
+    const int c = pt + i * NPROD;
+    const int d = (c % (DQK / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (rows[i] >= 0) {
+      valid |= 1u << i;
+      const uint8_t* rec = a.kv_pool + (size_t)rows[i] * ROWB;
+      if (d < DL) {
+        const uint2 codes = __ldg(reinterpret_cast<const uint2*>(rec + d));
+        v = make_uint4(codes.x, codes.y, __ldg(reinterpret_cast<const uint32_t*>(rec + DL) + (d >> 7)), 0u);
+      } else {
+        v = __ldg(reinterpret_cast<const uint4*>(rec + DL + 16 + 2 * (d - DL)));
+      }
+    }
+    raw[i] = v;
+  }
+  return valid;
 }
 
 __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a, float* __restrict__ part_o,
@@ -178,10 +260,12 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint32_t s_taddr;
-  __shared__ __align__(8) uint64_t s_bar_s, s_bar_o;
-  __shared__ float s_alpha[MH];  // each head's rescale factor for this block
-  __shared__ int s_rescale;
-  const int tid = threadIdx.x, warp = tid >> 5, wg = tid >> 7;
+  // barrier pairs (tile / buffer b & 1): tile full, S full, P full, P . V done
+  __shared__ __align__(8) uint64_t s_tile_full[2], s_s_full[2], s_p_full[2], s_o_done[2];
+  __shared__ int s_abort;
+  __shared__ float s_l[MH], s_m[MH];
+  volatile int* abort = &s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = tid >> 7;
   const int head = tid & (MH - 1);  // this thread's tensor-memory lane
   const int r = blockIdx.x, u = blockIdx.y, p = blockIdx.z;
   const int per = (a.top_k + a.splits - 1) / a.splits;
@@ -196,10 +280,14 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
     else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
-  if (nblk > 0) gather_block(a, r, j_begin, j_end, 0, base);
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar_s)) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar_o)) : "memory");
+    for (int k = 0; k < 2; ++k) {
+      bar_init(&s_tile_full[k], NPROD);
+      bar_init(&s_s_full[k], 1);
+      bar_init(&s_p_full[k], MH);
+      bar_init(&s_o_done[k], 1);
+    }
+    s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -208,79 +296,120 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  fence_async_smem();  // Q is read by the tensor cores
   tc_before();
   __syncthreads();
   tc_after();
   const uint32_t tbase = s_taddr;
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's tensor-memory lanes
-  const float sl2 = a.sm_scale * 1.4426950408889634f;      // scores in log2 units
-  // operand descriptors at their tiles' starts (start addresses then step in 16-B units)
-  const uint64_t dq0 = mdesc(smem_u32(base + SQ), 16, 1024);
-  const uint64_t dkv0 = mdesc(smem_u32(base + SKV), 16, 1024);
-  const uint64_t dp0 = mdesc(smem_u32(base + SP), 16, 1024);
-  const uint64_t dv0 = mdesc(smem_u32(base + SKV + (u * (HALF / 64)) * (BJ * 128)), BJ * 128, 1024);
   float m_run = -INFINITY, l_run = 0.f;
-  bool ok = true;
 
-  for (int b = 0; b < nblk; ++b) {
-    const int buf = b & 1;
-    asm volatile("cp.async.wait_group 0;" ::: "memory");  // this block's records have landed
-    // the tile is free once the previous block's P . V has read it; a wait that ran out
-    // ends the loop for the whole CTA
-    if (b > 0 && !bar_wait(&s_bar_o, (b - 1) & 1)) ok = false;
-    if (!__syncthreads_and(ok)) break;
-    // dequantise, one 16-B chunk (8 dims) of the tile per step: latent = e4m3 x scale -> bf16,
-    // RoPE copied; invalid rows are zero
-    {
-      const uint8_t* raw = base + SRAW;
-      const int32_t* valid = reinterpret_cast<const int32_t*>(base + SVALID) + buf * BJ;
-      for (int c = tid; c < BJ * (DQK / 8); c += T) {
-        const int row = c / (DQK / 8), d = (c - row * (DQK / 8)) * 8;
-        uint4 chunk = make_uint4(0u, 0u, 0u, 0u);
-        if (valid[row]) {
-          const uint8_t* rec = raw + row * ROWB;
-          if (d < DL) {
-            const float sc = reinterpret_cast<const float*>(rec + DL)[d >> 7];
-            const uint2 codes = *reinterpret_cast<const uint2*>(rec + d);
-            const float2 v0 = e4m3x2((uint16_t)(codes.x & 0xFFFFu)), v1 = e4m3x2((uint16_t)(codes.x >> 16));
-            const float2 v2 = e4m3x2((uint16_t)(codes.y & 0xFFFFu)), v3 = e4m3x2((uint16_t)(codes.y >> 16));
-            __nv_bfloat162 b0 = __floats2bfloat162_rn(v0.x * sc, v0.y * sc), b1 = __floats2bfloat162_rn(v1.x * sc, v1.y * sc);
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(v2.x * sc, v2.y * sc), b3 = __floats2bfloat162_rn(v3.x * sc, v3.y * sc);
-            chunk = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
-                               *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
-          } else {
-            chunk = *reinterpret_cast<const uint4*>(rec + DL + 16 + 2 * (d - DL));
-          }
-        }
-        *reinterpret_cast<uint4*>(base + SKV + (d >> 6) * (BJ * 128) + sw128(row, d & 63)) = chunk;
-      }
+  if (tid >= PROD0) {
+    // ---- producers: gather and dequantise block b into tile b & 1 once P . V of block b - 2
+    // has read it; the next block's row numbers and records load while this one is stored
+    const int pt = tid - PROD0;
+    int32_t rows[PER_PROD];
+    uint4 raw[PER_PROD];
+    uint32_t vmask = 0;
+    if (nblk > 0) {
+      load_rows(a, r, j_begin, j_end, pt, rows);
+      vmask = load_raw(a, pt, rows, raw);
+      if (nblk > 1) load_rows(a, r, j_begin + BJ, j_end, pt, rows);
     }
-    fence_async_smem();
-    tc_before();
-    __syncthreads();
-    tc_after();
-    // the raw buffer is consumed: the next block's records go out under this block's math
-    if (b + 1 < nblk) gather_block(a, r, j_begin, j_end, b + 1, base);
-    if (tid == 0) {  // S = Q . K^T: 9 atoms x 4 steps of K 16; descriptors step by constants
+    // Tile b & 1 last held block b - 2. S of that block (its K, every atom) is done once S full
+    // fired; P . V (its V: the four latent atoms of this half) once P . V done fired. So the
+    // five atoms P . V never reads are filled first, and only the V atoms wait for P . V.
+    const auto fill = [&](uint8_t* tile, bool v_part) {
 #pragma unroll
-      for (int kk = 0; kk < ATOMS * 4; ++kk) {
-        const int at = kk >> 2, w = kk & 3;
-        mma(tbase + S_COL, dq0 + (uint64_t)((at * (MH * 128) + w * 32) >> 4),
-            dkv0 + (uint64_t)((at * (BJ * 128) + w * 32) >> 4), kIdescS, kk > 0);
+      for (int i = 0; i < PER_PROD; ++i) {
+        const int c = pt + i * NPROD;
+        if (c >= CHUNKS) continue;
+        const int row = c / (DQK / 8), d = (c - row * (DQK / 8)) * 8;
+        if ((d < DL && (d >> 8) == u) != v_part) continue;
+        const uint4 v = raw[i];
+        uint4 chunk = v;
+        if (d < DL) {
+          const float sc = __uint_as_float(v.z);
+          const float2 v0 = e4m3x2((uint16_t)(v.x & 0xFFFFu)), v1 = e4m3x2((uint16_t)(v.x >> 16));
+          const float2 v2 = e4m3x2((uint16_t)(v.y & 0xFFFFu)), v3 = e4m3x2((uint16_t)(v.y >> 16));
+          __nv_bfloat162 b0 = __floats2bfloat162_rn(v0.x * sc, v0.y * sc), b1 = __floats2bfloat162_rn(v1.x * sc, v1.y * sc);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(v2.x * sc, v2.y * sc), b3 = __floats2bfloat162_rn(v3.x * sc, v3.y * sc);
+          chunk = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                             *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+        }
+        *reinterpret_cast<uint4*>(tile + (d >> 6) * (BJ * 128) + sw128(row, d & 63)) = chunk;
       }
-      commit(&s_bar_s);
+    };
+    for (int b = 0; b < nblk; ++b) {
+      uint8_t* tile = base + SKV + (b & 1) * KV_TILE;
+      int32_t* valid = reinterpret_cast<int32_t*>(base + SVALID) + (b & 1) * BJ;
+      if (b >= 2 && !pipe_wait(s_o_done, b - 2, abort)) break;
+      fill(tile, false);
+      fill(tile, true);
+      // a row's validity, from the thread that holds its first chunk
+#pragma unroll
+      for (int i = 0; i < PER_PROD; ++i) {
+        const int c = pt + i * NPROD;
+        if (c < CHUNKS && c % (DQK / 8) == 0) valid[c / (DQK / 8)] = (int32_t)((vmask >> i) & 1u);
+      }
+      fence_async_smem();
+      bar_arrive(&s_tile_full[b & 1]);
+      if (b + 1 < nblk) {
+        vmask = load_raw(a, pt, rows, raw);  // block b + 1 (its rows came in the previous step)
+        if (b + 2 < nblk) load_rows(a, r, j_begin + (b + 2) * BJ, j_end, pt, rows);
+      }
     }
-    if (!bar_wait(&s_bar_s, b & 1)) ok = false;
-    if (!__syncthreads_and(ok)) break;
-    tc_after();
-    // online softmax: warpgroup 0, one head per thread, over this block's 32 rows
-    if (wg == 0) {
+  } else if (warp == ISSUER_WARP) {
+    // ---- issuer: S of block b as soon as its tile is full, then P . V of block b - 1
+    const uint64_t dq0 = mdesc(smem_u32(base + SQ), 16, 1024);
+    for (int b = 0; b <= nblk; ++b) {
+      if (b < nblk) {
+        if (!__all_sync(0xffffffffu, pipe_wait(s_tile_full, b, abort))) break;  // the warp leaves together
+        tc_after();
+        if (lane == 0) {
+          const uint64_t dkv0 = mdesc(smem_u32(base + SKV + (b & 1) * KV_TILE), 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < ATOMS * 4; ++kk) {
+            const int at = kk >> 2, w = kk & 3;
+            mma(tbase + S_COL + 32 * (b & 1), dq0 + (uint64_t)((at * (MH * 128) + w * 32) >> 4),
+                dkv0 + (uint64_t)((at * (BJ * 128) + w * 32) >> 4), kIdescS, kk > 0);
+          }
+          commit(&s_s_full[b & 1]);
+        }
+        __syncwarp();
+      }
+      if (b >= 1) {
+        const int pb = b - 1;
+        if (!__all_sync(0xffffffffu, pipe_wait(s_p_full, pb, abort))) break;
+        tc_after();
+        if (lane == 0) {
+          const uint64_t dv0 =
+              mdesc(smem_u32(base + SKV + (pb & 1) * KV_TILE + (u * (HALF / 64)) * (BJ * 128)), BJ * 128, 1024);
+#pragma unroll
+          for (int kk = 0; kk < BJ / 16; ++kk)
+            mma_ta(tbase + O_COL, tbase + P_COL + 16 * (pb & 1) + 8 * kk, dv0 + (uint64_t)((kk * 2048) >> 4), kIdescO,
+                   (pb > 0 || kk > 0) ? 1u : 0u);
+          commit(&s_o_done[pb & 1]);
+        }
+        __syncwarp();
+      }
+    }
+  } else if (wg == 0) {
+    // ---- softmax: warpgroup 0, one head per thread
+    const float sl2 = a.sm_scale * 1.4426950408889634f;  // scores in log2 units
+    for (int b = 0; b < nblk; ++b) {
+      // every exit is taken by the whole warpgroup (it meets at named barrier 1 below)
+      bool got = pipe_wait(s_tile_full, b, abort);
+      got = got && pipe_wait(s_s_full, b, abort);
+      if (!__syncthreads_and_wg0(got)) break;
+      tc_after();
       float s[BJ];
       {
         float t0[16], t1[16];
-        tmem_ld16(tbase + lane_off + S_COL, t0);
-        tmem_ld16(tbase + lane_off + S_COL + 16, t1);
-        const int32_t* valid = reinterpret_cast<const int32_t*>(base + SVALID) + buf * BJ;
+        tmem_ld16(tbase + lane_off + S_COL + 32 * (b & 1), t0);
+        tmem_ld16(tbase + lane_off + S_COL + 32 * (b & 1) + 16, t1);
+        const int32_t* valid = reinterpret_cast<const int32_t*>(base + SVALID) + (b & 1) * BJ;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           s[j] = valid[j] ? t0[j] * sl2 : -INFINITY;
@@ -295,61 +424,53 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
       // O in tensor memory is rescaled only on those rare jumps.
       const float m_new = bm > m_run + kRescaleLog2 || m_run == -INFINITY ? fmaxf(m_run, bm) : m_run;
       const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);  // m_run = -inf: O is still 0
+      if (__syncthreads_or_wg0(b > 0 && alpha != 1.f)) {
+        // O must hold every earlier block before it is scaled: wait for P . V of block b - 1
+        if (!__syncthreads_and_wg0(pipe_wait(s_o_done, b - 1, abort))) break;
+        tc_after();
+        for (int c = 0; c < HALF; c += 16) {
+          float v[16];
+          tmem_ld16(tbase + lane_off + O_COL + c, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] *= alpha;
+          tmem_st16(tbase + lane_off + O_COL + c, v);
+        }
+      }
       float psum = 0.f;
+      float pk[16];  // bf16 pairs, bit-cast, for the 16 tensor-memory columns of P
 #pragma unroll
       for (int j = 0; j < BJ; j += 2) {
         const float p0 = m_new == -INFINITY ? 0.f : exp2f(s[j] - m_new);
         const float p1 = m_new == -INFINITY ? 0.f : exp2f(s[j + 1] - m_new);
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
         psum += __low2float(pb) + __high2float(pb);  // the normaliser sums what P . V uses
-        *reinterpret_cast<__nv_bfloat162*>(base + SP + sw128(tid, j)) = pb;
+        pk[j >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&pb));
       }
+      tmem_st16(tbase + lane_off + P_COL + 16 * (b & 1), pk);
       l_run = l_run * alpha + psum;
       m_run = m_new;
-      s_alpha[tid] = alpha;
-      const int any = __syncthreads_or_wg0(alpha != 1.f);
-      if (tid == 0) s_rescale = b > 0 && any;
-    }
-    __syncthreads();
-    // rescale O where a running maximum grew (the previous P . V is complete: waited above);
-    // warpgroup g takes columns [g * HALF / WG, (g + 1) * HALF / WG) of its lanes
-    if (s_rescale) {
-      const float alpha = s_alpha[head];
-      for (int c = wg * (HALF / WG); c < (wg + 1) * (HALF / WG); c += 16) {
-        float v[16];
-        tmem_ld16(tbase + lane_off + O_COL + c, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] *= alpha;
-        tmem_st16(tbase + lane_off + O_COL + c, v);
-      }
-    }
-    fence_async_smem();
-    tc_before();
-    __syncthreads();
-    tc_after();
-    if (tid == 0) {  // O += P . V over the block's 32 rows: 2 steps of K 16, N = this half's 256 dims
-#pragma unroll
-      for (int kk = 0; kk < BJ / 16; ++kk)
-        mma(tbase + O_COL, dp0 + (uint64_t)((kk * 32) >> 4), dv0 + (uint64_t)((kk * 2048) >> 4), kIdescO,
-            (b > 0 || kk > 0) ? 1u : 0u);
-      commit(&s_bar_o);
+      tc_before();
+      bar_arrive(&s_p_full[b & 1]);
     }
   }
-  if (ok && nblk > 0 && !bar_wait(&s_bar_o, (nblk - 1) & 1)) ok = false;
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  ok = __syncthreads_and(ok);
+  // every role is done issuing; wait for the last P . V, then read O out
+  bool ok = !*abort;
+  if (ok && nblk > 0 && !pipe_wait(s_o_done, nblk - 1, abort)) ok = false;
+  ok = __syncthreads_and(ok && !*abort);
   tc_after();
   if (!ok) {  // outputs are not valid: flag it and leave them alone
     if (tid == 0) atomicOr(err, HS_FLAG_TIMEOUT);
+    // give any MMA still in flight one more bound before the tensor memory is released
+    s_abort = 0;
+    if (nblk > 0) pipe_wait(s_o_done, nblk - 1, abort);
     tc_before();
     __syncthreads();
     if (warp == 0)
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS) : "memory");
     return;
   }
-  // write this split's normalised output and log-sum-exp for head tid
-  // warpgroup 0 holds each head's l and m: hand them to warpgroup 1 through shared memory
-  __shared__ float s_l[MH], s_m[MH];
+  // write this split's normalised output and log-sum-exp: warpgroup 0 holds each head's l and
+  // m; every warpgroup reads 64 of the 256 columns of its lanes
   if (wg == 0) {
     s_l[tid] = l_run;
     s_m[tid] = m_run;
