@@ -360,11 +360,11 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
   int staged = 0;
 
   if (predict) {
-    cp_async_words(c_tk, tk_g, ne);
     if (g.bits_smem)
       cp_async_words(reinterpret_cast<int32_t*>(smem + cl.bits), reinterpret_cast<const int32_t*>(bits_g),
                      g.bit_words);
     cp_async_commit();
+    for (int e = tid; e < ne; e += T) c_tk[e] = tk_g[e];  // plain loads: the row may be host memory
     cp_async_wait_all();
     __syncthreads();
     for (int e = tid; e < ne; e += T) {
@@ -573,14 +573,15 @@ __global__ void __launch_bounds__(T, 1)
   }
   const bool fast = S <= H;
 
-  // ---- phase 0: state into shared memory, asynchronously
-  cp_async_words(s_tk, tk_g, K);
+  // ---- phase 0: state into shared memory: the slot state asynchronously, the top-k row by
+  // plain loads (top_k_tokens may be pinned host memory, which cp.async is not used on)
   if (g.dbl_smem) cp_async_words(s_dbl_staged, dbl_g, H + 1);
   if (!fast) {
     cp_async_words(s_tok, tok_g, H);
     cp_async_words(s_stamp, st_g, H);
   }
   cp_async_commit();
+  for (int i = tid; i < K; i += T) s_tk[i] = tk_g[i];
   for (int h = tid; h < HS; h += T) s_hash[h] = kEmpty;
   for (int i = tid; i < K; i += T) s_claim[i] = INF;
   if (tid < SC_COUNT) s_sc[tid] = tid == SC_LO ? 0xffffffffu : 0u;

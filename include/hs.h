@@ -60,8 +60,8 @@
  * CUDA device memory of the device current at hs_create. Host pools are pinned and mapped
  * (cudaHostAlloc(..., cudaHostAllocMapped) or hs_host_register); the kernels read and
  * write them directly over the host link. All arrays are dense, row-major, int32:
- *   top_k_tokens         [R, K]            device, read
- *   seq_lens             [R]               device, read
+ *   top_k_tokens         [R, K]            device or pinned host (below), read
+ *   seq_lens             [R]               device or pinned host, read
  *   host_cache_locs      [R, max_context]  device, read      token -> host row
  *   device_buffer_locs   [R, H+1]          device, read      slot -> device row; slot H is
  *                                                            the newest-token row
@@ -69,8 +69,14 @@
  *   lru_slots            [R, H]            device, read/write per-slot LRU stamp
  *   lru_clock            [R]               device, read/write per-request clock
  *   resident_pages       [R, max_pages]    device, read, or NULL   page -> device page
- *   out_rows             [R, K]            device, write     physical row per entry
- *   miss_counts          [R]               device, write, or NULL
+ *   out_rows             [R, K]            device or pinned host, write   physical row per entry
+ *   miss_counts          [R]               device or pinned host, write, or NULL
+ * Zero-copy step I/O: top_k_tokens, seq_lens, out_rows and miss_counts may instead be pinned,
+ * mapped host memory (cudaHostAlloc, or registered, and addressed by its unified pointer) for
+ * a scheduler that produces and consumes them on the host. The kernels then read the inputs
+ * and write the outputs over the host link themselves, with plain loads and stores, and no
+ * separate copies are needed; the caller must not touch those buffers until the stream has
+ * passed the call. Every other array stays in device memory.
  * Initial state: long requests tokens = -1, stamps = 0, clock = 0; requests with
  * S <= H hold token s in slot s (rows already written) for s < S.
  * Preconditions not checked on the device: device_buffer_locs rows are distinct and

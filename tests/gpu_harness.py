@@ -39,7 +39,9 @@ def host_pools(wl: W.Workload, nthreads: int = 0):
 
 
 class GpuSim:
-    def __init__(self, wl: W.Workload, host, dev_init, device: str = "cuda"):
+    def __init__(self, wl: W.Workload, host, dev_init, device: str = "cuda", host_io: bool = False):
+        """host_io: the step's top-k, seq_lens, row table and miss counts live in pinned host
+        memory, which the kernels read and write directly (zero-copy step I/O)."""
         self.wl = wl
         self.host = host
         self.registered = []
@@ -56,10 +58,11 @@ class GpuSim:
         self.tok = torch.from_numpy(tok).to(dev)
         self.st = torch.from_numpy(st).to(dev)
         self.clk = torch.from_numpy(clk).to(dev)
-        self.out = torch.full((wl.R, wl.K), -7, dtype=torch.int32, device=dev)
-        self.miss = torch.full((wl.R,), -7, dtype=torch.int32, device=dev)
-        self.tk = torch.empty((wl.R, wl.K), dtype=torch.int32, device=dev)
-        self.sl = torch.empty((wl.R,), dtype=torch.int32, device=dev)
+        io = (lambda t: t.pin_memory()) if host_io else (lambda t: t.to(dev))
+        self.out = io(torch.full((wl.R, wl.K), -7, dtype=torch.int32))
+        self.miss = io(torch.full((wl.R,), -7, dtype=torch.int32))
+        self.tk = io(torch.empty((wl.R, wl.K), dtype=torch.int32))
+        self.sl = io(torch.empty((wl.R,), dtype=torch.int32))
         self.cfg = hs.make_config(wl.R, wl.K, wl.H, wl.B, wl.L, wl.ps, wl.max_context, wl.max_pages)
         self.ws = torch.zeros(hs.hs_workspace_bytes(self.cfg), dtype=torch.uint8, device=dev)
         self.h = hs.hs_create(self.cfg, host, self.dev, wl.host_rows, wl.device_rows, self.ws)

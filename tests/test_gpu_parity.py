@@ -44,11 +44,11 @@ def compare_pools(gpu, orc, what):
             raise AssertionError(f"{what}: device pool layer {layer} differs in {len(rows)} rows, e.g. {rows[:8]}")
 
 
-def run_parity(wl, host=None, steps=None, pool_every=8, graph_from=None):
+def run_parity(wl, host=None, steps=None, pool_every=8, graph_from=None, host_io=False):
     GpuSim, host_pools = _gpu()
     host = host if host is not None else host_pools(wl)
     orc = OracleSim(wl, host_pools=host)
-    gpu = GpuSim(wl, host, orc.dev)
+    gpu = GpuSim(wl, host, orc.dev, host_io=host_io)
     steps = wl.steps if steps is None else steps
     graph = None
     try:
@@ -135,6 +135,14 @@ def test_ragged_shapes(shape):
 
 def test_graph_capture_replay():
     run_parity(W.make("dsa", requests=8, steps=12), pool_every=4, graph_from=2)
+
+
+def test_zero_copy_step_io():
+    """top_k_tokens, seq_lens, out_rows and miss_counts in pinned host memory: the kernels read
+    and write them over the host link (copy CTAs, the fast path and graph replay included)."""
+    run_parity(W.make("dsa", requests=8, steps=10, seq0=(6000, 9000, 300, 7000, 8000, 4100, 20000, 5000)),
+               pool_every=2, graph_from=4, host_io=True)
+    run_parity(W.make("mixed1m", requests=4, steps=6), pool_every=3, host_io=True)
 
 
 def test_graph_capture_replay_indexshare():

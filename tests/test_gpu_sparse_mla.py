@@ -111,7 +111,9 @@ def check(q, pool, out_rows, sm_scale, go, glse, what):
 
 
 @pytest.mark.parametrize("R,Hq,K,splits", [(2, 128, 256, 1), (3, 128, 2048, 2), (2, 64, 100, 1), (1, 16, 333, 4),
-                                           (4, 128, 1024, 4)])
+                                           (4, 128, 1024, 4),
+                                           (2, 128, 600, 16),  # the most splits: two blocks each
+                                           (2, 128, 5, 16)])   # most splits hold no row at all
 def test_sparse_mla_matches_oracle(R, Hq, K, splits):
     hs = _gpu()
     q, pool, out_rows, sm = make_case(R * 7 + K, R, Hq, K, pool_rows=3000)
