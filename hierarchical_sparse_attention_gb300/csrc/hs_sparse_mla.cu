@@ -105,20 +105,6 @@ __device__ __forceinline__ uint64_t gtime() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait for a phase of an mbarrier; false when the bound ran out.
-__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = gtime();
-  for (;;) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if (gtime() - t0 > kWaitNs) return false;
-  }
-}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
