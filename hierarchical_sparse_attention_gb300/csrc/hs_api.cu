@@ -272,7 +272,7 @@ hs_status hs_sparse_mla_decode(int32_t num_requests, int32_t num_heads, int32_t 
                                const uint16_t* q, const uint8_t* kv_pool, int64_t pool_rows,
                                const int32_t* out_rows, float sm_scale, float* o, float* lse, void* workspace,
                                size_t workspace_bytes, uint32_t* error_flags, hs_stream_t stream) {
-  if (num_requests < 0 || num_heads < 1 || num_heads > 128 || top_k < 1 || splits < 1 ||
+  if (num_requests < 0 || num_heads < 1 || num_heads > 128 || top_k < 1 || top_k > HS_MAX_TOP_K || splits < 1 ||
       splits > HS_MAX_MLA_SPLITS || pool_rows < 1)
     return HS_ERR_INVALID_ARG;
   if (num_requests == 0) return HS_OK;

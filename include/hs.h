@@ -300,7 +300,8 @@ HS_API hs_status hs_invalidate_host_rows(hs_handle* h, int32_t num_requests, con
  * CTAs, merged by log-sum-exp in a second kernel.
  *   q        [R, num_heads, 576] bf16 bits, device, 16-byte aligned (num_heads <= 128)
  *   kv_pool  [pool_rows, 656] bytes, device (a layer's device pool), 16-byte aligned
- *   out_rows [R, top_k] device (hs_resolve's output); rows outside the pool count as -1
+ *   out_rows [R, top_k] device (hs_resolve's output), top_k <= HS_MAX_TOP_K; rows outside
+ *            the pool count as -1
  *   o        [R, num_heads, 512] fp32, device, 16-byte aligned; lse [R, num_heads] fp32, device
  *   workspace: hs_sparse_mla_workspace_bytes(R, num_heads, splits) device bytes (0 for one split)
  *   error_flags: device uint32, HS_FLAG_TIMEOUT OR-ed in if a bounded wait ran out.
