@@ -12,26 +12,29 @@
 //   o[h]    = softmax_j(s[h]) . latent,   lse[h] = log sum_j exp s[h, j]
 // (MLA decode with the absorbed projection: keys are the 576-dim rows, values their latent.)
 //
-// Layout of the work: a CTA of 512 threads takes (request r, half u of the 512 value dims,
-// split p of the rows) and runs a three-role pipeline over blocks of 32 rows:
-//   - producers (warps 5-15) gather each block's 656-B records through the row table straight
-//     into registers (the next block's loads are in flight while the current one is
-//     dequantised), dequantise the latent to bf16 (e4m3 -> f16 in hardware, times the row's
-//     scale), copy the RoPE part, and fill one of two swizzled K-major tiles;
-//   - one issuer warp (warp 4) runs S = Q . K^T (36 MMAs of M 128, N 32, K 16) for a block as
-//     soon as its tile is full, and O += P . V (two MMAs of N 256) for the previous block once
-//     its probabilities are in;
+// Layout of the work: a CTA of 512 threads takes (request r, quarter u of the 512 value dims,
+// split p of the rows) and runs a three-role pipeline over blocks of 64 rows:
+//   - producers (warps 5-15) gather each block's 656-B records through the row table (staged
+//     in shared memory) straight into registers, 32 rows at a time with the next 32 rows'
+//     loads in flight, dequantise the latent to bf16 (e4m3 -> f16 in hardware, times the row's
+//     scale), copy the RoPE part, and fill one of three swizzled K-major tiles (72 KB each);
+//   - one issuer warp (warp 4) runs S = Q . K^T for a block as soon as its tile is full and the
+//     softmax has read the previous S (36 MMAs of M 128, N 64, K 16, with Q as the A operand in
+//     tensor memory), and O += P . V for the previous block once its probabilities are in (four
+//     MMAs of N 128, P as the A operand in tensor memory);
 //   - the softmax warpgroup (warps 0-3, one head per thread, tensor-memory lane = head) reads
-//     S, runs the online softmax and writes P as bf16 into tensor memory, where P . V takes it
-//     as the A operand.
-// The request's Q, 128 x 576 bf16, sits in shared memory in the 128-byte-swizzled K-major layout
-// (144 KB), next to the two 36 KB tiles. Tensor memory holds two S buffers, two P buffers and O
-// (128 x 256 fp32). O is rescaled only when a head's block maximum passes its reference maximum
-// by more than 2^8 (a lazy rescale: P is computed against the reference and stays below 2^8).
+//     S into registers, runs the online softmax and writes P as bf16 pairs into tensor memory.
+// Tensor memory (512 columns): Q (128 heads x 576 bf16, 288 columns), S (128 x 64 fp32), P
+// (128 x 64 bf16, 32 columns) and O (128 x 128 fp32). Q in tensor memory leaves shared memory
+// to the tiles; the cost is that the four quarter-CTAs of a request each compute S. A
+// tcgen05.mma costs about the same up to N 64 (issue-bound), so 64-row blocks halve that cost
+// per row. O is rescaled only when a head's block maximum passes its reference maximum by
+// more than 2^8 (a lazy rescale: P is computed against the reference and stays below 2^8).
 // The roles hand blocks over through mbarriers: tile full (producers -> issuer and softmax),
-// S full (issuer -> softmax), P full (softmax -> issuer), P . V done (issuer -> producers, which
-// may then refill that tile, and softmax, before a rescale). Every wait is bounded. With more
-// than one split a small kernel merges the splits by their log-sum-exp.
+// S full (issuer -> softmax), S read (softmax -> issuer), P full (softmax -> issuer), P . V done
+// (issuer -> producers, which may then refill that tile, and softmax, before it rewrites P or
+// rescales O). Every wait is bounded. With more than one split a small kernel merges the
+// splits by their log-sum-exp.
 #include "hs_internal.h"
 
 #include <cuda_bf16.h>
@@ -43,26 +46,31 @@ namespace {
 constexpr int T = 512;           // threads: four warpgroups
 constexpr int WG = T / 128;      // warpgroups sharing the tensor-memory lanes (by column) at readout
 constexpr int MH = 128;          // MMA M: heads (padded with zero rows)
-constexpr int BJ = 32;           // rows per block (MMA N of S, K of P . V)
+constexpr int BJ = 64;           // rows per block (MMA N of S, K of P . V)
+constexpr int HB = 32;           // rows a producer pass fills (a block is two passes)
 constexpr int DQK = 576, DL = 512, ROWB = 656;
 constexpr int ATOMS = DQK / 64;  // 9 swizzle atoms of 64 bf16 along the 576 dims
-constexpr int HALF = DL / 2;     // value dims per CTA
+constexpr int NQ = 4;            // CTAs per (request, split): each takes a quarter of the value dims
+constexpr int HALF = DL / NQ;    // value dims per CTA (128)
 constexpr int ISSUER_WARP = 4;   // warp 4 issues the MMAs; warps 0-3 run the softmax
 constexpr int PROD0 = 160;       // first producer thread (warps 5-15)
 constexpr int NPROD = T - PROD0;
-constexpr int CHUNKS = BJ * (DQK / 8);                 // 16-byte tile chunks per block
+constexpr int CHUNKS = HB * (DQK / 8);                 // 16-byte tile chunks per producer pass
 constexpr int PER_PROD = (CHUNKS + NPROD - 1) / NPROD;  // chunks per producer thread
+constexpr int NT = 3;            // tiles in flight
+constexpr int ROWS_CAP = 2048;   // a split's row-table entries staged in shared memory
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL = 0;    // S of block b at S_COL + 32 (b & 1)
-constexpr uint32_t P_COL = 64;   // P of block b (bf16 pairs) at P_COL + 16 (b & 1)
-constexpr uint32_t O_COL = 256;
+constexpr uint32_t Q_COL = 0;    // Q, the A operand of S = Q . K^T: 288 columns of bf16 pairs
+constexpr uint32_t S_COL = 288;  // S of the current block, 64 columns (one buffer)
+constexpr uint32_t P_COL = 352;  // P of the current block (bf16 pairs), 32 columns (one buffer)
+constexpr uint32_t O_COL = 384;  // O, 128 x 128 fp32
 
 // shared memory carve-up (offsets from a 1024-B aligned base)
-constexpr uint32_t SQ = 0;                               // 9 atoms x 128 rows x 128 B
-constexpr uint32_t SKV = SQ + ATOMS * MH * 128;          // two tiles of 9 atoms x 32 rows x 128 B
+constexpr uint32_t SKV = 0;                              // NT tiles of 9 atoms x 32 rows x 128 B
 constexpr uint32_t KV_TILE = ATOMS * BJ * 128;
-constexpr uint32_t SVALID = SKV + 2 * KV_TILE;           // 2 x 32 int (row valid, per tile)
-constexpr uint32_t SMEM_USED = SVALID + 2 * BJ * 4;
+constexpr uint32_t SVALID = SKV + NT * KV_TILE;          // NT x 32 int (row valid, per tile)
+constexpr uint32_t SROWS = SVALID + NT * BJ * 4;         // the split's rows of the row table
+constexpr uint32_t SMEM_USED = SROWS + ROWS_CAP * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;        // + alignment slack
 constexpr uint64_t kWaitNs = 100000000ull;               // 100 ms bound on an mbarrier wait
 constexpr float kRescaleLog2 = 8.f;                      // reference-maximum slack (log2 units)
@@ -89,13 +97,6 @@ __host__ __device__ constexpr uint32_t idesc(int n, int m, bool b_mn_major) {
 constexpr uint32_t kIdescS = idesc(BJ, MH, false);   // S = Q . K^T
 constexpr uint32_t kIdescO = idesc(HALF, MH, true);  // O += P . V (V read MN-major)
 
-__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(id), "r"(acc)
-      : "memory");
-}
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -127,9 +128,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
       "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -165,7 +163,8 @@ __device__ __forceinline__ float2 e4m3x2(uint16_t codes) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h2));
 }
 
-// MMA with A in tensor memory (P of P . V): lane m = row m, column c = A[m][2c], A[m][2c + 1].
+// MMA with A in tensor memory (Q of S, P of P . V): lane m = row m, column c = A[m][2c],
+// A[m][2c + 1].
 __device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
@@ -179,11 +178,11 @@ __device__ __forceinline__ void bar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void bar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// Bounded wait for the completion of use k of a two-deep barrier pair (parity of k / 2); false
-// when the bound ran out or another role gave up (abort set).
-__device__ __forceinline__ bool pipe_wait(uint64_t* pair, int k, volatile int* abort) {
-  uint64_t* bar = pair + (k & 1);
-  const uint32_t parity = (uint32_t)(k >> 1) & 1u;
+// Bounded wait for the completion of use k of a ring of `depth` barriers (barrier k % depth,
+// parity of k / depth); false when the bound ran out or another role gave up (abort set).
+__device__ __forceinline__ bool pipe_wait(uint64_t* ring, int depth, int k, volatile int* abort) {
+  uint64_t* bar = ring + (k % depth);
+  const uint32_t parity = (uint32_t)(k / depth) & 1u;
   const uint64_t t0 = gtime();
   for (;;) {
     uint32_t done;
@@ -201,34 +200,23 @@ __device__ __forceinline__ bool pipe_wait(uint64_t* pair, int k, volatile int* a
 }
 
 // A producer's chunks of one block: chunk c = (thread - PROD0) + i * NPROD covers row c / 72,
-// dims [8 (c % 72), 8 (c % 72) + 8). rows[] holds each chunk's pool row (-1: none).
-__device__ __forceinline__ void load_rows(const SparseMlaArgs& a, int r, int j0, int j_end, int pt,
-                                          int32_t (&rows)[PER_PROD]) {
-#pragma unroll
-  for (int i = 0; i < PER_PROD; ++i) {
-    const int c = pt + i * NPROD;
-    const int j = j0 + c / (DQK / 8);
-    int32_t pr = -1;
-    if (c < CHUNKS && j < j_end) {
-      pr = __ldg(a.out_rows + (size_t)r * a.top_k + j);
-      if (!(pr >= 0 && (int64_t)pr < a.pool_rows)) pr = -1;
-    }
-    rows[i] = pr;
-  }
-}
+// dims [8 (c % 72), 8 (c % 72) + 8).
 // The raw bytes of those chunks: 8 codes and the block's scale for a latent chunk, 16 bytes of
 // RoPE otherwise.
-__device__ __forceinline__ uint32_t load_raw(const SparseMlaArgs& a, int pt, const int32_t (&rows)[PER_PROD],
+// rows: this block's 32 entries of the row table (shared memory); n: how many are real.
+__device__ __forceinline__ uint32_t load_raw(const SparseMlaArgs& a, int pt, const int32_t* rows, int n,
                                              uint4 (&raw)[PER_PROD]) {
   uint32_t valid = 0;  // bit i: chunk i's row is a pool row
 #pragma unroll
   for (int i = 0; i < PER_PROD; ++i) {
     const int c = pt + i * NPROD;
     const int d = (c % (DQK / 8)) * 8;
+    const int row = c / (DQK / 8);
+    const int32_t pr = c < CHUNKS && row < n ? rows[row] : -1;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (rows[i] >= 0) {
+    if (pr >= 0 && (int64_t)pr < a.pool_rows) {
       valid |= 1u << i;
-      const uint8_t* rec = a.kv_pool + (size_t)rows[i] * ROWB;
+      const uint8_t* rec = a.kv_pool + (size_t)pr * ROWB;
       if (d < DL) {
         const uint2 codes = __ldg(reinterpret_cast<const uint2*>(rec + d));
         v = make_uint4(codes.x, codes.y, __ldg(reinterpret_cast<const uint32_t*>(rec + DL) + (d >> 7)), 0u);
@@ -246,10 +234,10 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint32_t s_taddr;
-  // barrier pairs (tile / buffer b & 1): tile full, S full, P full, P . V done
-  __shared__ __align__(8) uint64_t s_tile_full[2], s_s_full[2], s_p_full[2], s_o_done[2];
+  // barrier rings: tile full and P . V done per tile (b % NT), S full and P full per buffer
+  // (b & 1), Q in tensor memory
+  __shared__ __align__(8) uint64_t s_tile_full[NT], s_o_done[NT], s_s_full, s_s_free, s_p_full, s_q_full;
   __shared__ int s_abort;
-  __shared__ float s_l[MH], s_m[MH];
   volatile int* abort = &s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = tid >> 7;
   const int head = tid & (MH - 1);  // this thread's tensor-memory lane
@@ -258,21 +246,15 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   const int j_begin = p * per, j_end = min(a.top_k, j_begin + per);
   const int nblk = j_end > j_begin ? (j_end - j_begin + BJ - 1) / BJ : 0;
 
-  // Q of request r into the swizzled K-major tile (zero rows past the last head)
-  for (int c = tid; c < MH * (DQK / 8); c += T) {
-    const int h = c / (DQK / 8), ch = c - h * (DQK / 8), d = ch * 8;
-    uint8_t* dst = base + SQ + (d >> 6) * (MH * 128) + sw128(h, d & 63);
-    if (h < a.num_heads) cp16(smem_u32(dst), a.q + ((size_t)r * a.num_heads + h) * DQK + d);
-    else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-  }
-  asm volatile("cp.async.commit_group;" ::: "memory");
   if (tid == 0) {
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < NT; ++k) {
       bar_init(&s_tile_full[k], NPROD);
-      bar_init(&s_s_full[k], 1);
-      bar_init(&s_p_full[k], MH);
       bar_init(&s_o_done[k], 1);
     }
+    bar_init(&s_s_full, 1);
+    bar_init(&s_s_free, MH);
+    bar_init(&s_p_full, MH);
+    bar_init(&s_q_full, MH);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -282,37 +264,62 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  fence_async_smem();  // Q is read by the tensor cores
   tc_before();
   __syncthreads();
   tc_after();
   const uint32_t tbase = s_taddr;
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's tensor-memory lanes
   float m_run = -INFINITY, l_run = 0.f;
+  if (wg == 0) {
+    // Q of request r into tensor memory, one head per lane (zero past the last head): the A
+    // operand of S = Q . K^T, column c holding dims 2c and 2c + 1
+    const int h = tid;
+    const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)r * a.num_heads + h) * DQK);
+    for (int c0 = 0; c0 < DQK / 2; c0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 w = h < a.num_heads ? __ldg(src + (c0 * 2) / 8 + k) : make_uint4(0u, 0u, 0u, 0u);
+        v[4 * k] = __uint_as_float(w.x);
+        v[4 * k + 1] = __uint_as_float(w.y);
+        v[4 * k + 2] = __uint_as_float(w.z);
+        v[4 * k + 3] = __uint_as_float(w.w);
+      }
+      tmem_st16(tbase + lane_off + Q_COL + c0, v);
+    }
+    tc_before();
+    bar_arrive(&s_q_full);
+  }
 
   if (tid >= PROD0) {
     // ---- producers: gather and dequantise block b into tile b & 1 once P . V of block b - 2
     // has read it; the next block's row numbers and records load while this one is stored
     const int pt = tid - PROD0;
-    int32_t rows[PER_PROD];
+    // the split's part of the row table, once, so each block's record loads wait on nothing else
+    // (a split of more than ROWS_CAP rows reads them from the row table in global memory)
+    const int32_t* g_rows = a.out_rows + (size_t)r * a.top_k + j_begin;
+    int32_t* s_rows = reinterpret_cast<int32_t*>(base + SROWS);
+    const bool staged = j_end - j_begin <= ROWS_CAP;
+    if (staged)
+      for (int i = pt; i < j_end - j_begin; i += NPROD) s_rows[i] = __ldg(g_rows + i);
+    asm volatile("bar.sync 2, %0;" ::"n"(NPROD) : "memory");  // producers only
+    const int32_t* rows_src = staged ? s_rows : g_rows;
+    // pass k fills rows [32 (k & 1), 32 (k & 1) + 32) of block k / 2
+    const auto pass_rows = [&](int k) { return rows_src + k * HB; };
+    const auto pass_n = [&](int k) { return min(HB, j_end - j_begin - k * HB); };
     uint4 raw[PER_PROD];
     uint32_t vmask = 0;
-    if (nblk > 0) {
-      load_rows(a, r, j_begin, j_end, pt, rows);
-      vmask = load_raw(a, pt, rows, raw);
-      if (nblk > 1) load_rows(a, r, j_begin + BJ, j_end, pt, rows);
-    }
+    if (nblk > 0) vmask = load_raw(a, pt, pass_rows(0), pass_n(0), raw);
     // Tile b & 1 last held block b - 2. S of that block (its K, every atom) is done once S full
     // fired; P . V (its V: the four latent atoms of this half) once P . V done fired. So the
     // five atoms P . V never reads are filled first, and only the V atoms wait for P . V.
-    const auto fill = [&](uint8_t* tile, bool v_part) {
+    const auto fill = [&](uint8_t* tile, int half) {
 #pragma unroll
       for (int i = 0; i < PER_PROD; ++i) {
         const int c = pt + i * NPROD;
         if (c >= CHUNKS) continue;
-        const int row = c / (DQK / 8), d = (c - row * (DQK / 8)) * 8;
-        if ((d < DL && (d >> 8) == u) != v_part) continue;
+        const int hrow = c / (DQK / 8), d = (c - hrow * (DQK / 8)) * 8;
+        const int row = half * HB + hrow;
         const uint4 v = raw[i];
         uint4 chunk = v;
         if (d < DL) {
@@ -327,56 +334,60 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
         *reinterpret_cast<uint4*>(tile + (d >> 6) * (BJ * 128) + sw128(row, d & 63)) = chunk;
       }
     };
+    const int npass = (j_end - j_begin + HB - 1) / HB;
     for (int b = 0; b < nblk; ++b) {
-      uint8_t* tile = base + SKV + (b & 1) * KV_TILE;
-      int32_t* valid = reinterpret_cast<int32_t*>(base + SVALID) + (b & 1) * BJ;
-      if (b >= 2 && !pipe_wait(s_o_done, b - 2, abort)) break;
-      fill(tile, false);
-      fill(tile, true);
-      // a row's validity, from the thread that holds its first chunk
+      if (b >= NT && !pipe_wait(s_o_done, NT, b - NT, abort)) break;
+      uint8_t* tile = base + SKV + (b % NT) * KV_TILE;
+      int32_t* valid = reinterpret_cast<int32_t*>(base + SVALID) + (b % NT) * BJ;
+      for (int half = 0; half < 2; ++half) {
+        const int k = 2 * b + half;
+        fill(tile, half);
+        // a row's validity, from the thread that holds its first chunk
 #pragma unroll
-      for (int i = 0; i < PER_PROD; ++i) {
-        const int c = pt + i * NPROD;
-        if (c < CHUNKS && c % (DQK / 8) == 0) valid[c / (DQK / 8)] = (int32_t)((vmask >> i) & 1u);
+        for (int i = 0; i < PER_PROD; ++i) {
+          const int c = pt + i * NPROD;
+          if (c < CHUNKS && c % (DQK / 8) == 0) valid[half * HB + c / (DQK / 8)] = (int32_t)((vmask >> i) & 1u);
+        }
+        if (k + 1 < npass) vmask = load_raw(a, pt, pass_rows(k + 1), pass_n(k + 1), raw);
+        else vmask = load_raw(a, pt, pass_rows(k + 1), 0, raw);  // past the end: zero rows
       }
       fence_async_smem();
-      bar_arrive(&s_tile_full[b & 1]);
-      if (b + 1 < nblk) {
-        vmask = load_raw(a, pt, rows, raw);  // block b + 1 (its rows came in the previous step)
-        if (b + 2 < nblk) load_rows(a, r, j_begin + (b + 2) * BJ, j_end, pt, rows);
-      }
+      bar_arrive(&s_tile_full[b % NT]);
     }
   } else if (warp == ISSUER_WARP) {
-    // ---- issuer: S of block b as soon as its tile is full, then P . V of block b - 1
-    const uint64_t dq0 = mdesc(smem_u32(base + SQ), 16, 1024);
-    for (int b = 0; b <= nblk; ++b) {
+    // ---- issuer: S of block b as soon as its tile is full (Q from tensor memory), then
+    // P . V of block b - 1
+    const bool q_in = __all_sync(0xffffffffu, nblk == 0 || pipe_wait(&s_q_full, 1, 0, abort));
+    for (int b = 0; q_in && b <= nblk; ++b) {
       if (b < nblk) {
-        if (!__all_sync(0xffffffffu, pipe_wait(s_tile_full, b, abort))) break;  // the warp leaves together
+        bool go = pipe_wait(s_tile_full, NT, b, abort);
+        go = go && (b == 0 || pipe_wait(&s_s_free, 1, b - 1, abort));  // the softmax holds S of b - 1
+        if (!__all_sync(0xffffffffu, go)) break;  // the warp leaves together
         tc_after();
         if (lane == 0) {
-          const uint64_t dkv0 = mdesc(smem_u32(base + SKV + (b & 1) * KV_TILE), 16, 1024);
+          const uint64_t dkv0 = mdesc(smem_u32(base + SKV + (b % NT) * KV_TILE), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < ATOMS * 4; ++kk) {
             const int at = kk >> 2, w = kk & 3;
-            mma(tbase + S_COL + 32 * (b & 1), dq0 + (uint64_t)((at * (MH * 128) + w * 32) >> 4),
-                dkv0 + (uint64_t)((at * (BJ * 128) + w * 32) >> 4), kIdescS, kk > 0);
+            mma_ta(tbase + S_COL, tbase + Q_COL + 8 * kk, dkv0 + (uint64_t)((at * (BJ * 128) + w * 32) >> 4), kIdescS,
+                   kk > 0);
           }
-          commit(&s_s_full[b & 1]);
+          commit(&s_s_full);
         }
         __syncwarp();
       }
       if (b >= 1) {
         const int pb = b - 1;
-        if (!__all_sync(0xffffffffu, pipe_wait(s_p_full, pb, abort))) break;
+        if (!__all_sync(0xffffffffu, pipe_wait(&s_p_full, 1, pb, abort))) break;
         tc_after();
         if (lane == 0) {
           const uint64_t dv0 =
-              mdesc(smem_u32(base + SKV + (pb & 1) * KV_TILE + (u * (HALF / 64)) * (BJ * 128)), BJ * 128, 1024);
+              mdesc(smem_u32(base + SKV + (pb % NT) * KV_TILE + (u * (HALF / 64)) * (BJ * 128)), BJ * 128, 1024);
 #pragma unroll
           for (int kk = 0; kk < BJ / 16; ++kk)
-            mma_ta(tbase + O_COL, tbase + P_COL + 16 * (pb & 1) + 8 * kk, dv0 + (uint64_t)((kk * 2048) >> 4), kIdescO,
+            mma_ta(tbase + O_COL, tbase + P_COL + 8 * kk, dv0 + (uint64_t)((kk * 2048) >> 4), kIdescO,
                    (pb > 0 || kk > 0) ? 1u : 0u);
-          commit(&s_o_done[pb & 1]);
+          commit(&s_o_done[pb % NT]);
         }
         __syncwarp();
       }
@@ -386,22 +397,23 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
     const float sl2 = a.sm_scale * 1.4426950408889634f;  // scores in log2 units
     for (int b = 0; b < nblk; ++b) {
       // every exit is taken by the whole warpgroup (it meets at named barrier 1 below)
-      bool got = pipe_wait(s_tile_full, b, abort);
-      got = got && pipe_wait(s_s_full, b, abort);
+      bool got = pipe_wait(s_tile_full, NT, b, abort);
+      got = got && pipe_wait(&s_s_full, 1, b, abort);
       if (!__syncthreads_and_wg0(got)) break;
       tc_after();
       float s[BJ];
       {
-        float t0[16], t1[16];
-        tmem_ld16(tbase + lane_off + S_COL + 32 * (b & 1), t0);
-        tmem_ld16(tbase + lane_off + S_COL + 32 * (b & 1) + 16, t1);
-        const int32_t* valid = reinterpret_cast<const int32_t*>(base + SVALID) + (b & 1) * BJ;
+        const int32_t* valid = reinterpret_cast<const int32_t*>(base + SVALID) + (b % NT) * BJ;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          s[j] = valid[j] ? t0[j] * sl2 : -INFINITY;
-          s[16 + j] = valid[16 + j] ? t1[j] * sl2 : -INFINITY;
+        for (int q = 0; q < BJ / 16; ++q) {
+          float t[16];
+          tmem_ld16(tbase + lane_off + S_COL + 16 * q, t);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) s[16 * q + j] = valid[16 * q + j] ? t[j] * sl2 : -INFINITY;
         }
       }
+      tc_before();
+      bar_arrive(&s_s_free);  // S is in registers: the next block's S may overwrite it
       float bm = -INFINITY;
 #pragma unroll
       for (int j = 0; j < BJ; ++j) bm = fmaxf(bm, s[j]);
@@ -410,10 +422,11 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
       // O in tensor memory is rescaled only on those rare jumps.
       const float m_new = bm > m_run + kRescaleLog2 || m_run == -INFINITY ? fmaxf(m_run, bm) : m_run;
       const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);  // m_run = -inf: O is still 0
+      // P . V of block b - 1 must be done before P is rewritten (one buffer) and before O is
+      // scaled
+      if (!__syncthreads_and_wg0(b == 0 || pipe_wait(s_o_done, NT, b - 1, abort))) break;
+      tc_after();
       if (__syncthreads_or_wg0(b > 0 && alpha != 1.f)) {
-        // O must hold every earlier block before it is scaled: wait for P . V of block b - 1
-        if (!__syncthreads_and_wg0(pipe_wait(s_o_done, b - 1, abort))) break;
-        tc_after();
         for (int c = 0; c < HALF; c += 16) {
           float v[16];
           tmem_ld16(tbase + lane_off + O_COL + c, v);
@@ -423,32 +436,35 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
         }
       }
       float psum = 0.f;
-      float pk[16];  // bf16 pairs, bit-cast, for the 16 tensor-memory columns of P
 #pragma unroll
-      for (int j = 0; j < BJ; j += 2) {
-        const float p0 = m_new == -INFINITY ? 0.f : exp2f(s[j] - m_new);
-        const float p1 = m_new == -INFINITY ? 0.f : exp2f(s[j + 1] - m_new);
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        psum += __low2float(pb) + __high2float(pb);  // the normaliser sums what P . V uses
-        pk[j >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&pb));
+      for (int q = 0; q < BJ / 32; ++q) {
+        float pk[16];  // bf16 pairs, bit-cast, for 16 tensor-memory columns of P
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = m_new == -INFINITY ? 0.f : exp2f(s[32 * q + j] - m_new);
+          const float p1 = m_new == -INFINITY ? 0.f : exp2f(s[32 * q + j + 1] - m_new);
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+          psum += __low2float(pb) + __high2float(pb);  // the normaliser sums what P . V uses
+          pk[j >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&pb));
+        }
+        tmem_st16(tbase + lane_off + P_COL + 16 * q, pk);
       }
-      tmem_st16(tbase + lane_off + P_COL + 16 * (b & 1), pk);
       l_run = l_run * alpha + psum;
       m_run = m_new;
       tc_before();
-      bar_arrive(&s_p_full[b & 1]);
+      bar_arrive(&s_p_full);
     }
   }
   // every role is done issuing; wait for the last P . V, then read O out
   bool ok = !*abort;
-  if (ok && nblk > 0 && !pipe_wait(s_o_done, nblk - 1, abort)) ok = false;
+  if (ok && nblk > 0 && !pipe_wait(s_o_done, NT, nblk - 1, abort)) ok = false;
   ok = __syncthreads_and(ok && !*abort);
   tc_after();
   if (!ok) {  // outputs are not valid: flag it and leave them alone
     if (tid == 0) atomicOr(err, HS_FLAG_TIMEOUT);
     // give any MMA still in flight one more bound before the tensor memory is released
     s_abort = 0;
-    if (nblk > 0) pipe_wait(s_o_done, nblk - 1, abort);
+    if (nblk > 0) pipe_wait(s_o_done, NT, nblk - 1, abort);
     tc_before();
     __syncthreads();
     if (warp == 0)
@@ -456,7 +472,10 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
     return;
   }
   // write this split's normalised output and log-sum-exp: warpgroup 0 holds each head's l and
-  // m; every warpgroup reads 64 of the 256 columns of its lanes
+  // m (handed over through the first tile, unused now); every warpgroup reads a quarter of the
+  // columns of its lanes
+  float* s_l = reinterpret_cast<float*>(base + SKV);
+  float* s_m = s_l + MH;
   if (wg == 0) {
     s_l[tid] = l_run;
     s_m[tid] = m_run;
@@ -519,7 +538,7 @@ cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, floa
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const bool direct = a.splits == 1;
-  sparse_mla_kernel<<<dim3(num_requests, 2, a.splits), T, SMEM_BYTES, stream>>>(
+  sparse_mla_kernel<<<dim3(num_requests, NQ, a.splits), T, SMEM_BYTES, stream>>>(
       a, direct ? a.o : part_o, direct ? a.lse : part_lse, err);
   e = cudaGetLastError();
   if (e != cudaSuccess || direct) return e;
