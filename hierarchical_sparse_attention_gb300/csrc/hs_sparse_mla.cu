@@ -292,8 +292,8 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   }
 
   if (tid >= PROD0) {
-    // ---- producers: gather and dequantise block b into tile b & 1 once P . V of block b - 2
-    // has read it; the next block's row numbers and records load while this one is stored
+    // ---- producers: gather and dequantise block b into tile b % NT once P . V of block b - NT
+    // has read it, 32 rows per pass; the next pass's records load while this one is stored
     const int pt = tid - PROD0;
     // the split's part of the row table, once, so each block's record loads wait on nothing else
     // (a split of more than ROWS_CAP rows reads them from the row table in global memory)
@@ -310,9 +310,7 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
     uint4 raw[PER_PROD];
     uint32_t vmask = 0;
     if (nblk > 0) vmask = load_raw(a, pt, pass_rows(0), pass_n(0), raw);
-    // Tile b & 1 last held block b - 2. S of that block (its K, every atom) is done once S full
-    // fired; P . V (its V: the four latent atoms of this half) once P . V done fired. So the
-    // five atoms P . V never reads are filled first, and only the V atoms wait for P . V.
+    // dequantise this thread's chunks of rows [32 half, 32 half + 32) of a block into its tile
     const auto fill = [&](uint8_t* tile, int half) {
 #pragma unroll
       for (int i = 0; i < PER_PROD; ++i) {
