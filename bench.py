@@ -428,6 +428,7 @@ def run_ours(args, ws, rank, local):
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     total_s = max_over_ranks(sum(step_ms) * 1e-3, ws)
     err = hs.hs_get_error(h, clear=True)
+    copy_ctas, launches_per_resolve = hs.hs_launch_shape(h)
     misses = miss_acc[W_:].sum(dim=1).cpu().numpy()  # per timed step, all requests
     rows_timed = valid_rows * K_
     value = ws * rows_timed / total_s
@@ -547,7 +548,9 @@ def run_ours(args, ws, rank, local):
                      "traffic": traffic.get("sysmem_read_bytes_per_launch"),
                      "traffic_metric": "ncu syslts sysmem read sectors x 32 B per launch (null: kernel changed)",
                      "algorithmic_bytes_per_launch": float(miss_bytes.mean()),
-                     "kernel": "resolve_kernel",
+                     "kernel": "resolve_kernel" if launches_per_resolve == 1 else
+                               "resolve_kernel + gather_kernel (no copy CTAs: follower layers gathered)",
+                     "copy_ctas_per_request": copy_ctas,
                      "peak_source": "pinned cudaMemcpy H2D, 1 GiB, best of 12, measured in this run",
                      "hbm": {"achieved": hbm_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": hbm_gbs / hbm_peak,
                              "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)",
@@ -566,7 +569,7 @@ def run_ours(args, ws, rank, local):
                                  "copy of the outputs in the graph"},
         "host_pool": ("huge pages, hs_host_register" if _HOST_POOLS[key][0][1]
                       else "cudaHostAlloc (host could not back the pool with huge pages)"),
-        "gpu_launches": 2 * K_,
+        "gpu_launches": (launches_per_resolve + 1) * K_,
         "device_flags": err,
         "clocks": clocks.summary(),
     }
@@ -775,10 +778,17 @@ def run_split(args, ws, rank, local):
                     evs[1 + l].record(stream)  # every layer ready at once
         hs.hs_backup(h, R, sl_buf, hcl, dbl, rp, stream)
 
-    # steps interleave the variants (fused, then split, on the same step's inputs), so both
-    # meet the host pool in the same state
+    # steps interleave the variants on the same step's inputs, so all meet the host pool in the
+    # same state; the order rotates each step, since the first to read a step's rows pays for
+    # the host pages it is first to reach
+    variants = ("fused", "split", "split0")
+
+    def rotated(s):
+        k = s % len(variants)
+        return variants[k:] + variants[:k]
+
     for s in range(W_):
-        for v in ("fused", "split", "split0"):
+        for v in rotated(s):
             one_step(s, v, None)
     torch.cuda.synchronize()
     evs = {v: [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(K_)]
@@ -786,12 +796,16 @@ def run_split(args, ws, rank, local):
     barrier(ws)
     torch.cuda.synchronize()
     for i in range(K_):
-        for v in ("fused", "split", "split0"):
+        for v in rotated(W_ + i):
             one_step(W_ + i, v, evs[v][i])
     torch.cuda.synchronize()
     barrier(ws)
     res = {v: np.array([[e[0].elapsed_time(e[1 + l]) * 1e3 for l in range(L)] for e in evs[v]]) for v in evs}
     err = 0
+    copy_ctas, per_resolve = hs.hs_launch_shape(handles["fused"])
+    order = 2  # the two kernels that group the plan by host region before follower gathers
+    split_launches = (per_resolve if copy_ctas == 0 else 1 + order) + (L - 1) + 1
+    split0_launches = 1 + order + 1 + (L - 1) + 1
     for h in handles.values():
         err |= hs.hs_get_error(h, clear=True)
         hs.hs_destroy(h)
@@ -815,7 +829,8 @@ def run_split(args, ws, rank, local):
         "split0_layer_ready_us_p50": [float(x) for x in np.median(s0, 0)],
         "split0": "hs_resolve_layers(copy_layers=0), hs_gather(0, 1) on the same stream, followers on the copy stream",
         "misses_per_step": float(miss.sum().item()),
-        "gpu_launches": K_ * (1 + (L - 1) + 1), "device_flags": err,
+        "gpu_launches": K_ * ((per_resolve + 1) + split_launches + split0_launches), "device_flags": err,
+        "copy_ctas_per_request": copy_ctas,
         "host_pool": "huge pages, hs_host_register" if pools[0][1] else "cudaHostAlloc",
     }
     if rank == 0:

@@ -32,7 +32,7 @@ EXPORTS = ("hs_workspace_bytes", "hs_create", "hs_resolve", "hs_backup", "hs_get
            "hs_status_str", "hs_host_register", "hs_host_unregister", "hs_resolve_noalloc",
            "hs_invalidate_tokens", "hs_invalidate_host_rows", "hs_resolve_layers", "hs_gather",
            "hs_resolve_spec", "hs_backup_spec", "hs_reset_hints", "hs_sparse_mla_workspace_bytes",
-           "hs_sparse_mla_decode")
+           "hs_sparse_mla_decode", "hs_launch_shape")
 HS_MAX_SPEC_QUERIES = 8
 HS_NOALLOC_MAX_LAYERS = 8
 
@@ -72,6 +72,8 @@ def _load() -> ctypes.CDLL:
     lib.hs_sparse_mla_decode.restype = ctypes.c_int
     lib.hs_reset_hints.argtypes = [P, P]
     lib.hs_reset_hints.restype = ctypes.c_int
+    lib.hs_launch_shape.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+    lib.hs_launch_shape.restype = ctypes.c_int
     lib.hs_resolve_spec.argtypes = [P, i32, i32] + [P] * 10 + [P]
     lib.hs_resolve_spec.restype = ctypes.c_int
     lib.hs_backup_spec.argtypes = [P, i32, i32] + [P] * 5 + [P]
@@ -251,6 +253,13 @@ def hs_sparse_mla_decode(num_requests: int, num_heads: int, top_k: int, splits: 
 
 def hs_reset_hints(h: Handle, stream=None) -> None:
     _check(_lib.hs_reset_hints(h.ptr if h else None, _stream(stream)), "hs_reset_hints")
+
+
+def hs_launch_shape(h: Handle):
+    """(copy CTAs per request, kernel launches per hs_resolve) chosen by hs_create."""
+    c, n = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(_lib.hs_launch_shape(h.ptr if h else None, ctypes.byref(c), ctypes.byref(n)), "hs_launch_shape")
+    return int(c.value), int(n.value)
 
 
 def hs_get_error(h: Handle, clear: bool = False) -> int:

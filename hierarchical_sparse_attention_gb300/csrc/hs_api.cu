@@ -15,6 +15,11 @@ struct hs_handle {
   int32_t* plan_tok;       // follower plan inside the caller's workspace: tokens [R, K],
   int32_t* plan_dst;       //   device rows [R, K],
   int32_t* plan_cnt;       //   counts [R]
+  hs::OrderArgs order;     // the plan's misses in host-region order (hs_gather copies these)
+  // What the last resolve left for hs_gather, as the calls were issued (stream order is call
+  // order for calls on one stream, and a graph replays its calls in capture order).
+  enum { kNoPlan, kPlan, kPairs, kSpec } plan_state;
+  int32_t plan_requests;   // num_requests of that resolve
   int device;
 };
 
@@ -46,7 +51,8 @@ extern "C" {
 
 size_t hs_workspace_bytes(const hs_config* cfg) {
   return config_ok(cfg) ? hs::kWorkspaceBytes + hs::hint_bytes(cfg->max_requests, cfg->max_context) +
-                              hs::plan_bytes(cfg->max_requests, cfg->top_k)
+                              hs::plan_bytes(cfg->max_requests, cfg->top_k) +
+                              hs::order_bytes(cfg->max_requests, cfg->top_k)
                         : 0;
 }
 
@@ -78,6 +84,12 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   if (g.hash_bits < ceil_log2(cfg->top_k) + 1) g.hash_bits = ceil_log2(cfg->top_k) + 1;  // room for the aliases
   g.host_rows = host_rows;
   g.device_rows = device_rows;
+  // host regions of at most kOrderRegionBytes (at least one row), coarser for pools that
+  // need more than kOrderRegions of them
+  g.order_shift = 0;
+  while (((int64_t)2 << g.order_shift) * g.B <= hs::kOrderRegionBytes) ++g.order_shift;
+  while (((host_rows - 1) >> g.order_shift) + 1 > hs::kOrderRegions) ++g.order_shift;
+  g.order_regions = (int32_t)(((host_rows - 1) >> g.order_shift) + 1);
 
   hs::Pools pools{};
   bool a16 = (g.B % 16) == 0, a4 = (g.B % 4) == 0;
@@ -123,6 +135,9 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   uint8_t* plan = ws + hs::kWorkspaceBytes + hs::hint_bytes(cfg->max_requests, cfg->max_context);
   if (cudaMemset(plan, 0, hs::plan_bytes(cfg->max_requests, cfg->top_k)) != cudaSuccess)
     return HS_ERR_CUDA;  // no plan yet: a gather before the first resolve copies nothing
+  uint8_t* order = plan + hs::plan_bytes(cfg->max_requests, cfg->top_k);
+  if (cudaMemset(order, 0, hs::order_bytes(cfg->max_requests, cfg->top_k)) != cudaSuccess)
+    return HS_ERR_CUDA;  // region counts and the count kernel's ticket start at zero
   if (cudaMemcpy(ws + hs::kPoolsOffset, &pools, sizeof(pools), cudaMemcpyHostToDevice) != cudaSuccess)
     return HS_ERR_CUDA;
 
@@ -137,6 +152,12 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   h->plan_tok = reinterpret_cast<int32_t*>(plan);
   h->plan_dst = h->plan_tok + RK;
   h->plan_cnt = h->plan_dst + RK;
+  int32_t* o = reinterpret_cast<int32_t*>(order);
+  h->order = hs::OrderArgs{nullptr, h->plan_tok, h->plan_dst, h->plan_cnt, o, o + RK, o + 2 * RK,
+                           o + 3 * RK, o + 3 * RK + (hs::kOrderRegions + 1),
+                           o + 3 * RK + 2 * (hs::kOrderRegions + 1),
+                           reinterpret_cast<uint32_t*>(o + 3 * RK + 2 * (hs::kOrderRegions + 1) + 1), (int64_t)RK};
+  h->plan_state = hs_handle::kNoPlan;
   h->device = dev;
   *out = h;
   return HS_OK;
@@ -154,11 +175,29 @@ hs_status hs_resolve_layers(hs_handle* h, int32_t num_requests, const int32_t* t
       !lru_slots || !lru_clock || !out_rows)
     return HS_ERR_INVALID_ARG;
   if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
+  // Without copy CTAs (more requests than the SMs give clusters to), each resolve CTA would
+  // copy its own miss rows, in miss order, once its exact pass is done. The resolve then
+  // copies nothing; its plan is put in host-region order and one gather over a wide grid
+  // copies every layer's rows, in stream order, with the same results. The ordered plan is
+  // also built whenever follower layers are left for hs_gather.
+  const bool gather_after = h->g.copy_ctas == 0 && copy_layers > 0;
+  const bool order = h->g.copy_ctas == 0 || copy_layers < h->cfg.num_layers;
   hs::ResolveArgs a{h->hint,   top_k_tokens, seq_lens,   host_cache_locs, device_buffer_locs, device_buffer_tokens,
-                    lru_slots, lru_clock,    resident_pages, out_rows,   miss_counts,        copy_layers,
+                    lru_slots, lru_clock,    resident_pages, out_rows,   miss_counts,        gather_after ? 0 : copy_layers,
                     h->plan_tok, h->plan_dst, h->plan_cnt, -1, 1};
   if (hs::launch_resolve(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
     return HS_ERR_CUDA;
+  h->plan_state = order ? hs_handle::kPairs : hs_handle::kPlan;
+  h->plan_requests = num_requests;
+  if (order) {
+    hs::OrderArgs oa = h->order;
+    oa.host_cache_locs = host_cache_locs;
+    if (hs::launch_order(h->g, oa, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+      return HS_ERR_CUDA;
+    if (gather_after &&
+        hs::launch_gather_pairs(h->g, h->pools, oa, num_requests, 0, copy_layers, (cudaStream_t)stream) != cudaSuccess)
+      return HS_ERR_CUDA;
+  }
   return HS_OK;
 }
 
@@ -186,6 +225,7 @@ hs_status hs_resolve_spec(hs_handle* h, int32_t num_requests, int32_t num_querie
     return HS_ERR_INVALID_ARG;
   if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
   const size_t RK = (size_t)num_requests * (size_t)h->cfg.top_k;
+  h->plan_state = hs_handle::kSpec;
   // The verify steps run in order on the stream, one launch each, over the shared state.
   for (int32_t q = 0; q < num_queries; ++q) {
     hs::ResolveArgs a{h->hint,   top_k_tokens + q * RK, committed_lens, host_cache_locs, device_buffer_locs,
@@ -218,6 +258,15 @@ hs_status hs_gather(hs_handle* h, int32_t num_requests, const int32_t* host_cach
   if (first_layer < 0 || num_layers < 0 || first_layer + num_layers > h->cfg.num_layers) return HS_ERR_INVALID_ARG;
   if (num_requests == 0 || num_layers == 0) return HS_OK;
   if (!host_cache_locs) return HS_ERR_INVALID_ARG;
+  if (h->plan_state == hs_handle::kSpec) return HS_ERR_INVALID_ARG;  // a speculative batch records no plan
+  if (h->plan_state == hs_handle::kPairs) {
+    // the ordered plan covers the resolve's requests, all of them
+    if (num_requests != h->plan_requests) return HS_ERR_INVALID_ARG;
+    if (hs::launch_gather_pairs(h->g, h->pools, h->order, num_requests, first_layer, num_layers,
+                                (cudaStream_t)stream) != cudaSuccess)
+      return HS_ERR_CUDA;
+    return HS_OK;
+  }
   hs::GatherArgs a{host_cache_locs, h->plan_tok, h->plan_dst, h->plan_cnt, first_layer, num_layers};
   if (hs::launch_gather(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
     return HS_ERR_CUDA;
@@ -298,6 +347,13 @@ hs_status hs_reset_hints(hs_handle* h, hs_stream_t stream) {
     cudaGetLastError();
     return HS_ERR_CUDA;
   }
+  return HS_OK;
+}
+
+hs_status hs_launch_shape(const hs_handle* h, int32_t* copy_ctas, int32_t* resolve_launches) {
+  if (!h) return HS_ERR_INVALID_ARG;
+  if (copy_ctas) *copy_ctas = h->g.copy_ctas;
+  if (resolve_launches) *resolve_launches = h->g.copy_ctas == 0 ? 4 : 1;
   return HS_OK;
 }
 

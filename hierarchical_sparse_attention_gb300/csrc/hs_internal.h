@@ -38,6 +38,9 @@ struct Geometry {
                       // reads it from global memory (large H, where the table does not fit)
   int32_t bit_words;  // uint32 words per request in the residency bitmap (a multiple of 4)
   int32_t bits_smem;  // 1: each copy CTA stages its request's bitmap row in shared memory
+  int32_t order_shift;    // host rows [b << order_shift, (b + 1) << order_shift) form host region b
+  int32_t order_regions;  // regions covering the host pool (<= kOrderRegions); region
+                          // order_regions collects misses whose host row is out of range
   int64_t host_rows, device_rows;
 };
 
@@ -68,6 +71,23 @@ struct GatherArgs {
   const int32_t* plan_dst;
   const int32_t* plan_cnt;
   int32_t first_layer, num_layers;
+};
+
+// The last resolve's misses as (host row, device row) pairs grouped by host region, built by
+// launch_order and copied by launch_gather_pairs. Arrays live in the workspace (order_bytes).
+struct OrderArgs {
+  const int32_t* host_cache_locs;
+  const int32_t* plan_tok;
+  const int32_t* plan_dst;
+  const int32_t* plan_cnt;
+  int32_t* miss_src;   // [R, K] per plan entry: host row, -1 out of range, -2 no device row
+  int32_t* pair_src;   // [R * K] host rows (-1: zero-fill), grouped by region
+  int32_t* pair_dst;   // [R * K] device rows
+  int32_t* counts;     // [kOrderRegions + 1] misses per region (zero between steps)
+  int32_t* cursors;    // [kOrderRegions + 1] next free position per region
+  int32_t* n_pairs;    // pairs in the list
+  uint32_t* ticket;    // CTAs of the count kernel done (zero between steps)
+  int64_t capacity;    // max_requests * K
 };
 
 struct BackupArgs {
@@ -133,6 +153,16 @@ inline size_t plan_bytes(int64_t max_requests, int64_t top_k) {
   return (size_t)(((max_requests * top_k * 8 + max_requests * 4) + 255) & ~(int64_t)255);
 }
 
+// After the plan: the host-ordered copy of it (OrderArgs). A gather that takes the misses in
+// host-address order, so that neighbouring rows share a 2 MB host region, reuses the GPU's
+// translation of each region for several rows; in the order the resolve found them, misses
+// spread over several large pools ran at about half the link rate.
+constexpr int32_t kOrderRegions = 16384;
+constexpr int64_t kOrderRegionBytes = 2 << 20;
+inline size_t order_bytes(int64_t max_requests, int64_t top_k) {
+  return (size_t)((((max_requests * top_k * 3 + 2 * (int64_t)(kOrderRegions + 1) + 2) * 4) + 255) & ~(int64_t)255);
+}
+
 // Dynamic shared memory of one resolve-kernel CTA for geometry g.
 size_t resolve_smem_bytes(const Geometry& g);
 // Fit the resolve CTA's tables to the device's shared memory (sets g.dbl_smem, and for the
@@ -146,6 +176,13 @@ cudaError_t launch_backup(const Geometry& g, const Pools* pools, const BackupArg
                           uint32_t* err_word, cudaStream_t stream);
 cudaError_t launch_gather(const Geometry& g, const Pools* pools, const GatherArgs& a, int32_t num_requests,
                           uint32_t* err_word, cudaStream_t stream);
+// Two launches: count the plan's misses per host region (the last CTA turns the counts into
+// region offsets), then place each miss's (host row, device row) pair in its region.
+cudaError_t launch_order(const Geometry& g, const OrderArgs& a, int32_t num_requests, uint32_t* err_word,
+                         cudaStream_t stream);
+// Copy the ordered pairs' rows for layers [first_layer, first_layer + num_layers).
+cudaError_t launch_gather_pairs(const Geometry& g, const Pools* pools, const OrderArgs& a, int32_t num_requests,
+                                int32_t first_layer, int32_t num_layers, cudaStream_t stream);
 size_t sparse_mla_smem_bytes();
 cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, float* part_o, float* part_lse,
                               uint32_t* err, cudaStream_t stream);

@@ -171,7 +171,13 @@ typedef struct hs_handle hs_handle;
  *     probe, so bits left stale by changes the caller makes to the state arrays cost time,
  *     never correctness;
  *   - the follower plan of the last resolve: miss tokens and device rows, max_requests x
- *     top_k int32 each, then max_requests counts (hs_gather replays it).
+ *     top_k int32 each, then max_requests counts (hs_gather replays it);
+ *   - the same misses grouped by 2 MB region of the host pool: per plan entry its host row,
+ *     then (host row, device row) pairs, max_requests x top_k int32 each, and two tables of
+ *     16,385 per-region int32 counters. A copy that takes the rows region by region reuses
+ *     the GPU's address translation of each region for several rows; in the order the
+ *     resolve finds them, rows spread over several large pools moved at about half the
+ *     host link's rate.
  * The caller keeps the workspace for the handle's lifetime and does not write to it. */
 HS_API size_t hs_workspace_bytes(const hs_config* cfg);
 
@@ -185,7 +191,11 @@ HS_API hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* 
                     int64_t host_rows, int64_t device_rows, void* workspace, hs_handle** out);
 
 /* One decode step of the resolver for requests 0..num_requests-1 (layout above): one
- * kernel launch on `stream`, no allocation, no synchronisation, capturable in a CUDA
+ * kernel launch on `stream` -- four when the configuration leaves no room for copy CTAs
+ * (more requests than the GPU has SMs, or rows not 16-byte copyable): the resolve then
+ * records the miss plan without copying, two small kernels group the misses by host
+ * region, and a gather kernel copies every layer's rows, with the same results
+ * (hs_launch_shape tells which). No allocation, no synchronisation, capturable in a CUDA
  * graph. num_requests == 0 is a no-op. */
 HS_API hs_status hs_resolve(hs_handle* h, int32_t num_requests, const int32_t* top_k_tokens,
                      const int32_t* seq_lens, const int32_t* host_cache_locs,
@@ -198,8 +208,10 @@ HS_API hs_status hs_resolve(hs_handle* h, int32_t num_requests, const int32_t* t
  * and copy only their own bytes). The step is resolved exactly as by hs_resolve, but miss
  * rows are copied only for layers [0, copy_layers) (0 <= copy_layers <= num_layers), and
  * the miss plan -- per request, the miss tokens and their device rows in miss order -- is
- * kept in the workspace for hs_gather. hs_resolve is this call with copy_layers =
- * num_layers (it records the plan too). Same rules as hs_resolve. */
+ * kept in the workspace for hs_gather. When copy_layers < num_layers, or the geometry has
+ * no copy CTAs, the call also groups the plan by host region (two more launches), and the
+ * gathers that follow copy the rows in that order. hs_resolve is this call with
+ * copy_layers = num_layers (it records the plan too). Same rules as hs_resolve. */
 HS_API hs_status hs_resolve_layers(hs_handle* h, int32_t num_requests, const int32_t* top_k_tokens,
                                    const int32_t* seq_lens, const int32_t* host_cache_locs,
                                    const int32_t* device_buffer_locs, int32_t* device_buffer_tokens,
@@ -246,8 +258,11 @@ HS_API hs_status hs_backup_spec(hs_handle* h, int32_t num_requests, int32_t num_
  * planned miss, zeros (HS_FLAG_HOSTROW) when the host row is out of range -- with no LRU
  * work. host_cache_locs [R, max_context] device, read (the resolve's). It must run after
  * that resolve (same stream, or an event) and before the next one; calls for different
- * layers may run on other streams concurrently. One kernel launch; no allocation, no
- * synchronisation; graph-capturable. num_layers == 0 is a no-op. */
+ * layers may run on other streams concurrently. When that resolve grouped its plan by host
+ * region (hs_resolve_layers), the rows are copied in that order and num_requests must be
+ * the resolve's; otherwise the plan of requests 0..num_requests-1 is replayed in miss order.
+ * HS_ERR_INVALID_ARG after hs_resolve_spec, which records no plan. One kernel launch, layer
+ * by layer; no allocation, no synchronisation; graph-capturable. num_layers == 0 is a no-op. */
 HS_API hs_status hs_gather(hs_handle* h, int32_t num_requests, const int32_t* host_cache_locs,
                            int32_t first_layer, int32_t num_layers, hs_stream_t stream);
 
@@ -320,6 +335,12 @@ HS_API hs_status hs_sparse_mla_decode(int32_t num_requests, int32_t num_heads, i
  * and each hit sets its bit back. Results never depend on it: stale bits cost only speed.
  * One cudaMemsetAsync of about max_requests x max_context / 8 bytes; graph-capturable. */
 HS_API hs_status hs_reset_hints(hs_handle* h, hs_stream_t stream);
+
+/* The launch shape hs_create chose for this handle (host only; no device work). copy_ctas:
+ * copy CTAs clustered with each request's resolve CTA, 0..3. resolve_launches: kernel launches one hs_resolve makes, 1, or 4 when
+ * copy_ctas is 0 (the rows then move in a gather over the plan grouped by host region).
+ * Either pointer may be NULL. HS_ERR_INVALID_ARG for a NULL handle. */
+HS_API hs_status hs_launch_shape(const hs_handle* h, int32_t* copy_ctas, int32_t* resolve_launches);
 
 /* Read the workspace error word (synchronises the device; not for the hot path). With
  * clear != 0 the word is reset to zero. Returns HS_ERR_DEVICE_FLAGGED when any bit is set. */

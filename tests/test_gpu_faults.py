@@ -17,15 +17,33 @@ pytestmark = pytest.mark.gpu
 ERR = dict(TOKEN=1, DUP=2, STATE=4, HOSTROW=8, DEVROW=16, SEQLEN=32)
 
 
-@pytest.fixture
-def pair():
+def _make_pair(requests=4, layers=1):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from gpu_harness import GpuSim, host_pools
-    wl = W.make("dsa", requests=4, top_k=256, hot_slots=512, steps=12, seq0=(6000, 7000, 8000, 300))
+    seq0 = (6000, 7000, 8000, 300) + (5000,) * (requests - 4)
+    wl = W.make("dsa", requests=requests, top_k=256, hot_slots=512, steps=12, seq0=seq0, layers=layers)
     host = host_pools(wl)
     orc = OracleSim(wl, host_pools=host)
     gpu = GpuSim(wl, host, orc.dev)
+    return wl, orc, gpu
+
+
+@pytest.fixture
+def pair():
+    wl, orc, gpu = _make_pair()
+    yield wl, orc, gpu
+    gpu.close()
+
+
+@pytest.fixture(params=["copy_ctas", "no_copy_ctas"])
+def pair_any(request):
+    """The 4-request shape (copy CTAs beside each resolve CTA), and 160 requests x 2 layers,
+    which leave no SM for copy CTAs: the resolve records its plan, the plan is grouped by
+    host region, and a gather copies both layers."""
+    import hierarchical_sparse_attention_gb300 as hs
+    wl, orc, gpu = _make_pair(*((4, 1) if request.param == "copy_ctas" else (160, 2)))
+    assert (hs.hs_launch_shape(gpu.h)[0] == 0) == (request.param == "no_copy_ctas")
     yield wl, orc, gpu
     gpu.close()
 
@@ -108,8 +126,8 @@ def test_bad_and_repeated_tokens(pair):
     assert err == ERR["TOKEN"] | ERR["DUP"]
 
 
-def test_host_row_out_of_range_zero_fills(pair):
-    wl, orc, gpu = pair
+def test_host_row_out_of_range_zero_fills(pair_any):
+    wl, orc, gpu = pair_any
     warm(wl, orc, gpu)
     tk = wl.top_k_tokens(3)
     hcl = wl.host_cache_locs.copy()
@@ -122,8 +140,8 @@ def test_host_row_out_of_range_zero_fills(pair):
     assert err == ERR["HOSTROW"]
 
 
-def test_device_row_out_of_range(pair):
-    wl, orc, gpu = pair
+def test_device_row_out_of_range(pair_any):
+    wl, orc, gpu = pair_any
     warm(wl, orc, gpu)
     dbl = wl.device_buffer_locs.copy()
     dbl[0, wl.H] = wl.device_rows + 3  # reserved newest row of a long request

@@ -105,6 +105,31 @@ def test_indexshare_4_layers():
     run_parity(W.make("indexshare"), pool_every=32)
 
 
+def test_no_copy_ctas_resolve_and_gather_in_a_graph():
+    """80 requests leave no SM for copy CTAs, so hs_resolve is four launches: the resolve
+    (recording its plan, copying nothing), the two kernels that group the plan by host region,
+    and a gather of all 3 layers. Eager for two steps, then the four replayed from a CUDA
+    graph; every layer's rows match the oracle."""
+    import hierarchical_sparse_attention_gb300 as hs
+    GpuSim, host_pools = _gpu()
+    wl = W.make("indexshare", 9, requests=80, top_k=64, hot_slots=128, steps=6, layers=3, seq_range=(1000, 3000))
+    host = host_pools(wl)
+    gpu = GpuSim(wl, host, OracleSim(wl, host_pools=host).dev)
+    try:
+        assert hs.hs_launch_shape(gpu.h) == (0, 4)
+    finally:
+        gpu.close()
+    run_parity(wl, host=host, graph_from=2)
+    few = W.make("indexshare", 9, requests=4, top_k=64, hot_slots=128, steps=1, layers=3, seq_range=(1000, 3000))
+    host = host_pools(few)
+    gpu = GpuSim(few, host, OracleSim(few, host_pools=host).dev)
+    try:
+        copy_ctas, launches = hs.hs_launch_shape(gpu.h)
+        assert copy_ctas > 0 and launches == 1
+    finally:
+        gpu.close()
+
+
 def test_miss_rate_sweep():
     _, host_pools = _gpu()
     base = W.make("sweep_h4096_f0.8")

@@ -149,5 +149,16 @@ def test_leader_only_step_matches_the_oracle():
         with pytest.raises(hs.HsError):
             hs.hs_resolve_layers(gpu.h, wl.R, gpu.tk, gpu.sl, gpu.hcl, gpu.dbl, gpu.tok, gpu.st, gpu.clk, gpu.rp,
                                  gpu.out, gpu.miss, wl.L + 1)
+        # the plan was grouped by host region over all the resolve's requests: a gather of
+        # fewer is refused; after a speculative batch (which records no plan) any gather is
+        hs.hs_gather(gpu.h, wl.R, gpu.hcl, 1, 1)
+        with pytest.raises(hs.HsError):
+            hs.hs_gather(gpu.h, wl.R - 1, gpu.hcl, 1, 1)
+        committed = (gpu.sl - 1).contiguous()
+        hs.hs_resolve_spec(gpu.h, wl.R, 1, gpu.tk, committed, gpu.hcl, gpu.dbl, gpu.tok, gpu.st, gpu.clk, gpu.rp,
+                           gpu.out, gpu.miss)
+        with pytest.raises(hs.HsError):
+            hs.hs_gather(gpu.h, wl.R, gpu.hcl, 1, 1)
+        torch.cuda.synchronize()
     finally:
         gpu.close()
