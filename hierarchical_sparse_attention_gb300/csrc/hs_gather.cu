@@ -99,29 +99,29 @@ __global__ void __launch_bounds__(T) gather_kernel(const Geometry g, const Pools
   if (flags) atomicOr(err_word, flags);
 }
 
-constexpr int kOrderThreads = 256;  // one plan entry per thread
+constexpr int kOrderThreads = 1024;  // one CTA per request; its threads stride over the plan
 constexpr int32_t kNoRow = -2;      // plan entry without a device row: nothing to copy
+constexpr int kScanBatch = 8;       // counters loaded together in the region scan
 
 __device__ __forceinline__ int32_t region_of(const Geometry& g, int32_t src) {
   return src >= 0 ? (src >> g.order_shift) : g.order_regions;
 }
 
-// Count the plan's misses per host region. Each CTA takes kOrderThreads entries of one
-// request; the last CTA to finish (a ticket taken after a fence, so every count is in L2)
-// turns the counts into exclusive offsets, zeroes them for the next step and stores the total.
+// Count the plan's misses per host region. One CTA per request walks its plan; the last CTA
+// to finish (a ticket taken after a fence, so every count is in L2) turns the counts into
+// exclusive offsets, zeroes them for the next step and stores the total. (CTAs per run of
+// entries, most of them empty, spent more time taking the one ticket in turn than counting.)
 __global__ void __launch_bounds__(kOrderThreads) order_count_kernel(const Geometry g, const OrderArgs a,
                                                                     uint32_t* __restrict__ err_word) {
   __shared__ int32_t s_warp[kOrderThreads / 32];
   __shared__ int s_last;
   const int r = blockIdx.x;
-  const int j = (int)blockIdx.y * kOrderThreads + (int)threadIdx.x;
-  const int m = a.plan_cnt[r];
-  if (j < m && j < g.K) {
+  const int m = min(a.plan_cnt[r], g.K);
+  for (int j = threadIdx.x; j < m; j += kOrderThreads) {
     const size_t at = (size_t)r * g.K + j;
-    const int32_t d = a.plan_dst[at];
+    const int32_t d = a.plan_dst[at], t = a.plan_tok[at];
     int32_t src = kNoRow;
     if (d >= 0) {
-      const int32_t t = a.plan_tok[at];
       const int32_t hr = (t >= 0 && t < g.max_context) ? a.host_cache_locs[(size_t)r * g.max_context + t] : -1;
       src = (hr >= 0 && (int64_t)hr < g.host_rows) ? hr : -1;
       if (src < 0) atomicOr(err_word, HS_FLAG_HOSTROW);  // its rows are zero-filled, as the resolve's are
@@ -131,16 +131,23 @@ __global__ void __launch_bounds__(kOrderThreads) order_count_kernel(const Geomet
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(a.ticket, 1u) == gridDim.x * gridDim.y - 1;
+  if (threadIdx.x == 0) s_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  // each thread scans a contiguous run of counters, eight loads in flight at a time (the
+  // counters sit in L2; one dependent load per counter made this the kernel's longest part)
   const int n = g.order_regions + 1;
   const int per = (n + kOrderThreads - 1) / kOrderThreads;
   const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
   int sum = 0;
-#pragma unroll 8
-  for (int i = lo; i < hi; ++i) sum += __ldcg(a.counts + i);
+  for (int i0 = lo; i0 < hi; i0 += kScanBatch) {
+    int v[kScanBatch];
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) v[u] = i0 + u < hi ? __ldcg(a.counts + i0 + u) : 0;
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) sum += v[u];
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = sum;
 #pragma unroll
@@ -152,11 +159,17 @@ __global__ void __launch_bounds__(kOrderThreads) order_count_kernel(const Geomet
   __syncthreads();
   int run = incl - sum;
   for (int w = 0; w < warp; ++w) run += s_warp[w];
-  for (int i = lo; i < hi; ++i) {
-    const int c = __ldcg(a.counts + i);
-    a.cursors[i] = run;
-    run += c;
-    a.counts[i] = 0;
+  for (int i0 = lo; i0 < hi; i0 += kScanBatch) {
+    int v[kScanBatch];
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) v[u] = i0 + u < hi ? __ldcg(a.counts + i0 + u) : 0;
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u)
+      if (i0 + u < hi) {
+        a.cursors[i0 + u] = run;
+        run += v[u];
+        a.counts[i0 + u] = 0;
+      }
   }
   if (threadIdx.x == kOrderThreads - 1) {
     *a.n_pairs = run;  // the last thread's range ends the array: run is the total
@@ -164,19 +177,19 @@ __global__ void __launch_bounds__(kOrderThreads) order_count_kernel(const Geomet
   }
 }
 
-// Place each counted miss at its region's next position.
+// Place each counted miss at its region's next position (one CTA per request).
 __global__ void __launch_bounds__(kOrderThreads) order_scatter_kernel(const Geometry g, const OrderArgs a) {
   const int r = blockIdx.x;
-  const int j = (int)blockIdx.y * kOrderThreads + (int)threadIdx.x;
-  const int m = a.plan_cnt[r];
-  if (j >= m || j >= g.K) return;
-  const size_t at = (size_t)r * g.K + j;
-  const int32_t src = a.miss_src[at];
-  if (src == kNoRow) return;
-  const int pos = atomicAdd(a.cursors + region_of(g, src), 1);
-  if (pos < 0 || pos >= a.capacity) return;  // only a workspace the caller overwrote gets here
-  a.pair_src[pos] = src;
-  a.pair_dst[pos] = a.plan_dst[at];
+  const int m = min(a.plan_cnt[r], g.K);
+  for (int j = threadIdx.x; j < m; j += kOrderThreads) {
+    const size_t at = (size_t)r * g.K + j;
+    const int32_t src = a.miss_src[at], d = a.plan_dst[at];
+    if (src == kNoRow) continue;
+    const int pos = atomicAdd(a.cursors + region_of(g, src), 1);
+    if (pos < 0 || pos >= a.capacity) continue;  // only a workspace the caller overwrote gets here
+    a.pair_src[pos] = src;
+    a.pair_dst[pos] = d;
+  }
 }
 
 // Copy rows of the ordered pairs: a CTA takes M consecutive pairs of one layer; blocks are
@@ -237,9 +250,8 @@ cudaError_t launch_gather(const Geometry& g, const Pools* pools, const GatherArg
 
 cudaError_t launch_order(const Geometry& g, const OrderArgs& a, int32_t num_requests, uint32_t* err_word,
                          cudaStream_t stream) {
-  const dim3 grid(num_requests, (g.K + kOrderThreads - 1) / kOrderThreads);
-  order_count_kernel<<<grid, kOrderThreads, 0, stream>>>(g, a, err_word);
-  order_scatter_kernel<<<grid, kOrderThreads, 0, stream>>>(g, a);
+  order_count_kernel<<<num_requests, kOrderThreads, 0, stream>>>(g, a, err_word);
+  order_scatter_kernel<<<num_requests, kOrderThreads, 0, stream>>>(g, a);
   return cudaGetLastError();
 }
 
