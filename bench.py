@@ -190,16 +190,17 @@ def newest_rows(wl, step):
 
 
 def ncu_traffic(config: str) -> dict:
-    """Per-launch traffic of the resolve kernel from the committed ncu capture, when that
-    capture was taken on this workload and on the kernel source as it is now; else {}."""
+    """Per-launch traffic of the workload's dominant kernel from the committed ncu capture,
+    when one was taken on this workload and on the kernel source as it is now; else {}."""
     try:
-        rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
-        code = kernel_code_hash(os.path.join(ROOT, rec["kernel_source"]))
-    except (OSError, ValueError, KeyError):
-        return {}
-    if rec.get("workload") != config or code != rec.get("code_sha256_16"):
-        return {}
-    return rec
+        recs = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))["records"]
+        for rec in recs:
+            if rec.get("workload") == config and \
+                    kernel_code_hash(os.path.join(ROOT, rec["kernel_source"])) == rec.get("code_sha256_16"):
+                return rec
+    except (OSError, ValueError, KeyError, TypeError):
+        pass
+    return {}
 
 
 def kernel_code_hash(path: str) -> str:
@@ -549,7 +550,8 @@ def run_ours(args, ws, rank, local):
                      "traffic_metric": "ncu syslts sysmem read sectors x 32 B per launch (null: kernel changed)",
                      "algorithmic_bytes_per_launch": float(miss_bytes.mean()),
                      "kernel": "resolve_kernel" if launches_per_resolve == 1 else
-                               "resolve_kernel + gather_kernel (no copy CTAs: follower layers gathered)",
+                               "gather_pairs_kernel (no copy CTAs; the timed call also runs resolve_kernel, "
+                               "order_count_kernel and order_scatter_kernel)",
                      "copy_ctas_per_request": copy_ctas,
                      "peak_source": "pinned cudaMemcpy H2D, 1 GiB, best of 12, measured in this run",
                      "hbm": {"achieved": hbm_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": hbm_gbs / hbm_peak,
