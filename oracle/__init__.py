@@ -58,6 +58,9 @@ def _load():
         lib.oracle_resolve_plan.restype = None
         lib.oracle_resolve_spec.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32, ctypes.c_int32] + [P] * 13
         lib.oracle_resolve_spec.restype = None
+        lib.oracle_resolve_spec_plan.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32, ctypes.c_int32] + [P] * 13 + \
+            [ctypes.c_int32, P, P, P]
+        lib.oracle_resolve_spec_plan.restype = None
         lib.oracle_backup_spec.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32, ctypes.c_int32] + [P] * 8
         lib.oracle_backup_spec.restype = None
         lib.oracle_gather.argtypes = [ctypes.POINTER(Geom), ctypes.c_int32, P, P, P, P, ctypes.c_int32,
@@ -202,12 +205,25 @@ class Oracle:
                                              ctypes.byref(err))
         return int(err.value)
 
+    def new_spec_plan(self, Q: int, R: int) -> "Plan":
+        """Room for a speculative batch's plans: slice q (tokens[q], dst[q], count[q]) is
+        verify step q's miss plan; step_plan(plan, q) views it as a one-step Plan."""
+        return Plan(np.zeros((Q, R, self.g.top_k), np.int32), np.zeros((Q, R, self.g.top_k), np.int32),
+                    np.zeros((Q, R), np.int32))
+
+    @staticmethod
+    def step_plan(plan: "Plan", q: int) -> "Plan":
+        return Plan(plan.tokens[q], plan.dst[q], plan.count[q])
+
     def resolve_spec(self, top_k_tokens, committed_lens, host_cache_locs, device_buffer_locs,
                      device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows, miss_counts,
-                     host_pools, device_pools) -> int:
+                     host_pools, device_pools, copy_layers: Optional[int] = None,
+                     plan: Optional["Plan"] = None) -> int:
         """A speculative batch of Q = top_k_tokens.shape[0] verify steps, in order: step q
         resolves top_k_tokens[q] for committed_lens + q + 1 tokens into out_rows[q];
-        device_buffer_locs is [R, H + Q] (H slots, then Q reserved rows)."""
+        device_buffer_locs is [R, H + Q] (H slots, then Q reserved rows). With copy_layers <
+        num_layers each step copies only the leader layers; with a plan (new_spec_plan) each
+        step records its miss plan in its slice, for gather(step_plan(plan, q), ...)."""
         g = self.g
         Q, R = top_k_tokens.shape[0], committed_lens.shape[0]
         _i32(top_k_tokens, (Q, R, g.top_k)); _i32(committed_lens); _i32(host_cache_locs, (R, g.max_context))
@@ -220,10 +236,18 @@ class Oracle:
         err = ctypes.c_uint32(0)
         hp = self._pools(host_pools, g.host_rows)
         dp = self._pools(device_pools, g.device_rows)
-        self.lib.oracle_resolve_spec(ctypes.byref(g), R, Q, _p(top_k_tokens), _p(committed_lens),
-                                     _p(host_cache_locs), _p(device_buffer_locs), _p(device_buffer_tokens),
-                                     _p(lru_slots), _p(lru_clock), _p(resident_pages), _p(out_rows),
-                                     _p(miss_counts), hp, dp, ctypes.byref(err))
+        args = (ctypes.byref(g), R, Q, _p(top_k_tokens), _p(committed_lens), _p(host_cache_locs),
+                _p(device_buffer_locs), _p(device_buffer_tokens), _p(lru_slots), _p(lru_clock),
+                _p(resident_pages), _p(out_rows), _p(miss_counts), hp, dp, ctypes.byref(err))
+        if copy_layers is None and plan is None:
+            self.lib.oracle_resolve_spec(*args)
+        else:
+            cl = g.num_layers if copy_layers is None else int(copy_layers)
+            assert 0 <= cl <= g.num_layers
+            if plan is not None:
+                _i32(plan.tokens, (Q, R, g.top_k)); _i32(plan.dst, (Q, R, g.top_k)); _i32(plan.count, (Q, R))
+            self.lib.oracle_resolve_spec_plan(*args, cl, _p(plan.tokens) if plan else None,
+                                              _p(plan.dst) if plan else None, _p(plan.count) if plan else None)
         return int(err.value)
 
     def backup_spec(self, num_queries: int, committed_lens, accepted, host_cache_locs, device_buffer_locs,

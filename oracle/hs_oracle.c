@@ -297,6 +297,14 @@ void oracle_resolve_plan(const oracle_geom* g, int32_t num_requests, const int32
                copy_layers, plan_tokens, plan_dst, plan_count, -1, 1);
 }
 
+void oracle_resolve_spec_plan(const oracle_geom* g, int32_t num_requests, int32_t num_queries,
+                              const int32_t* top_k_tokens, const int32_t* committed_lens,
+                              const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
+                              int32_t* device_buffer_tokens, int32_t* lru_slots, int32_t* lru_clock,
+                              const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
+                              uint8_t* const* host_pools, uint8_t* const* device_pools, uint32_t* err,
+                              int32_t copy_layers, int32_t* plan_tokens, int32_t* plan_dst, int32_t* plan_count);
+
 /*
  * A speculative batch ([vLLM-arch] speculative decoding: each verify step is resolved and
  * consumed in order, with its own replayable plan rows and the request's shared hot state,
@@ -312,12 +320,34 @@ void oracle_resolve_spec(const oracle_geom* g, int32_t num_requests, int32_t num
                          int32_t* device_buffer_tokens, int32_t* lru_slots, int32_t* lru_clock,
                          const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
                          uint8_t* const* host_pools, uint8_t* const* device_pools, uint32_t* err) {
+  oracle_resolve_spec_plan(g, num_requests, num_queries, top_k_tokens, committed_lens, host_cache_locs,
+                           device_buffer_locs, device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows,
+                           miss_counts, host_pools, device_pools, err, g->num_layers, NULL, NULL, NULL);
+}
+
+/*
+ * The same batch for a layer group split into leader and followers ([vLLM-impl] 7.4: with
+ * IndexShare the follower layers replay the leader's miss plan; under MTP each verify step
+ * is its own resolve over its own slice of the workspace, sharing the request's hot state;
+ * [vLLM-arch] speculative decoding: every verify step has its own replayable plan rows).
+ * Verify step q copies its misses' rows for layers [0, copy_layers) only and records its
+ * miss plan in slice q: plan_tokens / plan_dst [Q, R, K], plan_count [Q, R] (all NULL:
+ * none kept). oracle_gather on slice q then copies step q's rows for the followers.
+ */
+void oracle_resolve_spec_plan(const oracle_geom* g, int32_t num_requests, int32_t num_queries,
+                              const int32_t* top_k_tokens, const int32_t* committed_lens,
+                              const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
+                              int32_t* device_buffer_tokens, int32_t* lru_slots, int32_t* lru_clock,
+                              const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
+                              uint8_t* const* host_pools, uint8_t* const* device_pools, uint32_t* err,
+                              int32_t copy_layers, int32_t* plan_tokens, int32_t* plan_dst, int32_t* plan_count) {
   const int64_t RK = (int64_t)num_requests * g->top_k;
   for (int32_t q = 0; q < num_queries; ++q)
     resolve_call(g, num_requests, top_k_tokens + q * RK, committed_lens, host_cache_locs, device_buffer_locs,
                  device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows + q * RK,
                  miss_counts ? miss_counts + (int64_t)q * num_requests : NULL, host_pools, device_pools, err,
-                 g->num_layers, NULL, NULL, NULL, q, num_queries);
+                 copy_layers, plan_tokens ? plan_tokens + q * RK : NULL, plan_dst ? plan_dst + q * RK : NULL,
+                 plan_count ? plan_count + (int64_t)q * num_requests : NULL, q, num_queries);
 }
 
 /* The whole step: every layer of the group gets its miss rows; no plan is kept. */

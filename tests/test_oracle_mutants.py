@@ -50,6 +50,8 @@ MUTANTS = [
     ("spec_marks_before_s0_only", "t <= base; ++t) tokens[t] = t;", "t < base; ++t) tokens[t] = t;"),
     ("spec_backup_first_reserved_row", "if (row < 0) row = t + 1 <= H ? dbl[t] : dbl[H + j];",
      "if (row < 0) row = t + 1 <= H ? dbl[t] : dbl[H];"),
+    ("spec_plans_share_one_slice", "copy_layers, plan_tokens ? plan_tokens + q * RK : NULL, plan_dst ? plan_dst + q * RK : NULL,",
+     "copy_layers, plan_tokens, plan_dst,"),
 ]
 
 

@@ -415,7 +415,8 @@ def run_all_pins() -> int:
     checks += [sp.test_leader_only_leaves_followers]
     import test_oracle_spec as spec
     checks += [spec.test_spec_golden, lambda: spec.test_one_query_batch_is_a_plain_step("tiny"),
-               lambda: spec.test_replayable_plans("dsa_small", 4)]
+               lambda: spec.test_replayable_plans("dsa_small", 4),
+               lambda: spec.test_leader_batch_and_step_gathers_equal_the_full_batch(1)]
     failed = 0
     for c in checks:
         try:

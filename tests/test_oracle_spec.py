@@ -159,6 +159,25 @@ class SpecRun:
             self.prev[r] = tk[Q - 1, r][tk[Q - 1, r] >= 0]
         return out, miss, err
 
+    def resolve_split(self, tk, copy_layers):
+        """The batch with only layers [0, copy_layers) copied by the verify steps, each step's
+        miss plan recorded, then every step's plan gathered for the follower layers, in step
+        order. Returns (out, miss, err, plan)."""
+        wl, Q = self.wl, self.Q
+        out = np.zeros((Q, wl.R, wl.K), np.int32)
+        miss = np.zeros((Q, wl.R), np.int32)
+        plan = self.orc.new_spec_plan(Q, wl.R)
+        err = self.orc.resolve_spec(tk, self.S0, wl.host_cache_locs, self.dbl, self.tok, self.st, self.clk,
+                                    wl.resident_pages, out, miss, self.host, self.dev, copy_layers=copy_layers,
+                                    plan=plan)
+        if copy_layers < wl.L:
+            for q in range(Q):
+                err |= self.orc.gather(self.orc.step_plan(plan, q), wl.host_cache_locs, copy_layers,
+                                       wl.L - copy_layers, self.host, self.dev)
+        for r in range(wl.R):
+            self.prev[r] = tk[Q - 1, r][tk[Q - 1, r] >= 0]
+        return out, miss, err, plan
+
     def batch(self):
         self.forward()
         tk = self.topk()
@@ -228,3 +247,70 @@ def test_too_small_a_buffer_breaks_replay():
         found = found or bool(_overwrites(run, tk, out))
         run.accept()
     assert found, "with H < (Q + 1) * K some verify step should reuse an earlier step's row"
+
+
+@pytest.mark.parametrize("copy_layers", [0, 1, 3])
+def test_leader_batch_and_step_gathers_equal_the_full_batch(copy_layers):
+    """IndexShare under MTP: verify steps that copy only the leader layers and record their own
+    plans, then each step's plan replayed for the followers in step order, leave every layer's
+    pool, the row tables, the miss counts and the slot state exactly as the full batch does;
+    each step's plan holds as many misses as its miss count."""
+    wl = _spec_workload("indexshare_small")
+    assert wl.L == 3
+    Q = 2
+    full = SpecRun(wl, Q, seed=3, hot_slots=(Q + 1) * wl.K)
+    split = SpecRun(wl, Q, seed=3, hot_slots=(Q + 1) * wl.K)
+    for b in range(6):
+        full.forward()
+        split.forward()
+        tk = full.topk()
+        assert np.array_equal(tk, split.topk())
+        out_f, miss_f, err_f = full.resolve(tk)
+        out_s, miss_s, err_s, plan = split.resolve_split(tk, copy_layers)
+        assert err_f == err_s == 0
+        assert np.array_equal(out_f, out_s) and np.array_equal(miss_f, miss_s)
+        assert np.array_equal(plan.count, miss_s), f"batch {b}: plan counts"
+        assert int(miss_s.sum()) > 0
+        for name in ("tok", "st", "clk"):
+            assert np.array_equal(getattr(full, name), getattr(split, name)), f"batch {b}: {name}"
+        for layer in range(wl.L):
+            assert np.array_equal(full.dev[layer], split.dev[layer]), f"batch {b}: layer {layer} pool"
+        acc = full.rng.integers(1, Q + 1, size=wl.R).astype(np.int32)
+        split.rng.integers(1, Q + 1, size=wl.R)
+        assert full.accept(acc.copy())[2] == 0
+        assert split.accept(acc.copy())[2] == 0
+
+
+def test_step_gathers_out_of_step_order_can_differ():
+    """The follower replay must follow step order: replaying the steps' plans backwards leaves
+    some follower row with a later step's token overwritten by an earlier step's, once a slot
+    is reused within a batch (a buffer too small to keep every step's rows)."""
+    wl = _spec_workload("indexshare_small")
+    Q = 4
+    runs = [SpecRun(wl, Q, seed=3, hot_slots=Q * wl.K // 2) for _ in range(2)]
+    differs = False
+    for b in range(6):
+        for run in runs:
+            run.forward()
+        tk = runs[0].topk()
+        runs[1].topk()
+        plans = []
+        for run in runs:
+            out = np.zeros((Q, wl.R, wl.K), np.int32)
+            miss = np.zeros((Q, wl.R), np.int32)
+            plan = run.orc.new_spec_plan(Q, wl.R)
+            run.orc.resolve_spec(tk, run.S0, wl.host_cache_locs, run.dbl, run.tok, run.st, run.clk,
+                                 wl.resident_pages, out, miss, run.host, run.dev, copy_layers=1, plan=plan)
+            plans.append(plan)
+        for q in range(Q):
+            runs[0].orc.gather(runs[0].orc.step_plan(plans[0], q), wl.host_cache_locs, 1, wl.L - 1,
+                               runs[0].host, runs[0].dev)
+        for q in reversed(range(Q)):
+            runs[1].orc.gather(runs[1].orc.step_plan(plans[1], q), wl.host_cache_locs, 1, wl.L - 1,
+                               runs[1].host, runs[1].dev)
+        differs = differs or any(not np.array_equal(runs[0].dev[l], runs[1].dev[l]) for l in range(1, wl.L))
+        acc = runs[0].rng.integers(1, Q + 1, size=wl.R).astype(np.int32)
+        runs[1].rng.integers(1, Q + 1, size=wl.R)
+        for run in runs:
+            run.accept(acc.copy(), check=False)
+    assert differs
