@@ -32,7 +32,7 @@ EXPORTS = ("hs_workspace_bytes", "hs_create", "hs_resolve", "hs_backup", "hs_get
            "hs_status_str", "hs_host_register", "hs_host_unregister", "hs_resolve_noalloc",
            "hs_invalidate_tokens", "hs_invalidate_host_rows", "hs_resolve_layers", "hs_gather",
            "hs_resolve_spec", "hs_backup_spec", "hs_reset_hints", "hs_sparse_mla_workspace_bytes",
-           "hs_sparse_mla_decode", "hs_launch_shape")
+           "hs_sparse_mla_decode", "hs_launch_shape", "hs_resolve_spec_layers", "hs_gather_spec")
 HS_MAX_SPEC_QUERIES = 8
 HS_NOALLOC_MAX_LAYERS = 8
 
@@ -76,6 +76,10 @@ def _load() -> ctypes.CDLL:
     lib.hs_launch_shape.restype = ctypes.c_int
     lib.hs_resolve_spec.argtypes = [P, i32, i32] + [P] * 10 + [P]
     lib.hs_resolve_spec.restype = ctypes.c_int
+    lib.hs_resolve_spec_layers.argtypes = [P, i32, i32] + [P] * 10 + [i32, P]
+    lib.hs_resolve_spec_layers.restype = ctypes.c_int
+    lib.hs_gather_spec.argtypes = [P, i32, P, i32, i32, i32, P]
+    lib.hs_gather_spec.restype = ctypes.c_int
     lib.hs_backup_spec.argtypes = [P, i32, i32] + [P] * 5 + [P]
     lib.hs_backup_spec.restype = ctypes.c_int
     lib.hs_gather.restype = ctypes.c_int
@@ -204,6 +208,22 @@ def hs_resolve_spec(h: Handle, num_requests: int, num_queries: int, top_k_tokens
                                 _addr(device_buffer_tokens), _addr(lru_slots), _addr(lru_clock),
                                 _addr(resident_pages), _addr(out_rows), _addr(miss_counts), _stream(stream)),
            "hs_resolve_spec")
+
+
+def hs_resolve_spec_layers(h: Handle, num_requests: int, num_queries: int, top_k_tokens, committed_lens,
+                           host_cache_locs, device_buffer_locs, device_buffer_tokens, lru_slots, lru_clock,
+                           resident_pages, out_rows, miss_counts, copy_layers: int, stream=None) -> None:
+    _check(_lib.hs_resolve_spec_layers(h.ptr if h else None, num_requests, num_queries, _addr(top_k_tokens),
+                                       _addr(committed_lens), _addr(host_cache_locs), _addr(device_buffer_locs),
+                                       _addr(device_buffer_tokens), _addr(lru_slots), _addr(lru_clock),
+                                       _addr(resident_pages), _addr(out_rows), _addr(miss_counts), copy_layers,
+                                       _stream(stream)), "hs_resolve_spec_layers")
+
+
+def hs_gather_spec(h: Handle, num_requests: int, host_cache_locs, query: int, first_layer: int, num_layers: int,
+                   stream=None) -> None:
+    _check(_lib.hs_gather_spec(h.ptr if h else None, num_requests, _addr(host_cache_locs), query, first_layer,
+                               num_layers, _stream(stream)), "hs_gather_spec")
 
 
 def hs_backup_spec(h: Handle, num_requests: int, num_queries: int, committed_lens, accepted, host_cache_locs,

@@ -14,12 +14,14 @@ struct hs_handle {
   uint32_t* hint;          // residency bitmap inside the caller's workspace
   int32_t* plan_tok;       // follower plan inside the caller's workspace: tokens [R, K],
   int32_t* plan_dst;       //   device rows [R, K],
-  int32_t* plan_cnt;       //   counts [R]
+  int32_t* plan_cnt;       //   counts [R] (slice 0; verify step q of a batch uses slice q)
+  size_t plan_slice;       // int32 elements from one plan slice to the next
   hs::OrderArgs order;     // the plan's misses in host-region order (hs_gather copies these)
   // What the last resolve left for hs_gather, as the calls were issued (stream order is call
   // order for calls on one stream, and a graph replays its calls in capture order).
   enum { kNoPlan, kPlan, kPairs, kSpec } plan_state;
   int32_t plan_requests;   // num_requests of that resolve
+  int32_t spec_queries;    // verify steps of the last speculative batch (its plans: slices 0..Q-1)
   int device;
 };
 
@@ -51,7 +53,7 @@ extern "C" {
 
 size_t hs_workspace_bytes(const hs_config* cfg) {
   return config_ok(cfg) ? hs::kWorkspaceBytes + hs::hint_bytes(cfg->max_requests, cfg->max_context) +
-                              hs::plan_bytes(cfg->max_requests, cfg->top_k) +
+                              hs::kPlanSlices * hs::plan_bytes(cfg->max_requests, cfg->top_k) +
                               hs::order_bytes(cfg->max_requests, cfg->top_k)
                         : 0;
 }
@@ -133,9 +135,9 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
       cudaSuccess)
     return HS_ERR_CUDA;  // no token is known to be resident yet
   uint8_t* plan = ws + hs::kWorkspaceBytes + hs::hint_bytes(cfg->max_requests, cfg->max_context);
-  if (cudaMemset(plan, 0, hs::plan_bytes(cfg->max_requests, cfg->top_k)) != cudaSuccess)
+  if (cudaMemset(plan, 0, hs::kPlanSlices * hs::plan_bytes(cfg->max_requests, cfg->top_k)) != cudaSuccess)
     return HS_ERR_CUDA;  // no plan yet: a gather before the first resolve copies nothing
-  uint8_t* order = plan + hs::plan_bytes(cfg->max_requests, cfg->top_k);
+  uint8_t* order = plan + hs::kPlanSlices * hs::plan_bytes(cfg->max_requests, cfg->top_k);
   if (cudaMemset(order, 0, hs::order_bytes(cfg->max_requests, cfg->top_k)) != cudaSuccess)
     return HS_ERR_CUDA;  // region counts and the count kernel's ticket start at zero
   if (cudaMemcpy(ws + hs::kPoolsOffset, &pools, sizeof(pools), cudaMemcpyHostToDevice) != cudaSuccess)
@@ -152,6 +154,7 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   h->plan_tok = reinterpret_cast<int32_t*>(plan);
   h->plan_dst = h->plan_tok + RK;
   h->plan_cnt = h->plan_dst + RK;
+  h->plan_slice = hs::plan_bytes(cfg->max_requests, cfg->top_k) / sizeof(int32_t);
   int32_t* o = reinterpret_cast<int32_t*>(order);
   h->order = hs::OrderArgs{nullptr, h->plan_tok, h->plan_dst, h->plan_cnt, o, o + RK, o + 2 * RK,
                            o + 3 * RK, o + 3 * RK + (hs::kOrderRegions + 1),
@@ -212,13 +215,15 @@ hs_status hs_resolve(hs_handle* h, int32_t num_requests, const int32_t* top_k_to
                            h->cfg.num_layers, stream);
 }
 
-hs_status hs_resolve_spec(hs_handle* h, int32_t num_requests, int32_t num_queries, const int32_t* top_k_tokens,
-                          const int32_t* committed_lens, const int32_t* host_cache_locs,
-                          const int32_t* device_buffer_locs, int32_t* device_buffer_tokens, int32_t* lru_slots,
-                          int32_t* lru_clock, const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
-                          hs_stream_t stream) {
+hs_status hs_resolve_spec_layers(hs_handle* h, int32_t num_requests, int32_t num_queries,
+                                 const int32_t* top_k_tokens, const int32_t* committed_lens,
+                                 const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
+                                 int32_t* device_buffer_tokens, int32_t* lru_slots, int32_t* lru_clock,
+                                 const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
+                                 int32_t copy_layers, hs_stream_t stream) {
   if (!h || num_requests < 0 || num_requests > h->cfg.max_requests) return HS_ERR_INVALID_ARG;
   if (num_queries < 1 || num_queries > HS_MAX_SPEC_QUERIES) return HS_ERR_INVALID_ARG;
+  if (copy_layers < 0 || copy_layers > h->cfg.num_layers) return HS_ERR_INVALID_ARG;
   if (num_requests == 0) return HS_OK;
   if (!top_k_tokens || !committed_lens || !host_cache_locs || !device_buffer_locs || !device_buffer_tokens ||
       !lru_slots || !lru_clock || !out_rows)
@@ -226,15 +231,61 @@ hs_status hs_resolve_spec(hs_handle* h, int32_t num_requests, int32_t num_querie
   if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
   const size_t RK = (size_t)num_requests * (size_t)h->cfg.top_k;
   h->plan_state = hs_handle::kSpec;
-  // The verify steps run in order on the stream, one launch each, over the shared state.
+  h->plan_requests = num_requests;
+  h->spec_queries = num_queries;
+  // Without copy CTAs, each verify step is resolved without copies, its plan is grouped by
+  // host region and the leader layers' rows are gathered, as for a plain step.
+  const bool gather_after = h->g.copy_ctas == 0 && copy_layers > 0;
+  // The verify steps run in order on the stream over the shared state; step q records its
+  // miss plan in plan slice q.
   for (int32_t q = 0; q < num_queries; ++q) {
+    int32_t* ptok = h->plan_tok + q * h->plan_slice;
+    int32_t* pdst = h->plan_dst + q * h->plan_slice;
+    int32_t* pcnt = h->plan_cnt + q * h->plan_slice;
     hs::ResolveArgs a{h->hint,   top_k_tokens + q * RK, committed_lens, host_cache_locs, device_buffer_locs,
                       device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows + q * RK,
-                      miss_counts ? miss_counts + (size_t)q * num_requests : nullptr, h->cfg.num_layers,
-                      nullptr,   nullptr,      nullptr,  q, num_queries};
+                      miss_counts ? miss_counts + (size_t)q * num_requests : nullptr,
+                      gather_after ? 0 : copy_layers, ptok, pdst, pcnt, q, num_queries};
     if (hs::launch_resolve(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
       return HS_ERR_CUDA;
+    if (gather_after) {
+      hs::OrderArgs oa = h->order;
+      oa.host_cache_locs = host_cache_locs;
+      oa.plan_tok = ptok;
+      oa.plan_dst = pdst;
+      oa.plan_cnt = pcnt;
+      if (hs::launch_order(h->g, oa, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess ||
+          hs::launch_gather_pairs(h->g, h->pools, oa, num_requests, 0, copy_layers, (cudaStream_t)stream) !=
+              cudaSuccess)
+        return HS_ERR_CUDA;
+    }
   }
+  return HS_OK;
+}
+
+hs_status hs_resolve_spec(hs_handle* h, int32_t num_requests, int32_t num_queries, const int32_t* top_k_tokens,
+                          const int32_t* committed_lens, const int32_t* host_cache_locs,
+                          const int32_t* device_buffer_locs, int32_t* device_buffer_tokens, int32_t* lru_slots,
+                          int32_t* lru_clock, const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
+                          hs_stream_t stream) {
+  if (!h) return HS_ERR_INVALID_ARG;
+  return hs_resolve_spec_layers(h, num_requests, num_queries, top_k_tokens, committed_lens, host_cache_locs,
+                                device_buffer_locs, device_buffer_tokens, lru_slots, lru_clock, resident_pages,
+                                out_rows, miss_counts, h->cfg.num_layers, stream);
+}
+
+hs_status hs_gather_spec(hs_handle* h, int32_t num_requests, const int32_t* host_cache_locs, int32_t query,
+                         int32_t first_layer, int32_t num_layers, hs_stream_t stream) {
+  if (!h || num_requests < 0 || num_requests > h->cfg.max_requests) return HS_ERR_INVALID_ARG;
+  if (first_layer < 0 || num_layers < 0 || first_layer + num_layers > h->cfg.num_layers) return HS_ERR_INVALID_ARG;
+  if (h->plan_state != hs_handle::kSpec || query < 0 || query >= h->spec_queries) return HS_ERR_INVALID_ARG;
+  if (num_requests != h->plan_requests) return HS_ERR_INVALID_ARG;
+  if (num_requests == 0 || num_layers == 0) return HS_OK;
+  if (!host_cache_locs) return HS_ERR_INVALID_ARG;
+  hs::GatherArgs a{host_cache_locs, h->plan_tok + query * h->plan_slice, h->plan_dst + query * h->plan_slice,
+                   h->plan_cnt + query * h->plan_slice, first_layer, num_layers};
+  if (hs::launch_gather(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+    return HS_ERR_CUDA;
   return HS_OK;
 }
 
@@ -258,7 +309,7 @@ hs_status hs_gather(hs_handle* h, int32_t num_requests, const int32_t* host_cach
   if (first_layer < 0 || num_layers < 0 || first_layer + num_layers > h->cfg.num_layers) return HS_ERR_INVALID_ARG;
   if (num_requests == 0 || num_layers == 0) return HS_OK;
   if (!host_cache_locs) return HS_ERR_INVALID_ARG;
-  if (h->plan_state == hs_handle::kSpec) return HS_ERR_INVALID_ARG;  // a speculative batch records no plan
+  if (h->plan_state == hs_handle::kSpec) return HS_ERR_INVALID_ARG;  // a batch's plans: hs_gather_spec
   if (h->plan_state == hs_handle::kPairs) {
     // the ordered plan covers the resolve's requests, all of them
     if (num_requests != h->plan_requests) return HS_ERR_INVALID_ARG;

@@ -147,8 +147,10 @@ inline size_t hint_bytes(int64_t max_requests, int64_t max_context) {
 }
 constexpr int32_t kBitsSmemMax = 64 * 1024;  // largest bitmap row a copy CTA stages
 
-// After the hints: the follower plan the last resolve recorded, tokens [R, K], device rows
-// [R, K] and counts [R] (int32 each).
+// After the hints: the follower plans, kPlanSlices slices of tokens [R, K], device rows
+// [R, K] and counts [R] (int32 each). A plain resolve records its plan in slice 0; verify
+// step q of a speculative batch records its own in slice q.
+constexpr int kPlanSlices = HS_MAX_SPEC_QUERIES;
 inline size_t plan_bytes(int64_t max_requests, int64_t top_k) {
   return (size_t)(((max_requests * top_k * 8 + max_requests * 4) + 255) & ~(int64_t)255);
 }

@@ -170,8 +170,10 @@ typedef struct hs_handle hs_handle;
  *     exact slot probe finishes (a clear bit predicts a miss). Every result comes from the
  *     probe, so bits left stale by changes the caller makes to the state arrays cost time,
  *     never correctness;
- *   - the follower plan of the last resolve: miss tokens and device rows, max_requests x
- *     top_k int32 each, then max_requests counts (hs_gather replays it);
+ *   - the follower plans: HS_MAX_SPEC_QUERIES slices, each miss tokens and device rows,
+ *     max_requests x top_k int32 each, then max_requests counts, rounded up to 256 bytes. A
+ *     plain resolve records its plan in slice 0 (hs_gather replays it), verify step q of a
+ *     speculative batch in slice q (hs_gather_spec);
  *   - the same misses grouped by 2 MB region of the host pool: per plan entry its host row,
  *     then (host row, device row) pairs, max_requests x top_k int32 each, and two tables of
  *     16,385 per-region int32 counters. A copy that takes the rows region by region reuses
@@ -224,7 +226,8 @@ HS_API hs_status hs_resolve_layers(hs_handle* h, int32_t num_requests, const int
  * plan rows and the request's shared hot state; "vLLM Hybrid HiSparse source
  * implementation analysis", 7.4 and 7.1: one resolve per verify step, a buffer of
  * (n_spec + 2) x top_k rows). num_queries = Q = n_spec + 1 (1..HS_MAX_SPEC_QUERIES) verify
- * steps run in order, one kernel launch each: step q resolves top_k_tokens[q] for
+ * steps run in order, one kernel launch each (four without copy CTAs, as for
+ * hs_resolve): step q resolves top_k_tokens[q] for
  * committed_lens[r] + q + 1 tokens into out_rows[q] and miss_counts[q]. The batch's
  * positions t >= S0 = committed_lens[r] (the token the last round sampled, then the drafts;
  * the forward pass has written them) resolve to the reserved rows H + (t - S0): with Q
@@ -233,13 +236,37 @@ HS_API hs_status hs_resolve_layers(hs_handle* h, int32_t num_requests, const int
  * resolved: every step's out_rows stay valid until the batch is consumed. On the fast path a
  * batch records slots S0 - Q .. S0 (committed), never its drafts.
  *   top_k_tokens [Q, R, K], out_rows [Q, R, K], miss_counts [Q, R] or NULL; the rest as in
- *   hs_resolve. No follower plan is recorded. */
+ *   hs_resolve. Every layer's miss rows are copied, and step q records its miss plan in
+ *   plan slice q (hs_gather_spec). */
 HS_API hs_status hs_resolve_spec(hs_handle* h, int32_t num_requests, int32_t num_queries,
                                  const int32_t* top_k_tokens, const int32_t* committed_lens,
                                  const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
                                  int32_t* device_buffer_tokens, int32_t* lru_slots, int32_t* lru_clock,
                                  const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
                                  hs_stream_t stream);
+
+/* hs_resolve_spec for a layer group split into a leader and followers (IndexShare under
+ * MTP: "vLLM Hybrid HiSparse source implementation analysis", 7.4, followers replay the
+ * leader's plan and every verify step is its own resolve over its own workspace slice).
+ * The batch is resolved exactly as by hs_resolve_spec, but each verify step copies miss
+ * rows only for layers [0, copy_layers) (0 <= copy_layers <= num_layers); its plan is kept
+ * in slice q for hs_gather_spec. hs_resolve_spec is this call with copy_layers = num_layers.
+ * Same rules as hs_resolve_spec. */
+HS_API hs_status hs_resolve_spec_layers(hs_handle* h, int32_t num_requests, int32_t num_queries,
+                                        const int32_t* top_k_tokens, const int32_t* committed_lens,
+                                        const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
+                                        int32_t* device_buffer_tokens, int32_t* lru_slots, int32_t* lru_clock,
+                                        const int32_t* resident_pages, int32_t* out_rows, int32_t* miss_counts,
+                                        int32_t copy_layers, hs_stream_t stream);
+
+/* Follower gather of one verify step of the last speculative batch: copy step `query`'s
+ * miss rows (0 <= query < that batch's num_queries) for layers [first_layer, first_layer +
+ * num_layers), as hs_gather does for a plain step, in miss order. num_requests must be the
+ * batch's. When a slot is reused within the batch (H < (Q + 1) x top_k), replay the steps
+ * in step order so that each row ends with the last step's token. HS_ERR_INVALID_ARG when
+ * the last resolve was not a speculative batch. One kernel launch, graph-capturable. */
+HS_API hs_status hs_gather_spec(hs_handle* h, int32_t num_requests, const int32_t* host_cache_locs,
+                                int32_t query, int32_t first_layer, int32_t num_layers, hs_stream_t stream);
 
 /* Eager backup after a speculative batch: the first accepted[r] positions S0 + j of the
  * batch (S0 = committed_lens[r], 0 <= accepted <= num_queries) are now committed, and each
@@ -261,8 +288,9 @@ HS_API hs_status hs_backup_spec(hs_handle* h, int32_t num_requests, int32_t num_
  * layers may run on other streams concurrently. When that resolve grouped its plan by host
  * region (hs_resolve_layers), the rows are copied in that order and num_requests must be
  * the resolve's; otherwise the plan of requests 0..num_requests-1 is replayed in miss order.
- * HS_ERR_INVALID_ARG after hs_resolve_spec, which records no plan. One kernel launch, layer
- * by layer; no allocation, no synchronisation; graph-capturable. num_layers == 0 is a no-op. */
+ * HS_ERR_INVALID_ARG after a speculative batch (its steps' plans: hs_gather_spec). One
+ * kernel launch, layer by layer; no allocation, no synchronisation; graph-capturable.
+ * num_layers == 0 is a no-op. */
 HS_API hs_status hs_gather(hs_handle* h, int32_t num_requests, const int32_t* host_cache_locs,
                            int32_t first_layer, int32_t num_layers, hs_stream_t stream);
 

@@ -46,14 +46,30 @@ class GpuSpec:
                 self.dev[layer].view(-1, wl.B)[row] = torch.from_numpy(wl.rows(layer, r, [t])[0]).cuda()
                 self.host[layer][h * wl.B:(h + 1) * wl.B] = 0xEE
 
-    def resolve(self, tk, S0):
+    def resolve(self, tk, S0, copy_layers=None, side=False):
+        """The batch through hs_resolve_spec, or, with copy_layers, through
+        hs_resolve_spec_layers and then every verify step's hs_gather_spec for the follower
+        layers in step order (on a side stream behind an event when `side`)."""
         import hierarchical_sparse_attention_gb300 as hs
         wl, Q = self.run.wl, tk.shape[0]
         g_tk = torch.from_numpy(tk).cuda()
         out = torch.full((Q, wl.R, wl.K), -7, dtype=torch.int32, device="cuda")
         miss = torch.full((Q, wl.R), -7, dtype=torch.int32, device="cuda")
-        hs.hs_resolve_spec(self.h, wl.R, Q, g_tk, torch.from_numpy(S0).cuda(), self.hcl, self.dbl, self.tok, self.st,
-                           self.clk, self.rp, out, miss)
+        args = (self.h, wl.R, Q, g_tk, torch.from_numpy(S0).cuda(), self.hcl, self.dbl, self.tok, self.st,
+                self.clk, self.rp, out, miss)
+        if copy_layers is None:
+            hs.hs_resolve_spec(*args)
+        else:
+            stream = torch.cuda.current_stream()
+            hs.hs_resolve_spec_layers(*args, copy_layers, stream)
+            gs = torch.cuda.Stream() if side else stream
+            if side:
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                gs.wait_event(ev)
+            if copy_layers < wl.L:
+                for q in range(Q):
+                    hs.hs_gather_spec(self.h, wl.R, self.hcl, q, copy_layers, wl.L - copy_layers, gs)
         torch.cuda.synchronize()
         return out.cpu().numpy(), miss.cpu().numpy()
 
@@ -65,18 +81,23 @@ class GpuSpec:
         torch.cuda.synchronize()
 
 
-def run_spec_parity(name, Q, batches, hot_slots=None, fixed_accept=None, steps=40):
+def run_spec_parity(name, Q, batches, hot_slots=None, fixed_accept=None, steps=40, copy_layers=None, side=False,
+                    wl=None, expect_copy_ctas=None):
+    """GPU batches against the oracle's full batches (hs_resolve_spec; the oracle pins that a
+    leader-only batch plus per-step follower gathers equals it)."""
     import hierarchical_sparse_attention_gb300 as hs
-    wl = _spec_workload(name, steps)
+    wl = _spec_workload(name, steps) if wl is None else wl
     run = SpecRun(wl, Q, seed=5, hot_slots=(Q + 1) * wl.K if hot_slots is None else hot_slots)
     gpu = GpuSpec(run)
+    if expect_copy_ctas is not None:
+        assert (hs.hs_launch_shape(gpu.h)[0] > 0) == expect_copy_ctas
     try:
         for b in range(batches):
             writes = run.forward()
             gpu.forward(writes)
             tk = run.topk()
             S0 = run.S0.copy()
-            out, miss = gpu.resolve(tk, S0)
+            out, miss = gpu.resolve(tk, S0, copy_layers, side)
             o_out, o_miss, oerr = run.resolve(tk)
             np.testing.assert_array_equal(out, o_out, err_msg=f"batch {b}: out_rows")
             np.testing.assert_array_equal(miss, o_miss, err_msg=f"batch {b}: miss_counts")
@@ -117,3 +138,54 @@ def test_spec_tiny_fast_path_and_transition():
 def test_spec_one_query_matches_plain_steps():
     """Q = 1 batches through the spec entry points against the oracle's plain steps."""
     run_spec_parity("dsa_small", 1, 8, fixed_accept=1)
+
+
+def test_spec_indexshare_leader_then_step_gathers():
+    """IndexShare under MTP: each verify step copies layer 0 and records its plan; the
+    followers replay every step's plan in step order."""
+    run_spec_parity("indexshare_small", 2, 6, copy_layers=1)
+
+
+def test_spec_indexshare_no_leader_copies_side_stream():
+    run_spec_parity("indexshare_small", 3, 6, copy_layers=0, side=True)
+
+
+def _wide_indexshare(steps=40):
+    import workloads as W
+    return W.make("indexshare", 12, requests=80, top_k=64, hot_slots=128, steps=steps, layers=3,
+                  seq_range=(1000, 3000))
+
+
+def test_spec_without_copy_ctas():
+    """80 requests leave no SM for copy CTAs: every verify step is the resolve without copies,
+    the grouping by host region and the gather, for the full batch and the split one."""
+    run_spec_parity(None, 2, 4, wl=_wide_indexshare(), expect_copy_ctas=False)
+    run_spec_parity(None, 2, 4, wl=_wide_indexshare(), copy_layers=1, expect_copy_ctas=False)
+
+
+def test_gather_spec_misuse():
+    import hierarchical_sparse_attention_gb300 as hs
+    wl = _spec_workload("indexshare_small")
+    Q = 2
+    run = SpecRun(wl, Q, seed=5, hot_slots=(Q + 1) * wl.K)
+    gpu = GpuSpec(run)
+    try:
+        with pytest.raises(hs.HsError):  # no batch yet
+            hs.hs_gather_spec(gpu.h, wl.R, gpu.hcl, 0, 1, 1)
+        gpu.forward(run.forward())
+        tk = run.topk()
+        gpu.resolve(tk, run.S0.copy(), copy_layers=1)
+        hs.hs_gather_spec(gpu.h, wl.R, gpu.hcl, Q - 1, 1, 2)
+        for bad in ((wl.R, Q, 1, 1), (wl.R, -1, 1, 1), (wl.R - 1, 0, 1, 1), (wl.R, 0, 2, 2)):
+            with pytest.raises(hs.HsError):
+                hs.hs_gather_spec(gpu.h, bad[0], gpu.hcl, bad[1], bad[2], bad[3])
+        with pytest.raises(hs.HsError):  # a batch's plans are replayed per step
+            hs.hs_gather(gpu.h, wl.R, gpu.hcl, 1, 1)
+        with pytest.raises(hs.HsError):
+            hs.hs_resolve_spec_layers(gpu.h, wl.R, Q, torch.from_numpy(tk).cuda(), torch.from_numpy(run.S0).cuda(),
+                                      gpu.hcl, gpu.dbl, gpu.tok, gpu.st, gpu.clk, gpu.rp,
+                                      torch.empty((Q, wl.R, wl.K), dtype=torch.int32, device="cuda"), None,
+                                      wl.L + 1)
+        torch.cuda.synchronize()
+    finally:
+        gpu.close()
