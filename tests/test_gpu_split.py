@@ -116,6 +116,12 @@ def test_split_without_copy_ctas():
                      seq_range=(1000, 3000)), 1, [(1, 2)], check_plan=True)
 
 
+def test_full_resolve_then_regather_in_miss_order():
+    """A full hs_resolve with copy CTAs copies every layer and keeps its plan in miss order (no
+    host-region grouping); hs_gather of every layer then replays it with the same bytes."""
+    run_split(_indexshare_small(), 3, [(0, 3)])
+
+
 def test_split_four_layers_dsa_rows():
     run_split(W.make("indexshare", 7, requests=6, top_k=256, hot_slots=512, steps=6, layers=4,
                      seq_range=(4000, 9000)), 2, [(2, 1), (3, 1)], mode="side")
