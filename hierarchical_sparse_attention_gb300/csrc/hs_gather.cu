@@ -1,4 +1,5 @@
-// Follower gather: replay the leader's miss plan for other layers of the group.
+// Miss-row copies that run apart from the resolve kernel: follower gathers and the copies of
+// a step without copy CTAs.
 //
 // Sources (page title, section): "vLLM Hybrid HiSparse source implementation analysis", 7.4
 // (layers that share the indexer see the same indices and the same slot plan; only their
@@ -6,15 +7,19 @@
 // LRU work) and "vLLM HiSparse local KV offload architecture", "Performance invariants"
 // (compatible layers still share one miss plan).
 //
-// The plan is what the last hs_resolve / hs_resolve_layers recorded in the workspace: per
-// request, the miss tokens and their device rows in miss order. A CTA takes a run of
-// kGatherMisses misses of one request and one layer, looks up their host rows, and copies
-// the rows with 16-byte (else 4- or 1-byte) loads streamed past the caches, several in
-// flight per thread. The grid is layer-major: a copy that reads all layers' pools at once
-// spreads over several times the host pages and ran at about half the rate of one layer at
-// a time. Run on a copy stream, one call per layer (or per
-// few layers) with an event after each, layer l + 1's rows move while layer l's attention
-// runs. Bound: the host link (miss rows), like the resolve's own copies.
+// The plan is what the last resolve recorded in the workspace: per request, the miss tokens
+// and their device rows in miss order. Two forms copy it:
+//   - gather_kernel replays it as recorded: a CTA takes a run of kGatherMisses misses of one
+//     request and one layer, looks up their host rows and streams the rows;
+//   - order_count_kernel and order_scatter_kernel first regroup it as (host row, device row)
+//     pairs by 2 MB region of the host pool, and gather_pairs_kernel copies those. Rows that
+//     share a region are then requested together and share the GPU's translation of it; in
+//     miss order, rows spread over several large pools moved at about half the link's rate.
+// Both copy with 16-byte (else 4- or 1-byte) loads streamed past the caches, several in
+// flight per thread, and both grids are layer-major: one layer's rows move before the next
+// layer's start, so the host pages read at any moment span one layer's pool. Called on a copy
+// stream, one call per layer with an event after each, layer l + 1's rows move while layer
+// l's attention runs. Bound: the host link.
 #include "hs_internal.h"
 
 namespace hs {
@@ -239,8 +244,7 @@ __global__ void __launch_bounds__(T) gather_pairs_kernel(const Geometry g, const
 
 cudaError_t launch_gather(const Geometry& g, const Pools* pools, const GatherArgs& a, int32_t num_requests,
                           uint32_t* err_word, cudaStream_t stream) {
-  // layer-major: blocks are dispatched z-slowest, so one layer's rows move before the next
-  // layer's start and the host pages being read at any moment span one layer's pool
+  // layer-major: blocks are dispatched z-slowest
   const dim3 grid(num_requests, (g.K + kGatherMisses - 1) / kGatherMisses, a.num_layers);
   if (g.vec == 16) gather_kernel<16><<<grid, kGatherThreads, 0, stream>>>(g, pools, a, err_word);
   else if (g.vec == 4) gather_kernel<4><<<grid, kGatherThreads, 0, stream>>>(g, pools, a, err_word);
