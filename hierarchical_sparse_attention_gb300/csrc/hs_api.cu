@@ -155,11 +155,19 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   h->plan_dst = h->plan_tok + RK;
   h->plan_cnt = h->plan_dst + RK;
   h->plan_slice = hs::plan_bytes(cfg->max_requests, cfg->top_k) / sizeof(int32_t);
-  int32_t* o = reinterpret_cast<int32_t*>(order);
-  h->order = hs::OrderArgs{nullptr, h->plan_tok, h->plan_dst, h->plan_cnt, o, o + RK, o + 2 * RK,
-                           o + 3 * RK, o + 3 * RK + (hs::kOrderRegions + 1),
-                           o + 3 * RK + 2 * (hs::kOrderRegions + 1),
-                           reinterpret_cast<uint32_t*>(o + 3 * RK + 2 * (hs::kOrderRegions + 1) + 1), (int64_t)RK};
+  hs::OrderArgs& oa = h->order;  // the region laid out as hs::order_bytes counts it
+  oa = hs::OrderArgs{};
+  oa.plan_tok = h->plan_tok;
+  oa.plan_dst = h->plan_dst;
+  oa.plan_cnt = h->plan_cnt;
+  oa.miss_src = reinterpret_cast<int32_t*>(order);
+  oa.pair_src = oa.miss_src + RK;
+  oa.pair_dst = oa.pair_src + RK;
+  oa.counts = oa.pair_dst + RK;
+  oa.cursors = oa.counts + (hs::kOrderRegions + 1);
+  oa.n_pairs = oa.cursors + (hs::kOrderRegions + 1);
+  oa.ticket = reinterpret_cast<uint32_t*>(oa.n_pairs + 1);
+  oa.capacity = (int64_t)RK;
   h->plan_state = hs_handle::kNoPlan;
   h->device = dev;
   *out = h;
