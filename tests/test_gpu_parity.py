@@ -168,6 +168,10 @@ def test_zero_copy_step_io():
     run_parity(W.make("dsa", requests=8, steps=10, seq0=(6000, 9000, 300, 7000, 8000, 4100, 20000, 5000)),
                pool_every=2, graph_from=4, host_io=True)
     run_parity(W.make("mixed1m", requests=4, steps=6), pool_every=3, host_io=True)
+    # 80 requests, no copy CTAs: the grouping and gather kernels behind a resolve that read
+    # the step's inputs from host memory
+    run_parity(W.make("indexshare", 9, requests=80, top_k=64, hot_slots=128, steps=4, layers=2,
+                      seq_range=(1000, 3000)), pool_every=1, graph_from=2, host_io=True)
 
 
 def test_graph_capture_replay_indexshare():
