@@ -64,6 +64,15 @@ def test_host_side_errors_without_gpu():
     with pytest.raises(hs.HsError) as e:
         hs.hs_backup(None, 1, None, None, None, None)
     assert e.value.status == hs.HS_ERR_INVALID_ARG
+    # the calls added for split layer groups and launch shapes refuse a missing handle too
+    for call in (lambda: hs.hs_launch_shape(None),
+                 lambda: hs.hs_gather(None, 1, None, 0, 1),
+                 lambda: hs.hs_gather_spec(None, 1, None, 0, 0, 1),
+                 lambda: hs.hs_resolve_layers(None, 1, *([None] * 10), 1),
+                 lambda: hs.hs_resolve_spec_layers(None, 1, 1, *([None] * 10), 1)):
+        with pytest.raises(hs.HsError) as e:
+            call()
+        assert e.value.status == hs.HS_ERR_INVALID_ARG
     for s in range(6):
         assert hs.hs_status_str(s)
 
