@@ -130,6 +130,15 @@ def test_no_copy_ctas_resolve_and_gather_in_a_graph():
         gpu.close()
 
 
+def test_no_copy_ctas_edges():
+    """Without copy CTAs: every request on the fast path (an empty plan, no pairs to copy), and
+    the largest top_k with a ragged sequence mix."""
+    run_parity(W.make("indexshare", 10, requests=80, top_k=64, hot_slots=128, steps=4, layers=2,
+                      seq_range=(60, 100)), pool_every=1)
+    run_parity(W.make("indexshare", 11, requests=80, top_k=4096, hot_slots=4096, steps=3, layers=2,
+                      seq_range=(3000, 9000)), pool_every=1)
+
+
 def test_miss_rate_sweep():
     _, host_pools = _gpu()
     base = W.make("sweep_h4096_f0.8")
