@@ -16,12 +16,13 @@ struct hs_handle {
   int32_t* plan_dst;       //   device rows [R, K],
   int32_t* plan_cnt;       //   counts [R] (slice 0; verify step q of a batch uses slice q)
   size_t plan_slice;       // int32 elements from one plan slice to the next
-  hs::OrderArgs order;     // the plan's misses in host-region order (hs_gather copies these)
+  hs::OrderArgs order;     // the plans' misses in host-region order (slice 0's pairs; order_slice)
   // What the last resolve left for hs_gather, as the calls were issued (stream order is call
   // order for calls on one stream, and a graph replays its calls in capture order).
   enum { kNoPlan, kPlan, kPairs, kSpec } plan_state;
   int32_t plan_requests;   // num_requests of that resolve
   int32_t spec_queries;    // verify steps of the last speculative batch (its plans: slices 0..Q-1)
+  bool spec_ordered;       // that batch's plans were also grouped by host region
   int device;
 };
 
@@ -46,6 +47,20 @@ int ceil_log2(int64_t x) {
 }
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// The host-ordered arrays of plan slice q (the plain plan is slice 0).
+hs::OrderArgs order_slice(const hs_handle* h, int32_t q, const int32_t* host_cache_locs) {
+  hs::OrderArgs oa = h->order;
+  const size_t RK = (size_t)h->cfg.max_requests * (size_t)h->cfg.top_k;
+  oa.host_cache_locs = host_cache_locs;
+  oa.plan_tok = h->plan_tok + q * h->plan_slice;
+  oa.plan_dst = h->plan_dst + q * h->plan_slice;
+  oa.plan_cnt = h->plan_cnt + q * h->plan_slice;
+  oa.pair_src = h->order.pair_src + 2 * (size_t)q * RK;
+  oa.pair_dst = h->order.pair_dst + 2 * (size_t)q * RK;
+  oa.n_pairs = h->order.n_pairs + q;
+  return oa;
+}
 
 }  // namespace
 
@@ -161,12 +176,12 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   oa.plan_dst = h->plan_dst;
   oa.plan_cnt = h->plan_cnt;
   oa.miss_src = reinterpret_cast<int32_t*>(order);
-  oa.pair_src = oa.miss_src + RK;
-  oa.pair_dst = oa.pair_src + RK;
-  oa.counts = oa.pair_dst + RK;
+  oa.pair_src = oa.miss_src + RK;                    // slice q: + 2 q RK
+  oa.pair_dst = oa.pair_src + RK;                    // slice q: + 2 q RK
+  oa.counts = oa.pair_src + 2 * hs::kPlanSlices * RK;
   oa.cursors = oa.counts + (hs::kOrderRegions + 1);
-  oa.n_pairs = oa.cursors + (hs::kOrderRegions + 1);
-  oa.ticket = reinterpret_cast<uint32_t*>(oa.n_pairs + 1);
+  oa.n_pairs = oa.cursors + (hs::kOrderRegions + 1);  // slice q: + q
+  oa.ticket = reinterpret_cast<uint32_t*>(oa.n_pairs + hs::kPlanSlices);
   oa.capacity = (int64_t)RK;
   h->plan_state = hs_handle::kNoPlan;
   h->device = dev;
@@ -201,8 +216,7 @@ hs_status hs_resolve_layers(hs_handle* h, int32_t num_requests, const int32_t* t
   h->plan_state = order ? hs_handle::kPairs : hs_handle::kPlan;
   h->plan_requests = num_requests;
   if (order) {
-    hs::OrderArgs oa = h->order;
-    oa.host_cache_locs = host_cache_locs;
+    const hs::OrderArgs oa = order_slice(h, 0, host_cache_locs);
     if (hs::launch_order(h->g, oa, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
       return HS_ERR_CUDA;
     if (gather_after &&
@@ -238,12 +252,15 @@ hs_status hs_resolve_spec_layers(hs_handle* h, int32_t num_requests, int32_t num
     return HS_ERR_INVALID_ARG;
   if (resident_pages && h->cfg.page_size <= 0) return HS_ERR_INVALID_ARG;
   const size_t RK = (size_t)num_requests * (size_t)h->cfg.top_k;
+  // Without copy CTAs, each verify step is resolved without copies, its plan is grouped by
+  // host region and the leader layers' rows are gathered, as for a plain step; each step's
+  // plan is also grouped whenever follower layers are left for hs_gather_spec.
+  const bool gather_after = h->g.copy_ctas == 0 && copy_layers > 0;
+  const bool order = h->g.copy_ctas == 0 || copy_layers < h->cfg.num_layers;
   h->plan_state = hs_handle::kSpec;
   h->plan_requests = num_requests;
   h->spec_queries = num_queries;
-  // Without copy CTAs, each verify step is resolved without copies, its plan is grouped by
-  // host region and the leader layers' rows are gathered, as for a plain step.
-  const bool gather_after = h->g.copy_ctas == 0 && copy_layers > 0;
+  h->spec_ordered = order;
   // The verify steps run in order on the stream over the shared state; step q records its
   // miss plan in plan slice q.
   for (int32_t q = 0; q < num_queries; ++q) {
@@ -256,13 +273,11 @@ hs_status hs_resolve_spec_layers(hs_handle* h, int32_t num_requests, int32_t num
                       gather_after ? 0 : copy_layers, ptok, pdst, pcnt, q, num_queries};
     if (hs::launch_resolve(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
       return HS_ERR_CUDA;
-    if (gather_after) {
-      hs::OrderArgs oa = h->order;
-      oa.host_cache_locs = host_cache_locs;
-      oa.plan_tok = ptok;
-      oa.plan_dst = pdst;
-      oa.plan_cnt = pcnt;
-      if (hs::launch_order(h->g, oa, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess ||
+    if (order) {
+      const hs::OrderArgs oa = order_slice(h, q, host_cache_locs);
+      if (hs::launch_order(h->g, oa, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+        return HS_ERR_CUDA;
+      if (gather_after &&
           hs::launch_gather_pairs(h->g, h->pools, oa, num_requests, 0, copy_layers, (cudaStream_t)stream) !=
               cudaSuccess)
         return HS_ERR_CUDA;
@@ -290,6 +305,12 @@ hs_status hs_gather_spec(hs_handle* h, int32_t num_requests, const int32_t* host
   if (num_requests != h->plan_requests) return HS_ERR_INVALID_ARG;
   if (num_requests == 0 || num_layers == 0) return HS_OK;
   if (!host_cache_locs) return HS_ERR_INVALID_ARG;
+  if (h->spec_ordered) {
+    if (hs::launch_gather_pairs(h->g, h->pools, order_slice(h, query, host_cache_locs), num_requests, first_layer,
+                                num_layers, (cudaStream_t)stream) != cudaSuccess)
+      return HS_ERR_CUDA;
+    return HS_OK;
+  }
   hs::GatherArgs a{host_cache_locs, h->plan_tok + query * h->plan_slice, h->plan_dst + query * h->plan_slice,
                    h->plan_cnt + query * h->plan_slice, first_layer, num_layers};
   if (hs::launch_gather(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)

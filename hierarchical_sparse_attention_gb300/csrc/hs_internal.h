@@ -81,7 +81,7 @@ struct OrderArgs {
   const int32_t* plan_dst;
   const int32_t* plan_cnt;
   int32_t* miss_src;   // [R, K] per plan entry: host row, -1 out of range, -2 no device row
-  int32_t* pair_src;   // [R * K] host rows (-1: zero-fill), grouped by region
+  int32_t* pair_src;   // [R * K] host rows (-1: zero-fill), grouped by region (one plan slice's)
   int32_t* pair_dst;   // [R * K] device rows
   int32_t* counts;     // [kOrderRegions + 1] misses per region (zero between steps)
   int32_t* cursors;    // [kOrderRegions + 1] next free position per region
@@ -155,14 +155,19 @@ inline size_t plan_bytes(int64_t max_requests, int64_t top_k) {
   return (size_t)(((max_requests * top_k * 8 + max_requests * 4) + 255) & ~(int64_t)255);
 }
 
-// After the plan: the host-ordered copy of it (OrderArgs). A gather that takes the misses in
+// After the plans: their host-ordered copies (OrderArgs). A gather that takes the misses in
 // host-address order, so that neighbouring rows share a 2 MB host region, reuses the GPU's
 // translation of each region for several rows; in the order the resolve found them, misses
-// spread over several large pools ran at about half the link rate.
+// spread over several large pools ran at about half the link rate. Layout (int32): per plan
+// entry its host row [R, K]; per plan slice its pairs' host rows and device rows [R * K]
+// each; the region counters and cursors [kOrderRegions + 1] each; per plan slice its pair
+// count; the count kernel's CTA ticket.
 constexpr int32_t kOrderRegions = 16384;
 constexpr int64_t kOrderRegionBytes = 2 << 20;
 inline size_t order_bytes(int64_t max_requests, int64_t top_k) {
-  return (size_t)((((max_requests * top_k * 3 + 2 * (int64_t)(kOrderRegions + 1) + 2) * 4) + 255) & ~(int64_t)255);
+  const int64_t rk = max_requests * top_k;
+  return (size_t)((((rk * (1 + 2 * kPlanSlices) + 2 * (int64_t)(kOrderRegions + 1) + kPlanSlices + 1) * 4) + 255) &
+                  ~(int64_t)255);
 }
 
 // Dynamic shared memory of one resolve-kernel CTA for geometry g.

@@ -174,9 +174,10 @@ typedef struct hs_handle hs_handle;
  *     max_requests x top_k int32 each, then max_requests counts, rounded up to 256 bytes. A
  *     plain resolve records its plan in slice 0 (hs_gather replays it), verify step q of a
  *     speculative batch in slice q (hs_gather_spec);
- *   - the same misses grouped by 2 MB region of the host pool: per plan entry its host row,
- *     then (host row, device row) pairs, max_requests x top_k int32 each, and two tables of
- *     16,385 per-region int32 counters. A copy that takes the rows region by region reuses
+ *   - the same misses grouped by 2 MB region of the host pool: per plan entry its host row
+ *     (max_requests x top_k int32), then per plan slice its (host row, device row) pairs
+ *     (2 x max_requests x top_k int32), two tables of 16,385 per-region int32 counters and
+ *     the pair counts. A copy that takes the rows region by region reuses
  *     the GPU's address translation of each region for several rows; in the order the
  *     resolve finds them, rows spread over several large pools moved at about half the
  *     host link's rate.
@@ -250,8 +251,9 @@ HS_API hs_status hs_resolve_spec(hs_handle* h, int32_t num_requests, int32_t num
  * leader's plan and every verify step is its own resolve over its own workspace slice).
  * The batch is resolved exactly as by hs_resolve_spec, but each verify step copies miss
  * rows only for layers [0, copy_layers) (0 <= copy_layers <= num_layers); its plan is kept
- * in slice q for hs_gather_spec. hs_resolve_spec is this call with copy_layers = num_layers.
- * Same rules as hs_resolve_spec. */
+ * in slice q for hs_gather_spec. When copy_layers < num_layers, or the geometry has no copy
+ * CTAs, each step's plan is also grouped by host region (two more launches per step).
+ * hs_resolve_spec is this call with copy_layers = num_layers. Same rules as hs_resolve_spec. */
 HS_API hs_status hs_resolve_spec_layers(hs_handle* h, int32_t num_requests, int32_t num_queries,
                                         const int32_t* top_k_tokens, const int32_t* committed_lens,
                                         const int32_t* host_cache_locs, const int32_t* device_buffer_locs,
@@ -261,8 +263,8 @@ HS_API hs_status hs_resolve_spec_layers(hs_handle* h, int32_t num_requests, int3
 
 /* Follower gather of one verify step of the last speculative batch: copy step `query`'s
  * miss rows (0 <= query < that batch's num_queries) for layers [first_layer, first_layer +
- * num_layers), as hs_gather does for a plain step, in miss order. num_requests must be the
- * batch's. When a slot is reused within the batch (H < (Q + 1) x top_k), replay the steps
+ * num_layers), as hs_gather does for a plain step: in host-region order when the batch
+ * grouped its plans, else in miss order. num_requests must be the batch's. When a slot is reused within the batch (H < (Q + 1) x top_k), replay the steps
  * in step order so that each row ends with the last step's token. HS_ERR_INVALID_ARG when
  * the last resolve was not a speculative batch. One kernel launch, graph-capturable. */
 HS_API hs_status hs_gather_spec(hs_handle* h, int32_t num_requests, const int32_t* host_cache_locs,
