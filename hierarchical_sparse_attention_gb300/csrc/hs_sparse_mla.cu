@@ -16,7 +16,8 @@
 // split p of the rows) and runs a three-role pipeline over blocks of 64 rows:
 //   - producers (warps 5-15) gather each block's 656-B records through the row table (staged
 //     in shared memory) straight into registers, 32 rows at a time with the next 32 rows'
-//     loads in flight, dequantise the latent to bf16 (e4m3 -> f16 in hardware, times the row's
+//     loads in flight, 16-byte loads of 16 latent codes (plus their block's scale) or of 8
+//     RoPE dims each; they dequantise the latent to bf16 (e4m3 -> f16 in hardware, times the
 //     scale), copy the RoPE part, and fill one of three swizzled K-major tiles (72 KB each);
 //   - one issuer warp (warp 4) runs S = Q . K^T for a block as soon as its tile is full and the
 //     softmax has read the previous S (36 MMAs of M 128, N 64, K 16, with Q as the A operand in
@@ -55,8 +56,9 @@ constexpr int HALF = DL / NQ;    // value dims per CTA (128)
 constexpr int ISSUER_WARP = 4;   // warp 4 issues the MMAs; warps 0-3 run the softmax
 constexpr int PROD0 = 160;       // first producer thread (warps 5-15)
 constexpr int NPROD = T - PROD0;
-constexpr int CHUNKS = HB * (DQK / 8);                 // 16-byte tile chunks per producer pass
-constexpr int PER_PROD = (CHUNKS + NPROD - 1) / NPROD;  // chunks per producer thread
+constexpr int ITEMS_ROW = DL / 16 + (DQK - DL) / 8;     // per row: 32 latent items of 16 dims, 8 RoPE of 8
+constexpr int CHUNKS = HB * ITEMS_ROW;                 // producer items per pass
+constexpr int PER_PROD = (CHUNKS + NPROD - 1) / NPROD;  // items per producer thread
 constexpr int NT = 3;            // tiles in flight
 constexpr int ROWS_CAP = 2048;   // a split's row-table entries staged in shared memory
 constexpr uint32_t TMEM_COLS = 512;
@@ -199,32 +201,32 @@ __device__ __forceinline__ bool pipe_wait(uint64_t* ring, int depth, int k, vola
   }
 }
 
-// A producer's chunks of one block: chunk c = (thread - PROD0) + i * NPROD covers row c / 72,
-// dims [8 (c % 72), 8 (c % 72) + 8).
-// The raw bytes of those chunks: 8 codes and the block's scale for a latent chunk, 16 bytes of
-// RoPE otherwise.
-// rows: this block's 32 entries of the row table (shared memory); n: how many are real.
+// A producer's items of one pass: item c = (thread - PROD0) + i * NPROD covers row
+// c / ITEMS_ROW; item it = c % ITEMS_ROW < 32 is latent dims [16 it, 16 it + 16) (16 codes in
+// one load, and the scale of their 128-dim block), else RoPE dims [512 + 8 j, +8), j = it - 32.
+// rows: this pass's entries of the row table (shared memory); n: how many are real.
 __device__ __forceinline__ uint32_t load_raw(const SparseMlaArgs& a, int pt, const int32_t* rows, int n,
-                                             uint4 (&raw)[PER_PROD]) {
-  uint32_t valid = 0;  // bit i: chunk i's row is a pool row
+                                             uint4 (&raw)[PER_PROD], float (&scl)[PER_PROD]) {
+  uint32_t valid = 0;  // bit i: item i's row is a pool row
 #pragma unroll
   for (int i = 0; i < PER_PROD; ++i) {
     const int c = pt + i * NPROD;
-    const int d = (c % (DQK / 8)) * 8;
-    const int row = c / (DQK / 8);
+    const int row = c / ITEMS_ROW, it = c - row * ITEMS_ROW;
     const int32_t pr = c < CHUNKS && row < n ? rows[row] : -1;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    float sc = 0.f;
     if (pr >= 0 && (int64_t)pr < a.pool_rows) {
       valid |= 1u << i;
       const uint8_t* rec = a.kv_pool + (size_t)pr * ROWB;
-      if (d < DL) {
-        const uint2 codes = __ldg(reinterpret_cast<const uint2*>(rec + d));
-        v = make_uint4(codes.x, codes.y, __ldg(reinterpret_cast<const uint32_t*>(rec + DL) + (d >> 7)), 0u);
+      if (it < DL / 16) {
+        v = __ldg(reinterpret_cast<const uint4*>(rec) + it);
+        sc = __ldg(reinterpret_cast<const float*>(rec + DL) + (it >> 3));
       } else {
-        v = __ldg(reinterpret_cast<const uint4*>(rec + DL + 16 + 2 * (d - DL)));
+        v = __ldg(reinterpret_cast<const uint4*>(rec + DL + 16) + (it - DL / 16));
       }
     }
     raw[i] = v;
+    scl[i] = sc;
   }
   return valid;
 }
@@ -308,28 +310,34 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
     const auto pass_rows = [&](int k) { return rows_src + k * HB; };
     const auto pass_n = [&](int k) { return min(HB, j_end - j_begin - k * HB); };
     uint4 raw[PER_PROD];
+    float scl[PER_PROD];
     uint32_t vmask = 0;
-    if (nblk > 0) vmask = load_raw(a, pt, pass_rows(0), pass_n(0), raw);
-    // dequantise this thread's chunks of rows [32 half, 32 half + 32) of a block into its tile
+    if (nblk > 0) vmask = load_raw(a, pt, pass_rows(0), pass_n(0), raw, scl);
+    const auto to_bf16 = [](uint32_t codes2x2, float sc) {  // four codes to two bf16 pairs
+      const float2 v0 = e4m3x2((uint16_t)(codes2x2 & 0xFFFFu)), v1 = e4m3x2((uint16_t)(codes2x2 >> 16));
+      __nv_bfloat162 b0 = __floats2bfloat162_rn(v0.x * sc, v0.y * sc), b1 = __floats2bfloat162_rn(v1.x * sc, v1.y * sc);
+      return make_uint2(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1));
+    };
+    // dequantise this thread's items of rows [32 half, 32 half + 32) of a block into its tile
     const auto fill = [&](uint8_t* tile, int half) {
 #pragma unroll
       for (int i = 0; i < PER_PROD; ++i) {
         const int c = pt + i * NPROD;
         if (c >= CHUNKS) continue;
-        const int hrow = c / (DQK / 8), d = (c - hrow * (DQK / 8)) * 8;
+        const int hrow = c / ITEMS_ROW, it = c - hrow * ITEMS_ROW;
         const int row = half * HB + hrow;
         const uint4 v = raw[i];
-        uint4 chunk = v;
-        if (d < DL) {
-          const float sc = __uint_as_float(v.z);
-          const float2 v0 = e4m3x2((uint16_t)(v.x & 0xFFFFu)), v1 = e4m3x2((uint16_t)(v.x >> 16));
-          const float2 v2 = e4m3x2((uint16_t)(v.y & 0xFFFFu)), v3 = e4m3x2((uint16_t)(v.y >> 16));
-          __nv_bfloat162 b0 = __floats2bfloat162_rn(v0.x * sc, v0.y * sc), b1 = __floats2bfloat162_rn(v1.x * sc, v1.y * sc);
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(v2.x * sc, v2.y * sc), b3 = __floats2bfloat162_rn(v3.x * sc, v3.y * sc);
-          chunk = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
-                             *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+        if (it < DL / 16) {
+          const int d = 16 * it;
+          const uint2 p0 = to_bf16(v.x, scl[i]), p1 = to_bf16(v.y, scl[i]);
+          const uint2 p2 = to_bf16(v.z, scl[i]), p3 = to_bf16(v.w, scl[i]);
+          *reinterpret_cast<uint4*>(tile + (d >> 6) * (BJ * 128) + sw128(row, d & 63)) = make_uint4(p0.x, p0.y, p1.x, p1.y);
+          *reinterpret_cast<uint4*>(tile + ((d + 8) >> 6) * (BJ * 128) + sw128(row, (d + 8) & 63)) =
+              make_uint4(p2.x, p2.y, p3.x, p3.y);
+        } else {
+          const int d = DL + 8 * (it - DL / 16);
+          *reinterpret_cast<uint4*>(tile + (d >> 6) * (BJ * 128) + sw128(row, d & 63)) = v;
         }
-        *reinterpret_cast<uint4*>(tile + (d >> 6) * (BJ * 128) + sw128(row, d & 63)) = chunk;
       }
     };
     const int npass = (j_end - j_begin + HB - 1) / HB;
@@ -340,14 +348,14 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
       for (int half = 0; half < 2; ++half) {
         const int k = 2 * b + half;
         fill(tile, half);
-        // a row's validity, from the thread that holds its first chunk
+        // a row's validity, from the thread that holds its first item
 #pragma unroll
         for (int i = 0; i < PER_PROD; ++i) {
           const int c = pt + i * NPROD;
-          if (c < CHUNKS && c % (DQK / 8) == 0) valid[half * HB + c / (DQK / 8)] = (int32_t)((vmask >> i) & 1u);
+          if (c < CHUNKS && c % ITEMS_ROW == 0) valid[half * HB + c / ITEMS_ROW] = (int32_t)((vmask >> i) & 1u);
         }
-        if (k + 1 < npass) vmask = load_raw(a, pt, pass_rows(k + 1), pass_n(k + 1), raw);
-        else vmask = load_raw(a, pt, pass_rows(k + 1), 0, raw);  // past the end: zero rows
+        if (k + 1 < npass) vmask = load_raw(a, pt, pass_rows(k + 1), pass_n(k + 1), raw, scl);
+        else vmask = load_raw(a, pt, pass_rows(k + 1), 0, raw, scl);  // past the end: zero rows
       }
       fence_async_smem();
       bar_arrive(&s_tile_full[b % NT]);
