@@ -2,14 +2,16 @@
 
 One step = one decode step of the whole hot path for the batch: hs_resolve (classify,
 hit / LRU refresh, victim pick, miss-row copies from pinned host memory, row table) and
-hs_backup (newest-token row back to host). Workload: the DSA decode shape -- 32 requests
-at seq_len 131072 (+1 per step), top_k 2048, 4096 hot slots, 656-byte FP8 MLA rows, one
-layer, top-k 90 % reused step to step plus the last 64 tokens. Inputs are seeded and
-synthetic and sit in device memory (host pool: pinned host memory) before timing starts;
-L2 is flushed (256 MiB write) between timed steps.
+hs_backup (newest-token row back to host). Default workload: IndexShare -- 256 requests at
+seq_len uniform in [32768, 65536] (+1 per step), one top-k of 2048 shared by 4 sparse-MLA
+layers, 4096 hot slots, 656-byte FP8 MLA rows, top-k 85 % reused step to step plus the newest
+token, eager backup every step; the four layers' host rows interleaved in one pinned pool
+(--host-layout). --config dsa is the DSA decode shape (32 requests at seq_len 131072, one
+layer). Inputs are seeded and synthetic and sit in device memory (host pool: pinned host
+memory) before timing starts; L2 is flushed (256 MiB write) between timed steps.
 
 Prints one JSON line. --impl reference times the CPU oracle (the plain policy
-definition) on the same workload instead.
+definition) on the same workload and steps instead.
 """
 from __future__ import annotations
 
@@ -39,7 +41,15 @@ def parse():
     ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="dsa")
+    ap.add_argument("--config", default=None,
+                    help="workload (default: indexshare for the decode step and the split, the largest "
+                         "configuration on one GPU; dsa for the other ops)")
+    ap.add_argument("--host-layout", default="auto", choices=["auto", "layer_first", "page_first"],
+                    help="host KV pool layout: one pool per layer, or one pool whose row holds every layer's "
+                         "bytes of a token (auto: page_first for a layer group of more than one layer)")
+    ap.add_argument("--rehearsal", default="disjoint", choices=["disjoint", "timed", "none"],
+                    help="untimed steps replayed before timing: steps after the timed range (disjoint), the "
+                         "timed steps' own inputs (timed), or none")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -137,12 +147,13 @@ def max_over_ranks(x: float, ws: int) -> float:
 _POOL_OBJS = []  # workloads.HostPool objects behind the arrays in use
 
 
-def alloc_host(nbytes: int):
+def alloc_host(nbytes: int, bind=None):
     """Host pool bytes: huge pages when the host gives the whole pool, else driver-pinned
     memory (workloads.HostPool: the GPU reads random host rows fastest from huge pages).
+    bind(addr, nbytes): places the mapping on a memory node before its pages are touched.
     Returns (array, needs hs_host_register)."""
     import workloads as W
-    pool = W.HostPool(nbytes)
+    pool = W.HostPool(nbytes, before_fault=bind)
     _POOL_OBJS.append(pool)
     return pool.array, pool.needs_register
 
@@ -214,25 +225,66 @@ def kernel_code_hash(path: str) -> str:
 
 
 # ------------------------------------------------------------------------------------------
-def cpu_oracle_run(wl, host, steps, nthreads=1):
-    """Time the CPU oracle over `steps` decode steps (resolve + backup, bytes included).
-    Requests are split over `nthreads` Python threads (ctypes drops the GIL)."""
+def config_of(name: str):
+    import workloads as W
+    if name.startswith("sweep_h"):
+        h, f = name[len("sweep_h"):].split("_f")
+        return W.sweep_config(int(h), float(f))
+    return W.CONFIGS[name]
+
+
+def host_layout_for(args) -> str:
+    """The host pool layout of the run: as asked, or for "auto" every layer's bytes of a token
+    in one host row when the layer group has several layers (the layout the pair gather reads
+    as one span per miss), else one pool per layer."""
+    if args.host_layout != "auto":
+        return args.host_layout
+    return "page_first" if config_of(args.config).layers > 1 else "layer_first"
+
+
+def make_workload(args, rank: int, steps: int):
+    import workloads as W
+    return W.make(args.config, args.seed + 1000 * rank, steps=steps, host_layout=host_layout_for(args))
+
+
+def total_steps_of(args) -> int:
+    """Warm-up, timed, and (for a disjoint rehearsal) K more steps after the timed range."""
+    return args.warmup + args.steps + (args.steps if args.rehearsal == "disjoint" else 0)
+
+
+def workload_desc(args, wl) -> str:
+    """The workload string both arms print, from the configuration alone."""
+    c = wl.cfg
+    seq = (f"seq_len U[{c.seq_range[0]}, {c.seq_range[1]}]+1/step" if c.seq_range
+           else f"seq_len {int(wl.seq0[0])}+1/step")
+    return (f"{args.config}: {wl.R} requests x {seq}, top_k {wl.K}, {wl.H} hot slots, {wl.B}-byte rows, "
+            f"{wl.L} layer(s), host pools {c.host_layout.replace('_', '-')}, seed {args.seed}, "
+            f"timed steps {args.warmup}..{args.warmup + args.steps - 1} after {args.warmup} warm-up steps")
+
+
+def cpu_oracle_run(wl, host, warm_steps, timed_steps, nthreads=1):
+    """Time the CPU oracle over decode steps [warm_steps, warm_steps + timed_steps) (resolve +
+    backup, bytes included) after running steps [0, warm_steps) untimed, so it times the same
+    steps the GPU does. Requests are split over `nthreads` Python threads (ctypes drops the
+    GIL). `host` are the per-layer host pools of wl's layout."""
     import oracle
     from_state = wl.initial_state()
     dev = []
+    rq, tk0, rows0 = wl.initial_device_writes()
     for l in range(wl.L):
         p = np.full(wl.device_rows * wl.B, 0xA5, dtype=np.uint8)
-        rq, tk, rows = wl.initial_device_writes()
-        wl.scatter_rows(l, rq, tk, rows, p)
+        wl.scatter_rows(l, rq, tk0, rows0, p)
         dev.append(p)
     tokens, stamps, clock = from_state
     out = np.zeros((wl.R, wl.K), dtype=np.int32)
     miss = np.zeros(wl.R, dtype=np.int32)
-    orc = oracle.Oracle(wl.K, wl.H, wl.B, wl.L, wl.max_context, wl.host_rows, wl.device_rows, wl.ps, wl.max_pages)
+    stride = wl.host_row_stride if wl.cfg.host_layout == "page_first" else 0
+    orc = oracle.Oracle(wl.K, wl.H, wl.B, wl.L, wl.max_context, wl.host_rows, wl.device_rows, wl.ps, wl.max_pages,
+                        stride)
     shards = np.array_split(np.arange(wl.R), nthreads)
     elapsed = 0.0
     rows_done = 0
-    for step in range(steps):
+    for step in range(warm_steps + timed_steps):
         nr, nd = newest_rows(wl, step)
         for l in range(wl.L):
             dev[l].reshape(-1, wl.B)[nr] = nd[l]
@@ -258,79 +310,143 @@ def cpu_oracle_run(wl, host, steps, nthreads=1):
             for t in th:
                 t.join()
         orc.backup(S, wl.host_cache_locs, wl.device_buffer_locs, wl.resident_pages, host, dev)
-        elapsed += time.perf_counter() - t0
-        rows_done += int((tk >= 0).sum())
+        if step >= warm_steps:
+            elapsed += time.perf_counter() - t0
+            rows_done += int((tk >= 0).sum())
     return rows_done, elapsed
+
+
+def oracle_host_pools(wl):
+    """Plain host pools of wl's layout for a CPU-only oracle run."""
+    if wl.cfg.host_layout == "page_first":
+        base = np.zeros(wl.host_pool_bytes, dtype=np.uint8)
+        views = wl.host_layer_views(base)
+        for l, v in enumerate(views):
+            wl.fill_host_pool(l, v)
+        return views
+    host = [np.zeros(wl.host_rows * wl.B, dtype=np.uint8) for _ in range(wl.L)]
+    for l in range(wl.L):
+        wl.fill_host_pool(l, host[l])
+    return host
 
 
 # ------------------------------------------------------------------------------------------
 def run_reference(args, ws, rank):
+    """The reference arm: the CPU oracle, as it stands, on this machine's host cores, timed over
+    the same steps of the same workload as our arm (the warm-up steps run untimed first)."""
     if rank != 0:
         return
-    import workloads as W
-    steps = args.warmup + args.steps
-    wl = W.make(args.config, args.seed, steps=steps)
-    host = [np.empty(wl.host_rows * wl.B, dtype=np.uint8) for _ in range(wl.L)]  # CPU only
-    for l in range(wl.L):
-        wl.fill_host_pool(l, host[l])
-    for s in range(steps):
+    wl = make_workload(args, 0, total_steps_of(args))
+    host = oracle_host_pools(wl)
+    for s in range(args.warmup + args.steps):
         wl.top_k_tokens(s)
-    rows, sec = cpu_oracle_run(wl, host, steps)
+    rows, sec = cpu_oracle_run(wl, host, args.warmup, args.steps)
     value = rows / sec
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / steps, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": {"workload": f"{args.config}: {wl.R} requests, seq_len {int(wl.seq0[0])}+, top_k {wl.K}, "
-                               f"hot slots {wl.H}, {wl.B}-byte rows, {wl.L} layer(s)",
-                   "global_batch": wl.R, "seq_len": int(wl.seq0[0]), "parallelism": "cpu"},
+        "config": {"workload": workload_desc(args, wl), "global_batch": wl.R * args.gpus,
+                   "seq_len": int(wl.seq0[0]), "parallelism": "cpu"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{steps} decode steps of the full workload, single-threaded C oracle"},
+                         "sample": f"decode steps {args.warmup}..{args.warmup + args.steps - 1} of the workload "
+                                   f"(after {args.warmup} untimed warm-up steps), single-threaded C oracle, "
+                                   "resolve + row copies + backup"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------------------------------
+def rank_numa_node(local_rank: int, query=None) -> int:
+    """The host memory node for this rank's host pools: the one nearest its GPU ("Hierarchical
+    Sparse Attention" (Alibaba Tair KVCache), 2.4.4: the per-GPU host copy rate depends on NUMA
+    binding). query(device) -> node defaults to hs_host_numa_node; -1: leave the placement to
+    the kernel's default policy."""
+    if query is None:
+        import hierarchical_sparse_attention_gb300 as hs
+        query = hs.hs_host_numa_node
+    try:
+        return int(query(local_rank))
+    except Exception:  # noqa: BLE001 - no device or no answer: default placement
+        return -1
+
+
+def alloc_host_pools(wl, node: int = -1):
+    """Host pools of wl's layout, placed on memory node `node` (-1: default) before their pages
+    are touched, then filled. Returns (per-layer pool views, [(array, needs registering)])."""
+    import hierarchical_sparse_attention_gb300 as hs
+    bind = None
+    if node is not None and node >= 0:
+        bind = lambda addr, n: hs.hs_host_bind_node(addr, n, node)  # noqa: E731
+    if wl.cfg.host_layout == "page_first":
+        arr, reg = alloc_host(wl.host_pool_bytes, bind)
+        views = wl.host_layer_views(arr)
+        for l, v in enumerate(views):
+            wl.fill_host_pool(l, v)
+        return views, [(arr, reg)]
+    pools = [alloc_host(wl.host_rows * wl.B, bind) for _ in range(wl.L)]
+    for l, (arr, reg) in enumerate(pools):
+        wl.fill_host_pool(l, arr)
+    return [arr for arr, _ in pools], pools
+
+
+def build_host_pools(wl, hs, node: int = -1):
+    """alloc_host_pools, then each pool registered (pinned and mapped) and read from the GPU
+    TOUCH_PASSES times."""
+    views, pools = alloc_host_pools(wl, node)
+    for arr, reg in pools:
+        touch_host_pool_from_gpu(hs.hs_host_register(arr) if reg else host_device_ptr(arr), arr.nbytes)
+    return views, pools
+
+
+def job_throughput(rows_this_rank: int, seconds_this_rank: float, ws: int) -> float:
+    """Whole-job rows/s: every rank resolves a batch of the same shape (weak scaling), so the
+    job resolves ws x its rows in the slowest rank's time."""
+    return ws * rows_this_rank / max_over_ranks(seconds_this_rank, ws)
+
+
+def release_host_pools(hs, pools):
+    for arr, reg in pools:
+        if reg:
+            hs.hs_host_unregister(arr)
+    for obj in _POOL_OBJS:
+        obj.free()
+    _POOL_OBJS.clear()
+
+
 def run_ours(args, ws, rank, local):
     import torch
     import hierarchical_sparse_attention_gb300 as hs
-    import workloads as W
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     W_, K_ = args.warmup, args.steps
-    total_steps = W_ + K_
-    wl = W.make(args.config, args.seed + 1000 * rank, steps=total_steps)
+    total_steps = total_steps_of(args)
+    wl = make_workload(args, rank, total_steps)
     R, K, H, B, L = wl.R, wl.K, wl.H, wl.B, wl.L
+    layout = wl.cfg.host_layout
+    numa_node = rank_numa_node(local)
 
-    # ---- inputs: host pool (pinned, mapped), device pool, tables, all steps' top-k. The
-    # sweep points share one host layout, so their host pool is built once.
-    key = (args.config.split("_")[0], args.seed + 1000 * rank, wl.host_rows, B, L, total_steps)
+    # ---- inputs: host pools (pinned, mapped, on the GPU's host memory node), device pools,
+    # tables, all steps' top-k. The sweep points share one host layout, so their host pools
+    # are built once.
+    key = (args.config.split("_")[0], args.seed + 1000 * rank, wl.host_rows, B, L, total_steps, layout)
     if key not in _HOST_POOLS:
         for old in list(_HOST_POOLS):
-            for p, reg in _HOST_POOLS.pop(old):
-                if reg:
-                    hs.hs_host_unregister(p)
-            for obj in _POOL_OBJS:
-                obj.free()
-            _POOL_OBJS.clear()
-        pools = [alloc_host(wl.host_rows * B) for _ in range(L)]
-        for l, (arr, reg) in enumerate(pools):
-            wl.fill_host_pool(l, arr)
-            touch_host_pool_from_gpu(hs.hs_host_register(arr) if reg else host_device_ptr(arr), arr.nbytes)
-        _HOST_POOLS[key] = pools
-    host = [arr for arr, _ in _HOST_POOLS[key]]
+            release_host_pools(hs, _HOST_POOLS.pop(old)[1])
+        _HOST_POOLS[key] = build_host_pools(wl, hs, numa_node)
+    host, pool_objs = _HOST_POOLS[key]
     dpool = []
+    rq, tk0, rows0 = wl.initial_device_writes()
     for l in range(L):
         init = np.full(wl.device_rows * B, 0xA5, dtype=np.uint8)
-        rq, tk0, rows0 = wl.initial_device_writes()
         wl.scatter_rows(l, rq, tk0, rows0, init)
         dpool.append(torch.from_numpy(init).to(dev))
     topk_all = torch.from_numpy(np.stack([wl.top_k_tokens(s) for s in range(total_steps)])).to(dev)
     seq_all = torch.from_numpy(np.stack([wl.seq_lens(s) for s in range(total_steps)])).to(dev)
-    valid_rows = int((topk_all >= 0).sum().item()) // total_steps  # per step (no padding here)
+    valid_rows = int((topk_all[W_:W_ + K_] >= 0).sum().item()) // K_  # per timed step (no padding here)
     newest = [newest_rows(wl, s) for s in range(total_steps)]
     newest_idx = torch.from_numpy(np.stack([n[0] for n in newest])).to(dev)
     newest_dat = [torch.from_numpy(np.stack([n[1][l] for n in newest])).to(dev) for l in range(L)]
@@ -344,10 +460,12 @@ def run_ours(args, ws, rank, local):
     out = torch.empty((R, K), dtype=torch.int32, device=dev)
     miss = torch.empty((R,), dtype=torch.int32, device=dev)
     miss_acc = torch.zeros((total_steps, R), dtype=torch.int64, device=dev)
-    cfg = hs.make_config(R, K, H, B, L, wl.ps, wl.max_context, wl.max_pages)
+    stride = wl.host_row_stride if layout == "page_first" else 0
+    cfg = hs.make_config(R, K, H, B, L, wl.ps, wl.max_context, wl.max_pages, stride)
     wsp = torch.zeros(hs.hs_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
     h = hs.hs_create(cfg, host, dpool, wl.host_rows, wl.device_rows, wsp)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    copy_ctas, launches_per_resolve = hs.hs_launch_shape(h)
 
     def forward_stand_in(s):
         """What the forward pass leaves before the resolve: the newest token's row written to
@@ -397,15 +515,18 @@ def run_ours(args, ws, rank, local):
         resolve(torch.cuda.current_stream())
         backup(torch.cuda.current_stream())
     stream.wait_stream(cap)
-    # Rehearsal: the timed steps' inputs once, untimed, then the state is reset. The GPU's
-    # first reads of host-pool regions can stall ~0.5 ms each (more so after other processes
-    # churned host memory); a serving process pays that once at start-up, so the timed steps
-    # should not. The timed region below is still exactly K steps.
-    reset_state_and_warm()
-    for i in range(K_):
-        forward_stand_in(W_ + i)
-        graph.replay()
-    torch.cuda.synchronize()
+    # Rehearsal, untimed, then the state is reset: the GPU's first reads of host-pool regions
+    # can stall ~0.5 ms each (more so after other processes churned host memory); a serving
+    # process pays that once at start-up, so the timed steps should not. "disjoint" replays the
+    # K steps after the timed range (other rows of the same sequences), never the timed steps'
+    # own inputs; "timed" replays the timed steps themselves (kept for comparison only).
+    rehearsal = {"disjoint": range(W_ + K_, W_ + 2 * K_), "timed": range(W_, W_ + K_), "none": range(0)}[args.rehearsal]
+    if len(rehearsal):
+        reset_state_and_warm()
+        for s in rehearsal:
+            forward_stand_in(s)
+            graph.replay()
+        torch.cuda.synchronize()
     reset_state_and_warm()
 
     # ---- timed region A: K graph-replayed steps, per-step events, L2 flushed between steps
@@ -427,34 +548,48 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
     barrier(ws)
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    total_s = max_over_ranks(sum(step_ms) * 1e-3, ws)
     err = hs.hs_get_error(h, clear=True)
-    copy_ctas, launches_per_resolve = hs.hs_launch_shape(h)
-    misses = miss_acc[W_:].sum(dim=1).cpu().numpy()  # per timed step, all requests
+    misses = miss_acc[W_:W_ + K_].sum(dim=1).cpu().numpy()  # per timed step, all requests
     rows_timed = valid_rows * K_
-    value = ws * rows_timed / total_s
+    value = job_throughput(rows_timed, sum(step_ms) * 1e-3, ws)
 
-    # ---- pass B: the same steps eagerly, with an event between the two calls, for the
-    # resolve kernel's own duration (the dominant kernel of the roofline)
+    # ---- pass B: the same steps eagerly, with events around the dominant kernel. With copy
+    # CTAs that is the one resolve launch. Without them hs_resolve is the resolve, the grouping
+    # by host region and the pair gather; the same four kernels are issued here as
+    # hs_resolve_layers(copy_layers = 0) (resolve + grouping) and hs_gather of every layer
+    # (the gather alone), so the gather's own duration is measured.
+    split = launches_per_resolve > 1
     reset_state_and_warm()
-    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_)]
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K_)]
     torch.cuda._sleep(int(2e6 * (5 + K_ // 4)))
     for i in range(K_):
         s = W_ + i
         forward_stand_in(s)
         flush.zero_()
         evb[i][0].record(stream)
-        resolve(stream)
-        evb[i][1].record(stream)
-        backup(stream)
+        if split:
+            hs.hs_resolve_layers(h, R, tk_buf, sl_buf, hcl, dbl, tok, st, clk, rp, out, miss, 0, stream)
+            evb[i][1].record(stream)
+            hs.hs_gather(h, R, hcl, 0, L, stream)
+        else:
+            resolve(stream)
+            evb[i][1].record(stream)
         evb[i][2].record(stream)
+        backup(stream)
+        evb[i][3].record(stream)
+        miss_acc[s].copy_(miss)
     torch.cuda.synchronize()
-    res_ms = [e[0].elapsed_time(e[1]) for e in evb]
-    bak_ms = [e[1].elapsed_time(e[2]) for e in evb]
-    miss_bytes = misses.astype(np.float64) * B * L  # host-link bytes read per resolve launch
+    if not np.array_equal(miss_acc[W_:W_ + K_].sum(dim=1).cpu().numpy(), misses):
+        raise RuntimeError("pass B resolved different miss counts from the timed pass")
+    res_ms = [e[0].elapsed_time(e[2]) for e in evb]     # the whole hs_resolve work
+    dom_ms = [e[1 if split else 0].elapsed_time(e[2]) for e in evb]  # the dominant kernel alone
+    bak_ms = [e[2].elapsed_time(e[3]) for e in evb]
+    miss_bytes = misses.astype(np.float64) * B * L  # host-link bytes read per resolve (all layers)
+    dom_s = np.array(dom_ms) * 1e-3
     res_s = np.array(res_ms) * 1e-3
-    link_gbs = float(miss_bytes.sum() / res_s.sum() / 1e9)
-    # HBM algorithmic bytes of one resolve launch: top-k, seq_lens, slot map + stamps read,
+    link_gbs = float(miss_bytes.sum() / dom_s.sum() / 1e9)
+    call_gbs = float(miss_bytes.sum() / res_s.sum() / 1e9)
+    # HBM algorithmic bytes of the resolve's work: top-k, seq_lens, slot map + stamps read,
     # host-row lookups for misses, slot->row table, state writes, row table, the residency
     # bitmap row of each request, miss rows written
     bit_row_bytes = (wl.max_context + 127) // 128 * 16
@@ -467,7 +602,7 @@ def run_ours(args, ws, rank, local):
     except (OSError, ValueError):
         pass
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
-    traffic = ncu_traffic(args.config)
+    traffic = ncu_traffic(f"{args.config}/{layout}")
 
     # ---- end to end through the C ABI with host buffers, as a serving loop runs it: one pinned
     # input block (the step's top-k rows and seq_lens) that the host scheduler refills before each
@@ -526,39 +661,48 @@ def run_ours(args, ws, rank, local):
     e2e_value, e2e_ms = e2e_pass(True)
     h2d_b = 4 * R * K + 4 * R
     d2h_b = 4 * R * K + 4 * R
+    dominant = "resolve_kernel" if not split else "gather_pairs_kernel"
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K_, "warmup": W_,
         "ms_per_step": float(np.mean(step_ms)), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int32", "data": "synthetic",
-        "config": {"workload": f"{args.config}: {R} requests x seq_len {int(wl.seq0[0])}+1/step, top_k {K}, "
-                               f"{H} hot slots, {B}-byte rows, {L} layer(s)",
+        "config": {"workload": workload_desc(args, wl),
                    "global_batch": R * ws, "seq_len": int(wl.seq0[0]), "parallelism": f"requests sharded, dp{ws}",
                    "l2": "flushed between timed steps (256 MiB write)",
                    "step": "hs_resolve + hs_backup replayed as one CUDA graph",
-                   "rehearsal": "before timing, the K timed steps' inputs replayed once untimed, state reset"},
+                   "host_layout": layout,
+                   "rehearsal": {"disjoint": f"before timing, steps {W_ + K_}..{W_ + 2 * K_ - 1} (after the timed "
+                                             "range) replayed once untimed, state reset",
+                                 "timed": "before timing, the K timed steps' inputs replayed once untimed, state reset",
+                                 "none": "none"}[args.rehearsal]},
         "p50_step_us": 1e3 * float(np.median(step_ms)), "p90_step_us": 1e3 * float(np.percentile(step_ms, 90)),
         "p50_resolve_us": 1e3 * float(np.median(res_ms)), "p90_resolve_us": 1e3 * float(np.percentile(res_ms, 90)),
         "p50_backup_us": 1e3 * float(np.median(bak_ms)),
-        "resolve_timing": "eager launches, CUDA events around hs_resolve alone",
+        "p50_dominant_kernel_us": 1e3 * float(np.median(dom_ms)),
+        "resolve_timing": "eager launches, CUDA events around the resolve work alone (without copy CTAs: "
+                          "hs_resolve_layers(0) + hs_gather of every layer, the same four kernels as hs_resolve)",
         "step_us_per_step": [round(1e3 * x, 1) for x in step_ms],
+        "dominant_kernel_us_per_step": [round(1e3 * x, 1) for x in dom_ms],
         "misses_per_step": float(misses.mean()), "miss_h2d_gbs": link_gbs, "h2d_ceiling_gbs": h2d_ceiling,
         "miss_h2d_frac_of_ceiling": link_gbs / h2d_ceiling,
+        "miss_h2d_gbs_whole_call": call_gbs,
         "roofline": {"bound": "host_link", "achieved": link_gbs, "peak": h2d_ceiling, "unit": "GB/s",
                      "frac": link_gbs / h2d_ceiling,
                      "traffic": traffic.get("sysmem_read_bytes_per_launch"),
                      "traffic_metric": "ncu syslts sysmem read sectors x 32 B per launch (null: kernel changed)",
                      "algorithmic_bytes_per_launch": float(miss_bytes.mean()),
-                     "kernel": "resolve_kernel" if launches_per_resolve == 1 else
-                               "gather_pairs_kernel (no copy CTAs; the timed call also runs resolve_kernel, "
-                               "order_count_kernel and order_scatter_kernel)",
+                     "kernel": dominant,
+                     "kernel_timing": "CUDA events around the kernel's own launch on the launching stream, "
+                                      "eager pass over the timed steps",
                      "copy_ctas_per_request": copy_ctas,
                      "peak_source": "pinned cudaMemcpy H2D, 1 GiB, best of 12, measured in this run",
                      "hbm": {"achieved": hbm_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": hbm_gbs / hbm_peak,
                              "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)",
                              "traffic": (traffic["dram_read_bytes_per_launch"] + traffic["dram_write_bytes_per_launch"])
                              if traffic else None,
-                             "algorithmic_bytes_per_launch": float(hbm_bytes.mean())}},
+                             "algorithmic_bytes_per_launch": float(hbm_bytes.mean()),
+                             "timing": "the whole resolve work (all its launches)"}},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
                 "steps": e2e_steps, "p50_step_us": 1e3 * float(np.median(e2e_ms)),
                 "timing": "wall clock per step, graph launch to stream sync; the step's inputs are in one "
@@ -569,22 +713,22 @@ def run_ours(args, ws, rank, local):
                 "copies_value": e2e_copy_value, "copies_p50_step_us": 1e3 * float(np.median(e2e_copy_ms)),
                 "copies_timing": "the same step with one H2D copy of the inputs into device buffers and one D2H "
                                  "copy of the outputs in the graph"},
-        "host_pool": ("huge pages, hs_host_register" if _HOST_POOLS[key][0][1]
+        "host_pool": ("huge pages, hs_host_register" if pool_objs[0][1]
                       else "cudaHostAlloc (host could not back the pool with huge pages)"),
+        "host_numa_node": numa_node,
         "gpu_launches": (launches_per_resolve + 1) * K_,
         "device_flags": err,
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        sample_steps = min(total_steps, 24)
-        wl_cpu = W.make(args.config, args.seed, steps=sample_steps)
-        rows_c, sec_c = cpu_oracle_run(wl_cpu, host, sample_steps)
+        wl_cpu = make_workload(args, 0, W_ + K_)
+        rows_c, sec_c = cpu_oracle_run(wl_cpu, host, W_, K_)
         line["cpu_baseline"] = {"value": rows_c / sec_c, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": f"first {sample_steps} decode steps of the same workload, "
-                                          "single-threaded C oracle (resolve + row copies + backup)"}
+                                "sample": f"the timed decode steps {W_}..{W_ + K_ - 1} of the same workload "
+                                          f"(after {W_} untimed warm-up steps), single-threaded C oracle "
+                                          "(resolve + row copies + backup)"}
         ncores = len(os.sched_getaffinity(0))
-        rows_m, sec_m = cpu_oracle_run(W.make(args.config, args.seed, steps=sample_steps), host, sample_steps,
-                                       nthreads=ncores)
+        rows_m, sec_m = cpu_oracle_run(make_workload(args, 0, W_ + K_), host, W_, K_, nthreads=ncores)
         line["cpu_baseline_threaded"] = {"value": rows_m / sec_m, "unit": UNIT, "cores": ncores,
                                          "kind": "oracle sharded by request over threads"}
     hs.hs_destroy(h)
@@ -706,14 +850,10 @@ def run_split(args, ws, rank, local):
     copy = torch.cuda.Stream()
     W_, K_ = args.warmup, args.steps
     total = W_ + K_
-    wl = W.make(args.config, args.seed + 1000 * rank, steps=total)
+    wl = make_workload(args, rank, total)
     R, K, H, B, L = wl.R, wl.K, wl.H, wl.B, wl.L
     assert L >= 2, "the split needs at least two layers"
-    pools = [alloc_host(wl.host_rows * B) for _ in range(L)]
-    for l, (arr, reg) in enumerate(pools):
-        wl.fill_host_pool(l, arr)
-        touch_host_pool_from_gpu(hs.hs_host_register(arr) if reg else host_device_ptr(arr), arr.nbytes)
-    host = [arr for arr, _ in pools]
+    host, pools = build_host_pools(wl, hs, rank_numa_node(local))
     dpool = []
     for l in range(L):
         init = np.full(wl.device_rows * B, 0xA5, dtype=np.uint8)
@@ -733,7 +873,8 @@ def run_split(args, ws, rank, local):
     sl_buf = torch.empty((R,), dtype=torch.int32, device=dev)
     out = torch.empty((R, K), dtype=torch.int32, device=dev)
     miss = torch.empty((R,), dtype=torch.int32, device=dev)
-    cfg = hs.make_config(R, K, H, B, L, wl.ps, wl.max_context, wl.max_pages)
+    cfg = hs.make_config(R, K, H, B, L, wl.ps, wl.max_context, wl.max_pages,
+                         wl.host_row_stride if wl.cfg.host_layout == "page_first" else 0)
     wsps = {v: torch.zeros(hs.hs_workspace_bytes(cfg), dtype=torch.uint8, device=dev) for v in ("fused", "split", "split0")}
     handles = {v: hs.hs_create(cfg, host, dpool, wl.host_rows, wl.device_rows, wsps[v]) for v in wsps}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -819,7 +960,8 @@ def run_split(args, ws, rank, local):
         "metric": "time to first layer ready (leader resolve + follower gathers)", "value": float(sp[:, 0].mean()),
         "unit": "us", "n_gpus": ws, "steps": K_, "warmup": W_, "ms_per_step": float(sp[:, -1].mean()) / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": f"{args.config}: {R} requests, top_k {K}, {H} hot slots, {B}-byte rows, {L} layers",
+        "config": {"workload": f"{args.config}: {R} requests, top_k {K}, {H} hot slots, {B}-byte rows, {L} layers, "
+                               f"host pools {wl.cfg.host_layout.replace('_', '-')}",
                    "l2": "flushed between timed steps (256 MiB write)",
                    "split": "hs_resolve_layers(copy_layers=1) then hs_gather(l, 1) for l = 1..L-1 on a copy stream"},
         "split_layer_ready_us_mean": [float(x) for x in sp.mean(0)],
@@ -1202,6 +1344,8 @@ def run_spec(args, ws, rank, local):
 
 def main():
     args = parse()
+    if args.config is None:
+        args.config = "indexshare" if args.op in ("step", "split") else "dsa"
     ws, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, ws, rank)
@@ -1212,8 +1356,6 @@ def main():
     elif args.op == "spec":
         run_spec(args, ws, rank, local)
     elif args.op == "split":
-        if args.config == "dsa":
-            args.config = "indexshare"  # the split needs a layer group
         run_split(args, ws, rank, local)
     elif args.op != "step":
         run_invalidate(args, ws, rank, local)

@@ -32,14 +32,15 @@ EXPORTS = ("hs_workspace_bytes", "hs_create", "hs_resolve", "hs_backup", "hs_get
            "hs_status_str", "hs_host_register", "hs_host_unregister", "hs_resolve_noalloc",
            "hs_invalidate_tokens", "hs_invalidate_host_rows", "hs_resolve_layers", "hs_gather",
            "hs_resolve_spec", "hs_backup_spec", "hs_reset_hints", "hs_sparse_mla_workspace_bytes",
-           "hs_sparse_mla_decode", "hs_launch_shape", "hs_resolve_spec_layers", "hs_gather_spec")
+           "hs_sparse_mla_decode", "hs_launch_shape", "hs_resolve_spec_layers", "hs_gather_spec",
+           "hs_host_numa_node", "hs_host_bind_node")
 HS_MAX_SPEC_QUERIES = 8
 HS_NOALLOC_MAX_LAYERS = 8
 
 
 class hs_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("max_requests", "top_k", "hot_slots", "row_bytes", "num_layers",
-                                              "page_size", "max_context", "max_pages")]
+                                              "page_size", "max_context", "max_pages", "host_row_stride")]
 
 
 class HsError(RuntimeError):
@@ -97,6 +98,10 @@ def _load() -> ctypes.CDLL:
     lib.hs_host_register.restype = ctypes.c_int
     lib.hs_host_unregister.argtypes = [P]
     lib.hs_host_unregister.restype = ctypes.c_int
+    lib.hs_host_numa_node.argtypes = [i32, ctypes.POINTER(i32)]
+    lib.hs_host_numa_node.restype = ctypes.c_int
+    lib.hs_host_bind_node.argtypes = [P, sz, i32]
+    lib.hs_host_bind_node.restype = ctypes.c_int
     lib.hs_resolve_noalloc.argtypes = [cfgp, P, P, i64, i64, i32] + [P] * 11 + [P]
     lib.hs_resolve_noalloc.restype = ctypes.c_int
     return lib
@@ -151,8 +156,11 @@ def hs_status_str(status: int) -> str:
 
 
 def make_config(max_requests: int, top_k: int, hot_slots: int, row_bytes: int, num_layers: int = 1,
-                page_size: int = 0, max_context: int = 0, max_pages: int = 0) -> hs_config:
-    return hs_config(max_requests, top_k, hot_slots, row_bytes, num_layers, page_size, max_context, max_pages)
+                page_size: int = 0, max_context: int = 0, max_pages: int = 0, host_row_stride: int = 0) -> hs_config:
+    """host_row_stride: bytes between host rows of one layer (0: row_bytes, one pool per layer;
+    num_layers * row_bytes with pools base + l * row_bytes: every layer of a token in one row)."""
+    return hs_config(max_requests, top_k, hot_slots, row_bytes, num_layers, page_size, max_context, max_pages,
+                     host_row_stride)
 
 
 def hs_workspace_bytes(cfg: hs_config) -> int:
@@ -309,6 +317,18 @@ def hs_host_register(host_array, nbytes: Optional[int] = None) -> int:
 
 def hs_host_unregister(host_array) -> None:
     _check(_lib.hs_host_unregister(_addr(host_array)), "hs_host_unregister")
+
+
+def hs_host_numa_node(device: int) -> int:
+    """The host memory node nearest `device`, or -1 when the platform does not say."""
+    n = ctypes.c_int32(-1)
+    _check(_lib.hs_host_numa_node(device, ctypes.byref(n)), "hs_host_numa_node")
+    return int(n.value)
+
+
+def hs_host_bind_node(addr, nbytes: int, node: int) -> None:
+    """Prefer memory node `node` for the untouched pages of [addr, addr + nbytes)."""
+    _check(_lib.hs_host_bind_node(_addr(addr), nbytes, node), "hs_host_bind_node")
 
 
 def hs_resolve_noalloc(cfg: hs_config, host_pools: Sequence, device_pools: Sequence, host_rows: int,

@@ -1,6 +1,10 @@
 // C ABI of libhs (declared in include/hs.h): host-side validation, pool binding and
 // the stream-ordered launches. Nothing here allocates device or pinned memory or
 // synchronises on the hot path (hs_resolve / hs_backup).
+#include <sys/syscall.h>
+#include <unistd.h>
+
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 
@@ -28,6 +32,8 @@ struct hs_handle {
 
 namespace {
 
+constexpr int kNodeMaskWords = 16;  // host memory nodes 0..1023
+
 bool config_ok(const hs_config* c) {
   if (!c) return false;
   if (c->max_requests < 1 || c->top_k < 1 || c->top_k > HS_MAX_TOP_K) return false;
@@ -37,6 +43,7 @@ bool config_ok(const hs_config* c) {
   if (c->page_size > 0 &&
       (int64_t)c->max_pages * c->page_size < (int64_t)c->max_context)
     return false;
+  if (c->host_row_stride != 0 && c->host_row_stride < c->row_bytes) return false;
   return true;
 }
 
@@ -64,29 +71,17 @@ hs::OrderArgs order_slice(const hs_handle* h, int32_t q, const int32_t* host_cac
 
 }  // namespace
 
-extern "C" {
+namespace hs {
 
-size_t hs_workspace_bytes(const hs_config* cfg) {
-  return config_ok(cfg) ? hs::kWorkspaceBytes + hs::hint_bytes(cfg->max_requests, cfg->max_context) +
-                              hs::kPlanSlices * hs::plan_bytes(cfg->max_requests, cfg->top_k) +
-                              hs::order_bytes(cfg->max_requests, cfg->top_k)
-                        : 0;
-}
-
-hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* device_pools,
-                    int64_t host_rows, int64_t device_rows, void* workspace, hs_handle** out) {
-  if (!out) return HS_ERR_INVALID_ARG;
-  *out = nullptr;
-  if (!cfg || !host_pools || !device_pools || !workspace) return HS_ERR_INVALID_ARG;
+hs_status make_geometry(const hs_config* cfg, void* const* host_pools, void* const* device_pools,
+                        int64_t host_rows, int64_t device_rows, bool with_hints, int dev, Geometry* out,
+                        Pools* pools_out) {
+  if (!cfg || !host_pools || !device_pools || !out || !pools_out) return HS_ERR_INVALID_ARG;
   if (!config_ok(cfg)) return HS_ERR_INVALID_CONFIG;
   // Row tables are int32: every row index must fit.
   if (host_rows < 1 || device_rows < 1 || host_rows > INT32_MAX || device_rows > INT32_MAX)
     return HS_ERR_INVALID_ARG;
-
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
-
-  hs::Geometry g{};
+  Geometry g{};
   g.K = cfg->top_k;
   g.H = cfg->hot_slots;
   g.B = cfg->row_bytes;
@@ -94,22 +89,23 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   g.page_size = cfg->page_size;
   g.max_context = cfg->max_context;
   g.max_pages = cfg->max_pages;
-  g.bit_words = hs::hint_words(cfg->max_context);
+  g.bit_words = with_hints ? hint_words(cfg->max_context) : 0;
   g.hash_bits = ceil_log2(4 * (int64_t)cfg->top_k);  // top-k hash at most a quarter full
   if (g.hash_bits < 5) g.hash_bits = 5;
   g.sort_cap = 1 << ceil_log2(cfg->top_k);
   if (g.hash_bits < ceil_log2(cfg->top_k) + 1) g.hash_bits = ceil_log2(cfg->top_k) + 1;  // room for the aliases
   g.host_rows = host_rows;
   g.device_rows = device_rows;
-  // host regions of at most kOrderRegionBytes (at least one row), coarser for pools that
-  // need more than kOrderRegions of them
+  g.host_stride = cfg->host_row_stride > 0 ? cfg->host_row_stride : cfg->row_bytes;
+  // host regions of at most kOrderRegionBytes of host addresses (at least one row), coarser
+  // for pools that would need more than kOrderRegions of them
   g.order_shift = 0;
-  while (((int64_t)2 << g.order_shift) * g.B <= hs::kOrderRegionBytes) ++g.order_shift;
-  while (((host_rows - 1) >> g.order_shift) + 1 > hs::kOrderRegions) ++g.order_shift;
+  while (((int64_t)2 << g.order_shift) * g.host_stride <= kOrderRegionBytes) ++g.order_shift;
+  while (((host_rows - 1) >> g.order_shift) + 1 > kOrderRegions) ++g.order_shift;
   g.order_regions = (int32_t)(((host_rows - 1) >> g.order_shift) + 1);
 
-  hs::Pools pools{};
-  bool a16 = (g.B % 16) == 0, a4 = (g.B % 4) == 0;
+  Pools pools{};
+  bool a16 = (g.B % 16) == 0 && (g.host_stride % 16) == 0, a4 = (g.B % 4) == 0 && (g.host_stride % 4) == 0;
   for (int l = 0; l < g.L; ++l) {
     if (!host_pools[l] || !device_pools[l]) return HS_ERR_INVALID_ARG;
     cudaPointerAttributes ha{}, da{};
@@ -130,6 +126,46 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
     a4 = a4 && aligned(pools.host[l], 4) && aligned(pools.dev[l], 4);
   }
   g.vec = a16 ? 16 : (a4 ? 4 : 1);
+  // "page first": layer l's rows start l * B into one pool whose rows are L * B apart
+  g.host_interleaved = g.L > 1 && g.host_stride == (int64_t)g.L * g.B;
+  for (int l = 1; l < g.L && g.host_interleaved; ++l)
+    g.host_interleaved = pools.host[l] == pools.host[0] + (size_t)l * g.B;
+
+  if (const cudaError_t e = resolve_prepare(g, cfg->max_requests); e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorInvalidValue ? HS_ERR_INVALID_CONFIG : HS_ERR_CUDA;
+  }
+  *out = g;
+  *pools_out = pools;
+  return HS_OK;
+}
+
+}  // namespace hs
+
+extern "C" {
+
+size_t hs_workspace_bytes(const hs_config* cfg) {
+  return config_ok(cfg) ? hs::kWorkspaceBytes + hs::hint_bytes(cfg->max_requests, cfg->max_context) +
+                              hs::kPlanSlices * hs::plan_bytes(cfg->max_requests, cfg->top_k) +
+                              hs::order_bytes(cfg->max_requests, cfg->top_k)
+                        : 0;
+}
+
+hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* device_pools,
+                    int64_t host_rows, int64_t device_rows, void* workspace, hs_handle** out) {
+  if (!out) return HS_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !host_pools || !device_pools || !workspace) return HS_ERR_INVALID_ARG;
+  if (!config_ok(cfg)) return HS_ERR_INVALID_CONFIG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
+  hs::Geometry g{};
+  hs::Pools pools{};
+  if (const hs_status st = hs::make_geometry(cfg, host_pools, device_pools, host_rows, device_rows, true, dev, &g,
+                                             &pools);
+      st != HS_OK)
+    return st;
 
   cudaPointerAttributes wa{};
   if (cudaPointerGetAttributes(&wa, workspace) != cudaSuccess) {
@@ -139,11 +175,6 @@ hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* 
   if ((wa.type != cudaMemoryTypeDevice && wa.type != cudaMemoryTypeManaged) || wa.device != dev ||
       !aligned(workspace, 16))
     return HS_ERR_INVALID_ARG;
-
-  if (const cudaError_t e = hs::resolve_prepare(g, cfg->max_requests); e != cudaSuccess) {
-    cudaGetLastError();
-    return e == cudaErrorInvalidValue ? HS_ERR_INVALID_CONFIG : HS_ERR_CUDA;
-  }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (cudaMemset(ws, 0, hs::kWorkspaceBytes) != cudaSuccess) return HS_ERR_CUDA;
   if (cudaMemset(ws + hs::kWorkspaceBytes, 0, hs::hint_bytes(cfg->max_requests, cfg->max_context)) !=
@@ -475,6 +506,47 @@ hs_status hs_host_register(void* ptr, size_t bytes, void** device_ptr) {
     cudaHostUnregister(ptr);
     return HS_ERR_CUDA;
   }
+  return HS_OK;
+}
+
+hs_status hs_host_numa_node(int32_t device, int32_t* node) {
+  if (!node) return HS_ERR_INVALID_ARG;
+  *node = -1;
+  int v = -1;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrHostNumaId, device) == cudaSuccess && v >= 0) {
+    *node = v;
+    return HS_OK;
+  }
+  cudaGetLastError();
+  char bus[32] = {};
+  if (cudaDeviceGetPCIBusId(bus, (int)sizeof(bus), device) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  for (char* c = bus; *c; ++c)
+    if (*c >= 'A' && *c <= 'F') *c = (char)(*c - 'A' + 'a');  // sysfs spells the address in lower case
+  char path[96];
+  std::snprintf(path, sizeof(path), "/sys/bus/pci/devices/%s/numa_node", bus);
+  if (FILE* f = std::fopen(path, "r")) {
+    int n = -1;
+    if (std::fscanf(f, "%d", &n) == 1 && n >= 0) *node = n;
+    std::fclose(f);
+  }
+  return HS_OK;
+}
+
+hs_status hs_host_bind_node(void* ptr, size_t bytes, int32_t node) {
+  if (!ptr || !bytes || node < 0 || node >= 64 * kNodeMaskWords) return HS_ERR_INVALID_ARG;
+  const uintptr_t page = (uintptr_t)sysconf(_SC_PAGESIZE);
+  const uintptr_t lo = (uintptr_t)ptr & ~(page - 1);
+  const uintptr_t hi = ((uintptr_t)ptr + bytes + page - 1) & ~(page - 1);
+  unsigned long mask[kNodeMaskWords] = {};
+  mask[node / 64] = 1ul << (node % 64);
+  constexpr int kMpolPreferred = 1;  // <linux/mempolicy.h> MPOL_PREFERRED
+  // the kernel reads maxnode - 1 bits of the mask
+  if (syscall(SYS_mbind, (void*)lo, (unsigned long)(hi - lo), kMpolPreferred, mask,
+              (unsigned long)(64 * kNodeMaskWords + 1), 0u) != 0)
+    return HS_ERR_CUDA;
   return HS_OK;
 }
 

@@ -19,7 +19,7 @@ namespace {
 __device__ __forceinline__ void copy_row(const Geometry& g, const Pools* __restrict__ pools, int l, int64_t row,
                                          int64_t host, int lane) {
   const uint8_t* src = pools->dev[l] + (size_t)row * g.B;
-  uint8_t* dst = const_cast<uint8_t*>(pools->host[l]) + (size_t)host * g.B;
+  uint8_t* dst = const_cast<uint8_t*>(pools->host[l]) + (size_t)host * g.host_stride;
   if (g.vec == 16) {
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
     uint4* d4 = reinterpret_cast<uint4*>(dst);

@@ -16,8 +16,11 @@
 //     share a region are then requested together and share the GPU's translation of it; in
 //     miss order, rows spread over several large pools moved at about half the link's rate.
 // Both copy with 16-byte (else 4- or 1-byte) loads streamed past the caches, several in
-// flight per thread, and both grids are layer-major: one layer's rows move before the next
-// layer's start, so the host pages read at any moment span one layer's pool. Called on a copy
+// flight per thread. With one host pool per layer both go layer-major: one layer's rows move
+// before the next layer's start, so the host pages read at any moment span one layer's pool.
+// With every layer's bytes of a token in one host row ("page first", the other host layout of
+// "Hierarchical Sparse Attention" (Alibaba Tair KVCache), 2.4.4 "I/O Transfer Kernel"), the
+// pair gather reads each miss's layers as one contiguous span instead. Called on a copy
 // stream, one call per layer with an event after each, layer l + 1's rows move while layer
 // l's attention runs. Bound: the host link.
 #include "hs_internal.h"
@@ -28,6 +31,7 @@ namespace {
 constexpr int T = kGatherThreads;
 constexpr int M = kGatherMisses;
 constexpr int kUnroll = 4;
+constexpr int kGatherCtasPerSm = 2048 / T;  // a full SM's threads
 
 template <int V>
 struct Piece;
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(T) gather_kernel(const Geometry g, const Pools
         if (d >= 0) {
           const int32_t sr = s_src[j];
           dst[u] = dev + (size_t)d * g.B + (size_t)q * V;
-          v[u] = sr >= 0 ? P::load(host + (size_t)sr * g.B + (size_t)q * V) : P::zero();
+          v[u] = sr >= 0 ? P::load(host + (size_t)sr * g.host_stride + (size_t)q * V) : P::zero();
         }
       }
     }
@@ -197,46 +201,62 @@ __global__ void __launch_bounds__(kOrderThreads) order_scatter_kernel(const Geom
   }
 }
 
-// Copy rows of the ordered pairs: a CTA takes M consecutive pairs of one layer; blocks are
-// dispatched layer-major (blockIdx.y slowest).
+// Copy rows of the ordered pairs for layers [first_layer, first_layer + num_layers). The grid
+// is persistent (a few CTAs per SM, as many as one wave holds): the pair count is known only
+// on the device, and a grid sized for the largest count spent a wave's worth of time per
+// layer on CTAs with nothing to copy. The work is a list of items, each M consecutive pairs;
+// CTA b takes items b, b + gridDim.x, ... so the CTAs move through the list together.
+//   - Layers in one pool each ("layer first"): an item is (layer, M pairs), layer-major, so
+//     the host rows read at any moment lie in one layer's pool.
+//   - Interleaved host rows ("page first", g.host_interleaved): an item is M pairs of every
+//     requested layer. Host row h of layers [first_layer, first_layer + num_layers) is then
+//     one contiguous span of num_layers * B bytes, read front to back; only the device side
+//     splits it by layer.
 template <int V>
 __global__ void __launch_bounds__(T) gather_pairs_kernel(const Geometry g, const Pools* __restrict__ pools,
-                                                         const OrderArgs a, int first_layer) {
+                                                         const OrderArgs a, int first_layer, int num_layers) {
   __shared__ int32_t s_src[M], s_dst[M];
   using P = Piece<V>;
   const int64_t n = min((int64_t)*a.n_pairs, a.capacity);
-  const int64_t j0 = (int64_t)blockIdx.x * M;
-  if (j0 >= n) return;
-  const int nm = (int)min((int64_t)M, n - j0);
-  const int layer = first_layer + (int)blockIdx.y;
-  const uint8_t* host = pools->host[layer];
-  uint8_t* dev = pools->dev[layer];
-  if ((int)threadIdx.x < nm) {
-    s_src[threadIdx.x] = a.pair_src[j0 + threadIdx.x];
-    s_dst[threadIdx.x] = a.pair_dst[j0 + threadIdx.x];
-  }
-  __syncthreads();
+  const int64_t chunks = (n + M - 1) / M;
+  const bool span = g.host_interleaved != 0;
   const int per_row = g.B / V;
-  const int total = nm * per_row;
-  for (int base = threadIdx.x; base < total; base += T * kUnroll) {
-    typename P::type v[kUnroll];
-    uint8_t* dst[kUnroll];
+  const int64_t items = span ? chunks : chunks * num_layers;
+  for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+    const int layer0 = span ? first_layer : first_layer + (int)(item / chunks);
+    const int64_t j0 = (span ? item : item % chunks) * M;
+    const int nm = (int)min((int64_t)M, n - j0);
+    const int nl = span ? num_layers : 1;  // layers this item copies, from layer0 on
+    __syncthreads();  // the previous item is done with the pair table
+    if ((int)threadIdx.x < nm) {
+      s_src[threadIdx.x] = a.pair_src[j0 + threadIdx.x];
+      s_dst[threadIdx.x] = a.pair_dst[j0 + threadIdx.x];
+    }
+    __syncthreads();
+    const uint8_t* host = pools->host[layer0];
+    const int per_pair = per_row * nl;
+    const int total = nm * per_pair;
+    for (int base = threadIdx.x; base < total; base += T * kUnroll) {
+      typename P::type v[kUnroll];
+      uint8_t* dst[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int c = base + u * T;
-      dst[u] = nullptr;
-      if (c < total) {
-        const int j = c / per_row, q = c - j * per_row;
-        const int32_t d = s_dst[j], sr = s_src[j];
-        if (d >= 0) {
-          dst[u] = dev + (size_t)d * g.B + (size_t)q * V;
-          v[u] = sr >= 0 ? P::load(host + (size_t)sr * g.B + (size_t)q * V) : P::zero();
+      for (int u = 0; u < kUnroll; ++u) {
+        const int c = base + u * T;
+        dst[u] = nullptr;
+        if (c < total) {
+          const int j = c / per_pair, qs = c - j * per_pair;  // piece qs of the pair's span
+          const int l = qs / per_row, q = qs - l * per_row;
+          const int32_t d = s_dst[j], sr = s_src[j];
+          if (d >= 0) {
+            dst[u] = pools->dev[layer0 + l] + (size_t)d * g.B + (size_t)q * V;
+            v[u] = sr >= 0 ? P::load(host + (size_t)sr * g.host_stride + (size_t)qs * V) : P::zero();
+          }
         }
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (dst[u]) *reinterpret_cast<typename P::type*>(dst[u]) = v[u];
+      for (int u = 0; u < kUnroll; ++u)
+        if (dst[u]) *reinterpret_cast<typename P::type*>(dst[u]) = v[u];
+    }
   }
 }
 
@@ -261,11 +281,17 @@ cudaError_t launch_order(const Geometry& g, const OrderArgs& a, int32_t num_requ
 
 cudaError_t launch_gather_pairs(const Geometry& g, const Pools* pools, const OrderArgs& a, int32_t num_requests,
                                 int32_t first_layer, int32_t num_layers, cudaStream_t stream) {
-  const int64_t most = (int64_t)num_requests * g.K;  // the pair count is known only on the device
-  const dim3 grid((unsigned)((most + M - 1) / M), num_layers);
-  if (g.vec == 16) gather_pairs_kernel<16><<<grid, T, 0, stream>>>(g, pools, a, first_layer);
-  else if (g.vec == 4) gather_pairs_kernel<4><<<grid, T, 0, stream>>>(g, pools, a, first_layer);
-  else gather_pairs_kernel<1><<<grid, T, 0, stream>>>(g, pools, a, first_layer);
+  // the pair count is known only on the device: at most num_requests * K pairs, so no more
+  // CTAs than items, and no more than one wave (kGatherCtasPerSm per SM)
+  const int64_t most = (int64_t)num_requests * g.K;
+  const int64_t items = ((most + M - 1) / M) * (g.host_interleaved ? 1 : num_layers);
+  int64_t ctas = (int64_t)(g.sms > 0 ? g.sms : 1) * kGatherCtasPerSm;
+  if (ctas > items) ctas = items;
+  if (ctas < 1) ctas = 1;
+  const dim3 grid((unsigned)ctas);
+  if (g.vec == 16) gather_pairs_kernel<16><<<grid, T, 0, stream>>>(g, pools, a, first_layer, num_layers);
+  else if (g.vec == 4) gather_pairs_kernel<4><<<grid, T, 0, stream>>>(g, pools, a, first_layer, num_layers);
+  else gather_pairs_kernel<1><<<grid, T, 0, stream>>>(g, pools, a, first_layer, num_layers);
   return cudaGetLastError();
 }
 

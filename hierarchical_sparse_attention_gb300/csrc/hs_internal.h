@@ -41,6 +41,11 @@ struct Geometry {
   int32_t order_shift;    // host rows [b << order_shift, (b + 1) << order_shift) form host region b
   int32_t order_regions;  // regions covering the host pool (<= kOrderRegions); region
                           // order_regions collects misses whose host row is out of range
+  int32_t host_interleaved;  // 1: host_pools[l] = host_pools[0] + l * B and host_stride =
+                             // L * B ("page first"): one host row holds every layer's
+                             // bytes, so a miss of layers [a, b) is one contiguous span
+  int32_t sms;               // SMs of the device (grid size of the persistent pair gather)
+  int64_t host_stride;       // bytes from one host row to the next inside a layer's pool
   int64_t host_rows, device_rows;
 };
 
@@ -169,6 +174,16 @@ inline size_t order_bytes(int64_t max_requests, int64_t top_k) {
   return (size_t)((((rk * (1 + 2 * kPlanSlices) + 2 * (int64_t)(kOrderRegions + 1) + kPlanSlices + 1) * 4) + 255) &
                   ~(int64_t)255);
 }
+
+// The geometry and pools table of one layer group, shared by hs_create and
+// hs_resolve_noalloc: validates the configuration, the row counts and the pools (host pools
+// pinned and mapped, device pools on `dev`), derives the hash, sort and host-region sizes
+// and the copy width, and fits the resolve kernel to the device (resolve_prepare).
+// with_hints: the caller's workspace holds the residency bitmap. Returns HS_OK,
+// HS_ERR_INVALID_ARG, HS_ERR_INVALID_CONFIG or HS_ERR_CUDA.
+hs_status make_geometry(const hs_config* cfg, void* const* host_pools, void* const* device_pools,
+                        int64_t host_rows, int64_t device_rows, bool with_hints, int dev, Geometry* g,
+                        Pools* pools);
 
 // Dynamic shared memory of one resolve-kernel CTA for geometry g.
 size_t resolve_smem_bytes(const Geometry& g);

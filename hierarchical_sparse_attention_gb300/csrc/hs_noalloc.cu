@@ -13,6 +13,7 @@
 // contents. Each call rewrites the pools table and zeroes the error word before the kernel
 // runs, so results never depend on an earlier call; but two calls whose work overlaps on
 // the GPU (different streams, no ordering between them) race on the array.
+#include <cstring>
 #include <mutex>
 
 #include "hs_internal.h"
@@ -23,35 +24,79 @@ namespace {
 // the same layout as the workspace hs_create binds. kWorkspaceBytes = 256 bytes.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[hs::kWorkspaceBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-unsigned char* g_scratch_addr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
+// Writes one call's pools table into the scratch array and clears its error word, in stream
+// order before the resolve. A kernel argument carries the table, so nothing is copied from
+// host memory (a copy from a stack variable would be pageable and could block the host).
+__global__ void noalloc_setup_kernel(const hs::Pools pools, unsigned char* scratch) {
+  *reinterpret_cast<hs::Pools*>(scratch + hs::kPoolsOffset) = pools;
+  *reinterpret_cast<uint32_t*>(scratch + hs::kErrOffset) = 0u;
+}
 
-// Device-side address of the scratch array for the current device. In host code the
-// symbol names only a host-side stand-in, so the address is looked up once per device
-// (with that device current) and cached.
-hs_status scratch_for(int dev, unsigned char** out) {
+constexpr int kMaxDevices = 64;
+
+// Per-device set-up, kept so that later calls with the same configuration and pools skip
+// the host-side checks and kernel fitting (pointer queries, function attributes).
+struct DeviceSetup {
+  unsigned char* scratch;  // device address of g_noalloc_scratch on this device
+  bool valid;              // cfg / pools below describe geom / pools_table
+  hs_config cfg;
+  const void* host_pools[hs::kMaxLayers];
+  const void* device_pools[hs::kMaxLayers];
+  int64_t host_rows, device_rows;
+  hs::Geometry geom;
+  hs::Pools pools_table;
+};
+
+std::mutex g_setup_mutex;
+DeviceSetup g_setup[kMaxDevices] = {};
+
+bool same_call(const DeviceSetup& s, const hs_config* cfg, void* const* host_pools, void* const* device_pools,
+               int64_t host_rows, int64_t device_rows) {
+  if (!s.valid || std::memcmp(&s.cfg, cfg, sizeof(hs_config)) != 0 || s.host_rows != host_rows ||
+      s.device_rows != device_rows)
+    return false;
+  for (int l = 0; l < cfg->num_layers; ++l)
+    if (s.host_pools[l] != host_pools[l] || s.device_pools[l] != device_pools[l]) return false;
+  return true;
+}
+
+// The device address of the scratch array and the geometry for this call, on device `dev`
+// (current). In host code the array's name is only a host-side stand-in, so its device
+// address is looked up once per device, with that device current, and cached.
+hs_status setup_for(int dev, const hs_config* cfg, void* const* host_pools, void* const* device_pools,
+                    int64_t host_rows, int64_t device_rows, unsigned char** scratch, hs::Geometry* g,
+                    hs::Pools* pools) {
   if (dev < 0 || dev >= kMaxDevices) return HS_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_addr[dev]) {
+  DeviceSetup& s = g_setup[dev];
+  if (!s.scratch) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
       return HS_ERR_CUDA;
     }
-    g_scratch_addr[dev] = static_cast<unsigned char*>(p);
+    s.scratch = static_cast<unsigned char*>(p);
   }
-  *out = g_scratch_addr[dev];
+  if (!same_call(s, cfg, host_pools, device_pools, host_rows, device_rows)) {
+    s.valid = false;
+    // no hint table here (misses start their transfer after the exact probe)
+    const hs_status st =
+        hs::make_geometry(cfg, host_pools, device_pools, host_rows, device_rows, false, dev, &s.geom, &s.pools_table);
+    if (st != HS_OK) return st;
+    s.cfg = *cfg;
+    for (int l = 0; l < cfg->num_layers; ++l) {
+      s.host_pools[l] = host_pools[l];
+      s.device_pools[l] = device_pools[l];
+    }
+    s.host_rows = host_rows;
+    s.device_rows = device_rows;
+    s.valid = true;
+  }
+  *scratch = s.scratch;
+  *g = s.geom;
+  *pools = s.pools_table;
   return HS_OK;
 }
-
-int ceil_log2_i64(int64_t x) {
-  int b = 0;
-  while (((int64_t)1 << b) < x) ++b;
-  return b;
-}
-
-bool aligned_to(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 }  // namespace
 
@@ -64,16 +109,9 @@ hs_status hs_resolve_noalloc(const hs_config* cfg, void* const* host_pools, void
                              int32_t* lru_clock, const int32_t* resident_pages, int32_t* out_rows,
                              int32_t* miss_counts, uint32_t* error_flags, hs_stream_t stream) {
   if (!cfg || !host_pools || !device_pools) return HS_ERR_INVALID_ARG;
-  // Configuration limits are those of hs_create; the scratch array holds the pools table
-  // of at most HS_NOALLOC_MAX_LAYERS layers, and anything larger is refused here.
+  // The scratch array holds the pools table of at most HS_NOALLOC_MAX_LAYERS layers; a
+  // larger group is refused here. Every other limit is hs_create's (make_geometry).
   if (cfg->num_layers < 1 || cfg->num_layers > HS_NOALLOC_MAX_LAYERS) return HS_ERR_INVALID_CONFIG;
-  if (cfg->max_requests < 1 || cfg->top_k < 1 || cfg->top_k > HS_MAX_TOP_K || cfg->hot_slots < cfg->top_k ||
-      cfg->hot_slots > HS_MAX_HOT_SLOTS || cfg->row_bytes < 1 || cfg->max_context < 1 || cfg->page_size < 0 ||
-      cfg->max_pages < 0 ||
-      (cfg->page_size > 0 && (int64_t)cfg->max_pages * cfg->page_size < (int64_t)cfg->max_context))
-    return HS_ERR_INVALID_CONFIG;
-  if (host_rows < 1 || device_rows < 1 || host_rows > INT32_MAX || device_rows > INT32_MAX)
-    return HS_ERR_INVALID_ARG;
   if (num_requests < 0 || num_requests > cfg->max_requests) return HS_ERR_INVALID_ARG;
   if (num_requests == 0) return HS_OK;
   if (!top_k_tokens || !seq_lens || !host_cache_locs || !device_buffer_locs || !device_buffer_tokens ||
@@ -84,60 +122,19 @@ hs_status hs_resolve_noalloc(const hs_config* cfg, void* const* host_pools, void
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
   unsigned char* scratch = nullptr;
-  const hs_status st = scratch_for(dev, &scratch);
-  if (st != HS_OK) return st;
-
   hs::Geometry g{};
-  g.K = cfg->top_k;
-  g.H = cfg->hot_slots;
-  g.B = cfg->row_bytes;
-  g.L = cfg->num_layers;
-  g.page_size = cfg->page_size;
-  g.max_context = cfg->max_context;
-  g.max_pages = cfg->max_pages;
-  g.hash_bits = ceil_log2_i64(4 * (int64_t)cfg->top_k);  // top-k hash at most a quarter full
-  if (g.hash_bits < 5) g.hash_bits = 5;
-  g.sort_cap = 1 << ceil_log2_i64(cfg->top_k);
-  if (g.hash_bits < ceil_log2_i64(cfg->top_k) + 1) g.hash_bits = ceil_log2_i64(cfg->top_k) + 1;
-  g.host_rows = host_rows;
-  g.device_rows = device_rows;
-
   hs::Pools pools{};
-  bool a16 = (g.B % 16) == 0, a4 = (g.B % 4) == 0;
-  for (int l = 0; l < g.L; ++l) {
-    if (!host_pools[l] || !device_pools[l]) return HS_ERR_INVALID_ARG;
-    cudaPointerAttributes ha{}, da{};
-    if (cudaPointerGetAttributes(&ha, host_pools[l]) != cudaSuccess ||
-        cudaPointerGetAttributes(&da, device_pools[l]) != cudaSuccess) {
-      cudaGetLastError();
-      return HS_ERR_INVALID_ARG;
-    }
-    if (ha.type != cudaMemoryTypeHost || !ha.devicePointer) return HS_ERR_INVALID_ARG;
-    if ((da.type != cudaMemoryTypeDevice && da.type != cudaMemoryTypeManaged) || da.device != dev)
-      return HS_ERR_INVALID_ARG;
-    pools.host[l] = static_cast<const uint8_t*>(ha.devicePointer);
-    pools.dev[l] = static_cast<uint8_t*>(device_pools[l]);
-    a16 = a16 && aligned_to(pools.host[l], 16) && aligned_to(pools.dev[l], 16);
-    a4 = a4 && aligned_to(pools.host[l], 4) && aligned_to(pools.dev[l], 4);
-  }
-  g.vec = a16 ? 16 : (a4 ? 4 : 1);
-  if (hs::resolve_prepare(g, cfg->max_requests) != cudaSuccess) {
-    cudaGetLastError();
-    return HS_ERR_INVALID_CONFIG;  // shared memory does not fit this device
-  }
+  if (const hs_status st = setup_for(dev, cfg, host_pools, device_pools, host_rows, device_rows, &scratch, &g, &pools);
+      st != HS_OK)
+    return st;
 
   cudaStream_t s = (cudaStream_t)stream;
-  // The pools table comes from a stack copy: cudaMemcpyAsync from pageable memory has
-  // taken the bytes by the time it returns. The error word must start each call at zero.
-  if (cudaMemcpyAsync(scratch + hs::kPoolsOffset, &pools, sizeof(pools), cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemsetAsync(scratch + hs::kErrOffset, 0, sizeof(uint32_t), s) != cudaSuccess) {
-    cudaGetLastError();
-    return HS_ERR_CUDA;
-  }
-  // no hint table here (misses start their transfer after the exact probe) and no plan
+  noalloc_setup_kernel<<<1, 1, 0, s>>>(pools, scratch);
+  if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
+  // no hint table and no plan: every layer's rows are copied by the resolve kernel itself
   hs::ResolveArgs a{nullptr,   top_k_tokens, seq_lens,       host_cache_locs, device_buffer_locs, device_buffer_tokens,
                     lru_slots, lru_clock,    resident_pages, out_rows,        miss_counts,        g.L,
-                    nullptr,   nullptr,      nullptr,        -1,              1};  // every layer; no plan
+                    nullptr,   nullptr,      nullptr,        -1,              1};
   uint32_t* err_word = reinterpret_cast<uint32_t*>(scratch + hs::kErrOffset);
   if (hs::launch_resolve(g, reinterpret_cast<const hs::Pools*>(scratch + hs::kPoolsOffset), a, num_requests,
                          err_word, s) != cudaSuccess)

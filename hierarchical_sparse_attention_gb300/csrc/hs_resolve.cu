@@ -286,7 +286,7 @@ __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc
           if (d >= 0) {
             dst[u] = reinterpret_cast<uint4*>(p.dev[l] + (size_t)d * g.B) + q;
             const int32_t s = psrc[j];
-            v[u] = s >= 0 ? load_host16(reinterpret_cast<const uint4*>(p.host[l] + (size_t)s * g.B) + q)
+            v[u] = s >= 0 ? load_host16(reinterpret_cast<const uint4*>(p.host[l] + (size_t)s * g.host_stride) + q)
                           : make_uint4(0u, 0u, 0u, 0u);
           }
         }
@@ -303,7 +303,7 @@ __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc
       const int j = c / per_miss, rem = c - j * per_miss, l = rem / per_row, q = rem - l * per_row;
       const int32_t d = pdst[j], s = psrc[j];
       if (d < 0) continue;
-      uint32_t v = s >= 0 ? reinterpret_cast<const uint32_t*>(p.host[l] + (size_t)s * g.B)[q] : 0u;
+      uint32_t v = s >= 0 ? reinterpret_cast<const uint32_t*>(p.host[l] + (size_t)s * g.host_stride)[q] : 0u;
       reinterpret_cast<uint32_t*>(p.dev[l] + (size_t)d * g.B)[q] = v;
     }
   } else {
@@ -313,7 +313,7 @@ __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc
       const int j = c / per_miss, rem = c - j * per_miss, l = rem / g.B, q = rem - l * g.B;
       const int32_t d = pdst[j], s = psrc[j];
       if (d < 0) continue;
-      p.dev[l][(size_t)d * g.B + q] = s >= 0 ? p.host[l][(size_t)s * g.B + q] : (uint8_t)0;
+      p.dev[l][(size_t)d * g.B + q] = s >= 0 ? p.host[l][(size_t)s * g.host_stride + q] : (uint8_t)0;
     }
   }
 }
@@ -400,7 +400,7 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
         if (c < total) {
           const int k = c / per_miss, rem = c - k * per_miss, l = rem / per_row, qq = rem - l * per_row;
           const int32_t hr = c_hrow[c_list[k]];
-          v[u] = hr >= 0 ? load_host16(reinterpret_cast<const uint4*>(p.host[l] + (size_t)hr * g.B) + qq)
+          v[u] = hr >= 0 ? load_host16(reinterpret_cast<const uint4*>(p.host[l] + (size_t)hr * g.host_stride) + qq)
                          : make_uint4(0u, 0u, 0u, 0u);
         }
       }
@@ -460,7 +460,7 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
         const int e = c_dlist[j];
         const int32_t hr = c_hrow[e];
         dst[u] = reinterpret_cast<uint4*>(p.dev[l] + (size_t)c_res[e] * g.B) + qq;
-        v[u] = hr >= 0 ? load_host16(reinterpret_cast<const uint4*>(p.host[l] + (size_t)hr * g.B) + qq)
+        v[u] = hr >= 0 ? load_host16(reinterpret_cast<const uint4*>(p.host[l] + (size_t)hr * g.host_stride) + qq)
                        : make_uint4(0u, 0u, 0u, 0u);
       }
     }
@@ -1062,6 +1062,7 @@ cudaError_t resolve_prepare(Geometry& g, int32_t max_requests) {
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, resolve_kernel);
   if (e != cudaSuccess) return e;
   const int max_dynamic = optin - (int)fa.sharedSizeBytes;
+  g.sms = sms;
   g.copy_ctas = 0;
   g.copy_cap = 0;
   g.bits_smem = 0;

@@ -146,7 +146,19 @@ typedef enum {
  *   num_layers    L, 1..HS_MAX_LAYERS
  *   page_size     residency page size in tokens; 0 disables resident_pages
  *   max_context   row stride of host_cache_locs; seq_len may not exceed it
- *   max_pages     row stride of resident_pages; >= ceil(max_context / page_size) */
+ *   max_pages     row stride of resident_pages; >= ceil(max_context / page_size)
+ *   host_row_stride  bytes from host row h to host row h + 1 inside one layer's host pool;
+ *                 0 means row_bytes. Host row h of layer l is read at
+ *                 host_pools[l] + h * host_row_stride. With row_bytes (one pool per layer,
+ *                 "layer first") each layer's rows are back to back. With
+ *                 num_layers * row_bytes and host_pools[l] = base + l * row_bytes ("page
+ *                 first") one host row holds every layer's bytes of a token, so a miss reads
+ *                 one contiguous span for the whole group. Both are layouts of the host IO
+ *                 kernel in "Hierarchical Sparse Attention" (Alibaba Tair KVCache), 2.4.4
+ *                 "I/O Transfer Kernel" (layer_first, page_first); "vLLM Hybrid HiSparse
+ *                 source implementation analysis", 2.1 and 2.3, likewise packs a hot unit's
+ *                 leader and follower layers into one combined page and sizes host blocks by
+ *                 one stride. Must be 0 or >= row_bytes. */
 typedef struct {
   int32_t max_requests;
   int32_t top_k;
@@ -156,6 +168,7 @@ typedef struct {
   int32_t page_size;
   int32_t max_context;
   int32_t max_pages;
+  int32_t host_row_stride;
 } hs_config;
 
 typedef struct hs_handle hs_handle;
@@ -181,20 +194,36 @@ typedef struct hs_handle hs_handle;
  *     the GPU's address translation of each region for several rows; in the order the
  *     resolve finds them, rows spread over several large pools moved at about half the
  *     host link's rate.
- * The caller keeps the workspace for the handle's lifetime and does not write to it. */
+ * The caller keeps the workspace for the handle's lifetime and does not write to it.
+ * Why the caller allocates it: "vLLM HiSparse local KV offload architecture", "Ownership"
+ * -- the allocator provides GPU capacity and holds no KV semantics, while the runtime that
+ * resolves hits and picks victims owns the bytes bound to it; here the caller plays the
+ * allocator and the library the runtime, so the library never allocates device memory.
+ * Host only: no device work, no allocation. */
 HS_API size_t hs_workspace_bytes(const hs_config* cfg);
 
-/* Validate the configuration and bind the pools. host_pools / device_pools are arrays of
- * num_layers pointers to [host_rows, row_bytes] pinned+mapped host pools and
- * [device_rows, row_bytes] device pools. workspace is caller-owned device memory of
- * hs_workspace_bytes(cfg) bytes, zeroed here (synchronously). Allocates only the small
- * host-side handle. Returns HS_ERR_INVALID_ARG / HS_ERR_INVALID_CONFIG / HS_ERR_CUDA on
- * failure, with *out set to NULL. */
+/* Validate the configuration and bind the pools ("vLLM HiSparse local KV offload
+ * architecture", "Ownership": the runtime binds host and hot storage that others allocate;
+ * "Performance invariants": hot misses copy straight from registered pinned host memory).
+ * host_pools / device_pools are arrays of num_layers pointers to pinned+mapped host pools
+ * (host_rows rows of row_bytes, host_row_stride apart) and [device_rows, row_bytes] device
+ * pools. workspace is caller-owned device memory of hs_workspace_bytes(cfg) bytes, zeroed
+ * here (synchronously: set-up, not the decode path). Allocates only the small host-side
+ * handle; the pointers must stay valid for its lifetime. Returns HS_ERR_INVALID_ARG (a NULL
+ * or misplaced pointer: host pools not pinned and mapped, device pools or workspace not on
+ * the current device, workspace not 16-byte aligned), HS_ERR_INVALID_CONFIG (limits above,
+ * or tables that do not fit the device's shared memory) or HS_ERR_CUDA, with *out set to
+ * NULL. */
 HS_API hs_status hs_create(const hs_config* cfg, void* const* host_pools, void* const* device_pools,
                     int64_t host_rows, int64_t device_rows, void* workspace, hs_handle** out);
 
-/* One decode step of the resolver for requests 0..num_requests-1 (layout above): one
- * kernel launch on `stream` -- four when the configuration leaves no room for copy CTAs
+/* One decode step of the resolver for requests 0..num_requests-1 (layout and policy above;
+ * "HiSparse: moving the long-context decode capacity bottleneck from GPU memory to CPU
+ * memory", "Core: swap-in CUDA kernel" names its arguments; "vLLM HiSparse local KV offload
+ * architecture", "Hot-row lookup and LRU" orders resident, hot, host; "Performance
+ * invariants": every decision on the GPU, no device scalar readback or CPU round trip,
+ * capturable in a CUDA graph). One kernel launch on `stream` -- four when the configuration
+ * leaves no room for copy CTAs
  * (more requests than the GPU has SMs, or rows not 16-byte copyable): the resolve then
  * records the miss plan without copying, two small kernels group the misses by host
  * region, and a gather kernel copies every layer's rows, with the same results
@@ -372,14 +401,27 @@ HS_API hs_status hs_reset_hints(hs_handle* h, hs_stream_t stream);
  * Either pointer may be NULL. HS_ERR_INVALID_ARG for a NULL handle. */
 HS_API hs_status hs_launch_shape(const hs_handle* h, int32_t* copy_ctas, int32_t* resolve_launches);
 
-/* Read the workspace error word (synchronises the device; not for the hot path). With
- * clear != 0 the word is reset to zero. Returns HS_ERR_DEVICE_FLAGGED when any bit is set. */
+/* Read the workspace error word: the HS_FLAG_* bits the kernels OR in when they meet bad
+ * data ("vLLM Hybrid HiSparse source implementation analysis", 7.2: corrupt slot state is
+ * downgraded to a re-miss rather than trusted, and a source row out of range zero-fills its
+ * destination; the kernels never trap). It synchronises the device, so it is kept off the
+ * decode path ("vLLM HiSparse local KV offload architecture", "Performance invariants": no
+ * device scalar readback per step; 7.1 of the analysis reads its statistics only every 2000
+ * calls, outside capture). With clear != 0 the word is reset to zero. Returns
+ * HS_ERR_DEVICE_FLAGGED when any bit is set, HS_ERR_INVALID_ARG for a NULL argument,
+ * HS_ERR_CUDA when a CUDA call fails. */
 HS_API hs_status hs_get_error(hs_handle* h, uint32_t* flags, int clear);
 
-/* Free the host-side handle. Buffers stay the caller's. NULL is accepted. */
+/* Free the host-side handle and nothing else: the pools, tables, state and workspace stay
+ * the caller's ("vLLM HiSparse local KV offload architecture", "Ownership": the allocator
+ * owns capacity, the runtime binds it). Call it after the last stream work that uses the
+ * handle has been issued; work already queued keeps running. NULL is accepted. Always
+ * HS_OK. */
 HS_API hs_status hs_destroy(hs_handle* h);
 
-/* Static description of a status code. */
+/* Static, NUL-terminated description of a status code (never NULL; unknown codes give
+ * "unknown status"). The codes follow the error split of this header: host-side validation
+ * returns a status at once, device anomalies become HS_FLAG_* bits. */
 HS_API const char* hs_status_str(hs_status s);
 
 /* Page-lock an existing host range for the kernels' direct access (cudaHostRegister with
@@ -388,6 +430,26 @@ HS_API hs_status hs_host_register(void* ptr, size_t bytes, void** device_ptr);
 
 /* Undo hs_host_register. */
 HS_API hs_status hs_host_unregister(void* ptr);
+
+/* Host memory placement for the host pools. "Hierarchical Sparse Attention" (Alibaba Tair
+ * KVCache), 2.4.4 "I/O Transfer Kernel", reaches its per-GPU copy rate with NUMA binding: the
+ * pinned host pool a GPU reads should sit in the host memory nearest that GPU. On a node
+ * whose CPUs each serve some of the GPUs, one process per GPU places its own pools.
+ *
+ * hs_host_numa_node: the host memory node nearest `device` (cudaDevAttrHostNumaId, else the
+ * numa_node of the device's PCI function in sysfs), or -1 in *node when the platform does not
+ * say. Host only; HS_ERR_INVALID_ARG for a NULL node, HS_ERR_CUDA when the device cannot be
+ * queried.
+ *
+ * hs_host_bind_node: give [ptr, ptr + bytes) a preferred-node memory policy (mbind,
+ * MPOL_PREFERRED) for `node`, so the pages it has not touched yet are taken from that node
+ * (falling back to others when it is full). Call it on a fresh anonymous mapping before its
+ * pages are first touched and before hs_host_register; pages already present do not move.
+ * ptr is rounded down and the end up to whole pages. No allocation, no device work.
+ * HS_ERR_INVALID_ARG for a NULL range or a negative node, HS_ERR_CUDA (the system error) when
+ * the kernel refuses the policy. */
+HS_API hs_status hs_host_numa_node(int32_t device, int32_t* node);
+HS_API hs_status hs_host_bind_node(void* ptr, size_t bytes, int32_t node);
 
 /* hs_resolve for callers that cannot allocate device memory. The pages have no
  * counterpart for this entry point: it exists for callers with no way to make the
@@ -404,10 +466,13 @@ HS_API hs_status hs_host_unregister(void* ptr);
  * no cudaFree, no allocating library routine.
  *
  * The first call on a device, with that device current, looks up the array's device
- * address (cudaGetSymbolAddress) and caches it; make that first call before any stream
- * capture. Each call then queues, on `stream`, a copy of the pools table and a clear of
- * the error word into the array, the resolve kernel, and, when error_flags is not NULL,
- * a copy of this call's HS_FLAG_* bits into error_flags (one uint32 in device memory).
+ * address (cudaGetSymbolAddress), checks the pools and fits the kernel to the device, and
+ * caches all three; make that first call before any stream capture. A later call with the
+ * same configuration and pools reuses them; a changed configuration or pool set redoes the
+ * set-up on the host (no allocation). Each call then queues, on `stream`, a one-thread
+ * kernel that writes the pools table into the array and clears its error word, the resolve
+ * kernel, and, when error_flags is not NULL, a copy of this call's HS_FLAG_* bits into
+ * error_flags (one uint32 in device memory). Nothing is copied from host memory.
  * All calls share the array and it keeps the last call's contents, so calls whose work
  * overlaps on the GPU (on streams not ordered against each other) race; order them on
  * one stream. Returns the status codes of hs_create and hs_resolve. */

@@ -30,7 +30,7 @@ class Geom(ctypes.Structure):
                 ("row_bytes", ctypes.c_int32), ("num_layers", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("max_context", ctypes.c_int32),
                 ("max_pages", ctypes.c_int32), ("host_rows", ctypes.c_int64),
-                ("device_rows", ctypes.c_int64)]
+                ("device_rows", ctypes.c_int64), ("host_row_stride", ctypes.c_int64)]
 
 
 def build(force: bool = False) -> str:
@@ -106,16 +106,23 @@ class Oracle:
 
     def __init__(self, top_k: int, hot_slots: int, row_bytes: int, num_layers: int,
                  max_context: int, host_rows: int, device_rows: int, page_size: int = 0,
-                 max_pages: int = 0):
+                 max_pages: int = 0, host_row_stride: int = 0):
+        """host_row_stride: bytes between host rows of one layer's pool (0: row_bytes). With
+        num_layers * row_bytes the host pools are views base[l * row_bytes:] of one array."""
+        assert host_row_stride == 0 or host_row_stride >= row_bytes
         self.g = Geom(top_k, hot_slots, row_bytes, num_layers, page_size, max_context, max_pages,
-                      host_rows, device_rows)
+                      host_rows, device_rows, host_row_stride)
         self.lib = _load()
 
-    def _pools(self, pools: Sequence[np.ndarray], rows: int):
+    def _pools(self, pools: Sequence[np.ndarray], rows: int, stride: int = 0):
         assert len(pools) == self.g.num_layers
+        stride = stride or self.g.row_bytes
         for p in pools:
-            assert p.dtype == np.uint8 and p.flags.c_contiguous and p.size >= rows * self.g.row_bytes
+            assert p.dtype == np.uint8 and p.flags.c_contiguous and p.size >= (rows - 1) * stride + self.g.row_bytes
         return (ctypes.c_void_p * len(pools))(*[p.ctypes.data for p in pools])
+
+    def _host(self, pools: Sequence[np.ndarray]):
+        return self._pools(pools, self.g.host_rows, self.g.host_row_stride)
 
     def resolve(self, top_k_tokens, seq_lens, host_cache_locs, device_buffer_locs,
                 device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows,
@@ -133,7 +140,7 @@ class Oracle:
         if miss_counts is not None:
             _i32(miss_counts, (R,))
         err = ctypes.c_uint32(0)
-        hp = self._pools(host_pools, g.host_rows)
+        hp = self._host(host_pools)
         dp = self._pools(device_pools, g.device_rows)
         args = (ctypes.byref(g), R, _p(top_k_tokens), _p(seq_lens), _p(host_cache_locs),
                 _p(device_buffer_locs), _p(device_buffer_tokens), _p(lru_slots), _p(lru_clock),
@@ -161,7 +168,7 @@ class Oracle:
         _i32(host_cache_locs, (R, g.max_context))
         assert 0 <= first_layer and first_layer + num_layers <= g.num_layers
         err = ctypes.c_uint32(0)
-        hp = self._pools(host_pools, g.host_rows)
+        hp = self._host(host_pools)
         dp = self._pools(device_pools, g.device_rows)
         self.lib.oracle_gather(ctypes.byref(g), R, _p(plan.count), _p(plan.tokens), _p(plan.dst),
                                _p(host_cache_locs), first_layer, num_layers, hp, dp, ctypes.byref(err))
@@ -175,7 +182,7 @@ class Oracle:
         if resident_pages is not None:
             _i32(resident_pages, (R, g.max_pages))
         err = ctypes.c_uint32(0)
-        hp = self._pools(host_pools, g.host_rows)
+        hp = self._host(host_pools)
         dp = self._pools(device_pools, g.device_rows)
         self.lib.oracle_backup(ctypes.byref(g), R, _p(seq_lens), _p(host_cache_locs),
                                _p(device_buffer_locs), _p(resident_pages), hp, dp, ctypes.byref(err))
@@ -234,7 +241,7 @@ class Oracle:
         if miss_counts is not None:
             _i32(miss_counts, (Q, R))
         err = ctypes.c_uint32(0)
-        hp = self._pools(host_pools, g.host_rows)
+        hp = self._host(host_pools)
         dp = self._pools(device_pools, g.device_rows)
         args = (ctypes.byref(g), R, Q, _p(top_k_tokens), _p(committed_lens), _p(host_cache_locs),
                 _p(device_buffer_locs), _p(device_buffer_tokens), _p(lru_slots), _p(lru_clock),
@@ -260,7 +267,7 @@ class Oracle:
         if resident_pages is not None:
             _i32(resident_pages, (R, g.max_pages))
         err = ctypes.c_uint32(0)
-        hp = self._pools(host_pools, g.host_rows)
+        hp = self._host(host_pools)
         dp = self._pools(device_pools, g.device_rows)
         self.lib.oracle_backup_spec(ctypes.byref(g), R, num_queries, _p(committed_lens), _p(accepted),
                                     _p(host_cache_locs), _p(device_buffer_locs), _p(resident_pages), hp, dp,

@@ -31,23 +31,37 @@
  *                      Residency" (resident tokens read in place, hot tokens refresh their
  *                      LRU entry, misses copy one row from pinned host memory).
  *
- * Readings where the pages leave a step open (each is listed in the design notes):
+ * Readings where the pages leave a step open (the plainest reading the rest of the pages
+ * supports, with the passage it rests on):
  *   - The LRU state is a per-slot stamp plus a per-request clock; a slow-path call
  *     first advances the clock (c = clock + 1) and stamps every slot it touches with c.
+ *     [vLLM-impl] 7.1 keeps a per-slot order and rewrites it every call with the hits at
+ *     the most-recent end (7.2 phase 4); a stamp of the call's clock orders the slots the
+ *     same way and lives in device memory, so no host value enters the step.
  *   - Victims: slots not hit in this call, free slots first by ascending index, then
  *     occupied slots by ascending (stamp, slot). The j-th miss (top-k array order)
- *     takes the j-th victim.
+ *     takes the j-th victim. [Tair-HSA] 2.4.3: evict only when the buffer is full, the
+ *     coldest first; [vLLM-impl] 7.2 phase 3 hands the misses, compacted in order, the
+ *     oldest evictable slots in turn. The lowest slot breaks ties.
  *   - The newest token (seq_len - 1), when not resident and not on the fast path,
- *     resolves to the reserved slot H.
+ *     resolves to the reserved slot H: [SGLang-analysis] "How capacity is computed" pads
+ *     each request's buffer with room for the token the step adds.
  *   - A token >= seq_len outputs -1 (ERR_TOKEN); a repeated valid token keeps its first
- *     occurrence and the later ones output -1 (ERR_DUP).
+ *     occurrence and the later ones output -1 (ERR_DUP). [vLLM-impl] 7.1: padding rows
+ *     output -1 for attention to mask; one output row per distinct token keeps every
+ *     entry's row distinct.
  *   - Corrupt slot state (stamp outside [0, c-1], token outside [-1, seq_len-2]) is
- *     reset to free with stamp 0 (ERR_STATE). If several slots hold a looked-up token,
- *     the lowest slot is the hit (ERR_STATE).
+ *     reset to free with stamp 0 (ERR_STATE): [vLLM-impl] 7.2 phase 3, an out-of-range slot
+ *     is downgraded to a re-miss instead of being trusted. If several slots hold a
+ *     looked-up token, the lowest slot is the hit (ERR_STATE) and the other holders are not
+ *     hits: [vLLM-impl] 7.2 phase 2 sorts each slot into exactly two classes by probing the
+ *     top-k hash with its key -- a hit that gives the entry its row, or an evictable slot --
+ *     and one entry has one row, so one holder serves it and the rest are evictable with
+ *     their stamps. A held token nobody looks up is not probed, so its duplicates stay.
  *   - A miss whose host row is outside the host pool gets a zeroed destination
- *     (ERR_HOSTROW); a physical row outside the device pool outputs -1 and nothing is
- *     written (ERR_DEVROW); seq_len outside [0, max_context] skips the request
- *     (ERR_SEQLEN).
+ *     (ERR_HOSTROW, [vLLM-impl] 7.2, the gather kernel); a physical row outside the device
+ *     pool outputs -1 and nothing is written (ERR_DEVROW); seq_len outside
+ *     [0, max_context] skips the request (ERR_SEQLEN).
  *
  * Parity pins (tests, not this file): brute-force enumeration of victim choices on tiny
  * inputs, reduction to textbook LRU at top_k = 1, the pages' invariants (injective slot
@@ -67,7 +81,18 @@
 typedef struct {
   int32_t top_k, hot_slots, row_bytes, num_layers, page_size, max_context, max_pages;
   int64_t host_rows, device_rows;
+  int64_t host_row_stride; /* bytes from host row h to h + 1 in one layer's pool; 0 = row_bytes */
 } oracle_geom;
+
+/* Host row h of layer l. The host pool layouts of "Hierarchical Sparse Attention" (Alibaba
+ * Tair KVCache), 2.4.4 "I/O Transfer Kernel": layer first (one pool per layer, rows
+ * row_bytes apart) or page first (one row holds every layer's bytes of a token, the pools
+ * given as base + l * row_bytes, rows num_layers * row_bytes apart). Either way the row
+ * starts host_row_stride * h bytes into the layer's pool. */
+static uint8_t* host_row(const oracle_geom* g, uint8_t* const* host_pools, int32_t l, int64_t h) {
+  const int64_t stride = g->host_row_stride > 0 ? g->host_row_stride : g->row_bytes;
+  return host_pools[l] + (size_t)h * (size_t)stride;
+}
 
 enum { E_PAD = 0, E_BAD, E_DUP, E_VALID, E_RES, E_NEWEST, E_DONE, E_MISS };
 
@@ -277,7 +302,7 @@ static void resolve_call(const oracle_geom* g, int32_t num_requests, const int32
       if (!host_ok) *err |= OR_ERR_HOSTROW;
       for (int32_t l = 0; l < copy_layers; ++l) {
         uint8_t* dst = device_pools[l] + (size_t)d * (size_t)B;
-        if (host_ok) memcpy(dst, host_pools[l] + (size_t)h * (size_t)B, (size_t)B);
+        if (host_ok) memcpy(dst, host_row(g, host_pools, l, h), (size_t)B);
         else memset(dst, 0, (size_t)B);
       }
     }
@@ -391,7 +416,7 @@ void oracle_gather(const oracle_geom* g, int32_t num_requests, const int32_t* pl
           memset(to, 0, (size_t)B);
           continue;
         }
-        memcpy(to, host_pools[l] + (size_t)src_row * (size_t)B, (size_t)B);
+        memcpy(to, host_row(g, host_pools, l, src_row), (size_t)B);
       }
     }
   }
@@ -420,8 +445,7 @@ void oracle_backup(const oracle_geom* g, int32_t num_requests, const int32_t* se
     int64_t h = host_cache_locs[(int64_t)r * g->max_context + t];
     if (h < 0 || h >= g->host_rows) { *err |= OR_ERR_HOSTROW; continue; }
     for (int32_t l = 0; l < g->num_layers; ++l)
-      memcpy(host_pools[l] + (size_t)h * (size_t)B, device_pools[l] + (size_t)row * (size_t)B,
-             (size_t)B);
+      memcpy(host_row(g, host_pools, l, h), device_pools[l] + (size_t)row * (size_t)B, (size_t)B);
   }
 }
 
@@ -520,7 +544,7 @@ void oracle_backup_spec(const oracle_geom* g, int32_t num_requests, int32_t num_
       const int64_t h = host_cache_locs[(int64_t)r * g->max_context + t];
       if (h < 0 || h >= g->host_rows) { *err |= OR_ERR_HOSTROW; continue; }
       for (int32_t l = 0; l < g->num_layers; ++l)
-        memcpy(host_pools[l] + (size_t)h * (size_t)B, device_pools[l] + (size_t)row * (size_t)B, (size_t)B);
+        memcpy(host_row(g, host_pools, l, h), device_pools[l] + (size_t)row * (size_t)B, (size_t)B);
     }
   }
 }

@@ -13,20 +13,29 @@ import numpy as np
 import workloads as W
 
 
-def host_pools_for(wl: W.Workload, nthreads: int = 0):
+def host_pools_for(wl: W.Workload, nthreads: int = 0, with_bases: bool = False):
+    """Plain (unpinned) host pools holding every token's row: one array per layer, or for a
+    page-first layout per-layer views of one array. with_bases: also return the distinct
+    arrays behind the views."""
+    if wl.cfg.host_layout == "page_first":
+        base = np.zeros(wl.host_pool_bytes, dtype=np.uint8)
+        views = wl.host_layer_views(base)
+        for layer, v in enumerate(views):
+            wl.fill_host_pool(layer, v, nthreads)
+        return (views, [base]) if with_bases else views
     pools = []
     for layer in range(wl.L):
-        p = np.empty(wl.host_rows * wl.B, dtype=np.uint8)
+        p = np.zeros(wl.host_rows * wl.B, dtype=np.uint8)
         wl.fill_host_pool(layer, p, nthreads)
         pools.append(p)
-    return pools
+    return (pools, list(pools)) if with_bases else pools
 
 
 def device_pool_model(wl: W.Workload):
     pools = []
+    rq, tk, rows = wl.initial_device_writes()
     for layer in range(wl.L):
         p = np.full(wl.device_rows * wl.B, W.POISON_DEVICE, dtype=np.uint8)
-        rq, tk, rows = wl.initial_device_writes()
         wl.scatter_rows(layer, rq, tk, rows, p)
         pools.append(p)
     return pools
@@ -46,7 +55,7 @@ def poison_host_newest(wl: W.Workload, step: int, host_pools):
     for r in range(wl.R):
         h = int(wl.host_cache_locs[r, int(S[r]) - 1])
         for p in host_pools:
-            p[h * wl.B:(h + 1) * wl.B] = W.POISON_HOST
+            wl.host_row_bytes_of(p, h)[:] = W.POISON_HOST
 
 
 def host_newest_ok(wl: W.Workload, step: int, host_pools) -> bool:
@@ -55,7 +64,7 @@ def host_newest_ok(wl: W.Workload, step: int, host_pools) -> bool:
         t = int(S[r]) - 1
         h = int(wl.host_cache_locs[r, t])
         for layer, p in enumerate(host_pools):
-            if not np.array_equal(p[h * wl.B:(h + 1) * wl.B], wl.rows(layer, r, [t])[0]):
+            if not np.array_equal(wl.host_row_bytes_of(p, h), wl.rows(layer, r, [t])[0]):
                 return False
     return True
 
@@ -64,13 +73,19 @@ class OracleSim:
     """The oracle run over a workload, step by step (all arrays numpy)."""
 
     def __init__(self, wl: W.Workload, host_pools=None, nthreads: int = 0):
+        """host_pools: per-layer host pools to use; by default the run fills its own, so no
+        other party (the GPU run in particular) ever writes the bytes it reads."""
         import oracle
         self.wl = wl
-        self.host = host_pools if host_pools is not None else host_pools_for(wl, nthreads)
+        if host_pools is not None:
+            self.host, self.host_bases = host_pools, list(host_pools)
+        else:
+            self.host, self.host_bases = host_pools_for(wl, nthreads, with_bases=True)
         self.dev = device_pool_model(wl)
         self.tokens, self.stamps, self.clock = wl.initial_state()
+        stride = wl.host_row_stride if wl.cfg.host_layout == "page_first" else 0
         self.orc = oracle.Oracle(wl.K, wl.H, wl.B, wl.L, wl.max_context, wl.host_rows, wl.device_rows,
-                                 wl.ps, wl.max_pages)
+                                 wl.ps, wl.max_pages, stride)
         self.out = np.full((wl.R, wl.K), -1, dtype=np.int32)
         self.miss = np.zeros(wl.R, dtype=np.int32)
 

@@ -11,7 +11,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import workloads as W  # noqa: E402
-from harness import OracleSim, poison_host_newest  # noqa: E402
+from harness import OracleSim, poison_host_newest  # noqa: E402,F401
 
 pytestmark = pytest.mark.gpu
 ERR = dict(TOKEN=1, DUP=2, STATE=4, HOSTROW=8, DEVROW=16, SEQLEN=32)
@@ -20,20 +20,28 @@ ERR = dict(TOKEN=1, DUP=2, STATE=4, HOSTROW=8, DEVROW=16, SEQLEN=32)
 def _make_pair(requests=4, layers=1):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    from gpu_harness import GpuSim, host_pools
+    from gpu_harness import make_pair
     seq0 = (6000, 7000, 8000, 300) + (5000,) * (requests - 4)
     wl = W.make("dsa", requests=requests, top_k=256, hot_slots=512, steps=12, seq0=seq0, layers=layers)
-    host = host_pools(wl)
-    orc = OracleSim(wl, host_pools=host)
-    gpu = GpuSim(wl, host, orc.dev)
+    orc, gpu = make_pair(wl)
     return wl, orc, gpu
+
+
+def _done(orc, gpu, what):
+    """Both runs' host pools agree at the end (the GPU's written only by its backups), and no
+    guard around the GPU's pools or workspace changed."""
+    from gpu_harness import close_pair, final_host_check
+    try:
+        final_host_check(orc, gpu, what)
+    finally:
+        close_pair(gpu)
 
 
 @pytest.fixture
 def pair():
     wl, orc, gpu = _make_pair()
     yield wl, orc, gpu
-    gpu.close()
+    _done(orc, gpu, "faults")
 
 
 @pytest.fixture(params=["copy_ctas", "no_copy_ctas"])
@@ -45,7 +53,7 @@ def pair_any(request):
     wl, orc, gpu = _make_pair(*((4, 1) if request.param == "copy_ctas" else (160, 2)))
     assert (hs.hs_launch_shape(gpu.h)[0] == 0) == (request.param == "no_copy_ctas")
     yield wl, orc, gpu
-    gpu.close()
+    _done(orc, gpu, f"faults ({request.param})")
 
 
 def step_both(wl, orc, gpu, step, tk=None, sl=None, hcl=None, dbl=None):
@@ -53,6 +61,7 @@ def step_both(wl, orc, gpu, step, tk=None, sl=None, hcl=None, dbl=None):
     gpu.write_newest(step)
     orc.write_newest(step)
     poison_host_newest(wl, step, orc.host)
+    poison_host_newest(wl, step, gpu.host)
     tk = wl.top_k_tokens(step) if tk is None else tk
     sl = wl.seq_lens(step) if sl is None else sl
     gpu.upload(step, top_k=tk, seq_lens=sl)
@@ -188,6 +197,10 @@ def test_api_misuse():
         with pytest.raises(hs.HsError) as e:
             hs.hs_create(big, [host], [dev], 1000, 1000, ws)
         assert e.value.status == hs.HS_ERR_INVALID_CONFIG
+        short = hs.make_config(2, 64, 128, 576, 1, 0, 1024, 0, 500)  # host rows closer than a row
+        with pytest.raises(hs.HsError) as e:
+            hs.hs_create(short, [host], [dev], 1000, 1000, ws)
+        assert e.value.status == hs.HS_ERR_INVALID_CONFIG
         h = hs.hs_create(cfg, [host], [dev], 1000, 1000, ws)
         i32 = lambda *s: torch.zeros(s, dtype=torch.int32, device="cuda")  # noqa: E731
         tk, sl, hcl, dbl = i32(2, 64), i32(2), i32(2, 1024), i32(2, 129)
@@ -230,13 +243,11 @@ def test_two_handles_with_different_shared_memory_sizes():
     """Creating a smaller handle after a larger one must not break the larger one's launches."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    from gpu_harness import GpuSim, host_pools
+    from gpu_harness import close_pair, make_pair
     big = W.make("dsa", requests=2, top_k=2048, hot_slots=6144, steps=2, seq0=(20000, 30000))
     small = W.make("tiny", steps=2)
-    hb, hsm = host_pools(big), host_pools(small)
-    ob, osm = OracleSim(big, host_pools=hb), OracleSim(small, host_pools=hsm)
-    gb = GpuSim(big, hb, ob.dev)
-    gs = GpuSim(small, hsm, osm.dev)  # created second, needs less shared memory
+    ob, gb = make_pair(big)
+    osm, gs = make_pair(small)  # created second, needs less shared memory
     try:
         for s in range(2):
             for wl, o, g in ((big, ob, gb), (small, osm, gs)):
@@ -251,8 +262,8 @@ def test_two_handles_with_different_shared_memory_sizes():
                 np.testing.assert_array_equal(g.state()["out"], o.out)
                 np.testing.assert_array_equal(g.state()["stamps"], o.stamps)
     finally:
-        gb.close()
-        gs.close()
+        close_pair(gb)
+        close_pair(gs)
 
 
 def test_stale_or_garbage_hints_do_not_change_results(pair):

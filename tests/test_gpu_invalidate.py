@@ -9,7 +9,7 @@ torch = pytest.importorskip("torch")
 
 import oracle  # noqa: E402
 import workloads as W  # noqa: E402
-from harness import OracleSim, host_newest_ok, poison_host_newest  # noqa: E402
+from harness import host_newest_ok, poison_host_newest  # noqa: E402
 from test_gpu_parity import _gpu, compare_pools, compare_step  # noqa: E402
 
 pytestmark = pytest.mark.gpu
@@ -52,21 +52,20 @@ def _compare_state(gpu, orc, what):
 
 def run_with_invalidation(wl, every=3, seed=0):
     import hierarchical_sparse_attention_gb300 as hs
-    GpuSim, host_pools = _gpu()
-    host = host_pools(wl)
-    orc = OracleSim(wl, host_pools=host)
-    gpu = GpuSim(wl, host, orc.dev)
+    gh = _gpu()
+    orc, gpu = gh.make_pair(wl)
     rng = np.random.default_rng(seed)
     try:
         for step in range(wl.steps):
             gpu.write_newest(step)
             orc.write_newest(step)
-            poison_host_newest(wl, step, host)
+            poison_host_newest(wl, step, gpu.host)
+            poison_host_newest(wl, step, orc.host)
             gpu.upload(step)
             gpu.resolve()
             gpu.backup()
             torch.cuda.synchronize()
-            assert host_newest_ok(wl, step, host)
+            assert host_newest_ok(wl, step, gpu.host)
             oerr = orc.resolve(step) | orc.backup(step)
             gerr = compare_step(gpu, orc, f"{wl.cfg.name} step {step}")
             assert gerr == oerr, f"step {step}: flags gpu {gerr} oracle {oerr}"
@@ -86,8 +85,9 @@ def run_with_invalidation(wl, every=3, seed=0):
             gerr = _compare_state(gpu, orc, f"{wl.cfg.name} after step {step}, invalidate by {kind}")
             assert gerr == oerr, f"invalidate by {kind}: flags gpu {gerr} oracle {oerr}"
         compare_pools(gpu, orc, f"{wl.cfg.name} end")
+        gh.final_host_check(orc, gpu, f"{wl.cfg.name} end")
     finally:
-        gpu.close()
+        gh.close_pair(gpu)
 
 
 def test_invalidate_tiny():
@@ -128,7 +128,7 @@ def test_invalidate_dsa_full_size(form):
     """The dsa decode shape (32 requests, 4096 slots, seq 131072) on a seeded state, one CTA
     per request as in every call."""
     import hierarchical_sparse_attention_gb300 as hs
-    GpuSim, host_pools = _gpu()
+    _gpu()
     wl = W.make("dsa", 0, steps=2)
     rng = np.random.default_rng(21)
     S = wl.seq_lens(0)
@@ -168,11 +168,9 @@ def test_invalidate_dsa_full_size(form):
 def test_invalidate_edge_cases():
     """Long clear lists (several hash passes), a bad seq_len, an unsorted row list, empty lists."""
     import hierarchical_sparse_attention_gb300 as hs
-    GpuSim, host_pools = _gpu()
+    gh = _gpu()
     wl = W.make("tiny", 4)
-    host = host_pools(wl)
-    orc = OracleSim(wl, host_pools=host)
-    gpu = GpuSim(wl, host, orc.dev)
+    orc, gpu = gh.make_pair(wl)
     rng = np.random.default_rng(8)
     try:
         for step in range(6):
@@ -218,7 +216,8 @@ def test_invalidate_edge_cases():
         for step in range(6, 10):
             gpu.write_newest(step)
             orc.write_newest(step)
-            poison_host_newest(wl, step, host)
+            poison_host_newest(wl, step, gpu.host)
+            poison_host_newest(wl, step, orc.host)
             gpu.upload(step)
             gpu.resolve()
             gpu.backup()
@@ -226,5 +225,6 @@ def test_invalidate_edge_cases():
             oerr = orc.resolve(step) | orc.backup(step)
             assert compare_step(gpu, orc, f"after edge cases, step {step}") == oerr
         compare_pools(gpu, orc, "after edge cases")
+        gh.final_host_check(orc, gpu, "after edge cases")
     finally:
-        gpu.close()
+        gh.close_pair(gpu)

@@ -5,6 +5,12 @@ table, the miss counts, the slot map, the stamps, the clock and the error flags 
 step, the eager backup's host rows every step, and the whole device pools (hot rows,
 reserved rows, resident pages) at intervals and at the end. All comparisons are exact:
 the path is integer bookkeeping and byte copies.
+
+The two sides share no memory: the oracle fills and keeps its own host pools, the GPU gets
+pinned pools with guard rows around them (and around its device pools and workspace). So
+besides agreeing with the oracle, every row a GPU step resolved must hold the bytes the seeded
+generator gives its token (regenerated, in every layer), and at the end the GPU's whole host
+pools -- written only by its backups -- must equal the oracle's, with every guard intact.
 """
 import numpy as np
 import pytest
@@ -16,13 +22,15 @@ from harness import OracleSim, host_newest_ok, poison_host_newest  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
+ROWS_EVERY_STEP = 1 << 20  # check the resolved rows every step when a step has at most this many
+
 
 def _gpu():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import hierarchical_sparse_attention_gb300 as hs  # noqa: F401
-    from gpu_harness import GpuSim, host_pools
-    return GpuSim, host_pools
+    import gpu_harness
+    return gpu_harness
 
 
 def compare_step(gpu, orc, what):
@@ -44,18 +52,28 @@ def compare_pools(gpu, orc, what):
             raise AssertionError(f"{what}: device pool layer {layer} differs in {len(rows)} rows, e.g. {rows[:8]}")
 
 
-def run_parity(wl, host=None, steps=None, pool_every=8, graph_from=None, host_io=False):
-    GpuSim, host_pools = _gpu()
-    host = host if host is not None else host_pools(wl)
-    orc = OracleSim(wl, host_pools=host)
-    gpu = GpuSim(wl, host, orc.dev, host_io=host_io)
+def run_parity(wl, pools=None, steps=None, pool_every=8, graph_from=None, host_io=False):
+    """pools: (gpu host pools, their base arrays, oracle host pools) to reuse across runs of
+    one host layout; by default each side gets fresh ones."""
+    gh = _gpu()
+    if pools is None:
+        host, bases = gh.host_pools(wl)
+        orc = OracleSim(wl)
+        own = True
+    else:
+        host, bases, orc_host = pools
+        orc = OracleSim(wl, host_pools=orc_host)
+        own = False
+    gpu = gh.GpuSim(wl, host, orc.dev, host_io=host_io, host_bases=bases)
     steps = wl.steps if steps is None else steps
+    rows_every = 1 if wl.R * wl.K * wl.L <= ROWS_EVERY_STEP else pool_every
     graph = None
     try:
         for step in range(steps):
             gpu.write_newest(step)
             orc.write_newest(step)
-            poison_host_newest(wl, step, host)
+            poison_host_newest(wl, step, gpu.host)
+            poison_host_newest(wl, step, orc.host)
             gpu.upload(step)
             if graph_from is not None and step >= graph_from:
                 if graph is None:
@@ -71,15 +89,22 @@ def run_parity(wl, host=None, steps=None, pool_every=8, graph_from=None, host_io
                 gpu.resolve()
                 gpu.backup()
             torch.cuda.synchronize()
-            assert host_newest_ok(wl, step, host), f"step {step}: backup did not restore the newest host rows"
+            what = f"{wl.cfg.name} step {step}"
+            assert host_newest_ok(wl, step, gpu.host), f"{what}: backup did not restore the newest host rows"
             oerr = orc.resolve(step)
             oerr |= orc.backup(step)
-            gerr = compare_step(gpu, orc, f"{wl.cfg.name} step {step}")
-            assert gerr == oerr, f"step {step}: flags gpu {gerr} oracle {oerr}"
-            if (step + 1) % pool_every == 0 or step == steps - 1:
-                compare_pools(gpu, orc, f"{wl.cfg.name} step {step}")
+            gerr = compare_step(gpu, orc, what)
+            assert gerr == oerr, f"{what}: flags gpu {gerr} oracle {oerr}"
+            last = step == steps - 1
+            if (step + 1) % rows_every == 0 or last:
+                gh.resolved_rows_ok(wl, gpu, wl.top_k_tokens(step), gpu.state()["out"], what)
+            if (step + 1) % pool_every == 0 or last:
+                compare_pools(gpu, orc, what)
+        gh.final_host_check(orc, gpu, f"{wl.cfg.name} after {steps} steps")
     finally:
         gpu.close()
+        if own:
+            gh.free_host(bases)
     return orc
 
 
@@ -111,23 +136,21 @@ def test_no_copy_ctas_resolve_and_gather_in_a_graph():
     and a gather of all 3 layers. Eager for two steps, then the four replayed from a CUDA
     graph; every layer's rows match the oracle."""
     import hierarchical_sparse_attention_gb300 as hs
-    GpuSim, host_pools = _gpu()
+    gh = _gpu()
     wl = W.make("indexshare", 9, requests=80, top_k=64, hot_slots=128, steps=6, layers=3, seq_range=(1000, 3000))
-    host = host_pools(wl)
-    gpu = GpuSim(wl, host, OracleSim(wl, host_pools=host).dev)
+    orc, gpu = gh.make_pair(wl)
     try:
         assert hs.hs_launch_shape(gpu.h) == (0, 4)
     finally:
-        gpu.close()
-    run_parity(wl, host=host, graph_from=2)
+        gh.close_pair(gpu)
+    run_parity(wl, graph_from=2)
     few = W.make("indexshare", 9, requests=4, top_k=64, hot_slots=128, steps=1, layers=3, seq_range=(1000, 3000))
-    host = host_pools(few)
-    gpu = GpuSim(few, host, OracleSim(few, host_pools=host).dev)
+    orc, gpu = gh.make_pair(few)
     try:
         copy_ctas, launches = hs.hs_launch_shape(gpu.h)
         assert copy_ctas > 0 and launches == 1
     finally:
-        gpu.close()
+        gh.close_pair(gpu)
 
 
 def test_no_copy_ctas_edges():
@@ -140,14 +163,20 @@ def test_no_copy_ctas_edges():
 
 
 def test_miss_rate_sweep():
-    _, host_pools = _gpu()
+    from harness import host_pools_for
+    gh = _gpu()
     base = W.make("sweep_h4096_f0.8")
-    host = host_pools(base)  # token rows and host layout do not depend on the sweep point
-    for h in W.SWEEP_HOT:
-        for f in W.SWEEP_REUSE:
-            wl = W.make(f"sweep_h{h}_f{f}")
-            assert wl.host_rows == base.host_rows
-            run_parity(wl, host=host, pool_every=32)
+    # token rows and host layout do not depend on the sweep point: one set of pools per side
+    host, bases = gh.host_pools(base)
+    orc_host = host_pools_for(base)
+    try:
+        for h in W.SWEEP_HOT:
+            for f in W.SWEEP_REUSE:
+                wl = W.make(f"sweep_h{h}_f{f}")
+                assert wl.host_rows == base.host_rows
+                run_parity(wl, pools=(host, bases, orc_host), pool_every=32)
+    finally:
+        gh.free_host(bases)
 
 
 @pytest.mark.parametrize("shape", [
@@ -191,3 +220,29 @@ def test_large_buffer_row_table_in_global():
     """H = 5 x top_k = 10,240 slots at top_k 2048 (the speculative sizing): the resolve CTA's
     shared memory cannot hold the slot -> row table too, so it reads it from global memory."""
     run_parity(W.make("dsa", 8, requests=3, hot_slots=10240, steps=8, seq0=(40000, 52000, 30000)))
+
+
+def test_page_first_host_layout():
+    """One host pool whose row h holds every layer's bytes of a token (host_row_stride =
+    L x B, layer l at l x B): copy CTAs reading a miss's layers as one span, the resolve
+    without copy CTAs followed by the pair gather in span mode (eager, then from a graph), and
+    the backup writing into the strided rows."""
+    run_parity(W.make("indexshare", 12, requests=8, top_k=256, hot_slots=512, steps=6, layers=3,
+                      seq_range=(3000, 9000), host_layout="page_first"), pool_every=1)
+    run_parity(W.make("indexshare", 13, requests=80, top_k=64, hot_slots=128, steps=6, layers=3,
+                      seq_range=(1000, 3000), host_layout="page_first"), pool_every=1, graph_from=2)
+
+
+@pytest.mark.parametrize("shape", [
+    dict(requests=3, top_k=300, hot_slots=700, row_bytes=100, layers=3, seq0=(9000, 2000, 400)),  # 4-byte path
+    dict(requests=2, top_k=77, hot_slots=131, row_bytes=37, layers=2, seq0=(5000, 90)),  # byte path
+    dict(requests=90, top_k=40, hot_slots=64, row_bytes=48, layers=2, seq0=tuple(range(50, 950, 10))),
+])
+def test_page_first_ragged(shape):
+    run_parity(W.make("tiny", fmt=W.FMT_U8, steps=6, host_layout="page_first", **shape), pool_every=1)
+
+
+def test_indexshare_page_first():
+    """The IndexShare workload at full size with its four layers' host caches interleaved
+    row by row in one pool."""
+    run_parity(W.make("indexshare", host_layout="page_first"), pool_every=32)

@@ -134,17 +134,16 @@ def test_sparse_mla_masked_and_out_of_pool_rows():
 def test_sparse_mla_reads_the_resolvers_rows():
     """The consumer over the row table and device pool a decode step of the resolver left."""
     hs = _gpu()
-    from gpu_harness import GpuSim, host_pools
-    from harness import OracleSim, poison_host_newest
+    from gpu_harness import close_pair, make_pair
+    from harness import poison_host_newest
     wl = W.make("dsa", 3, requests=3, top_k=512, hot_slots=1024, steps=4, seq0=(6000, 9000, 700))
-    host = host_pools(wl)
-    orc = OracleSim(wl, host_pools=host)
-    gpu = GpuSim(wl, host, orc.dev)
+    orc, gpu = make_pair(wl)
     try:
         for step in range(wl.steps):
             gpu.write_newest(step)
             orc.write_newest(step)
-            poison_host_newest(wl, step, host)
+            poison_host_newest(wl, step, gpu.host)
+            poison_host_newest(wl, step, orc.host)
             gpu.upload(step)
             gpu.resolve()
             gpu.backup()
@@ -170,4 +169,42 @@ def test_sparse_mla_reads_the_resolvers_rows():
         check(q, pool, orc.out, sm, o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
               "after the resolver")
     finally:
-        gpu.close()
+        close_pair(gpu)
+
+
+def _distinct_rows_case(seed, R, Hq, K, pool_rows, sm_scale=None):
+    """R requests of K distinct valid rows each from a pool of fp8 MLA rows (as a resolved
+    step gives them: every entry a row, no two alike), seeded N(0, 1) queries."""
+    wl = W.make("dsa", seed, requests=R, top_k=min(K, 2048), steps=2)
+    rng = np.random.default_rng(seed)
+    pool = wl.rows(0, 0, rng.integers(0, 1 << 20, size=pool_rows).astype(np.int32)).reshape(-1)
+    out_rows = np.stack([rng.choice(pool_rows, size=K, replace=False) for _ in range(R)]).astype(np.int32)
+    q = wl.queries_bf16(0, Hq)
+    if sm_scale is None:
+        lat, rope = M.dequant_rows(pool, np.arange(64))
+        qq = M.bf16_decode(q[0])
+        sm_scale = float(np.float32(1.0 / (qq[:, :512] @ lat.T + qq[:, 512:] @ rope.T).std()))
+    return q, pool, out_rows, sm_scale
+
+
+def test_sparse_mla_bench_shape_one_split():
+    """The shape the consumer is timed at: 32 requests x 128 heads x 2,048 rows in one split,
+    i.e. 32 blocks of 64 rows per CTA through the three-tile ring, with the staged row table
+    at its 2,048-entry limit; the bench's sm_scale 1/1400 and the tests' unit-spread scale."""
+    hs = _gpu()
+    for sm in (1.0 / 1400, None):
+        q, pool, out_rows, scale = _distinct_rows_case(31, 32, 128, 2048, pool_rows=32 * 2048 + 4096, sm_scale=sm)
+        go, glse, err = run_gpu(hs, q, pool, out_rows, scale, 1)
+        assert err == 0
+        check(q, pool, out_rows, scale, go, glse, f"32 x 128 x 2048, 1 split, sm_scale {scale:.3g}")
+
+
+def test_sparse_mla_top_k_4096_one_split():
+    """4,096 rows in one split: more than the staged row table holds, so the producers read
+    the split's rows from global memory; 64 blocks per CTA."""
+    hs = _gpu()
+    q, pool, out_rows, sm = _distinct_rows_case(32, 4, 128, 4096, pool_rows=20000)
+    out_rows[1, ::7] = -1  # masked entries spread over the table
+    go, glse, err = run_gpu(hs, q, pool, out_rows, sm, 1)
+    assert err == 0
+    check(q, pool, out_rows, sm, go, glse, "top_k 4096, 1 split")

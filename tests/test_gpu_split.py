@@ -9,7 +9,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import workloads as W  # noqa: E402
-from harness import OracleSim, host_newest_ok, poison_host_newest  # noqa: E402
+from harness import host_newest_ok, poison_host_newest  # noqa: E402
 from test_gpu_parity import _gpu, compare_pools, compare_step  # noqa: E402
 
 pytestmark = pytest.mark.gpu
@@ -27,11 +27,9 @@ def _plan_views(gpu):
 def run_split(wl, copy_layers, gathers, mode="same", steps=None, check_plan=True):
     """mode: 'same' stream, 'side' (a copy stream behind per-layer events), or 'graph'."""
     import hierarchical_sparse_attention_gb300 as hs
-    GpuSim, host_pools = _gpu()
-    host = host_pools(wl)
-    orc = OracleSim(wl, host_pools=host)
+    gh = _gpu()
+    orc, gpu = gh.make_pair(wl)
     oplan = orc.orc.new_plan(wl.R)
-    gpu = GpuSim(wl, host, orc.dev)
     side = torch.cuda.Stream()
     graph = None
 
@@ -56,7 +54,8 @@ def run_split(wl, copy_layers, gathers, mode="same", steps=None, check_plan=True
         for step in range(wl.steps if steps is None else steps):
             gpu.write_newest(step)
             orc.write_newest(step)
-            poison_host_newest(wl, step, host)
+            poison_host_newest(wl, step, gpu.host)
+            poison_host_newest(wl, step, orc.host)
             gpu.upload(step)
             cur = torch.cuda.current_stream()
             if mode == "graph":
@@ -71,7 +70,7 @@ def run_split(wl, copy_layers, gathers, mode="same", steps=None, check_plan=True
             else:
                 gpu_step(cur)
             torch.cuda.synchronize()
-            assert host_newest_ok(wl, step, host)
+            assert host_newest_ok(wl, step, gpu.host)
             oerr = orc.orc.resolve(wl.top_k_tokens(step), wl.seq_lens(step), wl.host_cache_locs,
                                    wl.device_buffer_locs, orc.tokens, orc.stamps, orc.clock, wl.resident_pages,
                                    orc.out, orc.miss, orc.host, orc.dev, copy_layers=wl.L, plan=oplan)
@@ -88,8 +87,10 @@ def run_split(wl, copy_layers, gathers, mode="same", steps=None, check_plan=True
                     m = int(pc[r])
                     np.testing.assert_array_equal(pt[r, :m], oplan.tokens[r, :m], err_msg=f"step {step} r {r}")
                     np.testing.assert_array_equal(pd[r, :m], oplan.dst[r, :m], err_msg=f"step {step} r {r}")
+            gh.resolved_rows_ok(wl, gpu, wl.top_k_tokens(step), gpu.state()["out"], f"split step {step}")
+        gh.final_host_check(orc, gpu, f"{wl.cfg.name} split")
     finally:
-        gpu.close()
+        gh.close_pair(gpu)
 
 
 def _indexshare_small(**kw):
@@ -122,6 +123,16 @@ def test_full_resolve_then_regather_in_miss_order():
     run_split(_indexshare_small(), 3, [(0, 3)])
 
 
+def test_split_page_first_host_rows():
+    """Every layer's bytes of a token in one host row: the followers' gather copies each miss's
+    follower layers as one span, on the same stream and inside a graph, with and without copy
+    CTAs."""
+    run_split(_indexshare_small(host_layout="page_first"), 1, [(1, 2)])
+    run_split(_indexshare_small(host_layout="page_first"), 1, [(1, 1), (2, 1)], mode="graph")
+    run_split(W.make("indexshare", 8, requests=80, top_k=64, hot_slots=128, steps=4, layers=3,
+                     seq_range=(1000, 3000), host_layout="page_first"), 2, [(2, 1)], mode="side")
+
+
 def test_split_four_layers_dsa_rows():
     run_split(W.make("indexshare", 7, requests=6, top_k=256, hot_slots=512, steps=6, layers=4,
                      seq_range=(4000, 9000)), 2, [(2, 1), (3, 1)], mode="side")
@@ -131,11 +142,9 @@ def test_leader_only_step_matches_the_oracle():
     """copy_layers = 1 and no gather: the followers' pools keep their old rows, exactly as the
     oracle's leader-only step leaves them."""
     import hierarchical_sparse_attention_gb300 as hs
-    GpuSim, host_pools = _gpu()
+    gh = _gpu()
     wl = _indexshare_small(steps=3)
-    host = host_pools(wl)
-    orc = OracleSim(wl, host_pools=host)
-    gpu = GpuSim(wl, host, orc.dev)
+    orc, gpu = gh.make_pair(wl)
     try:
         for step in range(wl.steps):
             gpu.write_newest(step)
@@ -166,5 +175,6 @@ def test_leader_only_step_matches_the_oracle():
         with pytest.raises(hs.HsError):
             hs.hs_gather(gpu.h, wl.R, gpu.hcl, 1, 1)
         torch.cuda.synchronize()
+        gpu.check_guards("leader only")
     finally:
-        gpu.close()
+        gh.close_pair(gpu)

@@ -1,12 +1,15 @@
 """Multi-rank host logic of bench.py on CPU (gloo, world size 2).
 
 Requests shard across ranks with no data-path collective: each rank resolves its own batch
-(seed offset by rank) and only the step time is reduced (max over ranks). The reference arm
-prints from rank 0 alone.
+(seed offset by rank) and only the step time is reduced (max over ranks); the job's value is
+every rank's rows over that time. Each rank places its host pools on the memory node beside its
+GPU (a fake GPU -> node map here) before their pages are touched. The reference arm prints from
+rank 0 alone.
 """
 import os
 import socket
 
+import numpy as np
 import pytest
 import torch
 import torch.distributed as dist
@@ -23,6 +26,9 @@ def _free_port():
     return port
 
 
+FAKE_NODES = {0: 0, 1: 0}  # GPU -> host memory node, as a two-GPU rank pair on one CPU would have
+
+
 def _worker(rank, ws, port, out):
     import sys
     sys.path[:0] = [ROOT]
@@ -30,29 +36,49 @@ def _worker(rank, ws, port, out):
     dist.init_process_group("gloo", rank=rank, world_size=ws)
     import bench
     import workloads as W
-    local_time = 1.0 + rank  # rank 1 is the slower one
-    t = bench.max_over_ranks(local_time, ws)
-    wl = W.make("dsa", 0 + 1000 * rank, requests=2, steps=2)
+    # whole-job throughput as the bench reports it: every rank's rows over the slowest time
+    rows = 4096  # the same batch shape on every rank
+    value = bench.job_throughput(rows, 1.0 + rank, ws)  # rank 1 is the slower one
+    # each rank's pools go to the node its GPU sits beside, before any page is touched
+    node = bench.rank_numa_node(rank, query=FAKE_NODES.__getitem__)
+    # a pool smaller than a huge page: an anonymous mapping on any host (no driver-pinned fallback)
+    wl = W.make("tiny", 1000 * rank, requests=2, steps=2, seq0=(1000, 100))
+    views, pools = bench.alloc_host_pools(wl, node)
+    addr = "%x" % pools[0][0].ctypes.data
+    policy = next((ln.split()[1] for ln in open("/proc/self/numa_maps") if ln.startswith(addr + " ")), None)
+    filled = bool(np.array_equal(wl.host_row_bytes_of(views[0], int(wl.host_cache_locs[0, 5])),
+                                 wl.rows(0, 0, [5])[0]))
     first = wl.top_k_tokens(1)[0, :8].tolist()
     gathered = [None] * ws
     dist.all_gather_object(gathered, first)
-    out[rank] = (t, gathered[0] != gathered[1])
+    out[rank] = (value, gathered[0] != gathered[1], node, policy, filled)
     bench.barrier(ws)
     dist.destroy_process_group()
 
 
-def test_two_ranks_max_time_and_independent_shards():
+def test_two_ranks_job_value_numa_placement_and_independent_shards():
     port = _free_port()
     manager = mp.Manager()
     out = manager.dict()
     mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
     for rank in range(2):
-        t, differ = out[rank]
-        assert t == 2.0  # every rank reports the slowest rank's time
+        value, differ, node, policy, filled = out[rank]
+        assert value == pytest.approx(2 * 4096 / 2.0)  # 2 ranks x 4096 rows in the slower rank's 2 s
         assert differ  # ranks resolve different synthetic batches
-    # whole-job throughput: all ranks' rows over the max time
-    rows_per_rank = 65536 * 4
-    assert 2 * rows_per_rank / 2.0 == rows_per_rank
+        assert node == FAKE_NODES[rank]
+        assert policy == f"prefer:{node}", policy  # the pool's pages come from the rank's node
+        assert filled
+
+
+def test_rank_numa_node_without_an_answer():
+    import sys
+    sys.path[:0] = [ROOT]
+    import bench
+
+    def no_device(dev):
+        raise RuntimeError("no CUDA device")
+    assert bench.rank_numa_node(0, query=no_device) == -1
+    assert bench.rank_numa_node(3, query={3: 7}.__getitem__) == 7
 
 
 def _ref_worker(rank, ws, port, out):
@@ -62,7 +88,8 @@ def _ref_worker(rank, ws, port, out):
     sys.path[:0] = [ROOT]
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(ws))
     import bench
-    args = type("A", (), dict(impl="reference", config="tiny", seed=0, steps=2, warmup=1, gpus=ws))()
+    args = type("A", (), dict(impl="reference", config="tiny", seed=0, steps=2, warmup=1, gpus=ws,
+                              host_layout="auto", rehearsal="disjoint"))()
     dist.init_process_group("gloo", rank=rank, world_size=ws)
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):

@@ -50,6 +50,10 @@ MUTANTS = [
     ("spec_marks_before_s0_only", "t <= base; ++t) tokens[t] = t;", "t < base; ++t) tokens[t] = t;"),
     ("spec_backup_first_reserved_row", "if (row < 0) row = t + 1 <= H ? dbl[t] : dbl[H + j];",
      "if (row < 0) row = t + 1 <= H ? dbl[t] : dbl[H];"),
+    ("host_stride_ignored", "const int64_t stride = g->host_row_stride > 0 ? g->host_row_stride : g->row_bytes;",
+     "const int64_t stride = g->row_bytes;"),
+    ("duplicate_holder_highest_slot", "      if (holders[t] == 0) lowest_slot[t] = s;\n",
+     "      lowest_slot[t] = s;\n"),
     ("spec_plans_share_one_slice", "copy_layers, plan_tokens ? plan_tokens + q * RK : NULL, plan_dst ? plan_dst + q * RK : NULL,",
      "copy_layers, plan_tokens, plan_dst,"),
 ]

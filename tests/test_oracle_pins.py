@@ -67,6 +67,46 @@ def test_hand_trace():
         assert int(q.clock[0]) == st["clock"]
 
 
+def test_duplicate_holders_golden():
+    """A slot map holding two tokens twice, worked by hand from the resolve kernel's phases 2
+    and 3 ("vLLM Hybrid HiSparse source implementation analysis", 7.2): a looked-up token's
+    lowest holder serves it, its other holder stays evictable, and ages out like any slot."""
+    g = json.load(open(os.path.join(GOLDEN, "duplicate_holders_h5_k2.json")))
+    q = OneRequest(g["hot_slots"], g["top_k"], dbl=g["device_buffer_locs"])
+    q.tokens[0, :] = g["initial"]["tokens"]
+    q.stamps[0, :] = g["initial"]["stamps"]
+    q.clock[0] = g["initial"]["clock"]
+    for st in g["steps"]:
+        out, miss, err = q.step(st["seq_len"], st["top_k"])
+        assert out.tolist() == st["out"], st["why"]
+        assert miss == st["miss"] and err == st["err"], st["why"]
+        assert q.tokens[0].tolist() == st["tokens"], st["why"]
+        assert q.stamps[0].tolist() == st["stamps"], st["why"]
+        assert int(q.clock[0]) == st["clock"]
+
+
+def test_page_first_layout_changes_only_addresses():
+    """Every layer's bytes of a token in one host row ("Hierarchical Sparse Attention" (Alibaba
+    Tair KVCache), 2.4.4, page_first): the same steps give the same row tables, slot state,
+    flags and device pools as one host pool per layer, and after every backup host row h of
+    layer l in the shared pool holds exactly layer l's row h of the layer-first pools."""
+    wl_a = small_workload("indexshare_small")
+    wl_b = W.make("indexshare", 0, host_layout="page_first", **{k: v for k, v in SMALL["indexshare_small"].items()
+                                                                   if k != "base"})
+    a, b = OracleSim(wl_a), OracleSim(wl_b)
+    assert wl_b.host_row_stride == wl_b.L * wl_b.B and len(b.host_bases) == 1
+    for step in range(wl_a.steps):
+        assert a.step(step) == b.step(step) == 0
+        for name in ("out", "miss", "tokens", "stamps", "clock"):
+            np.testing.assert_array_equal(getattr(a, name), getattr(b, name), err_msg=f"step {step}: {name}")
+        for layer in range(wl_a.L):
+            assert np.array_equal(a.dev[layer], b.dev[layer]), f"step {step}: device pool {layer}"
+        shared = b.host_bases[0].reshape(wl_b.host_rows, wl_b.L, wl_b.B)
+        for layer in range(wl_a.L):
+            assert np.array_equal(shared[:, layer, :], a.host[layer].reshape(wl_a.host_rows, wl_a.B)), \
+                f"step {step}: host layer {layer}"
+
+
 def test_pages_arithmetic():
     g = json.load(open(os.path.join(GOLDEN, "pages_arithmetic.json")))
     row = g["fp8_mla_row"]
@@ -398,7 +438,8 @@ def test_backup_locations():
 def run_all_pins() -> int:
     """Run every pin above in-process; returns the number that failed (used on purpose-
     broken oracle builds by test_oracle_mutants)."""
-    checks = [test_hand_trace, test_pages_arithmetic, test_fast_path_identity_and_transition,
+    checks = [test_hand_trace, test_duplicate_holders_golden, test_page_first_layout_changes_only_addresses,
+              test_pages_arithmetic, test_fast_path_identity_and_transition,
               test_first_step_takes_free_slots_in_order, test_full_reuse_gives_zero_misses_after_warmup,
               test_all_padding_changes_nothing_but_the_clock, test_resident_first, test_error_paths,
               test_slot_holding_the_newest_token_is_corrupt, test_backup_locations]

@@ -73,7 +73,7 @@ def _rowgen():
         lib.rowgen_rows.restype = None
         lib.rowgen_scatter.argtypes = [u64, i32, i32, i32, P, P, P, i64, P]
         lib.rowgen_scatter.restype = None
-        lib.rowgen_fill_pool.argtypes = [u64, i32, i32, i32, i32, P, P, i32, P, i32]
+        lib.rowgen_fill_pool.argtypes = [u64, i32, i32, i32, i32, P, P, i32, P, i32, i64]
         lib.rowgen_fill_pool.restype = i32
         _lib = lib
     return _lib
@@ -144,7 +144,9 @@ class HostPool:
     portable). `array` is the bytes; `needs_register` tells whether the caller must still
     page-lock it (hs_host_register), i.e. the huge-page path."""
 
-    def __init__(self, nbytes: int):
+    def __init__(self, nbytes: int, before_fault=None):
+        """before_fault(addr, nbytes): called on the fresh mapping before any of its pages is
+        touched (to set its memory policy: place it on a memory node)."""
         import mmap
         self.nbytes = int(nbytes)
         self._mmap = None
@@ -152,6 +154,8 @@ class HostPool:
         huge = _huge_page_bytes()
         m = mmap.mmap(-1, max(self.nbytes, 1), flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
         arr = np.frombuffer(m, dtype=np.uint8, count=self.nbytes)
+        if before_fault is not None and self.nbytes:
+            before_fault(arr.ctypes.data, len(m))
         ok = False
         try:
             m.madvise(mmap.MADV_HUGEPAGE)
@@ -211,6 +215,8 @@ class Config:
     resident_tail_pages: int = 0  # "mixed": pages at the end of the step-0 sequence on the GPU
     resident_frac: float = 0.0  # "mixed": share of top-k drawn from the resident tail
     backup: bool = True  # run the eager backup every step
+    host_layout: str = "layer_first"  # "layer_first": one host pool per layer; "page_first": one
+    # pool whose row h holds every layer's bytes of a token (layer l at l * row_bytes)
 
 
 CONFIGS: Dict[str, Config] = {
@@ -509,14 +515,38 @@ class Workload:
         _rowgen().rowgen_scatter(self.seed, self.cfg.fmt, self.B, layer, _ptr(rq), _ptr(tk), _ptr(dr),
                                  len(dr), _ptr(pool))
 
+    # ---- host pool layout ----------------------------------------------------------
+    @property
+    def host_row_stride(self) -> int:
+        """Bytes from one host row to the next inside a layer's pool."""
+        return self.L * self.B if self.cfg.host_layout == "page_first" else self.B
+
+    @property
+    def host_pool_bytes(self) -> int:
+        """Bytes of one layer's pool (layer first) or of the one shared pool (page first)."""
+        return self.host_rows * self.B * (self.L if self.cfg.host_layout == "page_first" else 1)
+
+    def host_layer_views(self, base: np.ndarray) -> List[np.ndarray]:
+        """Per-layer pool views of one page-first pool: layer l starts l * B bytes in."""
+        assert self.cfg.host_layout == "page_first"
+        return [base[layer * self.B:] for layer in range(self.L)]
+
+    def host_row_bytes_of(self, pool: np.ndarray, row: int) -> np.ndarray:
+        """The B bytes of host row `row` in one layer's pool (view)."""
+        s = self.host_row_stride
+        return pool[row * s: row * s + self.B]
+
     def fill_host_pool(self, layer: int, pool: np.ndarray, nthreads: int = 0) -> None:
+        """Write every token's row of `layer` into its host row of `pool` (one layer's pool,
+        or that layer's view of a page-first pool)."""
         assert pool.dtype == np.uint8 and pool.flags.c_contiguous
-        assert pool.size >= self.host_rows * self.B
+        assert pool.size >= (self.host_rows - 1) * self.host_row_stride + self.B
         if nthreads <= 0:
             nthreads = max(1, len(os.sched_getaffinity(0)))
         sm = np.ascontiguousarray(self.seq_max, dtype=np.int32)
         _rowgen().rowgen_fill_pool(self.seed, self.cfg.fmt, self.B, layer, self.R, _ptr(sm),
-                                   _ptr(self.host_cache_locs), self.max_context, _ptr(pool), nthreads)
+                                   _ptr(self.host_cache_locs), self.max_context, _ptr(pool), nthreads,
+                                   self.host_row_stride)
 
 
 def make(name: str, seed: int = 0, **overrides) -> Workload:

@@ -123,6 +123,7 @@ void rowgen_scatter(uint64_t seed, int32_t fmt, int32_t row_bytes, int32_t layer
 typedef struct {
   uint64_t seed;
   int32_t fmt, row_bytes, layer, num_requests, max_context;
+  int64_t row_stride;
   const int32_t* seq_max;
   const int32_t* host_cache_locs;
   uint8_t* pool;
@@ -137,17 +138,19 @@ static void* fill_worker(void* arg) {
       int32_t h = loc[t];
       if (h < 0) continue;
       make_row(j->seed, j->fmt, j->row_bytes, j->layer, r, t,
-               j->pool + (size_t)h * (size_t)j->row_bytes);
+               j->pool + (size_t)h * (size_t)j->row_stride);
     }
   }
   return NULL;
 }
 
-/* Fill one layer's host pool: row host_cache_locs[r][t] <- row(layer, r, t) for t < seq_max[r].
+/* Fill one layer's host pool: row host_cache_locs[r][t] <- row(layer, r, t) for t < seq_max[r],
+ * host row h starting h * row_stride bytes into `pool` (row_stride 0: row_bytes).
  * Work is split by request over up to `nthreads` threads. Returns 0 on success. */
 int32_t rowgen_fill_pool(uint64_t seed, int32_t fmt, int32_t row_bytes, int32_t layer,
                          int32_t num_requests, const int32_t* seq_max, const int32_t* host_cache_locs,
-                         int32_t max_context, uint8_t* pool, int32_t nthreads) {
+                         int32_t max_context, uint8_t* pool, int32_t nthreads, int64_t row_stride) {
+  if (row_stride <= 0) row_stride = row_bytes;
   if (nthreads < 1) nthreads = 1;
   if (nthreads > 256) nthreads = 256;
   if (nthreads > num_requests) nthreads = num_requests > 0 ? num_requests : 1;
@@ -159,7 +162,7 @@ int32_t rowgen_fill_pool(uint64_t seed, int32_t fmt, int32_t row_bytes, int32_t 
     fill_job* j = &jobs[i];
     j->seed = seed; j->fmt = fmt; j->row_bytes = row_bytes; j->layer = layer;
     j->num_requests = num_requests; j->max_context = max_context; j->seq_max = seq_max;
-    j->host_cache_locs = host_cache_locs; j->pool = pool;
+    j->host_cache_locs = host_cache_locs; j->pool = pool; j->row_stride = row_stride;
     j->r0 = i * per;
     j->r1 = (i + 1) * per < num_requests ? (i + 1) * per : num_requests;
     started[i] = 0;
