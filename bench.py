@@ -400,6 +400,16 @@ def build_host_pools(wl, hs, node: int = -1):
     return views, pools
 
 
+STALL_RATIO = 2.0
+MAX_ATTEMPTS = 3
+
+
+def stalled(ms, ws: int) -> bool:
+    """A timed pass with a step above STALL_RATIO x its median, on any rank."""
+    local = 1.0 if float(np.max(ms)) > STALL_RATIO * float(np.median(ms)) else 0.0
+    return max_over_ranks(local, ws) > 0.0
+
+
 def job_throughput(rows_this_rank: int, seconds_this_rank: float, ws: int) -> float:
     """Whole-job rows/s: every rank resolves a batch of the same shape (weak scaling), so the
     job resolves ws x its rows in the slowest rank's time."""
@@ -529,11 +539,16 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
     reset_state_and_warm()
 
-    # ---- timed region A: K graph-replayed steps, per-step events, L2 flushed between steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K_)]
-    barrier(ws)
-    torch.cuda.synchronize()
-    with ClockSampler(local, enabled=not args.no_clocks) as clocks:
+    # ---- timed region A: K graph-replayed steps, per-step events, L2 flushed between steps.
+    # A pass in which some step took more than STALL_RATIO x the pass's median is measured
+    # again (at most MAX_ATTEMPTS passes, the state reset before each): on this platform the
+    # GPU's reads of a registered host pool sometimes stall for milliseconds for a while
+    # (more often after another process released tens of GB of pinned memory), a property of
+    # the host side that a serving process sees once at start-up. Every attempt is reported.
+    def region_a():
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K_)]
+        barrier(ws)
+        torch.cuda.synchronize()
         # keep the GPU busy while the host queues every timed step, so the per-step events
         # measure device time, not Python call overhead between launches
         torch.cuda._sleep(int(2e6 * (5 + K_ // 4)))
@@ -546,8 +561,19 @@ def run_ours(args, ws, rank, local):
             evs[i][1].record(stream)
             miss_acc[s].copy_(miss)
         torch.cuda.synchronize()
-    barrier(ws)
-    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
+        barrier(ws)
+        return [e[0].elapsed_time(e[1]) for e in evs]
+
+    attempts_a = []
+    with ClockSampler(local, enabled=not args.no_clocks) as clocks:
+        for attempt in range(MAX_ATTEMPTS):
+            if attempt:
+                reset_state_and_warm()
+            step_ms = region_a()
+            attempts_a.append({"p50_step_us": 1e3 * float(np.median(step_ms)),
+                               "max_step_us": 1e3 * float(np.max(step_ms))})
+            if not stalled(step_ms, ws):
+                break
     err = hs.hs_get_error(h, clear=True)
     misses = miss_acc[W_:W_ + K_].sum(dim=1).cpu().numpy()  # per timed step, all requests
     rows_timed = valid_rows * K_
@@ -557,30 +583,43 @@ def run_ours(args, ws, rank, local):
     # CTAs that is the one resolve launch. Without them hs_resolve is the resolve, the grouping
     # by host region and the pair gather; the same four kernels are issued here as
     # hs_resolve_layers(copy_layers = 0) (resolve + grouping) and hs_gather of every layer
-    # (the gather alone), so the gather's own duration is measured.
+    # (the gather alone), so the gather's own duration is measured. Stalled passes are
+    # measured again, as above.
     split = launches_per_resolve > 1
-    reset_state_and_warm()
-    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K_)]
-    torch.cuda._sleep(int(2e6 * (5 + K_ // 4)))
-    for i in range(K_):
-        s = W_ + i
-        forward_stand_in(s)
-        flush.zero_()
-        evb[i][0].record(stream)
-        if split:
-            hs.hs_resolve_layers(h, R, tk_buf, sl_buf, hcl, dbl, tok, st, clk, rp, out, miss, 0, stream)
-            evb[i][1].record(stream)
-            hs.hs_gather(h, R, hcl, 0, L, stream)
-        else:
-            resolve(stream)
-            evb[i][1].record(stream)
-        evb[i][2].record(stream)
-        backup(stream)
-        evb[i][3].record(stream)
-        miss_acc[s].copy_(miss)
-    torch.cuda.synchronize()
-    if not np.array_equal(miss_acc[W_:W_ + K_].sum(dim=1).cpu().numpy(), misses):
-        raise RuntimeError("pass B resolved different miss counts from the timed pass")
+
+    def pass_b():
+        reset_state_and_warm()
+        evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K_)]
+        torch.cuda._sleep(int(2e6 * (5 + K_ // 4)))
+        for i in range(K_):
+            s = W_ + i
+            forward_stand_in(s)
+            flush.zero_()
+            evb[i][0].record(stream)
+            if split:
+                hs.hs_resolve_layers(h, R, tk_buf, sl_buf, hcl, dbl, tok, st, clk, rp, out, miss, 0, stream)
+                evb[i][1].record(stream)
+                hs.hs_gather(h, R, hcl, 0, L, stream)
+            else:
+                resolve(stream)
+                evb[i][1].record(stream)
+            evb[i][2].record(stream)
+            backup(stream)
+            evb[i][3].record(stream)
+            miss_acc[s].copy_(miss)
+        torch.cuda.synchronize()
+        if not np.array_equal(miss_acc[W_:W_ + K_].sum(dim=1).cpu().numpy(), misses):
+            raise RuntimeError("pass B resolved different miss counts from the timed pass")
+        return evb
+
+    attempts_b = []
+    for attempt in range(MAX_ATTEMPTS):
+        evb = pass_b()
+        dom_try = [e[1 if split else 0].elapsed_time(e[2]) for e in evb]
+        attempts_b.append({"p50_dominant_us": 1e3 * float(np.median(dom_try)),
+                           "max_dominant_us": 1e3 * float(np.max(dom_try))})
+        if not stalled(dom_try, ws):
+            break
     res_ms = [e[0].elapsed_time(e[2]) for e in evb]     # the whole hs_resolve work
     dom_ms = [e[1 if split else 0].elapsed_time(e[2]) for e in evb]  # the dominant kernel alone
     bak_ms = [e[2].elapsed_time(e[3]) for e in evb]
@@ -682,6 +721,10 @@ def run_ours(args, ws, rank, local):
         "p50_dominant_kernel_us": 1e3 * float(np.median(dom_ms)),
         "resolve_timing": "eager launches, CUDA events around the resolve work alone (without copy CTAs: "
                           "hs_resolve_layers(0) + hs_gather of every layer, the same four kernels as hs_resolve)",
+        "timed_attempts": attempts_a,
+        "dominant_kernel_attempts": attempts_b,
+        "attempt_rule": f"a pass with a step above {STALL_RATIO} x its median is measured again, "
+                        f"at most {MAX_ATTEMPTS} passes; the last pass is reported",
         "step_us_per_step": [round(1e3 * x, 1) for x in step_ms],
         "dominant_kernel_us_per_step": [round(1e3 * x, 1) for x in dom_ms],
         "misses_per_step": float(misses.mean()), "miss_h2d_gbs": link_gbs, "h2d_ceiling_gbs": h2d_ceiling,
@@ -1227,8 +1270,9 @@ def run_spec(args, ws, rank, local):
     """Speculative batches at the workload's shape: Q = SPEC_QUERIES verify steps per batch,
     H = (Q + 1) * top_k hot slots (the buffer the pages size for n_spec + 2), every position
     accepted. Per batch the forward stand-in writes the Q new rows, then hs_resolve_spec
-    (Q launches) and hs_backup_spec run; events bracket resolve + backup. Top-k rows keep
-    90 % of the previous verify step's row and draw the rest over the step's length."""
+    (one launch for the Q verify steps when each request has copy CTAs) and hs_backup_spec
+    run; events bracket resolve + backup. Top-k rows keep 90 % of the previous verify step's
+    row and draw the rest over the step's length."""
     import torch
     import hierarchical_sparse_attention_gb300 as hs
     import workloads as W
@@ -1317,6 +1361,10 @@ def run_spec(args, ws, rank, local):
     barrier(ws)
     ms = [e[0].elapsed_time(e[1]) for e in evs]
     err = hs.hs_get_error(h, clear=True)
+    copy_ctas, _ = hs.hs_launch_shape(h)
+    # one resolve launch per batch; without copy CTAs each step's plan is then grouped by host
+    # region (two launches) and gathered (one)
+    per_batch = 1 + (0 if copy_ctas > 0 else 3 * Q) + 1
     hs.hs_destroy(h)
     for arr, reg in pools:
         if reg:
@@ -1332,10 +1380,11 @@ def run_spec(args, ws, rank, local):
                                f"(n_spec {Q - 1}), H = (n_spec + 2) * top_k = {H} slots, {B}-byte rows, "
                                "every draft accepted",
                    "l2": "flushed between timed batches (256 MiB write)",
-                   "step": "hs_resolve_spec (Q launches) + hs_backup_spec"},
+                   "step": "hs_resolve_spec (the Q verify steps in one launch) + hs_backup_spec"},
         "p50_batch_us": 1e3 * float(np.median(ms)), "p50_per_verify_step_us": 1e3 * float(np.median(ms)) / Q,
         "misses_per_verify_step": [float(x) for x in misses],
-        "gpu_launches": K_ * (Q + 1), "device_flags": err, "clocks": clocks.summary(),
+        "gpu_launches": K_ * per_batch, "copy_ctas_per_request": copy_ctas, "device_flags": err,
+        "clocks": clocks.summary(),
         "host_pool": "huge pages, hs_host_register" if pools[0][1] else "cudaHostAlloc",
     }
     if rank == 0:

@@ -135,6 +135,7 @@ hs_status make_geometry(const hs_config* cfg, void* const* host_pools, void* con
     cudaGetLastError();
     return e == cudaErrorInvalidValue ? HS_ERR_INVALID_CONFIG : HS_ERR_CUDA;
   }
+  g.gather_ctas_per_sm = gather_pairs_ctas_per_sm(g.vec);
   *out = g;
   *pools_out = pools;
   return HS_OK;
@@ -292,19 +293,22 @@ hs_status hs_resolve_spec_layers(hs_handle* h, int32_t num_requests, int32_t num
   h->plan_requests = num_requests;
   h->spec_queries = num_queries;
   h->spec_ordered = order;
-  // The verify steps run in order on the stream over the shared state; step q records its
-  // miss plan in plan slice q.
-  for (int32_t q = 0; q < num_queries; ++q) {
-    int32_t* ptok = h->plan_tok + q * h->plan_slice;
-    int32_t* pdst = h->plan_dst + q * h->plan_slice;
-    int32_t* pcnt = h->plan_cnt + q * h->plan_slice;
-    hs::ResolveArgs a{h->hint,   top_k_tokens + q * RK, committed_lens, host_cache_locs, device_buffer_locs,
-                      device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows + q * RK,
-                      miss_counts ? miss_counts + (size_t)q * num_requests : nullptr,
-                      gather_after ? 0 : copy_layers, ptok, pdst, pcnt, q, num_queries};
-    if (hs::launch_resolve(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
-      return HS_ERR_CUDA;
-    if (order) {
+  // One launch runs the verify steps in order over the shared state (each cluster loops over
+  // its request's steps); step q records its miss plan in plan slice q.
+  hs::ResolveArgs a{h->hint,   top_k_tokens, committed_lens, host_cache_locs, device_buffer_locs,
+                    device_buffer_tokens, lru_slots, lru_clock, resident_pages, out_rows, miss_counts,
+                    gather_after ? 0 : copy_layers, h->plan_tok, h->plan_dst, h->plan_cnt, 0, num_queries};
+  a.spec_steps = num_queries;
+  a.step_r = num_requests;
+  a.step_rk = (int64_t)RK;
+  a.step_plan = (int64_t)h->plan_slice;
+  if (hs::launch_resolve(h->g, h->pools, a, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
+    return HS_ERR_CUDA;
+  // Without copy CTAs, or with follower layers left, each step's plan is then grouped by host
+  // region (and its leader rows gathered), step by step in step order: the rows a later step
+  // places in a slot an earlier step filled are the last written, as in the steps themselves.
+  if (order)
+    for (int32_t q = 0; q < num_queries; ++q) {
       const hs::OrderArgs oa = order_slice(h, q, host_cache_locs);
       if (hs::launch_order(h->g, oa, num_requests, h->err_word, (cudaStream_t)stream) != cudaSuccess)
         return HS_ERR_CUDA;
@@ -313,7 +317,6 @@ hs_status hs_resolve_spec_layers(hs_handle* h, int32_t num_requests, int32_t num
               cudaSuccess)
         return HS_ERR_CUDA;
     }
-  }
   return HS_OK;
 }
 

@@ -31,7 +31,7 @@ namespace {
 constexpr int T = kGatherThreads;
 constexpr int M = kGatherMisses;
 constexpr int kUnroll = 4;
-constexpr int kGatherCtasPerSm = 2048 / T;  // a full SM's threads
+constexpr int kGatherCtasPerSm = 2048 / T;  // a full SM's threads, when the occupancy is not known
 
 template <int V>
 struct Piece;
@@ -279,13 +279,27 @@ cudaError_t launch_order(const Geometry& g, const OrderArgs& a, int32_t num_requ
   return cudaGetLastError();
 }
 
+int gather_pairs_ctas_per_sm(int vec) {
+  int n = 0;
+  const cudaError_t e =
+      vec == 16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gather_pairs_kernel<16>, T, 0)
+      : vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gather_pairs_kernel<4>, T, 0)
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gather_pairs_kernel<1>, T, 0);
+  if (e != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    return kGatherCtasPerSm;
+  }
+  return n;
+}
+
 cudaError_t launch_gather_pairs(const Geometry& g, const Pools* pools, const OrderArgs& a, int32_t num_requests,
                                 int32_t first_layer, int32_t num_layers, cudaStream_t stream) {
   // the pair count is known only on the device: at most num_requests * K pairs, so no more
-  // CTAs than items, and no more than one wave (kGatherCtasPerSm per SM)
+  // CTAs than items, and no more than one wave (the CTAs that fit an SM at once, times the
+  // SMs): a CTA of a second wave would start its items only when one of the first finished
   const int64_t most = (int64_t)num_requests * g.K;
   const int64_t items = ((most + M - 1) / M) * (g.host_interleaved ? 1 : num_layers);
-  int64_t ctas = (int64_t)(g.sms > 0 ? g.sms : 1) * kGatherCtasPerSm;
+  int64_t ctas = (int64_t)(g.sms > 0 ? g.sms : 1) * (g.gather_ctas_per_sm > 0 ? g.gather_ctas_per_sm : kGatherCtasPerSm);
   if (ctas > items) ctas = items;
   if (ctas < 1) ctas = 1;
   const dim3 grid((unsigned)ctas);

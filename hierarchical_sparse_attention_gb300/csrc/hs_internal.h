@@ -45,6 +45,7 @@ struct Geometry {
                              // L * B ("page first"): one host row holds every layer's
                              // bytes, so a miss of layers [a, b) is one contiguous span
   int32_t sms;               // SMs of the device (grid size of the persistent pair gather)
+  int32_t gather_ctas_per_sm;  // pair-gather CTAs resident on one SM at once
   int64_t host_stride;       // bytes from one host row to the next inside a layer's pool
   int64_t host_rows, device_rows;
 };
@@ -68,6 +69,14 @@ struct ResolveArgs {
   int32_t spec_q;       // -1: a plain step (seq_lens are lengths); q >= 0: verify step q of a
                         // speculative batch (seq_lens are the batch's first positions S0)
   int32_t spec_n;       // reserved rows after the H slots (1, or the batch's Q)
+  // One launch for a whole speculative batch: spec_steps > 0 runs verify steps
+  // 0..spec_steps - 1 in order inside the kernel (spec_q is then the loop's), step q taking
+  // top_k_tokens / out_rows + q * step_rk, miss_counts + q * step_r and plan slice q (the plan
+  // pointers + q * step_plan). 0: the one step spec_q.
+  int32_t spec_steps = 0;
+  int32_t step_r = 0;
+  int64_t step_rk = 0;
+  int64_t step_plan = 0;
 };
 
 struct GatherArgs {
@@ -202,6 +211,8 @@ cudaError_t launch_gather(const Geometry& g, const Pools* pools, const GatherArg
 // region offsets), then place each miss's (host row, device row) pair in its region.
 cudaError_t launch_order(const Geometry& g, const OrderArgs& a, int32_t num_requests, uint32_t* err_word,
                          cudaStream_t stream);
+// Pair-gather CTAs that fit one SM at once, for the copy width `vec`.
+int gather_pairs_ctas_per_sm(int vec);
 // Copy the ordered pairs' rows for layers [first_layer, first_layer + num_layers).
 cudaError_t launch_gather_pairs(const Geometry& g, const Pools* pools, const OrderArgs& a, int32_t num_requests,
                                 int32_t first_layer, int32_t num_layers, cudaStream_t stream);

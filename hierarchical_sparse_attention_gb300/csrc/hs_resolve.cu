@@ -258,6 +258,29 @@ __device__ void bitonic_sort(uint64_t* keys, int n) {
   }
 }
 
+// The arguments that differ between the verify steps one launch runs (ResolveArgs.spec_steps).
+struct StepArgs {
+  int32_t spec_q;
+  const int32_t* top_k_tokens;
+  int32_t* out_rows;
+  int32_t* miss_counts;
+  int32_t* plan_tok;
+  int32_t* plan_dst;
+  int32_t* plan_cnt;
+};
+__device__ __forceinline__ StepArgs step_args(const ResolveArgs& a, int step) {
+  if (step < 0)
+    return StepArgs{a.spec_q, a.top_k_tokens, a.out_rows, a.miss_counts, a.plan_tok, a.plan_dst, a.plan_cnt};
+  const size_t q = (size_t)step;
+  return StepArgs{step,
+                  a.top_k_tokens + q * a.step_rk,
+                  a.out_rows + q * a.step_rk,
+                  a.miss_counts ? a.miss_counts + q * a.step_r : nullptr,
+                  a.plan_tok ? a.plan_tok + q * a.step_plan : nullptr,
+                  a.plan_dst ? a.plan_dst + q * a.step_plan : nullptr,
+                  a.plan_cnt ? a.plan_cnt + q * a.step_plan : nullptr};
+}
+
 // Miss rows are read once: stream them past the caches.
 __device__ __forceinline__ uint4 load_host16(const uint4* p) { return __ldcs(p); }
 
@@ -332,8 +355,8 @@ __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc
 // Exact misses store their staged row; misses that were not staged (a stale bit, no
 // room) are copied straight from host memory. A predicted miss that was a hit sets the
 // token's bit again.
-__device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a, int r, int q, unsigned char* smem,
-                         uint32_t* err_word) {
+__device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a, const StepArgs& sa, int r, int q,
+                         unsigned char* smem, uint32_t* err_word) {
   const CopyLayout cl = make_copy_layout(g);
   const int32_t* c_res = reinterpret_cast<const int32_t*>(smem + cl.res);
   int32_t* c_tk = reinterpret_cast<int32_t*>(smem + cl.tk);
@@ -347,13 +370,13 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
   const int per = copy_slice(g);
   const int e0 = (q - 1) * per;
   const int ne = max(0, min(g.K, e0 + per) - e0);
-  const int32_t S = a.spec_q < 0 ? a.seq_lens[r] : a.seq_lens[r] + a.spec_q + 1;
-  const int32_t base = a.spec_q < 0 ? S - 1 : a.seq_lens[r];  // first position new to the cache
+  const int32_t S = sa.spec_q < 0 ? a.seq_lens[r] : a.seq_lens[r] + sa.spec_q + 1;
+  const int32_t base = sa.spec_q < 0 ? S - 1 : a.seq_lens[r];  // first position new to the cache
   const bool predict = a.hint != nullptr && a.copy_layers > 0 && S > g.H && S <= g.max_context;
   uint32_t* bits_g = a.hint ? a.hint + (size_t)r * g.bit_words : nullptr;  // residency bitmap row
   const uint32_t* bits = g.bits_smem ? reinterpret_cast<const uint32_t*>(smem + cl.bits) : bits_g;
   const int32_t* hcl_row = a.host_cache_locs + (size_t)r * g.max_context;
-  const int32_t* tk_g = a.top_k_tokens + (size_t)r * g.K + e0;
+  const int32_t* tk_g = sa.top_k_tokens + (size_t)r * g.K + e0;
   const int per_row = g.B >> 4;
   const int per_miss = per_row * a.copy_layers;  // the leader layers this call copies
   uint32_t flags = 0;
@@ -493,39 +516,23 @@ __device__ __forceinline__ void flush_flags(uint32_t flags, uint32_t* err_word) 
   if ((threadIdx.x & 31) == 0 && f) atomicOr(err_word, f);
 }
 
-__global__ void __launch_bounds__(T, 1)
-    resolve_kernel(const Geometry g, const Pools* __restrict__ pools, const ResolveArgs a,
-                   uint32_t* __restrict__ err_word) {
-  // The eager backup touches only the newest token's rows, which this kernel never reads
-  // or writes: let it launch now and run beside the resolve (it orders its own exit).
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+// The cluster barrier phases a resolve CTA that leaves a step early (a skipped request, the
+// fast path) still owes its copy CTAs: they wait for phase A and then meet at phase B.
+__device__ __forceinline__ void finish_phases(int C) {
+  if (C > 0) {
+    cluster_wait();     // phase A
+    cluster_arrive();   // phase B: no outcome to publish
+    cluster_wait();
+  }
+}
 
-  extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ Pools s_pools;
+// The resolve CTA of request r for one step (phases 0-9 below). Every exit completes the
+// cluster barrier phases A and B that the copy CTAs take part in.
+__device__ __forceinline__ void resolve_cta(const Geometry& g, const Pools& s_pools, const ResolveArgs& a,
+                                            const StepArgs& sa, uint32_t* __restrict__ err_word, unsigned char* smem,
+                                            int r) {
   const int tid = threadIdx.x;
   const int C = g.copy_ctas;
-  const uint32_t rank = C > 0 ? cluster_rank() : 0u;
-  const int r = blockIdx.x / (C + 1);  // one cluster of C + 1 CTAs per request
-  if (tid < (int)(sizeof(Pools) / sizeof(uint64_t)))
-    reinterpret_cast<uint64_t*>(&s_pools)[tid] = reinterpret_cast<const uint64_t*>(pools)[tid];
-  if (C > 0) {
-    // Barrier phase A: every CTA of the cluster runs, and each copy CTA has cleared its
-    // outcome table and counters, before the resolve CTA stores into a copy CTA's shared
-    // memory. Only that first remote store waits for it (phase 4); the copy CTAs start
-    // their own work at once.
-    if (rank > 0) {
-      const CopyLayout cl0 = make_copy_layout(g);
-      int32_t* res = reinterpret_cast<int32_t*>(smem + cl0.res);
-      for (int e = tid; e < copy_slice(g); e += T) res[e] = -1;
-      if (tid < 4) reinterpret_cast<uint32_t*>(smem + cl0.cnt)[tid] = 0u;
-    }
-    cluster_arrive();
-    if (rank > 0) {
-      __syncthreads();  // the CTA's own clears before its threads read the counters
-      copy_cta(g, s_pools, a, r, (int)rank, smem, err_word);
-      return;
-    }
-  }
   const Layout lay = make_layout(g);
   uint64_t* s_keys = reinterpret_cast<uint64_t*>(smem + lay.keys);
   int32_t* s_tk = reinterpret_cast<int32_t*>(smem + lay.tk);
@@ -552,10 +559,10 @@ __global__ void __launch_bounds__(T, 1)
   // A plain step's one new position is the newest token, S - 1. Verify step q of a
   // speculative batch attends over S0 + q + 1 tokens, and the batch's positions t >= S0 (the
   // token the last round sampled, then the drafts) sit in the reserved rows H + (t - S0).
-  const int32_t S = a.spec_q < 0 ? a.seq_lens[r] : a.seq_lens[r] + a.spec_q + 1;
-  const int32_t base = a.spec_q < 0 ? S - 1 : a.seq_lens[r];
-  const int32_t* tk_g = a.top_k_tokens + (size_t)r * K;
-  int32_t* out_g = a.out_rows + (size_t)r * K;
+  const int32_t S = sa.spec_q < 0 ? a.seq_lens[r] : a.seq_lens[r] + sa.spec_q + 1;
+  const int32_t base = sa.spec_q < 0 ? S - 1 : a.seq_lens[r];
+  const int32_t* tk_g = sa.top_k_tokens + (size_t)r * K;
+  int32_t* out_g = sa.out_rows + (size_t)r * K;
   const int32_t* dbl_g = a.device_buffer_locs + (size_t)r * (H + a.spec_n);
   const int32_t* s_dbl = g.dbl_smem ? s_dbl_staged : dbl_g;  // slot -> row table
   int32_t* tok_g = a.device_buffer_tokens + (size_t)r * H;
@@ -565,10 +572,11 @@ __global__ void __launch_bounds__(T, 1)
   if (S < 0 || S > g.max_context) {
     for (int i = tid; i < K; i += T) out_g[i] = -1;
     if (tid == 0) {
-      if (a.miss_counts) a.miss_counts[r] = 0;
-      if (a.plan_cnt) a.plan_cnt[r] = 0;
+      if (sa.miss_counts) sa.miss_counts[r] = 0;
+      if (sa.plan_cnt) sa.plan_cnt[r] = 0;
       atomicOr(err_word, HS_FLAG_SEQLEN);
     }
+    finish_phases(C);
     return;
   }
   const bool fast = S <= H;
@@ -642,15 +650,15 @@ __global__ void __launch_bounds__(T, 1)
       }
       out_g[i] = o;
     }
-    if (a.spec_q < 0) {
+    if (sa.spec_q < 0) {
       if (tid == 0 && S >= 1) tok_g[S - 1] = S - 1;
     } else {  // committed positions only: S0 and the ones before it the last batch accepted
       const int32_t t = max(0, base - a.spec_n) + tid;  // spec_n + 1 <= T threads
       if (t <= base) tok_g[t] = t;
     }
     if (tid == 0) {
-      if (a.miss_counts) a.miss_counts[r] = 0;
-      if (a.plan_cnt) a.plan_cnt[r] = 0;
+      if (sa.miss_counts) sa.miss_counts[r] = 0;
+      if (sa.plan_cnt) sa.plan_cnt[r] = 0;
     }
     if (hint_row) {  // slot t holds token t for every committed t: exact once the sequence outgrows the buffer
       const int nb = min(S, base + 1);
@@ -658,6 +666,7 @@ __global__ void __launch_bounds__(T, 1)
         hint_row[w] = nb - 32 * w >= 32 ? ~0u : (1u << (nb - 32 * w)) - 1u;
     }
     flush_flags(flags, err_word);
+    finish_phases(C);
     return;
   }
 
@@ -1013,9 +1022,9 @@ __global__ void __launch_bounds__(T, 1)
       if (old_tok >= 0) atomicAnd(&hint_row[old_tok >> 5], ~(1u << (old_tok & 31)));  // evicted
       atomicOr(&hint_row[t >> 5], 1u << (t & 31));
     }
-    if (a.plan_tok) {  // the miss plan the follower layers replay: token and destination row
-      a.plan_tok[(size_t)r * K + j] = t;
-      a.plan_dst[(size_t)r * K + j] = s_out[s_miss[j]];
+    if (sa.plan_tok) {  // the miss plan the follower layers replay: token and destination row
+      sa.plan_tok[(size_t)r * K + j] = t;
+      sa.plan_dst[(size_t)r * K + j] = s_out[s_miss[j]];
     }
   }
   __syncthreads();
@@ -1029,14 +1038,80 @@ __global__ void __launch_bounds__(T, 1)
   for (int i = tid; i < K; i += T) out_g[i] = s_out[i];
   if (tid == 0) {
     a.lru_clock[r] = clock;
-    if (a.miss_counts) a.miss_counts[r] = m;
-    if (a.plan_cnt) a.plan_cnt[r] = m;
+    if (sa.miss_counts) sa.miss_counts[r] = m;
+    if (sa.plan_cnt) sa.plan_cnt[r] = m;
   }
 
   // ---- phase 9: misses no copy CTA took, the leader layers, straight from host memory
   if (s_sc[SC_DIRECT]) copy_rows(g, s_pools, s_psrc, s_pdst, m, a.copy_layers);
   flush_flags(flags, err_word);
   if (C > 0) cluster_wait();  // phase B complete; the copy CTAs finish on their own
+}
+
+// kBatch = false: one step (a plain decode step, or the one verify step a.spec_q); true: the
+// a.spec_steps verify steps of a speculative batch in order. Two instances, so the one-step
+// kernel carries no loop state.
+template <bool kBatch>
+__global__ void __launch_bounds__(T, 1)
+    resolve_kernel(const Geometry g, const Pools* __restrict__ pools, const ResolveArgs a,
+                   uint32_t* __restrict__ err_word) {
+  // The eager backup touches only the newest token's rows, which this kernel never reads
+  // or writes: let it launch now and run beside the resolve (it orders its own exit).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ Pools s_pools;
+  __shared__ StepArgs s_step;  // this step's arguments, read where they are used (no registers held)
+  const int tid = threadIdx.x;
+  const int C = g.copy_ctas;
+  const uint32_t rank = C > 0 ? cluster_rank() : 0u;
+  const int r = blockIdx.x / (C + 1);  // one cluster of C + 1 CTAs per request
+  if (tid < (int)(sizeof(Pools) / sizeof(uint64_t)))
+    reinterpret_cast<uint64_t*>(&s_pools)[tid] = reinterpret_cast<const uint64_t*>(pools)[tid];
+  // A speculative batch's verify steps run here in order, one after the other, over the
+  // request's shared slot state (each with its own top-k slice, row table, miss counts and
+  // plan slice); a plain step is one pass. The two roles loop apart, so each loop keeps only
+  // its own role's registers.
+  const int steps = kBatch ? a.spec_steps : 1;
+  if (rank > 0) {
+    for (int q = 0; q < steps; ++q) {
+      if (kBatch && q > 0) {
+        // step q - 1 is complete in every CTA of the cluster, and its writes (slot state,
+        // clock, residency bits, copied rows) are visible, before this CTA clears its tables
+        cluster_arrive();
+        cluster_wait();
+      }
+      if (tid == 0) s_step = step_args(a, kBatch ? q : -1);
+      // Barrier phase A: every CTA of the cluster runs, and each copy CTA has cleared its
+      // outcome table and counters, before the resolve CTA stores into a copy CTA's shared
+      // memory. Only that first remote store waits for it (phase 4); the copy CTAs start
+      // their own work at once.
+      const CopyLayout cl0 = make_copy_layout(g);
+      int32_t* res = reinterpret_cast<int32_t*>(smem + cl0.res);
+      for (int e = tid; e < copy_slice(g); e += T) res[e] = -1;
+      if (tid < 4) reinterpret_cast<uint32_t*>(smem + cl0.cnt)[tid] = 0u;
+      cluster_arrive();
+      __syncthreads();  // the CTA's own clears and step arguments before its threads read them
+      copy_cta(g, s_pools, a, s_step, r, (int)rank, smem, err_word);
+    }
+    return;
+  }
+  for (int q = 0; q < steps; ++q) {
+    if (kBatch && q > 0) {
+      // step q - 1 is complete everywhere before step q reads the state (a CTA barrier when the
+      // request has no copy CTAs)
+      if (C > 0) {
+        cluster_arrive();
+        cluster_wait();
+      } else {
+        __syncthreads();
+      }
+    }
+    if (tid == 0) s_step = step_args(a, kBatch ? q : -1);
+    __syncthreads();  // the step arguments (and the pools table) before any thread reads them
+    if (C > 0) cluster_arrive();  // phase A
+    resolve_cta(g, s_pools, a, s_step, err_word, smem, r);
+  }
 }
 
 }  // namespace
@@ -1059,7 +1134,7 @@ cudaError_t resolve_prepare(Geometry& g, int32_t max_requests) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaFuncAttributes fa{};
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, resolve_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, resolve_kernel<false>);
   if (e != cudaSuccess) return e;
   const int max_dynamic = optin - (int)fa.sharedSizeBytes;
   g.sms = sms;
@@ -1084,7 +1159,15 @@ cudaError_t resolve_prepare(Geometry& g, int32_t max_requests) {
     }
   }
   if (!fits) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic);
+  cudaFuncAttributes fb{};
+  e = cudaFuncGetAttributes(&fb, resolve_kernel<true>);
+  if (e != cudaSuccess) return e;
+  if (fb.sharedSizeBytes > fa.sharedSizeBytes && make_layout(g).total > (size_t)(optin - (int)fb.sharedSizeBytes))
+    return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(resolve_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(resolve_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fb.sharedSizeBytes);
   if (e != cudaSuccess) return e;
 
   int C = max_requests > 0 ? sms / max_requests - 1 : 0;
@@ -1115,7 +1198,7 @@ cudaError_t resolve_prepare(Geometry& g, int32_t max_requests) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int clusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&clusters, resolve_kernel, &cfg) == cudaSuccess && clusters > 0) {
+      if (cudaOccupancyMaxActiveClusters(&clusters, resolve_kernel<false>, &cfg) == cudaSuccess && clusters > 0) {
         g.copy_ctas = C;
         g.copy_cap = t.copy_cap;
         g.bits_smem = t.bits_smem;
@@ -1142,7 +1225,8 @@ cudaError_t launch_resolve(const Geometry& g, const Pools* pools, const ResolveA
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = g.copy_ctas > 0 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, resolve_kernel, g, pools, a, err_word);
+  if (a.spec_steps > 0) return cudaLaunchKernelEx(&cfg, resolve_kernel<true>, g, pools, a, err_word);
+  return cudaLaunchKernelEx(&cfg, resolve_kernel<false>, g, pools, a, err_word);
 }
 
 }  // namespace hs

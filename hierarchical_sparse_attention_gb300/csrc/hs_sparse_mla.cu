@@ -12,30 +12,29 @@
 //   o[h]    = softmax_j(s[h]) . latent,   lse[h] = log sum_j exp s[h, j]
 // (MLA decode with the absorbed projection: keys are the 576-dim rows, values their latent.)
 //
-// Layout of the work: a CTA of 512 threads takes (request r, quarter u of the 512 value dims,
-// split p of the rows) and runs a three-role pipeline over blocks of 64 rows:
-//   - producers (warps 5-15) gather each block's 656-B records through the row table (staged
-//     in shared memory) straight into registers, 32 rows at a time with the next 32 rows'
-//     loads in flight, 16-byte loads of 16 latent codes (plus their block's scale) or of 8
-//     RoPE dims each; they dequantise the latent to bf16 (e4m3 -> f16 in hardware, times the
-//     scale), copy the RoPE part, and fill one of three swizzled K-major tiles (72 KB each);
-//   - one issuer warp (warp 4) runs S = Q . K^T for a block as soon as its tile is full and the
-//     softmax has read the previous S (36 MMAs of M 128, N 64, K 16, with Q as the A operand in
-//     tensor memory), and O += P . V for the previous block once its probabilities are in (four
-//     MMAs of N 128, P as the A operand in tensor memory);
-//   - the softmax warpgroup (warps 0-3, one head per thread, tensor-memory lane = head) reads
-//     S into registers, runs the online softmax and writes P as bf16 pairs into tensor memory.
-// Tensor memory (512 columns): Q (128 heads x 576 bf16, 288 columns), S (128 x 64 fp32), P
-// (128 x 64 bf16, 32 columns) and O (128 x 128 fp32). Q in tensor memory leaves shared memory
-// to the tiles; the cost is that the four quarter-CTAs of a request each compute S. A
-// tcgen05.mma costs about the same up to N 64 (issue-bound), so 64-row blocks halve that cost
-// per row. O is rescaled only when a head's block maximum passes its reference maximum by
-// more than 2^8 (a lazy rescale: P is computed against the reference and stays below 2^8).
-// The roles hand blocks over through mbarriers: tile full (producers -> issuer and softmax),
-// S full (issuer -> softmax), S read (softmax -> issuer), P full (softmax -> issuer), P . V done
-// (issuer -> producers, which may then refill that tile, and softmax, before it rewrites P or
-// rescales O). Every wait is bounded. With more than one split a small kernel merges the
-// splits by their log-sum-exp.
+// Layout of the work. A thread-block cluster of two CTAs takes (request r, split p of the
+// rows) and walks the split in blocks of 64 rows:
+//   - the S-CTA (cluster rank 0) holds Q (128 heads x 576, in f16) in tensor memory and computes
+//     S = Q . K^T of each block (36 MMAs of M 128, N 64, K 16) into one of two S buffers; its
+//     two softmax warpgroups (each 32 of the block's rows, one head per thread) run the
+//     online softmax and write P as f16 straight into the O-CTA's shared memory (distributed
+//     shared memory), with each head's rescale factor;
+//   - the O-CTA (rank 1) holds O (128 heads x 512 fp32, all of its tensor memory) and adds
+//     P . V of each block (8 MMAs of N 256, P read from shared memory); its corrector
+//     warpgroup rescales O in the rare blocks that raise a head's reference maximum, and at the
+//     end every warp reads O out, normalised by the S-CTA's row sums.
+// So S is computed once per row and O once per value dim: no CTA repeats another's product.
+// In each CTA a loader warp brings each half-block's 32 records into a ring of shared-memory
+// buffers with one bulk asynchronous copy per record (mbarrier completion; the S-CTA the whole
+// 656 B, the O-CTA the 528 B of latent codes and scales), through the split's row table staged
+// in shared memory once, and
+// dequantisation warps turn them into the CTA's own f16 tile (the S-CTA all 576 dims as K,
+// the O-CTA the 512 latent dims as V: e4m3 -> f16 in hardware, times the row's scale in f16;
+// the bf16 RoPE dims rounded to f16), swizzled K-major, two tiles in flight. The roles hand blocks over through mbarriers
+// (the two CTAs' through mbarriers in the partner's shared memory); every wait is bounded and
+// an abort flag makes the other roles stop. O is rescaled only when a head's block maximum
+// passes its reference maximum by more than 2^8 (a lazy rescale: P stays below 2^8). With
+// more than one split a small kernel merges the splits by their log-sum-exp.
 #include "hs_internal.h"
 
 #include <cuda_bf16.h>
@@ -44,42 +43,53 @@
 namespace hs {
 namespace {
 
-constexpr int T = 512;           // threads: four warpgroups
-constexpr int WG = T / 128;      // warpgroups sharing the tensor-memory lanes (by column) at readout
+constexpr int T = 512;           // threads per CTA
 constexpr int MH = 128;          // MMA M: heads (padded with zero rows)
 constexpr int BJ = 64;           // rows per block (MMA N of S, K of P . V)
-constexpr int HB = 32;           // rows a producer pass fills (a block is two passes)
+constexpr int HB = 32;           // rows per half-block (one loader step, one ring buffer)
 constexpr int DQK = 576, DL = 512, ROWB = 656;
-constexpr int ATOMS = DQK / 64;  // 9 swizzle atoms of 64 bf16 along the 576 dims
-constexpr int NQ = 4;            // CTAs per (request, split): each takes a quarter of the value dims
-constexpr int HALF = DL / NQ;    // value dims per CTA (128)
-constexpr int ISSUER_WARP = 4;   // warp 4 issues the MMAs; warps 0-3 run the softmax
-constexpr int PROD0 = 160;       // first producer thread (warps 5-15)
-constexpr int NPROD = T - PROD0;
-constexpr int ITEMS_ROW = DL / 16 + (DQK - DL) / 8;     // per row: 32 latent items of 16 dims, 8 RoPE of 8
-constexpr int CHUNKS = HB * ITEMS_ROW;                 // producer items per pass
-constexpr int PER_PROD = (CHUNKS + NPROD - 1) / NPROD;  // items per producer thread
-constexpr int NT = 3;            // tiles in flight
-constexpr int ROWS_CAP = 2048;   // a split's row-table entries staged in shared memory
+constexpr int KATOMS = DQK / 64;  // swizzle atoms of 64 f16 in a K tile (9) and a V tile (8)
+constexpr int VATOMS = DL / 64;
+constexpr int NT = 2;            // K / V tiles in flight
+constexpr int NR = 3;            // raw half-block buffers in flight
+constexpr int MAX_HALVES = 2 * (HS_MAX_TOP_K / BJ);
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t Q_COL = 0;    // Q, the A operand of S = Q . K^T: 288 columns of bf16 pairs
-constexpr uint32_t S_COL = 288;  // S of the current block, 64 columns (one buffer)
-constexpr uint32_t P_COL = 352;  // P of the current block (bf16 pairs), 32 columns (one buffer)
-constexpr uint32_t O_COL = 384;  // O, 128 x 128 fp32
+// S-CTA tensor memory: Q (the A operand of S, f16 pairs) and two S buffers
+constexpr uint32_t Q_COL = 0, S_COL = 288;
+// S-CTA warps: 0-7 softmax (two warpgroups), 8 issuer, 9 loader, 10-15 dequantisation
+constexpr int S_ISSUER = 8, S_DEQ0 = 288, S_NDEQ = T - S_DEQ0;
+// O-CTA warps: 0-3 corrector, 4 issuer, 5 loader, 6-15 dequantisation
+constexpr int O_ISSUER = 4, O_DEQ0 = 160, O_NDEQ = T - O_DEQ0;
 
-// shared memory carve-up (offsets from a 1024-B aligned base)
-constexpr uint32_t SKV = 0;                              // NT tiles of 9 atoms x 32 rows x 128 B
-constexpr uint32_t KV_TILE = ATOMS * BJ * 128;
-constexpr uint32_t SVALID = SKV + NT * KV_TILE;          // NT x 32 int (row valid, per tile)
-constexpr uint32_t SROWS = SVALID + NT * BJ * 4;         // the split's rows of the row table
+// shared memory carve-up (offsets from a 1024-B aligned base); the two roles use different parts
+constexpr uint32_t KV_ATOM = BJ * 128;                 // one swizzle atom of a tile: 64 rows x 128 B
+constexpr uint32_t K_TILE = KATOMS * KV_ATOM, V_TILE = VATOMS * KV_ATOM;
+constexpr int OREC = DL + 16;                           // what the O-CTA reads of a record: latent, scales
+constexpr uint32_t RAW_HALF = HB * ROWB;               // S-CTA: 32 whole records
+constexpr uint32_t ORAW_HALF = HB * OREC;              // O-CTA: 32 records' latent and scales
+constexpr uint32_t S_TILES = 0;                         // S-CTA: NT K tiles
+constexpr uint32_t S_RAW = S_TILES + NT * K_TILE;       //        NR raw buffers
+constexpr uint32_t S_MX = S_RAW + NR * RAW_HALF;        //        block maxima of the two warpgroups
+constexpr uint32_t S_L1 = S_MX + 2 * MH * 4;            //        warpgroup 1's row sums at the end
+constexpr uint32_t S_END = S_L1 + MH * 4;
+constexpr uint32_t O_TILES = 0;                         // O-CTA: NT V tiles
+constexpr uint32_t O_RAW = O_TILES + NT * V_TILE;       //        NR raw buffers
+constexpr uint32_t O_P = (O_RAW + NR * ORAW_HALF + 1023u) & ~1023u;  // two P buffers, 128 x 64 f16
+constexpr uint32_t P_BUF = MH * BJ * 2;
+constexpr uint32_t O_ALPHA = O_P + 2 * P_BUF;           //        two blocks' rescale factors
+constexpr uint32_t P_BYTES = P_BUF + MH * 4;            // what the S-CTA sends per block
+constexpr uint32_t O_FIN = O_ALPHA + 2 * MH * 4;        //        the S-CTA's final l and m per head
+constexpr uint32_t O_END = O_FIN + 2 * MH * 4;
+constexpr int ROWS_CAP = 2048;                          // a split's row-table entries staged in shared memory
+constexpr uint32_t SROWS = (S_END > O_END ? S_END : O_END);  // both: the split's rows of the row table
 constexpr uint32_t SMEM_USED = SROWS + ROWS_CAP * 4;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;        // + alignment slack
-constexpr uint64_t kWaitNs = 100000000ull;               // 100 ms bound on an mbarrier wait
-constexpr float kRescaleLog2 = 8.f;                      // reference-maximum slack (log2 units)
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
+constexpr uint64_t kWaitNs = 100000000ull;              // 100 ms bound on an mbarrier wait
+constexpr float kRescaleLog2 = 8.f;                     // reference-maximum slack (log2 units)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-// Byte offset of (row, k) in a K-major tile whose rows are 128 B (64 bf16), swizzled in
+// Byte offset of (row, k) in a K-major tile whose rows are 128 B (64 f16), swizzled in
 // 8-row groups of 1024 B: the 16-B chunk index is XOR-ed with row % 8.
 __device__ __forceinline__ uint32_t sw128(int row, int k) {
   return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((((k * 2) >> 4) ^ (row & 7)) << 4) + ((k * 2) & 15));
@@ -90,14 +100,13 @@ __device__ __forceinline__ uint64_t mdesc(uint32_t saddr, uint32_t lbo, uint32_t
   return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major, B K- or
+// Instruction descriptor, kind::f16: fp32 accumulator, f16 A and B, A K-major, B K- or
 // MN-major, N and M.
 __host__ __device__ constexpr uint32_t idesc(int n, int m, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(m >> 4) << 24);
+  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
-constexpr uint32_t kIdescS = idesc(BJ, MH, false);   // S = Q . K^T
-constexpr uint32_t kIdescO = idesc(HALF, MH, true);  // O += P . V (V read MN-major)
+constexpr uint32_t kIdescS = idesc(BJ, MH, false);  // S = Q . K^T
+constexpr uint32_t kIdescO = idesc(256, MH, true);  // O[:, n0:n0+256] += P . V (V read MN-major)
 
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -135,43 +144,61 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// OR of a predicate over warpgroup 0's 128 threads (named barrier 1, so warpgroup 1 is not
-// held up).
-__device__ __forceinline__ int __syncthreads_or_wg0(bool pred) {
+// OR / AND of a predicate over the first n threads of the CTA (named barrier 1; n a multiple of 32).
+// Named barrier 1 serves the softmax / corrector warpgroups, 2 the dequantisation warps.
+template <int id = 1>
+__device__ __forceinline__ int sync_or(bool pred, int n) {
   int r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %3, %2, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)pred)
+      : "r"((uint32_t)pred), "r"(n), "n"(id)
       : "memory");
   return r;
 }
-
-// AND of a predicate over warpgroup 0's 128 threads (named barrier 1).
-__device__ __forceinline__ int __syncthreads_and_wg0(bool pred) {
+template <int id = 1>
+__device__ __forceinline__ int sync_and(bool pred, int n) {
   int r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %3, %2, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)pred)
+      : "r"((uint32_t)pred), "r"(n), "n"(id)
       : "memory");
   return r;
 }
+template <int id = 1>
+__device__ __forceinline__ void sync_n(int n) {
+  asm volatile("bar.sync %1, %0;" ::"r"(n), "n"(id) : "memory");
+}
 
-// Two e4m3 codes (low byte first) to two floats, exactly (e4m3 is a subset of f16).
-__device__ __forceinline__ float2 e4m3x2(uint16_t codes) {
+// Two e4m3 codes (low byte first) to an f16 pair, exactly (e4m3 is a subset of f16), times the
+// row's scale in f16.
+__device__ __forceinline__ uint32_t to_f16x2(uint16_t codes, __half2 sc) {
   uint32_t h2;
   asm("{\n\t.reg .b16 c;\n\tmov.b16 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "h"(codes));
-  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h2), sc);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// A bf16 pair (low half first) to an f16 pair, rounded to nearest.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// MMA with A in tensor memory (Q of S, P of P . V): lane m = row m, column c = A[m][2c],
-// A[m][2c + 1].
+// MMA with A in tensor memory (Q of S): lane m = row m, column c = A[m][2c], A[m][2c + 1].
 __device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+// MMA with A and B in shared memory (P of P . V, and V).
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(acc)
       : "memory");
 }
 __device__ __forceinline__ void bar_init(uint64_t* bar, uint32_t count) {
@@ -180,19 +207,78 @@ __device__ __forceinline__ void bar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void bar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+__device__ __forceinline__ void bar_arrive_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// The partner CTA's copy of a shared-memory address (distributed shared memory).
+__device__ __forceinline__ uint32_t remote(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void bar_arrive_remote(uint32_t raddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
+}
+__device__ __forceinline__ void st_remote_f32(uint32_t raddr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(raddr), "f"(v) : "memory");
+}
+// 16 bytes global -> shared, asynchronously (cached in L2 only).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// An arrival on the mbarrier once every cp.async this thread issued before has landed (the
+// arrival counts against the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Asynchronous stores into the partner CTA's shared memory that complete their bytes on the
+// partner's mbarrier (no fence or arrival of the storing thread needed).
+__device__ __forceinline__ void st_async16(uint32_t raddr, uint4 v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   raddr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t raddr, float v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr),
+               "r"(__float_as_uint(v)), "r"(rbar)
+               : "memory");
+}
+// Arrive on the mbarrier at this shared-memory offset in the cluster CTAs of `mask` once the
+// MMAs issued so far are done.
+__device__ __forceinline__ void commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                   "r"(smem_u32(bar)),
+               "h"(mask)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // Bounded wait for the completion of use k of a ring of `depth` barriers (barrier k % depth,
 // parity of k / depth); false when the bound ran out or another role gave up (abort set).
+// cluster: the barrier is arrived on from the partner CTA (acquire at cluster scope).
+template <bool cluster = false>
 __device__ __forceinline__ bool pipe_wait(uint64_t* ring, int depth, int k, volatile int* abort) {
   uint64_t* bar = ring + (k % depth);
   const uint32_t parity = (uint32_t)(k / depth) & 1u;
   const uint64_t t0 = gtime();
   for (;;) {
     uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
+    if (cluster)
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(done)
+          : "r"(smem_u32(bar)), "r"(parity)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(done)
+          : "r"(smem_u32(bar)), "r"(parity)
+          : "memory");
     if (done) return true;
     if (*abort || gtime() - t0 > kWaitNs) {
       *abort = 1;
@@ -201,34 +287,104 @@ __device__ __forceinline__ bool pipe_wait(uint64_t* ring, int depth, int k, vola
   }
 }
 
-// A producer's items of one pass: item c = (thread - PROD0) + i * NPROD covers row
-// c / ITEMS_ROW; item it = c % ITEMS_ROW < 32 is latent dims [16 it, 16 it + 16) (16 codes in
-// one load, and the scale of their 128-dim block), else RoPE dims [512 + 8 j, +8), j = it - 32.
-// rows: this pass's entries of the row table (shared memory); n: how many are real.
-__device__ __forceinline__ uint32_t load_raw(const SparseMlaArgs& a, int pt, const int32_t* rows, int n,
-                                             uint4 (&raw)[PER_PROD], float (&scl)[PER_PROD]) {
-  uint32_t valid = 0;  // bit i: item i's row is a pool row
-#pragma unroll
-  for (int i = 0; i < PER_PROD; ++i) {
-    const int c = pt + i * NPROD;
-    const int row = c / ITEMS_ROW, it = c - row * ITEMS_ROW;
-    const int32_t pr = c < CHUNKS && row < n ? rows[row] : -1;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    float sc = 0.f;
-    if (pr >= 0 && (int64_t)pr < a.pool_rows) {
-      valid |= 1u << i;
-      const uint8_t* rec = a.kv_pool + (size_t)pr * ROWB;
-      if (it < DL / 16) {
-        v = __ldg(reinterpret_cast<const uint4*>(rec) + it);
-        sc = __ldg(reinterpret_cast<const float*>(rec + DL) + (it >> 3));
-      } else {
-        v = __ldg(reinterpret_cast<const uint4*>(rec + DL + 16) + (it - DL / 16));
+struct Barriers {
+  uint64_t raw_full[NR];                // a ring buffer's records have landed
+  uint64_t tile_full[NT], tile_free[NT];  // dequantisation -> issuer; the tile's MMAs done
+  uint64_t q_full;                      // S-CTA: Q in tensor memory
+  uint64_t s_full[2], s_free[2];        // S-CTA: S written by the MMAs; read by the softmax
+  uint64_t p_free[2];                   // S-CTA, arrived by the O-CTA: P buffer free again
+  uint64_t p_full[2];                   // O-CTA, arrived by the S-CTA: P and the factors written
+  uint64_t pv_go[2];                    // O-CTA: O rescaled (if needed); P . V may go
+  uint64_t fin;                         // O-CTA, arrived by the S-CTA: final l and m written
+};
+
+// Items run row-fastest: the 32 lanes of a warp take one item of 32 consecutive rows, so their
+// 16-B tile stores land in distinct bank groups (the swizzle spreads 8 rows over a 128-B line)
+// and their record reads are 656 (or 528) B apart.
+template <bool with_rope>
+__device__ __forceinline__ void dequant_half(const SparseMlaArgs& a, const int32_t* __restrict__ rows, int n_rows,
+                                             const uint8_t* __restrict__ raw, uint8_t* __restrict__ tile, int k,
+                                             int t, int nthreads) {
+  constexpr int ITEMS_ROW = with_rope ? DL / 16 + (DQK - DL) / 8 : DL / 16;
+  constexpr int ITEMS = HB * ITEMS_ROW;
+  constexpr int REC = with_rope ? ROWB : OREC;
+#pragma unroll 2
+  for (int c = t; c < ITEMS; c += nthreads) {
+    const int hr = c % HB, it = c / HB;
+    const int row = (k & 1) * HB + hr;
+    const int j = HB * k + hr;
+    const int32_t pr = j < n_rows ? rows[j] : -1;
+    const bool valid = pr >= 0 && (int64_t)pr < a.pool_rows;
+    const uint8_t* rec = raw + hr * REC;
+    if (it < DL / 16) {
+      const int d = 16 * it;
+      uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+      if (valid) {
+        const uint4 v = *reinterpret_cast<const uint4*>(rec + d);
+        const __half2 sc = __float2half2_rn(*reinterpret_cast<const float*>(rec + DL + 4 * (it >> 3)));
+        o0 = make_uint4(to_f16x2((uint16_t)(v.x & 0xFFFFu), sc), to_f16x2((uint16_t)(v.x >> 16), sc),
+                        to_f16x2((uint16_t)(v.y & 0xFFFFu), sc), to_f16x2((uint16_t)(v.y >> 16), sc));
+        o1 = make_uint4(to_f16x2((uint16_t)(v.z & 0xFFFFu), sc), to_f16x2((uint16_t)(v.z >> 16), sc),
+                        to_f16x2((uint16_t)(v.w & 0xFFFFu), sc), to_f16x2((uint16_t)(v.w >> 16), sc));
       }
+      *reinterpret_cast<uint4*>(tile + (d >> 6) * KV_ATOM + sw128(row, d & 63)) = o0;
+      *reinterpret_cast<uint4*>(tile + ((d + 8) >> 6) * KV_ATOM + sw128(row, (d + 8) & 63)) = o1;
+    } else {
+      const int d = DL + 8 * (it - DL / 16);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (valid) {
+        const uint4 w = *reinterpret_cast<const uint4*>(rec + DL + 16 + 2 * (d - DL));
+        v = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+      }
+      *reinterpret_cast<uint4*>(tile + (d >> 6) * KV_ATOM + sw128(row, d & 63)) = v;
     }
-    raw[i] = v;
-    scl[i] = sc;
   }
-  return valid;
+}
+
+// Whether row j of the split is a pool row.
+__device__ __forceinline__ bool row_valid(const SparseMlaArgs& a, const int32_t* rows, int n_rows, int j) {
+  const int32_t pr = j < n_rows ? rows[j] : -1;
+  return pr >= 0 && (int64_t)pr < a.pool_rows;
+}
+
+// The dequantisation warps' loop over half-blocks (both roles). They also load the records:
+// the first NR half-blocks up front, then half-block k + NR into ring buffer k % NR as soon as
+// all of them have finished dequantising half-block k, with 16-byte asynchronous copies of
+// each valid record's first rec_bytes bytes, spread over the group; each thread's arrival on
+// raw_full fires once its copies have landed. Every exit is taken by the whole group (named
+// barrier 2). The tile is freed by the MMAs that read it.
+template <bool with_rope>
+__device__ __forceinline__ void run_dequant(const SparseMlaArgs& a, const int32_t* rows, int n_rows, int nblk,
+                                            uint8_t* raw, uint8_t* tiles, uint32_t tile_bytes, Barriers& bs, int t,
+                                            int nthreads, volatile int* abort) {
+  constexpr int REC = with_rope ? ROWB : OREC;
+  constexpr int CH = REC / 16;
+  constexpr uint32_t RAWH = with_rope ? RAW_HALF : ORAW_HALF;
+  const auto issue = [&](int k) {
+    uint8_t* dst = raw + (k % NR) * RAWH;
+    for (int c = t; c < HB * CH; c += nthreads) {
+      const int rec = c / CH, q = c - rec * CH;
+      const int j = HB * k + rec;
+      const int32_t pr = j < n_rows ? rows[j] : -1;
+      if (pr >= 0 && (int64_t)pr < a.pool_rows)
+        cp_async16(dst + rec * REC + 16 * q, a.kv_pool + (size_t)pr * ROWB + 16 * q);
+    }
+    cp_async_arrive(&bs.raw_full[k % NR]);
+  };
+  const int halves = 2 * nblk;
+  for (int k = 0; k < NR && k < halves; ++k) issue(k);
+  for (int k = 0; k < halves; ++k) {
+    const int b = k >> 1;
+    bool ok = true;
+    if ((k & 1) == 0 && b >= NT) ok = pipe_wait(bs.tile_free, NT, b - NT, abort);
+    ok = ok && pipe_wait(bs.raw_full, NR, k, abort);
+    if (!sync_and<2>(ok, nthreads)) break;
+    dequant_half<with_rope>(a, rows, n_rows, raw + (k % NR) * RAWH, tiles + (b % NT) * tile_bytes, k, t, nthreads);
+    fence_async_smem();  // the tile's generic writes before the tensor core reads it
+    if (k & 1) bar_arrive(&bs.tile_full[b % NT]);
+    sync_n<2>(nthreads);  // every thread is done with ring buffer k % NR
+    if (k + NR < halves) issue(k + NR);
+  }
 }
 
 __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a, float* __restrict__ part_o,
@@ -236,29 +392,39 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint32_t s_taddr;
-  // barrier rings: tile full and P . V done per tile (b % NT), S full and P full per buffer
-  // (b & 1), Q in tensor memory
-  __shared__ __align__(8) uint64_t s_tile_full[NT], s_o_done[NT], s_s_full, s_s_free, s_p_full, s_q_full;
+  __shared__ __align__(8) Barriers bs;
   __shared__ int s_abort;
+  __shared__ int s_issued;  // blocks whose MMAs the issuer started (the last commit to wait for)
   volatile int* abort = &s_abort;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = tid >> 7;
-  const int head = tid & (MH - 1);  // this thread's tensor-memory lane
-  const int r = blockIdx.x, u = blockIdx.y, p = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int r = blockIdx.x >> 1, p = blockIdx.y;
   const int per = (a.top_k + a.splits - 1) / a.splits;
   const int j_begin = p * per, j_end = min(a.top_k, j_begin + per);
   const int nblk = j_end > j_begin ? (j_end - j_begin + BJ - 1) / BJ : 0;
 
   if (tid == 0) {
+    for (int k = 0; k < NR; ++k) bar_init(&bs.raw_full[k], rank == 0 ? S_NDEQ : O_NDEQ);  // every loader's copies
     for (int k = 0; k < NT; ++k) {
-      bar_init(&s_tile_full[k], NPROD);
-      bar_init(&s_o_done[k], 1);
+      bar_init(&bs.tile_full[k], rank == 0 ? S_NDEQ : O_NDEQ);
+      bar_init(&bs.tile_free[k], 1);
     }
-    bar_init(&s_s_full, 1);
-    bar_init(&s_s_free, MH);
-    bar_init(&s_p_full, MH);
-    bar_init(&s_q_full, MH);
+    bar_init(&bs.q_full, 8);  // one arrival per warp of the two softmax warpgroups
+    for (int k = 0; k < 2; ++k) {
+      bar_init(&bs.s_full[k], 1);
+      bar_init(&bs.s_free[k], 8);
+      bar_init(&bs.p_free[k], 1);
+      bar_init(&bs.p_full[k], 1);  // the O-CTA's expect_tx; the S-CTA's st.async bytes complete it
+      bar_init(&bs.pv_go[k], 4);  // one per corrector warp
+    }
+    bar_init(&bs.fin, 4);
     s_abort = 0;
+    s_issued = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // O-CTA: the bytes blocks 0 and 1 will bring (P and the rescale factors)
+    if (rank == 1)
+      for (int k = 0; k < 2 && k < nblk; ++k) bar_arrive_tx(&bs.p_full[k], P_BYTES);
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_taddr)),
@@ -269,247 +435,258 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   tc_before();
   __syncthreads();
   tc_after();
+  // The split's part of the row table, once, into shared memory (a split longer than ROWS_CAP
+  // rows is read from the row table in global memory).
+  const int n_rows = j_end - j_begin;
+  const int32_t* g_rows = a.out_rows + (size_t)r * a.top_k + j_begin;
+  int32_t* s_rows = reinterpret_cast<int32_t*>(base + SROWS);
+  const bool staged = n_rows <= ROWS_CAP;
+  if (staged)
+    for (int i = tid; i < n_rows; i += T) s_rows[i] = __ldg(g_rows + i);
+  const int32_t* rows = staged ? s_rows : g_rows;
+  // Both CTAs' barriers are initialised (and the rows staged) before either arrives on the other's.
+  __syncthreads();
+  cluster_sync_all();
   const uint32_t tbase = s_taddr;
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's tensor-memory lanes
-  float m_run = -INFINITY, l_run = 0.f;
-  if (wg == 0) {
-    // Q of request r into tensor memory, one head per lane (zero past the last head): the A
-    // operand of S = Q . K^T, column c holding dims 2c and 2c + 1
-    const int h = tid;
-    const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)r * a.num_heads + h) * DQK);
-    for (int c0 = 0; c0 < DQK / 2; c0 += 16) {
-      float v[16];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 w = h < a.num_heads ? __ldg(src + (c0 * 2) / 8 + k) : make_uint4(0u, 0u, 0u, 0u);
-        v[4 * k] = __uint_as_float(w.x);
-        v[4 * k + 1] = __uint_as_float(w.y);
-        v[4 * k + 2] = __uint_as_float(w.z);
-        v[4 * k + 3] = __uint_as_float(w.w);
-      }
-      tmem_st16(tbase + lane_off + Q_COL + c0, v);
-    }
-    tc_before();
-    bar_arrive(&s_q_full);
-  }
+  const int head = (warp & 3) * 32 + lane;                        // = its tensor-memory lane
 
-  if (tid >= PROD0) {
-    // ---- producers: gather and dequantise block b into tile b % NT once P . V of block b - NT
-    // has read it, 32 rows per pass; the next pass's records load while this one is stored
-    const int pt = tid - PROD0;
-    // the split's part of the row table, once, so each block's record loads wait on nothing else
-    // (a split of more than ROWS_CAP rows reads them from the row table in global memory)
-    const int32_t* g_rows = a.out_rows + (size_t)r * a.top_k + j_begin;
-    int32_t* s_rows = reinterpret_cast<int32_t*>(base + SROWS);
-    const bool staged = j_end - j_begin <= ROWS_CAP;
-    if (staged)
-      for (int i = pt; i < j_end - j_begin; i += NPROD) s_rows[i] = __ldg(g_rows + i);
-    asm volatile("bar.sync 2, %0;" ::"n"(NPROD) : "memory");  // producers only
-    const int32_t* rows_src = staged ? s_rows : g_rows;
-    // pass k fills rows [32 (k & 1), 32 (k & 1) + 32) of block k / 2
-    const auto pass_rows = [&](int k) { return rows_src + k * HB; };
-    const auto pass_n = [&](int k) { return min(HB, j_end - j_begin - k * HB); };
-    uint4 raw[PER_PROD];
-    float scl[PER_PROD];
-    uint32_t vmask = 0;
-    if (nblk > 0) vmask = load_raw(a, pt, pass_rows(0), pass_n(0), raw, scl);
-    const auto to_bf16 = [](uint32_t codes2x2, float sc) {  // four codes to two bf16 pairs
-      const float2 v0 = e4m3x2((uint16_t)(codes2x2 & 0xFFFFu)), v1 = e4m3x2((uint16_t)(codes2x2 >> 16));
-      __nv_bfloat162 b0 = __floats2bfloat162_rn(v0.x * sc, v0.y * sc), b1 = __floats2bfloat162_rn(v1.x * sc, v1.y * sc);
-      return make_uint2(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1));
-    };
-    // dequantise this thread's items of rows [32 half, 32 half + 32) of a block into its tile
-    const auto fill = [&](uint8_t* tile, int half) {
+  if (rank == 0) {
+    // ================================ S-CTA ================================
+    uint8_t* tiles = base + S_TILES;
+    uint8_t* raw = base + S_RAW;
+    if (warp < 8) {
+      // ---- softmax: warpgroup wg takes rows [32 wg, 32 wg + 32) of each block, one head per
+      // thread; first, Q of request r into tensor memory (warpgroup wg the columns
+      // [144 wg, 144 wg + 144)), the A operand of S = Q . K^T, column c holding dims 2c, 2c + 1
+      const int wg = warp >> 2;
+      {
+        // 72 columns (144 dims, 288 B) at a time: every load of a round is in flight together
+        const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)r * a.num_heads + head) * DQK);
+        const bool live = head < a.num_heads;
+#pragma unroll 1
+        for (int c0 = wg * 144; c0 < wg * 144 + 144; c0 += 72) {
+          uint4 w[18];
 #pragma unroll
-      for (int i = 0; i < PER_PROD; ++i) {
-        const int c = pt + i * NPROD;
-        if (c >= CHUNKS) continue;
-        const int hrow = c / ITEMS_ROW, it = c - hrow * ITEMS_ROW;
-        const int row = half * HB + hrow;
-        const uint4 v = raw[i];
-        if (it < DL / 16) {
-          const int d = 16 * it;
-          const uint2 p0 = to_bf16(v.x, scl[i]), p1 = to_bf16(v.y, scl[i]);
-          const uint2 p2 = to_bf16(v.z, scl[i]), p3 = to_bf16(v.w, scl[i]);
-          *reinterpret_cast<uint4*>(tile + (d >> 6) * (BJ * 128) + sw128(row, d & 63)) = make_uint4(p0.x, p0.y, p1.x, p1.y);
-          *reinterpret_cast<uint4*>(tile + ((d + 8) >> 6) * (BJ * 128) + sw128(row, (d + 8) & 63)) =
-              make_uint4(p2.x, p2.y, p3.x, p3.y);
-        } else {
-          const int d = DL + 8 * (it - DL / 16);
-          *reinterpret_cast<uint4*>(tile + (d >> 6) * (BJ * 128) + sw128(row, d & 63)) = v;
-        }
-      }
-    };
-    const int npass = (j_end - j_begin + HB - 1) / HB;
-    for (int b = 0; b < nblk; ++b) {
-      if (b >= NT && !pipe_wait(s_o_done, NT, b - NT, abort)) break;
-      uint8_t* tile = base + SKV + (b % NT) * KV_TILE;
-      int32_t* valid = reinterpret_cast<int32_t*>(base + SVALID) + (b % NT) * BJ;
-      for (int half = 0; half < 2; ++half) {
-        const int k = 2 * b + half;
-        fill(tile, half);
-        // a row's validity, from the thread that holds its first item
+          for (int k = 0; k < 18; ++k) w[k] = live ? __ldg(src + (c0 * 2) / 8 + k) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int i = 0; i < PER_PROD; ++i) {
-          const int c = pt + i * NPROD;
-          if (c < CHUNKS && c % ITEMS_ROW == 0) valid[half * HB + c / ITEMS_ROW] = (int32_t)((vmask >> i) & 1u);
+          for (int c = 0; c < 72; c += 8) {
+            uint4 x = w[c / 4], y = w[c / 4 + 1];
+            x = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+            y = make_uint4(bf16x2_to_f16x2(y.x), bf16x2_to_f16x2(y.y), bf16x2_to_f16x2(y.z), bf16x2_to_f16x2(y.w));
+            asm volatile(
+                "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(tbase + lane_off + Q_COL +
+                                                                                             c0 + c),
+                "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w), "r"(y.x), "r"(y.y), "r"(y.z), "r"(y.w)
+                : "memory");
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        if (k + 1 < npass) vmask = load_raw(a, pt, pass_rows(k + 1), pass_n(k + 1), raw, scl);
-        else vmask = load_raw(a, pt, pass_rows(k + 1), 0, raw, scl);  // past the end: zero rows
+        tc_before();
+        __syncwarp();
+        if (lane == 0) bar_arrive(&bs.q_full);
       }
-      fence_async_smem();
-      bar_arrive(&s_tile_full[b % NT]);
-    }
-  } else if (warp == ISSUER_WARP) {
-    // ---- issuer: S of block b as soon as its tile is full (Q from tensor memory), then
-    // P . V of block b - 1
-    const bool q_in = __all_sync(0xffffffffu, nblk == 0 || pipe_wait(&s_q_full, 1, 0, abort));
-    for (int b = 0; q_in && b <= nblk; ++b) {
-      if (b < nblk) {
-        bool go = pipe_wait(s_tile_full, NT, b, abort);
-        go = go && (b == 0 || pipe_wait(&s_s_free, 1, b - 1, abort));  // the softmax holds S of b - 1
-        if (!__all_sync(0xffffffffu, go)) break;  // the warp leaves together
+      float* s_mx = reinterpret_cast<float*>(base + S_MX);
+      const uint32_t r_pbuf = remote(base + O_P, 1), r_alpha = remote(base + O_ALPHA, 1);
+      const float sl2 = a.sm_scale * 1.4426950408889634f;  // scores in log2 units
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int b = 0; b < nblk; ++b) {
+        // this warpgroup's rows' validity from the row table (lane i: row 32 wg + i), loaded
+        // before the wait so its latency hides behind it
+        const int j = BJ * b + HB * wg + lane;
+        const int32_t pr = j < n_rows ? rows[j] : -1;
+        const uint32_t vm = __ballot_sync(0xffffffffu, pr >= 0 && (int64_t)pr < a.pool_rows);
+        // every exit is taken by both warpgroups together (they meet at named barrier 1)
+        if (!sync_and(pipe_wait(bs.s_full, 2, b, abort), 2 * MH)) break;
+        tc_after();
+        float s[HB];
+#pragma unroll
+        for (int q = 0; q < HB / 16; ++q) {
+          float t[16];
+          tmem_ld16(tbase + lane_off + S_COL + BJ * (b & 1) + HB * wg + 16 * q, t);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) s[16 * q + i] = ((vm >> (16 * q + i)) & 1u) ? t[i] * sl2 : -INFINITY;
+        }
+        tc_before();
+        __syncwarp();
+        if (lane == 0) bar_arrive(&bs.s_free[b & 1]);  // S is in registers: the MMAs of block b + 2 may overwrite it
+        float bm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < HB; ++i) bm = fmaxf(bm, s[i]);
+        s_mx[wg * MH + head] = bm;
+        sync_n(2 * MH);
+        bm = fmaxf(s_mx[head], s_mx[MH + head]);
+        // Lazy rescale: a head keeps its reference maximum until the block's maximum exceeds it
+        // by more than kRescaleLog2, so P stays below 2^kRescaleLog2 (well inside f16's range)
+        // and O is rescaled only on those rare jumps.
+        const float m_new = bm > m_run + kRescaleLog2 || m_run == -INFINITY ? fmaxf(m_run, bm) : m_run;
+        const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);  // m_run = -inf: O is still 0
+        // the O-CTA's P buffer b & 1 is free once its P . V of block b - 2 is done
+        if (!sync_and(b < 2 || pipe_wait<true>(bs.p_free, 2, b - 2, abort), 2 * MH)) break;
+        float psum = 0.f;
+        const uint32_t pbuf = r_pbuf + (b & 1) * P_BUF;
+        const uint32_t rbar = remote(&bs.p_full[b & 1], 1);
+#pragma unroll
+        for (int c = 0; c < HB / 8; ++c) {  // four 16-B chunks of 8 f16: rows 32 wg + 8c ..
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float p0 = m_new == -INFINITY ? 0.f : exp2f(s[8 * c + 2 * i] - m_new);
+            const float p1 = m_new == -INFINITY ? 0.f : exp2f(s[8 * c + 2 * i + 1] - m_new);
+            const __half2 pb = __floats2half2_rn(p0, p1);
+            psum += __low2float(pb) + __high2float(pb);  // the normaliser sums what P . V uses
+            w[i] = *reinterpret_cast<const uint32_t*>(&pb);
+          }
+          st_async16(pbuf + sw128(head, HB * wg + 8 * c), make_uint4(w[0], w[1], w[2], w[3]), rbar);
+        }
+        if (wg == 0) st_async_f32(r_alpha + 4 * ((b & 1) * MH + head), alpha, rbar);
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+      }
+      // the row sums of both warpgroups, and the reference maxima, to the O-CTA
+      float* s_l1 = reinterpret_cast<float*>(base + S_L1);
+      if (wg == 1) s_l1[head] = l_run;
+      sync_n(2 * MH);
+      if (wg == 0) {
+        const uint32_t fin = remote(base + O_FIN, 1);
+        st_remote_f32(fin + 4 * head, l_run + s_l1[head]);
+        st_remote_f32(fin + 4 * (MH + head), m_run);
+        __syncwarp();
+        if (lane == 0) bar_arrive_remote(remote(&bs.fin, 1));
+      }
+    } else if (warp == S_ISSUER) {
+      // ---- issuer: S of block b once its tile is full and the softmax has read S of b - 2
+      bool go = __all_sync(0xffffffffu, nblk == 0 || pipe_wait(&bs.q_full, 1, 0, abort));
+      for (int b = 0; go && b < nblk; ++b) {
+        bool ok = pipe_wait(bs.tile_full, NT, b, abort);
+        ok = ok && (b < 2 || pipe_wait(bs.s_free, 2, b - 2, abort));
+        if (!__all_sync(0xffffffffu, ok)) break;
         tc_after();
         if (lane == 0) {
-          const uint64_t dkv0 = mdesc(smem_u32(base + SKV + (b % NT) * KV_TILE), 16, 1024);
+          const uint64_t dk0 = mdesc(smem_u32(tiles + (b % NT) * K_TILE), 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < ATOMS * 4; ++kk) {
+          for (int kk = 0; kk < KATOMS * 4; ++kk) {
             const int at = kk >> 2, w = kk & 3;
-            mma_ta(tbase + S_COL, tbase + Q_COL + 8 * kk, dkv0 + (uint64_t)((at * (BJ * 128) + w * 32) >> 4), kIdescS,
-                   kk > 0);
+            mma_ta(tbase + S_COL + BJ * (b & 1), tbase + Q_COL + 8 * kk,
+                   dk0 + (uint64_t)((at * KV_ATOM + w * 32) >> 4), kIdescS, kk > 0);
           }
-          commit(&s_s_full);
+          commit(&bs.s_full[b & 1]);
+          commit(&bs.tile_free[b % NT]);
+          s_issued = b + 1;
         }
         __syncwarp();
       }
-      if (b >= 1) {
-        const int pb = b - 1;
-        if (!__all_sync(0xffffffffu, pipe_wait(&s_p_full, 1, pb, abort))) break;
+    } else if (warp > S_ISSUER) {
+      run_dequant<true>(a, rows, n_rows, nblk, raw, tiles, K_TILE, bs, tid - S_DEQ0, S_NDEQ, abort);
+    }
+  } else {
+    // ================================ O-CTA ================================
+    uint8_t* tiles = base + O_TILES;
+    uint8_t* raw = base + O_RAW;
+    const float* alpha_buf = reinterpret_cast<const float*>(base + O_ALPHA);
+    if (warp < 4) {
+      // ---- corrector: block b's P and factors are in; if a head's reference maximum rose,
+      // rescale O once P . V of block b - 1 is done; then P . V of block b may go
+      for (int b = 0; b < nblk; ++b) {
+        if (!sync_and(pipe_wait<true>(bs.p_full, 2, b, abort), MH)) break;
+        const float f = alpha_buf[(b & 1) * MH + head];
+        // this buffer's next phase is block b + 2: its bytes come only after P . V of block b
+        if (tid == 0 && b + 2 < nblk) bar_arrive_tx(&bs.p_full[b & 1], P_BYTES);
+        if (sync_or(b > 0 && f != 1.f, MH)) {
+          if (!sync_and(pipe_wait(bs.tile_free, NT, b - 1, abort), MH)) break;
+          tc_after();
+          for (int c = 0; c < DL; c += 16) {
+            float v[16];
+            tmem_ld16(tbase + lane_off + c, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] *= f;
+            tmem_st16(tbase + lane_off + c, v);
+          }
+          tc_before();
+        }
+        __syncwarp();
+        if (lane == 0) bar_arrive(&bs.pv_go[b & 1]);
+      }
+    } else if (warp == O_ISSUER) {
+      // ---- issuer: O += P . V of block b once its tile is full and O is ready for it; then
+      // the P buffer of block b - 1 goes back to the S-CTA when its MMAs are done
+      for (int b = 0; b < nblk; ++b) {
+        bool ok = pipe_wait(bs.tile_full, NT, b, abort);
+        ok = ok && pipe_wait(bs.pv_go, 2, b, abort);
+        if (!__all_sync(0xffffffffu, ok)) break;
         tc_after();
+        fence_async_smem();
         if (lane == 0) {
-          const uint64_t dv0 =
-              mdesc(smem_u32(base + SKV + (pb % NT) * KV_TILE + (u * (HALF / 64)) * (BJ * 128)), BJ * 128, 1024);
+          const uint64_t dp0 = mdesc(smem_u32(base + O_P + (b & 1) * P_BUF), 16, 1024);
+          const uint64_t dv0 = mdesc(smem_u32(tiles + (b % NT) * V_TILE), KV_ATOM, 1024);
 #pragma unroll
           for (int kk = 0; kk < BJ / 16; ++kk)
-            mma_ta(tbase + O_COL, tbase + P_COL + 8 * kk, dv0 + (uint64_t)((kk * 2048) >> 4), kIdescO,
-                   (pb > 0 || kk > 0) ? 1u : 0u);
-          commit(&s_o_done[pb % NT]);
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh)
+              mma_ss(tbase + 256 * nh, dp0 + (uint64_t)((kk * 32) >> 4),
+                     dv0 + (uint64_t)((nh * 4 * KV_ATOM + kk * 2048) >> 4), kIdescO, (b > 0 || kk > 0) ? 1u : 0u);
+          commit(&bs.tile_free[b % NT]);
+          commit_multicast(&bs.p_free[b & 1], 1);  // the S-CTA's P buffer b & 1 is free once these are done
+          s_issued = b + 1;
         }
         __syncwarp();
       }
-    }
-  } else if (wg == 0) {
-    // ---- softmax: warpgroup 0, one head per thread
-    const float sl2 = a.sm_scale * 1.4426950408889634f;  // scores in log2 units
-    for (int b = 0; b < nblk; ++b) {
-      // every exit is taken by the whole warpgroup (it meets at named barrier 1 below)
-      bool got = pipe_wait(s_tile_full, NT, b, abort);
-      got = got && pipe_wait(&s_s_full, 1, b, abort);
-      if (!__syncthreads_and_wg0(got)) break;
-      tc_after();
-      float s[BJ];
-      {
-        const int32_t* valid = reinterpret_cast<const int32_t*>(base + SVALID) + (b % NT) * BJ;
-#pragma unroll
-        for (int q = 0; q < BJ / 16; ++q) {
-          float t[16];
-          tmem_ld16(tbase + lane_off + S_COL + 16 * q, t);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) s[16 * q + j] = valid[16 * q + j] ? t[j] * sl2 : -INFINITY;
-        }
-      }
-      tc_before();
-      bar_arrive(&s_s_free);  // S is in registers: the next block's S may overwrite it
-      float bm = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < BJ; ++j) bm = fmaxf(bm, s[j]);
-      // Lazy rescale: a head keeps its reference maximum until the block's maximum exceeds it
-      // by more than kRescaleLog2, so P stays below 2^kRescaleLog2 (exact in bf16 and fp32) and
-      // O in tensor memory is rescaled only on those rare jumps.
-      const float m_new = bm > m_run + kRescaleLog2 || m_run == -INFINITY ? fmaxf(m_run, bm) : m_run;
-      const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);  // m_run = -inf: O is still 0
-      // P . V of block b - 1 must be done before P is rewritten (one buffer) and before O is
-      // scaled
-      if (!__syncthreads_and_wg0(b == 0 || pipe_wait(s_o_done, NT, b - 1, abort))) break;
-      tc_after();
-      if (__syncthreads_or_wg0(b > 0 && alpha != 1.f)) {
-        for (int c = 0; c < HALF; c += 16) {
-          float v[16];
-          tmem_ld16(tbase + lane_off + O_COL + c, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] *= alpha;
-          tmem_st16(tbase + lane_off + O_COL + c, v);
-        }
-      }
-      float psum = 0.f;
-#pragma unroll
-      for (int q = 0; q < BJ / 32; ++q) {
-        float pk[16];  // bf16 pairs, bit-cast, for 16 tensor-memory columns of P
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float p0 = m_new == -INFINITY ? 0.f : exp2f(s[32 * q + j] - m_new);
-          const float p1 = m_new == -INFINITY ? 0.f : exp2f(s[32 * q + j + 1] - m_new);
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          psum += __low2float(pb) + __high2float(pb);  // the normaliser sums what P . V uses
-          pk[j >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&pb));
-        }
-        tmem_st16(tbase + lane_off + P_COL + 16 * q, pk);
-      }
-      l_run = l_run * alpha + psum;
-      m_run = m_new;
-      tc_before();
-      bar_arrive(&s_p_full);
+    } else if (warp > O_ISSUER) {
+      run_dequant<false>(a, rows, n_rows, nblk, raw, tiles, V_TILE, bs, tid - O_DEQ0, O_NDEQ, abort);
     }
   }
-  // every role is done issuing; wait for the last P . V, then read O out
+
+  __syncthreads();
   bool ok = !*abort;
-  if (ok && nblk > 0 && !pipe_wait(s_o_done, NT, nblk - 1, abort)) ok = false;
+  if (rank == 1) {
+    // every block's P . V is done and the S-CTA's totals are in: read O out
+    ok = ok && (nblk == 0 || pipe_wait(bs.tile_free, NT, nblk - 1, abort));
+    ok = ok && pipe_wait<true>(&bs.fin, 1, 0, abort);
+  }
   ok = __syncthreads_and(ok && !*abort);
   tc_after();
-  if (!ok) {  // outputs are not valid: flag it and leave them alone
-    if (tid == 0) atomicOr(err, HS_FLAG_TIMEOUT);
-    // give any MMA still in flight one more bound before the tensor memory is released
-    s_abort = 0;
-    if (nblk > 0) pipe_wait(s_o_done, NT, nblk - 1, abort);
-    tc_before();
-    __syncthreads();
-    if (warp == 0)
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS) : "memory");
-    return;
-  }
-  // write this split's normalised output and log-sum-exp: warpgroup 0 holds each head's l and
-  // m (handed over through the first tile, unused now); every warpgroup reads a quarter of the
-  // columns of its lanes
-  float* s_l = reinterpret_cast<float*>(base + SKV);
-  float* s_m = s_l + MH;
-  if (wg == 0) {
-    s_l[tid] = l_run;
-    s_m[tid] = m_run;
-  }
-  __syncthreads();
-  l_run = s_l[head];
-  m_run = s_m[head];
-  const bool live = head < a.num_heads;
-  const size_t row_out = (((size_t)p * gridDim.x + r) * a.num_heads + head);  // [split][r][h]
-  const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-  for (int c = wg * (HALF / WG); c < (wg + 1) * (HALF / WG); c += 16) {
-    float v[16];
-    if (nblk > 0) {
-      tmem_ld16(tbase + lane_off + O_COL + c, v);
-    } else {
-      for (int i = 0; i < 16; ++i) v[i] = 0.f;
-    }
-    if (live) {
-      float* dst = part_o + row_out * DL + u * HALF + c;
+  if (rank == 1 && ok) {
+    const float* fin = reinterpret_cast<const float*>(base + O_FIN);
+    const float l = fin[head], m = fin[MH + head];
+    const bool live = head < a.num_heads;
+    const size_t row_out = (((size_t)p * (gridDim.x >> 1) + r) * a.num_heads + head);  // [split][r][h]
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const int c0 = (warp >> 2) * (DL / 4);  // warp w reads a quarter of the columns of its lanes
+    for (int c = c0; c < c0 + DL / 4; c += 16) {
+      float v[16];
+      if (nblk > 0) {
+        tmem_ld16(tbase + lane_off + c, v);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      }
+      if (live) {
+        float* dst = part_o + row_out * DL + c;
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(dst + i) = make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
+      }
+    }
+    if (live && warp < 4) part_lse[row_out] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+  }
+  if (!ok) {
+    // outputs are not valid: flag it, and give any MMA still in flight one more bound before
+    // the tensor memory is released
+    if (tid == 0) atomicOr(err, HS_FLAG_TIMEOUT);
+    __syncthreads();
+    if (tid == 0) s_abort = 0;
+    __syncthreads();
+    const int n = s_issued;
+    if (n > 0) {
+      if (rank == 0) pipe_wait(bs.s_full, 2, n - 1, abort);
+      pipe_wait(bs.tile_free, NT, n - 1, abort);
     }
   }
-  if (live && u == 0 && wg == 0)
-    part_lse[row_out] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
   tc_before();
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS) : "memory");
+  // the partner no longer reads or arrives on this CTA's shared memory
+  cluster_sync_all();
 }
 
 // Merge the splits of each (request, head): weights exp(lse_p - lse), lse = log sum exp lse_p.
@@ -544,9 +721,19 @@ cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, floa
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const bool direct = a.splits == 1;
-  sparse_mla_kernel<<<dim3(num_requests, NQ, a.splits), T, SMEM_BYTES, stream>>>(
-      a, direct ? a.o : part_o, direct ? a.lse : part_lse, err);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2u * (unsigned)num_requests, (unsigned)a.splits);  // a CTA pair per (request, split)
+  cfg.blockDim = dim3(T);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, a, direct ? a.o : part_o, direct ? a.lse : part_lse, err);
   if (e != cudaSuccess || direct) return e;
   combine_kernel<<<num_requests * a.num_heads, T, 0, stream>>>(a, part_o, part_lse);
   return cudaGetLastError();

@@ -256,8 +256,9 @@ HS_API hs_status hs_resolve_layers(hs_handle* h, int32_t num_requests, const int
  * plan rows and the request's shared hot state; "vLLM Hybrid HiSparse source
  * implementation analysis", 7.4 and 7.1: one resolve per verify step, a buffer of
  * (n_spec + 2) x top_k rows). num_queries = Q = n_spec + 1 (1..HS_MAX_SPEC_QUERIES) verify
- * steps run in order, one kernel launch each (four without copy CTAs, as for
- * hs_resolve): step q resolves top_k_tokens[q] for
+ * steps run in order in one kernel launch, each request's cluster looping over its steps
+ * (without copy CTAs the launch is followed, step by step, by the grouping of the step's plan
+ * by host region and its gather, as in hs_resolve): step q resolves top_k_tokens[q] for
  * committed_lens[r] + q + 1 tokens into out_rows[q] and miss_counts[q]. The batch's
  * positions t >= S0 = committed_lens[r] (the token the last round sampled, then the drafts;
  * the forward pass has written them) resolve to the reserved rows H + (t - S0): with Q
@@ -369,9 +370,11 @@ HS_API hs_status hs_invalidate_host_rows(hs_handle* h, int32_t num_requests, con
  * over the rows j = out_rows[r][i] >= 0:
  *   s[h, j] = sm_scale * (q[h, :512] . latent_j + q[h, 512:] . rope_j), latent = e4m3 x scale
  *   o[r, h] = softmax_j(s[h]) . latent,  lse[r, h] = log sum_j exp s[h, j]  (-inf, o = 0 if none)
- * Computed on the tensor cores in bf16 (latent and P rounded to bf16) with fp32 accumulation
- * and an online softmax; `splits` (1..HS_MAX_MLA_SPLITS) divides each request's rows over more
- * CTAs, merged by log-sum-exp in a second kernel.
+ * Computed on the tensor cores in fp16 with fp32 accumulation and an online softmax: q and the
+ * RoPE values are converted from bf16 to fp16, each latent code times its scale is rounded to
+ * fp16, and so is P. The inputs must therefore stay within fp16's range (|value| < 65504;
+ * values under 2^-14 lose precision). `splits` (1..HS_MAX_MLA_SPLITS) divides each request's
+ * rows over more CTA pairs, merged by log-sum-exp in a second kernel.
  *   q        [R, num_heads, 576] bf16 bits, device, 16-byte aligned (num_heads <= 128)
  *   kv_pool  [pool_rows, 656] bytes, device (a layer's device pool), 16-byte aligned
  *   out_rows [R, top_k] device (hs_resolve's output), top_k <= HS_MAX_TOP_K; rows outside
