@@ -18,19 +18,23 @@
 //     S = Q . K^T of each block (36 MMAs of M 128, N 64, K 16) into one of two S buffers; its
 //     two softmax warpgroups (each 32 of the block's rows, one head per thread) run the
 //     online softmax and write P as f16 straight into the O-CTA's shared memory (distributed
-//     shared memory), with each head's rescale factor;
+//     shared memory, asynchronous stores that complete on the O-CTA's mbarrier), with each
+//     head's rescale factor;
 //   - the O-CTA (rank 1) holds O (128 heads x 512 fp32, all of its tensor memory) and adds
 //     P . V of each block (8 MMAs of N 256, P read from shared memory); its corrector
 //     warpgroup rescales O in the rare blocks that raise a head's reference maximum, and at the
 //     end every warp reads O out, normalised by the S-CTA's row sums.
 // So S is computed once per row and O once per value dim: no CTA repeats another's product.
-// In each CTA a loader warp brings each half-block's 32 records into a ring of shared-memory
-// buffers with one bulk asynchronous copy per record (mbarrier completion; the S-CTA the whole
-// 656 B, the O-CTA the 528 B of latent codes and scales), through the split's row table staged
-// in shared memory once, and
-// dequantisation warps turn them into the CTA's own f16 tile (the S-CTA all 576 dims as K,
-// the O-CTA the 512 latent dims as V: e4m3 -> f16 in hardware, times the row's scale in f16;
-// the bf16 RoPE dims rounded to f16), swizzled K-major, two tiles in flight. The roles hand blocks over through mbarriers
+// In each CTA a loader warp brings the half-blocks of 32 records into a ring of shared-memory
+// buffers (16-byte asynchronous copies, mbarrier completion; the S-CTA whole 656-B records,
+// the O-CTA their 528 B of latent codes and scales) through the split's row table
+// staged in shared memory once, and dequantisation warps turn them into the CTA's own f16
+// tile (the S-CTA all 576 dims as K, the O-CTA the 512 latent dims as V: e4m3 -> f16 in
+// hardware, times the row's scale in f16; bf16 RoPE rounded to f16), swizzled K-major, two
+// tiles in flight. The pair exchanges only P: shared memory between two CTAs moves ~41 GB/s
+// per direction, well below what each SM reads from L2. Q is staged in shared memory with
+// coalesced copies (over the K tiles, before the first block) and moved into tensor memory
+// from there. The roles hand blocks over through mbarriers
 // (the two CTAs' through mbarriers in the partner's shared memory); every wait is bounded and
 // an abort flag makes the other roles stop. O is rescaled only when a head's block maximum
 // passes its reference maximum by more than 2^8 (a lazy rescale: P stays below 2^8). With
@@ -52,29 +56,35 @@ constexpr int KATOMS = DQK / 64;  // swizzle atoms of 64 f16 in a K tile (9) and
 constexpr int VATOMS = DL / 64;
 constexpr int NT = 2;            // K / V tiles in flight
 constexpr int NR = 3;            // raw half-block buffers in flight
-constexpr int MAX_HALVES = 2 * (HS_MAX_TOP_K / BJ);
 constexpr uint32_t TMEM_COLS = 512;
 // S-CTA tensor memory: Q (the A operand of S, f16 pairs) and two S buffers
 constexpr uint32_t Q_COL = 0, S_COL = 288;
+// Each CTA loads and dequantises what its own operand needs: the S-CTA whole records (656 B,
+// K = all 576 dims), the O-CTA their latent codes and scales (528 B, V = the 512 latent dims).
+// Shared memory between the CTAs moves only ~41 GB/s per direction, far below what the two
+// SMs read from L2, so the pair exchanges P and nothing else.
+constexpr int S_REC = ROWB, O_REC = DL + 16;          // bytes of a record in the raw buffers
+constexpr int S_CH = S_REC / 16, O_CH = O_REC / 16;   // their 16-B chunks
+constexpr int S_ITEMS = DL / 16 + (DQK - DL) / 8;     // dequantisation items per row: 16 codes or 8 RoPE dims
+constexpr int O_ITEMS = DL / 16;
 // S-CTA warps: 0-7 softmax (two warpgroups), 8 issuer, 9 loader, 10-15 dequantisation
-constexpr int S_ISSUER = 8, S_DEQ0 = 288, S_NDEQ = T - S_DEQ0;
+constexpr int S_ISSUER = 8, S_LOADER = 9, S_DEQW0 = 10, S_NDEQW = T / 32 - S_DEQW0;
 // O-CTA warps: 0-3 corrector, 4 issuer, 5 loader, 6-15 dequantisation
-constexpr int O_ISSUER = 4, O_DEQ0 = 160, O_NDEQ = T - O_DEQ0;
+constexpr int O_ISSUER = 4, O_LOADER = 5, O_DEQW0 = 6, O_NDEQW = T / 32 - O_DEQW0;
 
 // shared memory carve-up (offsets from a 1024-B aligned base); the two roles use different parts
 constexpr uint32_t KV_ATOM = BJ * 128;                 // one swizzle atom of a tile: 64 rows x 128 B
 constexpr uint32_t K_TILE = KATOMS * KV_ATOM, V_TILE = VATOMS * KV_ATOM;
-constexpr int OREC = DL + 16;                           // what the O-CTA reads of a record: latent, scales
-constexpr uint32_t RAW_HALF = HB * ROWB;               // S-CTA: 32 whole records
-constexpr uint32_t ORAW_HALF = HB * OREC;              // O-CTA: 32 records' latent and scales
+constexpr int QPITCH = DQK * 2 + 16;                   // a head's staged Q row (padded: conflict-free reads)
 constexpr uint32_t S_TILES = 0;                         // S-CTA: NT K tiles
-constexpr uint32_t S_RAW = S_TILES + NT * K_TILE;       //        NR raw buffers
-constexpr uint32_t S_MX = S_RAW + NR * RAW_HALF;        //        block maxima of the two warpgroups
+constexpr uint32_t S_QSTAGE = 0;                        //        Q staged over them before the first block
+constexpr uint32_t S_RAW = MH * QPITCH;                 //        NR raw buffers
+constexpr uint32_t S_MX = S_RAW + NR * HB * S_REC;      //        block maxima of the two warpgroups
 constexpr uint32_t S_L1 = S_MX + 2 * MH * 4;            //        warpgroup 1's row sums at the end
 constexpr uint32_t S_END = S_L1 + MH * 4;
 constexpr uint32_t O_TILES = 0;                         // O-CTA: NT V tiles
 constexpr uint32_t O_RAW = O_TILES + NT * V_TILE;       //        NR raw buffers
-constexpr uint32_t O_P = (O_RAW + NR * ORAW_HALF + 1023u) & ~1023u;  // two P buffers, 128 x 64 f16
+constexpr uint32_t O_P = (O_RAW + NR * HB * O_REC + 1023u) & ~1023u;  // two P buffers, 128 x 64 f16
 constexpr uint32_t P_BUF = MH * BJ * 2;
 constexpr uint32_t O_ALPHA = O_P + 2 * P_BUF;           //        two blocks' rescale factors
 constexpr uint32_t P_BYTES = P_BUF + MH * 4;            // what the S-CTA sends per block
@@ -85,7 +95,11 @@ constexpr uint32_t SROWS = (S_END > O_END ? S_END : O_END);  // both: the split'
 constexpr uint32_t SMEM_USED = SROWS + ROWS_CAP * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
 constexpr uint64_t kWaitNs = 100000000ull;              // 100 ms bound on an mbarrier wait
+constexpr uint32_t kSuspendNs = 20000;                  // a waiting thread sleeps up to this long per try
+                                                        // (it wakes when the phase completes), so waiting
+                                                        // warps leave the issue slots to the working ones
 constexpr float kRescaleLog2 = 8.f;                     // reference-maximum slack (log2 units)
+static_assert(S_RAW >= NT * K_TILE, "the staged Q covers the K tiles only");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -268,16 +282,16 @@ __device__ __forceinline__ bool pipe_wait(uint64_t* ring, int depth, int k, vola
     uint32_t done;
     if (cluster)
       asm volatile(
-          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
           "selp.u32 %0, 1, 0, p;\n\t}"
           : "=r"(done)
-          : "r"(smem_u32(bar)), "r"(parity)
+          : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
           : "memory");
     else
       asm volatile(
-          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
           : "=r"(done)
-          : "r"(smem_u32(bar)), "r"(parity)
+          : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
           : "memory");
     if (done) return true;
     if (*abort || gtime() - t0 > kWaitNs) {
@@ -288,102 +302,119 @@ __device__ __forceinline__ bool pipe_wait(uint64_t* ring, int depth, int k, vola
 }
 
 struct Barriers {
-  uint64_t raw_full[NR];                // a ring buffer's records have landed
-  uint64_t tile_full[NT], tile_free[NT];  // dequantisation -> issuer; the tile's MMAs done
-  uint64_t q_full;                      // S-CTA: Q in tensor memory
+  uint64_t raw_full[NR];                // loader -> dequantisation: a ring buffer's records have landed
+  uint64_t raw_free[NR];                // every dequantisation warp is done with a ring buffer
+  uint64_t tile_full[NT];               // dequantisation -> issuer: the tile is written
+  uint64_t tile_free[NT];               // the MMAs that read the tile are done
+  uint64_t q_full;                      // S-CTA: Q in tensor memory (its staging area is free)
   uint64_t s_full[2], s_free[2];        // S-CTA: S written by the MMAs; read by the softmax
   uint64_t p_free[2];                   // S-CTA, arrived by the O-CTA: P buffer free again
   uint64_t p_full[2];                   // O-CTA, arrived by the S-CTA: P and the factors written
   uint64_t pv_go[2];                    // O-CTA: O rescaled (if needed); P . V may go
+  uint64_t mma_done;                    // O-CTA: the MMAs it issued so far are done
   uint64_t fin;                         // O-CTA, arrived by the S-CTA: final l and m written
 };
 
-// Items run row-fastest: the 32 lanes of a warp take one item of 32 consecutive rows, so their
-// 16-B tile stores land in distinct bank groups (the swizzle spreads 8 rows over a 128-B line)
-// and their record reads are 656 (or 528) B apart.
-template <bool with_rope>
-__device__ __forceinline__ void dequant_half(const SparseMlaArgs& a, const int32_t* __restrict__ rows, int n_rows,
-                                             const uint8_t* __restrict__ raw, uint8_t* __restrict__ tile, int k,
-                                             int t, int nthreads) {
-  constexpr int ITEMS_ROW = with_rope ? DL / 16 + (DQK - DL) / 8 : DL / 16;
-  constexpr int ITEMS = HB * ITEMS_ROW;
-  constexpr int REC = with_rope ? ROWB : OREC;
-#pragma unroll 2
-  for (int c = t; c < ITEMS; c += nthreads) {
-    const int hr = c % HB, it = c / HB;
-    const int row = (k & 1) * HB + hr;
-    const int j = HB * k + hr;
+// The loader warp: half-block k's records into ring buffer k % NR once every dequantisation
+// warp is done with half-block k - NR, as 16-byte asynchronous copies (lane l takes chunks
+// l, l + 32, ... of the 32 records, so a warp's copies read whole records in order); each
+// lane's arrival on raw_full fires once its copies have landed. The S-CTA copies whole records,
+// the O-CTA their first DL + 16 bytes (latent codes, scales).
+template <bool kS>
+__device__ __forceinline__ void run_loader(const SparseMlaArgs& a, const int32_t* rows, int n_rows, int nblk,
+                                           uint8_t* raw, Barriers& bs, int lane, volatile int* abort) {
+  constexpr int CH = kS ? S_CH : O_CH;
+  constexpr int REC = kS ? S_REC : O_REC;
+  const int halves = 2 * nblk;
+  for (int k = 0; k < halves; ++k) {
+    if (k >= NR && !__all_sync(0xffffffffu, pipe_wait(bs.raw_free, NR, k - NR, abort))) break;
+    const int j = HB * k + lane;
     const int32_t pr = j < n_rows ? rows[j] : -1;
-    const bool valid = pr >= 0 && (int64_t)pr < a.pool_rows;
-    const uint8_t* rec = raw + hr * REC;
-    if (it < DL / 16) {
-      const int d = 16 * it;
-      uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
-      if (valid) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rec + d);
-        const __half2 sc = __float2half2_rn(*reinterpret_cast<const float*>(rec + DL + 4 * (it >> 3)));
-        o0 = make_uint4(to_f16x2((uint16_t)(v.x & 0xFFFFu), sc), to_f16x2((uint16_t)(v.x >> 16), sc),
-                        to_f16x2((uint16_t)(v.y & 0xFFFFu), sc), to_f16x2((uint16_t)(v.y >> 16), sc));
-        o1 = make_uint4(to_f16x2((uint16_t)(v.z & 0xFFFFu), sc), to_f16x2((uint16_t)(v.z >> 16), sc),
-                        to_f16x2((uint16_t)(v.w & 0xFFFFu), sc), to_f16x2((uint16_t)(v.w >> 16), sc));
+    const int32_t mine = pr >= 0 && (int64_t)pr < a.pool_rows ? pr : -1;  // lane l: record l
+    uint8_t* dst = raw + (k % NR) * (HB * REC);
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      const int c = 32 * i + lane, rec = c / CH, q = c - rec * CH;
+      const int32_t src = __shfl_sync(0xffffffffu, mine, rec);
+      if (src >= 0) cp_async16(dst + rec * REC + 16 * q, a.kv_pool + (size_t)src * ROWB + 16 * q);
+    }
+    cp_async_arrive(&bs.raw_full[k % NR]);
+  }
+}
+
+// One dequantisation warp's part of a half-block: items it = wq, wq + NW, ... of each of the
+// 32 rows (lane = row of the half), so its 16-B reads of the raw records (272 or 400 B apart)
+// and its tile stores (8 rows spread over a 128-B line by the swizzle) hit distinct banks.
+// Latent items (16 codes): e4m3 -> f16 times the row's scale; RoPE items (S only, 8 dims):
+// bf16 -> f16. Rows outside the pool are written as zeros.
+template <bool kS>
+__device__ __forceinline__ void dequant_half(const uint8_t* __restrict__ rec, uint8_t* __restrict__ tile, int row,
+                                             bool valid, int wq) {
+  constexpr int ITEMS = kS ? S_ITEMS : O_ITEMS;
+  constexpr int NW = kS ? S_NDEQW : O_NDEQW;
+  const uint32_t rb = (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
+  const int x = row & 7;
+  const auto at = [&](int d) {  // byte offset of (row, dim d) in the tile
+    return (uint32_t)((d >> 6) * KV_ATOM) + rb + ((uint32_t)(((d & 63) >> 3) ^ x) << 4);
+  };
+#pragma unroll
+  for (int it0 = 0; it0 < ITEMS; it0 += NW) {
+    const int it = it0 + wq;
+    if (it < ITEMS) {
+      if (it < DL / 16) {
+        const int d = 16 * it;
+        uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+        if (valid) {
+          const uint4 v = *reinterpret_cast<const uint4*>(rec + d);
+          const __half2 sc = __float2half2_rn(*reinterpret_cast<const float*>(rec + DL + 4 * (d >> 7)));
+          o0 = make_uint4(to_f16x2((uint16_t)(v.x & 0xFFFFu), sc), to_f16x2((uint16_t)(v.x >> 16), sc),
+                          to_f16x2((uint16_t)(v.y & 0xFFFFu), sc), to_f16x2((uint16_t)(v.y >> 16), sc));
+          o1 = make_uint4(to_f16x2((uint16_t)(v.z & 0xFFFFu), sc), to_f16x2((uint16_t)(v.z >> 16), sc),
+                          to_f16x2((uint16_t)(v.w & 0xFFFFu), sc), to_f16x2((uint16_t)(v.w >> 16), sc));
+        }
+        *reinterpret_cast<uint4*>(tile + at(d)) = o0;
+        *reinterpret_cast<uint4*>(tile + at(d + 8)) = o1;
+      } else {
+        const int e = it - DL / 16;  // RoPE dims DL + 8e .. (S only)
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+          const uint4 w = *reinterpret_cast<const uint4*>(rec + DL + 16 + 16 * e);
+          v = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+        }
+        *reinterpret_cast<uint4*>(tile + at(DL + 8 * e)) = v;
       }
-      *reinterpret_cast<uint4*>(tile + (d >> 6) * KV_ATOM + sw128(row, d & 63)) = o0;
-      *reinterpret_cast<uint4*>(tile + ((d + 8) >> 6) * KV_ATOM + sw128(row, (d + 8) & 63)) = o1;
-    } else {
-      const int d = DL + 8 * (it - DL / 16);
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (valid) {
-        const uint4 w = *reinterpret_cast<const uint4*>(rec + DL + 16 + 2 * (d - DL));
-        v = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
-      }
-      *reinterpret_cast<uint4*>(tile + (d >> 6) * KV_ATOM + sw128(row, d & 63)) = v;
     }
   }
 }
 
-// Whether row j of the split is a pool row.
-__device__ __forceinline__ bool row_valid(const SparseMlaArgs& a, const int32_t* rows, int n_rows, int j) {
-  const int32_t pr = j < n_rows ? rows[j] : -1;
-  return pr >= 0 && (int64_t)pr < a.pool_rows;
-}
-
-// The dequantisation warps' loop over half-blocks (both roles). They also load the records:
-// the first NR half-blocks up front, then half-block k + NR into ring buffer k % NR as soon as
-// all of them have finished dequantising half-block k, with 16-byte asynchronous copies of
-// each valid record's first rec_bytes bytes, spread over the group; each thread's arrival on
-// raw_full fires once its copies have landed. Every exit is taken by the whole group (named
-// barrier 2). The tile is freed by the MMAs that read it.
-template <bool with_rope>
+// A dequantisation warp's loop over half-blocks. In the S-CTA it waits, before its first tile
+// store, until Q has left the staging area (which the K tiles overlay). Each warp goes at its
+// own pace: it frees the ring buffer when done with it, and its lane 0 arrives on tile_full
+// after the block's second half.
+template <bool kS>
 __device__ __forceinline__ void run_dequant(const SparseMlaArgs& a, const int32_t* rows, int n_rows, int nblk,
-                                            uint8_t* raw, uint8_t* tiles, uint32_t tile_bytes, Barriers& bs, int t,
-                                            int nthreads, volatile int* abort) {
-  constexpr int REC = with_rope ? ROWB : OREC;
-  constexpr int CH = REC / 16;
-  constexpr uint32_t RAWH = with_rope ? RAW_HALF : ORAW_HALF;
-  const auto issue = [&](int k) {
-    uint8_t* dst = raw + (k % NR) * RAWH;
-    for (int c = t; c < HB * CH; c += nthreads) {
-      const int rec = c / CH, q = c - rec * CH;
-      const int j = HB * k + rec;
-      const int32_t pr = j < n_rows ? rows[j] : -1;
-      if (pr >= 0 && (int64_t)pr < a.pool_rows)
-        cp_async16(dst + rec * REC + 16 * q, a.kv_pool + (size_t)pr * ROWB + 16 * q);
-    }
-    cp_async_arrive(&bs.raw_full[k % NR]);
-  };
+                                            const uint8_t* raw, uint8_t* tiles, Barriers& bs, int wq, int lane,
+                                            volatile int* abort) {
+  constexpr int REC = kS ? S_REC : O_REC;
+  constexpr uint32_t TB = kS ? K_TILE : V_TILE;
   const int halves = 2 * nblk;
-  for (int k = 0; k < NR && k < halves; ++k) issue(k);
   for (int k = 0; k < halves; ++k) {
     const int b = k >> 1;
     bool ok = true;
-    if ((k & 1) == 0 && b >= NT) ok = pipe_wait(bs.tile_free, NT, b - NT, abort);
+    if (kS && k == 0) ok = pipe_wait(&bs.q_full, 1, 0, abort);
+    if ((k & 1) == 0 && b >= NT) ok = ok && pipe_wait(bs.tile_free, NT, b - NT, abort);
     ok = ok && pipe_wait(bs.raw_full, NR, k, abort);
-    if (!sync_and<2>(ok, nthreads)) break;
-    dequant_half<with_rope>(a, rows, n_rows, raw + (k % NR) * RAWH, tiles + (b % NT) * tile_bytes, k, t, nthreads);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const int j = HB * k + lane;
+    const int32_t pr = j < n_rows ? rows[j] : -1;
+    dequant_half<kS>(raw + (k % NR) * (HB * REC) + lane * REC, tiles + (b % NT) * TB, (k & 1) * HB + lane,
+                     pr >= 0 && (int64_t)pr < a.pool_rows, wq);
     fence_async_smem();  // the tile's generic writes before the tensor core reads it
-    if (k & 1) bar_arrive(&bs.tile_full[b % NT]);
-    sync_n<2>(nthreads);  // every thread is done with ring buffer k % NR
-    if (k + NR < halves) issue(k + NR);
+    __syncwarp();
+    if (lane == 0) {
+      bar_arrive(&bs.raw_free[k % NR]);
+      if (k & 1) bar_arrive(&bs.tile_full[b % NT]);
+    }
   }
 }
 
@@ -405,12 +436,17 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   const int nblk = j_end > j_begin ? (j_end - j_begin + BJ - 1) / BJ : 0;
 
   if (tid == 0) {
-    for (int k = 0; k < NR; ++k) bar_init(&bs.raw_full[k], rank == 0 ? S_NDEQ : O_NDEQ);  // every loader's copies
+    const int ndeqw = rank == 0 ? S_NDEQW : O_NDEQW;
+    for (int k = 0; k < NR; ++k) {
+      bar_init(&bs.raw_full[k], 32);  // one per loader lane
+      bar_init(&bs.raw_free[k], ndeqw);
+    }
     for (int k = 0; k < NT; ++k) {
-      bar_init(&bs.tile_full[k], rank == 0 ? S_NDEQ : O_NDEQ);
+      bar_init(&bs.tile_full[k], ndeqw);
       bar_init(&bs.tile_free[k], 1);
     }
     bar_init(&bs.q_full, 8);  // one arrival per warp of the two softmax warpgroups
+    bar_init(&bs.mma_done, 1);
     for (int k = 0; k < 2; ++k) {
       bar_init(&bs.s_full[k], 1);
       bar_init(&bs.s_free[k], 8);
@@ -460,28 +496,36 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
       // thread; first, Q of request r into tensor memory (warpgroup wg the columns
       // [144 wg, 144 wg + 144)), the A operand of S = Q . K^T, column c holding dims 2c, 2c + 1
       const int wg = warp >> 2;
-      {
-        // 72 columns (144 dims, 288 B) at a time: every load of a round is in flight together
-        const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)r * a.num_heads + head) * DQK);
-        const bool live = head < a.num_heads;
-#pragma unroll 1
-        for (int c0 = wg * 144; c0 < wg * 144 + 144; c0 += 72) {
-          uint4 w[18];
-#pragma unroll
-          for (int k = 0; k < 18; ++k) w[k] = live ? __ldg(src + (c0 * 2) / 8 + k) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int c = 0; c < 72; c += 8) {
-            uint4 x = w[c / 4], y = w[c / 4 + 1];
-            x = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
-            y = make_uint4(bf16x2_to_f16x2(y.x), bf16x2_to_f16x2(y.y), bf16x2_to_f16x2(y.z), bf16x2_to_f16x2(y.w));
-            asm volatile(
-                "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(tbase + lane_off + Q_COL +
-                                                                                             c0 + c),
-                "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w), "r"(y.x), "r"(y.y), "r"(y.z), "r"(y.w)
-                : "memory");
-          }
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      if (nblk > 0) {
+        // Q of request r ([num_heads][576] bf16, contiguous) into the staging area with
+        // coalesced 16-B copies, each head's row at a 1,168-B pitch; then each thread converts
+        // its head's half of the row (warpgroup wg the columns [144 wg, 144 wg + 144)) to f16
+        // pairs in tensor memory, the A operand of S = Q . K^T, column c holding dims 2c, 2c + 1
+        const uint8_t* qg = reinterpret_cast<const uint8_t*>(a.q + (size_t)r * a.num_heads * DQK);
+        uint8_t* qs = base + S_QSTAGE;
+        for (int c = tid; c < a.num_heads * (DQK / 8); c += 2 * MH) {
+          const int h = c / (DQK / 8), q = c - h * (DQK / 8);
+          cp_async16(qs + h * QPITCH + 16 * q, qg + 16 * (size_t)c);
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        sync_n(2 * MH);
+        const bool live = head < a.num_heads;
+        const uint8_t* src = qs + head * QPITCH;
+#pragma unroll 6
+        for (int c = 36 * wg; c < 36 * wg + 36; c += 2) {  // two 16-B chunks: 16 dims, 8 columns
+          uint4 x = make_uint4(0u, 0u, 0u, 0u), y = x;
+          if (live) {
+            x = *reinterpret_cast<const uint4*>(src + 16 * c);
+            y = *reinterpret_cast<const uint4*>(src + 16 * c + 16);
+          }
+          x = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+          y = make_uint4(bf16x2_to_f16x2(y.x), bf16x2_to_f16x2(y.y), bf16x2_to_f16x2(y.z), bf16x2_to_f16x2(y.w));
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                           tbase + lane_off + Q_COL + 4 * c),
+                       "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w), "r"(y.x), "r"(y.y), "r"(y.z), "r"(y.w)
+                       : "memory");
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_before();
         __syncwarp();
         if (lane == 0) bar_arrive(&bs.q_full);
@@ -576,8 +620,10 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
         }
         __syncwarp();
       }
-    } else if (warp > S_ISSUER) {
-      run_dequant<true>(a, rows, n_rows, nblk, raw, tiles, K_TILE, bs, tid - S_DEQ0, S_NDEQ, abort);
+    } else if (warp == S_LOADER) {
+      run_loader<true>(a, rows, n_rows, nblk, raw, bs, lane, abort);
+    } else {
+      run_dequant<true>(a, rows, n_rows, nblk, raw, tiles, bs, warp - S_DEQW0, lane, abort);
     }
   } else {
     // ================================ O-CTA ================================
@@ -627,21 +673,26 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
                      dv0 + (uint64_t)((nh * 4 * KV_ATOM + kk * 2048) >> 4), kIdescO, (b > 0 || kk > 0) ? 1u : 0u);
           commit(&bs.tile_free[b % NT]);
           commit_multicast(&bs.p_free[b & 1], 1);  // the S-CTA's P buffer b & 1 is free once these are done
+          commit(&bs.mma_done);
           s_issued = b + 1;
         }
         __syncwarp();
       }
-    } else if (warp > O_ISSUER) {
-      run_dequant<false>(a, rows, n_rows, nblk, raw, tiles, V_TILE, bs, tid - O_DEQ0, O_NDEQ, abort);
+    } else if (warp == O_LOADER) {
+      run_loader<false>(a, rows, n_rows, nblk, raw, bs, lane, abort);
+    } else {
+      run_dequant<false>(a, rows, n_rows, nblk, raw, tiles, bs, warp - O_DEQW0, lane, abort);
     }
   }
 
   __syncthreads();
-  bool ok = !*abort;
+  // this CTA's MMAs of every block are done; the O-CTA also has the S-CTA's totals, the S-CTA
+  // the O-CTA's last P-buffer releases (its last arrivals here)
+  bool ok = !*abort && (nblk == 0 || pipe_wait(bs.tile_free, NT, nblk - 1, abort));
   if (rank == 1) {
-    // every block's P . V is done and the S-CTA's totals are in: read O out
-    ok = ok && (nblk == 0 || pipe_wait(bs.tile_free, NT, nblk - 1, abort));
     ok = ok && pipe_wait<true>(&bs.fin, 1, 0, abort);
+  } else {
+    for (int b = nblk >= 2 ? nblk - 2 : 0; b < nblk; ++b) ok = ok && pipe_wait<true>(bs.p_free, 2, b, abort);
   }
   ok = __syncthreads_and(ok && !*abort);
   tc_after();
@@ -678,8 +729,10 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
     __syncthreads();
     const int n = s_issued;
     if (n > 0) {
-      if (rank == 0) pipe_wait(bs.s_full, 2, n - 1, abort);
-      pipe_wait(bs.tile_free, NT, n - 1, abort);
+      if (rank == 0)
+        pipe_wait(bs.s_full, 2, n - 1, abort);
+      else
+        pipe_wait(&bs.mma_done, 1, n - 1, abort);
     }
   }
   tc_before();
