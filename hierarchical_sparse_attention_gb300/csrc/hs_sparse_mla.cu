@@ -41,8 +41,12 @@
 // more than one split a small kernel merges the splits by their log-sum-exp.
 #include "hs_internal.h"
 
+#include <cuda.h>  // CUtensorMap and its encoder's types (the encoder is fetched through the runtime)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <cstring>
+#include <mutex>
 
 namespace hs {
 namespace {
@@ -64,7 +68,10 @@ constexpr uint32_t Q_COL = 0, S_COL = 288;
 // Shared memory between the CTAs moves only ~41 GB/s per direction, far below what the two
 // SMs read from L2, so the pair exchanges P and nothing else.
 constexpr int S_REC = ROWB, O_REC = DL + 16;          // bytes of a record in the raw buffers
-constexpr int S_CH = S_REC / 16, O_CH = O_REC / 16;   // their 16-B chunks
+// The loader gathers four records per tensor copy (rows of the pool seen as a 2-D tensor of
+// 8-byte elements, one row per record); each group of four lands 128-byte aligned.
+constexpr int S_GRP = (4 * S_REC + 127) / 128 * 128, O_GRP = (4 * O_REC + 127) / 128 * 128;
+constexpr int S_SLOT = HB / 4 * S_GRP, O_SLOT = HB / 4 * O_GRP;  // a ring buffer: one half-block
 constexpr int S_ITEMS = DL / 16 + (DQK - DL) / 8;     // dequantisation items per row: 16 codes or 8 RoPE dims
 constexpr int O_ITEMS = DL / 16;
 // S-CTA warps: 0-7 softmax (two warpgroups), 8 issuer, 9 loader, 10-15 dequantisation
@@ -79,12 +86,12 @@ constexpr int QPITCH = DQK * 2 + 16;                   // a head's staged Q row 
 constexpr uint32_t S_TILES = 0;                         // S-CTA: NT K tiles
 constexpr uint32_t S_QSTAGE = 0;                        //        Q staged over them before the first block
 constexpr uint32_t S_RAW = MH * QPITCH;                 //        NR raw buffers
-constexpr uint32_t S_MX = S_RAW + NR * HB * S_REC;      //        block maxima of the two warpgroups
+constexpr uint32_t S_MX = S_RAW + NR * S_SLOT;         //        block maxima of the two warpgroups
 constexpr uint32_t S_L1 = S_MX + 2 * MH * 4;            //        warpgroup 1's row sums at the end
 constexpr uint32_t S_END = S_L1 + MH * 4;
 constexpr uint32_t O_TILES = 0;                         // O-CTA: NT V tiles
 constexpr uint32_t O_RAW = O_TILES + NT * V_TILE;       //        NR raw buffers
-constexpr uint32_t O_P = (O_RAW + NR * HB * O_REC + 1023u) & ~1023u;  // two P buffers, 128 x 64 f16
+constexpr uint32_t O_P = (O_RAW + NR * O_SLOT + 1023u) & ~1023u;  // two P buffers, 128 x 64 f16
 constexpr uint32_t P_BUF = MH * BJ * 2;
 constexpr uint32_t O_ALPHA = O_P + 2 * P_BUF;           //        two blocks' rescale factors
 constexpr uint32_t P_BYTES = P_BUF + MH * 4;            // what the S-CTA sends per block
@@ -240,11 +247,6 @@ __device__ __forceinline__ void st_remote_f32(uint32_t raddr, float v) {
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
-// An arrival on the mbarrier once every cp.async this thread issued before has landed (the
-// arrival counts against the barrier's expected count).
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 // Asynchronous stores into the partner CTA's shared memory that complete their bytes on the
 // partner's mbarrier (no fence or arrival of the storing thread needed).
 __device__ __forceinline__ void st_async16(uint32_t raddr, uint4 v, uint32_t rbar) {
@@ -315,30 +317,34 @@ struct Barriers {
   uint64_t fin;                         // O-CTA, arrived by the S-CTA: final l and m written
 };
 
-// The loader warp: half-block k's records into ring buffer k % NR once every dequantisation
-// warp is done with half-block k - NR, as 16-byte asynchronous copies (lane l takes chunks
-// l, l + 32, ... of the 32 records, so a warp's copies read whole records in order); each
-// lane's arrival on raw_full fires once its copies have landed. The S-CTA copies whole records,
-// the O-CTA their first DL + 16 bytes (latent codes, scales).
+// The loader warp: half-block k's 32 records into ring buffer k % NR once every dequantisation
+// warp is done with half-block k - NR, as eight four-row tensor gathers (lane g < 8: records
+// 4g .. 4g + 3) that complete on raw_full; the S-CTA's tensor map spans whole records, the
+// O-CTA's their first DL + 16 bytes (latent codes, scales). Rows outside the pool (and the
+// rows past the split's end) are gathered as pool row 0 -- the dequantisation writes zeros for
+// them -- so every gather moves the same bytes; an empty pool gathers nothing.
 template <bool kS>
-__device__ __forceinline__ void run_loader(const SparseMlaArgs& a, const int32_t* rows, int n_rows, int nblk,
-                                           uint8_t* raw, Barriers& bs, int lane, volatile int* abort) {
-  constexpr int CH = kS ? S_CH : O_CH;
-  constexpr int REC = kS ? S_REC : O_REC;
+__device__ __forceinline__ void run_loader(const SparseMlaArgs& a, const CUtensorMap* tmap, const int32_t* rows,
+                                           int n_rows, int nblk, uint8_t* raw, Barriers& bs, int lane,
+                                           volatile int* abort) {
+  constexpr int REC = kS ? S_REC : O_REC, GRP = kS ? S_GRP : O_GRP, SLOT = kS ? S_SLOT : O_SLOT;
+  const bool any = a.pool_rows > 0;
   const int halves = 2 * nblk;
   for (int k = 0; k < halves; ++k) {
     if (k >= NR && !__all_sync(0xffffffffu, pipe_wait(bs.raw_free, NR, k - NR, abort))) break;
     const int j = HB * k + lane;
     const int32_t pr = j < n_rows ? rows[j] : -1;
-    const int32_t mine = pr >= 0 && (int64_t)pr < a.pool_rows ? pr : -1;  // lane l: record l
-    uint8_t* dst = raw + (k % NR) * (HB * REC);
+    const int32_t y = pr >= 0 && (int64_t)pr < a.pool_rows ? pr : 0;  // lane l: record l's pool row
+    int32_t y4[4];
 #pragma unroll
-    for (int i = 0; i < CH; ++i) {
-      const int c = 32 * i + lane, rec = c / CH, q = c - rec * CH;
-      const int32_t src = __shfl_sync(0xffffffffu, mine, rec);
-      if (src >= 0) cp_async16(dst + rec * REC + 16 * q, a.kv_pool + (size_t)src * ROWB + 16 * q);
-    }
-    cp_async_arrive(&bs.raw_full[k % NR]);
+    for (int i = 0; i < 4; ++i) y4[i] = __shfl_sync(0xffffffffu, y, (4 * lane + i) & 31);
+    if (lane == 0) bar_arrive_tx(&bs.raw_full[k % NR], any ? HB * REC : 0);
+    if (any && lane < HB / 4)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+          "%4, %5, %6}], [%7];" ::"r"(smem_u32(raw + (k % NR) * SLOT + lane * GRP)),
+          "l"(tmap), "r"(0), "r"(y4[0]), "r"(y4[1]), "r"(y4[2]), "r"(y4[3]), "r"(smem_u32(&bs.raw_full[k % NR]))
+          : "memory");
   }
 }
 
@@ -352,6 +358,10 @@ __device__ __forceinline__ void dequant_half(const uint8_t* __restrict__ rec, ui
                                              bool valid, int wq) {
   constexpr int ITEMS = kS ? S_ITEMS : O_ITEMS;
   constexpr int NW = kS ? S_NDEQW : O_NDEQW;
+  // Gather groups are 128-B aligned, so records 4 apart sit at the same bank offset: rows with
+  // bit 2 set take their items in an order rotated by four, which moves their reads to the
+  // other half of the banks (their tile stores stay spread by the swizzle).
+  const int rot = (row & 4) ? 4 : 0;
   const uint32_t rb = (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
   const int x = row & 7;
   const auto at = [&](int d) {  // byte offset of (row, dim d) in the tile
@@ -359,8 +369,8 @@ __device__ __forceinline__ void dequant_half(const uint8_t* __restrict__ rec, ui
   };
 #pragma unroll
   for (int it0 = 0; it0 < ITEMS; it0 += NW) {
-    const int it = it0 + wq;
-    if (it < ITEMS) {
+    if (it0 + wq < ITEMS) {
+      const int it = it0 + wq + rot < ITEMS ? it0 + wq + rot : it0 + wq + rot - ITEMS;
       if (it < DL / 16) {
         const int d = 16 * it;
         uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
@@ -395,7 +405,7 @@ template <bool kS>
 __device__ __forceinline__ void run_dequant(const SparseMlaArgs& a, const int32_t* rows, int n_rows, int nblk,
                                             const uint8_t* raw, uint8_t* tiles, Barriers& bs, int wq, int lane,
                                             volatile int* abort) {
-  constexpr int REC = kS ? S_REC : O_REC;
+  constexpr int REC = kS ? S_REC : O_REC, GRP = kS ? S_GRP : O_GRP, SLOT = kS ? S_SLOT : O_SLOT;
   constexpr uint32_t TB = kS ? K_TILE : V_TILE;
   const int halves = 2 * nblk;
   for (int k = 0; k < halves; ++k) {
@@ -407,8 +417,8 @@ __device__ __forceinline__ void run_dequant(const SparseMlaArgs& a, const int32_
     if (!__all_sync(0xffffffffu, ok)) break;
     const int j = HB * k + lane;
     const int32_t pr = j < n_rows ? rows[j] : -1;
-    dequant_half<kS>(raw + (k % NR) * (HB * REC) + lane * REC, tiles + (b % NT) * TB, (k & 1) * HB + lane,
-                     pr >= 0 && (int64_t)pr < a.pool_rows, wq);
+    dequant_half<kS>(raw + (k % NR) * SLOT + (lane >> 2) * GRP + (lane & 3) * REC, tiles + (b % NT) * TB,
+                     (k & 1) * HB + lane, pr >= 0 && (int64_t)pr < a.pool_rows, wq);
     fence_async_smem();  // the tile's generic writes before the tensor core reads it
     __syncwarp();
     if (lane == 0) {
@@ -418,8 +428,10 @@ __device__ __forceinline__ void run_dequant(const SparseMlaArgs& a, const int32_
   }
 }
 
-__global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a, float* __restrict__ part_o,
-                                                          float* __restrict__ part_lse, uint32_t* __restrict__ err) {
+__global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a, const __grid_constant__ CUtensorMap tm_s,
+                                                          const __grid_constant__ CUtensorMap tm_o,
+                                                          float* __restrict__ part_o, float* __restrict__ part_lse,
+                                                          uint32_t* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint32_t s_taddr;
@@ -438,7 +450,7 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   if (tid == 0) {
     const int ndeqw = rank == 0 ? S_NDEQW : O_NDEQW;
     for (int k = 0; k < NR; ++k) {
-      bar_init(&bs.raw_full[k], 32);  // one per loader lane
+      bar_init(&bs.raw_full[k], 1);  // the loader's arrival with the gathers' bytes
       bar_init(&bs.raw_free[k], ndeqw);
     }
     for (int k = 0; k < NT; ++k) {
@@ -621,7 +633,7 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
         __syncwarp();
       }
     } else if (warp == S_LOADER) {
-      run_loader<true>(a, rows, n_rows, nblk, raw, bs, lane, abort);
+      run_loader<true>(a, &tm_s, rows, n_rows, nblk, raw, bs, lane, abort);
     } else {
       run_dequant<true>(a, rows, n_rows, nblk, raw, tiles, bs, warp - S_DEQW0, lane, abort);
     }
@@ -679,7 +691,7 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
         __syncwarp();
       }
     } else if (warp == O_LOADER) {
-      run_loader<false>(a, rows, n_rows, nblk, raw, bs, lane, abort);
+      run_loader<false>(a, &tm_o, rows, n_rows, nblk, raw, bs, lane, abort);
     } else {
       run_dequant<false>(a, rows, n_rows, nblk, raw, tiles, bs, warp - O_DEQW0, lane, abort);
     }
@@ -738,29 +750,45 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   tc_before();
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS) : "memory");
+  // the merge kernel (if any) may launch; it waits for this grid's completion before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the partner no longer reads or arrives on this CTA's shared memory
   cluster_sync_all();
 }
 
 // Merge the splits of each (request, head): weights exp(lse_p - lse), lse = log sum exp lse_p.
-__global__ void __launch_bounds__(T) combine_kernel(const SparseMlaArgs a, const float* __restrict__ part_o,
-                                                    const float* __restrict__ part_lse) {
-  const int rh = blockIdx.x;  // r * num_heads + h
-  const int R = gridDim.x / a.num_heads;
-  const size_t stride = (size_t)R * a.num_heads;
+// One thread per four consecutive output dims, so every thread issues its splits' loads
+// together (the merge is a pass over the splits' partial outputs, bound by memory latency and
+// bandwidth, not arithmetic).
+constexpr int COMBINE_T = 256;
+__global__ void __launch_bounds__(COMBINE_T) combine_kernel(const SparseMlaArgs a, int rh_total,
+                                                            const float* __restrict__ part_o,
+                                                            const float* __restrict__ part_lse) {
+  // launched as a programmatic dependent of the attention kernel: wait until that grid has
+  // finished and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int g = blockIdx.x * COMBINE_T + threadIdx.x;  // (r * num_heads + h) * 128 + quarter-dim index
+  const int rh = g >> 7, c4 = g & 127;
+  if (rh >= rh_total) return;
+  const size_t stride = (size_t)rh_total;
   float mx = -INFINITY;
-  for (int p = 0; p < a.splits; ++p) mx = fmaxf(mx, part_lse[p * stride + rh]);
+  for (int p = 0; p < a.splits; ++p) mx = fmaxf(mx, __ldg(part_lse + p * stride + rh));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float z = 0.f;
-  for (int p = 0; p < a.splits; ++p) z += mx == -INFINITY ? 0.f : expf(part_lse[p * stride + rh] - mx);
-  for (int d = threadIdx.x; d < DL; d += T) {
-    float acc = 0.f;
+  if (mx != -INFINITY) {
+    for (int p = 0; p < a.splits; ++p) z += expf(__ldg(part_lse + p * stride + rh) - mx);
+    const float inv = 1.f / z;
     for (int p = 0; p < a.splits; ++p) {
-      const float w = mx == -INFINITY ? 0.f : expf(part_lse[p * stride + rh] - mx) / z;
-      acc += w * part_o[(p * stride + rh) * DL + d];
+      const float w = expf(__ldg(part_lse + p * stride + rh) - mx) * inv;
+      const float4 v = __ldg(reinterpret_cast<const float4*>(part_o + (p * stride + rh) * DL) + c4);
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
     }
-    a.o[(size_t)rh * DL + d] = acc;
   }
-  if (threadIdx.x == 0) a.lse[rh] = mx == -INFINITY ? -INFINITY : mx + logf(z);
+  reinterpret_cast<float4*>(a.o + (size_t)rh * DL)[c4] = acc;
+  if (c4 == 0) a.lse[rh] = mx == -INFINITY ? -INFINITY : mx + logf(z);
 }
 
 }  // namespace
@@ -769,10 +797,55 @@ static_assert(SMEM_BYTES <= 227 * 1024, "the consumer's shared memory exceeds a 
 
 size_t sparse_mla_smem_bytes() { return SMEM_BYTES; }
 
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, fetched once through the runtime (no link against the
+// driver library).
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// The pool as a 2-D tensor of 8-byte elements, one row per record (656 B = 82 elements), read
+// `box_bytes` at a time from the start of a row (one row per box: the gathers pick the rows).
+cudaError_t pool_map(CUtensorMap* m, const uint8_t* pool, int64_t rows, int box_bytes) {
+  EncodeTiled fn = encoder();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)(ROWB / 8), (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ROWB};
+  const cuuint32_t box[2] = {(cuuint32_t)(box_bytes / 8), 1u};
+  const cuuint32_t elem[2] = {1u, 1u};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(pool), dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, float* part_o, float* part_lse,
                               uint32_t* err, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  CUtensorMap tm_s, tm_o;  // an empty pool is never gathered from
+  memset(&tm_s, 0, sizeof(tm_s));
+  memset(&tm_o, 0, sizeof(tm_o));
+  if (a.pool_rows > 0) {
+    if ((e = pool_map(&tm_s, a.kv_pool, a.pool_rows, S_REC)) != cudaSuccess) return e;
+    if ((e = pool_map(&tm_o, a.kv_pool, a.pool_rows, O_REC)) != cudaSuccess) return e;
+  }
   const bool direct = a.splits == 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2u * (unsigned)num_requests, (unsigned)a.splits);  // a CTA pair per (request, split)
@@ -786,10 +859,19 @@ cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, floa
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, a, direct ? a.o : part_o, direct ? a.lse : part_lse, err);
+  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, a, tm_s, tm_o, direct ? a.o : part_o, direct ? a.lse : part_lse, err);
   if (e != cudaSuccess || direct) return e;
-  combine_kernel<<<num_requests * a.num_heads, T, 0, stream>>>(a, part_o, part_lse);
-  return cudaGetLastError();
+  const int rh_total = num_requests * a.num_heads;
+  cudaLaunchConfig_t mc = {};
+  mc.gridDim = dim3((unsigned)((rh_total * (DL / 4) + COMBINE_T - 1) / COMBINE_T));
+  mc.blockDim = dim3(COMBINE_T);
+  mc.stream = stream;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  mc.attrs = pdl;
+  mc.numAttrs = 1;
+  return cudaLaunchKernelEx(&mc, combine_kernel, a, rh_total, (const float*)part_o, (const float*)part_lse);
 }
 
 }  // namespace hs
