@@ -38,16 +38,17 @@
 //      comes from the age histogram (exact radix select when the histogram cannot decide);
 //      exactly the needed victims are gathered and ordered by (stamp, slot)
 //   7  pair miss j with victim j: update the map and the residency bitmap; publish each
-//      miss's device row to its copy CTA (distributed shared memory, then the release half
-//      of the split cluster barrier)
+//      miss's device row to its copy CTA (distributed shared memory, then a release-arrive
+//      on that copy CTA's publication mbarrier)
 //   8  write back the changed slots, the row table and the clock
 //   9  copy the misses no copy CTA took (only when the geometry runs without copy CTAs)
 //      straight from host memory
 // A copy CTA owns a slice of the top-k row. At kernel start it predicts its slice's
 // misses from the residency bitmap (a looked-up token whose bit is clear), looks
 // up their host rows and pulls them into shared memory while the resolve CTA does the
-// exact work; after the cluster barrier it stores the staged rows of exact misses to their
-// device rows and copies any unpredicted miss straight from host memory.
+// exact work; once the resolve CTA has published the outcomes (its own mbarrier, so it does
+// not wait for the other copy CTAs) it stores the staged rows of exact misses to their device
+// rows and copies any unpredicted miss straight from host memory.
 #include <climits>
 
 #include "hs_internal.h"
@@ -239,6 +240,36 @@ __device__ __forceinline__ void st_remote(const void* local_addr, uint32_t rank,
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
+constexpr int kPublishTryNs = 20000, kPublishTries = 10000;  // about 200 ms of tries at most
+
+// The resolve CTA tells copy CTA `rank` that this step's outcomes are in its shared memory:
+// an arrival (release, cluster scope) on the copy CTA's `pub` mbarrier. The calling thread
+// comes after a CTA barrier that follows every outcome store of the CTA.
+__device__ __forceinline__ void publish_to(uint64_t* pub, uint32_t rank) {
+  uint32_t raddr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_addr(pub)), "r"(rank));
+  asm volatile("fence.acq_rel.cluster;\n\tmbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr)
+               : "memory");
+}
+// A copy CTA's wait for phase `parity` of its `pub` mbarrier, by one thread (the others wait at
+// a CTA barrier). Each try sleeps until the phase completes or kPublishTryNs pass; the bound is
+// a count of tries, not a clock, because the waiting thread's own host loads may still be in
+// flight (a first access to host pages can stall far longer than the resolve CTA's work).
+// False if the bound ran out.
+__device__ __forceinline__ bool publish_wait(uint64_t* pub, uint32_t parity) {
+  for (int tries = 0; tries < kPublishTries; ++tries) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(pub)), "r"(parity), "n"(kPublishTryNs)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
 // Ascending bitonic sort of n (a power of two) 64-bit keys in shared memory.
 __device__ void bitonic_sort(uint64_t* keys, int n) {
   for (int k = 2; k <= n; k <<= 1) {
@@ -351,12 +382,12 @@ __device__ void copy_rows(const Geometry& g, const Pools& p, const int32_t* psrc
 // It looks up the predicted
 // misses' host rows and reads those rows into shared memory right away (16-byte loads,
 // kCopyUnroll in flight per thread), so the host-link transfer runs while the resolve CTA
-// does the exact work. The cluster barrier then publishes the exact outcome of every entry.
+// does the exact work. The resolve CTA then publishes the exact outcome of every entry.
 // Exact misses store their staged row; misses that were not staged (a stale bit, no
 // room) are copied straight from host memory. A predicted miss that was a hit sets the
 // token's bit again.
 __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a, const StepArgs& sa, int r, int q,
-                         unsigned char* smem, uint32_t* err_word) {
+                         int32_t seq_r, unsigned char* smem, uint64_t* pub, uint32_t pub_parity, uint32_t* err_word) {
   const CopyLayout cl = make_copy_layout(g);
   const int32_t* c_res = reinterpret_cast<const int32_t*>(smem + cl.res);
   int32_t* c_tk = reinterpret_cast<int32_t*>(smem + cl.tk);
@@ -370,9 +401,7 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
   const int per = copy_slice(g);
   const int e0 = (q - 1) * per;
   const int ne = max(0, min(g.K, e0 + per) - e0);
-  const int32_t S = sa.spec_q < 0 ? a.seq_lens[r] : a.seq_lens[r] + sa.spec_q + 1;
-  const int32_t base = sa.spec_q < 0 ? S - 1 : a.seq_lens[r];  // first position new to the cache
-  const bool predict = a.hint != nullptr && a.copy_layers > 0 && S > g.H && S <= g.max_context;
+  const bool may_predict = a.hint != nullptr && a.copy_layers > 0;
   uint32_t* bits_g = a.hint ? a.hint + (size_t)r * g.bit_words : nullptr;  // residency bitmap row
   const uint32_t* bits = g.bits_smem ? reinterpret_cast<const uint32_t*>(smem + cl.bits) : bits_g;
   const int32_t* hcl_row = a.host_cache_locs + (size_t)r * g.max_context;
@@ -382,12 +411,19 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
   uint32_t flags = 0;
   int staged = 0;
 
-  if (predict) {
+  // The prediction's inputs (the bitmap row, the top-k slice) are requested before the
+  // request's length is known, so their latency overlaps that of seq_lens.
+  if (may_predict) {
     if (g.bits_smem)
       cp_async_words(reinterpret_cast<int32_t*>(smem + cl.bits), reinterpret_cast<const int32_t*>(bits_g),
                      g.bit_words);
     cp_async_commit();
     for (int e = tid; e < ne; e += T) c_tk[e] = tk_g[e];  // plain loads: the row may be host memory
+  }
+  const int32_t S = sa.spec_q < 0 ? seq_r : seq_r + sa.spec_q + 1;
+  const int32_t base = sa.spec_q < 0 ? S - 1 : seq_r;  // first position new to the cache
+  const bool predict = may_predict && S > g.H && S <= g.max_context;
+  if (predict) {
     cp_async_wait_all();
     __syncthreads();
     for (int e = tid; e < ne; e += T) {
@@ -434,10 +470,14 @@ __device__ void copy_cta(const Geometry& g, const Pools& p, const ResolveArgs& a
       }
     }
   }
-  cluster_wait();    // phase A (arrived at kernel start)
-  cluster_arrive();  // phase B: the resolve CTA has published every entry's outcome
-  cluster_wait();
-  __syncthreads();
+  cluster_wait();  // phase A (arrived at kernel start)
+  cp_async_wait_all();  // the pools table, when no prediction waited for it
+  // The resolve CTA's outcomes for this step: each copy CTA goes on as soon as they are in and
+  // its own staged rows have landed, not when its sibling copy CTAs are done too.
+  if (!__syncthreads_and(tid != 0 || publish_wait(pub, pub_parity))) {
+    if (tid == 0) atomicOr(err_word, HS_FLAG_TIMEOUT);  // no outcomes: this CTA copies nothing
+    return;
+  }
 
   // staged entries that are exact misses
   for (int c = tid; c < staged * per_miss; c += T) {
@@ -516,21 +556,20 @@ __device__ __forceinline__ void flush_flags(uint32_t flags, uint32_t* err_word) 
   if ((threadIdx.x & 31) == 0 && f) atomicOr(err_word, f);
 }
 
-// The cluster barrier phases a resolve CTA that leaves a step early (a skipped request, the
-// fast path) still owes its copy CTAs: they wait for phase A and then meet at phase B.
-__device__ __forceinline__ void finish_phases(int C) {
+// What a resolve CTA that leaves a step early (a skipped request, the fast path) still owes
+// its copy CTAs: cluster barrier phase A, and the (empty) publication of the outcomes.
+__device__ __forceinline__ void finish_phases(int C, uint64_t* pub) {
   if (C > 0) {
-    cluster_wait();     // phase A
-    cluster_arrive();   // phase B: no outcome to publish
-    cluster_wait();
+    cluster_wait();  // phase A: the copy CTAs' publication barriers are initialised
+    if (threadIdx.x < C) publish_to(pub, threadIdx.x + 1);
   }
 }
 
-// The resolve CTA of request r for one step (phases 0-9 below). Every exit completes the
-// cluster barrier phases A and B that the copy CTAs take part in.
+// The resolve CTA of request r for one step (phases 0-9 below). Every exit completes cluster
+// barrier phase A and publishes the outcomes (none on an early exit) to each copy CTA.
 __device__ __forceinline__ void resolve_cta(const Geometry& g, const Pools& s_pools, const ResolveArgs& a,
                                             const StepArgs& sa, uint32_t* __restrict__ err_word, unsigned char* smem,
-                                            int r) {
+                                            uint64_t* pub, int r, int32_t seq_r) {
   const int tid = threadIdx.x;
   const int C = g.copy_ctas;
   const Layout lay = make_layout(g);
@@ -559,8 +598,8 @@ __device__ __forceinline__ void resolve_cta(const Geometry& g, const Pools& s_po
   // A plain step's one new position is the newest token, S - 1. Verify step q of a
   // speculative batch attends over S0 + q + 1 tokens, and the batch's positions t >= S0 (the
   // token the last round sampled, then the drafts) sit in the reserved rows H + (t - S0).
-  const int32_t S = sa.spec_q < 0 ? a.seq_lens[r] : a.seq_lens[r] + sa.spec_q + 1;
-  const int32_t base = sa.spec_q < 0 ? S - 1 : a.seq_lens[r];
+  const int32_t S = sa.spec_q < 0 ? seq_r : seq_r + sa.spec_q + 1;
+  const int32_t base = sa.spec_q < 0 ? S - 1 : seq_r;
   const int32_t* tk_g = sa.top_k_tokens + (size_t)r * K;
   int32_t* out_g = sa.out_rows + (size_t)r * K;
   const int32_t* dbl_g = a.device_buffer_locs + (size_t)r * (H + a.spec_n);
@@ -569,6 +608,19 @@ __device__ __forceinline__ void resolve_cta(const Geometry& g, const Pools& s_po
   int32_t* st_g = a.lru_slots + (size_t)r * H;
   uint32_t flags = 0;
 
+  // ---- phase 0: state into shared memory: the slot state asynchronously, the top-k row by
+  // plain loads (top_k_tokens may be pinned host memory, which cp.async is not used on). It is
+  // requested before the request's length is known (the slot state even if the request turns
+  // out to be on the fast path), so its latency overlaps that of seq_lens.
+  if (g.dbl_smem) cp_async_words(s_dbl_staged, dbl_g, H + 1);
+  cp_async_words(s_tok, tok_g, H);
+  cp_async_words(s_stamp, st_g, H);
+  cp_async_commit();
+  for (int i = tid; i < K; i += T) s_tk[i] = tk_g[i];
+  for (int h = tid; h < HS; h += T) s_hash[h] = kEmpty;
+  for (int i = tid; i < K; i += T) s_claim[i] = INF;
+  if (tid < SC_COUNT) s_sc[tid] = tid == SC_LO ? 0xffffffffu : 0u;
+  if (tid < 256) s_hist[tid] = 0;
   if (S < 0 || S > g.max_context) {
     for (int i = tid; i < K; i += T) out_g[i] = -1;
     if (tid == 0) {
@@ -576,24 +628,11 @@ __device__ __forceinline__ void resolve_cta(const Geometry& g, const Pools& s_po
       if (sa.plan_cnt) sa.plan_cnt[r] = 0;
       atomicOr(err_word, HS_FLAG_SEQLEN);
     }
-    finish_phases(C);
+    cp_async_wait_all();  // the copies issued above and at kernel start
+    finish_phases(C, pub);
     return;
   }
   const bool fast = S <= H;
-
-  // ---- phase 0: state into shared memory: the slot state asynchronously, the top-k row by
-  // plain loads (top_k_tokens may be pinned host memory, which cp.async is not used on)
-  if (g.dbl_smem) cp_async_words(s_dbl_staged, dbl_g, H + 1);
-  if (!fast) {
-    cp_async_words(s_tok, tok_g, H);
-    cp_async_words(s_stamp, st_g, H);
-  }
-  cp_async_commit();
-  for (int i = tid; i < K; i += T) s_tk[i] = tk_g[i];
-  for (int h = tid; h < HS; h += T) s_hash[h] = kEmpty;
-  for (int i = tid; i < K; i += T) s_claim[i] = INF;
-  if (tid < SC_COUNT) s_sc[tid] = tid == SC_LO ? 0xffffffffu : 0u;
-  if (tid < 256) s_hist[tid] = 0;
   cp_async_wait_all();
   __syncthreads();
 
@@ -666,7 +705,7 @@ __device__ __forceinline__ void resolve_cta(const Geometry& g, const Pools& s_po
         hint_row[w] = nb - 32 * w >= 32 ? ~0u : (1u << (nb - 32 * w)) - 1u;
     }
     flush_flags(flags, err_word);
-    finish_phases(C);
+    finish_phases(C, pub);
     return;
   }
 
@@ -1015,7 +1054,10 @@ __device__ __forceinline__ void resolve_cta(const Geometry& g, const Pools& s_po
       s_pdst[j] = d;
     }
   }
-  if (C > 0) cluster_arrive();  // phase B: every outcome is published to the copy CTAs
+  if (C > 0) {  // every outcome is in the copy CTAs' shared memory: publish it to each
+    __syncthreads();
+    if (tid < C) publish_to(pub, tid + 1);
+  }
   for (int j = tid; j < m; j += T) {  // this thread's misses of the loop above
     const int32_t t = s_tk[s_miss[j]], old_tok = s_vict[j];
     if (hint_row && old_tok >= -1) {
@@ -1045,7 +1087,6 @@ __device__ __forceinline__ void resolve_cta(const Geometry& g, const Pools& s_po
   // ---- phase 9: misses no copy CTA took, the leader layers, straight from host memory
   if (s_sc[SC_DIRECT]) copy_rows(g, s_pools, s_psrc, s_pdst, m, a.copy_layers);
   flush_flags(flags, err_word);
-  if (C > 0) cluster_wait();  // phase B complete; the copy CTAs finish on their own
 }
 
 // kBatch = false: one step (a plain decode step, or the one verify step a.spec_q); true: the
@@ -1060,14 +1101,22 @@ __global__ void __launch_bounds__(T, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ Pools s_pools;
+  __shared__ __align__(16) Pools s_pools;
   __shared__ StepArgs s_step;  // this step's arguments, read where they are used (no registers held)
+  __shared__ __align__(8) uint64_t s_pub;  // copy CTAs: the resolve CTA published this step's outcomes
   const int tid = threadIdx.x;
   const int C = g.copy_ctas;
   const uint32_t rank = C > 0 ? cluster_rank() : 0u;
   const int r = blockIdx.x / (C + 1);  // one cluster of C + 1 CTAs per request
-  if (tid < (int)(sizeof(Pools) / sizeof(uint64_t)))
-    reinterpret_cast<uint64_t*>(&s_pools)[tid] = reinterpret_cast<const uint64_t*>(pools)[tid];
+  // The pools table comes in asynchronously after the first release-arrive of barrier phase A
+  // (which would otherwise wait for it): no CTA waits for it before it needs a pool address
+  // (the copy CTAs before their first row load, the resolve CTA at the end of its phase 0).
+  static_assert(sizeof(Pools) % 16 == 0, "the pools table moves in 16-byte pieces");
+  const auto load_pools = [&] {
+    if (tid < (int)(sizeof(Pools) / 16))
+      cp_async16(reinterpret_cast<uint4*>(&s_pools) + tid, reinterpret_cast<const uint4*>(pools) + tid);
+    cp_async_commit();
+  };
   // A speculative batch's verify steps run here in order, one after the other, over the
   // request's shared slot state (each with its own top-k slice, row table, miss counts and
   // plan slice); a plain step is one pass. The two roles loop apart, so each loop keeps only
@@ -1090,9 +1139,17 @@ __global__ void __launch_bounds__(T, 1)
       int32_t* res = reinterpret_cast<int32_t*>(smem + cl0.res);
       for (int e = tid; e < copy_slice(g); e += T) res[e] = -1;
       if (tid < 4) reinterpret_cast<uint32_t*>(smem + cl0.cnt)[tid] = 0u;
+      if (q == 0 && tid == 0) {  // one phase per step; phase A orders the initialisation before the first arrival
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&s_pub)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      }
       cluster_arrive();
+      if (q == 0) load_pools();
       __syncthreads();  // the CTA's own clears and step arguments before its threads read them
-      copy_cta(g, s_pools, a, s_step, r, (int)rank, smem, err_word);
+      // Loaded after the release-arrive, which would otherwise wait for it (plain load: may be
+      // host memory); its latency overlaps the prediction's loads.
+      const int32_t seq_r = a.seq_lens[r];
+      copy_cta(g, s_pools, a, s_step, r, (int)rank, seq_r, smem, &s_pub, (uint32_t)q & 1u, err_word);
     }
     return;
   }
@@ -1110,7 +1167,9 @@ __global__ void __launch_bounds__(T, 1)
     if (tid == 0) s_step = step_args(a, kBatch ? q : -1);
     __syncthreads();  // the step arguments (and the pools table) before any thread reads them
     if (C > 0) cluster_arrive();  // phase A
-    resolve_cta(g, s_pools, a, s_step, err_word, smem, r);
+    if (q == 0) load_pools();
+    const int32_t seq_r = a.seq_lens[r];  // after the release-arrive, as in the copy CTAs
+    resolve_cta(g, s_pools, a, s_step, err_word, smem, &s_pub, r, seq_r);
   }
 }
 
