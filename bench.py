@@ -402,6 +402,10 @@ def build_host_pools(wl, hs, node: int = -1):
 
 STALL_RATIO = 2.0
 MAX_ATTEMPTS = 3
+# Host-pool readiness before timing: the warm-up replay's miss rows must cross the link at
+# COLD_FRAC of the in-run ceiling at least (a step at the dsa shape runs at ~0.45 of it, a
+# cold host at ~0.01); otherwise wait COLD_SLEEP_S and replay again, for COLD_WAIT_S at most.
+COLD_FRAC, COLD_SLEEP_S, COLD_WAIT_S = 0.15, 10.0, 240.0
 
 
 def stalled(ms, ws: int) -> bool:
@@ -530,6 +534,27 @@ def run_ours(args, ws, rank, local):
     # process pays that once at start-up, so the timed steps should not. "disjoint" replays the
     # K steps after the timed range (other rows of the same sequences), never the timed steps'
     # own inputs; "timed" replays the timed steps themselves (kept for comparison only).
+    # Host-pool readiness: on a freshly started GPU host the GPU's reads of the registered
+    # pools have run ~75x below the link's rate for the first minutes (steps of 80 ms instead
+    # of 1.1 ms, whole processes long). Time the warm-up replay (its first step fills an empty
+    # buffer, so it moves plenty of rows) until its miss rows cross the link at COLD_FRAC of
+    # the ceiling; every probe is reported.
+    ready_probes = []
+    t_ready = time.perf_counter()
+    while True:
+        e0.record(stream)
+        reset_state_and_warm()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        warm_bytes = float(miss_acc[:W_].sum().item()) * B * L
+        ready_probes.append(round(warm_bytes / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1))
+        ready = max_over_ranks(0.0 if ready_probes[-1] >= COLD_FRAC * h2d_ceiling else 1.0, ws) == 0.0
+        if ready or time.perf_counter() - t_ready + COLD_SLEEP_S > COLD_WAIT_S:
+            break
+        time.sleep(COLD_SLEEP_S)
+    host_ready = {"warmup_replay_gbs": ready_probes, "waited_s": round(time.perf_counter() - t_ready, 1),
+                  "rule": f"the warm-up replay's miss rows at >= {COLD_FRAC} x the ceiling before timing, "
+                          f"replayed every {COLD_SLEEP_S:.0f} s for {COLD_WAIT_S:.0f} s at most", "ready": ready}
     rehearsal = {"disjoint": range(W_ + K_, W_ + 2 * K_), "timed": range(W_, W_ + K_), "none": range(0)}[args.rehearsal]
     if len(rehearsal):
         reset_state_and_warm()
@@ -696,8 +721,17 @@ def run_ours(args, ws, rank, local):
                 raise RuntimeError(f"end-to-end step {s}: miss counts read back differ from the timed run")
         return ws * valid_rows * e2e_steps / max_over_ranks(sum(ms) * 1e-3, ws), ms
 
-    e2e_copy_value, e2e_copy_ms = e2e_pass(False)
-    e2e_value, e2e_ms = e2e_pass(True)
+    def e2e_measured(zero_copy):  # the stall rule of the timed passes
+        tries = []
+        for _ in range(MAX_ATTEMPTS):
+            v, ms = e2e_pass(zero_copy)
+            tries.append(round(1e3 * float(np.median(ms)), 1))
+            if not stalled(ms, ws):
+                break
+        return v, ms, tries
+
+    e2e_copy_value, e2e_copy_ms, e2e_copy_tries = e2e_measured(False)
+    e2e_value, e2e_ms, e2e_tries = e2e_measured(True)
     h2d_b = 4 * R * K + 4 * R
     d2h_b = 4 * R * K + 4 * R
     dominant = "resolve_kernel" if not split else "gather_pairs_kernel"
@@ -721,6 +755,7 @@ def run_ours(args, ws, rank, local):
         "p50_dominant_kernel_us": 1e3 * float(np.median(dom_ms)),
         "resolve_timing": "eager launches, CUDA events around the resolve work alone (without copy CTAs: "
                           "hs_resolve_layers(0) + hs_gather of every layer, the same four kernels as hs_resolve)",
+        "host_pool_readiness": host_ready,
         "timed_attempts": attempts_a,
         "dominant_kernel_attempts": attempts_b,
         "attempt_rule": f"a pass with a step above {STALL_RATIO} x its median is measured again, "
@@ -748,6 +783,7 @@ def run_ours(args, ws, rank, local):
                              "timing": "the whole resolve work (all its launches)"}},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
                 "steps": e2e_steps, "p50_step_us": 1e3 * float(np.median(e2e_ms)),
+                "attempts_p50_step_us": e2e_tries, "copies_attempts_p50_step_us": e2e_copy_tries,
                 "timing": "wall clock per step, graph launch to stream sync; the step's inputs are in one "
                           "pinned host block the host refills before each step and its outputs go to one "
                           "pinned host block: hs_resolve reads the top-k rows and seq_lens and writes the row "
@@ -1163,7 +1199,7 @@ def run_e2e(args, ws, rank, local):
     cfg = hs.make_config(R, K, H, B, L, wl.ps, wl.max_context, wl.max_pages)
     wsp = torch.zeros(hs.hs_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
     h = hs.hs_create(cfg, host, dpool, wl.host_rows, wl.device_rows, wsp)
-    Hq, splits = MLA_HEADS, 1  # one split: a wave of R x 4 CTAs, no merge kernel
+    Hq, splits = MLA_HEADS, 2  # two splits: 64 CTA pairs on 128 SMs, the fastest at this shape
     qs = [torch.from_numpy(wl.queries_bf16(i, Hq).view(np.int16)).to(dev) for i in range(4)]
     q_buf = torch.empty_like(qs[0])
     o = torch.empty((R, Hq, 512), dtype=torch.float32, device=dev)
@@ -1250,7 +1286,7 @@ def run_e2e(args, ws, rank, local):
         "metric": "decode steps/s with the sparse-MLA consumer (resolve + backup + attention)",
         "value": ws * K_ / t_step, "unit": "steps/s", "n_gpus": ws, "steps": K_, "warmup": W_,
         "ms_per_step": 1e3 * t_step / K_, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int32+bf16", "data": "synthetic",
+        "dtype": "int32+f16", "data": "synthetic",
         "config": {"workload": f"{args.config}: {R} requests, top_k {K}, {H} hot slots, {B}-byte fp8 MLA rows; "
                                f"attention {Hq} heads x 576/512 dims, {splits} split(s)",
                    "l2": "flushed between timed steps (256 MiB write)"},

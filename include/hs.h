@@ -470,7 +470,7 @@ HS_API hs_status hs_host_bind_node(void* ptr, size_t bytes, int32_t node);
  *
  * The first call on a device, with that device current, looks up the array's device
  * address (cudaGetSymbolAddress), checks the pools and fits the kernel to the device, and
- * caches all three; make that first call before any stream capture. A later call with the
+ * caches all three. A later call with the
  * same configuration and pools reuses them; a changed configuration or pool set redoes the
  * set-up on the host (no allocation). Each call then queues, on `stream`, a one-thread
  * kernel that writes the pools table into the array and clears its error word, the resolve
