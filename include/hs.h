@@ -113,7 +113,9 @@ typedef enum {
   HS_ERR_INVALID_CONFIG = 2, /* configuration the kernels cannot run (limits below) */
   HS_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
   HS_ERR_DEVICE_FLAGGED = 4, /* hs_get_error found HS_FLAG_* bits set */
-  HS_ERR_TIMEOUT = 5         /* reserved for bounded device waits (none in this version) */
+  HS_ERR_TIMEOUT = 5         /* not returned by this version: a bounded device wait that runs out
+                                sets HS_FLAG_TIMEOUT in the error word instead (the resolve's copy
+                                CTAs waiting for their outcomes, the consumer's role hand-offs) */
 } hs_status;
 
 /* Device-side anomaly bits in the workspace error word (sticky until cleared). */
