@@ -26,9 +26,9 @@
 //     end every warp reads O out, normalised by the S-CTA's row sums.
 // So S is computed once per row and O once per value dim: no CTA repeats another's product.
 // In each CTA a loader warp brings the half-blocks of 32 records into a ring of shared-memory
-// buffers (16-byte asynchronous copies, mbarrier completion; the S-CTA whole 656-B records,
-// the O-CTA their 528 B of latent codes and scales) through the split's row table
-// staged in shared memory once, and dequantisation warps turn them into the CTA's own f16
+// buffers (eight four-row tensor gathers per half-block, mbarrier completion; the S-CTA whole
+// 656-B records, the O-CTA their 528 B of latent codes and scales) through the split's row
+// table staged in shared memory once, and dequantisation warps turn them into the CTA's own f16
 // tile (the S-CTA all 576 dims as K, the O-CTA the 512 latent dims as V: e4m3 -> f16 in
 // hardware, times the row's scale in f16; bf16 RoPE rounded to f16), swizzled K-major, two
 // tiles in flight. The pair exchanges only P: shared memory between two CTAs moves ~41 GB/s
