@@ -391,9 +391,33 @@ def alloc_host_pools(wl, node: int = -1):
     return [arr for arr, _ in pools], pools
 
 
+def host_mem_available() -> int:
+    """MemAvailable of /proc/meminfo in bytes (0 when it cannot be read)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    return 0
+
+
+HOST_MEM_FRACTION = 0.85  # of MemAvailable, for all of one host's ranks' host pools together
+
+
 def build_host_pools(wl, hs, node: int = -1):
     """alloc_host_pools, then each pool registered (pinned and mapped) and read from the GPU
-    TOUCH_PASSES times."""
+    TOUCH_PASSES times. Refuses to start, like a serving process whose host pool does not fit
+    ("vLLM Hybrid HiSparse source implementation analysis": start-up checks the host memory),
+    when this host's ranks' pools together would take more than HOST_MEM_FRACTION of the
+    available memory, instead of driving the host out of memory."""
+    need = wl.host_pool_bytes if wl.cfg.host_layout == "page_first" else wl.host_rows * wl.B * wl.L
+    ranks = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    avail = host_mem_available()
+    if avail and ranks * need > HOST_MEM_FRACTION * avail:
+        raise MemoryError(f"host pools need {ranks} x {need / 1e9:.1f} GB on this host, more than "
+                          f"{HOST_MEM_FRACTION:.0%} of the {avail / 1e9:.0f} GB available")
     views, pools = alloc_host_pools(wl, node)
     for arr, reg in pools:
         touch_host_pool_from_gpu(hs.hs_host_register(arr) if reg else host_device_ptr(arr), arr.nbytes)
