@@ -106,6 +106,9 @@ constexpr uint32_t kSuspendNs = 20000;                  // a waiting thread slee
                                                         // (it wakes when the phase completes), so waiting
                                                         // warps leave the issue slots to the working ones
 constexpr float kRescaleLog2 = 8.f;                     // reference-maximum slack (log2 units)
+constexpr int EPI_PITCH = 36;                           // floats per staged row of the read-out (16-B aligned,
+                                                        // and 8 lanes' 16-B stores hit distinct banks)
+static_assert(16 * 32 * EPI_PITCH * 4 <= NT * V_TILE, "the read-out staging fits the V tiles' space");
 static_assert(S_RAW >= NT * K_TILE, "the staged Q covers the K tiles only");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -709,28 +712,43 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   ok = __syncthreads_and(ok && !*abort);
   tc_after();
   if (rank == 1 && ok) {
+    // O out, normalised: warp w holds heads 32 (w & 3) .. + 31 (its tensor-memory lanes) and
+    // reads a quarter of their columns, 32 at a time; each 32 x 32 piece goes through the
+    // warp's own staging rows in shared memory (the V tiles' space, free now) so that every
+    // global store writes whole 128-byte lines: 8 lanes per row, 4 rows per instruction.
     const float* fin = reinterpret_cast<const float*>(base + O_FIN);
     const float l = fin[head], m = fin[MH + head];
-    const bool live = head < a.num_heads;
-    const size_t row_out = (((size_t)p * (gridDim.x >> 1) + r) * a.num_heads + head);  // [split][r][h]
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    const int c0 = (warp >> 2) * (DL / 4);  // warp w reads a quarter of the columns of its lanes
-    for (int c = c0; c < c0 + DL / 4; c += 16) {
-      float v[16];
+    const int head0 = (warp & 3) * 32;
+    float* out_rows = part_o + (((size_t)p * (gridDim.x >> 1) + r) * a.num_heads) * DL;  // [split][r][h][DL]
+    float* stg = reinterpret_cast<float*>(base + O_TILES) + warp * (32 * EPI_PITCH);
+    const int c0 = (warp >> 2) * (DL / 4);
+    for (int c = c0; c < c0 + DL / 4; c += 32) {
+      float v[32];
       if (nblk > 0) {
-        tmem_ld16(tbase + lane_off + c, v);
+        tmem_ld16(tbase + lane_off + c, *reinterpret_cast<float(*)[16]>(v));
+        tmem_ld16(tbase + lane_off + c + 16, *reinterpret_cast<float(*)[16]>(v + 16));
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
-      if (live) {
-        float* dst = part_o + row_out * DL + c;
 #pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4*>(dst + i) = make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(stg + lane * EPI_PITCH + i) =
+            make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + (lane >> 3), q4 = lane & 7;  // row of the piece, four-float column
+        if (head0 + rr < a.num_heads)
+          *reinterpret_cast<float4*>(out_rows + (size_t)(head0 + rr) * DL + c + 4 * q4) =
+              *reinterpret_cast<const float4*>(stg + rr * EPI_PITCH + 4 * q4);
       }
+      __syncwarp();
     }
-    if (live && warp < 4) part_lse[row_out] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    if (head < a.num_heads && warp < 4)
+      part_lse[((size_t)p * (gridDim.x >> 1) + r) * a.num_heads + head] =
+          l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
   }
   if (!ok) {
     // outputs are not valid: flag it, and give any MMA still in flight one more bound before
