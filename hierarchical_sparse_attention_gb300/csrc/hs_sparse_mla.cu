@@ -82,7 +82,8 @@ constexpr int O_ISSUER = 4, O_LOADER = 5, O_DEQW0 = 6, O_NDEQW = T / 32 - O_DEQW
 // shared memory carve-up (offsets from a 1024-B aligned base); the two roles use different parts
 constexpr uint32_t KV_ATOM = BJ * 128;                 // one swizzle atom of a tile: 64 rows x 128 B
 constexpr uint32_t K_TILE = KATOMS * KV_ATOM, V_TILE = VATOMS * KV_ATOM;
-constexpr int QPITCH = DQK * 2 + 16;                   // a head's staged Q row (padded: conflict-free reads)
+constexpr uint32_t QBOX = MH * 128;                     // a staged Q box: 128 heads x 64 dims (128 B), swizzled
+constexpr int QPITCH = DQK * 2 + 16;                   // the staging area's extent per head
 constexpr uint32_t S_TILES = 0;                         // S-CTA: NT K tiles
 constexpr uint32_t S_QSTAGE = 0;                        //        Q staged over them before the first block
 constexpr uint32_t S_RAW = MH * QPITCH;                 //        NR raw buffers
@@ -246,10 +247,6 @@ __device__ __forceinline__ void bar_arrive_remote(uint32_t raddr) {
 __device__ __forceinline__ void st_remote_f32(uint32_t raddr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(raddr), "f"(v) : "memory");
 }
-// 16 bytes global -> shared, asynchronously (cached in L2 only).
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
 // Asynchronous stores into the partner CTA's shared memory that complete their bytes on the
 // partner's mbarrier (no fence or arrival of the storing thread needed).
 __device__ __forceinline__ void st_async16(uint32_t raddr, uint4 v, uint32_t rbar) {
@@ -311,6 +308,7 @@ struct Barriers {
   uint64_t raw_free[NR];                // every dequantisation warp is done with a ring buffer
   uint64_t tile_full[NT];               // dequantisation -> issuer: the tile is written
   uint64_t tile_free[NT];               // the MMAs that read the tile are done
+  uint64_t q_raw;                       // S-CTA: Q's boxes have landed in the staging area
   uint64_t q_full;                      // S-CTA: Q in tensor memory (its staging area is free)
   uint64_t s_full[2], s_free[2];        // S-CTA: S written by the MMAs; read by the softmax
   uint64_t p_free[2];                   // S-CTA, arrived by the O-CTA: P buffer free again
@@ -433,6 +431,7 @@ __device__ __forceinline__ void run_dequant(const SparseMlaArgs& a, const int32_
 
 __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a, const __grid_constant__ CUtensorMap tm_s,
                                                           const __grid_constant__ CUtensorMap tm_o,
+                                                          const __grid_constant__ CUtensorMap tm_q,
                                                           float* __restrict__ part_o, float* __restrict__ part_lse,
                                                           uint32_t* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -460,6 +459,7 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
       bar_init(&bs.tile_full[k], ndeqw);
       bar_init(&bs.tile_free[k], 1);
     }
+    bar_init(&bs.q_raw, 1);   // the issuing thread's arrival with the boxes' bytes
     bar_init(&bs.q_full, 8);  // one arrival per warp of the two softmax warpgroups
     bar_init(&bs.mma_done, 1);
     for (int k = 0; k < 2; ++k) {
@@ -512,26 +512,30 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
       // [144 wg, 144 wg + 144)), the A operand of S = Q . K^T, column c holding dims 2c, 2c + 1
       const int wg = warp >> 2;
       if (nblk > 0) {
-        // Q of request r ([num_heads][576] bf16, contiguous) into the staging area with
-        // coalesced 16-B copies, each head's row at a 1,168-B pitch; then each thread converts
-        // its head's half of the row (warpgroup wg the columns [144 wg, 144 wg + 144)) to f16
-        // pairs in tensor memory, the A operand of S = Q . K^T, column c holding dims 2c, 2c + 1
-        const uint8_t* qg = reinterpret_cast<const uint8_t*>(a.q + (size_t)r * a.num_heads * DQK);
+        // Q of request r into the staging area as nine tensor boxes of 128 heads x 64 dims
+        // (128 B per head, 16-B chunks swizzled by head % 8, so the per-head reads below hit
+        // distinct banks); then each thread converts its head's half of the row (warpgroup wg
+        // the columns [144 wg, 144 wg + 144)) to f16 pairs in tensor memory, the A operand of
+        // S = Q . K^T, column c holding dims 2c, 2c + 1. Heads past num_heads read as zeros.
         uint8_t* qs = base + S_QSTAGE;
-        for (int c = tid; c < a.num_heads * (DQK / 8); c += 2 * MH) {
-          const int h = c / (DQK / 8), q = c - h * (DQK / 8);
-          cp_async16(qs + h * QPITCH + 16 * q, qg + 16 * (size_t)c);
+        if (tid == 0) {
+          bar_arrive_tx(&bs.q_raw, (DQK / 64) * QBOX);
+          for (int bx = 0; bx < DQK / 64; ++bx)
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+                "[%4];" ::"r"(smem_u32(qs + bx * QBOX)),
+                "l"(&tm_q), "r"(64 * bx), "r"(r * a.num_heads), "r"(smem_u32(&bs.q_raw))
+                : "memory");
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        sync_n(2 * MH);
-        const bool live = head < a.num_heads;
-        const uint8_t* src = qs + head * QPITCH;
+        const bool landed = sync_and(pipe_wait(&bs.q_raw, 1, 0, abort), 2 * MH);  // every softmax thread takes part
+        const bool live = landed && head < a.num_heads;
+        const uint8_t* src = qs + head * 128;
 #pragma unroll 6
         for (int c = 36 * wg; c < 36 * wg + 36; c += 2) {  // two 16-B chunks: 16 dims, 8 columns
           uint4 x = make_uint4(0u, 0u, 0u, 0u), y = x;
           if (live) {
-            x = *reinterpret_cast<const uint4*>(src + 16 * c);
-            y = *reinterpret_cast<const uint4*>(src + 16 * c + 16);
+            x = *reinterpret_cast<const uint4*>(src + (c >> 3) * QBOX + ((((c & 7)) ^ (head & 7)) << 4));
+            y = *reinterpret_cast<const uint4*>(src + ((c + 1) >> 3) * QBOX + ((((c + 1) & 7) ^ (head & 7)) << 4));
           }
           x = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
           y = make_uint4(bf16x2_to_f16x2(y.x), bf16x2_to_f16x2(y.y), bf16x2_to_f16x2(y.z), bf16x2_to_f16x2(y.w));
@@ -851,15 +855,32 @@ cudaError_t pool_map(CUtensorMap* m, const uint8_t* pool, int64_t rows, int box_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Q ([rows = requests x heads][576] bf16) as a 2-D tensor read in boxes of 128 rows x 64 dims
+// (128 B), swizzled in 128-byte rows (the 16-B chunk index XOR-ed with the row % 8); rows past
+// the end read as zeros.
+cudaError_t q_map(CUtensorMap* m, const uint16_t* q, int64_t rows) {
+  EncodeTiled fn = encoder();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)DQK, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)DQK * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)MH};
+  const cuuint32_t elem[2] = {1u, 1u};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(q), dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, float* part_o, float* part_lse,
                               uint32_t* err, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  CUtensorMap tm_s, tm_o;  // an empty pool is never gathered from
+  CUtensorMap tm_s, tm_o, tm_q;  // an empty pool is never gathered from
   memset(&tm_s, 0, sizeof(tm_s));
   memset(&tm_o, 0, sizeof(tm_o));
+  if ((e = q_map(&tm_q, a.q, (int64_t)num_requests * a.num_heads)) != cudaSuccess) return e;
   if (a.pool_rows > 0) {
     if ((e = pool_map(&tm_s, a.kv_pool, a.pool_rows, S_REC)) != cudaSuccess) return e;
     if ((e = pool_map(&tm_o, a.kv_pool, a.pool_rows, O_REC)) != cudaSuccess) return e;
@@ -877,7 +898,8 @@ cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, floa
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, a, tm_s, tm_o, direct ? a.o : part_o, direct ? a.lse : part_lse, err);
+  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, a, tm_s, tm_o, tm_q, direct ? a.o : part_o, direct ? a.lse : part_lse,
+                         err);
   if (e != cudaSuccess || direct) return e;
   const int rh_total = num_requests * a.num_heads;
   cudaLaunchConfig_t mc = {};
