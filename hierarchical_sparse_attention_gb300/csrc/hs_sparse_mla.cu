@@ -97,7 +97,8 @@ constexpr uint32_t P_BUF = MH * BJ * 2;
 constexpr uint32_t O_ALPHA = O_P + 2 * P_BUF;           //        two blocks' rescale factors
 constexpr uint32_t P_BYTES = P_BUF + MH * 4;            // what the S-CTA sends per block
 constexpr uint32_t O_FIN = O_ALPHA + 2 * MH * 4;        //        the S-CTA's final l and m per head
-constexpr uint32_t O_END = O_FIN + 2 * MH * 4;
+constexpr uint32_t O_XLSE = O_FIN + 2 * MH * 4;         //        fused merge: the other split's lse per head
+constexpr uint32_t O_END = O_XLSE + MH * 4;
 constexpr int ROWS_CAP = 2048;                          // a split's row-table entries staged in shared memory
 constexpr uint32_t SROWS = (S_END > O_END ? S_END : O_END);  // both: the split's rows of the row table
 constexpr uint32_t SMEM_USED = SROWS + ROWS_CAP * 4;
@@ -316,6 +317,7 @@ struct Barriers {
   uint64_t pv_go[2];                    // O-CTA: O rescaled (if needed); P . V may go
   uint64_t mma_done;                    // O-CTA: the MMAs it issued so far are done
   uint64_t fin;                         // O-CTA, arrived by the S-CTA: final l and m written
+  uint64_t xch;                         // fused merge, O-CTA: the other split's O-CTA wrote its half for this one
 };
 
 // The loader warp: half-block k's 32 records into ring buffer k % NR once every dequantisation
@@ -429,6 +431,9 @@ __device__ __forceinline__ void run_dequant(const SparseMlaArgs& a, const int32_
   }
 }
 
+// kCluster 2: one CTA pair per (request, split); 4: the two splits of a request as two pairs of
+// one cluster, whose O-CTAs merge the splits at the end (no merge kernel).
+template <int kCluster>
 __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a, const __grid_constant__ CUtensorMap tm_s,
                                                           const __grid_constant__ CUtensorMap tm_o,
                                                           const __grid_constant__ CUtensorMap tm_q,
@@ -442,9 +447,12 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   __shared__ int s_issued;  // blocks whose MMAs the issuer started (the last commit to wait for)
   volatile int* abort = &s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint32_t rank;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-  const int r = blockIdx.x >> 1, p = blockIdx.y;
+  uint32_t crank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+  const uint32_t rank = crank & 1u;     // 0: S-CTA, 1: O-CTA
+  const uint32_t partner = crank ^ 1u;  // the other CTA of this pair
+  const int r = blockIdx.x / kCluster;
+  const int p = kCluster == 4 ? (int)(crank >> 1) : (int)blockIdx.y;
   const int per = (a.top_k + a.splits - 1) / a.splits;
   const int j_begin = p * per, j_end = min(a.top_k, j_begin + per);
   const int nblk = j_end > j_begin ? (j_end - j_begin + BJ - 1) / BJ : 0;
@@ -470,6 +478,7 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
       bar_init(&bs.pv_go[k], 4);  // one per corrector warp
     }
     bar_init(&bs.fin, 4);
+    bar_init(&bs.xch, 1);  // fused merge: one release by the other split's O-CTA
     s_abort = 0;
     s_issued = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -550,7 +559,7 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
         if (lane == 0) bar_arrive(&bs.q_full);
       }
       float* s_mx = reinterpret_cast<float*>(base + S_MX);
-      const uint32_t r_pbuf = remote(base + O_P, 1), r_alpha = remote(base + O_ALPHA, 1);
+      const uint32_t r_pbuf = remote(base + O_P, partner), r_alpha = remote(base + O_ALPHA, partner);
       const float sl2 = a.sm_scale * 1.4426950408889634f;  // scores in log2 units
       float m_run = -INFINITY, l_run = 0.f;
       for (int b = 0; b < nblk; ++b) {
@@ -588,7 +597,7 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
         if (!sync_and(b < 2 || pipe_wait<true>(bs.p_free, 2, b - 2, abort), 2 * MH)) break;
         float psum = 0.f;
         const uint32_t pbuf = r_pbuf + (b & 1) * P_BUF;
-        const uint32_t rbar = remote(&bs.p_full[b & 1], 1);
+        const uint32_t rbar = remote(&bs.p_full[b & 1], partner);
 #pragma unroll
         for (int c = 0; c < HB / 8; ++c) {  // four 16-B chunks of 8 f16: rows 32 wg + 8c ..
           uint32_t w[4];
@@ -611,11 +620,11 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
       if (wg == 1) s_l1[head] = l_run;
       sync_n(2 * MH);
       if (wg == 0) {
-        const uint32_t fin = remote(base + O_FIN, 1);
+        const uint32_t fin = remote(base + O_FIN, partner);
         st_remote_f32(fin + 4 * head, l_run + s_l1[head]);
         st_remote_f32(fin + 4 * (MH + head), m_run);
         __syncwarp();
-        if (lane == 0) bar_arrive_remote(remote(&bs.fin, 1));
+        if (lane == 0) bar_arrive_remote(remote(&bs.fin, partner));
       }
     } else if (warp == S_ISSUER) {
       // ---- issuer: S of block b once its tile is full and the softmax has read S of b - 2
@@ -691,7 +700,7 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
               mma_ss(tbase + 256 * nh, dp0 + (uint64_t)((kk * 32) >> 4),
                      dv0 + (uint64_t)((nh * 4 * KV_ATOM + kk * 2048) >> 4), kIdescO, (b > 0 || kk > 0) ? 1u : 0u);
           commit(&bs.tile_free[b % NT]);
-          commit_multicast(&bs.p_free[b & 1], 1);  // the S-CTA's P buffer b & 1 is free once these are done
+          commit_multicast(&bs.p_free[b & 1], (uint16_t)(1u << partner));  // the S-CTA's P buffer is free once these are done
           commit(&bs.mma_done);
           s_issued = b + 1;
         }
@@ -717,17 +726,18 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
   tc_after();
   if (rank == 1 && ok) {
     // O out, normalised: warp w holds heads 32 (w & 3) .. + 31 (its tensor-memory lanes) and
-    // reads a quarter of their columns, 32 at a time; each 32 x 32 piece goes through the
-    // warp's own staging rows in shared memory (the V tiles' space, free now) so that every
-    // global store writes whole 128-byte lines: 8 lanes per row, 4 rows per instruction.
+    // reads its columns 32 at a time; each 32 x 32 piece goes through the warp's own staging
+    // rows in shared memory (the V tiles' space, free now) so that every global store writes
+    // whole 128-byte lines: 8 lanes per row, 4 rows per instruction.
     const float* fin = reinterpret_cast<const float*>(base + O_FIN);
     const float l = fin[head], m = fin[MH + head];
     const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float lse = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    const int nreq = (int)(gridDim.x / kCluster);
     const int head0 = (warp & 3) * 32;
-    float* out_rows = part_o + (((size_t)p * (gridDim.x >> 1) + r) * a.num_heads) * DL;  // [split][r][h][DL]
     float* stg = reinterpret_cast<float*>(base + O_TILES) + warp * (32 * EPI_PITCH);
-    const int c0 = (warp >> 2) * (DL / 4);
-    for (int c = c0; c < c0 + DL / 4; c += 32) {
+    // columns c .. c + 31 of the warp's heads, normalised, into its staging rows
+    auto stage = [&](int c) {
       float v[32];
       if (nblk > 0) {
         tmem_ld16(tbase + lane_off + c, *reinterpret_cast<float(*)[16]>(v));
@@ -741,18 +751,97 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
         *reinterpret_cast<float4*>(stg + lane * EPI_PITCH + i) =
             make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
       __syncwarp();
+    };
+    // the staged piece at column c, as is, to rows [h][DL] from `rows`
+    auto put = [&](float* rows, int c) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int rr = 4 * i + (lane >> 3), q4 = lane & 7;  // row of the piece, four-float column
         if (head0 + rr < a.num_heads)
-          *reinterpret_cast<float4*>(out_rows + (size_t)(head0 + rr) * DL + c + 4 * q4) =
+          *reinterpret_cast<float4*>(rows + (size_t)(head0 + rr) * DL + c + 4 * q4) =
               *reinterpret_cast<const float4*>(stg + rr * EPI_PITCH + 4 * q4);
       }
       __syncwarp();
+    };
+    float* own_rows = part_o + (((size_t)p * nreq + r) * a.num_heads) * DL;  // [split][r][h][DL]
+    if (kCluster == 2) {
+      const int c0 = (warp >> 2) * (DL / 4);  // a quarter of the columns per warp
+      for (int c = c0; c < c0 + DL / 4; c += 32) {
+        stage(c);
+        put(own_rows, c);
+      }
+      if (head < a.num_heads && warp < 4) part_lse[((size_t)p * nreq + r) * a.num_heads + head] = lse;
+    } else {
+      // Both splits of request r in this cluster: the O-CTA of split p merges columns
+      // [256 p, 256 p + 256) of both and hands the other 256 columns of its own output, and its
+      // lse, to the other split's O-CTA. Warp w takes 64 columns of each half (w >> 2 picks them).
+      const int q = 1 - p;
+      const uint32_t xo = crank ^ 2u;  // the other split's O-CTA
+      const int cj = (warp >> 2) * (DL / 8);
+      for (int c = DL / 2 * q + cj; c < DL / 2 * q + cj + DL / 8; c += 32) {
+        stage(c);
+        put(own_rows, c);
+      }
+      if (warp < 4) st_remote_f32(remote(base + O_XLSE, xo) + 4 * head, lse);
+      // every thread's hand-off stores before one release at cluster scope
+      __syncthreads();
+      if (tid == 0) {
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+        bar_arrive_remote(remote(&bs.xch, xo));
+      }
+      const bool go = __all_sync(0xffffffffu, pipe_wait<true>(&bs.xch, 1, 0, abort));
+      if (!go && lane == 0) atomicOr(err, HS_FLAG_TIMEOUT);
+      // the two splits' weights for this lane's head and the merged lse (the merge kernel's
+      // arithmetic, in split order)
+      const float other = reinterpret_cast<const float*>(base + O_XLSE)[head];
+      const float l0 = p == 0 ? lse : other, l1 = p == 0 ? other : lse;
+      const float mx = fmaxf(fmaxf(-INFINITY, l0), l1);
+      float w0 = 0.f, w1 = 0.f, lse_all = -INFINITY;
+      if (mx != -INFINITY) {
+        const float z = expf(l0 - mx) + expf(l1 - mx);
+        const float iz = 1.f / z;
+        w0 = expf(l0 - mx) * iz;
+        w1 = expf(l1 - mx) * iz;
+        lse_all = mx + logf(z);
+      }
+      const float* other_rows = part_o + (((size_t)q * nreq + r) * a.num_heads) * DL;
+      float* out_rows = a.o + ((size_t)r * a.num_heads) * DL;
+      for (int c = DL / 2 * p + cj; go && c < DL / 2 * p + cj + DL / 8; c += 32) {
+        // the other split's piece first (from L2), so its latency overlaps the staging
+        float4 ys[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + (lane >> 3), q4 = lane & 7;
+          ys[i] = head0 + rr < a.num_heads
+                      ? __ldcg(reinterpret_cast<const float4*>(other_rows + (size_t)(head0 + rr) * DL + c + 4 * q4))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        stage(c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + (lane >> 3), q4 = lane & 7;
+          const size_t at = (size_t)(head0 + rr) * DL + c + 4 * q4;
+          const float wa = __shfl_sync(0xffffffffu, w0, rr), wb = __shfl_sync(0xffffffffu, w1, rr);
+          if (head0 + rr < a.num_heads) {
+            const float4 x = *reinterpret_cast<const float4*>(stg + rr * EPI_PITCH + 4 * q4);
+            const float4 y = ys[i];
+            const float4 v0 = p == 0 ? x : y, v1 = p == 0 ? y : x;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            acc.x += wa * v0.x;
+            acc.y += wa * v0.y;
+            acc.z += wa * v0.z;
+            acc.w += wa * v0.w;
+            acc.x += wb * v1.x;
+            acc.y += wb * v1.y;
+            acc.z += wb * v1.z;
+            acc.w += wb * v1.w;
+            *reinterpret_cast<float4*>(out_rows + at) = acc;
+          }
+        }
+        __syncwarp();
+      }
+      if (go && p == 0 && warp < 4 && head < a.num_heads) a.lse[(size_t)r * a.num_heads + head] = lse_all;
     }
-    if (head < a.num_heads && warp < 4)
-      part_lse[((size_t)p * (gridDim.x >> 1) + r) * a.num_heads + head] =
-          l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
   }
   if (!ok) {
     // outputs are not valid: flag it, and give any MMA still in flight one more bound before
@@ -873,10 +962,58 @@ cudaError_t q_map(CUtensorMap* m, const uint16_t* q, int64_t rows) {
 
 }  // namespace
 
+namespace {
+
+// The kernel's launch: a cluster of kCluster CTAs per request and split group, with the dynamic
+// shared memory it needs.
+template <int kCluster>
+cudaLaunchConfig_t mla_config(int32_t num_requests, int splits, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = kCluster == 4 ? dim3(4u * (unsigned)num_requests, 1u)  // both splits' pairs of a request
+                              : dim3(2u * (unsigned)num_requests, (unsigned)splits);  // a pair per (request, split)
+  cfg.blockDim = dim3(T);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Four-CTA clusters of this kernel that the device holds at once (queried once per device).
+int fused_clusters_resident() {
+  static std::mutex mu;
+  static int cached[64];
+  static bool known[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!known[dev]) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = mla_config<4>(1, 2, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_mla_kernel<4>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    cached[dev] = n;
+    known[dev] = true;
+  }
+  return cached[dev];
+}
+
+}  // namespace
+
 cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, float* part_o, float* part_lse,
                               uint32_t* err, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(sparse_mla_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
+      cudaSuccess)
+    return e;
   CUtensorMap tm_s, tm_o, tm_q;  // an empty pool is never gathered from
   memset(&tm_s, 0, sizeof(tm_s));
   memset(&tm_o, 0, sizeof(tm_o));
@@ -885,21 +1022,16 @@ cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, floa
     if ((e = pool_map(&tm_s, a.kv_pool, a.pool_rows, S_REC)) != cudaSuccess) return e;
     if ((e = pool_map(&tm_o, a.kv_pool, a.pool_rows, O_REC)) != cudaSuccess) return e;
   }
-  const bool direct = a.splits == 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2u * (unsigned)num_requests, (unsigned)a.splits);  // a CTA pair per (request, split)
-  cfg.blockDim = dim3(T);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, a, tm_s, tm_o, tm_q, direct ? a.o : part_o, direct ? a.lse : part_lse,
-                         err);
+  // two splits whose four-CTA clusters all fit at once: merged inside the kernel
+  if (a.splits == 2 && fused_clusters_resident() >= num_requests) {
+    const cudaLaunchConfig_t cfg = mla_config<4>(num_requests, 2, stream, attr);
+    return cudaLaunchKernelEx(&cfg, sparse_mla_kernel<4>, a, tm_s, tm_o, tm_q, part_o, part_lse, err);
+  }
+  const bool direct = a.splits == 1;
+  const cudaLaunchConfig_t cfg = mla_config<2>(num_requests, a.splits, stream, attr);
+  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel<2>, a, tm_s, tm_o, tm_q, direct ? a.o : part_o,
+                         direct ? a.lse : part_lse, err);
   if (e != cudaSuccess || direct) return e;
   const int rh_total = num_requests * a.num_heads;
   cudaLaunchConfig_t mc = {};

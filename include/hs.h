@@ -376,7 +376,9 @@ HS_API hs_status hs_invalidate_host_rows(hs_handle* h, int32_t num_requests, con
  * RoPE values are converted from bf16 to fp16, each latent code times its scale is rounded to
  * fp16, and so is P. The inputs must therefore stay within fp16's range (|value| < 65504;
  * values under 2^-14 lose precision). `splits` (1..HS_MAX_MLA_SPLITS) divides each request's
- * rows over more CTA pairs, merged by log-sum-exp in a second kernel.
+ * rows over more CTA pairs, whose partial outputs are merged by log-sum-exp: for two splits,
+ * when a four-CTA cluster per request fits the device in one wave, inside the kernel (the two
+ * pairs of a request share a cluster); otherwise in a second kernel.
  *   q        [R, num_heads, 576] bf16 bits, device, 16-byte aligned (num_heads <= 128)
  *   kv_pool  [pool_rows, 656] bytes, device (a layer's device pool), 16-byte aligned
  *   out_rows [R, top_k] device (hs_resolve's output), top_k <= HS_MAX_TOP_K; rows outside

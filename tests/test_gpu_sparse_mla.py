@@ -114,7 +114,10 @@ def check(q, pool, out_rows, sm_scale, go, glse, what):
 @pytest.mark.parametrize("R,Hq,K,splits", [(2, 128, 256, 1), (3, 128, 2048, 2), (2, 64, 100, 1), (1, 16, 333, 4),
                                            (4, 128, 1024, 4),
                                            (2, 128, 600, 16),  # the most splits: two blocks each
-                                           (2, 128, 5, 16)])   # most splits hold no row at all
+                                           (2, 128, 5, 16),    # most splits hold no row at all
+                                           (2, 48, 300, 2),    # two splits, heads not a multiple of 32
+                                           (3, 16, 1, 2),      # two splits, the second empty
+                                           (64, 128, 512, 2)])  # two splits, more requests than four-CTA clusters fit at once
 def test_sparse_mla_matches_oracle(R, Hq, K, splits):
     hs = _gpu()
     q, pool, out_rows, sm = make_case(R * 7 + K, R, Hq, K, pool_rows=3000)
@@ -200,6 +203,16 @@ def test_sparse_mla_bench_shape_one_split():
         check(q, pool, out_rows, scale, go, glse, f"32 x 128 x 2048, 1 split, sm_scale {scale:.3g}")
 
 
+def test_sparse_mla_bench_shape_two_splits():
+    """The same shape in two splits of 1,024 rows: the split pairs of a request run as one
+    four-CTA cluster and merge inside the kernel."""
+    hs = _gpu()
+    q, pool, out_rows, scale = _distinct_rows_case(33, 32, 128, 2048, pool_rows=32 * 2048 + 4096, sm_scale=1.0 / 1400)
+    go, glse, err = run_gpu(hs, q, pool, out_rows, scale, 2)
+    assert err == 0
+    check(q, pool, out_rows, scale, go, glse, "32 x 128 x 2048, 2 splits")
+
+
 def test_sparse_mla_top_k_4096_one_split():
     """4,096 rows in one split: more than the staged row table holds, so the producers read
     the split's rows from global memory; 64 blocks per CTA."""
@@ -209,3 +222,54 @@ def test_sparse_mla_top_k_4096_one_split():
     go, glse, err = run_gpu(hs, q, pool, out_rows, sm, 1)
     assert err == 0
     check(q, pool, out_rows, sm, go, glse, "top_k 4096, 1 split")
+
+
+_CAPTURE_SCRIPT = r"""
+import sys
+import numpy as np
+import torch
+sys.path[:0] = [sys.argv[1], sys.argv[2]]
+import test_gpu_sparse_mla as T
+import hierarchical_sparse_attention_gb300 as hs
+R, Hq, K, splits = 4, 128, 700, 2
+q, pool, out_rows, sm = T.make_case(11, R, Hq, K, pool_rows=3000)
+d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+g_q, g_pool, g_rows = d(q.view(np.int16)), d(pool), d(out_rows)
+wsb = hs.hs_sparse_mla_workspace_bytes(R, Hq, splits)
+res = []
+for mode in ("graph", "eager"):
+    o = torch.full((R, Hq, 512), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((R, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    args = (R, Hq, K, splits, g_q, g_pool, pool.size // 656, g_rows, sm, o, lse, ws, wsb, err)
+    torch.cuda.synchronize()
+    if mode == "graph":
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            hs.hs_sparse_mla_decode(*args, stream=s)
+        g.replay()
+    else:
+        hs.hs_sparse_mla_decode(*args)
+    torch.cuda.synchronize()
+    res.append((o.cpu(), lse.cpu(), int(err.item())))
+(go, gl, ge), (eo, el, ee) = res
+assert ge == 0 and ee == 0, (ge, ee)
+assert torch.equal(go, eo) and torch.equal(gl, el), "graph replay differs from the eager call"
+print("ok")
+"""
+
+
+def test_sparse_mla_first_call_inside_a_graph_capture():
+    """The process's first consumer call is made while a stream is being captured (the launch
+    shape is chosen then): the replayed graph gives the eager call's outputs bit for bit."""
+    _gpu()
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    p = subprocess.run([sys.executable, "-c", _CAPTURE_SCRIPT, here, root], cwd=root, capture_output=True, text=True,
+                       timeout=300)
+    assert p.returncode == 0 and p.stdout.strip().endswith("ok"), p.stdout[-2000:] + p.stderr[-2000:]
