@@ -482,6 +482,20 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
     s_abort = 0;
     s_issued = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (rank == 0 && nblk > 0) {
+      // S-CTA: Q of request r into the staging area (over the K tiles) as nine tensor boxes of
+      // 128 heads x 64 dims, 128 B per head with its 16-B chunks swizzled by head % 8; issued
+      // first, so that they land while the row table is staged. Heads past num_heads read as
+      // zeros.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // q_raw's init, seen by the copies
+      bar_arrive_tx(&bs.q_raw, (DQK / 64) * QBOX);
+      for (int bx = 0; bx < DQK / 64; ++bx)
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+            "[%4];" ::"r"(smem_u32(base + S_QSTAGE + bx * QBOX)),
+            "l"(&tm_q), "r"(64 * bx), "r"(r * a.num_heads), "r"(smem_u32(&bs.q_raw))
+            : "memory");
+    }
     // O-CTA: the bytes blocks 0 and 1 will bring (P and the rescale factors)
     if (rank == 1)
       for (int k = 0; k < 2 && k < nblk; ++k) bar_arrive_tx(&bs.p_full[k], P_BYTES);
@@ -521,21 +535,11 @@ __global__ void __launch_bounds__(T, 1) sparse_mla_kernel(const SparseMlaArgs a,
       // [144 wg, 144 wg + 144)), the A operand of S = Q . K^T, column c holding dims 2c, 2c + 1
       const int wg = warp >> 2;
       if (nblk > 0) {
-        // Q of request r into the staging area as nine tensor boxes of 128 heads x 64 dims
-        // (128 B per head, 16-B chunks swizzled by head % 8, so the per-head reads below hit
-        // distinct banks); then each thread converts its head's half of the row (warpgroup wg
-        // the columns [144 wg, 144 wg + 144)) to f16 pairs in tensor memory, the A operand of
-        // S = Q . K^T, column c holding dims 2c, 2c + 1. Heads past num_heads read as zeros.
-        uint8_t* qs = base + S_QSTAGE;
-        if (tid == 0) {
-          bar_arrive_tx(&bs.q_raw, (DQK / 64) * QBOX);
-          for (int bx = 0; bx < DQK / 64; ++bx)
-            asm volatile(
-                "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-                "[%4];" ::"r"(smem_u32(qs + bx * QBOX)),
-                "l"(&tm_q), "r"(64 * bx), "r"(r * a.num_heads), "r"(smem_u32(&bs.q_raw))
-                : "memory");
-        }
+        // Q's staged boxes (requested at kernel start; the swizzle makes the per-head reads
+        // below hit distinct banks): each thread converts its head's half of the row
+        // (warpgroup wg the columns [144 wg, 144 wg + 144)) to f16 pairs in tensor memory, the
+        // A operand of S = Q . K^T, column c holding dims 2c, 2c + 1.
+        const uint8_t* qs = base + S_QSTAGE;
         const bool landed = sync_and(pipe_wait(&bs.q_raw, 1, 0, abort), 2 * MH);  // every softmax thread takes part
         const bool live = landed && head < a.num_heads;
         const uint8_t* src = qs + head * 128;
