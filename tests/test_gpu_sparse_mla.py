@@ -273,3 +273,19 @@ def test_sparse_mla_first_call_inside_a_graph_capture():
     p = subprocess.run([sys.executable, "-c", _CAPTURE_SCRIPT, here, root], cwd=root, capture_output=True, text=True,
                        timeout=300)
     assert p.returncode == 0 and p.stdout.strip().endswith("ok"), p.stdout[-2000:] + p.stderr[-2000:]
+
+
+def test_sparse_mla_in_kernel_merge_matches_the_merge_kernel():
+    """Two splits over the same 32 requests, once as the first 32 of 64 (more four-CTA clusters
+    than fit at once: two-CTA pairs and the merge kernel) and once alone (four-CTA clusters
+    merging inside the kernel): the same partial outputs, merged with the same arithmetic, so
+    the outputs agree to rounding."""
+    hs = _gpu()
+    q, pool, out_rows, sm = _distinct_rows_case(34, 64, 128, 512, pool_rows=40000)
+    o64, l64, e64 = run_gpu(hs, q, pool, out_rows, sm, 2)
+    o32, l32, e32 = run_gpu(hs, q[:32], pool, out_rows[:32], sm, 2)
+    assert e64 == 0 and e32 == 0
+    scale = float(np.abs(o64[:32]).max())
+    assert np.abs(o32 - o64[:32]).max() <= 1e-6 * scale, "in-kernel merge differs from the merge kernel"
+    assert np.abs(l32 - l64[:32]).max() <= 1e-6
+    check(q[:32], pool, out_rows[:32], sm, o32, l32, "32 x 128 x 512, 2 splits, merged inside")
