@@ -185,6 +185,7 @@ class _DeviceView:
 
 
 TOUCH_PASSES = 8
+LINK_WARM_BYTES = 2 << 30  # host-pool bytes the GPU reads right before each timed pass
 
 
 def touch_host_pool_from_gpu(dev_ptr: int, nbytes: int) -> None:
@@ -432,6 +433,8 @@ def build_host_pools(wl, hs, node: int = -1):
 
 
 STALL_RATIO = 2.0
+SLOW_RATIO = 3.0  # a later pass whose median step exceeds this x the graph-replayed pass's median
+SLOW_FLOOR_MS = 0.2  # (or this, if larger: host-synchronised steps of tiny workloads are longer)
 MAX_ATTEMPTS = 6
 STALL_PAUSE_S = 5.0  # after a stalled pass the GPU spins this long (clocks stay up) before the next
 # Host-pool readiness before timing: the busiest step of the warm-up replay must move its miss
@@ -441,10 +444,12 @@ STALL_PAUSE_S = 5.0  # after a stalled pass the GPU spins this long (clocks stay
 COLD_FRAC, COLD_SLEEP_S, COLD_WAIT_S = 0.35, 10.0, 240.0
 
 
-def stalled(ms, ws: int) -> bool:
-    """A timed pass with a step above STALL_RATIO x its median, on any rank."""
-    local = 1.0 if float(np.max(ms)) > STALL_RATIO * float(np.median(ms)) else 0.0
-    return max_over_ranks(local, ws) > 0.0
+def stalled(ms, ws: int, ref_ms: float = 0.0) -> bool:
+    """A timed pass with a step above STALL_RATIO x its median, or (ref_ms > 0) a median above
+    SLOW_RATIO x ref_ms (a pass slow from end to end), on any rank."""
+    med = float(np.median(ms))
+    bad = float(np.max(ms)) > STALL_RATIO * med or (ref_ms > 0.0 and med > SLOW_RATIO * ref_ms)
+    return max_over_ranks(1.0 if bad else 0.0, ws) > 0.0
 
 
 def pick_pass(passes, clean: bool, ws: int) -> int:
@@ -502,6 +507,21 @@ def run_ours(args, ws, rank, local):
             release_host_pools(hs, _HOST_POOLS.pop(old)[1])
         _HOST_POOLS[key] = build_host_pools(wl, hs, numa_node)
     host, pool_objs = _HOST_POOLS[key]
+    # Right before each timed pass the GPU reads LINK_WARM_BYTES of the host pools (queued after
+    # the spin that covers the host's queueing of the steps, so no step is timed behind it): on
+    # some boxes a pass that began after tens of ms without host reads ran its first ~20 steps
+    # at 20-50 ms each, ramping back to ~1.1 ms, while passes straight after host reads did not.
+    link_views = [torch.as_tensor(_DeviceView(host_device_ptr(arr), arr.nbytes), device="cuda")
+                  for arr, _ in pool_objs]
+
+    def link_warm():
+        left = LINK_WARM_BYTES // 8
+        for v in link_views:
+            n = min(left, v.numel())
+            if n > 0:
+                v[:n].sum()
+            left -= n
+
     dpool = []
     rq, tk0, rows0 = wl.initial_device_writes()
     for l in range(L):
@@ -634,6 +654,7 @@ def run_ours(args, ws, rank, local):
         # keep the GPU busy while the host queues every timed step, so the per-step events
         # measure device time, not Python call overhead between launches
         torch.cuda._sleep(int(2e6 * (5 + K_ // 4)))
+        link_warm()
         for i in range(K_):
             s = W_ + i
             forward_stand_in(s)
@@ -679,6 +700,7 @@ def run_ours(args, ws, rank, local):
         reset_state_and_warm()
         evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K_)]
         torch.cuda._sleep(int(2e6 * (5 + K_ // 4)))
+        link_warm()
         for i in range(K_):
             s = W_ + i
             forward_stand_in(s)
@@ -710,7 +732,7 @@ def run_ours(args, ws, rank, local):
         passes_b.append(dom_try)
         attempts_b.append({"p50_dominant_us": 1e3 * float(np.median(dom_try)),
                            "max_dominant_us": 1e3 * float(np.max(dom_try))})
-        clean_b = not stalled(dom_try, ws)
+        clean_b = not stalled(dom_try, ws, max(float(np.median(step_ms)), SLOW_FLOOR_MS))
         if clean_b:
             break
     reported_b = pick_pass(passes_b, clean_b, ws)
@@ -800,7 +822,7 @@ def run_ours(args, ws, rank, local):
             v, ms = e2e_pass(zero_copy)
             runs.append((v, ms))
             tries.append(round(1e3 * float(np.median(ms)), 1))
-            clean = not stalled(ms, ws)
+            clean = not stalled(ms, ws, max(float(np.median(step_ms)), SLOW_FLOOR_MS))
             if clean:
                 break
         v, ms = runs[pick_pass([m for _, m in runs], clean, ws)]
@@ -834,9 +856,11 @@ def run_ours(args, ws, rank, local):
         "host_pool_readiness": host_ready,
         "timed_attempts": attempts_a,
         "dominant_kernel_attempts": attempts_b,
-        "attempt_rule": f"a pass with a step above {STALL_RATIO} x its median is measured again after a "
-                        f"{STALL_PAUSE_S:.0f} s pause, at most {MAX_ATTEMPTS} passes; the first clean pass is "
-                        f"reported, else (every pass stalled) the one with the lowest median",
+        "attempt_rule": f"a pass with a step above {STALL_RATIO} x its median (the eager and end-to-end "
+                        f"passes also: a median above {SLOW_RATIO} x the graph-replayed pass's, at least "
+                        f"{SLOW_FLOOR_MS} ms) is measured again after a {STALL_PAUSE_S:.0f} s pause, at most "
+                        f"{MAX_ATTEMPTS} passes; the first clean pass is reported, else (every pass stalled) "
+                        f"the one with the lowest median",
         "reported_attempts": {"timed": reported_a, "dominant_kernel": reported_b},
         "step_us_per_step": [round(1e3 * x, 1) for x in step_ms],
         "dominant_kernel_us_per_step": [round(1e3 * x, 1) for x in dom_ms],
