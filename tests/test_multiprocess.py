@@ -107,3 +107,34 @@ def test_reference_arm_prints_from_rank0_only():
     line = json.loads(out[0].strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert out[1].strip() == ""
+
+
+def _rules_worker(rank, ws, port, out):
+    import sys
+    sys.path[:0] = [ROOT]
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(ws))
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    import bench
+    # rank 1 stalls in its first pass (one step at 10x), rank 0 never does
+    first = [1.0, 1.0, 1.1, 10.0 if rank == 1 else 1.0]
+    second = [1.2, 1.2, 1.3, 1.2] if rank == 0 else [0.9, 0.9, 1.0, 0.9]
+    stalled_first = bench.stalled(first, ws)
+    # a pass slow from end to end on rank 0 only, against the graph-replayed median 1.0 ms
+    slow = bench.stalled([5.0, 5.0, 5.1] if rank == 0 else [1.0, 1.0, 1.1], ws, 1.0)
+    # no pass was clean: the one with the lowest median over the ranks, the same on every rank
+    picked = bench.pick_pass([first, second], False, ws)
+    out[rank] = (stalled_first, slow, picked)
+    bench.barrier(ws)
+    dist.destroy_process_group()
+
+
+def test_two_ranks_agree_on_stalled_passes_and_the_reported_one():
+    port = _free_port()
+    manager = mp.Manager()
+    out = manager.dict()
+    mp.spawn(_rules_worker, args=(2, port, out), nprocs=2, join=True)
+    assert out[0] == out[1]  # every rank takes the same decision
+    stalled_first, slow, picked = out[0]
+    assert stalled_first  # rank 1's outlier stalls the pass for both
+    assert slow  # rank 0's slow pass does too
+    assert picked == 0  # medians over ranks: first max(1.0, 1.05) = 1.05, second max(1.2, 0.9) = 1.2
