@@ -12,15 +12,15 @@
 //   o[h]    = softmax_j(s[h]) . latent,   lse[h] = log sum_j exp s[h, j]
 // (MLA decode with the absorbed projection: keys are the 576-dim rows, values their latent.)
 //
-// Layout of the work. A thread-block cluster of two CTAs takes (request r, split p of the
-// rows) and walks the split in blocks of 64 rows:
-//   - the S-CTA (cluster rank 0) holds Q (128 heads x 576, in f16) in tensor memory and computes
+// Layout of the work. A pair of CTAs in one thread-block cluster takes (request r, split p of
+// the rows) and walks the split in blocks of 64 rows:
+//   - the S-CTA (even cluster rank) holds Q (128 heads x 576, in f16) in tensor memory and computes
 //     S = Q . K^T of each block (36 MMAs of M 128, N 64, K 16) into one of two S buffers; its
 //     two softmax warpgroups (each 32 of the block's rows, one head per thread) run the
 //     online softmax and write P as f16 straight into the O-CTA's shared memory (distributed
 //     shared memory, asynchronous stores that complete on the O-CTA's mbarrier), with each
 //     head's rescale factor;
-//   - the O-CTA (rank 1) holds O (128 heads x 512 fp32, all of its tensor memory) and adds
+//   - the O-CTA (the odd rank after it) holds O (128 heads x 512 fp32, all of its tensor memory) and adds
 //     P . V of each block (8 MMAs of N 256, P read from shared memory); its corrector
 //     warpgroup rescales O in the rare blocks that raise a head's reference maximum, and at the
 //     end every warp reads O out, normalised by the S-CTA's row sums.
@@ -32,13 +32,16 @@
 // tile (the S-CTA all 576 dims as K, the O-CTA the 512 latent dims as V: e4m3 -> f16 in
 // hardware, times the row's scale in f16; bf16 RoPE rounded to f16), swizzled K-major, two
 // tiles in flight. The pair exchanges only P: shared memory between two CTAs moves ~41 GB/s
-// per direction, well below what each SM reads from L2. Q is staged in shared memory with
-// coalesced copies (over the K tiles, before the first block) and moved into tensor memory
-// from there. The roles hand blocks over through mbarriers
+// per direction, well below what each SM reads from L2. Q comes into shared memory as nine
+// swizzled 2-D tensor boxes, requested at kernel start (over the K tiles, before the first
+// block), and moves into tensor memory from there. The roles hand blocks over through mbarriers
 // (the two CTAs' through mbarriers in the partner's shared memory); every wait is bounded and
 // an abort flag makes the other roles stop. O is rescaled only when a head's block maximum
-// passes its reference maximum by more than 2^8 (a lazy rescale: P stays below 2^8). With
-// more than one split a small kernel merges the splits by their log-sum-exp.
+// passes its reference maximum by more than 2^8 (a lazy rescale: P stays below 2^8). Splits
+// merge by their log-sum-exp: two splits inside the kernel, the two pairs of a request sharing
+// a four-CTA cluster whose O-CTAs each merge half of the value dims (when every request's
+// cluster fits the device at once); otherwise, and for other split counts, in a small second
+// kernel. Clusters of two CTAs serve one split and the fallback.
 #include "hs_internal.h"
 
 #include <cuda.h>  // CUtensorMap and its encoder's types (the encoder is fetched through the runtime)
