@@ -100,3 +100,21 @@ def test_dominant_row():
     q = (qf.view(np.uint32) >> 16).astype(np.uint16)
     o, _ = M.sparse_mla_decode(q, pool, np.array([[0, 1, 2, 3]], np.int32), 1.0)
     assert np.allclose(o[0, 0], latent[2], rtol=1e-6, atol=1e-6)
+
+
+def test_disjoint_halves_merge_by_log_sum_exp():
+    """Attention over a row set equals the log-sum-exp merge of attention over any two disjoint
+    parts of it (the identity the split kernels and their merge rely on): a slip in the oracle's
+    normalisation or its lse (a missing log z, a sum over the wrong axis) breaks it."""
+    rng = np.random.default_rng(7)
+    pool = _rows(rng, 40)
+    q = _q(rng, 2, 5)
+    sm = 1.0 / 900
+    rows = rng.permutation(40)[:24].astype(np.int32).reshape(2, 12)
+    o, lse = M.sparse_mla_decode(q, pool, rows, sm)
+    oa, la = M.sparse_mla_decode(q, pool, rows[:, :5], sm)
+    ob, lb = M.sparse_mla_decode(q, pool, rows[:, 5:], sm)
+    lm = np.logaddexp(la, lb)
+    om = np.exp(la - lm)[..., None] * oa + np.exp(lb - lm)[..., None] * ob
+    assert np.allclose(lse, lm, rtol=0, atol=1e-9)
+    assert np.allclose(o, om, rtol=0, atol=1e-9 * np.abs(o).max())
