@@ -23,7 +23,8 @@ With no valid entry, o = 0 and lse = -inf. (MLA decode with the absorbed project
 are the 576-dim rows, values their 512-dim latent part.)
 
 Parity pins (tests/test_oracle_sparse_mla.py): e4m3 decode of the format's landmark codes,
-and attention closed forms (one row, uniform scores, duplicated rows, masking, permutation).
+attention closed forms (one row, uniform scores, duplicated rows, masking, permutation, one
+dominant row), and the log-sum-exp merge of two disjoint parts of a row set into the whole.
 """
 from __future__ import annotations
 
