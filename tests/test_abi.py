@@ -84,3 +84,33 @@ def test_product_path_does_not_touch_the_oracle():
             if f.endswith((".py", ".cu", ".h", ".cuh", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"\boracle\b", text), f"{f} mentions the oracle"
+
+
+def test_consumer_host_side_validation_without_gpu():
+    """hs_sparse_mla_workspace_bytes sizes the split workspace (0 where none is needed or the
+    shape is refused); hs_sparse_mla_decode refuses bad shapes, missing or misaligned buffers
+    and a short workspace before any launch, and does nothing for zero requests."""
+    import hierarchical_sparse_attention_gb300 as hs
+    ws = hs.hs_sparse_mla_workspace_bytes
+    assert ws(32, 128, 2) == 2 * 32 * 128 * (512 + 1) * 4  # partial outputs and lse per split
+    assert ws(32, 128, 1) == 0  # one split writes o and lse directly
+    for bad in ((0, 128, 2), (32, 0, 2), (32, 129, 2), (32, 128, 0), (32, 128, hs.HS_MAX_MLA_SPLITS + 1)):
+        assert ws(*bad) == 0
+    A = 1 << 20  # a 16-byte aligned stand-in address: nothing is launched in these calls
+    good = dict(R=2, H=128, K=64, splits=2, q=A, pool=A, rows_n=100, out_rows=A, o=A, lse=A, wsp=A,
+                wsb=ws(2, 128, 2), err=A)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        hs.hs_sparse_mla_decode(a["R"], a["H"], a["K"], a["splits"], a["q"], a["pool"], a["rows_n"],
+                                a["out_rows"], 0.1, a["o"], a["lse"], a["wsp"], a["wsb"], a["err"])
+
+    refused = [dict(R=-1), dict(H=0), dict(H=129), dict(K=0), dict(K=hs.HS_MAX_TOP_K + 1), dict(splits=0),
+               dict(splits=hs.HS_MAX_MLA_SPLITS + 1), dict(rows_n=0), dict(q=None), dict(pool=None),
+               dict(out_rows=None), dict(o=None), dict(lse=None), dict(err=None), dict(q=A + 8),
+               dict(pool=A + 4), dict(o=A + 8), dict(wsp=None), dict(wsb=good["wsb"] - 1), dict(wsp=A + 8)]
+    for kw in refused:
+        with pytest.raises(hs.HsError) as e:
+            call(**kw)
+        assert e.value.status == hs.HS_ERR_INVALID_ARG, kw
+    call(R=0, q=None, pool=A, out_rows=None, o=None, lse=None, wsp=None, wsb=0, err=None)  # no work, no launch
