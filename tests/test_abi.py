@@ -69,7 +69,12 @@ def test_host_side_errors_without_gpu():
                  lambda: hs.hs_gather(None, 1, None, 0, 1),
                  lambda: hs.hs_gather_spec(None, 1, None, 0, 0, 1),
                  lambda: hs.hs_resolve_layers(None, 1, *([None] * 10), 1),
-                 lambda: hs.hs_resolve_spec_layers(None, 1, 1, *([None] * 10), 1)):
+                 lambda: hs.hs_resolve_spec_layers(None, 1, 1, *([None] * 10), 1),
+                 lambda: hs.hs_resolve_spec(None, 1, 1, *([None] * 10)),
+                 lambda: hs.hs_backup_spec(None, 1, 1, *([None] * 5)),
+                 lambda: hs.hs_invalidate_tokens(None, 1, *([None] * 5)),
+                 lambda: hs.hs_invalidate_host_rows(None, 1, None, None, None, 0, None, None),
+                 lambda: hs.hs_reset_hints(None)):
         with pytest.raises(hs.HsError) as e:
             call()
         assert e.value.status == hs.HS_ERR_INVALID_ARG
