@@ -1251,7 +1251,7 @@ def run_mla(args, ws, rank, local):
                                     "nominal dense rate, so the bf16 figure stands for the fp16 operands",
                      "hbm": {"achieved": bytes_alg / t / 1e9, "peak": measured_hbm_peak(), "unit": "GB/s",
                              "algorithmic_bytes_per_launch": bytes_alg}},
-        "gpu_launches": args.steps * (1 if best == 1 else 2), "device_flags": int(err.item()),
+        "gpu_launches": args.steps * hs.hs_sparse_mla_launches(R, Hq, best), "device_flags": int(err.item()),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -1301,7 +1301,8 @@ def run_e2e(args, ws, rank, local):
     cfg = hs.make_config(R, K, H, B, L, wl.ps, wl.max_context, wl.max_pages)
     wsp = torch.zeros(hs.hs_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
     h = hs.hs_create(cfg, host, dpool, wl.host_rows, wl.device_rows, wsp)
-    Hq, splits = MLA_HEADS, 2  # two splits: 64 CTA pairs on 128 SMs, the fastest at this shape
+    resolve_launches = hs.hs_launch_shape(h)[1]
+    Hq, splits = MLA_HEADS, 2  # two splits: 64 CTA pairs on 128 SMs (one cluster of four per request)
     qs = [torch.from_numpy(wl.queries_bf16(i, Hq).view(np.int16)).to(dev) for i in range(4)]
     q_buf = torch.empty_like(qs[0])
     o = torch.empty((R, Hq, 512), dtype=torch.float32, device=dev)
@@ -1395,7 +1396,8 @@ def run_e2e(args, ws, rank, local):
         "p50_us": {k: v[1] for k, v in times.items()},
         "mean_us": {k: 1e6 * v[0] / K_ for k, v in times.items()},
         "top_k_rows_resolved_per_s_in_step": ws * rows / t_step,
-        "gpu_launches": K_ * (2 + 2), "device_flags": err, "attention_flags": int(merr.item()),
+        "gpu_launches": K_ * (resolve_launches + 1 + hs.hs_sparse_mla_launches(R, Hq, splits)),
+        "device_flags": err, "attention_flags": int(merr.item()),
         "host_pool": "huge pages, hs_host_register" if pools[0][1] else "cudaHostAlloc",
     }
     if rank == 0:

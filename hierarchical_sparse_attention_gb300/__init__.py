@@ -33,7 +33,7 @@ EXPORTS = ("hs_workspace_bytes", "hs_create", "hs_resolve", "hs_backup", "hs_get
            "hs_invalidate_tokens", "hs_invalidate_host_rows", "hs_resolve_layers", "hs_gather",
            "hs_resolve_spec", "hs_backup_spec", "hs_reset_hints", "hs_sparse_mla_workspace_bytes",
            "hs_sparse_mla_decode", "hs_launch_shape", "hs_resolve_spec_layers", "hs_gather_spec",
-           "hs_host_numa_node", "hs_host_bind_node")
+           "hs_host_numa_node", "hs_host_bind_node", "hs_sparse_mla_launches")
 HS_MAX_SPEC_QUERIES = 8
 HS_NOALLOC_MAX_LAYERS = 8
 
@@ -69,6 +69,8 @@ def _load() -> ctypes.CDLL:
     lib.hs_gather.argtypes = [P, i32, P, i32, i32, P]
     lib.hs_sparse_mla_workspace_bytes.argtypes = [i32, i32, i32]
     lib.hs_sparse_mla_workspace_bytes.restype = sz
+    lib.hs_sparse_mla_launches.argtypes = [i32, i32, i32]
+    lib.hs_sparse_mla_launches.restype = i32
     lib.hs_sparse_mla_decode.argtypes = [i32, i32, i32, i32, P, P, i64, P, ctypes.c_float, P, P, P, sz, P, P]
     lib.hs_sparse_mla_decode.restype = ctypes.c_int
     lib.hs_reset_hints.argtypes = [P, P]
@@ -269,6 +271,11 @@ def hs_invalidate_host_rows(h: Handle, num_requests: int, seq_lens, host_cache_l
 
 def hs_sparse_mla_workspace_bytes(num_requests: int, num_heads: int, splits: int) -> int:
     return int(_lib.hs_sparse_mla_workspace_bytes(num_requests, num_heads, splits))
+
+
+def hs_sparse_mla_launches(num_requests: int, num_heads: int, splits: int) -> int:
+    """Kernel launches of one hs_sparse_mla_decode call of this shape on the current device."""
+    return int(_lib.hs_sparse_mla_launches(num_requests, num_heads, splits))
 
 
 def hs_sparse_mla_decode(num_requests: int, num_heads: int, top_k: int, splits: int, q, kv_pool, pool_rows: int,

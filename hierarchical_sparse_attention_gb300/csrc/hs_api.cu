@@ -431,6 +431,12 @@ size_t hs_sparse_mla_workspace_bytes(int32_t num_requests, int32_t num_heads, in
   return rows * 512 * sizeof(float) + rows * sizeof(float);
 }
 
+int32_t hs_sparse_mla_launches(int32_t num_requests, int32_t num_heads, int32_t splits) {
+  if (num_requests < 1 || num_heads < 1 || num_heads > 128 || splits < 1 || splits > HS_MAX_MLA_SPLITS) return 0;
+  if (splits == 1) return 1;  // no device query needed
+  return hs::sparse_mla_launches(num_requests, splits);
+}
+
 hs_status hs_sparse_mla_decode(int32_t num_requests, int32_t num_heads, int32_t top_k, int32_t splits,
                                const uint16_t* q, const uint8_t* kv_pool, int64_t pool_rows,
                                const int32_t* out_rows, float sm_scale, float* o, float* lse, void* workspace,

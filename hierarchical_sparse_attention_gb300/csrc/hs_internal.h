@@ -217,6 +217,9 @@ int gather_pairs_ctas_per_sm(int vec);
 cudaError_t launch_gather_pairs(const Geometry& g, const Pools* pools, const OrderArgs& a, int32_t num_requests,
                                 int32_t first_layer, int32_t num_layers, cudaStream_t stream);
 size_t sparse_mla_smem_bytes();
+// Kernel launches launch_sparse_mla makes for this request count and split count on the
+// current device (1: one split, or two merged inside the kernel; 2: with the merge kernel).
+int sparse_mla_launches(int32_t num_requests, int splits);
 cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, float* part_o, float* part_lse,
                               uint32_t* err, cudaStream_t stream);
 cudaError_t launch_invalidate_tokens(const Geometry& g, const InvalidateArgs& a, int32_t num_requests,

@@ -1012,7 +1012,21 @@ int fused_clusters_resident() {
   return cached[dev];
 }
 
+// Two splits merge inside the kernel when every request's four-CTA cluster fits at once.
+bool merge_in_kernel(int32_t num_requests, int splits) {
+  return splits == 2 && fused_clusters_resident() >= num_requests;
+}
+
 }  // namespace
+
+int sparse_mla_launches(int32_t num_requests, int splits) {
+  if (cudaFuncSetAttribute(sparse_mla_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return splits == 1 ? 1 : 2;
+  }
+  return splits == 1 || merge_in_kernel(num_requests, splits) ? 1 : 2;
+}
 
 cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, float* part_o, float* part_lse,
                               uint32_t* err, cudaStream_t stream) {
@@ -1031,7 +1045,7 @@ cudaError_t launch_sparse_mla(const SparseMlaArgs& a, int32_t num_requests, floa
   }
   cudaLaunchAttribute attr[1];
   // two splits whose four-CTA clusters all fit at once: merged inside the kernel
-  if (a.splits == 2 && fused_clusters_resident() >= num_requests) {
+  if (merge_in_kernel(num_requests, a.splits)) {
     const cudaLaunchConfig_t cfg = mla_config<4>(num_requests, 2, stream, attr);
     return cudaLaunchKernelEx(&cfg, sparse_mla_kernel<4>, a, tm_s, tm_o, tm_q, part_o, part_lse, err);
   }

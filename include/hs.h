@@ -388,6 +388,11 @@ HS_API hs_status hs_invalidate_host_rows(hs_handle* h, int32_t num_requests, con
  *   error_flags: device uint32, HS_FLAG_TIMEOUT OR-ed in if a bounded wait ran out.
  * Two kernel launches at most; no allocation, no synchronisation; graph-capturable. */
 HS_API size_t hs_sparse_mla_workspace_bytes(int32_t num_requests, int32_t num_heads, int32_t splits);
+/* The kernel launches one hs_sparse_mla_decode call makes for this shape on the current device:
+ * 1 (one split, or two splits merged inside the kernel), 2 (the attention kernel and the merge
+ * kernel), 0 for a shape hs_sparse_mla_decode refuses (num_requests < 1 here). For two splits
+ * the first call on a device asks the runtime how many four-CTA clusters fit at once. */
+HS_API int32_t hs_sparse_mla_launches(int32_t num_requests, int32_t num_heads, int32_t splits);
 HS_API hs_status hs_sparse_mla_decode(int32_t num_requests, int32_t num_heads, int32_t top_k, int32_t splits,
                                       const uint16_t* q, const uint8_t* kv_pool, int64_t pool_rows,
                                       const int32_t* out_rows, float sm_scale, float* o, float* lse,

@@ -98,6 +98,9 @@ def test_consumer_host_side_validation_without_gpu():
     import hierarchical_sparse_attention_gb300 as hs
     ws = hs.hs_sparse_mla_workspace_bytes
     assert ws(32, 128, 2) == 2 * 32 * 128 * (512 + 1) * 4  # partial outputs and lse per split
+    assert hs.hs_sparse_mla_launches(32, 128, 1) == 1  # one split: one launch, no device query
+    for bad in ((0, 128, 2), (32, 0, 2), (32, 129, 2), (32, 128, 0), (32, 128, hs.HS_MAX_MLA_SPLITS + 1)):
+        assert hs.hs_sparse_mla_launches(*bad) == 0
     assert ws(32, 128, 1) == 0  # one split writes o and lse directly
     for bad in ((0, 128, 2), (32, 0, 2), (32, 129, 2), (32, 128, 0), (32, 128, hs.HS_MAX_MLA_SPLITS + 1)):
         assert ws(*bad) == 0

@@ -207,6 +207,7 @@ def test_sparse_mla_bench_shape_two_splits():
     """The same shape in two splits of 1,024 rows: the split pairs of a request run as one
     four-CTA cluster and merge inside the kernel."""
     hs = _gpu()
+    assert hs.hs_sparse_mla_launches(32, 128, 2) == 1  # merged inside the kernel: no second launch
     q, pool, out_rows, scale = _distinct_rows_case(33, 32, 128, 2048, pool_rows=32 * 2048 + 4096, sm_scale=1.0 / 1400)
     go, glse, err = run_gpu(hs, q, pool, out_rows, scale, 2)
     assert err == 0
@@ -281,6 +282,7 @@ def test_sparse_mla_in_kernel_merge_matches_the_merge_kernel():
     merging inside the kernel): the same partial outputs, merged with the same arithmetic, so
     the outputs agree to rounding."""
     hs = _gpu()
+    assert hs.hs_sparse_mla_launches(64, 128, 2) == 2  # 256 CTAs in clusters of four: the merge kernel
     q, pool, out_rows, sm = _distinct_rows_case(34, 64, 128, 512, pool_rows=40000)
     o64, l64, e64 = run_gpu(hs, q, pool, out_rows, sm, 2)
     o32, l32, e32 = run_gpu(hs, q[:32], pool, out_rows[:32], sm, 2)
